@@ -1,0 +1,167 @@
+"""ctypes wrapper around swa_oracle.c (fp64 CPU oracle).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg import this module.  The product path (the CUDA library and
+its Python binding) never imports it and shares no code with it.
+
+What the C file computes is the plain definition of masked softmax attention
+and its closed-form backward; the passages it follows are listed in its
+header.  This wrapper only builds the shared object, converts inputs to the
+C calling convention and allocates the fp64 outputs.
+
+Inputs may be torch tensors (bf16 or float64, CPU) or numpy arrays (uint16
+holding bf16 bit patterns, or float64), all shaped [B, H, L, D].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libswa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile swa_oracle.c into oracle/_build/libswa_oracle.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        # no OpenMP runtime: the pragmas are ignored and the oracle runs on one core
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            L, I, D, P = ctypes.c_long, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+            lib.swa_oracle_fwd.argtypes = [P, P, P, I, L, L, L, L, L, L, D, I, P, P]
+            lib.swa_oracle_bwd.argtypes = [P, P, P, P, I, L, L, L, L, L, L, D, I, P, P, P, P, P, P, P]
+            lib.swa_oracle_rows.argtypes = [P, P, P, P, I, L, L, L, L, L, L, D, I, L, L, P, L, P, P, P, P]
+            lib.swa_oracle_key_rows.argtypes = [P, P, P, P, I, L, L, L, L, L, L, D, I, L, L, P, L, P, P]
+            for f in (lib.swa_oracle_fwd, lib.swa_oracle_bwd, lib.swa_oracle_rows, lib.swa_oracle_key_rows):
+                f.restype = ctypes.c_int
+            lib.swa_oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().swa_oracle_num_threads())
+
+
+def _as_array(x):
+    """Return (contiguous numpy array, is_f64) for a bf16 / fp64 tensor or array."""
+    try:
+        import torch
+
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), 0
+            if x.dtype == torch.float64:
+                return x.numpy(), 1
+            raise TypeError(f"oracle inputs must be bf16 or float64, got {x.dtype}")
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return x, 0
+    if x.dtype == np.float64:
+        return x, 1
+    raise TypeError(f"oracle inputs must be uint16 (bf16 bits) or float64, got {x.dtype}")
+
+
+def _prep(q, k, v, dO=None):
+    arrs = [_as_array(t) for t in (q, k, v) + ((dO,) if dO is not None else ())]
+    kinds = {a[1] for a in arrs}
+    if len(kinds) != 1:
+        raise TypeError("q, k, v (and dO) must share one element type")
+    B, Hq, L, D = arrs[0][0].shape
+    Bk, Hkv, Lk, Dk = arrs[1][0].shape
+    if (Bk, Lk, Dk) != (B, L, D) or arrs[2][0].shape != arrs[1][0].shape:
+        raise ValueError("k and v must be [B, Hkv, L, D] matching q's B, L, D")
+    if dO is not None and arrs[3][0].shape != arrs[0][0].shape:
+        raise ValueError("dO must have q's shape")
+    return [a[0] for a in arrs], kinds.pop(), (B, Hq, Hkv, L, D)
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def forward(q, k, v, window: int, scale: float, band_only: bool = False):
+    """Return (o [B,Hq,L,D], lse [B,Hq,L]) in fp64."""
+    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v)
+    o = np.empty((B, Hq, L, D), np.float64)
+    lse = np.empty((B, Hq, L), np.float64)
+    rc = _load().swa_oracle_fwd(*map(_ptr, arrs), f64, B, Hq, Hkv, L, D, int(window), float(scale),
+                                int(band_only), _ptr(o), _ptr(lse))
+    if rc:
+        raise RuntimeError(f"swa_oracle_fwd failed ({rc})")
+    return o, lse
+
+
+def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False):
+    """Return dict with o, lse, delta, dq, dk, dv (fp64) and delta_gap."""
+    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v, dO)
+    out = dict(
+        o=np.empty((B, Hq, L, D)), lse=np.empty((B, Hq, L)), delta=np.empty((B, Hq, L)),
+        dq=np.empty((B, Hq, L, D)), dk=np.empty((B, Hkv, L, D)), dv=np.empty((B, Hkv, L, D)),
+    )
+    gap = ctypes.c_double(0.0)
+    rc = _load().swa_oracle_bwd(*map(_ptr, arrs), f64, B, Hq, Hkv, L, D, int(window), float(scale),
+                                int(band_only), *(_ptr(out[n]) for n in ("o", "lse", "delta", "dq", "dk", "dv")),
+                                ctypes.byref(gap))
+    if rc:
+        raise RuntimeError(f"swa_oracle_bwd failed ({rc})")
+    out["delta_gap"] = gap.value
+    return out
+
+
+def rows(q, k, v, dO, window: int, scale: float, b: int, h: int, row_ids, band_only: bool = False):
+    """Selected query rows of head (b, h): dict o [n,D], lse [n], and with dO also delta [n], dq [n,D]."""
+    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v, dO)
+    ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
+    n = ids.size
+    out = dict(o=np.empty((n, D)), lse=np.empty(n), delta=np.empty(n), dq=np.empty((n, D)))
+    dptr = _ptr(arrs[3]) if dO is not None else None
+    rc = _load().swa_oracle_rows(_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), dptr, f64, B, Hq, Hkv, L, D,
+                                 int(window), float(scale), int(band_only), int(b), int(h), _ptr(ids), n,
+                                 _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["delta"]), _ptr(out["dq"]))
+    if rc:
+        raise RuntimeError(f"swa_oracle_rows failed ({rc})")
+    if dO is None:
+        del out["delta"], out["dq"]
+    return out
+
+
+def key_rows(q, k, v, dO, window: int, scale: float, b: int, kvh: int, key_ids, band_only: bool = False):
+    """Selected key rows of kv head (b, kvh): dict dk [n,D], dv [n,D]."""
+    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v, dO)
+    ids = np.ascontiguousarray(np.asarray(key_ids, dtype=np.int64))
+    n = ids.size
+    out = dict(dk=np.empty((n, D)), dv=np.empty((n, D)))
+    rc = _load().swa_oracle_key_rows(*map(_ptr, arrs), f64, B, Hq, Hkv, L, D, int(window), float(scale),
+                                     int(band_only), int(b), int(kvh), _ptr(ids), n,
+                                     _ptr(out["dk"]), _ptr(out["dv"]))
+    if rc:
+        raise RuntimeError(f"swa_oracle_key_rows failed ({rc})")
+    return out

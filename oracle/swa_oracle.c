@@ -1,0 +1,407 @@
+/*
+ * swa_oracle.c -- fp64 CPU oracle for causal / sliding-window attention with
+ * grouped-query heads: forward (output and per-row logsumexp) and the
+ * closed-form softmax backward (dq, dk, dv).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * What it computes is the plain definition, written out with no blocking,
+ * fusion or reordering:
+ *
+ *   s_ij  = scale * q_i . k_j                         for every key j < L
+ *   s_ij  = -inf  when j is outside band(i)
+ *   band(i) = { j : j <= i  and  (W == 0  or  i - j < W) }
+ *   lse_i = m_i + ln sum_j exp(s_ij - m_i),  m_i = max_j s_ij
+ *   P_ij  = exp(s_ij - lse_i)                  (exactly 0 outside the band)
+ *   o_i   = sum_j P_ij v_j
+ *   dP_ij = dO_i . v_j
+ *   Delta_i = sum_j P_ij dP_ij                 (checked against dO_i . o_i)
+ *   dS_ij = P_ij (dP_ij - Delta_i)
+ *   dq_i  = scale * sum_j dS_ij k_j
+ *   dk_j  = scale * sum_{h in group} sum_i dS_ij q_i
+ *   dv_j  = sum_{h in group} sum_i P_ij dO_i
+ *
+ * Passages followed:
+ *  - Mask rule: "Lab 028 lab detail: Off NVIDIA, you fix the platform
+ *    yourself", "Plan for the build" step 4 (P is zeroed where
+ *    j < i + diag_off - window_size + 1, with diag_off = 0 for
+ *    self-attention) and "What I changed, in plain terms" item 4 (a key that
+ *    is window_size or more positions behind the query's diagonal is
+ *    zeroed); causal tiles above the diagonal are skipped ("What the code
+ *    says").  A window of 0 is read as plain causal.
+ *  - Forward writes the logsumexp, the per-row softmax normaliser the
+ *    backward reuses: same page, "What I changed, in plain terms" item 1.
+ *  - Backward stores the per-row LSE and recomputes P: "Training -- design
+ *    (ORPO, flash-CCE head, prefix sharing, segmented backward)" section 6
+ *    "Kernel-fusion notes"; ground truth is the dense matmul / softmax
+ *    decomposition of section 5.2 "Attention backward".
+ *  - Grouped-query heads: query head h reads kv head h / (Hq / Hkv):
+ *    "MiniCPM5 Decode Megakernel -- end-to-end build plan", section 4.1
+ *    stage 5 and section 6 "Pitfalls".
+ *
+ * Layout: every tensor is row-major [B, H, L, D] (lse / delta [B, Hq, L]).
+ * Inputs are either raw bf16 bit patterns (uint16) or fp64; bf16 values are
+ * widened exactly to fp64.  All arithmetic is fp64.
+ *
+ * The backward is organised in two passes over the definition: a row pass
+ * (per query row: s, lse, P, o, Delta, dq) and a column pass (per key row:
+ * dk, dv, summing over every query row and every head of the group in
+ * ascending order).  Both passes evaluate the same formulas above; the
+ * column pass takes lse_i and Delta_i from the row pass.
+ *
+ * "band_only" skips the key (or query) positions outside the band.  Those
+ * terms are exact zeros (exp(-inf) = 0), and the in-band terms are summed in
+ * the same ascending order, so both modes give bitwise-equal results; this
+ * is checked by a test.  It exists only to make the timed CPU baseline finish
+ * on long sequences.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    const void *q, *k, *v, *dO;
+    int is_f64;               /* 1: fp64 arrays, 0: bf16 bit patterns */
+    long B, Hq, Hkv, L, D, W;
+    double scale;
+    int band_only;
+} ctx_t;
+
+static double bf16_bits_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double ld(const ctx_t* c, const void* base, long idx) {
+    if (c->is_f64) return ((const double*)base)[idx];
+    return bf16_bits_to_f64(((const uint16_t*)base)[idx]);
+}
+
+/* Offset of row i of head h of batch b in a [B, H, L, D] tensor. */
+static long row_off(const ctx_t* c, long b, long h, long H, long i) {
+    return ((b * H + h) * c->L + i) * c->D;
+}
+
+/* Key j is visible to query i. */
+static int in_band(long i, long j, long W) {
+    if (j > i) return 0;
+    if (W > 0 && i - j >= W) return 0;
+    return 1;
+}
+
+/* Range of key positions the row pass visits for query i. */
+static void key_range(const ctx_t* c, long i, long* j0, long* j1) {
+    if (c->band_only) {
+        *j0 = (c->W > 0 && i - c->W + 1 > 0) ? i - c->W + 1 : 0;
+        *j1 = i;
+    } else {
+        *j0 = 0;
+        *j1 = c->L - 1;
+    }
+}
+
+/* Range of query positions the column pass visits for key j. */
+static void query_range(const ctx_t* c, long j, long* i0, long* i1) {
+    if (c->band_only) {
+        *i0 = j;
+        *i1 = (c->W > 0 && j + c->W - 1 < c->L - 1) ? j + c->W - 1 : c->L - 1;
+    } else {
+        *i0 = 0;
+        *i1 = c->L - 1;
+    }
+}
+
+/*
+ * Row pass for query row i of head h (batch b).  s and dp are scratch of L
+ * doubles.  Writes o_row[D], *lse; when dO is given also *delta (sum_j P dP),
+ * *delta_alt (dO_i . o_i) and, if dq_row is not NULL, dq_row[D].
+ */
+static void row_pass(const ctx_t* c, long b, long h, long i, double* s, double* dp,
+                     double* o_row, double* lse, double* delta, double* delta_alt,
+                     double* dq_row) {
+    const long D = c->D;
+    const long kvh = h / (c->Hq / c->Hkv);
+    const long qo = row_off(c, b, h, c->Hq, i);
+    long j0, j1;
+    key_range(c, i, &j0, &j1);
+
+    /* scores */
+    double m = -INFINITY;
+    for (long j = j0; j <= j1; ++j) {
+        if (!in_band(i, j, c->W)) { s[j] = -INFINITY; continue; }
+        const long ko = row_off(c, b, kvh, c->Hkv, j);
+        double acc = 0.0;
+        for (long d = 0; d < D; ++d) acc += ld(c, c->q, qo + d) * ld(c, c->k, ko + d);
+        s[j] = c->scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    /* logsumexp */
+    double sum = 0.0;
+    for (long j = j0; j <= j1; ++j) sum += exp(s[j] - m);
+    const double lse_i = m + log(sum);
+    *lse = lse_i;
+    /* output */
+    for (long d = 0; d < D; ++d) o_row[d] = 0.0;
+    for (long j = j0; j <= j1; ++j) {
+        const double p = exp(s[j] - lse_i);
+        const long vo = row_off(c, b, kvh, c->Hkv, j);
+        for (long d = 0; d < D; ++d) o_row[d] += p * ld(c, c->v, vo + d);
+    }
+    if (!c->dO) return;
+
+    /* dP, Delta (both forms) */
+    const long go = row_off(c, b, h, c->Hq, i);
+    double dl = 0.0;
+    for (long j = j0; j <= j1; ++j) {
+        const long vo = row_off(c, b, kvh, c->Hkv, j);
+        double acc = 0.0;
+        for (long d = 0; d < D; ++d) acc += ld(c, c->dO, go + d) * ld(c, c->v, vo + d);
+        dp[j] = acc;
+        dl += exp(s[j] - lse_i) * acc;
+    }
+    double da = 0.0;
+    for (long d = 0; d < D; ++d) da += ld(c, c->dO, go + d) * o_row[d];
+    *delta = dl;
+    *delta_alt = da;
+    if (!dq_row) return;
+
+    /* dq */
+    for (long d = 0; d < D; ++d) dq_row[d] = 0.0;
+    for (long j = j0; j <= j1; ++j) {
+        const double p = exp(s[j] - lse_i);
+        const double ds = p * (dp[j] - dl);
+        const long ko = row_off(c, b, kvh, c->Hkv, j);
+        for (long d = 0; d < D; ++d) dq_row[d] += c->scale * ds * ld(c, c->k, ko + d);
+    }
+}
+
+/*
+ * Column pass for key row j of kv head kvh (batch b): dk_row[D], dv_row[D].
+ * lse and delta are [B, Hq, L] arrays from the row pass; only the rows of
+ * the group's heads that can see key j are read.
+ */
+static void col_pass(const ctx_t* c, long b, long kvh, long j, const double* lse,
+                     const double* delta, double* dk_row, double* dv_row) {
+    const long D = c->D;
+    const long G = c->Hq / c->Hkv;
+    const long ko = row_off(c, b, kvh, c->Hkv, j);
+    long i0, i1;
+    query_range(c, j, &i0, &i1);
+    for (long d = 0; d < D; ++d) { dk_row[d] = 0.0; dv_row[d] = 0.0; }
+    for (long g = 0; g < G; ++g) {
+        const long h = kvh * G + g;
+        for (long i = i0; i <= i1; ++i) {
+            const long qo = row_off(c, b, h, c->Hq, i);
+            const long ri = (b * c->Hq + h) * c->L + i;
+            double s;
+            if (in_band(i, j, c->W)) {
+                double acc = 0.0;
+                for (long d = 0; d < D; ++d) acc += ld(c, c->q, qo + d) * ld(c, c->k, ko + d);
+                s = c->scale * acc;
+            } else {
+                s = -INFINITY;
+            }
+            const double p = exp(s - lse[ri]);
+            double dpv = 0.0;
+            for (long d = 0; d < D; ++d) dpv += ld(c, c->dO, qo + d) * ld(c, c->v, ko + d);
+            const double ds = p * (dpv - delta[ri]);
+            for (long d = 0; d < D; ++d) {
+                dk_row[d] += c->scale * ds * ld(c, c->q, qo + d);
+                dv_row[d] += p * ld(c, c->dO, qo + d);
+            }
+        }
+    }
+}
+
+static int check_shape(long B, long Hq, long Hkv, long L, long D, long W) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || W < 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    return 0;
+}
+
+int swa_oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Forward over every row.  o: [B,Hq,L,D], lse: [B,Hq,L]. */
+int swa_oracle_fwd(const void* q, const void* k, const void* v, int is_f64, long B, long Hq,
+                   long Hkv, long L, long D, long W, double scale, int band_only, double* o,
+                   double* lse) {
+    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
+    ctx_t c = {q, k, v, NULL, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
+    const long rows = B * Hq * L;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!s) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            if (!s) continue;
+            const long i = r % L, bh = r / L, h = bh % Hq, b = bh / Hq;
+            row_pass(&c, b, h, i, s, NULL, o + r * D, lse + r, NULL, NULL, NULL);
+        }
+        free(s);
+    }
+    return err;
+}
+
+/*
+ * Forward and backward over every row and key.  Outputs o, dq: [B,Hq,L,D];
+ * dk, dv: [B,Hkv,L,D]; lse, delta: [B,Hq,L].  *delta_gap receives
+ * max_i |sum_j P dP - dO_i . o_i|.
+ */
+int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                   long B, long Hq, long Hkv, long L, long D, long W, double scale,
+                   int band_only, double* o, double* lse, double* delta, double* dq,
+                   double* dk, double* dv, double* delta_gap) {
+    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
+    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
+    const long rows = B * Hq * L;
+    const long keys = B * Hkv * L;
+    double gap = 0.0;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+        double my_gap = 0.0;
+        if (!s || !dp) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            if (!s || !dp) continue;
+            const long i = r % L, bh = r / L, h = bh % Hq, b = bh / Hq;
+            double da;
+            row_pass(&c, b, h, i, s, dp, o + r * D, lse + r, delta + r, &da, dq + r * D);
+            const double g = fabs(delta[r] - da);
+            if (g > my_gap) my_gap = g;
+        }
+#pragma omp critical
+        if (my_gap > gap) gap = my_gap;
+        free(s);
+        free(dp);
+    }
+    if (err) return err;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long r = 0; r < keys; ++r) {
+        const long j = r % L, bh = r / L, kvh = bh % Hkv, b = bh / Hkv;
+        col_pass(&c, b, kvh, j, lse, delta, dk + r * D, dv + r * D);
+    }
+    if (delta_gap) *delta_gap = gap;
+    return 0;
+}
+
+/*
+ * Selected query rows of one head: o, dq [n, D]; lse, delta [n].
+ * dO may be NULL (forward only; delta and dq are then left untouched).
+ */
+int swa_oracle_rows(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                    long B, long Hq, long Hkv, long L, long D, long W, double scale,
+                    int band_only, long b, long h, const long* rows, long n, double* o,
+                    double* lse, double* delta, double* dq) {
+    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
+    if (b < 0 || b >= B || h < 0 || h >= Hq) return -1;
+    for (long t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= L) return -1;
+    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!s || !dp) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long t = 0; t < n; ++t) {
+            if (!s || !dp) continue;
+            double da;
+            row_pass(&c, b, h, rows[t], s, dp, o + t * D, lse + t, dO ? delta + t : NULL, &da,
+                     dO ? dq + t * D : NULL);
+        }
+        free(s);
+        free(dp);
+    }
+    return err;
+}
+
+/*
+ * Selected key rows of one kv head: dk, dv [n, D].  First runs the row pass
+ * for every query row, of every head in the group, that can see one of the
+ * selected keys (lse_i and Delta_i), then the column pass for each key.
+ */
+int swa_oracle_key_rows(const void* q, const void* k, const void* v, const void* dO,
+                        int is_f64, long B, long Hq, long Hkv, long L, long D, long W,
+                        double scale, int band_only, long b, long kvh, const long* keys, long n,
+                        double* dk, double* dv) {
+    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
+    if (b < 0 || b >= B || kvh < 0 || kvh >= Hkv || n < 1 || !dO) return -1;
+    long jmin = L, jmax = -1;
+    for (long t = 0; t < n; ++t) {
+        if (keys[t] < 0 || keys[t] >= L) return -1;
+        if (keys[t] < jmin) jmin = keys[t];
+        if (keys[t] > jmax) jmax = keys[t];
+    }
+    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
+    const long G = Hq / Hkv;
+    /* query rows that can see any selected key: [jmin, jmax + W - 1] */
+    const long ilo = jmin;
+    const long ihi = (W > 0 && jmax + W - 1 < L - 1) ? jmax + W - 1 : L - 1;
+    const long nr = ihi - ilo + 1;
+    /* lse / delta laid out as full [B, Hq, L] arrays so col_pass can index them */
+    double* lse = (double*)calloc((size_t)(B * Hq * L), sizeof(double));
+    double* delta = (double*)calloc((size_t)(B * Hq * L), sizeof(double));
+    double* obuf = (double*)malloc(sizeof(double) * (size_t)(G * nr * D));
+    if (!lse || !delta || !obuf) {
+        free(lse); free(delta); free(obuf);
+        return -2;
+    }
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+        if (!s || !dp) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < G * nr; ++r) {
+            if (!s || !dp) continue;
+            const long g = r / nr, i = ilo + r % nr, h = kvh * G + g;
+            const long ri = (b * Hq + h) * L + i;
+            double da;
+            row_pass(&c, b, h, i, s, dp, obuf + r * D, lse + ri, delta + ri, &da, NULL);
+        }
+        free(s);
+        free(dp);
+    }
+    if (!err) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (long t = 0; t < n; ++t) col_pass(&c, b, kvh, keys[t], lse, delta, dk + t * D, dv + t * D);
+    }
+    free(lse);
+    free(delta);
+    free(obuf);
+    return err;
+}

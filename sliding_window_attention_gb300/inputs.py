@@ -1,0 +1,101 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module holds no attention arithmetic: only shapes and random-number
+recipes.  It is the one piece the CUDA path's tests and the oracle share.
+
+Recipe (all on the CPU, so both sides see identical bf16 values):
+  gen = torch.Generator().manual_seed(seed)
+  q, k, v, dO drawn in that order with torch.randn(shape, float32, gen)
+  dO multiplied by `do_scale` in fp32
+  with outliers: per (b, kv head), round(frac * L) distinct key rows drawn
+    without replacement (torch.randperm with the same generator, after dO),
+    multiplied by `outlier_mult` in fp32
+  finally every tensor is rounded to bf16 (round-to-nearest-even).
+
+The five named workloads are shaped like the pages' Gemma-style sliding and
+global layers: the sliding layers use D=256, 16 kv heads, 32 query heads and
+a 1,024-token window; the global layers D=512 with 4 kv heads ("Lab 028 lab
+detail", "Starting point"), and the long step is 30,553 tokens ("Model
+step").  Peaky softmax rows (scores in the 20s on real activations, "fp32
+gradient truth", layer-level table) are imitated by scaling 1% of the key
+rows by 8.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    L: int
+    D: int
+    window: int
+    do_scale: float = 1.0
+    outlier_frac: float = 0.0
+    outlier_mult: float = 8.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def pairs(self) -> int:
+        """In-band (query, key) pairs over all batches and query heads."""
+        return self.B * self.Hq * band_pairs(self.L, self.window)
+
+    def fwd_flops(self) -> int:
+        return 4 * self.D * self.pairs()
+
+    def bwd_flops(self) -> int:
+        return 10 * self.D * self.pairs()
+
+
+def band_pairs(L: int, window: int) -> int:
+    """Number of (i, j) with j <= i and (window == 0 or i - j < window)."""
+    if window <= 0 or window >= L:
+        return L * (L + 1) // 2
+    w = window
+    # rows 0..w-1 see i+1 keys, the remaining rows see w keys
+    return w * (w + 1) // 2 + (L - w) * w
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_l256_d64_w64", 1, 2, 1, 256, 64, 64, seed=20260001),
+        Workload("causal_gqa_l8192_d128", 1, 8, 4, 8192, 128, 0, seed=20260002),
+        Workload("sliding_l8192_d256_w1024", 1, 32, 16, 8192, 256, 1024, do_scale=0.1, seed=20260003),
+        Workload("global_l16384_d512", 1, 32, 4, 16384, 512, 0, do_scale=0.1, seed=20260004),
+        Workload("ragged_l30553_d256_w1024_outliers", 1, 32, 16, 30553, 256, 1024,
+                 outlier_frac=0.01, seed=20260005),
+    ]
+}
+
+
+def make_inputs(B, Hq, Hkv, L, D, seed, do_scale=1.0, outlier_frac=0.0, outlier_mult=8.0):
+    """Return (q, k, v, dO) as contiguous CPU bf16 tensors [B, H, L, D]."""
+    gen = torch.Generator().manual_seed(int(seed))
+    q = torch.randn((B, Hq, L, D), dtype=torch.float32, generator=gen)
+    k = torch.randn((B, Hkv, L, D), dtype=torch.float32, generator=gen)
+    v = torch.randn((B, Hkv, L, D), dtype=torch.float32, generator=gen)
+    dO = torch.randn((B, Hq, L, D), dtype=torch.float32, generator=gen)
+    if do_scale != 1.0:
+        dO.mul_(do_scale)
+    if outlier_frac > 0.0:
+        n = int(round(outlier_frac * L))
+        for b in range(B):
+            for h in range(Hkv):
+                idx = torch.randperm(L, generator=gen)[:n]
+                k[b, h, idx, :] *= outlier_mult
+    return tuple(t.to(torch.bfloat16).contiguous() for t in (q, k, v, dO))
+
+
+def workload_inputs(w: Workload):
+    return make_inputs(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed, w.do_scale, w.outlier_frac, w.outlier_mult)

@@ -1,0 +1,302 @@
+"""Pins for the fp64 CPU oracle: each test checks it against something other
+than itself -- a hand-worked example, the pages' mask rule, closed forms,
+finite differences, torch's own softmax / matmul autograd, and invariants.
+
+A plausible mistake anywhere in the oracle (dropped term, wrong sign, wrong
+index, transposed operand, off-by-one window) fails at least one of these.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from sliding_window_attention_gb300.inputs import make_inputs
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand64(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, dtype=torch.float64, generator=g) * scale).contiguous()
+
+
+def _torch_reference(q, k, v, dO, window, scale):
+    """Independent path: torch CPU fp64 masked softmax + matmul + autograd."""
+    q = q.double().clone().requires_grad_(True)
+    k = k.double().clone().requires_grad_(True)
+    v = v.double().clone().requires_grad_(True)
+    B, Hq, L, D = q.shape
+    G = Hq // k.shape[1]
+    kr = k.repeat_interleave(G, dim=1)
+    vr = v.repeat_interleave(G, dim=1)
+    s = scale * torch.matmul(q, kr.transpose(-1, -2))
+    i = torch.arange(L).view(L, 1)
+    j = torch.arange(L).view(1, L)
+    keep = j <= i
+    if window > 0:
+        keep = keep & (i - j < window)
+    s = s.masked_fill(~keep, float("-inf"))
+    p = torch.softmax(s, dim=-1)
+    o = torch.matmul(p, vr)
+    lse = torch.logsumexp(s, dim=-1)
+    (o * dO.double()).sum().backward()
+    return dict(o=o.detach(), lse=lse.detach(), dq=q.grad, dk=k.grad, dv=v.grad)
+
+
+def _read_golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLD, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *rest = line.split()
+        vals[key] = [float(x) for x in rest]
+    return vals
+
+
+# ---------------------------------------------------------------------------
+# worked examples from the pages' rules
+
+
+def test_hand_worked_two_tokens(oracle_mod):
+    g = _read_golden("hand_worked_l2.txt")
+    t = {n: torch.tensor(g[n], dtype=torch.float64).view(1, 1, 2, 1) for n in ("q", "k", "v", "dO")}
+    r = oracle_mod.backward(t["q"], t["k"], t["v"], t["dO"], int(g["window"][0]), g["scale"][0])
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[n].reshape(-1), g[n], rtol=1e-15, atol=1e-15, err_msg=n)
+
+
+def test_window_mask_matches_pages_rule(oracle_mod):
+    """With V = identity (D = L), o_i is row i of P; its zero pattern is the mask."""
+    lines = [l for l in open(os.path.join(GOLD, "window_mask_l8_w3.txt")) if l.strip() and not l.startswith("#")]
+    window = int(lines[0].split()[1])
+    mask = np.array([[int(x) for x in l.split()] for l in lines[1:]])
+    L = mask.shape[0]
+    q = _rand64((1, 1, L, L), 1)
+    k = _rand64((1, 1, L, L), 2)
+    v = torch.eye(L, dtype=torch.float64).view(1, 1, L, L).contiguous()
+    o, _ = oracle_mod.forward(q, k, v, window, 0.3)
+    P = o[0, 0]
+    assert np.array_equal(P != 0.0, mask == 1)
+    np.testing.assert_allclose(P.sum(-1), 1.0, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_window_one_closed_form(oracle_mod, G):
+    """Window 1: each query sees only itself, so o = v, lse = scale q.k, and
+    dQ, dK are exactly zero ("Lab 028 lab detail", "Gradient parity")."""
+    B, Hkv, L, D = 2, 2, 19, 8
+    Hq = G * Hkv
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=11)
+    scale = 0.37
+    r = oracle_mod.backward(q, k, v, dO, 1, scale)
+    qd, kd, vd, gd = (t.double().numpy() for t in (q, k, v, dO))
+    kv_of = np.arange(Hq) // G
+    np.testing.assert_array_equal(r["o"], vd[:, kv_of])
+    np.testing.assert_allclose(r["lse"], scale * np.einsum("bhld,bhld->bhl", qd, kd[:, kv_of]), rtol=1e-15, atol=1e-15)
+    assert np.all(r["dq"] == 0.0) and np.all(r["dk"] == 0.0)
+    np.testing.assert_allclose(r["dv"], gd.reshape(B, Hkv, G, L, D).sum(2), rtol=1e-15, atol=1e-15)
+
+
+@pytest.mark.parametrize("window", [0, 1, 4, 13])
+def test_zero_queries_uniform(oracle_mod, window):
+    """q = 0: every in-band score is 0, so P is uniform over the band,
+    lse_i = ln |band(i)| and o_i is the mean of v over the band."""
+    B, Hq, Hkv, L, D = 1, 2, 1, 17, 5
+    q = torch.zeros((B, Hq, L, D), dtype=torch.float64)
+    k = _rand64((B, Hkv, L, D), 3)
+    v = _rand64((B, Hkv, L, D), 4)
+    o, lse = oracle_mod.forward(q, k, v, window, 1.0)
+    for i in range(L):
+        j0 = 0 if window == 0 else max(0, i - window + 1)
+        n = i - j0 + 1
+        assert abs(lse[0, 0, i] - math.log(n)) < 1e-14
+        np.testing.assert_allclose(o[0, 1, i], v[0, 0, j0:i + 1].numpy().mean(0), rtol=1e-13, atol=1e-14)
+
+
+def test_single_token(oracle_mod):
+    q, k, v, dO = (_rand64((1, 3, 1, 4), s) for s in (5, 6, 7, 8))
+    k, v = k[:, :1].contiguous(), v[:, :1].contiguous()
+    r = oracle_mod.backward(q, k, v, dO, 0, 0.5)
+    np.testing.assert_array_equal(r["o"], np.broadcast_to(v.numpy(), r["o"].shape))
+    np.testing.assert_allclose(r["lse"][0, :, 0], 0.5 * (q[0, :, 0] * k[0, 0, 0]).sum(-1).numpy(), rtol=1e-15)
+    assert np.all(r["dq"] == 0) and np.all(r["dk"] == 0)
+
+
+# ---------------------------------------------------------------------------
+# library routine: torch fp64 softmax / matmul autograd on tiny shapes
+
+
+@pytest.mark.parametrize(
+    "B,Hq,Hkv,L,D,window",
+    [(1, 2, 1, 33, 16, 0), (2, 4, 2, 37, 8, 5), (1, 6, 2, 40, 12, 1), (1, 3, 3, 29, 4, 29), (2, 2, 1, 50, 8, 100),
+     (1, 8, 2, 64, 16, 17)],
+)
+def test_matches_torch_autograd(oracle_mod, B, Hq, Hkv, L, D, window):
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=100 + L + window)
+    scale = 1.0 / math.sqrt(D)
+    r = oracle_mod.backward(q, k, v, dO, window, scale)
+    ref = _torch_reference(q, k, v, dO, window, scale)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[n], ref[n].numpy(), rtol=1e-10, atol=1e-12, err_msg=n)
+
+
+# ---------------------------------------------------------------------------
+# finite differences on loss = sum(dO * O)
+
+
+@pytest.mark.parametrize("window,G", [(0, 1), (3, 2), (7, 1), (1, 2)])
+def test_finite_differences(oracle_mod, window, G):
+    B, Hkv, L, D = 1, 2, 14, 6
+    Hq = G * Hkv
+    q = _rand64((B, Hq, L, D), 21)
+    k = _rand64((B, Hkv, L, D), 22)
+    v = _rand64((B, Hkv, L, D), 23)
+    dO = _rand64((B, Hq, L, D), 24)
+    scale = 0.45
+    r = oracle_mod.backward(q, k, v, dO, window, scale)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_mod.forward(qq, kk, vv, window, scale)
+        return float((o * dO.numpy()).sum())
+
+    rng = np.random.default_rng(7)
+    eps = 1e-6
+    for name, grad in (("q", r["dq"]), ("k", r["dk"]), ("v", r["dv"])):
+        base = {"q": q, "k": k, "v": v}
+        t = base[name]
+        for _ in range(12):
+            idx = tuple(int(rng.integers(0, s)) for s in t.shape)
+            plus = t.clone()
+            plus[idx] += eps
+            minus = t.clone()
+            minus[idx] -= eps
+            args_p = dict(base, **{name: plus})
+            args_m = dict(base, **{name: minus})
+            fd = (loss(args_p["q"], args_p["k"], args_p["v"]) - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+# ---------------------------------------------------------------------------
+# invariants
+
+
+def test_rows_of_P_sum_to_one(oracle_mod):
+    q, k, _, _ = make_inputs(1, 2, 1, 70, 16, seed=31)
+    v = torch.ones((1, 1, 70, 16), dtype=torch.bfloat16)
+    for window in (0, 9):
+        o, _ = oracle_mod.forward(q, k, v, window, 0.25)
+        assert np.max(np.abs(o - 1.0)) <= 1e-12
+
+
+@pytest.mark.parametrize("window", [0, 6])
+def test_dv_equals_PT_dO(oracle_mod, window):
+    B, Hq, Hkv, L, D = 1, 4, 2, 31, 8
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=41)
+    scale = 0.3
+    r = oracle_mod.backward(q, k, v, dO, window, scale)
+    qd, kd, gd = q.double().numpy(), k.double().numpy(), dO.double().numpy()
+    G = Hq // Hkv
+    i = np.arange(L)[:, None]
+    j = np.arange(L)[None, :]
+    keep = (j <= i) & ((window == 0) | (i - j < window))
+    dv = np.zeros_like(r["dv"])
+    for h in range(Hq):
+        s = scale * qd[0, h] @ kd[0, h // G].T
+        P = np.where(keep, np.exp(s - r["lse"][0, h][:, None]), 0.0)
+        dv[0, h // G] += P.T @ gd[0, h]
+    np.testing.assert_allclose(r["dv"], dv, rtol=1e-11, atol=1e-12)
+
+
+def test_delta_two_forms_agree(oracle_mod):
+    q, k, v, dO = make_inputs(1, 4, 2, 45, 16, seed=51)
+    r = oracle_mod.backward(q, k, v, dO, 8, 0.25)
+    assert r["delta_gap"] <= 1e-12
+    np.testing.assert_allclose(r["delta"], np.einsum("bhld,bhld->bhl", dO.double().numpy(), r["o"]), atol=1e-12)
+
+
+def test_window_at_least_L_is_causal_bitwise(oracle_mod):
+    q, k, v, dO = make_inputs(1, 2, 1, 40, 8, seed=61)
+    a = oracle_mod.backward(q, k, v, dO, 0, 0.35)
+    for w in (40, 41, 1000):
+        b = oracle_mod.backward(q, k, v, dO, w, 0.35)
+        for n in ("o", "lse", "dq", "dk", "dv"):
+            assert np.array_equal(a[n], b[n]), (w, n)
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_gqa_equals_repeated_kv(oracle_mod, window):
+    B, Hq, Hkv, L, D = 1, 6, 2, 27, 8
+    G = Hq // Hkv
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=71)
+    a = oracle_mod.backward(q, k, v, dO, window, 0.4)
+    kr = k.repeat_interleave(G, dim=1).contiguous()
+    vr = v.repeat_interleave(G, dim=1).contiguous()
+    b = oracle_mod.backward(q, kr, vr, dO, window, 0.4)
+    for n in ("o", "lse", "dq"):
+        np.testing.assert_allclose(a[n], b[n], rtol=1e-12, atol=1e-13)
+    for n in ("dk", "dv"):
+        np.testing.assert_allclose(a[n], b[n].reshape(B, Hkv, G, L, D).sum(2), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [0, 4])
+def test_masked_positions_get_exact_zero_gradient(oracle_mod, window):
+    B, Hq, Hkv, L, D = 1, 2, 1, 23, 8
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=81)
+    i0, h0 = 13, 1
+    dO = torch.zeros_like(dO)
+    dO[0, h0, i0] = torch.linspace(-1, 1, D).to(torch.bfloat16)
+    r = oracle_mod.backward(q, k, v, dO, window, 0.3)
+    band = [j for j in range(L) if j <= i0 and (window == 0 or i0 - j < window)]
+    off = [j for j in range(L) if j not in band]
+    assert np.all(r["dk"][0, 0, off] == 0.0) and np.all(r["dv"][0, 0, off] == 0.0)
+    others = [i for i in range(L) if i != i0]
+    assert np.all(r["dq"][0, h0, others] == 0.0) and np.all(r["dq"][0, 1 - h0] == 0.0)
+    assert np.any(r["dq"][0, h0, i0] != 0.0) and np.any(r["dk"][0, 0, band] != 0.0)
+
+
+def test_causality_bitwise(oracle_mod):
+    q, k, v, _ = make_inputs(1, 2, 1, 30, 8, seed=91)
+    o1, l1 = oracle_mod.forward(q, k, v, 6, 0.3)
+    k2, v2 = k.clone(), v.clone()
+    k2[0, 0, 20:] = 3.0
+    v2[0, 0, 20:] = -5.0
+    o2, l2 = oracle_mod.forward(q, k2, v2, 6, 0.3)
+    assert np.array_equal(o1[:, :, :20], o2[:, :, :20]) and np.array_equal(l1[:, :, :20], l2[:, :, :20])
+    assert not np.array_equal(o1[:, :, 20:], o2[:, :, 20:])
+
+
+# ---------------------------------------------------------------------------
+# the oracle's own modes and sampled entry points agree with its full mode
+
+
+@pytest.mark.parametrize("window", [0, 7])
+def test_band_mode_bitwise_equals_full(oracle_mod, window):
+    q, k, v, dO = make_inputs(1, 4, 2, 50, 16, seed=101)
+    a = oracle_mod.backward(q, k, v, dO, window, 0.25)
+    b = oracle_mod.backward(q, k, v, dO, window, 0.25, band_only=True)
+    for n in ("o", "lse", "delta", "dq", "dk", "dv"):
+        assert np.array_equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("band", [False, True])
+def test_sampled_rows_and_keys_match_full(oracle_mod, band):
+    q, k, v, dO = make_inputs(2, 4, 2, 48, 16, seed=111)
+    window = 9
+    full = oracle_mod.backward(q, k, v, dO, window, 0.25)
+    rows = [0, 5, 31, 47]
+    r = oracle_mod.rows(q, k, v, dO, window, 0.25, 1, 3, rows, band_only=band)
+    for n in ("o", "dq"):
+        assert np.array_equal(r[n], full[n][1, 3, rows]), n
+    for n in ("lse", "delta"):
+        assert np.array_equal(r[n], full[n][1, 3, rows]), n
+    keys = [0, 7, 40, 47]
+    kr = oracle_mod.key_rows(q, k, v, dO, window, 0.25, 1, 1, keys, band_only=band)
+    for n in ("dk", "dv"):
+        assert np.array_equal(kr[n], full[n][1, 1, keys]), n
