@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark: one step = forward (o, lse) + backward (Delta, dK/dV, dQ) of
+causal / sliding-window GQA attention over one synthetic workload, through
+the C ABI, on each GPU of one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Prints ONE JSON line on rank 0.  `value` is useful TFLOP/s summed over all
+ranks: in-band (query, key) pairs x (4 D forward + 10 D backward) flops,
+divided by the device time of the K timed steps (max over ranks).  Each rank
+runs its own independent copy of the workload (weak scaling, no collective on
+the data path).  L2 is flushed (256 MiB write) before every timed step and
+the flush is outside the timed events.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "causal_gqa_l8192_d128"
+METRIC = "windowed attn fwd+bwd useful TFLOP/s & % bf16 TC peak; peak workspace GB"
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+# per-kernel algorithmic flops per in-band (query, key) pair, in units of D
+KERNEL_FLOPS_PER_PAIR_D = {
+    "fwd_simt": 4,        # S = Q K^T, O += P V
+    "bwd_dkdv_simt": 8,   # S, dP recomputed; dV += P^T dO; dK += dS^T Q
+    "bwd_dq_simt": 6,     # S, dP recomputed; dQ += dS K
+}
+HBM_KERNELS = {"bwd_delta"}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sliding_window_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/ncu_traffic.txt),
+    or None when absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            if parts[3] == digest:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower() in ("active", "0x1", "1"):
+                    reasons.add(name)
+        loaded = [r["sm"] for r in rows if r["power"] > 0] or [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local_rank
+
+
+def _oracle_sample_inputs(w, Ls):
+    from sliding_window_attention_gb300.inputs import make_inputs
+
+    G = w.Hq // w.Hkv
+    return make_inputs(1, G, 1, Ls, w.D, w.seed, w.do_scale, w.outlier_frac, w.outlier_mult)
+
+
+def oracle_sample_seconds(w, Ls, inputs=None):
+    """Seconds the fp64 oracle takes for its complete forward + backward (band
+    mode) on one kv-head group (G query heads) over the first Ls tokens."""
+    import oracle
+
+    q, k, v, dO = inputs if inputs is not None else _oracle_sample_inputs(w, Ls)
+    t0 = time.perf_counter()
+    oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_length(w, target_s: float) -> int:
+    """Sequence length Ls whose oracle sample takes about target_s seconds
+    (cost model: proportional to the in-band pair count)."""
+    import oracle
+    from sliding_window_attention_gb300.inputs import band_pairs
+
+    oracle.build()
+    Ls = min(256, w.L)
+    t = oracle_sample_seconds(w, Ls)
+    for _ in range(4):
+        if t >= 0.6 * target_s or Ls >= w.L:
+            break
+        want_pairs = band_pairs(Ls, w.window) * target_s / max(t, 1e-3)
+        lo, hi = Ls, w.L
+        while lo < hi:
+            mid = (lo + hi + 1) // 2
+            if band_pairs(mid, w.window) <= want_pairs:
+                lo = mid
+            else:
+                hi = mid - 1
+        if lo <= Ls:
+            break
+        Ls = lo
+        t = oracle_sample_seconds(w, Ls)
+    return Ls
+
+
+def oracle_useful_flops(w, Ls) -> int:
+    from sliding_window_attention_gb300.inputs import band_pairs
+
+    return 14 * w.D * (w.Hq // w.Hkv) * band_pairs(Ls, w.window)
+
+
+def cpu_oracle_sample(w, target_s: float):
+    """(useful TFLOP/s, seconds, Ls, threads) of one oracle sample of ~target_s."""
+    import oracle
+
+    Ls = oracle_sample_length(w, target_s)
+    secs = oracle_sample_seconds(w, Ls)
+    return oracle_useful_flops(w, Ls) / secs / 1e12, secs, Ls, oracle.num_threads()
+
+
+def run_reference(args, w, world, rank):
+    """The reference arm: the fp64 CPU oracle on the host cores, each step a
+    bounded sample of the same workload (one kv-head group, first Ls tokens)."""
+    if rank != 0:
+        return 0
+    import oracle
+
+    steps, warm = args.steps, args.warmup
+    per_step = max(0.5, min(8.0, 150.0 / max(1, steps + warm)))
+    Ls = oracle_sample_length(w, per_step)
+    inputs = _oracle_sample_inputs(w, Ls)
+    secs = []
+    for it in range(warm + steps):
+        t = oracle_sample_seconds(w, Ls, inputs)
+        if it >= warm:
+            secs.append(t)
+    flops = oracle_useful_flops(w, Ls)
+    value = flops * steps / sum(secs) / 1e12
+    G = w.Hq // w.Hkv
+    sample = (f"fp64 oracle fwd+bwd (band mode) on 1 kv-head group ({G} query heads) x first {Ls} tokens "
+              f"of {w.name} per step; useful flops counted as on the GPU")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": round(1e3 * sum(secs) / steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "D": w.D,
+                   "window": w.window},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w, world, rank, local_rank):
+    import torch
+
+    import sliding_window_attention_gb300 as swa
+    from sliding_window_attention_gb300.inputs import make_inputs
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device(f"cuda:{local_rank}")
+    peaks = load_peaks()
+
+    # each rank: one independent copy of the workload (seed offset by rank)
+    q_h, k_h, v_h, dO_h = make_inputs(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed + 7919 * rank, w.do_scale,
+                                      w.outlier_frac, w.outlier_mult)
+    q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, dO_h))
+    B, Hq, Hkv, L, D, W = w.B, w.Hq, w.Hkv, w.L, w.D, w.window
+    f32 = dict(dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    base_mem = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    o = torch.empty((B, Hq, L, D), **f32)
+    lse = torch.empty((B, Hq, L), **f32)
+    dq = torch.empty((B, Hq, L, D), **f32)
+    dk = torch.empty((B, Hkv, L, D), **f32)
+    dv = torch.empty((B, Hkv, L, D), **f32)
+    fws_b = swa.fwd_workspace_bytes(B, Hq, Hkv, L, D, W)
+    bws_b = swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W)
+    fws = torch.empty(max(fws_b, 256), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(bws_b, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        swa.swa_attn_fwd(q, k, v, o, lse, W, w.scale, fws, stream)
+        swa.swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, W, w.scale, bws, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status = swa.swa_attn_get_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {swa.strerror(status)}")
+    peak_above_inputs = torch.cuda.max_memory_allocated(dev) - base_mem - L2_FLUSH_BYTES
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    swa.profile_begin()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    kernels = swa.profile_end()
+    if dist is not None:
+        dist.barrier()
+    clock_info = clocks.stop() if clocks else None
+    status = swa.swa_attn_get_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status after timed steps: {swa.strerror(status)}")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    useful = w.fwd_flops() + w.bwd_flops()
+    value = world * useful * args.steps / (total_ms / 1e3) / 1e12
+    launches = sum(n for n, _ in kernels.values())
+
+    # end to end through the public API: pinned host inputs in, results out
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    hq, hk, hv, hdO = (pin(t) for t in (q_h, k_h, v_h, dO_h))
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdO))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_steps = max(3, min(args.steps, 10))
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (dO, hdO)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs_h, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        es.record(stream)
+        e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += es.elapsed_time(ee)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * useful * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    # roofline of the dominant kernel
+    top = max(kernels.items(), key=lambda kv: kv[1][1])
+    kname, (kl, kms) = top
+    avg_s = kms / kl / 1e3
+    if kname in HBM_KERNELS:
+        alg = B * Hq * L * (D * 4 + D * 2 + 4)
+        achieved = alg / avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        per_pair = KERNEL_FLOPS_PER_PAIR_D.get(kname, 4)
+        alg = per_pair * D * w.pairs()
+        achieved = alg / avg_s / 1e12
+        if kname.endswith("_simt"):
+            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
+        else:
+            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "peak_source": f"{peaks['source']} bf16 dense (burst)"}
+    roof["kernel"] = kname
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    traffic = ncu_traffic(kname, w.name)
+    roof["traffic"] = traffic
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            tf, secs, Ls, threads = cpu_oracle_sample(w, args.cpu_seconds)
+            G = w.Hq // w.Hkv
+            cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"fp64 oracle fwd+bwd (band mode), 1 kv-head group ({G} query heads) x first {Ls} "
+                             f"tokens of {w.name}, {secs:.1f} s; useful flops counted as on the GPU"}
+        per_kernel = {n: {"launches": c, "avg_ms": round(ms / c, 4), "share": round(ms / sum(x[1] for x in
+                      kernels.values()), 4)} for n, (c, ms) in kernels.items()}
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if all(n.endswith("_simt") or n in HBM_KERNELS for n in kernels) else "bf16",
+            "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
+            "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "L": L, "D": D, "window": W,
+                       "scale": round(w.scale, 6), "parallelism": f"replicas x{world} (one workload per GPU)",
+                       "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clock_info,
+            "kernels": per_kernel,
+            "workspace_gb": {"fwd": round(fws_b / 1e9, 4), "bwd": round(bws_b / 1e9, 4),
+                             "peak_above_inputs": round(peak_above_inputs / 1e9, 4)},
+            "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+            "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from sliding_window_attention_gb300.inputs import WORKLOADS
+
+    if args.workload not in WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
+    w = WORKLOADS[args.workload]
+    world, rank, local_rank = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+    return run_ours(args, w, world, rank, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

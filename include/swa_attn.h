@@ -1,0 +1,146 @@
+/*
+ * swa_attn.h -- C ABI of the GB300 (sm_103a) causal / sliding-window
+ * grouped-query attention library: forward with per-row logsumexp, and an
+ * O(L*D)-memory backward that never forms the L x L score matrix and skips
+ * every key tile outside the causal / window band.
+ *
+ * The operation (page "Lab 028 lab detail: Off NVIDIA, you fix the platform
+ * yourself", sections "Plan for the build" step 4 and "What I changed, in
+ * plain terms" items 1-5; page "Training -- design (ORPO, flash-CCE head,
+ * prefix sharing, segmented backward)" sections 5.2 and 6):
+ *
+ *   band(i) = { j : j <= i  and  (window == 0  or  i - j < window) }
+ *   s_ij    = scale * q_i . k_j              (j in band(i))
+ *   lse_i   = ln sum_{j in band(i)} exp(s_ij)
+ *   o_i     = sum_{j in band(i)} exp(s_ij - lse_i) v_j
+ *
+ * window == 0 means plain causal; window >= L is the same as causal.  A key
+ * that is window or more positions behind the query is masked ("zero P where
+ * j < i + diag_off - window_size + 1", diag_off = 0 here: queries and keys
+ * have the same length L).  Query head h reads kv head h / (Hq / Hkv)
+ * (page "MiniCPM5 Decode Megakernel -- end-to-end build plan", section 4.1
+ * stage 5).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are dense row-major [B, H, L, D]; lse is [B, Hq, L].
+ *  - q, k, v, dO hold bf16 values (raw 16-bit patterns, swa_bf16).
+ *    o, lse, dq, dk, dv are fp32.
+ *  - All tensor and workspace pointers are DEVICE pointers owned by the
+ *    caller.  The library allocates no device or host memory on these
+ *    paths.  Every output is fully overwritten (no accumulate-into).
+ *  - Tensor pointers must be 16-byte aligned; the workspace 256-byte aligned.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) of the current device, which must be an sm_103
+ *    GPU.  Return values report argument and launch errors only; failures
+ *    detected on the device (a bounded wait that ran out) are latched in a
+ *    per-device status word read by swa_attn_get_status().
+ *  - Supported head dims: 64, 128, 256, 512.  scale is any finite float.
+ *  - Thread safety: calls on different streams may overlap if they use
+ *    different workspaces.
+ */
+#ifndef SWA_ATTN_H
+#define SWA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t swa_bf16; /* bf16 bit pattern */
+
+/* Return codes (0 = success, negative = error). */
+#define SWA_OK 0
+#define SWA_ERR_NULL_POINTER -1   /* a required pointer is NULL */
+#define SWA_ERR_BAD_SHAPE -2      /* B, Hq, Hkv or L < 1 */
+#define SWA_ERR_BAD_GROUPS -3     /* Hq is not a multiple of Hkv */
+#define SWA_ERR_BAD_HEAD_DIM -4   /* D not in {64, 128, 256, 512} */
+#define SWA_ERR_BAD_WINDOW -5     /* window < 0 */
+#define SWA_ERR_BAD_SCALE -6      /* scale is NaN or infinite */
+#define SWA_ERR_MISALIGNED -7     /* tensor not 16-B or workspace not 256-B aligned */
+#define SWA_ERR_WORKSPACE -8      /* workspace_bytes below the query's value */
+#define SWA_ERR_CUDA -9           /* CUDA runtime / launch error */
+#define SWA_ERR_TOO_LARGE -10     /* sizes exceed the supported index range */
+#define SWA_ERR_DEVICE_TIMEOUT -11 /* a bounded device-side wait expired */
+#define SWA_ERR_UNSUPPORTED_DEVICE -12 /* current device is not sm_103 */
+
+/*
+ * Workspace bytes swa_attn_fwd needs for this shape (may be 0; a NULL
+ * workspace is then accepted).  Pure host function, no CUDA calls.
+ */
+size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window);
+
+/*
+ * Forward.  Reads q [B,Hq,L,D], k and v [B,Hkv,L,D] (bf16); writes
+ * o [B,Hq,L,D] (fp32, normalised attention output) and lse [B,Hq,L] (fp32,
+ * natural-log sum over the band of exp(scale * q_i . k_j)).  The forward
+ * writes the logsumexp the backward reuses ("Lab 028 lab detail", "What I
+ * changed, in plain terms" item 1).
+ * Returns SWA_OK or a negative SWA_ERR_* code; on an argument error nothing
+ * is enqueued.
+ */
+int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse,
+                 int B, int Hq, int Hkv, int L, int D, int window, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes swa_attn_bwd needs for this shape: O(B*Hq*L) floats for
+ * the row term Delta plus any per-call operand staging.  Pure host function.
+ */
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window);
+
+/*
+ * Backward of o with respect to q, k, v given the upstream gradient dO.
+ * Reads q, k, v, dO (bf16), o and lse (fp32, from swa_attn_fwd with the same
+ * arguments); writes dq [B,Hq,L,D], dk and dv [B,Hkv,L,D] (fp32).
+ * Recomputes P from lse instead of storing it ("Training -- design",
+ * section 6: store per-row LSE, recompute P), computes
+ * Delta_i = dO_i . o_i, dS = P (dP - Delta), and visits only key/query tile
+ * pairs that intersect the band ("Lab 028 lab detail", "What I changed, in
+ * plain terms" item 3).  dk and dv sum over the Hq/Hkv query heads of each
+ * kv head.  Deterministic: no floating-point atomics.
+ * Returns SWA_OK or a negative SWA_ERR_* code; on an argument error nothing
+ * is enqueued.
+ */
+int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o,
+                 const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv,
+                 int B, int Hq, int Hkv, int L, int D, int window, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Device-side status of the current device: synchronises `stream`, returns
+ * the first SWA_ERR_* code latched by a kernel since the previous call (or
+ * SWA_OK), and clears it.  Returns SWA_ERR_CUDA if the CUDA calls fail.
+ */
+int swa_attn_get_status(void* stream);
+
+/* Static, human-readable description of a return code. */
+const char* swa_attn_strerror(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int swa_attn_version(void);
+
+/*
+ * Optional kernel timing, for benchmarks.  Between swa_attn_profile_begin()
+ * and swa_attn_profile_end(), every kernel this library launches (from any
+ * host thread, on any stream of any device) is bracketed by two CUDA events
+ * recorded on the launch stream.  profile_end() waits for those events and
+ * writes per-kernel totals into out[0 .. *n_out - 1] (at most max_entries;
+ * kernels are named by what they compute).  This mode allocates host memory
+ * and CUDA events; it is the only one that does.
+ */
+typedef struct {
+    char name[48];       /* kernel name, NUL-terminated */
+    long long launches;  /* launches recorded */
+    double total_ms;     /* summed event-measured duration */
+} swa_attn_kernel_time;
+
+int swa_attn_profile_begin(void);
+int swa_attn_profile_end(swa_attn_kernel_time* out, int max_entries, int* n_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_ATTN_H */

@@ -1,0 +1,26 @@
+"""GB300 (sm_103a) causal / sliding-window grouped-query attention.
+
+The compute lives in libswa_attn.so (C ABI, include/swa_attn.h); this
+package is its thin Python binding plus the seeded input generators.
+The library is loaded on first use and every call fails loudly if it is
+missing: there is no CPU fallback.
+"""
+from ._native import (  # noqa: F401
+    SwaError,
+    backward,
+    bwd_workspace_bytes,
+    forward,
+    fwd_workspace_bytes,
+    load,
+    profile_begin,
+    profile_end,
+    strerror,
+    swa_attn_bwd,
+    swa_attn_fwd,
+    swa_attn_get_status,
+)
+
+__all__ = [
+    "SwaError", "backward", "bwd_workspace_bytes", "forward", "fwd_workspace_bytes", "load", "profile_begin", "profile_end", "strerror",
+    "swa_attn_bwd", "swa_attn_fwd", "swa_attn_get_status",
+]

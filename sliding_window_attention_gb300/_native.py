@@ -1,0 +1,185 @@
+"""Thin ctypes binding of libswa_attn.so (include/swa_attn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  There is no CPU fallback; if the library is
+missing or was not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+SO_PATH = os.path.join(_PKG, "libswa_attn.so")
+
+# names declared in include/swa_attn.h
+EXPORTED = (
+    "swa_attn_fwd_workspace_bytes",
+    "swa_attn_fwd",
+    "swa_attn_bwd_workspace_bytes",
+    "swa_attn_bwd",
+    "swa_attn_get_status",
+    "swa_attn_strerror",
+    "swa_attn_version",
+    "swa_attn_profile_begin",
+    "swa_attn_profile_end",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SwaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or SO_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} not found: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        I, Z, P, F = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+        shape = [I, I, I, I, I, I]
+        lib.swa_attn_fwd_workspace_bytes.argtypes = shape
+        lib.swa_attn_fwd_workspace_bytes.restype = Z
+        lib.swa_attn_bwd_workspace_bytes.argtypes = shape
+        lib.swa_attn_bwd_workspace_bytes.restype = Z
+        lib.swa_attn_fwd.argtypes = [P, P, P, P, P] + shape + [F, P, Z, P]
+        lib.swa_attn_fwd.restype = I
+        lib.swa_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P] + shape + [F, P, Z, P]
+        lib.swa_attn_bwd.restype = I
+        lib.swa_attn_get_status.argtypes = [P]
+        lib.swa_attn_get_status.restype = I
+        lib.swa_attn_strerror.argtypes = [I]
+        lib.swa_attn_strerror.restype = ctypes.c_char_p
+        lib.swa_attn_version.argtypes = []
+        lib.swa_attn_version.restype = I
+        lib.swa_attn_profile_begin.argtypes = []
+        lib.swa_attn_profile_begin.restype = I
+        lib.swa_attn_profile_end.argtypes = [P, I, ctypes.POINTER(I)]
+        lib.swa_attn_profile_end.restype = I
+        _lib = lib
+        return lib
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_longlong), ("total_ms", ctypes.c_double)]
+
+
+def profile_begin() -> None:
+    rc = load().swa_attn_profile_begin()
+    if rc:
+        raise SwaError(rc, "swa_attn_profile_begin")
+
+
+def profile_end(max_entries: int = 32) -> dict:
+    """Return {kernel name: (launches, total_ms)} recorded since profile_begin()."""
+    buf = (KernelTime * max_entries)()
+    n = ctypes.c_int(0)
+    rc = load().swa_attn_profile_end(buf, max_entries, ctypes.byref(n))
+    if rc:
+        raise SwaError(rc, "swa_attn_profile_end")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n.value)}
+
+
+def strerror(code: int) -> str:
+    return load().swa_attn_strerror(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dims(q, k, D=None):
+    B, Hq, L, D_ = q.shape
+    Hkv = k.shape[1]
+    return B, Hq, Hkv, L, D_
+
+
+def fwd_workspace_bytes(B, Hq, Hkv, L, D, window) -> int:
+    return int(load().swa_attn_fwd_workspace_bytes(B, Hq, Hkv, L, D, window))
+
+
+def bwd_workspace_bytes(B, Hq, Hkv, L, D, window) -> int:
+    return int(load().swa_attn_bwd_workspace_bytes(B, Hq, Hkv, L, D, window))
+
+
+def swa_attn_fwd(q, k, v, o, lse, window: int, scale: float, workspace=None, stream=None) -> None:
+    """Forward through the C ABI.  q,k,v: bf16 CUDA tensors [B,H,L,D]; o fp32
+    [B,Hq,L,D] and lse fp32 [B,Hq,L] are caller-allocated outputs."""
+    B, Hq, Hkv, L, D = _dims(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, D, int(window),
+                             float(scale), _ptr(workspace), nbytes, _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_fwd")
+
+
+def swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: float, workspace=None, stream=None) -> None:
+    """Backward through the C ABI; dq, dk, dv are caller-allocated fp32 outputs."""
+    B, Hq, Hkv, L, D = _dims(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                             _ptr(dv), B, Hq, Hkv, L, D, int(window), float(scale), _ptr(workspace), nbytes,
+                             _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_bwd")
+
+
+def swa_attn_get_status(stream=None) -> int:
+    return int(load().swa_attn_get_status(_stream_ptr(stream)))
+
+
+# ---------------------------------------------------------------------------
+# convenience wrappers: allocate outputs / workspace with torch, call the ABI
+
+
+def _workspace(nbytes, device):
+    import torch
+
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def forward(q, k, v, window: int, scale: float, stream=None):
+    """Return (o fp32, lse fp32) for bf16 CUDA tensors q [B,Hq,L,D], k/v [B,Hkv,L,D]."""
+    import torch
+
+    B, Hq, Hkv, L, D = _dims(q, k)
+    o = torch.empty((B, Hq, L, D), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    ws = _workspace(fwd_workspace_bytes(B, Hq, Hkv, L, D, window), q.device)
+    swa_attn_fwd(q, k, v, o, lse, window, scale, ws, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None):
+    """Return (dq, dk, dv) fp32."""
+    import torch
+
+    B, Hq, Hkv, L, D = _dims(q, k)
+    dq = torch.empty((B, Hq, L, D), dtype=torch.float32, device=q.device)
+    dk = torch.empty((B, Hkv, L, D), dtype=torch.float32, device=q.device)
+    dv = torch.empty((B, Hkv, L, D), dtype=torch.float32, device=q.device)
+    ws = _workspace(bwd_workspace_bytes(B, Hq, Hkv, L, D, window), q.device)
+    swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, window, scale, ws, stream)
+    return dq, dk, dv

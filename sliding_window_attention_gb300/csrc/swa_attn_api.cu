@@ -1,0 +1,260 @@
+// C-ABI entry points: argument validation, workspace layout, the per-device
+// status word, and launch orchestration on the caller's stream.  Every step
+// of the computation runs in the kernels; this file only checks arguments
+// and enqueues launches.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/swa_attn.h"
+#include "swa_internal.h"
+
+namespace {
+
+// ---- optional per-launch event timing (swa_attn_profile_begin/end) ----
+struct ProfRec {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+
+// Runs `f` (which enqueues one kernel on `s`); brackets it with events when
+// profiling is on.
+template <typename F>
+cudaError_t launch(const char* name, cudaStream_t s, F&& f) {
+  bool on;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    on = g_prof_on;
+  }
+  if (!on) return f();
+  ProfRec r{name, nullptr, nullptr};
+  if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess) return cudaErrorUnknown;
+  cudaEventRecord(r.start, s);
+  const cudaError_t e = f();
+  cudaEventRecord(r.stop, s);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_recs.push_back(r);
+  return e;
+}
+
+constexpr int kMaxDevices = 64;
+
+// Per-device status word: kernels latch the first device-side error here.
+__device__ int g_status_word;
+
+int* status_ptr_for_current_device(int* err) {
+  static int* cached[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = SWA_ERR_CUDA;
+    return nullptr;
+  }
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+      *err = SWA_ERR_CUDA;
+      return nullptr;
+    }
+    cached[dev] = static_cast<int*>(p);
+  }
+  *err = SWA_OK;
+  return cached[dev];
+}
+
+int check_device() {
+  static int ok_cache[kMaxDevices] = {0};  // 0 unknown, 1 ok, -1 bad
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SWA_ERR_CUDA;
+  if (ok_cache[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    ok_cache[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return ok_cache[dev] == 1 ? SWA_OK : SWA_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_shape(int B, int Hq, int Hkv, int L, int D, int window, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return SWA_ERR_BAD_SHAPE;
+  if (Hq % Hkv != 0) return SWA_ERR_BAD_GROUPS;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return SWA_ERR_BAD_HEAD_DIM;
+  if (window < 0) return SWA_ERR_BAD_WINDOW;
+  if (!isfinite(scale)) return SWA_ERR_BAD_SCALE;
+  // grid.y / grid.z carry heads and batch; element offsets must fit in int64 comfortably
+  if (Hq > 65535 || B > 65535) return SWA_ERR_TOO_LARGE;
+  const double elems = (double)B * Hq * L * D;
+  if (elems > 9.0e15) return SWA_ERR_TOO_LARGE;
+  return SWA_OK;
+}
+
+swa::Geom make_geom(int B, int Hq, int Hkv, int L, int D, int window, float scale) {
+  swa::Geom g;
+  g.B = B;
+  g.Hq = Hq;
+  g.Hkv = Hkv;
+  g.L = L;
+  g.D = D;
+  g.W = (window >= L) ? 0 : window;  // a window of L or more is plain causal
+  g.G = Hq / Hkv;
+  g.scale = scale;
+  return g;
+}
+
+// Backward workspace layout: [Delta: B*Hq*L fp32].
+size_t bwd_delta_bytes(int B, int Hq, int L) { return round_up((size_t)B * Hq * L * sizeof(float), 256); }
+
+}  // namespace
+
+extern "C" {
+
+int swa_attn_version(void) { return 100; }
+
+const char* swa_attn_strerror(int code) {
+  switch (code) {
+    case SWA_OK: return "success";
+    case SWA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case SWA_ERR_BAD_SHAPE: return "B, Hq, Hkv and L must be >= 1";
+    case SWA_ERR_BAD_GROUPS: return "Hq must be a multiple of Hkv";
+    case SWA_ERR_BAD_HEAD_DIM: return "head dim D must be 64, 128, 256 or 512";
+    case SWA_ERR_BAD_WINDOW: return "window must be >= 0 (0 = plain causal)";
+    case SWA_ERR_BAD_SCALE: return "scale must be finite";
+    case SWA_ERR_MISALIGNED: return "tensors must be 16-byte aligned and the workspace 256-byte aligned";
+    case SWA_ERR_WORKSPACE: return "workspace smaller than the size query returned";
+    case SWA_ERR_CUDA: return "CUDA runtime or launch error";
+    case SWA_ERR_TOO_LARGE: return "sizes exceed the supported range";
+    case SWA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+    case SWA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown error code";
+  }
+}
+
+size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
+  (void)B, (void)Hq, (void)Hkv, (void)L, (void)D, (void)window;
+  return 0;
+}
+
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
+  (void)Hkv, (void)D, (void)window;
+  if (B < 1 || Hq < 1 || L < 1) return 0;
+  return bwd_delta_bytes(B, Hq, L);
+}
+
+int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
+                 int Hkv, int L, int D, int window, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  if (!q || !k || !v || !o || !lse) return SWA_ERR_NULL_POINTER;
+  int rc = check_shape(B, Hq, Hkv, L, D, window, scale);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
+      !aligned(workspace, 256))
+    return SWA_ERR_MISALIGNED;
+  const size_t need = swa_attn_fwd_workspace_bytes(B, Hq, Hkv, L, D, window);
+  if (workspace_bytes < need || (need > 0 && !workspace)) return SWA_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  const swa::Geom g = make_geom(B, Hq, Hkv, L, D, window, scale);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch("fwd_simt", s, [&] { return swa::launch_fwd_simt(g, q, k, v, o, lse, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
+                 const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int L, int D,
+                 int window, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return SWA_ERR_NULL_POINTER;
+  int rc = check_shape(B, Hq, Hkv, L, D, window, scale);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
+      !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
+    return SWA_ERR_MISALIGNED;
+  const size_t need = swa_attn_bwd_workspace_bytes(B, Hq, Hkv, L, D, window);
+  if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  const swa::Geom g = make_geom(B, Hq, Hkv, L, D, window, scale);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* delta = static_cast<float*>(workspace);
+  if (launch("bwd_delta", s, [&] { return swa::launch_delta(g, o, dO, delta, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (launch("bwd_dkdv_simt", s,
+             [&] { return swa::launch_bwd_dkdv_simt(g, q, k, v, dO, lse, delta, dk, dv, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (launch("bwd_dq_simt", s, [&] { return swa::launch_bwd_dq_simt(g, q, k, v, dO, lse, delta, dq, s); }) !=
+      cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+int swa_attn_get_status(void* stream) {
+  int err = SWA_OK;
+  int* p = status_ptr_for_current_device(&err);
+  if (!p) return err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SWA_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return SWA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SWA_ERR_CUDA;
+  return host;
+}
+
+int swa_attn_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof_recs) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof_recs.clear();
+  g_prof_on = true;
+  return SWA_OK;
+}
+
+int swa_attn_profile_end(swa_attn_kernel_time* out, int max_entries, int* n_out) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = false;
+    recs.swap(g_prof_recs);
+  }
+  int rc = SWA_OK;
+  std::vector<swa_attn_kernel_time> agg;
+  for (auto& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      rc = SWA_ERR_CUDA;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+    size_t idx = 0;
+    while (idx < agg.size() && strncmp(agg[idx].name, r.name.c_str(), sizeof(agg[idx].name)) != 0) ++idx;
+    if (idx == agg.size()) {
+      swa_attn_kernel_time t;
+      memset(&t, 0, sizeof t);
+      strncpy(t.name, r.name.c_str(), sizeof(t.name) - 1);
+      agg.push_back(t);
+    }
+    agg[idx].launches += 1;
+    agg[idx].total_ms += ms;
+  }
+  int n = 0;
+  for (size_t i = 0; i < agg.size() && n < max_entries; ++i) {
+    if (out) out[n] = agg[i];
+    ++n;
+  }
+  if (n_out) *n_out = n;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// Internal interface between the C-ABI translation unit and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace swa {
+
+// Problem geometry shared by every kernel.
+struct Geom {
+  int B, Hq, Hkv, L, D, W, G;  // G = Hq / Hkv; W = 0 means plain causal
+  float scale;                 // softmax scale applied to q . k
+};
+
+// Device-side status codes latched into the per-device status word.
+enum : int { kStatusOk = 0, kStatusTimeout = -11 };
+
+// ---- SIMT kernels (fp32 arithmetic on bf16 inputs; any D in {64..512}) ----
+cudaError_t launch_fwd_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            float* o, float* lse, cudaStream_t s);
+cudaError_t launch_delta(const Geom& g, const float* o, const uint16_t* dO, float* delta, cudaStream_t s);
+cudaError_t launch_bwd_dkdv_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 const uint16_t* dO, const float* lse, const float* delta, float* dk,
+                                 float* dv, cudaStream_t s);
+cudaError_t launch_bwd_dq_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const uint16_t* dO, const float* lse, const float* delta, float* dq,
+                               cudaStream_t s);
+
+}  // namespace swa

@@ -1,0 +1,98 @@
+"""Host-only checks of the C-ABI library: it loads without a GPU, exports every
+symbol include/swa_attn.h declares, and rejects bad arguments before any CUDA
+call (so these run on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sliding_window_attention_gb300 import build as b
+    from sliding_window_attention_gb300 import _native
+
+    b.build()
+    return _native.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_attn_\w+)\s*\(", text)))
+
+
+def declared_codes():
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (SWA_\w+) (-?\d+)", open(HEADER).read())}
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    from sliding_window_attention_gb300 import _native
+
+    assert sorted(_native.EXPORTED) == names
+
+
+def test_strerror_covers_every_code(lib):
+    for name, code in declared_codes().items():
+        s = lib.swa_attn_strerror(code).decode()
+        assert s and s != "unknown error code", name
+    assert lib.swa_attn_strerror(12345).decode() == "unknown error code"
+    assert lib.swa_attn_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    # backward: at least one fp32 Delta per query row, O(L*D) at most
+    for (B, Hq, Hkv, L, D, W) in [(1, 2, 1, 256, 64, 64), (1, 32, 16, 30553, 256, 1024), (1, 32, 4, 16384, 512, 0)]:
+        nb = lib.swa_attn_bwd_workspace_bytes(B, Hq, Hkv, L, D, W)
+        assert nb >= B * Hq * L * 4
+        assert nb <= 8 * B * Hq * L * D + (1 << 20)
+        assert nb % 256 == 0
+        nf = lib.swa_attn_fwd_workspace_bytes(B, Hq, Hkv, L, D, W)
+        assert nf <= 8 * B * Hq * L * D + (1 << 20)
+        assert nf % 256 == 0
+
+
+def _fwd(lib, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, Hq=2, Hkv=1, L=16, D=64, W=0, scale=0.125,
+         ws=None, wsb=0):
+    P = ctypes.c_void_p
+    return lib.swa_attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, Hq, Hkv, L, D, W, ctypes.c_float(scale), P(ws), wsb,
+                            None)
+
+
+def _bwd(lib, ptrs=None, B=1, Hq=2, Hkv=1, L=16, D=64, W=0, scale=0.125, ws=0x10000, wsb=1 << 20):
+    P = ctypes.c_void_p
+    ptrs = ptrs or [0x1000 * (i + 1) for i in range(9)]
+    return lib.swa_attn_bwd(*(P(p) for p in ptrs), B, Hq, Hkv, L, D, W, ctypes.c_float(scale), P(ws), wsb, None)
+
+
+def test_argument_errors_are_reported_before_any_cuda_call(lib):
+    c = declared_codes()
+    assert _fwd(lib, q=0) == c["SWA_ERR_NULL_POINTER"]
+    assert _fwd(lib, B=0) == c["SWA_ERR_BAD_SHAPE"]
+    assert _fwd(lib, L=0) == c["SWA_ERR_BAD_SHAPE"]
+    assert _fwd(lib, Hq=3, Hkv=2) == c["SWA_ERR_BAD_GROUPS"]
+    assert _fwd(lib, D=96) == c["SWA_ERR_BAD_HEAD_DIM"]
+    assert _fwd(lib, W=-1) == c["SWA_ERR_BAD_WINDOW"]
+    assert _fwd(lib, scale=float("nan")) == c["SWA_ERR_BAD_SCALE"]
+    assert _fwd(lib, scale=float("inf")) == c["SWA_ERR_BAD_SCALE"]
+    assert _fwd(lib, q=0x1008) == c["SWA_ERR_MISALIGNED"]
+    assert _fwd(lib, Hq=70000, Hkv=1) == c["SWA_ERR_TOO_LARGE"]
+    ptrs = [0x1000 * (i + 1) for i in range(9)]
+    for idx in range(9):
+        bad = list(ptrs)
+        bad[idx] = 0
+        assert _bwd(lib, bad) == c["SWA_ERR_NULL_POINTER"], idx
+        bad[idx] = ptrs[idx] + 4
+        assert _bwd(lib, bad) == c["SWA_ERR_MISALIGNED"], idx
+    assert _bwd(lib, ws=0x10010) == c["SWA_ERR_MISALIGNED"]
+    assert _bwd(lib, wsb=16) == c["SWA_ERR_WORKSPACE"]
+    assert _bwd(lib, ws=0) == c["SWA_ERR_WORKSPACE"]
+    assert _bwd(lib, D=32) == c["SWA_ERR_BAD_HEAD_DIM"]

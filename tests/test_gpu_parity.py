@@ -1,0 +1,217 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded bf16 inputs.
+
+Small shapes are compared element by element over every output; the named
+full-size workloads are compared on sampled rows (o, lse, dq) and key rows
+(dk, dv) that the oracle computes one by one, plus properties that hold at
+any size.  The bar is in helpers.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close, assert_lse_close, errors, gpu_fwd_bwd
+from sliding_window_attention_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # B, Hq, Hkv, L, D, window
+    (1, 2, 1, 256, 64, 64),
+    (2, 4, 2, 300, 64, 0),
+    (1, 4, 1, 129, 128, 7),
+    (1, 2, 2, 1, 64, 0),
+    (1, 2, 1, 2, 128, 1),
+    (1, 4, 2, 127, 256, 128),
+    (1, 2, 1, 383, 512, 129),
+    (1, 8, 2, 515, 128, 1000),
+    (1, 4, 4, 1000, 64, 127),
+    (2, 2, 1, 257, 256, 1),
+    (1, 4, 2, 700, 512, 0),
+    (1, 2, 1, 1100, 128, 300),
+    (1, 4, 1, 2048, 512, 0),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,D,window", SMALL)
+def test_small_shapes_elementwise(oracle_mod, B, Hq, Hkv, L, D, window):
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=1000 + L + D + window)
+    scale = 1.0 / math.sqrt(D)
+    ref = oracle_mod.backward(q, k, v, dO, window, scale, band_only=True)
+    got = gpu_fwd_bwd(q, k, v, dO, window, scale)
+    assert_lse_close(got["lse"].numpy(), ref["lse"])
+    for n in ("o", "dq", "dk", "dv"):
+        assert_close(n, got[n].numpy(), ref[n])
+
+
+def test_tiny_workload_elementwise(oracle_mod):
+    w = WORKLOADS["tiny_l256_d64_w64"]
+    q, k, v, dO = workload_inputs(w)
+    ref = oracle_mod.backward(q, k, v, dO, w.window, w.scale)
+    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale)
+    assert_lse_close(got["lse"].numpy(), ref["lse"])
+    for n in ("o", "dq", "dk", "dv"):
+        assert_close(n, got[n].numpy(), ref[n])
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled outputs + any-size properties
+
+
+def _sample_rows(L, window, rng, n_random=6):
+    cand = {0, 1, 63, 64, 127, 128, 129, L // 2, L - 2, L - 1, L - (L % 128 or 128)}
+    if window:
+        cand |= {window - 1, window, window + 1}
+    cand |= set(int(x) for x in rng.integers(0, L, n_random))
+    return sorted(i for i in cand if 0 <= i < L)
+
+
+def _sample_keys(w, rng):
+    """Key rows whose oracle cost stays within seconds: the key's column needs
+    every query row that sees it, so for long causal rows keep keys late."""
+    L = w.L
+    if w.window:
+        lo = 0
+    else:
+        # rows [lo, L) each cost up to L keys; keep G * D * (L^2 - lo^2) bounded
+        budget = 4.0e9
+        G = w.Hq // w.Hkv
+        lo2 = max(0.0, L * L - budget / (G * w.D) * 2)
+        lo = int(math.sqrt(lo2))
+    cand = {lo, lo + 1, L - 1, L - 2, L - 129, L - 128, (lo + L) // 2}
+    cand |= set(int(x) for x in rng.integers(lo, L, 5))
+    return sorted(j for j in cand if lo <= j < L)
+
+
+@pytest.fixture(scope="module", params=[n for n in WORKLOADS if not n.startswith("tiny")])
+def full_run(request):
+    w = WORKLOADS[request.param]
+    q, k, v, dO = workload_inputs(w)
+    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale)
+    return w, (q, k, v, dO), got
+
+
+def test_full_workload_sampled(oracle_mod, full_run):
+    w, (q, k, v, dO), got = full_run
+    rng = np.random.default_rng(w.seed)
+    G = w.Hq // w.Hkv
+    for name in ("o", "dq", "dk", "dv", "lse"):
+        assert torch.isfinite(got[name]).all(), name
+    heads = sorted({0, w.Hq - 1, G, w.Hq // 2})
+    rows = _sample_rows(w.L, w.window, rng)
+    for h in heads:
+        r = oracle_mod.rows(q, k, v, dO, w.window, w.scale, 0, h, rows, band_only=True)
+        assert_lse_close(got["lse"][0, h, rows].numpy(), r["lse"])
+        assert_close(f"o[h={h}]", got["o"][0, h, rows].numpy(), r["o"])
+        assert_close(f"dq[h={h}]", got["dq"][0, h, rows].numpy(), r["dq"])
+    keys = _sample_keys(w, rng)
+    for kvh in sorted({0, w.Hkv - 1}):
+        r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True)
+        assert_close(f"dk[kvh={kvh}]", got["dk"][0, kvh, keys].numpy(), r["dk"])
+        assert_close(f"dv[kvh={kvh}]", got["dv"][0, kvh, keys].numpy(), r["dv"])
+
+
+def test_full_workload_properties(full_run):
+    """Any-size identities of the exact result: rows of P sum to one, so
+    sum_j dv_j = sum over the group's heads and all rows of dO; rows of dS sum
+    to zero, so sum_j dk_j = 0."""
+    w, (q, k, v, dO), got = full_run
+    G = w.Hq // w.Hkv
+    dv_sum = got["dv"].double().sum(2)                                  # [B, Hkv, D]
+    want = dO.double().view(w.B, w.Hkv, G, w.L, w.D).sum((2, 3))        # [B, Hkv, D]
+    ma, rf = errors(dv_sum.numpy(), want.numpy())
+    assert rf <= 1e-3, (ma, rf)
+    dk_sum = got["dk"].double().sum(2)
+    scale_ref = got["dk"].double().abs().sum(2).max().item()
+    assert dk_sum.abs().max().item() <= 1e-3 * scale_ref
+
+
+# ---------------------------------------------------------------------------
+# invariants on the GPU
+
+
+def test_deterministic_bitwise():
+    q, k, v, dO = make_inputs(1, 4, 2, 777, 128, seed=5)
+    a = gpu_fwd_bwd(q, k, v, dO, 100, 0.09)
+    b = gpu_fwd_bwd(q, k, v, dO, 100, 0.09)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_outputs_fully_overwritten():
+    import sliding_window_attention_gb300 as swa
+
+    B, Hq, Hkv, L, D, W = 1, 4, 2, 333, 64, 50
+    q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, L, D, seed=6))
+    nan = float("nan")
+    o = torch.full((B, Hq, L, D), nan, device="cuda")
+    lse = torch.full((B, Hq, L), nan, device="cuda")
+    swa.swa_attn_fwd(q, k, v, o, lse, W, 0.125)
+    dq = torch.full((B, Hq, L, D), nan, device="cuda")
+    dk = torch.full((B, Hkv, L, D), nan, device="cuda")
+    dv = torch.full((B, Hkv, L, D), nan, device="cuda")
+    ws = torch.full((swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W),), 0xFF, dtype=torch.uint8, device="cuda")
+    swa.swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, W, 0.125, ws)
+    torch.cuda.synchronize()
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_exact_zero_gradient_off_band(window):
+    B, Hq, Hkv, L, D = 1, 2, 1, 300, 64
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=7)
+    i0, h0 = 200, 1
+    dO = torch.zeros_like(dO)
+    dO[0, h0, i0] = torch.linspace(-1, 1, D).to(torch.bfloat16)
+    got = gpu_fwd_bwd(q, k, v, dO, window, 0.125)
+    band = [j for j in range(L) if j <= i0 and (window == 0 or i0 - j < window)]
+    off = [j for j in range(L) if j not in band]
+    assert (got["dk"][0, 0, off] == 0).all() and (got["dv"][0, 0, off] == 0).all()
+    others = [i for i in range(L) if i != i0]
+    assert (got["dq"][0, h0, others] == 0).all() and (got["dq"][0, 1 - h0] == 0).all()
+
+
+def test_causality_bitwise():
+    q, k, v, dO = make_inputs(1, 2, 1, 400, 128, seed=8)
+    a = gpu_fwd_bwd(q, k, v, dO, 0, 0.1)
+    k2, v2 = k.clone(), v.clone()
+    k2[0, 0, 260:] = 30.0
+    v2[0, 0, 260:] = -50.0
+    b = gpu_fwd_bwd(q, k2, v2, dO, 0, 0.1)
+    assert torch.equal(a["o"][:, :, :260], b["o"][:, :, :260])
+    assert torch.equal(a["lse"][:, :, :260], b["lse"][:, :, :260])
+
+
+def test_window_at_least_L_equals_causal_bitwise():
+    q, k, v, dO = make_inputs(1, 2, 1, 200, 64, seed=9)
+    a = gpu_fwd_bwd(q, k, v, dO, 0, 0.125)
+    for w in (200, 5000):
+        b = gpu_fwd_bwd(q, k, v, dO, w, 0.125)
+        for n in a:
+            assert torch.equal(a[n], b[n]), (w, n)
+
+
+def test_gqa_equals_repeated_kv():
+    B, Hq, Hkv, L, D, W = 1, 8, 2, 260, 128, 70
+    G = Hq // Hkv
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=10)
+    a = gpu_fwd_bwd(q, k, v, dO, W, 0.088)
+    b = gpu_fwd_bwd(q, k.repeat_interleave(G, 1).contiguous(), v.repeat_interleave(G, 1).contiguous(), dO, W, 0.088)
+    for n in ("o", "dq"):
+        assert_close(n, a[n].numpy(), b[n].numpy(), max_abs=1e-4, rel_fro=1e-5)
+    for n in ("dk", "dv"):
+        assert_close(n, a[n].numpy(), b[n].view(B, Hkv, G, L, D).sum(2).numpy(), max_abs=1e-4, rel_fro=1e-5)
+
+
+def test_errors_raise_through_binding():
+    import sliding_window_attention_gb300 as swa
+
+    q = torch.zeros((1, 3, 16, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(swa.SwaError) as ei:
+        swa.forward(q, k, k, 0, 0.125)
+    assert ei.value.code == -3
+    assert swa.swa_attn_get_status() == 0
