@@ -64,6 +64,7 @@ typedef uint16_t swa_bf16; /* bf16 bit pattern */
 #define SWA_ERR_TOO_LARGE -10     /* sizes exceed the supported index range */
 #define SWA_ERR_DEVICE_TIMEOUT -11 /* a bounded device-side wait expired */
 #define SWA_ERR_UNSUPPORTED_DEVICE -12 /* current device is not sm_103 */
+#define SWA_ERR_NOALLOC_LIMIT -13 /* B*Hq*L above swa_attn_bwd_noalloc's fixed scratch */
 
 /*
  * Workspace bytes swa_attn_fwd needs for this shape (may be 0; a NULL
@@ -117,6 +118,29 @@ int swa_attn_get_status(void* stream);
 
 /* Static, human-readable description of a return code. */
 const char* swa_attn_strerror(int code);
+
+/*
+ * swa_attn_bwd_noalloc: the same backward as swa_attn_bwd, for callers that
+ * cannot allocate device memory or pass a workspace -- for example code whose
+ * device memory all belongs to a host framework's allocator, or a plugin
+ * entry point whose fixed signature has no workspace argument.  (The pages
+ * have no counterpart; this is a deployment convenience of this library.)
+ *
+ * It takes no workspace: the per-row term Delta lives in a fixed array built
+ * into the library (8 MiB of fp32 on every GPU that loads the library, held
+ * until the process exits), so it supports B * Hq * L <= 2,097,152 and
+ * returns SWA_ERR_NOALLOC_LIMIT above that.  It calls no cudaMalloc or
+ * cudaFree.  Its first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture begins.  Every call shares the one array: calls
+ * whose kernels overlap on the GPU race on it, so serialise them (one stream,
+ * or events).  Other arguments, layouts, outputs and errors are as for
+ * swa_attn_bwd.
+ */
+int swa_attn_bwd_noalloc(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o,
+                         const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv,
+                         int B, int Hq, int Hkv, int L, int D, int window, float scale,
+                         void* stream);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int swa_attn_version(void);

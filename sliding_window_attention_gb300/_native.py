@@ -24,6 +24,7 @@ EXPORTED = (
     "swa_attn_version",
     "swa_attn_profile_begin",
     "swa_attn_profile_end",
+    "swa_attn_bwd_noalloc",
 )
 
 _lock = threading.Lock()
@@ -68,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.swa_attn_profile_begin.restype = I
         lib.swa_attn_profile_end.argtypes = [P, I, ctypes.POINTER(I)]
         lib.swa_attn_profile_end.restype = I
+        lib.swa_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P] + shape + [F, P]
+        lib.swa_attn_bwd_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -142,6 +145,15 @@ def swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: float, wor
                              _stream_ptr(stream))
     if rc:
         raise SwaError(rc, "swa_attn_bwd")
+
+
+def swa_attn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: float, stream=None) -> None:
+    """Backward without a workspace (fixed built-in scratch; see include/swa_attn.h)."""
+    B, Hq, Hkv, L, D = _dims(q, k)
+    rc = load().swa_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), B, Hq, Hkv, L, D, int(window), float(scale), _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_bwd_noalloc")
 
 
 def swa_attn_get_status(stream=None) -> int:

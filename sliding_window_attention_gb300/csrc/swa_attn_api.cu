@@ -137,6 +137,8 @@ const char* swa_attn_strerror(int code) {
     case SWA_ERR_TOO_LARGE: return "sizes exceed the supported range";
     case SWA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
     case SWA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+    case SWA_ERR_NOALLOC_LIMIT:
+      return "B*Hq*L exceeds the fixed scratch of swa_attn_bwd_noalloc (2,097,152 rows); use swa_attn_bwd";
     default: return "unknown error code";
   }
 }
