@@ -69,14 +69,20 @@ def load_peaks():
                 source="fallback")
 
 
-def source_digest() -> str:
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "sliding_window_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
-    return h.hexdigest()[:16]
+# source file that defines each kernel (for matching ncu counters to the current code)
+KERNEL_SOURCE = {
+    "fwd_simt": "simt_kernels.cu", "bwd_delta": "simt_kernels.cu", "bwd_dkdv_simt": "simt_kernels.cu",
+    "bwd_dq_simt": "simt_kernels.cu", "fwd_tc": "tc_fwd.cu", "convert_f16": "tc_fwd.cu",
+}
+
+
+def source_digest(kernel: str) -> str:
+    """First 16 hex digits of the sha256 of the kernel's source file."""
+    name = KERNEL_SOURCE.get(kernel)
+    if name is None:
+        return "unknown"
+    with open(os.path.join(ROOT, "sliding_window_attention_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -85,7 +91,7 @@ def ncu_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
