@@ -65,6 +65,7 @@ typedef uint16_t swa_bf16; /* bf16 bit pattern */
 #define SWA_ERR_DEVICE_TIMEOUT -11 /* a bounded device-side wait expired */
 #define SWA_ERR_UNSUPPORTED_DEVICE -12 /* current device is not sm_103 */
 #define SWA_ERR_NOALLOC_LIMIT -13 /* B*Hq*L above swa_attn_bwd_noalloc's fixed scratch */
+#define SWA_ERR_FP16_RANGE -14    /* device: an input magnitude overflowed the fp16 operand copy */
 
 /*
  * Workspace bytes swa_attn_fwd needs for this shape (may be 0; a NULL

@@ -116,6 +116,19 @@ swa::Geom make_geom(int B, int Hq, int Hkv, int L, int D, int window, float scal
 // Backward workspace layout: [Delta: B*Hq*L fp32].
 size_t bwd_delta_bytes(int B, int Hq, int L) { return round_up((size_t)B * Hq * L * sizeof(float), 256); }
 
+// Forward workspace layout on the tensor-core path: fp16 copies of q, k, v.
+struct FwdWs {
+  size_t q16, k16, v16, total;
+};
+FwdWs fwd_ws_layout(int B, int Hq, int Hkv, int L, int D) {
+  FwdWs w;
+  w.q16 = 0;
+  w.k16 = w.q16 + round_up((size_t)B * Hq * L * D * 2, 256);
+  w.v16 = w.k16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  w.total = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -137,6 +150,7 @@ const char* swa_attn_strerror(int code) {
     case SWA_ERR_TOO_LARGE: return "sizes exceed the supported range";
     case SWA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
     case SWA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+    case SWA_ERR_FP16_RANGE: return "an input magnitude overflowed the fp16 operand copy (|x| > 65504)";
     case SWA_ERR_NOALLOC_LIMIT:
       return "B*Hq*L exceeds the fixed scratch of swa_attn_bwd_noalloc (2,097,152 rows); use swa_attn_bwd";
     default: return "unknown error code";
@@ -144,8 +158,9 @@ const char* swa_attn_strerror(int code) {
 }
 
 size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
-  (void)B, (void)Hq, (void)Hkv, (void)L, (void)D, (void)window;
-  return 0;
+  (void)window;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || !swa::fwd_tc_supported(D)) return 0;
+  return fwd_ws_layout(B, Hq, Hkv, L, D).total;
 }
 
 size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
@@ -169,6 +184,24 @@ int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float*
   if (rc) return rc;
   const swa::Geom g = make_geom(B, Hq, Hkv, L, D, window, scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (swa::fwd_tc_supported(D)) {
+    int* status = status_ptr_for_current_device(&rc);
+    if (!status) return rc;
+    const FwdWs w = fwd_ws_layout(B, Hq, Hkv, L, D);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
+    uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
+    uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+    const uint16_t* src[3] = {q, k, v};
+    uint16_t* dst[3] = {q16, k16, v16};
+    const size_t n[3] = {(size_t)B * Hq * L * D, (size_t)B * Hkv * L * D, (size_t)B * Hkv * L * D};
+    if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 3, status, s); }) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q16, k16, v16, o, lse, status, s); }) !=
+        cudaSuccess)
+      return SWA_ERR_CUDA;
+    return SWA_OK;
+  }
   if (launch("fwd_simt", s, [&] { return swa::launch_fwd_simt(g, q, k, v, o, lse, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;
   return SWA_OK;

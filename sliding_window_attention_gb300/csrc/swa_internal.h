@@ -15,7 +15,7 @@ struct Geom {
 };
 
 // Device-side status codes latched into the per-device status word.
-enum : int { kStatusOk = 0, kStatusTimeout = -11 };
+enum : int { kStatusOk = 0, kStatusTimeout = -11, kStatusFp16Range = -14 };
 
 // ---- SIMT kernels (fp32 arithmetic on bf16 inputs; any D in {64..512}) ----
 cudaError_t launch_fwd_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -27,5 +27,14 @@ cudaError_t launch_bwd_dkdv_simt(const Geom& g, const uint16_t* q, const uint16_
 cudaError_t launch_bwd_dq_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const uint16_t* dO, const float* lse, const float* delta, float* dq,
                                cudaStream_t s);
+
+// ---- tensor-core path (tcgen05 + TMA + TMEM), fp16 operand copies ----
+// bf16 -> fp16 copies of up to four tensors (n[i] elements, multiples of 8);
+// latches kStatusFp16Range in *status if a finite input overflows fp16.
+cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
+                               int* status, cudaStream_t s);
+bool fwd_tc_supported(int D);
+cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+                          float* lse, int* status, cudaStream_t s);
 
 }  // namespace swa

@@ -1,0 +1,433 @@
+// Tensor-core forward for sm_103a: S = scale * Q K^T and O = P V on tcgen05
+// with accumulators in Tensor Memory, operand tiles staged by TMA.
+//
+// One CTA per (128-row query tile, query head).  Warp roles:
+//   warp 0      TMA producer: Q once, then K and V tiles through an NS-deep ring
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warps 4..7  softmax: thread r owns query row i0 + r (TMEM lane r); reads its
+//               S row from TMEM, applies the band mask on edge tiles, keeps the
+//               running max / sum, writes P (fp16) back into the S columns for
+//               the TS-form PV MMA, rescales O when the max grows, and writes
+//               O / l and lse at the end.
+// The key tiles visited are exactly those that intersect the query tile's
+// band ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself",
+// "What I changed, in plain terms" item 3); inside edge tiles P is zeroed
+// where j > i or i - j >= window (item 4).  The forward writes the row
+// logsumexp the backward reuses (item 1).
+//
+// Operands are fp16 copies of the bf16 inputs (exact for |x| in [2^-14,
+// 65504]): P is rounded to fp16 (11-bit significand) instead of bf16 for the
+// PV product.  S and O accumulate in fp32.
+//
+// Rescaling is lazy: the running max used for P only moves when the tile max
+// exceeds it by more than kRescaleLog2 (P values then stay <= 2^8, safe in
+// fp16 and fp32); the final O / l is exact for any such choice.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "swa_internal.h"
+#include "tc_ptx.cuh"
+
+namespace swa {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BN = (D <= 128) ? 128 : 64;  // key tile rows
+  static constexpr int NS = (D == 64) ? 4 : 2;      // K/V pipeline stages
+  static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks per row
+  static constexpr int Q_BYTES = kBM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int O_COL = 0;                   // O accumulator columns [0, D)
+  static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
+  static constexpr size_t SMEM = (size_t)Q_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 /*barriers*/ + 1024 /*align*/;
+  static_assert(D <= 256, "O must fit below the S buffers");
+  static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
+};
+
+struct FwdParams {
+  Geom g;
+  float* o;
+  float* lse;
+  int* status;
+  int n_qtiles;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int BN = C::BN, NS = C::NS, KCH = C::KCH;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = base;
+  unsigned char* sK = sQ + C::Q_BYTES;
+  unsigned char* sV = sK + NS * C::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::KV_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + NS;
+  uint64_t* v_full = k_empty + NS;
+  uint64_t* v_empty = v_full + NS;
+  uint64_t* s_full = v_empty + NS;  // [2]
+  uint64_t* p_full = s_full + 2;    // [2]
+  uint64_t* o_done = p_full + 2;    // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bh = blockIdx.x;  // b * Hq + h
+  const int b = bh / g.Hq, h = bh - b * g.Hq;
+  const int bkv = b * g.Hkv + h / g.G;
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first
+  const int i0 = qt * kBM;
+  const int ihi = min(i0 + kBM, g.L) - 1;
+  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
+  const int t_lo = jlo / BN, t_hi = ihi / BN;
+  const int nt = t_hi - t_lo + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full + s, 1);
+      mbar_init(p_full + s, 128);
+    }
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int c = 0; c < KCH; ++c) tma_load_3d(sQ + c * kBM * 128, &tmQ, q_full, c * 64, i0, bh);
+      for (int n = 0; n < nt; ++n) {
+        const int st = n % NS;
+        const uint32_t par = ((n / NS) & 1) ^ 1;
+        const int j0 = (t_lo + n) * BN;
+        if (n >= NS && !mbar_wait(k_empty + st, par, abort_flag)) break;
+        mbar_arrive_expect_tx(k_full + st, C::KV_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sK + st * C::KV_BYTES + c * BN * 128, &tmK, k_full + st, c * 64, j0, bkv);
+        if (n >= NS && !mbar_wait(v_empty + st, par, abort_flag)) break;
+        mbar_arrive_expect_tx(v_full + st, C::KV_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sV + st * C::KV_BYTES + c * BN * 128, &tmV, v_full + st, c * 64, j0, bkv);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(kBM, BN, 0, 0, 0, 0);   // Q (K-major) x K (K-major)
+      const uint32_t idPV = idesc_f16(kBM, D, 0, 0, 0, 1);   // P (TMEM) x V (MN-major)
+      const uint32_t qaddr = smem_u32(sQ);
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      auto issue_pv = [&](int m) -> bool {
+        const int st = m % NS, sb = m & 1;
+        if (!mbar_wait(p_full + sb, (m >> 1) & 1, abort_flag)) return false;
+        if (!mbar_wait(v_full + st, (m / NS) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t vaddr = smem_u32(sV + st * C::KV_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t bdesc = smem_desc_sw128(vaddr + ks * 2048, BN * 128, 1024);
+          mma_ts(tmem + C::O_COL, tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV, (m > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(o_done);
+        mma_commit(v_empty + st);
+        return true;
+      };
+      for (int n = 0; ok && n < nt; ++n) {
+        const int st = n % NS, sb = n & 1;
+        if (!mbar_wait(k_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kaddr = smem_u32(sK + st * C::KV_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;  // 16 fp16 = 32 bytes along K inside a 128-byte chunk
+          const uint64_t adesc = smem_desc_sw128(qaddr + (ks >> 2) * kBM * 128 + off, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(kaddr + (ks >> 2) * BN * 128 + off, 16, 1024);
+          mma_ss(tmem + C::S_COL + sb * BN, adesc, bdesc, idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full + sb);
+        mma_commit(k_empty + st);
+        if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(nt - 1);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax / correction / epilogue ----------------
+    const int r = threadIdx.x - 128;
+    const int i = i0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int n = 0; n < nt; ++n) {
+      const int sb = n & 1;
+      const int j0 = (t_lo + n) * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, rr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(rr[e]) * sl2;
+      }
+      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + kBM - 1 - j0 < g.W);
+      if (!full) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const int j = j0 + e;
+          const bool valid = (j <= i) && (g.W == 0 || i - j < g.W);
+          x[e] = valid ? x[e] : -INFINITY;
+        }
+      }
+      float tmax = x[0];
+#pragma unroll
+      for (int e = 1; e < BN; ++e) tmax = fmaxf(tmax, x[e]);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (tmax > m_run + kRescaleLog2) {
+        if (m_run != -INFINITY) {
+          alpha = exp2f(m_run - tmax);
+          rescale = true;
+        }
+        m_run = tmax;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = exp2f(x[c * 64 + 2 * e] - m_use);
+          const float p1 = exp2f(x[c * 64 + 2 * e + 1] - m_use);
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          const float2 back = __half22float2(hp);
+          psum += back.x + back.y;
+          pk[e] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        tmem_st32(tmem + lane_off + C::S_COL + sb * BN + c * 32, pk);
+      }
+      l_run = l_run * alpha + psum;
+      // Wait for PV(n-1) at every tile, not only when rescaling: this thread then
+      // has observed every earlier PV completion, so the o_done phase can be at
+      // most one ahead of the parity asked for (no aliasing of phase n-3 with
+      // n-1), and a rescale never overlaps an in-flight PV.
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) { ok = false; break; }
+        tc_fence_after();
+      }
+      // tcgen05.ld/st are warp-collective: the whole warp rescales if any row needs it
+      if (__any_sync(0xffffffffu, rescale) && n > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + C::O_COL + c * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st32(tmem + lane_off + C::O_COL + c * 32, rr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + sb);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nt - 1) & 1, abort_flag))) {
+      tc_fence_after();
+      const bool row_ok = i < g.L;
+      const float inv = 1.f / l_run;
+      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, rr);  // warp-collective: every lane loads
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float4 v4 = make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
+                                    __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
+            *reinterpret_cast<float4*>(orow + c * 32 + e) = v4;
+          }
+        }
+      }
+      if (row_ok) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_run)) * kLn2;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 -> fp16 operand copies (up to four tensors per launch).
+struct ConvertSeg {
+  const uint16_t* src;
+  uint16_t* dst;
+  long long n8;  // number of 8-element chunks
+};
+struct ConvertArgs {
+  ConvertSeg seg[4];
+  int nseg;
+  int* status;
+};
+
+__global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const ConvertArgs a) {
+  long long total = 0;
+  for (int s = 0; s < a.nseg; ++s) total += a.seg[s].n8;
+  bool overflow = false;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    long long k = idx;
+    int s = 0;
+    while (s < a.nseg - 1 && k >= a.seg[s].n8) {
+      k -= a.seg[s].n8;
+      ++s;
+    }
+    const uint4 in = reinterpret_cast<const uint4*>(a.seg[s].src)[k];
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16);
+      const float hi = __uint_as_float(w[e] & 0xffff0000u);
+      const __half2 hv = __floats2half2_rn(lo, hi);
+      const float2 back = __half22float2(hv);
+      overflow |= (isinf(back.x) && !isinf(lo)) || (isinf(back.y) && !isinf(hi));
+      o[e] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    reinterpret_cast<uint4*>(a.seg[s].dst)[k] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (overflow) atomicCAS(a.status, 0, kStatusFp16Range);
+}
+
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// 3-D fp16 tensor map over [heads, L, D] with a (64 x rows) box, 128-byte swizzle.
+cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int heads, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * L * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
+                               int* status, cudaStream_t s) {
+  ConvertArgs a;
+  a.nseg = count;
+  a.status = status;
+  long long total = 0;
+  for (int i = 0; i < count; ++i) {
+    a.seg[i].src = src[i];
+    a.seg[i].dst = dst[i];
+    a.seg[i].n8 = (long long)(n[i] / 8);
+    total += a.seg[i].n8;
+  }
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  convert_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+                            float* lse, int* status, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e;
+  if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, kBM)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+  auto kern = fwd_tc_kernel<D>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
+    return e;
+  FwdParams p;
+  p.g = g;
+  p.o = o;
+  p.lse = lse;
+  p.status = status;
+  p.n_qtiles = (g.L + kBM - 1) / kBM;
+  dim3 grid(g.B * g.Hq, p.n_qtiles);
+  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+bool fwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
+
+cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+                          float* lse, int* status, cudaStream_t s) {
+  switch (g.D) {
+    case 64: return fwd_tc_d<64>(g, q16, k16, v16, o, lse, status, s);
+    case 128: return fwd_tc_d<128>(g, q16, k16, v16, o, lse, status, s);
+    case 256: return fwd_tc_d<256>(g, q16, k16, v16, o, lse, status, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace swa

@@ -148,7 +148,9 @@ def test_outputs_fully_overwritten():
     nan = float("nan")
     o = torch.full((B, Hq, L, D), nan, device="cuda")
     lse = torch.full((B, Hq, L), nan, device="cuda")
-    swa.swa_attn_fwd(q, k, v, o, lse, W, 0.125)
+    fws = torch.full((max(256, swa.fwd_workspace_bytes(B, Hq, Hkv, L, D, W)),), 0xFF, dtype=torch.uint8,
+                     device="cuda")
+    swa.swa_attn_fwd(q, k, v, o, lse, W, 0.125, fws)
     dq = torch.full((B, Hq, L, D), nan, device="cuda")
     dk = torch.full((B, Hkv, L, D), nan, device="cuda")
     dv = torch.full((B, Hkv, L, D), nan, device="cuda")
