@@ -41,8 +41,10 @@ KERNEL_FLOPS_PER_PAIR_D = {
     "fwd_simt": 4,        # S = Q K^T, O += P V
     "bwd_dkdv_simt": 8,   # S, dP recomputed; dV += P^T dO; dK += dS^T Q
     "bwd_dq_simt": 6,     # S, dP recomputed; dQ += dS K
+    "bwd_dkdv_tc": 8,     # S^T, dP^T recomputed; dV += P^T dO; dK += dS^T Q (tcgen05)
+    "bwd_dq_tc": 6,       # S, dP recomputed; dQ += dS K (tcgen05)
 }
-HBM_KERNELS = {"bwd_delta", "convert_f16"}
+HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_rowstats"}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -74,6 +76,7 @@ def load_peaks():
 KERNEL_SOURCE = {
     "fwd_simt": "simt_kernels.cu", "bwd_delta": "simt_kernels.cu", "bwd_dkdv_simt": "simt_kernels.cu",
     "bwd_dq_simt": "simt_kernels.cu", "fwd_tc": "tc_fwd.cu", "convert_f16": "tc_fwd.cu",
+    "bwd_rowstats": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
 }
 
 
@@ -383,7 +386,7 @@ def run_ours(args, w, world, rank, local_rank):
     kname, (kl, kms) = top
     avg_s = kms / kl / 1e3
     if kname in HBM_KERNELS:
-        if kname == "bwd_delta":
+        if kname in ("bwd_delta", "bwd_rowstats"):
             alg = B * Hq * L * (D * 4 + D * 2 + 4)
         else:  # bf16 read + fp16 write of q, k, v (and dO in the backward)
             alg = 4 * D * L * B * (Hq + 2 * Hkv)

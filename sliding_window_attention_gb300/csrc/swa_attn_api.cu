@@ -116,6 +116,24 @@ swa::Geom make_geom(int B, int Hq, int Hkv, int L, int D, int window, float scal
 // Backward workspace layout: [Delta: B*Hq*L fp32].
 size_t bwd_delta_bytes(int B, int Hq, int L) { return round_up((size_t)B * Hq * L * sizeof(float), 256); }
 
+// Backward workspace layout on the tensor-core path:
+// [row stats (lse*log2e, Delta) : B*Hq*Lpad float2][q16][k16][v16][dO16].
+struct BwdTcWs {
+  size_t stats, q16, k16, v16, g16, total;
+  int Lpad;
+};
+BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int L, int D) {
+  BwdTcWs w;
+  w.Lpad = swa::bwd_stats_lpad(L);
+  w.stats = 0;
+  w.q16 = round_up((size_t)B * Hq * w.Lpad * 8, 256);
+  w.k16 = w.q16 + round_up((size_t)B * Hq * L * D * 2, 256);
+  w.v16 = w.k16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  w.g16 = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  w.total = w.g16 + round_up((size_t)B * Hq * L * D * 2, 256);
+  return w;
+}
+
 // Forward workspace layout on the tensor-core path: fp16 copies of q, k, v.
 struct FwdWs {
   size_t q16, k16, v16, total;
@@ -164,8 +182,9 @@ size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int wi
 }
 
 size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
-  (void)Hkv, (void)D, (void)window;
-  if (B < 1 || Hq < 1 || L < 1) return 0;
+  (void)window;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return 0;
+  if (swa::bwd_tc_supported(D)) return bwd_tc_ws_layout(B, Hq, Hkv, L, D).total;
   return bwd_delta_bytes(B, Hq, L);
 }
 
@@ -222,6 +241,35 @@ int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const 
   if (rc) return rc;
   const swa::Geom g = make_geom(B, Hq, Hkv, L, D, window, scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (swa::bwd_tc_supported(D)) {
+    int* status = status_ptr_for_current_device(&rc);
+    if (!status) return rc;
+    const BwdTcWs w = bwd_tc_ws_layout(B, Hq, Hkv, L, D);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    float2* stats = reinterpret_cast<float2*>(ws + w.stats);
+    uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
+    uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
+    uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+    uint16_t* g16 = reinterpret_cast<uint16_t*>(ws + w.g16);
+    const uint16_t* src[4] = {q, k, v, dO};
+    uint16_t* dst[4] = {q16, k16, v16, g16};
+    const size_t n[4] = {(size_t)B * Hq * L * D, (size_t)B * Hkv * L * D, (size_t)B * Hkv * L * D,
+                         (size_t)B * Hq * L * D};
+    if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 4, status, s); }) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    if (launch("bwd_rowstats", s, [&] { return swa::launch_rowstats(g, w.Lpad, o, dO, lse, stats, s); }) !=
+        cudaSuccess)
+      return SWA_ERR_CUDA;
+    if (launch("bwd_dkdv_tc", s, [&] {
+          return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, s);
+        }) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    if (launch("bwd_dq_tc", s, [&] {
+          return swa::launch_bwd_dq_tc(g, q16, k16, v16, g16, stats, w.Lpad, dq, status, s);
+        }) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    return SWA_OK;
+  }
   float* delta = static_cast<float*>(workspace);
   if (launch("bwd_delta", s, [&] { return swa::launch_delta(g, o, dO, delta, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;

@@ -2,6 +2,7 @@
 // translation units.  Not installed; not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -36,5 +37,22 @@ cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst,
 bool fwd_tc_supported(int D);
 cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
                           float* lse, int* status, cudaStream_t s);
+
+// 3-D fp16 tensor map over [heads, L, D] with a 64 x box_rows box and
+// 128-byte swizzle (rows at or beyond L read as zero).
+cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int heads, int box_rows);
+
+bool bwd_tc_supported(int D);
+// Padded row count of the backward's row-statistics array.
+int bwd_stats_lpad(int L);
+// stats[bh * Lpad + i] = (lse * log2(e), dO_i . o_i), zero for i >= L.
+cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint16_t* dO, const float* lse,
+                            float2* stats, cudaStream_t s);
+cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
+                               const uint16_t* g16, const float2* stats, int Lpad, float* dk, float* dv,
+                               int* status, cudaStream_t s);
+cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
+                             const uint16_t* g16, const float2* stats, int Lpad, float* dq, int* status,
+                             cudaStream_t s);
 
 }  // namespace swa

@@ -1,0 +1,617 @@
+// Tensor-core backward for sm_103a (head dims 64 and 128): a key-outer dK/dV
+// pass and a query-outer dQ pass, both on tcgen05 with accumulators in Tensor
+// Memory and operands staged by TMA.  P is recomputed from the forward's lse
+// instead of being stored ("Training -- design (ORPO, flash-CCE head, prefix
+// sharing, segmented backward)", section 6), and only tile pairs that meet
+// the causal / window band are visited ("Lab 028 lab detail: Off NVIDIA, you
+// fix the platform yourself", "What I changed, in plain terms" items 3-4).
+//
+// dK/dV kernel, one CTA per (128-row key tile, kv head):
+//   for every query head of the group and every 64-row query tile in band:
+//     S^T  = K Q^T,  dP^T = V dO^T                 (SS MMAs, fp32 in TMEM)
+//     P^T  = exp(scale S^T - lse),  dS^T = P^T (dP^T - Delta)   (thread = key row)
+//     dV  += P^T dO,  dK += dS^T Q                  (TS MMAs, A operand in TMEM)
+//   dK and dV stay in TMEM for the whole group loop: no atomics, deterministic.
+// dQ kernel, one CTA per (128-row query tile, query head):
+//   for every 64-row key tile in band: S = Q K^T, dP = dO V^T,
+//   dS = P (dP - Delta), dQ += dS K.  No read-modify-write of dQ in memory.
+//
+// Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner and the
+// single-thread MMA issuer, warps 4..7 the elementwise softmax-gradient
+// stage (one TMEM lane, i.e. one row, per thread).  Every mbarrier wait is
+// bounded (see tc_ptx.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "swa_internal.h"
+#include "tc_ptx.cuh"
+
+namespace swa {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 512 TMEM columns)
+
+// Row statistics for the backward: per (b*Hq + h, i < Lpad) the pair
+// (lse_i * log2(e), Delta_i = dO_i . o_i); zero for padding rows i >= L.
+__global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, int D, const float* __restrict__ o,
+                                                       const uint16_t* __restrict__ dO,
+                                                       const float* __restrict__ lse, float2* __restrict__ stats) {
+  const long row = ((long)blockIdx.x * 256 + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= (long)BH * Lpad) return;
+  const int bh = (int)(row / Lpad), i = (int)(row % Lpad);
+  float acc = 0.f, l2 = 0.f;
+  if (i < L) {
+    const size_t off = ((size_t)bh * L + i) * D;
+    for (int d = lane * 4; d < D; d += 128) {
+      const float4 ov = *reinterpret_cast<const float4*>(o + off + d);
+      const uint2 gv = *reinterpret_cast<const uint2*>(dO + off + d);
+      acc = fmaf(ov.x, __uint_as_float(gv.x << 16), acc);
+      acc = fmaf(ov.y, __uint_as_float(gv.x & 0xffff0000u), acc);
+      acc = fmaf(ov.z, __uint_as_float(gv.y << 16), acc);
+      acc = fmaf(ov.w, __uint_as_float(gv.y & 0xffff0000u), acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    l2 = lse[(size_t)bh * L + i] * kLog2e;
+  }
+  if (lane == 0) stats[row] = make_float2(l2, acc);
+}
+
+__device__ __forceinline__ bool in_band(int i, int j, int W) { return j <= i && (W == 0 || i - j < W); }
+
+// ===========================================================================
+// dK / dV
+template <int D>
+struct KvCfg {
+  static constexpr int BNK = 128;  // key rows per CTA (MMA M)
+  static constexpr int BM = 64;    // query rows per step (MMA N for S^T / dP^T, K for dV / dK)
+  static constexpr int NS = 2;     // Q / dO / stats stages
+  static constexpr int KCH = D / 64;
+  static constexpr int KV_BYTES = BNK * D * 2;  // K (or V) tile
+  static constexpr int QT_BYTES = BM * D * 2;   // Q (or dO) tile
+  static constexpr int ST_BYTES = BM * 8;       // (lse, Delta) pairs
+  static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, stats (padded to 1 KB)
+  static constexpr int DV_COL = 0, DK_COL = D, S_COL = 256, DP_COL = 384;
+  static constexpr size_t SMEM_USED = 2 * (size_t)KV_BYTES + NS * (size_t)STAGE_BYTES + 1024 + 1024;
+  static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
+  static_assert(2 * D <= 256, "dK and dV must fit below the S buffers");
+};
+
+struct BwdParams {
+  Geom g;
+  float* out0;  // dkdv: dk ; dq: dq
+  float* out1;  // dkdv: dv
+  const float2* stats;
+  int Lpad;
+  int n_tiles;
+  int* status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                   const __grid_constant__ CUtensorMap tmS, const BwdParams p) {
+  using C = KvCfg<D>;
+  constexpr int BNK = C::BNK, BM = C::BM, NS = C::NS, KCH = C::KCH;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sK = base;
+  unsigned char* sV = sK + C::KV_BYTES;
+  unsigned char* sStage = sV + C::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::STAGE_BYTES);
+  uint64_t* kv_full = bars;                // [1]
+  uint64_t* st_full = kv_full + 1;         // [NS]
+  uint64_t* st_empty = st_full + NS;       // [NS]
+  uint64_t* sdp_full = st_empty + NS;      // [2]
+  uint64_t* p_full = sdp_full + 2;         // [2]
+  uint64_t* acc_done = p_full + 2;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bkv = blockIdx.x;  // b * Hkv + kv head
+  const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
+  const int j0 = (int)blockIdx.y * BNK;
+  const int jhi = min(j0 + BNK, g.L) - 1;
+  const int ihi = g.W > 0 ? min(g.L - 1, jhi + g.W - 1) : g.L - 1;
+  const int t_lo = j0 / BM, t_hi = ihi / BM;
+  const int ntq = t_hi - t_lo + 1;
+  const int N = g.G * ntq;  // work items (head of group, query tile)
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(st_full + s, 1);
+      mbar_init(st_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sdp_full + s, 1);
+      mbar_init(p_full + s, 128);
+    }
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      prefetch_tmap(&tmS);
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_3d(sK + c * BNK * 128, &tmK, kv_full, c * 64, j0, bkv);
+        tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
+      }
+      for (int n = 0; n < N; ++n) {
+        const int st = n % NS;
+        const int gi = n / ntq, t = t_lo + n % ntq;
+        const int bh = b * g.Hq + kvh * g.G + gi;
+        if (n >= NS && !mbar_wait(st_empty + st, ((n / NS) & 1) ^ 1, abort_flag)) break;
+        unsigned char* stg = sStage + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(st_full + st, 2 * C::QT_BYTES + C::ST_BYTES);
+        for (int c = 0; c < KCH; ++c) {
+          tma_load_3d(stg + c * BM * 128, &tmQ, st_full + st, c * 64, t * BM, bh);
+          tma_load_3d(stg + C::QT_BYTES + c * BM * 128, &tmG, st_full + st, c * 64, t * BM, bh);
+        }
+        tma_load_2d(stg + 2 * C::QT_BYTES, &tmS, st_full + st, 2 * t * BM, bh);
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major)
+      const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (B MN-major)
+      const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV);
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      auto issue_grad = [&](int m) -> bool {
+        const int st = m % NS, sb = m & 1;
+        if (!mbar_wait(p_full + sb, (m >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(sStage + st * C::STAGE_BYTES);
+        const uint32_t gaddr = qaddr + C::QT_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks) {
+          const uint32_t acc = (m > 0 || ks > 0) ? 1u : 0u;
+          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + sb * BM + ks * 8,
+                 smem_desc_sw128(gaddr + ks * 2048, BM * 128, 1024), idG, acc);
+          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + sb * BM + ks * 8,
+                 smem_desc_sw128(qaddr + ks * 2048, BM * 128, 1024), idG, acc);
+        }
+        mma_commit(st_empty + st);
+        return true;
+      };
+      for (int n = 0; ok && n < N; ++n) {
+        const int st = n % NS, sb = n & 1;
+        if (!mbar_wait(st_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(sStage + st * C::STAGE_BYTES);
+        const uint32_t gaddr = qaddr + C::QT_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;
+          const uint32_t ck = (ks >> 2) * BNK * 128, cq = (ks >> 2) * BM * 128;
+          mma_ss(tmem + C::S_COL + sb * BM, smem_desc_sw128(kaddr + ck + off, 16, 1024),
+                 smem_desc_sw128(qaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          mma_ss(tmem + C::DP_COL + sb * BM, smem_desc_sw128(vaddr + ck + off, 16, 1024),
+                 smem_desc_sw128(gaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full + sb);
+        if (n >= 1 && !issue_grad(n - 1)) { ok = false; break; }
+      }
+      if (ok && issue_grad(N - 1)) mma_commit(acc_done);
+    }
+  } else if (warp >= 4) {
+    const int r = threadIdx.x - 128;
+    const int j = j0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+      const int st = n % NS, sb = n & 1;
+      const int i0 = (t_lo + n % ntq) * BM;
+      if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      const float2* stats = reinterpret_cast<const float2*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
+      uint32_t sv[BM], dv[BM];
+#pragma unroll
+      for (int c = 0; c < BM / 32; ++c) {
+        uint32_t a[32], bb[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, a);
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, bb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sv[c * 32 + e] = a[e];
+          dv[c * 32 + e] = bb[e];
+        }
+      }
+      const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
+      uint32_t pp[BM / 2], dd[BM / 2];
+#pragma unroll
+      for (int e = 0; e < BM; e += 2) {
+        float pr[2], dr[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = e + u;
+          const float2 rs = stats[c];
+          float pv = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -rs.x));
+          if (!full) {
+            const int i = i0 + c;
+            pv = (i < g.L && in_band(i, j, g.W)) ? pv : 0.f;
+          }
+          pr[u] = pv;
+          dr[u] = pv * (__uint_as_float(dv[c]) - rs.y);
+        }
+        pp[e / 2] = pack_half2(pr[0], pr[1]);
+        dd[e / 2] = pack_half2(dr[0], dr[1]);
+      }
+      tmem_st32(tmem + lane_off + C::S_COL + sb * BM, pp);
+      tmem_st32(tmem + lane_off + C::DP_COL + sb * BM, dd);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + sb);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
+      tc_fence_after();
+      const bool row_ok = j < g.L;
+      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32], bb[32];
+        tmem_ld32(tmem + lane_off + C::DK_COL + c * 32, a);
+        tmem_ld32(tmem + lane_off + C::DV_COL + c * 32, bb);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            *reinterpret_cast<float4*>(p.out0 + off + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * g.scale, __uint_as_float(a[e + 1]) * g.scale,
+                            __uint_as_float(a[e + 2]) * g.scale, __uint_as_float(a[e + 3]) * g.scale);
+            *reinterpret_cast<float4*>(p.out1 + off + c * 32 + e) =
+                make_float4(__uint_as_float(bb[e]), __uint_as_float(bb[e + 1]), __uint_as_float(bb[e + 2]),
+                            __uint_as_float(bb[e + 3]));
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dQ
+template <int D>
+struct DqCfg {
+  static constexpr int BMQ = 128;  // query rows per CTA (MMA M)
+  static constexpr int BN = 64;    // key rows per step
+  static constexpr int NS = 2;
+  static constexpr int KCH = D / 64;
+  static constexpr int QT_BYTES = BMQ * D * 2;  // Q (or dO) tile
+  static constexpr int KV_BYTES = BN * D * 2;   // K (or V) tile
+  static constexpr int DQ_COL = 0, S_COL = 256, DP_COL = 384;
+  static constexpr size_t SMEM_USED = 2 * (size_t)QT_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 + 1024;
+  static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
+  static_assert(D <= 256, "dQ must fit below the S buffers");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                 const BwdParams p) {
+  using C = DqCfg<D>;
+  constexpr int BMQ = C::BMQ, BN = C::BN, NS = C::NS, KCH = C::KCH;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = base;
+  unsigned char* sG = sQ + C::QT_BYTES;
+  unsigned char* sK = sG + C::QT_BYTES;
+  unsigned char* sV = sK + NS * C::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::KV_BYTES);
+  uint64_t* q_full = bars;              // [1]
+  uint64_t* kv_full = q_full + 1;       // [NS]
+  uint64_t* kv_empty = kv_full + NS;    // [NS]
+  uint64_t* sdp_full = kv_empty + NS;   // [2]
+  uint64_t* ds_full = sdp_full + 2;     // [2]
+  uint64_t* acc_done = ds_full + 2;     // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bh = blockIdx.x;
+  const int b = bh / g.Hq, h = bh - b * g.Hq;
+  const int bkv = b * g.Hkv + h / g.G;
+  const int qt = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
+  const int i0 = qt * BMQ;
+  const int ihi = min(i0 + BMQ, g.L) - 1;
+  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
+  const int t_lo = jlo / BN, t_hi = ihi / BN;
+  const int nt = t_hi - t_lo + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sdp_full + s, 1);
+      mbar_init(ds_full + s, 128);
+    }
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(q_full, 2 * C::QT_BYTES);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_3d(sQ + c * BMQ * 128, &tmQ, q_full, c * 64, i0, bh);
+        tma_load_3d(sG + c * BMQ * 128, &tmG, q_full, c * 64, i0, bh);
+      }
+      for (int n = 0; n < nt; ++n) {
+        const int st = n % NS;
+        const int j0 = (t_lo + n) * BN;
+        if (n >= NS && !mbar_wait(kv_empty + st, ((n / NS) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(kv_full + st, 2 * C::KV_BYTES);
+        for (int c = 0; c < KCH; ++c) {
+          tma_load_3d(sK + st * C::KV_BYTES + c * BN * 128, &tmK, kv_full + st, c * 64, j0, bkv);
+          tma_load_3d(sV + st * C::KV_BYTES + c * BN * 128, &tmV, kv_full + st, c * 64, j0, bkv);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BMQ, BN, 0, 0, 0, 0);  // Q x K^T, dO x V^T
+      const uint32_t idQ = idesc_f16(BMQ, D, 0, 0, 0, 1);   // dS x K (K MN-major)
+      const uint32_t qaddr = smem_u32(sQ), gaddr = smem_u32(sG);
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      auto issue_dq = [&](int m) -> bool {
+        const int st = m % NS, sb = m & 1;
+        if (!mbar_wait(ds_full + sb, (m >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = smem_u32(sK + st * C::KV_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts(tmem + C::DQ_COL, tmem + C::DP_COL + sb * BN + ks * 8,
+                 smem_desc_sw128(kaddr + ks * 2048, BN * 128, 1024), idQ, (m > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(kv_empty + st);
+        return true;
+      };
+      for (int n = 0; ok && n < nt; ++n) {
+        const int st = n % NS, sb = n & 1;
+        if (!mbar_wait(kv_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kaddr = smem_u32(sK + st * C::KV_BYTES);
+        const uint32_t vaddr = smem_u32(sV + st * C::KV_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;
+          const uint32_t cq = (ks >> 2) * BMQ * 128, ck = (ks >> 2) * BN * 128;
+          mma_ss(tmem + C::S_COL + sb * BN, smem_desc_sw128(qaddr + cq + off, 16, 1024),
+                 smem_desc_sw128(kaddr + ck + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          mma_ss(tmem + C::DP_COL + sb * BN, smem_desc_sw128(gaddr + cq + off, 16, 1024),
+                 smem_desc_sw128(vaddr + ck + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full + sb);
+        if (n >= 1 && !issue_dq(n - 1)) { ok = false; break; }
+      }
+      if (ok && issue_dq(nt - 1)) mma_commit(acc_done);
+    }
+  } else if (warp >= 4) {
+    const int r = threadIdx.x - 128;
+    const int i = i0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    const float2 rs = (i < g.L) ? p.stats[(size_t)bh * p.Lpad + i] : make_float2(0.f, 0.f);
+    bool ok = true;
+    for (int n = 0; n < nt; ++n) {
+      const int sb = n & 1;
+      const int j0 = (t_lo + n) * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[BN], dv[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t a[32], bb[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, a);
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, bb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sv[c * 32 + e] = a[e];
+          dv[c * 32 + e] = bb[e];
+        }
+      }
+      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + BMQ - 1 - j0 < g.W);
+      uint32_t dd[BN / 2];
+#pragma unroll
+      for (int e = 0; e < BN; e += 2) {
+        float dr[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = e + u;
+          float pv = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -rs.x));
+          if (!full) pv = in_band(i, j0 + c, g.W) ? pv : 0.f;
+          dr[u] = pv * (__uint_as_float(dv[c]) - rs.y);
+        }
+        dd[e / 2] = pack_half2(dr[0], dr[1]);
+      }
+      tmem_st32(tmem + lane_off + C::DP_COL + sb * BN, dd);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full + sb);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
+      tc_fence_after();
+      const bool row_ok = i < g.L;
+      float* row = p.out0 + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + C::DQ_COL + c * 32, a);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(row + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * g.scale, __uint_as_float(a[e + 1]) * g.scale,
+                            __uint_as_float(a[e + 2]) * g.scale, __uint_as_float(a[e + 3]) * g.scale);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// 2-D fp32 tensor map over the row statistics [BH, 2 * Lpad] with a
+// (2 * BM) x 1 box.
+cudaError_t make_tmap_stats(CUtensorMap* m, const void* ptr, int Lpad, int BH, int box_floats) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return cudaErrorNotSupported;
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  cuuint64_t dims[2] = {(cuuint64_t)2 * Lpad, (cuuint64_t)BH};
+  cuuint64_t strides[1] = {(cuuint64_t)2 * Lpad * 4};
+  cuuint32_t box[2] = {(cuuint32_t)box_floats, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
+                     const uint16_t* g16, const float2* stats, int Lpad, float* dq, float* dk, float* dv, int* status,
+                     cudaStream_t s, int which) {
+  cudaError_t e;
+  BwdParams p;
+  p.g = g;
+  p.stats = stats;
+  p.Lpad = Lpad;
+  p.status = status;
+  if (which == 0) {
+    using C = KvCfg<D>;
+    CUtensorMap tq, tk, tv, tg, ts;
+    if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e;
+    if ((e = make_tmap_stats(&ts, stats, Lpad, g.B * g.Hq, 2 * C::BM)) != cudaSuccess) return e;
+    auto kern = dkdv_tc_kernel<D>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
+      return e;
+    p.out0 = dk;
+    p.out1 = dv;
+    p.n_tiles = (g.L + C::BNK - 1) / C::BNK;
+    dim3 grid(g.B * g.Hkv, p.n_tiles);
+    kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, ts, p);
+  } else {
+    using C = DqCfg<D>;
+    CUtensorMap tq, tk, tv, tg;
+    if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+    auto kern = dq_tc_kernel<D>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
+      return e;
+    p.out0 = dq;
+    p.out1 = nullptr;
+    p.n_tiles = (g.L + C::BMQ - 1) / C::BMQ;
+    dim3 grid(g.B * g.Hq, p.n_tiles);
+    kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int D) { return D == 64 || D == 128; }
+
+int bwd_stats_lpad(int L) { return (L + 127) / 128 * 128; }
+
+cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint16_t* dO, const float* lse,
+                            float2* stats, cudaStream_t s) {
+  const long rows = (long)g.B * g.Hq * Lpad;
+  const long blocks = (rows * 32 + 255) / 256;
+  rowstats_kernel<<<(unsigned)blocks, 256, 0, s>>>(g.B * g.Hq, g.L, Lpad, g.D, o, dO, lse, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
+                               const uint16_t* g16, const float2* stats, int Lpad, float* dk, float* dv,
+                               int* status, cudaStream_t s) {
+  switch (g.D) {
+    case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
+    case 128: return bwd_tc_d<128>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
+                             const uint16_t* g16, const float2* stats, int Lpad, float* dq, int* status,
+                             cudaStream_t s) {
+  switch (g.D) {
+    case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
+    case 128: return bwd_tc_d<128>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace swa
