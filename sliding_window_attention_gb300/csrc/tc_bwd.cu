@@ -17,9 +17,10 @@
 //   dS = P (dP - Delta), dQ += dS K.  No read-modify-write of dQ in memory.
 //
 // Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner and the
-// single-thread MMA issuer, warps 4..7 the elementwise softmax-gradient
-// stage (one TMEM lane, i.e. one row, per thread).  Every mbarrier wait is
-// bounded (see tc_ptx.cuh).
+// single-thread MMA issuer, warps 4..7 and 8..11 two elementwise
+// softmax-gradient warpgroups (one TMEM lane, i.e. one row, per thread) that
+// take alternate steps, so one works while the other waits for its MMAs.
+// Every mbarrier wait is bounded (see tc_ptx.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -35,7 +36,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11: two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 512 TMEM columns)
 
@@ -67,6 +68,44 @@ __global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, 
 }
 
 __device__ __forceinline__ bool in_band(int i, int j, int W) { return j <= i && (W == 0 || i - j < W); }
+
+// dK/dV elementwise step for one key row and 32 query columns: P^T and
+// dS^T = P^T (dP^T - Delta) as fp16 pairs.  FULL: every column is in the band
+// (no mask code); otherwise columns outside [clo, chi] give exactly zero.
+template <bool FULL>
+__device__ __forceinline__ void kv_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float4* stats4,
+                                         float sl2, int cbase, int clo, int chi, uint32_t (&pp)[16],
+                                         uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float4 rs = stats4[(cbase + e) >> 1];  // (lse0*log2e, Delta0, lse1*log2e, Delta1)
+    float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -rs.x));
+    float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -rs.z));
+    if (!FULL) {
+      p0 = (cbase + e >= clo && cbase + e <= chi) ? p0 : 0.f;
+      p1 = (cbase + e + 1 >= clo && cbase + e + 1 <= chi) ? p1 : 0.f;
+    }
+    pp[e >> 1] = pack_half2(p0, p1);
+    dd[e >> 1] = pack_half2(p0 * (__uint_as_float(dv[e]) - rs.y), p1 * (__uint_as_float(dv[e + 1]) - rs.w));
+  }
+}
+
+// dQ elementwise step for one query row (lse*log2e = l2, Delta = dl) and 32
+// key columns: dS = P (dP - Delta) as fp16 pairs.
+template <bool FULL>
+__device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float sl2, float l2,
+                                         float dl, int cbase, int clo, int chi, uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -l2));
+    float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -l2));
+    if (!FULL) {
+      p0 = (cbase + e >= clo && cbase + e <= chi) ? p0 : 0.f;
+      p1 = (cbase + e + 1 >= clo && cbase + e + 1 <= chi) ? p1 : 0.f;
+    }
+    dd[e >> 1] = pack_half2(p0 * (__uint_as_float(dv[e]) - dl), p1 * (__uint_as_float(dv[e + 1]) - dl));
+  }
+}
 
 // ===========================================================================
 // dK / dV
@@ -222,76 +261,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && issue_grad(N - 1)) mma_commit(acc_done);
     }
   } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;
+    const int wg = (warp - 4) >> 2;                  // warpgroup: takes steps n with n % 2 == wg
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int j = j0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
     bool ok = true;
-    for (int n = 0; n < N; ++n) {
+    for (int n = wg; n < N; n += 2) {
       const int st = n % NS, sb = n & 1;
       const int i0 = (t_lo + n % ntq) * BM;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const float2* stats = reinterpret_cast<const float2*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
-      uint32_t sv[BM], dv[BM];
+      // (lse0 * log2e, Delta0, lse1 * log2e, Delta1) for query columns 2k, 2k+1
+      const float4* stats4 = reinterpret_cast<const float4*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
+      const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
+      // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
+      const int clo = max(0, j - i0);
+      const int chi = min(min(BM - 1, g.L - 1 - i0), g.W > 0 ? j + g.W - 1 - i0 : BM - 1);
 #pragma unroll
       for (int c = 0; c < BM / 32; ++c) {
-        uint32_t a[32], bb[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, a);
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, bb);
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, sv);
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, dv);
         tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[c * 32 + e] = a[e];
-          dv[c * 32 + e] = bb[e];
-        }
+        uint32_t pp[16], dd[16];
+        if (full) kv_chunk<true>(sv, dv, stats4, sl2, c * 32, clo, chi, pp, dd);
+        else kv_chunk<false>(sv, dv, stats4, sl2, c * 32, clo, chi, pp, dd);
+        // P^T / dS^T (fp16, two per column) overwrite columns already consumed
+        tmem_st16(tmem + lane_off + C::S_COL + sb * BM + c * 16, pp);
+        tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + c * 16, dd);
       }
-      const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
-      uint32_t pp[BM / 2], dd[BM / 2];
-#pragma unroll
-      for (int e = 0; e < BM; e += 2) {
-        float pr[2], dr[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = e + u;
-          const float2 rs = stats[c];
-          float pv = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -rs.x));
-          if (!full) {
-            const int i = i0 + c;
-            pv = (i < g.L && in_band(i, j, g.W)) ? pv : 0.f;
-          }
-          pr[u] = pv;
-          dr[u] = pv * (__uint_as_float(dv[c]) - rs.y);
-        }
-        pp[e / 2] = pack_half2(pr[0], pr[1]);
-        dd[e / 2] = pack_half2(dr[0], dr[1]);
-      }
-      tmem_st32(tmem + lane_off + C::S_COL + sb * BM, pp);
-      tmem_st32(tmem + lane_off + C::DP_COL + sb * BM, dd);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + sb);
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
+      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
       const bool row_ok = j < g.L;
       const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+      const uint32_t col = wg == 0 ? C::DK_COL : C::DV_COL;
+      const float mul = wg == 0 ? g.scale : 1.f;
+      float* dst = (wg == 0 ? p.out0 : p.out1) + off;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32], bb[32];
-        tmem_ld32(tmem + lane_off + C::DK_COL + c * 32, a);
-        tmem_ld32(tmem + lane_off + C::DV_COL + c * 32, bb);
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + col + c * 32, a);
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            *reinterpret_cast<float4*>(p.out0 + off + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * g.scale, __uint_as_float(a[e + 1]) * g.scale,
-                            __uint_as_float(a[e + 2]) * g.scale, __uint_as_float(a[e + 3]) * g.scale);
-            *reinterpret_cast<float4*>(p.out1 + off + c * 32 + e) =
-                make_float4(__uint_as_float(bb[e]), __uint_as_float(bb[e + 1]), __uint_as_float(bb[e + 2]),
-                            __uint_as_float(bb[e + 3]));
-          }
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
         }
       }
     }
@@ -442,55 +464,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && issue_dq(nt - 1)) mma_commit(acc_done);
     }
   } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;
+    const int wg = (warp - 4) >> 2;
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int i = i0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
     const float2 rs = (i < g.L) ? p.stats[(size_t)bh * p.Lpad + i] : make_float2(0.f, 0.f);
     bool ok = true;
-    for (int n = 0; n < nt; ++n) {
+    for (int n = wg; n < nt; n += 2) {
       const int sb = n & 1;
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[BN], dv[BN];
+      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + BMQ - 1 - j0 < g.W);
+      // key columns c of this tile visible to row i: j0 + c in [i - W + 1, i]
+      const int clo = g.W > 0 ? max(0, i - g.W + 1 - j0) : 0;
+      const int chi = min(BN - 1, i - j0);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
-        uint32_t a[32], bb[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, a);
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, bb);
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, sv);
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, dv);
         tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[c * 32 + e] = a[e];
-          dv[c * 32 + e] = bb[e];
-        }
+        uint32_t dd[16];
+        if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
+        else dq_chunk<false>(sv, dv, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
+        tmem_st16(tmem + lane_off + C::DP_COL + sb * BN + c * 16, dd);
       }
-      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + BMQ - 1 - j0 < g.W);
-      uint32_t dd[BN / 2];
-#pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        float dr[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = e + u;
-          float pv = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -rs.x));
-          if (!full) pv = in_band(i, j0 + c, g.W) ? pv : 0.f;
-          dr[u] = pv * (__uint_as_float(dv[c]) - rs.y);
-        }
-        dd[e / 2] = pack_half2(dr[0], dr[1]);
-      }
-      tmem_st32(tmem + lane_off + C::DP_COL + sb * BN, dd);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(ds_full + sb);
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
+      // each warpgroup writes half of the dQ columns
       const bool row_ok = i < g.L;
       float* row = p.out0 + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         uint32_t a[32];
         tmem_ld32(tmem + lane_off + C::DQ_COL + c * 32, a);
         tmem_wait_ld();

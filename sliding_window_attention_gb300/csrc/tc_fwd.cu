@@ -38,7 +38,6 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;
-constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -50,10 +49,14 @@ struct FwdCfg {
   static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks per row
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int O_COL = 0;                   // O accumulator columns [0, D)
+  static constexpr int NWG = 1;                     // softmax warpgroups (key-tile parity split)
+  static constexpr int THREADS = 128 + 128 * NWG;
+  static constexpr int O_COL = 0;                   // O of warpgroup w at [128 w, 128 w + D)
   static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
-  static constexpr size_t SMEM = (size_t)Q_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 /*barriers*/ + 1024 /*align*/;
+  // barriers (256 B) + the (m, l) exchange of the two warpgroups (2 x 128 float2)
+  static constexpr size_t SMEM = (size_t)Q_BYTES + 2 * (size_t)NS * KV_BYTES + 4096 + 1024 /*align*/;
   static_assert(D <= 256, "O must fit below the S buffers");
+  static_assert(NWG == 1 || D <= 128, "two O accumulators must fit below the S buffers");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
 };
 
@@ -65,12 +68,82 @@ struct FwdParams {
   int n_qtiles;
 };
 
+// One tile of the forward softmax for one row held in registers (raw scores
+// sr[BN]): returns the tile's scaled row maximum through *tmax_out after
+// pass 1; pass 2 (exp) runs in softmax_tile_p.  FULL: every entry is in the
+// band (no masking code at all); otherwise entries outside [clo, chi] are
+// masked in the scaled domain, which is correct for any sign of the scale.
+template <int BN, bool FULL>
+__device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], float sl2, int clo, int chi) {
+  float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+  if (FULL) {
+    if (sl2 >= 0.f) {
+#pragma unroll
+      for (int e = 0; e < BN; e += 4) {
+        a0 = fmaxf(a0, __uint_as_float(sr[e]));
+        a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
+        a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
+        a3 = fmaxf(a3, __uint_as_float(sr[e + 3]));
+      }
+      return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
+    }
+    float b0 = INFINITY, b1 = INFINITY, b2 = INFINITY, b3 = INFINITY;
+#pragma unroll
+    for (int e = 0; e < BN; e += 4) {
+      b0 = fminf(b0, __uint_as_float(sr[e]));
+      b1 = fminf(b1, __uint_as_float(sr[e + 1]));
+      b2 = fminf(b2, __uint_as_float(sr[e + 2]));
+      b3 = fminf(b3, __uint_as_float(sr[e + 3]));
+    }
+    return fminf(fminf(b0, b1), fminf(b2, b3)) * sl2;
+  }
+#pragma unroll
+  for (int e = 0; e < BN; e += 2) {
+    const float x0 = (e >= clo && e <= chi) ? __uint_as_float(sr[e]) * sl2 : -INFINITY;
+    const float x1 = (e + 1 >= clo && e + 1 <= chi) ? __uint_as_float(sr[e + 1]) * sl2 : -INFINITY;
+    if (e & 2) a1 = fmaxf(a1, fmaxf(x0, x1));
+    else a0 = fmaxf(a0, fmaxf(x0, x1));
+  }
+  return fmaxf(a0, a1);
+}
+
+// Pass 2: P = 2^(sl2 * s - m) for the row, rounded to fp16, packed two per
+// 32-bit TMEM column at p_taddr; returns the fp32 row sum.
+template <int BN, bool FULL>
+__device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, int clo, int chi,
+                                                uint32_t p_taddr) {
+  float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int col = c * 32 + e;
+      float p0, p1;
+      if (FULL) {
+        p0 = fast_exp2(fmaf(__uint_as_float(sr[col]), sl2, -m_use));
+        p1 = fast_exp2(fmaf(__uint_as_float(sr[col + 1]), sl2, -m_use));
+      } else {
+        const float x0 = (col >= clo && col <= chi) ? __uint_as_float(sr[col]) * sl2 : -INFINITY;
+        const float x1 = (col + 1 >= clo && col + 1 <= chi) ? __uint_as_float(sr[col + 1]) * sl2 : -INFINITY;
+        p0 = fast_exp2(x0 - m_use);
+        p1 = fast_exp2(x1 - m_use);
+      }
+      ps[(e >> 1) & 3] += p0 + p1;
+      const __half2 hp = __floats2half2_rn(p0, p1);
+      pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+    }
+    tmem_st16(p_taddr + c * 16, pk);
+  }
+  return (ps[0] + ps[1]) + (ps[2] + ps[3]);
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int BN = C::BN, NS = C::NS, KCH = C::KCH;
+  constexpr int BN = C::BN, NS = C::NS, KCH = C::KCH, NWG = C::NWG;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sQ = base;
@@ -84,9 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = v_full + NS;
   uint64_t* s_full = v_empty + NS;  // [2]
   uint64_t* p_full = s_full + 2;    // [2]
-  uint64_t* o_done = p_full + 2;    // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 1);
+  uint64_t* o_done = p_full + 2;    // [NWG]: PV into O of warpgroup w complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + NWG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* ml_x = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(bars) + 256);  // [NWG][128] (m, l)
 
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32;
@@ -112,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_full + s, 1);
       mbar_init(p_full + s, 128);
     }
-    mbar_init(o_done, 1);
+    for (int w = 0; w < NWG; ++w) mbar_init(o_done + w, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -163,9 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bdesc = smem_desc_sw128(vaddr + ks * 2048, BN * 128, 1024);
-          mma_ts(tmem + C::O_COL, tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV, (m > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + C::O_COL + 128 * (m % NWG), tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV,
+                 (m >= NWG || ks > 0) ? 1u : 0u);
         }
-        mma_commit(o_done);
+        mma_commit(o_done + (m % NWG));
         mma_commit(v_empty + st);
         return true;
       };
@@ -189,108 +264,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------- softmax / correction / epilogue ----------------
-    const int r = threadIdx.x - 128;
+    const int wg = (warp - 4) >> 2;  // takes key tiles n with n % NWG == wg, into its own O
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int i = i0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t o_col = C::O_COL + 128 * wg;
     const float sl2 = g.scale * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int n = 0; n < nt; ++n) {
+    int k = 0;  // tiles this warpgroup has processed
+    for (int n = wg; n < nt; n += NWG, ++k) {
       const int sb = n & 1;
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      float x[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(rr[e]) * sl2;
-      }
       const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + kBM - 1 - j0 < g.W);
-      if (!full) {
+      // the whole S row in registers: all loads issued, then one wait
+      uint32_t sr[BN];
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          const int j = j0 + e;
-          const bool valid = (j <= i) && (g.W == 0 || i - j < g.W);
-          x[e] = valid ? x[e] : -INFINITY;
-        }
-      }
-      float tmax = x[0];
-#pragma unroll
-      for (int e = 1; e < BN; ++e) tmax = fmaxf(tmax, x[e]);
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+      tmem_wait_ld();
+      // Visible key columns of this row inside the tile: [clo, chi] (edge tiles only).
+      const int clo = (g.W > 0) ? max(0, i - g.W + 1 - j0) : 0;
+      const int chi = min(BN - 1, i - j0);
+      const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, clo, chi)
+                              : softmax_tile_max<BN, false>(sr, sl2, clo, chi);
       float alpha = 1.f;
       bool rescale = false;
       if (tmax > m_run + kRescaleLog2) {
         if (m_run != -INFINITY) {
-          alpha = exp2f(m_run - tmax);
+          alpha = fast_exp2(m_run - tmax);
           rescale = true;
         }
         m_run = tmax;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float psum = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = exp2f(x[c * 64 + 2 * e] - m_use);
-          const float p1 = exp2f(x[c * 64 + 2 * e + 1] - m_use);
-          const __half2 hp = __floats2half2_rn(p0, p1);
-          const float2 back = __half22float2(hp);
-          psum += back.x + back.y;
-          pk[e] = *reinterpret_cast<const uint32_t*>(&hp);
-        }
-        tmem_st32(tmem + lane_off + C::S_COL + sb * BN + c * 32, pk);
-      }
+      const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN;
+      const float psum = full ? softmax_tile_p<BN, true>(sr, sl2, m_use, clo, chi, p_taddr)
+                              : softmax_tile_p<BN, false>(sr, sl2, m_use, clo, chi, p_taddr);
       l_run = l_run * alpha + psum;
       // Wait for PV(n-1) at every tile, not only when rescaling: this thread then
       // has observed every earlier PV completion, so the o_done phase can be at
       // most one ahead of the parity asked for (no aliasing of phase n-3 with
       // n-1), and a rescale never overlaps an in-flight PV.
-      if (n > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) { ok = false; break; }
+      if (k > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done + wg, (k - 1) & 1, abort_flag))) { ok = false; break; }
         tc_fence_after();
       }
       // tcgen05.ld/st are warp-collective: the whole warp rescales if any row needs it
-      if (__any_sync(0xffffffffu, rescale) && n > 0) {
+      if (__any_sync(0xffffffffu, rescale) && k > 0) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
-          tmem_ld32(tmem + lane_off + C::O_COL + c * 32, rr);
+          tmem_ld32(tmem + lane_off + o_col + c * 32, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st32(tmem + lane_off + C::O_COL + c * 32, rr);
+          tmem_st32(tmem + lane_off + o_col + c * 32, rr);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + sb);
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (nt - 1) & 1, abort_flag))) {
-      tc_fence_after();
-      const bool row_ok = i < g.L;
-      const float inv = 1.f / l_run;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+    // this warpgroup's O is final once its last PV completes (k tiles processed)
+    if (ok && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done + wg, (k - 1) & 1, abort_flag));
+    // merge the per-warpgroup softmax states: m = max(m_w), l = sum_w l_w 2^(m_w - m),
+    // O = sum_w O_w 2^(m_w - m) / l.  Each warpgroup writes half of the columns.
+    ml_x[wg * 128 + r] = make_float2(m_run, l_run);
+    tc_fence_before();
+    if (NWG == 2) asm volatile("bar.sync 1, 256;" ::: "memory");
+    else asm volatile("bar.sync 1, 128;" ::: "memory");
+    tc_fence_after();
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    if (ok) {
+      float m_tot = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, rr);  // warp-collective: every lane loads
-        tmem_wait_ld();
+      for (int w = 0; w < NWG; ++w) m_tot = fmaxf(m_tot, ml_x[w * 128 + r].x);
+      float f[NWG];
+      float l_tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWG; ++w) {
+        const float2 x = ml_x[w * 128 + r];
+        f[w] = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - m_tot);
+        l_tot += x.y * f[w];
+      }
+      const bool row_ok = i < g.L;
+      const float inv = 1.f / l_tot;
+#pragma unroll
+      for (int w = 0; w < NWG; ++w) f[w] *= inv;
+      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+      constexpr int CPW = D / 32 / NWG;  // 32-column chunks written per warpgroup
+#pragma unroll
+      for (int cc = 0; cc < CPW; ++cc) {
+        const int c = wg * CPW + cc;
+        uint32_t acc[NWG][32];
+#pragma unroll
+        for (int w = 0; w < NWG; ++w) tmem_ld32(tmem + lane_off + C::O_COL + 128 * w + c * 32, acc[w]);
+        tmem_wait_ld();  // warp-collective: every lane loads, only valid rows store
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            float4 v4 = make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
-                                    __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
-            *reinterpret_cast<float4*>(orow + c * 32 + e) = v4;
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float t = 0.f;
+#pragma unroll
+              for (int w = 0; w < NWG; ++w)  // skip a state with no keys: its TMEM O was never written
+                t = (f[w] == 0.f) ? t : fmaf(__uint_as_float(acc[w][e + u]), f[w], t);
+              v[u] = t;
+            }
+            *reinterpret_cast<float4*>(orow + c * 32 + e) = make_float4(v[0], v[1], v[2], v[3]);
           }
         }
       }
-      if (row_ok) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_run)) * kLn2;
+      if (row_ok && wg == 0) p.lse[(size_t)bh * g.L + i] = (m_tot + log2f(l_tot)) * kLn2;
     }
   }
 
@@ -414,7 +503,7 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   p.status = status;
   p.n_qtiles = (g.L + kBM - 1) / kBM;
   dim3 grid(g.B * g.Hq, p.n_qtiles);
-  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, p);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
