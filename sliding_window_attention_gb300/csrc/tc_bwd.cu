@@ -39,6 +39,8 @@ using namespace tc;
 constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11: two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 512 TMEM columns)
+constexpr int kSmemMax = 232448;         // dynamic shared memory per block on sm_103 (227 KB)
+constexpr int clamp_stages(int n) { return n < 2 ? 2 : (n > 8 ? 8 : n); }
 
 // Row statistics for the backward: per (b*Hq + h, i < Lpad) the pair
 // (lse_i * log2(e), Delta_i = dO_i . o_i); zero for padding rows i >= L.
@@ -113,15 +115,17 @@ template <int D>
 struct KvCfg {
   static constexpr int BNK = 128;  // key rows per CTA (MMA M)
   static constexpr int BM = 64;    // query rows per step (MMA N for S^T / dP^T, K for dV / dK)
-  static constexpr int NS = 2;     // Q / dO / stats stages
   static constexpr int KCH = D / 64;
   static constexpr int KV_BYTES = BNK * D * 2;  // K (or V) tile
   static constexpr int QT_BYTES = BM * D * 2;   // Q (or dO) tile
   static constexpr int ST_BYTES = BM * 8;       // (lse, Delta) pairs
   static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, stats (padded to 1 KB)
+  // Q / dO / stats stages: as many as shared memory holds (TMA latency hiding)
+  static constexpr int NS = clamp_stages((kSmemMax - 2048 - 2 * KV_BYTES) / STAGE_BYTES);
   static constexpr int DV_COL = 0, DK_COL = D, S_COL = 256, DP_COL = 384;
   static constexpr size_t SMEM_USED = 2 * (size_t)KV_BYTES + NS * (size_t)STAGE_BYTES + 1024 + 1024;
   static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
   static_assert(2 * D <= 256, "dK and dV must fit below the S buffers");
 };
 
@@ -335,13 +339,15 @@ template <int D>
 struct DqCfg {
   static constexpr int BMQ = 128;  // query rows per CTA (MMA M)
   static constexpr int BN = 64;    // key rows per step
-  static constexpr int NS = 2;
   static constexpr int KCH = D / 64;
   static constexpr int QT_BYTES = BMQ * D * 2;  // Q (or dO) tile
   static constexpr int KV_BYTES = BN * D * 2;   // K (or V) tile
+  // K / V stages: as many as shared memory holds (TMA latency hiding)
+  static constexpr int NS = clamp_stages((kSmemMax - 2048 - 2 * QT_BYTES) / (2 * KV_BYTES));
   static constexpr int DQ_COL = 0, S_COL = 256, DP_COL = 384;
   static constexpr size_t SMEM_USED = 2 * (size_t)QT_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 + 1024;
   static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
   static_assert(D <= 256, "dQ must fit below the S buffers");
 };
 

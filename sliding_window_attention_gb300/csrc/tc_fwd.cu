@@ -42,19 +42,25 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
+constexpr int kSmemMax = 232448;  // dynamic shared memory per block on sm_103 (227 KB)
+
 template <int D>
 struct FwdCfg {
   static constexpr int BN = (D <= 128) ? 128 : 64;  // key tile rows
-  static constexpr int NS = (D == 64) ? 4 : 2;      // K/V pipeline stages
+  static constexpr int NWG = 1;                     // softmax warpgroups (key-tile parity split)
+  static constexpr int THREADS = 128 + 128 * NWG;
   static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks per row
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NWG = 1;                     // softmax warpgroups (key-tile parity split)
-  static constexpr int THREADS = 128 + 128 * NWG;
+  static constexpr int BAR_BYTES = 2048;            // mbarriers (256 B) + (m, l) exchange (NWG x 1 KB)
+  // as many K/V stages as shared memory holds (TMA latency hiding), 2..8
+  static constexpr int NS_FIT = (kSmemMax - 1024 - BAR_BYTES - Q_BYTES) / (2 * KV_BYTES);
+  static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
   static constexpr int O_COL = 0;                   // O of warpgroup w at [128 w, 128 w + D)
   static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
-  // barriers (256 B) + the (m, l) exchange of the two warpgroups (2 x 128 float2)
-  static constexpr size_t SMEM = (size_t)Q_BYTES + 2 * (size_t)NS * KV_BYTES + 4096 + 1024 /*align*/;
+  static constexpr size_t SMEM = (size_t)Q_BYTES + 2 * (size_t)NS * KV_BYTES + BAR_BYTES + 1024 /*align*/;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
+  static_assert(256 + NWG * 1024 <= BAR_BYTES, "barrier region");
   static_assert(D <= 256, "O must fit below the S buffers");
   static_assert(NWG == 1 || D <= 128, "two O accumulators must fit below the S buffers");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
@@ -394,45 +400,43 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-// bf16 -> fp16 operand copies (up to four tensors per launch).
-struct ConvertSeg {
-  const uint16_t* src;
-  uint16_t* dst;
-  long long n8;  // number of 8-element chunks
-};
-struct ConvertArgs {
-  ConvertSeg seg[4];
-  int nseg;
-  int* status;
-};
-
-__global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const ConvertArgs a) {
-  long long total = 0;
-  for (int s = 0; s < a.nseg; ++s) total += a.seg[s].n8;
-  bool overflow = false;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    long long k = idx;
-    int s = 0;
-    while (s < a.nseg - 1 && k >= a.seg[s].n8) {
-      k -= a.seg[s].n8;
-      ++s;
-    }
-    const uint4 in = reinterpret_cast<const uint4*>(a.seg[s].src)[k];
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t o[4];
+// bf16 -> fp16 operand copies (up to four tensors per launch; blockIdx.y
+// selects the tensor).  Each thread moves two 16-byte vectors per iteration.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 in, bool& overflow) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float lo = __uint_as_float(w[e] << 16);
-      const float hi = __uint_as_float(w[e] & 0xffff0000u);
-      const __half2 hv = __floats2half2_rn(lo, hi);
-      const float2 back = __half22float2(hv);
-      overflow |= (isinf(back.x) && !isinf(lo)) || (isinf(back.y) && !isinf(hi));
-      o[e] = *reinterpret_cast<const uint32_t*>(&hv);
-    }
-    reinterpret_cast<uint4*>(a.seg[s].dst)[k] = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int e = 0; e < 4; ++e) {
+    const float lo = __uint_as_float(w[e] << 16);
+    const float hi = __uint_as_float(w[e] & 0xffff0000u);
+    const __half2 hv = __floats2half2_rn(lo, hi);
+    const float2 back = __half22float2(hv);
+    overflow |= (isinf(back.x) && !isinf(lo)) || (isinf(back.y) && !isinf(hi));
+    o[e] = *reinterpret_cast<const uint32_t*>(&hv);
   }
-  if (overflow) atomicCAS(a.status, 0, kStatusFp16Range);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const uint16_t* s0, uint16_t* d0, long long n0,
+                                                               const uint16_t* s1, uint16_t* d1, long long n1,
+                                                               const uint16_t* s2, uint16_t* d2, long long n2,
+                                                               const uint16_t* s3, uint16_t* d3, long long n3,
+                                                               int* status) {
+  const int seg = blockIdx.y;
+  const uint4* src = reinterpret_cast<const uint4*>(seg == 0 ? s0 : seg == 1 ? s1 : seg == 2 ? s2 : s3);
+  uint4* dst = reinterpret_cast<uint4*>(seg == 0 ? d0 : seg == 1 ? d1 : seg == 2 ? d2 : d3);
+  const long long n16 = (seg == 0 ? n0 : seg == 1 ? n1 : seg == 2 ? n2 : n3) / 8;  // 16-byte vectors
+  bool overflow = false;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; idx + stride < n16; idx += 2 * stride) {
+    const uint4 a = __ldcs(src + idx);
+    const uint4 b = __ldcs(src + idx + stride);
+    dst[idx] = bf16x8_to_f16x8(a, overflow);
+    dst[idx + stride] = bf16x8_to_f16x8(b, overflow);
+  }
+  if (idx < n16) dst[idx] = bf16x8_to_f16x8(__ldcs(src + idx), overflow);
+  if (overflow) atomicCAS(status, 0, kStatusFp16Range);
 }
 
 // ---------------------------------------------------------------------------
@@ -467,20 +471,25 @@ cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int hea
 
 cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
                                int* status, cudaStream_t s) {
-  ConvertArgs a;
-  a.nseg = count;
-  a.status = status;
-  long long total = 0;
+  if (count < 1 || count > 4) return cudaErrorInvalidValue;
+  const uint16_t* sp[4] = {nullptr, nullptr, nullptr, nullptr};
+  uint16_t* dp[4] = {nullptr, nullptr, nullptr, nullptr};
+  long long nn[4] = {0, 0, 0, 0};
+  long long most = 0;
   for (int i = 0; i < count; ++i) {
-    a.seg[i].src = src[i];
-    a.seg[i].dst = dst[i];
-    a.seg[i].n8 = (long long)(n[i] / 8);
-    total += a.seg[i].n8;
+    sp[i] = src[i];
+    dp[i] = dst[i];
+    nn[i] = (long long)n[i];
+    most = nn[i] > most ? nn[i] : most;
   }
-  long long blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  // blocks per tensor: enough for ~8 resident blocks per SM over all tensors
+  long long blocks = (most / 8 + 511) / 512;
+  const long long cap = (152LL * 8 + count - 1) / count;
+  if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  convert_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+  dim3 grid((unsigned)blocks, count);
+  convert_bf16_f16_kernel<<<grid, 256, 0, s>>>(sp[0], dp[0], nn[0], sp[1], dp[1], nn[1], sp[2], dp[2], nn[2], sp[3],
+                                              dp[3], nn[3], status);
   return cudaGetLastError();
 }
 
