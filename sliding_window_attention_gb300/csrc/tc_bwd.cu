@@ -17,7 +17,7 @@
 //   dS = P (dP - Delta), dQ += dS K.  No read-modify-write of dQ in memory.
 //
 // Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner and the
-// single-thread MMA issuer, warps 4..7 and 8..11 two elementwise
+// single-thread MMA issuer, warps 2..5 and 6..9 two elementwise
 // softmax-gradient warpgroups (one TMEM lane, i.e. one row, per thread) that
 // take alternate steps, so one works while the other waits for its MMAs.
 // Every mbarrier wait is bounded (see tc_ptx.cuh).
@@ -36,7 +36,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11: two elementwise warpgroups
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9: two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 512 TMEM columns)
 constexpr int kSmemMax = 232448;         // dynamic shared memory per block on sm_103 (227 KB)
@@ -264,8 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && issue_grad(N - 1)) mma_commit(acc_done);
     }
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;                  // warpgroup: takes steps n with n % 2 == wg
+  } else {
+    // warpgroup (warps 2-5 or 6-9): takes steps n with n % 2 == wg; a warp can
+    // only reach TMEM lanes 32 * (warp % 4) .. +31, which fixes its rows
+    const int wg = (warp - 2) >> 2;
     const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int j = j0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -282,15 +284,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
       const int clo = max(0, j - i0);
       const int chi = min(min(BM - 1, g.L - 1 - i0), g.W > 0 ? j + g.W - 1 - i0 : BM - 1);
+      // all S^T / dP^T columns of this step with one TMEM wait
+      uint32_t sv[BM], dv[BM];
 #pragma unroll
       for (int c = 0; c < BM / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, sv);
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, dv);
-        tmem_wait_ld();
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BM / 32; ++c) {
+        const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
+        const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
         uint32_t pp[16], dd[16];
-        if (full) kv_chunk<true>(sv, dv, stats4, sl2, c * 32, clo, chi, pp, dd);
-        else kv_chunk<false>(sv, dv, stats4, sl2, c * 32, clo, chi, pp, dd);
+        if (full) kv_chunk<true>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
+        else kv_chunk<false>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
         // P^T / dS^T (fp16, two per column) overwrite columns already consumed
         tmem_st16(tmem + lane_off + C::S_COL + sb * BM + c * 16, pp);
         tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + c * 16, dd);
@@ -469,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && issue_dq(nt - 1)) mma_commit(acc_done);
     }
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;
+  } else {
+    const int wg = (warp - 2) >> 2;  // warps 2-5 / 6-9, see the dK/dV kernel
     const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -486,15 +494,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key columns c of this tile visible to row i: j0 + c in [i - W + 1, i]
       const int clo = g.W > 0 ? max(0, i - g.W + 1 - j0) : 0;
       const int chi = min(BN - 1, i - j0);
+      uint32_t sv[BN], dv[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, sv);
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, dv);
-        tmem_wait_ld();
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
+        const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
         uint32_t dd[16];
-        if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
-        else dq_chunk<false>(sv, dv, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
+        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
+        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
         tmem_st16(tmem + lane_off + C::DP_COL + sb * BN + c * 16, dd);
       }
       tmem_wait_st();
