@@ -394,6 +394,8 @@ def run_ours(args, w, world, rank, local_rank):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         per_pair = KERNEL_FLOPS_PER_PAIR_D.get(kname, 4)
+        if kname == "bwd_dkdv_tc" and D > 128:
+            per_pair = 10  # dV-only pass (S^T, dV) + dK-only pass (S^T, dP^T, dK)
         alg = per_pair * D * w.pairs()
         achieved = alg / avg_s / 1e12
         if kname.endswith("_simt"):

@@ -1,4 +1,4 @@
-// Tensor-core backward for sm_103a (head dims 64 and 128): a key-outer dK/dV
+// Tensor-core backward for sm_103a (head dims 64, 128, 256): a key-outer dK/dV
 // pass and a query-outer dQ pass, both on tcgen05 with accumulators in Tensor
 // Memory and operands staged by TMA.  P is recomputed from the forward's lse
 // instead of being stored ("Training -- design (ORPO, flash-CCE head, prefix
@@ -27,6 +27,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "swa_internal.h"
 #include "tc_ptx.cuh"
@@ -71,10 +73,11 @@ __global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, 
 
 __device__ __forceinline__ bool in_band(int i, int j, int W) { return j <= i && (W == 0 || i - j < W); }
 
-// dK/dV elementwise step for one key row and 32 query columns: P^T and
-// dS^T = P^T (dP^T - Delta) as fp16 pairs.  FULL: every column is in the band
-// (no mask code); otherwise columns outside [clo, chi] give exactly zero.
-template <bool FULL>
+// dK/dV elementwise step for one key row and 32 query columns: P^T (if
+// WANT_P) and dS^T = P^T (dP^T - Delta) (if WANT_DS) as fp16 pairs.  FULL:
+// every column is in the band (no mask code); otherwise columns outside
+// [clo, chi] give exactly zero.
+template <bool FULL, bool WANT_P, bool WANT_DS>
 __device__ __forceinline__ void kv_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float4* stats4,
                                          float sl2, int cbase, int clo, int chi, uint32_t (&pp)[16],
                                          uint32_t (&dd)[16]) {
@@ -87,8 +90,9 @@ __device__ __forceinline__ void kv_chunk(const uint32_t (&sv)[32], const uint32_
       p0 = (cbase + e >= clo && cbase + e <= chi) ? p0 : 0.f;
       p1 = (cbase + e + 1 >= clo && cbase + e + 1 <= chi) ? p1 : 0.f;
     }
-    pp[e >> 1] = pack_half2(p0, p1);
-    dd[e >> 1] = pack_half2(p0 * (__uint_as_float(dv[e]) - rs.y), p1 * (__uint_as_float(dv[e + 1]) - rs.w));
+    if (WANT_P) pp[e >> 1] = pack_half2(p0, p1);
+    if (WANT_DS)
+      dd[e >> 1] = pack_half2(p0 * (__uint_as_float(dv[e]) - rs.y), p1 * (__uint_as_float(dv[e + 1]) - rs.w));
   }
 }
 
@@ -110,23 +114,36 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_
 }
 
 // ===========================================================================
-// dK / dV
-template <int D>
+// dK / dV.  MODE: both accumulators in one CTA (head dim <= 128), or, when
+// dK and dV of a 128-key tile do not both fit in the 512 TMEM columns (head
+// dim 256), a dV-only CTA (S^T, P^T, dV) and a dK-only CTA (S^T, dP^T, dS^T,
+// dK) launched as two kernels.
+enum { kModeBoth = 0, kModeDV = 1, kModeDK = 2 };
+
+template <int D, int MODE>
 struct KvCfg {
-  static constexpr int BNK = 128;  // key rows per CTA (MMA M)
-  static constexpr int BM = 64;    // query rows per step (MMA N for S^T / dP^T, K for dV / dK)
+  static constexpr int BNK = 128;                  // key rows per CTA (MMA M)
+  static constexpr int BM = (D <= 128) ? 64 : 32;  // query rows per step
+  static constexpr bool NEED_V = MODE != kModeDV;  // dP^T = V dO^T
+  static constexpr bool DO_DV = MODE != kModeDK;
+  static constexpr bool DO_DK = MODE != kModeDV;
   static constexpr int KCH = D / 64;
   static constexpr int KV_BYTES = BNK * D * 2;  // K (or V) tile
   static constexpr int QT_BYTES = BM * D * 2;   // Q (or dO) tile
   static constexpr int ST_BYTES = BM * 8;       // (lse, Delta) pairs
   static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, stats (padded to 1 KB)
+  static constexpr int RES_BYTES = (NEED_V ? 2 : 1) * KV_BYTES;  // resident K (and V)
   // Q / dO / stats stages: as many as shared memory holds (TMA latency hiding)
-  static constexpr int NS = clamp_stages((kSmemMax - 2048 - 2 * KV_BYTES) / STAGE_BYTES);
-  static constexpr int DV_COL = 0, DK_COL = D, S_COL = 256, DP_COL = 384;
-  static constexpr size_t SMEM_USED = 2 * (size_t)KV_BYTES + NS * (size_t)STAGE_BYTES + 1024 + 1024;
+  static constexpr int NS = clamp_stages((kSmemMax - 2048 - RES_BYTES) / STAGE_BYTES);
+  // TMEM: dV at 0 and dK at D (both), or the single accumulator at 0
+  static constexpr int DV_COL = 0;
+  static constexpr int DK_COL = (MODE == kModeDK) ? 0 : D;
+  static constexpr int S_COL = 256, DP_COL = 384;
+  static constexpr size_t SMEM_USED = (size_t)RES_BYTES + NS * (size_t)STAGE_BYTES + 1024 + 1024;
   static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(2 * D <= 256, "dK and dV must fit below the S buffers");
+  static_assert((MODE == kModeBoth ? 2 * D : D) <= 256, "accumulators must fit below the S buffers");
+  static_assert(S_COL + 2 * BM <= DP_COL && DP_COL + 2 * BM <= 512, "TMEM columns");
 };
 
 struct BwdParams {
@@ -139,18 +156,18 @@ struct BwdParams {
   int* status;
 };
 
-template <int D>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                    const __grid_constant__ CUtensorMap tmS, const BwdParams p) {
-  using C = KvCfg<D>;
+  using C = KvCfg<D, MODE>;
   constexpr int BNK = C::BNK, BM = C::BM, NS = C::NS, KCH = C::KCH;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sK = base;
-  unsigned char* sV = sK + C::KV_BYTES;
-  unsigned char* sStage = sV + C::KV_BYTES;
+  unsigned char* sV = sK + C::KV_BYTES;  // only used when C::NEED_V
+  unsigned char* sStage = sK + C::RES_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::STAGE_BYTES);
   uint64_t* kv_full = bars;                // [1]
   uint64_t* st_full = kv_full + 1;         // [NS]
@@ -202,10 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmG);
       prefetch_tmap(&tmS);
-      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      mbar_arrive_expect_tx(kv_full, C::RES_BYTES);
       for (int c = 0; c < KCH; ++c) {
         tma_load_3d(sK + c * BNK * 128, &tmK, kv_full, c * 64, j0, bkv);
-        tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
+        if (C::NEED_V) tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
       }
       for (int n = 0; n < N; ++n) {
         const int st = n % NS;
@@ -236,10 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks) {
           const uint32_t acc = (m > 0 || ks > 0) ? 1u : 0u;
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + sb * BM + ks * 8,
-                 smem_desc_sw128(gaddr + ks * 2048, BM * 128, 1024), idG, acc);
-          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + sb * BM + ks * 8,
-                 smem_desc_sw128(qaddr + ks * 2048, BM * 128, 1024), idG, acc);
+          if (C::DO_DV)
+            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + sb * BM + ks * 8,
+                   smem_desc_sw128(gaddr + ks * 2048, BM * 128, 1024), idG, acc);
+          if (C::DO_DK)
+            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + sb * BM + ks * 8,
+                   smem_desc_sw128(qaddr + ks * 2048, BM * 128, 1024), idG, acc);
         }
         mma_commit(st_empty + st);
         return true;
@@ -256,8 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ck = (ks >> 2) * BNK * 128, cq = (ks >> 2) * BM * 128;
           mma_ss(tmem + C::S_COL + sb * BM, smem_desc_sw128(kaddr + ck + off, 16, 1024),
                  smem_desc_sw128(qaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
-          mma_ss(tmem + C::DP_COL + sb * BM, smem_desc_sw128(vaddr + ck + off, 16, 1024),
-                 smem_desc_sw128(gaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          if (C::NEED_V)
+            mma_ss(tmem + C::DP_COL + sb * BM, smem_desc_sw128(vaddr + ck + off, 16, 1024),
+                   smem_desc_sw128(gaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
         }
         mma_commit(sdp_full + sb);
         if (n >= 1 && !issue_grad(n - 1)) { ok = false; break; }
@@ -289,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < BM / 32; ++c) {
         tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+        if (C::NEED_V)
+          tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
       }
       tmem_wait_ld();
 #pragma unroll
@@ -297,11 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
         uint32_t pp[16], dd[16];
-        if (full) kv_chunk<true>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
-        else kv_chunk<false>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
+        if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
+        else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
         // P^T / dS^T (fp16, two per column) overwrite columns already consumed
-        tmem_st16(tmem + lane_off + C::S_COL + sb * BM + c * 16, pp);
-        tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + c * 16, dd);
+        if (C::DO_DV) tmem_st16(tmem + lane_off + C::S_COL + sb * BM + c * 16, pp);
+        if (C::DO_DK) tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + c * 16, dd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -309,14 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
-      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
+      // both accumulators: warpgroup 0 writes dK (scaled), warpgroup 1 writes dV;
+      // one accumulator: each warpgroup writes half of its columns
       const bool row_ok = j < g.L;
       const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
-      const uint32_t col = wg == 0 ? C::DK_COL : C::DV_COL;
-      const float mul = wg == 0 ? g.scale : 1.f;
-      float* dst = (wg == 0 ? p.out0 : p.out1) + off;
+      const bool wr_dk = (MODE == kModeBoth) ? (wg == 0) : (MODE == kModeDK);
+      const uint32_t col = wr_dk ? C::DK_COL : C::DV_COL;
+      const float mul = wr_dk ? g.scale : 1.f;
+      float* dst = (wr_dk ? p.out0 : p.out1) + off;
+      constexpr int NCH = (MODE == kModeBoth) ? D / 32 : D / 64;  // 32-column chunks per warpgroup
+      const int c0 = (MODE == kModeBoth) ? 0 : wg * NCH;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = c0 + cc;
         uint32_t a[32];
         tmem_ld32(tmem + lane_off + col + c * 32, a);
         tmem_wait_ld();
@@ -345,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dQ
 template <int D>
 struct DqCfg {
-  static constexpr int BMQ = 128;  // query rows per CTA (MMA M)
-  static constexpr int BN = 64;    // key rows per step
+  static constexpr int BMQ = 128;                  // query rows per CTA (MMA M)
+  static constexpr int BN = (D <= 128) ? 64 : 32;  // key rows per step
   static constexpr int KCH = D / 64;
   static constexpr int QT_BYTES = BMQ * D * 2;  // Q (or dO) tile
   static constexpr int KV_BYTES = BN * D * 2;   // K (or V) tile
@@ -576,21 +602,34 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
   p.Lpad = Lpad;
   p.status = status;
   if (which == 0) {
-    using C = KvCfg<D>;
-    CUtensorMap tq, tk, tv, tg, ts;
-    if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e;
-    if ((e = make_tmap_stats(&ts, stats, Lpad, g.B * g.Hq, 2 * C::BM)) != cudaSuccess) return e;
-    auto kern = dkdv_tc_kernel<D>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
-      return e;
-    p.out0 = dk;
-    p.out1 = dv;
-    p.n_tiles = (g.L + C::BNK - 1) / C::BNK;
-    dim3 grid(g.B * g.Hkv, p.n_tiles);
-    kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, ts, p);
+    auto run = [&](auto mode_tag) -> cudaError_t {
+      constexpr int MODE = decltype(mode_tag)::value;
+      using C = KvCfg<D, MODE>;
+      CUtensorMap tq, tk, tv, tg, ts;
+      cudaError_t e2;
+      if ((e2 = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_stats(&ts, stats, Lpad, g.B * g.Hq, 2 * C::BM)) != cudaSuccess) return e2;
+      auto kern = dkdv_tc_kernel<D, MODE>;
+      if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
+          cudaSuccess)
+        return e2;
+      BwdParams pm = p;
+      pm.out0 = dk;
+      pm.out1 = dv;
+      pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
+      dim3 grid(g.B * g.Hkv, pm.n_tiles);
+      kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, ts, pm);
+      return cudaGetLastError();
+    };
+    if constexpr (D <= 128) {
+      return run(std::integral_constant<int, kModeBoth>{});
+    } else {
+      if ((e = run(std::integral_constant<int, kModeDV>{})) != cudaSuccess) return e;
+      return run(std::integral_constant<int, kModeDK>{});
+    }
   } else {
     using C = DqCfg<D>;
     CUtensorMap tq, tk, tv, tg;
@@ -612,7 +651,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
 
 }  // namespace
 
-bool bwd_tc_supported(int D) { return D == 64 || D == 128; }
+bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
 
 int bwd_stats_lpad(int L) { return (L + 127) / 128 * 128; }
 
@@ -630,6 +669,7 @@ cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_
   switch (g.D) {
     case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
     case 128: return bwd_tc_d<128>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
+    case 256: return bwd_tc_d<256>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -640,6 +680,7 @@ cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t*
   switch (g.D) {
     case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
     case 128: return bwd_tc_d<128>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
+    case 256: return bwd_tc_d<256>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
     default: return cudaErrorInvalidValue;
   }
 }
