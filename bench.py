@@ -161,6 +161,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, max_ms: float) -> float:
+    """Work of all ranks (each runs its own copy of the workload) over the slowest rank's time."""
+    return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -339,12 +355,9 @@ def run_ours(args, w, world, rank, local_rank):
         raise RuntimeError(f"device status after timed steps: {swa.strerror(status)}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     useful = w.fwd_flops() + w.bwd_flops()
-    value = world * useful * args.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(world, useful, args.steps, total_ms)
     launches = sum(n for n, _ in kernels.values())
 
     # end to end through the public API: pinned host inputs in, results out
@@ -375,11 +388,8 @@ def run_ours(args, w, world, rank, local_rank):
         ee.record(stream)
         torch.cuda.synchronize()
         e2e_ms += es.elapsed_time(ee)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * useful * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = whole_job_tflops(world, useful, e2e_steps, e2e_ms)
 
     # roofline of the dominant kernel
     top = max(kernels.items(), key=lambda kv: kv[1][1])

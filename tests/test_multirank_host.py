@@ -1,0 +1,85 @@
+"""Multi-rank host logic of bench.py, on CPU with gloo (world size 2).
+
+On the GPU machine bench.py runs one rank per GPU over NCCL; each rank runs its
+own copy of the workload and the only collectives are a barrier and the
+max-over-ranks of the timings.  These tests run that aggregation with gloo
+processes on the CPU, plus the reference arm under two ranks (rank 0 times
+the oracle, the other rank exits at once without work).
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out_q):
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    local_ms = [12.5, 20.0][rank]
+    dist.barrier()
+    m = bench.max_over_ranks(local_ms, dist, "cpu")
+    v = bench.whole_job_tflops(world, 1e12, 10, m)
+    out_q.put((rank, m, v))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_value_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, m, v in res:
+        assert m == 20.0  # every rank sees the slowest rank's time
+        # 2 ranks x 1e12 flop x 10 steps / 20 ms = 1000 TFLOP/s
+        assert abs(v - 1000.0) < 1e-9
+
+
+def test_single_process_helpers():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert abs(bench.whole_job_tflops(1, 2e12, 5, 10.0) - 1000.0) < 1e-9
+
+
+def test_reference_arm_two_ranks_rank0_only():
+    """torchrun-style environment, 2 ranks: rank 1 prints nothing and exits 0;
+    rank 0 prints one JSON line with impl=reference."""
+    outs = []
+    for rank in (1, 0):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2", MASTER_ADDR="127.0.0.1",
+                   MASTER_PORT=str(_free_port()))
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                            "--steps", "1", "--warmup", "0", "--workload", "tiny_l256_d64_w64"],
+                           env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append(r.stdout.strip())
+    assert outs[0] == ""
+    line = json.loads(outs[1].splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
