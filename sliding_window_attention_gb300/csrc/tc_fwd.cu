@@ -1,7 +1,9 @@
 // Tensor-core forward for sm_103a: S = scale * Q K^T and O = P V on tcgen05
 // with accumulators in Tensor Memory, operand tiles staged by TMA.
 //
-// One CTA per (128-row query tile, query head).  Warp roles:
+// One CTA per (128-row query tile, query head) -- and, at head dim 512, per
+// 256-column half of O: O does not fit in TMEM whole, so each half-CTA
+// recomputes S over the full head dim and accumulates its half.  Warp roles:
 //   warp 0      TMA producer: Q once, then K and V tiles through an NS-deep ring
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
 //   warps 4..7  softmax: thread r owns query row i0 + r (TMEM lane r); reads its
@@ -46,23 +48,30 @@ constexpr int kSmemMax = 232448;  // dynamic shared memory per block on sm_103 (
 
 template <int D>
 struct FwdCfg {
-  static constexpr int BN = (D <= 128) ? 128 : 64;  // key tile rows
+  // key tile rows: the K (and V) tiles must leave room for >= 2 pipeline stages
+  static constexpr int BN = (D <= 128) ? 128 : (D == 256 ? 64 : 32);
+  // output columns per CTA: all of D, or one 256-column half at D = 512 (O
+  // must fit in TMEM; the two halves each recompute S over the full D)
+  static constexpr int DV = (D <= 256) ? D : 256;
+  static constexpr int NSPLIT = D / DV;
   static constexpr int NWG = 1;                     // softmax warpgroups (key-tile parity split)
   static constexpr int THREADS = 128 + 128 * NWG;
-  static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks per row
+  static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks of a Q / K row
+  static constexpr int VCH = DV / 64;               // chunks of the V columns this CTA uses
   static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int K_BYTES = BN * D * 2;
+  static constexpr int V_BYTES = BN * DV * 2;
   static constexpr int BAR_BYTES = 2048;            // mbarriers (256 B) + (m, l) exchange (NWG x 1 KB)
   // as many K/V stages as shared memory holds (TMA latency hiding), 2..8
-  static constexpr int NS_FIT = (kSmemMax - 1024 - BAR_BYTES - Q_BYTES) / (2 * KV_BYTES);
+  static constexpr int NS_FIT = (kSmemMax - 1024 - BAR_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
-  static constexpr int O_COL = 0;                   // O of warpgroup w at [128 w, 128 w + D)
+  static constexpr int O_COL = 0;                   // O of warpgroup w at [128 w, 128 w + DV)
   static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
-  static constexpr size_t SMEM = (size_t)Q_BYTES + 2 * (size_t)NS * KV_BYTES + BAR_BYTES + 1024 /*align*/;
+  static constexpr size_t SMEM = (size_t)Q_BYTES + (size_t)NS * (K_BYTES + V_BYTES) + BAR_BYTES + 1024 /*align*/;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
   static_assert(256 + NWG * 1024 <= BAR_BYTES, "barrier region");
-  static_assert(D <= 256, "O must fit below the S buffers");
-  static_assert(NWG == 1 || D <= 128, "two O accumulators must fit below the S buffers");
+  static_assert(DV <= 256, "O must fit below the S buffers");
+  static_assert(NWG == 1 || DV <= 128, "two O accumulators must fit below the S buffers");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
 };
 
@@ -149,13 +158,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int BN = C::BN, NS = C::NS, KCH = C::KCH, NWG = C::NWG;
+  constexpr int BN = C::BN, NS = C::NS, KCH = C::KCH, NWG = C::NWG, DV = C::DV;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sQ = base;
   unsigned char* sK = sQ + C::Q_BYTES;
-  unsigned char* sV = sK + NS * C::KV_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::KV_BYTES);
+  unsigned char* sV = sK + NS * C::K_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::V_BYTES);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* k_empty = k_full + NS;
@@ -171,6 +180,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32;
   const int bh = blockIdx.x;  // b * Hq + h
+  const int zs = blockIdx.z;  // which DV-column slice of O (and V) this CTA computes
   const int b = bh / g.Hq, h = bh - b * g.Hq;
   const int bkv = b * g.Hkv + h / g.G;
   const int qt = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first
@@ -218,20 +228,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint32_t par = ((n / NS) & 1) ^ 1;
         const int j0 = (t_lo + n) * BN;
         if (n >= NS && !mbar_wait(k_empty + st, par, abort_flag)) break;
-        mbar_arrive_expect_tx(k_full + st, C::KV_BYTES);
+        mbar_arrive_expect_tx(k_full + st, C::K_BYTES);
         for (int c = 0; c < KCH; ++c)
-          tma_load_3d(sK + st * C::KV_BYTES + c * BN * 128, &tmK, k_full + st, c * 64, j0, bkv);
+          tma_load_3d(sK + st * C::K_BYTES + c * BN * 128, &tmK, k_full + st, c * 64, j0, bkv);
         if (n >= NS && !mbar_wait(v_empty + st, par, abort_flag)) break;
-        mbar_arrive_expect_tx(v_full + st, C::KV_BYTES);
-        for (int c = 0; c < KCH; ++c)
-          tma_load_3d(sV + st * C::KV_BYTES + c * BN * 128, &tmV, v_full + st, c * 64, j0, bkv);
+        mbar_arrive_expect_tx(v_full + st, C::V_BYTES);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_3d(sV + st * C::V_BYTES + c * BN * 128, &tmV, v_full + st, zs * DV + c * 64, j0, bkv);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (elect_one()) {
       const uint32_t idS = idesc_f16(kBM, BN, 0, 0, 0, 0);   // Q (K-major) x K (K-major)
-      const uint32_t idPV = idesc_f16(kBM, D, 0, 0, 0, 1);   // P (TMEM) x V (MN-major)
+      const uint32_t idPV = idesc_f16(kBM, DV, 0, 0, 0, 1);  // P (TMEM) x V (MN-major)
       const uint32_t qaddr = smem_u32(sQ);
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto issue_pv = [&](int m) -> bool {
@@ -239,7 +249,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (!mbar_wait(p_full + sb, (m >> 1) & 1, abort_flag)) return false;
         if (!mbar_wait(v_full + st, (m / NS) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vaddr = smem_u32(sV + st * C::KV_BYTES);
+        const uint32_t vaddr = smem_u32(sV + st * C::V_BYTES);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bdesc = smem_desc_sw128(vaddr + ks * 2048, BN * 128, 1024);
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int st = n % NS, sb = n & 1;
         if (!mbar_wait(k_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kaddr = smem_u32(sK + st * C::KV_BYTES);
+        const uint32_t kaddr = smem_u32(sK + st * C::K_BYTES);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks & 3) * 32;  // 16 fp16 = 32 bytes along K inside a 128-byte chunk
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // tcgen05.ld/st are warp-collective: the whole warp rescales if any row needs it
       if (__any_sync(0xffffffffu, rescale) && k > 0) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DV / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(tmem + lane_off + o_col + c * 32, rr);
           tmem_wait_ld();
@@ -360,8 +370,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const float inv = 1.f / l_tot;
 #pragma unroll
       for (int w = 0; w < NWG; ++w) f[w] *= inv;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
-      constexpr int CPW = D / 32 / NWG;  // 32-column chunks written per warpgroup
+      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D + zs * DV;
+      constexpr int CPW = DV / 32 / NWG;  // 32-column chunks written per warpgroup
 #pragma unroll
       for (int cc = 0; cc < CPW; ++cc) {
         const int c = wg * CPW + cc;
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
       }
-      if (row_ok && wg == 0) p.lse[(size_t)bh * g.L + i] = (m_tot + log2f(l_tot)) * kLn2;
+      if (row_ok && wg == 0 && zs == 0) p.lse[(size_t)bh * g.L + i] = (m_tot + log2f(l_tot)) * kLn2;
     }
   }
 
@@ -501,7 +511,7 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   cudaError_t e;
   if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, kBM)) != cudaSuccess) return e;
   if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;  // boxes of 64 columns
   auto kern = fwd_tc_kernel<D>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
     return e;
@@ -511,12 +521,12 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   p.lse = lse;
   p.status = status;
   p.n_qtiles = (g.L + kBM - 1) / kBM;
-  dim3 grid(g.B * g.Hq, p.n_qtiles);
+  dim3 grid(g.B * g.Hq, p.n_qtiles, C::NSPLIT);
   kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
-bool fwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
+bool fwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
 cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
                           float* lse, int* status, cudaStream_t s) {
@@ -524,6 +534,7 @@ cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k1
     case 64: return fwd_tc_d<64>(g, q16, k16, v16, o, lse, status, s);
     case 128: return fwd_tc_d<128>(g, q16, k16, v16, o, lse, status, s);
     case 256: return fwd_tc_d<256>(g, q16, k16, v16, o, lse, status, s);
+    case 512: return fwd_tc_d<512>(g, q16, k16, v16, o, lse, status, s);
     default: return cudaErrorInvalidValue;
   }
 }
