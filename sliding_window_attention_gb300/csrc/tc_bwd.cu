@@ -242,23 +242,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) {
       const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major)
       const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (B MN-major)
-      const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV);
+      const uint64_t kdk = smem_desc_sw128(smem_u32(sK), 16, 1024);  // K, K-major (resident)
+      const uint64_t vdk = smem_desc_sw128(smem_u32(sV), 16, 1024);  // V, K-major (resident)
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       auto issue_grad = [&](int m) -> bool {
         const int st = m % NS, sb = m & 1;
         if (!mbar_wait(p_full + sb, (m >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t qaddr = smem_u32(sStage + st * C::STAGE_BYTES);
-        const uint32_t gaddr = qaddr + C::QT_BYTES;
+        const uint64_t qmn = smem_desc_sw128(qaddr, BM * 128, 1024);               // Q, MN-major
+        const uint64_t gmn = smem_desc_sw128(qaddr + C::QT_BYTES, BM * 128, 1024);  // dO, MN-major
 #pragma unroll
         for (int ks = 0; ks < BM / 16; ++ks) {
           const uint32_t acc = (m > 0 || ks > 0) ? 1u : 0u;
           if (C::DO_DV)
-            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + sb * BM + ks * 8,
-                   smem_desc_sw128(gaddr + ks * 2048, BM * 128, 1024), idG, acc);
+            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + sb * BM + ks * 8, desc_add(gmn, ks * 2048), idG, acc);
           if (C::DO_DK)
-            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + sb * BM + ks * 8,
-                   smem_desc_sw128(qaddr + ks * 2048, BM * 128, 1024), idG, acc);
+            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + sb * BM + ks * 8, desc_add(qmn, ks * 2048), idG, acc);
         }
         mma_commit(st_empty + st);
         return true;
@@ -268,16 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(st_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t qaddr = smem_u32(sStage + st * C::STAGE_BYTES);
-        const uint32_t gaddr = qaddr + C::QT_BYTES;
+        const uint64_t qk = smem_desc_sw128(qaddr, 16, 1024);               // Q, K-major
+        const uint64_t gk = smem_desc_sw128(qaddr + C::QT_BYTES, 16, 1024);  // dO, K-major
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks & 3) * 32;
           const uint32_t ck = (ks >> 2) * BNK * 128, cq = (ks >> 2) * BM * 128;
-          mma_ss(tmem + C::S_COL + sb * BM, smem_desc_sw128(kaddr + ck + off, 16, 1024),
-                 smem_desc_sw128(qaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          mma_ss(tmem + C::S_COL + sb * BM, desc_add(kdk, ck + off), desc_add(qk, cq + off), idS, ks > 0 ? 1u : 0u);
           if (C::NEED_V)
-            mma_ss(tmem + C::DP_COL + sb * BM, smem_desc_sw128(vaddr + ck + off, 16, 1024),
-                   smem_desc_sw128(gaddr + cq + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + C::DP_COL + sb * BM, desc_add(vdk, ck + off), desc_add(gk, cq + off), idS,
+                   ks > 0 ? 1u : 0u);
         }
         mma_commit(sdp_full + sb);
         if (n >= 1 && !issue_grad(n - 1)) { ok = false; break; }
@@ -469,17 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_one()) {
       const uint32_t idS = idesc_f16(BMQ, BN, 0, 0, 0, 0);  // Q x K^T, dO x V^T
       const uint32_t idQ = idesc_f16(BMQ, D, 0, 0, 0, 1);   // dS x K (K MN-major)
-      const uint32_t qaddr = smem_u32(sQ), gaddr = smem_u32(sG);
+      const uint64_t qdk = smem_desc_sw128(smem_u32(sQ), 16, 1024);  // Q, K-major (resident)
+      const uint64_t gdk = smem_desc_sw128(smem_u32(sG), 16, 1024);  // dO, K-major (resident)
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto issue_dq = [&](int m) -> bool {
         const int st = m % NS, sb = m & 1;
         if (!mbar_wait(ds_full + sb, (m >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kaddr = smem_u32(sK + st * C::KV_BYTES);
+        const uint64_t kmn = smem_desc_sw128(smem_u32(sK + st * C::KV_BYTES), BN * 128, 1024);  // K, MN-major
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ts(tmem + C::DQ_COL, tmem + C::DP_COL + sb * BN + ks * 8,
-                 smem_desc_sw128(kaddr + ks * 2048, BN * 128, 1024), idQ, (m > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DQ_COL, tmem + C::DP_COL + sb * BN + ks * 8, desc_add(kmn, ks * 2048), idQ,
+                 (m > 0 || ks > 0) ? 1u : 0u);
         mma_commit(kv_empty + st);
         return true;
       };
@@ -487,16 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = n % NS, sb = n & 1;
         if (!mbar_wait(kv_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kaddr = smem_u32(sK + st * C::KV_BYTES);
-        const uint32_t vaddr = smem_u32(sV + st * C::KV_BYTES);
+        const uint64_t kk = smem_desc_sw128(smem_u32(sK + st * C::KV_BYTES), 16, 1024);  // K, K-major
+        const uint64_t vk = smem_desc_sw128(smem_u32(sV + st * C::KV_BYTES), 16, 1024);  // V, K-major
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks & 3) * 32;
           const uint32_t cq = (ks >> 2) * BMQ * 128, ck = (ks >> 2) * BN * 128;
-          mma_ss(tmem + C::S_COL + sb * BN, smem_desc_sw128(qaddr + cq + off, 16, 1024),
-                 smem_desc_sw128(kaddr + ck + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
-          mma_ss(tmem + C::DP_COL + sb * BN, smem_desc_sw128(gaddr + cq + off, 16, 1024),
-                 smem_desc_sw128(vaddr + ck + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          mma_ss(tmem + C::S_COL + sb * BN, desc_add(qdk, cq + off), desc_add(kk, ck + off), idS, ks > 0 ? 1u : 0u);
+          mma_ss(tmem + C::DP_COL + sb * BN, desc_add(gdk, cq + off), desc_add(vk, ck + off), idS, ks > 0 ? 1u : 0u);
         }
         mma_commit(sdp_full + sb);
         if (n >= 1 && !issue_dq(n - 1)) { ok = false; break; }

@@ -242,17 +242,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (elect_one()) {
       const uint32_t idS = idesc_f16(kBM, BN, 0, 0, 0, 0);   // Q (K-major) x K (K-major)
       const uint32_t idPV = idesc_f16(kBM, DV, 0, 0, 0, 1);  // P (TMEM) x V (MN-major)
-      const uint32_t qaddr = smem_u32(sQ);
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto issue_pv = [&](int m) -> bool {
         const int st = m % NS, sb = m & 1;
         if (!mbar_wait(p_full + sb, (m >> 1) & 1, abort_flag)) return false;
         if (!mbar_wait(v_full + st, (m / NS) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vaddr = smem_u32(sV + st * C::V_BYTES);
+        const uint64_t vdesc = smem_desc_sw128(smem_u32(sV + st * C::V_BYTES), BN * 128, 1024);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bdesc = smem_desc_sw128(vaddr + ks * 2048, BN * 128, 1024);
+          const uint64_t bdesc = desc_add(vdesc, ks * 2048);
           mma_ts(tmem + C::O_COL + 128 * (m % NWG), tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV,
                  (m >= NWG || ks > 0) ? 1u : 0u);
         }
@@ -264,12 +264,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const int st = n % NS, sb = n & 1;
         if (!mbar_wait(k_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kaddr = smem_u32(sK + st * C::K_BYTES);
+        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + st * C::K_BYTES), 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks & 3) * 32;  // 16 fp16 = 32 bytes along K inside a 128-byte chunk
-          const uint64_t adesc = smem_desc_sw128(qaddr + (ks >> 2) * kBM * 128 + off, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(kaddr + (ks >> 2) * BN * 128 + off, 16, 1024);
+          const uint64_t adesc = desc_add(qdesc, (ks >> 2) * kBM * 128 + off);
+          const uint64_t bdesc = desc_add(kdesc, (ks >> 2) * BN * 128 + off);
           mma_ss(tmem + C::S_COL + sb * BN, adesc, bdesc, idS, ks > 0 ? 1u : 0u);
         }
         mma_commit(s_full + sb);

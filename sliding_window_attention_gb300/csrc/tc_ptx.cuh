@@ -195,6 +195,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same descriptor advanced by byte_off bytes: only the start-address
+// field (bits 0-13, address >> 4) changes, and shared addresses stay below
+// 256 KB, so the low word never carries into the next field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 // a_bf16/b_bf16: operand type (0 = fp16, 1 = bf16); a_mn/b_mn: 1 = MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_bf16, int b_bf16, int a_mn, int b_mn) {
