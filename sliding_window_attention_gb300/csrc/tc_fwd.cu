@@ -67,12 +67,16 @@ struct FwdCfg {
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
   static constexpr int O_COL = 0;                   // O of warpgroup w at [128 w, 128 w + DV)
   static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
+  // row sums l = P . 1 accumulated by the tensor core (16 identical columns)
+  static constexpr int L_COL = (DV <= 128) ? 128 : S_COL + 2 * BN;
   static constexpr size_t SMEM = (size_t)Q_BYTES + (size_t)NS * (K_BYTES + V_BYTES) + BAR_BYTES + 1024 /*align*/;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
   static_assert(256 + NWG * 1024 <= BAR_BYTES, "barrier region");
   static_assert(DV <= 256, "O must fit below the S buffers");
   static_assert(NWG == 1 || DV <= 128, "two O accumulators must fit below the S buffers");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
+  static_assert(NWG == 1, "one softmax warpgroup (the row-sum accumulator is per warpgroup)");
+  static_assert(L_COL + 16 <= 512 && (L_COL >= S_COL + 2 * BN || L_COL + 16 <= S_COL), "TMEM columns for l");
 };
 
 struct FwdParams {
@@ -123,11 +127,10 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
 }
 
 // Pass 2: P = 2^(sl2 * s - m) for the row, rounded to fp16, packed two per
-// 32-bit TMEM column at p_taddr; returns the fp32 row sum.
+// 32-bit TMEM column at p_taddr.  (The row sum is taken by the tensor core.)
 template <int BN, bool FULL>
-__device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, int clo, int chi,
+__device__ __forceinline__ void softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, int clo, int chi,
                                                 uint32_t p_taddr) {
-  float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t pk[16];
@@ -144,13 +147,11 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float 
         p0 = fast_exp2(x0 - m_use);
         p1 = fast_exp2(x1 - m_use);
       }
-      ps[(e >> 1) & 3] += p0 + p1;
       const __half2 hp = __floats2half2_rn(p0, p1);
       pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
     }
     tmem_st16(p_taddr + c * 16, pk);
   }
-  return (ps[0] + ps[1]) + (ps[2] + ps[3]);
 }
 
 template <int D>
@@ -176,6 +177,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + NWG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* ml_x = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(bars) + 256);  // [NWG][128] (m, l)
+  // 16 x 16 block of fp16 ones (B operand of the row-sum MMA), no swizzle
+  uint32_t* ones = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(bars) + 1536);
 
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32;
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int t_lo = jlo / BN, t_hi = ihi / BN;
   const int nt = t_hi - t_lo + 1;
 
+  if (threadIdx.x < 128) ones[threadIdx.x] = 0x3C003C00u;  // two fp16 1.0 per word, 512 bytes
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < NS; ++s) {
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // ones[] is read by the tensor core
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -242,6 +247,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (elect_one()) {
       const uint32_t idS = idesc_f16(kBM, BN, 0, 0, 0, 0);   // Q (K-major) x K (K-major)
       const uint32_t idPV = idesc_f16(kBM, DV, 0, 0, 0, 1);  // P (TMEM) x V (MN-major)
+      const uint32_t idL = idesc_f16(kBM, 16, 0, 0, 0, 0);   // P (TMEM) x ones (K-major)
+      const uint64_t ones_desc = smem_desc_noswz(smem_u32(ones), 128, 256);
       const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto issue_pv = [&](int m) -> bool {
@@ -256,6 +263,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           mma_ts(tmem + C::O_COL + 128 * (m % NWG), tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV,
                  (m >= NWG || ks > 0) ? 1u : 0u);
         }
+        // l += P . 1: every 16 x 16 step reads the same block of ones
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts(tmem + C::L_COL, tmem + C::S_COL + sb * BN + ks * 8, ones_desc, idL, (m >= NWG || ks > 0) ? 1u : 0u);
         mma_commit(o_done + (m % NWG));
         mma_commit(v_empty + st);
         return true;
@@ -317,9 +328,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN;
-      const float psum = full ? softmax_tile_p<BN, true>(sr, sl2, m_use, clo, chi, p_taddr)
-                              : softmax_tile_p<BN, false>(sr, sl2, m_use, clo, chi, p_taddr);
-      l_run = l_run * alpha + psum;
+      if (full) softmax_tile_p<BN, true>(sr, sl2, m_use, clo, chi, p_taddr);
+      else softmax_tile_p<BN, false>(sr, sl2, m_use, clo, chi, p_taddr);
       // Wait for PV(n-1) at every tile, not only when rescaling: this thread then
       // has observed every earlier PV completion, so the o_done phase can be at
       // most one ahead of the parity asked for (no aliasing of phase n-3 with
@@ -339,6 +349,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
           tmem_st32(tmem + lane_off + o_col + c * 32, rr);
         }
+        uint32_t lr[16];
+        tmem_ld16(tmem + lane_off + C::L_COL, lr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) lr[e] = __float_as_uint(__uint_as_float(lr[e]) * alpha);
+        tmem_st16(tmem + lane_off + C::L_COL, lr);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -348,6 +364,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if (ok && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done + wg, (k - 1) & 1, abort_flag));
     // merge the per-warpgroup softmax states: m = max(m_w), l = sum_w l_w 2^(m_w - m),
     // O = sum_w O_w 2^(m_w - m) / l.  Each warpgroup writes half of the columns.
+    {
+      uint32_t lr[16];
+      tmem_ld16(tmem + lane_off + C::L_COL, lr);  // warp-collective
+      tmem_wait_ld();
+      l_run = (k > 0) ? __uint_as_float(lr[0]) : 0.f;
+    }
     ml_x[wg * 128 + r] = make_float2(m_run, l_run);
     tc_fence_before();
     if (NWG == 2) asm volatile("bar.sync 1, 256;" ::: "memory");
