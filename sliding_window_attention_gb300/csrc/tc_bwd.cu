@@ -18,8 +18,10 @@
 //
 // Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner and the
 // single-thread MMA issuer, warps 2..5 and 6..9 two elementwise
-// softmax-gradient warpgroups (one TMEM lane, i.e. one row, per thread) that
-// take alternate steps, so one works while the other waits for its MMAs.
+// softmax-gradient warpgroups (one TMEM lane, i.e. one row, per thread).  At
+// head dim <= 128 both warpgroups work on every step, each on half of its
+// columns, which halves the latency of the S -> P -> dV/dK chain; at head dim
+// 256 (32-column steps) they take alternate steps.
 // Every mbarrier wait is bounded (see tc_ptx.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -124,6 +126,11 @@ template <int D, int MODE>
 struct KvCfg {
   static constexpr int BNK = 128;                  // key rows per CTA (MMA M)
   static constexpr int BM = (D <= 128) ? 64 : 32;  // query rows per step
+  // SPLIT: both elementwise warpgroups take every step, 32 query columns each
+  // (halves the step's latency on the S -> P -> dV/dK chain); otherwise they
+  // take alternate steps
+  static constexpr bool SPLIT = BM == 64;
+  static constexpr int CW = SPLIT ? BM / 2 : BM;  // query columns per warpgroup per step
   static constexpr bool NEED_V = MODE != kModeDV;  // dP^T = V dO^T
   static constexpr bool DO_DV = MODE != kModeDK;
   static constexpr bool DO_DK = MODE != kModeDV;
@@ -175,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sdp_full = st_empty + NS;      // [2]
   uint64_t* p_full = sdp_full + 2;         // [2]
   uint64_t* acc_done = p_full + 2;         // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* ldd = acc_done + 1;            // [2] both warpgroups finished reading a buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ldd + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const Geom& g = p.g;
@@ -197,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sdp_full + s, 1);
-      mbar_init(p_full + s, 128);
+      mbar_init(p_full + s, C::SPLIT ? 256 : 128);
+      mbar_init(ldd + s, 256);
     }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
@@ -293,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
     bool ok = true;
-    for (int n = wg; n < N; n += 2) {
+    constexpr int CW = C::CW;
+    const int cw0 = C::SPLIT ? wg * CW : 0;
+    for (int n = C::SPLIT ? 0 : wg; n < N; n += C::SPLIT ? 1 : 2) {
       const int st = n % NS, sb = n & 1;
       const int i0 = (t_lo + n % ntq) * BM;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
@@ -304,25 +315,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
       const int clo = max(0, j - i0);
       const int chi = min(min(BM - 1, g.L - 1 - i0), g.W > 0 ? j + g.W - 1 - i0 : BM - 1);
-      // all S^T / dP^T columns of this step with one TMEM wait
-      uint32_t sv[BM], dv[BM];
+      // this warpgroup's S^T / dP^T columns with one TMEM wait
+      uint32_t sv[CW], dv[CW];
 #pragma unroll
-      for (int c = 0; c < BM / 32; ++c) {
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+      for (int c = 0; c < CW / 32; ++c) {
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + cw0 + c * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
         if (C::NEED_V)
-          tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+          tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + cw0 + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
       }
       tmem_wait_ld();
+      if (C::SPLIT) {
+        // packed fp16 results land on columns the other warpgroup reads: both
+        // finish reading this buffer first (bounded wait, not bar.sync)
+        mbar_arrive(ldd + sb);
+        if (!__all_sync(0xffffffffu, mbar_wait(ldd + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      }
 #pragma unroll
-      for (int c = 0; c < BM / 32; ++c) {
+      for (int c = 0; c < CW / 32; ++c) {
         const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
+        const int cb = cw0 + c * 32;  // tile-local query column of this chunk
         uint32_t pp[16], dd[16];
-        if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
-        else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, c * 32, clo, chi, pp, dd);
-        // P^T / dS^T (fp16, two per column) overwrite columns already consumed
-        if (C::DO_DV) tmem_st16(tmem + lane_off + C::S_COL + sb * BM + c * 16, pp);
-        if (C::DO_DK) tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + c * 16, dd);
+        if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, cb, clo, chi, pp, dd);
+        else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, cb, clo, chi, pp, dd);
+        // P^T / dS^T as fp16 pairs: query columns 2t, 2t+1 -> TMEM column t
+        if (C::DO_DV) tmem_st16(tmem + lane_off + C::S_COL + sb * BM + cb / 2, pp);
+        if (C::DO_DK) tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + cb / 2, dd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -373,6 +393,8 @@ template <int D>
 struct DqCfg {
   static constexpr int BMQ = 128;                  // query rows per CTA (MMA M)
   static constexpr int BN = (D <= 128) ? 64 : 32;  // key rows per step
+  static constexpr bool SPLIT = BN == 64;          // see KvCfg
+  static constexpr int CW = SPLIT ? BN / 2 : BN;   // key columns per warpgroup per step
   static constexpr int KCH = D / 64;
   static constexpr int QT_BYTES = BMQ * D * 2;  // Q (or dO) tile
   static constexpr int KV_BYTES = BN * D * 2;   // K (or V) tile
@@ -405,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sdp_full = kv_empty + NS;   // [2]
   uint64_t* ds_full = sdp_full + 2;     // [2]
   uint64_t* acc_done = ds_full + 2;     // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* ldd = acc_done + 1;         // [2] both warpgroups finished reading a buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ldd + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const Geom& g = p.g;
@@ -428,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sdp_full + s, 1);
-      mbar_init(ds_full + s, 128);
+      mbar_init(ds_full + s, C::SPLIT ? 256 : 128);
+      mbar_init(ldd + s, 256);
     }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
@@ -510,7 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = g.scale * kLog2e;
     const float2 rs = (i < g.L) ? p.stats[(size_t)bh * p.Lpad + i] : make_float2(0.f, 0.f);
     bool ok = true;
-    for (int n = wg; n < nt; n += 2) {
+    constexpr int CW = C::CW;
+    const int cw0 = C::SPLIT ? wg * CW : 0;
+    for (int n = C::SPLIT ? 0 : wg; n < nt; n += C::SPLIT ? 1 : 2) {
       const int sb = n & 1;
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
@@ -519,21 +545,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key columns c of this tile visible to row i: j0 + c in [i - W + 1, i]
       const int clo = g.W > 0 ? max(0, i - g.W + 1 - j0) : 0;
       const int chi = min(BN - 1, i - j0);
-      uint32_t sv[BN], dv[BN];
+      uint32_t sv[CW], dv[CW];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+      for (int c = 0; c < CW / 32; ++c) {
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + cw0 + c * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + cw0 + c * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
       }
       tmem_wait_ld();
+      if (C::SPLIT) {  // see the dK/dV kernel
+        mbar_arrive(ldd + sb);
+        if (!__all_sync(0xffffffffu, mbar_wait(ldd + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      }
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < CW / 32; ++c) {
         const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
+        const int cb = cw0 + c * 32;
         uint32_t dd[16];
-        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
-        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, c * 32, clo, chi, dd);
-        tmem_st16(tmem + lane_off + C::DP_COL + sb * BN + c * 16, dd);
+        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
+        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
+        tmem_st16(tmem + lane_off + C::DP_COL + sb * BN + cb / 2, dd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -546,6 +579,249 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* row = p.out0 + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
 #pragma unroll
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + C::DQ_COL + c * 32, a);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(row + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * g.scale, __uint_as_float(a[e + 1]) * g.scale,
+                            __uint_as_float(a[e + 2]) * g.scale, __uint_as_float(a[e + 3]) * g.scale);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dQ for head dim <= 128 with 128-row key steps, so every MMA has N >= 128
+// (tcgen05.mma with N <= 64 costs a fixed ~50 cycles per instruction and runs
+// at ~60% of the tensor rate; N >= 128 runs at the full rate).
+//
+// TMEM: dQ [0, D), two S buffers [128, 256) and [256, 384), one dP buffer
+// [384, 512).  Each warpgroup handles 64 of the 128 key columns of a step.
+// dS (fp16 pairs) is written back over the S buffer it came from, so the dP
+// buffer is free as soon as both warpgroups have read it: dP(n+1) is issued
+// while step n's elementwise work is still running.  S(n+2) reuses S(n)'s
+// buffer and is issued right after dQ(n), which reads dS(n) from it.
+// K tiles (used by S(n) and dQ(n)) and V tiles (used only by dP(n)) travel in
+// separate TMA rings so a V tile is released early.
+template <int D>
+struct Dq128Cfg {
+  static constexpr int BMQ = 128, BN = 128, CW = 64;  // CW: key columns per warpgroup
+  static constexpr int KCH = D / 64;
+  static constexpr int QT_BYTES = BMQ * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int NK = (D <= 64) ? 4 : 3;   // K ring depth
+  static constexpr int NV = (D <= 64) ? 4 : 2;   // V ring depth
+  static constexpr int DQ_COL = 0, S_COL = 128, DP_COL = 384;
+  static constexpr size_t SMEM = 2 * (size_t)QT_BYTES + (size_t)(NK + NV) * KV_BYTES + 1024 + 1024;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
+  static_assert(D <= 128, "dQ below the S buffers");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                    const BwdParams p) {
+  using C = Dq128Cfg<D>;
+  constexpr int BMQ = C::BMQ, BN = C::BN, NK = C::NK, NV = C::NV, KCH = C::KCH, CW = C::CW;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = base;
+  unsigned char* sG = sQ + C::QT_BYTES;
+  unsigned char* sK = sG + C::QT_BYTES;
+  unsigned char* sV = sK + NK * C::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NV * C::KV_BYTES);
+  uint64_t* q_full = bars;              // [1]
+  uint64_t* k_full = q_full + 1;        // [NK]
+  uint64_t* k_empty = k_full + NK;      // [NK]
+  uint64_t* v_full = k_empty + NK;      // [NV]
+  uint64_t* v_empty = v_full + NV;      // [NV]
+  uint64_t* sdp_full = v_empty + NV;    // [2] S(n) and dP(n) of step n are in TMEM
+  uint64_t* ds_full = sdp_full + 2;     // [2] dS(n) written over S buffer n % 2
+  uint64_t* ldd = ds_full + 2;          // [2] both warpgroups have read step n (frees the dP buffer)
+  uint64_t* acc_done = ldd + 2;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bh = blockIdx.x;
+  const int b = bh / g.Hq, h = bh - b * g.Hq;
+  const int bkv = b * g.Hkv + h / g.G;
+  const int qt = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
+  const int i0 = qt * BMQ;
+  const int ihi = min(i0 + BMQ, g.L) - 1;
+  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
+  const int t_lo = jlo / BN, t_hi = ihi / BN;
+  const int nt = t_hi - t_lo + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sdp_full + s, 1);
+      mbar_init(ds_full + s, 256);
+      mbar_init(ldd + s, 256);  // both warpgroups arrive; the MMA thread only waits
+    }
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(q_full, 2 * C::QT_BYTES);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_3d(sQ + c * BMQ * 128, &tmQ, q_full, c * 64, i0, bh);
+        tma_load_3d(sG + c * BMQ * 128, &tmG, q_full, c * 64, i0, bh);
+      }
+      // K and V of each step, each ring refilled as soon as its slot is released
+      for (int n = 0; n < nt; ++n) {
+        const int j0 = (t_lo + n) * BN;
+        const int sk = n % NK, sv = n % NV;
+        if (n >= NK && !mbar_wait(k_empty + sk, ((n / NK) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(k_full + sk, C::KV_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sK + sk * C::KV_BYTES + c * BN * 128, &tmK, k_full + sk, c * 64, j0, bkv);
+        if (n >= NV && !mbar_wait(v_empty + sv, ((n / NV) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(v_full + sv, C::KV_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sV + sv * C::KV_BYTES + c * BN * 128, &tmV, v_full + sv, c * 64, j0, bkv);
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BMQ, BN, 0, 0, 0, 0);  // Q x K^T, dO x V^T (both K-major), N = 128
+      const uint32_t idQ = idesc_f16(BMQ, D, 0, 0, 0, 1);   // dS (TMEM) x K (MN-major)
+      const uint64_t qdk = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t gdk = smem_desc_sw128(smem_u32(sG), 16, 1024);
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      auto issue_s = [&](int n) -> bool {  // S(n) into buffer n % 2
+        if (!mbar_wait(k_full + n % NK, (n / NK) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t kk = smem_desc_sw128(smem_u32(sK + (n % NK) * C::KV_BYTES), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;
+          mma_ss(tmem + C::S_COL + (n & 1) * BN, desc_add(qdk, (ks >> 2) * BMQ * 128 + off),
+                 desc_add(kk, (ks >> 2) * BN * 128 + off), idS, ks > 0 ? 1u : 0u);
+        }
+        return true;
+      };
+      auto issue_dp = [&](int n) -> bool {  // dP(n) into the dP buffer; completes step n's inputs
+        if (!mbar_wait(v_full + n % NV, (n / NV) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t vk = smem_desc_sw128(smem_u32(sV + (n % NV) * C::KV_BYTES), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;
+          mma_ss(tmem + C::DP_COL, desc_add(gdk, (ks >> 2) * BMQ * 128 + off),
+                 desc_add(vk, (ks >> 2) * BN * 128 + off), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(v_empty + n % NV);
+        mma_commit(sdp_full + (n & 1));  // covers S(n), issued earlier
+        return true;
+      };
+      if (ok) ok = issue_s(0) && issue_dp(0);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int n = 0; ok && n < nt; ++n) {
+        if (n + 1 < nt) {
+          // the dP buffer is free once both warpgroups have read dP(n)
+          if (!mbar_wait(ldd + (n & 1), (n >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!issue_dp(n + 1)) { ok = false; break; }
+        }
+        if (!mbar_wait(ds_full + (n & 1), (n >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kmn = smem_desc_sw128(smem_u32(sK + (n % NK) * C::KV_BYTES), BN * 128, 1024);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + (n & 1) * BN + ks * 8, desc_add(kmn, ks * 2048), idQ,
+                 (n > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(k_empty + n % NK);
+        if (n + 2 < nt && !issue_s(n + 2)) { ok = false; break; }
+      }
+      if (ok) mma_commit(acc_done);
+    }
+  } else {
+    const int wg = (warp - 2) >> 2;  // warps 2-5 / 6-9; warp % 4 fixes the TMEM lane quarter
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int i = i0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    const float2 rs = (i < g.L) ? p.stats[(size_t)bh * p.Lpad + i] : make_float2(0.f, 0.f);
+    const int cw0 = wg * CW;
+    bool ok = true;
+    for (int n = 0; n < nt; ++n) {
+      const int sb = n & 1;
+      const int j0 = (t_lo + n) * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + BMQ - 1 - j0 < g.W);
+      const int clo = g.W > 0 ? max(0, i - g.W + 1 - j0) : 0;  // visible key columns [clo, chi]
+      const int chi = min(BN - 1, i - j0);
+      uint32_t sv[CW], dv[CW];
+#pragma unroll
+      for (int c = 0; c < CW / 32; ++c) {
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + cw0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+        tmem_ld32(tmem + lane_off + C::DP_COL + cw0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(ldd + sb);  // also releases the dP buffer to the MMA thread
+      // the other warpgroup's packed dS lands on columns this one reads: wait for both
+      if (!__all_sync(0xffffffffu, mbar_wait(ldd + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+#pragma unroll
+      for (int c = 0; c < CW / 32; ++c) {
+        const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
+        const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
+        const int cb = cw0 + c * 32;
+        uint32_t dd[16];
+        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
+        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
+        tmem_st16(tmem + lane_off + C::S_COL + sb * BN + cb / 2, dd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full + sb);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
+      tc_fence_after();
+      const bool row_ok = i < g.L;
+      float* row = p.out0 + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+#pragma unroll
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {  // each warpgroup writes half the columns
         uint32_t a[32];
         tmem_ld32(tmem + lane_off + C::DQ_COL + c * 32, a);
         tmem_wait_ld();
@@ -629,6 +905,21 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       if ((e = run(std::integral_constant<int, kModeDV>{})) != cudaSuccess) return e;
       return run(std::integral_constant<int, kModeDK>{});
     }
+  } else if constexpr (D <= 128) {
+    using C = Dq128Cfg<D>;
+    CUtensorMap tq, tk, tv, tg;
+    if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+    auto kern = dq128_tc_kernel<D>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
+      return e;
+    p.out0 = dq;
+    p.out1 = nullptr;
+    p.n_tiles = (g.L + C::BMQ - 1) / C::BMQ;
+    dim3 grid(g.B * g.Hq, p.n_tiles);
+    kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
   } else {
     using C = DqCfg<D>;
     CUtensorMap tq, tk, tv, tg;
