@@ -941,7 +941,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
 
 }  // namespace
 
-bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
+bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
 int bwd_stats_lpad(int L) { return (L + 127) / 128 * 128; }
 
@@ -960,6 +960,7 @@ cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_
     case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
     case 128: return bwd_tc_d<128>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
     case 256: return bwd_tc_d<256>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
+    case 512: return launch_bwd_dkdv_tc512(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -971,6 +972,7 @@ cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t*
     case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
     case 128: return bwd_tc_d<128>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
     case 256: return bwd_tc_d<256>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);
+    case 512: return launch_bwd_dq_tc512(g, q16, k16, v16, g16, stats, Lpad, dq, status, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -269,5 +269,121 @@ __device__ __forceinline__ uint32_t elect_one() {
   return pred;
 }
 
+// ---- thread-block clusters and distributed shared memory ------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`
+// (a shared::cluster address).
+__device__ __forceinline__ uint32_t mapa(uint32_t cta_addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(cta_addr), "r"(rank));
+  return d;
+}
+
+// Whole-cluster barrier (every thread of every CTA), release / acquire.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait with cluster-scope acquire: data written by other CTAs of the
+// cluster before their release-arrive is visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Raise the abort flag in every CTA of the cluster (the flag sits at the same
+// shared offset in each CTA).
+__device__ __forceinline__ void cluster_abort(volatile int* abort, uint32_t nranks) {
+  const uint32_t a = smem_u32(const_cast<int*>(abort));
+  for (uint32_t r = 0; r < nranks; ++r)
+    asm volatile("st.volatile.shared::cluster.u32 [%0], %1;" ::"r"(mapa(a, r)), "r"(1u) : "memory");
+}
+
+// Bounded cluster-aware wait: gives up when this CTA's abort flag is raised
+// (by any CTA of the cluster) or after kWaitLimitCycles, in which case it
+// raises the flag in the whole cluster.
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t nranks) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      cluster_abort(abort, nranks);
+      return false;
+    }
+  }
+}
+
+// Wait for copies already in flight to land, ignoring the abort flag (used
+// only while unwinding, so that no copy writes into a CTA that has exited).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cl(bar, parity))
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  return true;
+}
+
+// 16 bytes from another CTA's shared memory.
+__device__ __forceinline__ void ld_dsmem_v4(uint32_t cluster_addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                            uint32_t& d) {
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(cluster_addr)
+               : "memory");
+}
+
+// 16 bytes into another CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Orders this thread's generic-proxy writes to shared memory anywhere in the
+// cluster before later async-proxy reads of it (tensor-core operand fetches
+// by the CTA that owns the memory, after it acquires the arrival that follows).
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_smem_v4(uint32_t cta_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cta_addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to later
+// async-proxy reads of this CTA's shared memory (bulk copies, MMA operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
+// another CTA's, completing `bytes` of transaction count on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                 uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
+
 }  // namespace tc
 }  // namespace swa
