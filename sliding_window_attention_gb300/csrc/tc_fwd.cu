@@ -6,11 +6,17 @@
 // recomputes S over the full head dim and accumulates its half.  Warp roles:
 //   warp 0      TMA producer: Q once, then K and V tiles through an NS-deep ring
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warps 4..7  softmax: thread r owns query row i0 + r (TMEM lane r); reads its
-//               S row from TMEM, applies the band mask on edge tiles, keeps the
-//               running max / sum, writes P (fp16) back into the S columns for
-//               the TS-form PV MMA, rescales O when the max grows, and writes
-//               O / l and lse at the end.
+//   warps 2..   softmax: thread r of a warpgroup owns query row i0 + r (TMEM
+//               lane r); reads its S row from TMEM, applies the band mask on
+//               edge tiles, keeps the running max / sum, writes P (fp16) back
+//               into the S columns for the TS-form PV MMA, rescales O when the
+//               max grows, and writes O / l and lse at the end.  At head dim
+//               <= 128 two warpgroups share every tile, 64 columns each (the
+//               row max is combined through shared memory, the row sums are
+//               kept per warpgroup in registers), which halves the softmax
+//               latency that separates S(n) from PV(n); at larger head dims
+//               one warpgroup takes whole tiles and the tensor core sums P
+//               against a block of ones.
 // The key tiles visited are exactly those that intersect the query tile's
 // band ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself",
 // "What I changed, in plain terms" item 3); inside edge tiles P is zeroed
@@ -54,14 +60,20 @@ struct FwdCfg {
   // must fit in TMEM; the two halves each recompute S over the full D)
   static constexpr int DV = (D <= 256) ? D : 256;
   static constexpr int NSPLIT = D / DV;
-  static constexpr int NWG = 1;                     // softmax warpgroups (key-tile parity split)
-  static constexpr int THREADS = 128 + 128 * NWG;
+  static constexpr int NWG = 1;                      // O accumulators
+  static constexpr bool SPLIT = (D <= 128);          // two softmax warpgroups share each tile's columns
+  static constexpr int THREADS = 64 + 128 * (SPLIT ? 2 : 1);  // warp 0 TMA, warp 1 MMA, warps 2.. softmax
   static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks of a Q / K row
   static constexpr int VCH = DV / 64;               // chunks of the V columns this CTA uses
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int K_BYTES = BN * D * 2;
   static constexpr int V_BYTES = BN * DV * 2;
-  static constexpr int BAR_BYTES = 2048;            // mbarriers (256 B) + (m, l) exchange (NWG x 1 KB)
+  // mbarriers (512 B), (m, l) exchange ([2][128] float2), row-max exchange
+  // ([2 parity][2 warpgroups][128] float), block of ones (512 B)
+  static constexpr int XCH_OFF = 512;
+  static constexpr int XM_OFF = XCH_OFF + (SPLIT ? 2048 : 1024);
+  static constexpr int ONES_OFF = XM_OFF + (SPLIT ? 2048 : 0);
+  static constexpr int BAR_BYTES = ONES_OFF + 512;
   // as many K/V stages as shared memory holds (TMA latency hiding), 2..8
   static constexpr int NS_FIT = (kSmemMax - 1024 - BAR_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
@@ -71,12 +83,12 @@ struct FwdCfg {
   static constexpr int L_COL = (DV <= 128) ? 128 : S_COL + 2 * BN;
   static constexpr size_t SMEM = (size_t)Q_BYTES + (size_t)NS * (K_BYTES + V_BYTES) + BAR_BYTES + 1024 /*align*/;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(256 + NWG * 1024 <= BAR_BYTES, "barrier region");
   static_assert(DV <= 256, "O must fit below the S buffers");
   static_assert(NWG == 1 || DV <= 128, "two O accumulators must fit below the S buffers");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
-  static_assert(NWG == 1, "one softmax warpgroup (the row-sum accumulator is per warpgroup)");
-  static_assert(L_COL + 16 <= 512 && (L_COL >= S_COL + 2 * BN || L_COL + 16 <= S_COL), "TMEM columns for l");
+  static_assert(SPLIT || (L_COL + 16 <= 512 && (L_COL >= S_COL + 2 * BN || L_COL + 16 <= S_COL)),
+                "TMEM columns for l");
+  static_assert(!SPLIT || BN == 128, "column split assumes 128-key tiles");
 };
 
 struct FwdParams {
@@ -127,10 +139,12 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
 }
 
 // Pass 2: P = 2^(sl2 * s - m) for the row, rounded to fp16, packed two per
-// 32-bit TMEM column at p_taddr.  (The row sum is taken by the tensor core.)
-template <int BN, bool FULL>
-__device__ __forceinline__ void softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, int clo, int chi,
-                                                uint32_t p_taddr) {
+// 32-bit TMEM column at p_taddr.  SUM: also returns the row sum of P (fp32);
+// otherwise the tensor core takes it.
+template <int BN, bool FULL, bool SUM>
+__device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, int clo, int chi,
+                                                 uint32_t p_taddr) {
+  float s0 = 0.f, s1 = 0.f;
 #pragma unroll
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t pk[16];
@@ -147,11 +161,16 @@ __device__ __forceinline__ void softmax_tile_p(const uint32_t (&sr)[BN], float s
         p0 = fast_exp2(x0 - m_use);
         p1 = fast_exp2(x1 - m_use);
       }
+      if (SUM) {
+        s0 += p0;
+        s1 += p1;
+      }
       const __half2 hp = __floats2half2_rn(p0, p1);
       pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
     }
     tmem_st16(p_taddr + c * 16, pk);
   }
+  return s0 + s1;
 }
 
 template <int D>
@@ -174,11 +193,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint64_t* s_full = v_empty + NS;  // [2]
   uint64_t* p_full = s_full + 2;    // [2]
   uint64_t* o_done = p_full + 2;    // [NWG]: PV into O of warpgroup w complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + NWG);
+  uint64_t* mx_bar = o_done + NWG;  // [2]: both warpgroups posted their partial row max (split mode)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mx_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float2* ml_x = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(bars) + 256);  // [NWG][128] (m, l)
+  float2* ml_x = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(bars) + C::XCH_OFF);  // [2][128] (m, l)
+  float* xm = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bars) + C::XM_OFF);  // [2][2][128]
   // 16 x 16 block of fp16 ones (B operand of the row-sum MMA), no swizzle
-  uint32_t* ones = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(bars) + 1536);
+  uint32_t* ones = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(bars) + C::ONES_OFF);
 
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32;
@@ -204,9 +225,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + s, 1);
-      mbar_init(p_full + s, 128);
+      mbar_init(p_full + s, C::SPLIT ? 256 : 128);
     }
     for (int w = 0; w < NWG; ++w) mbar_init(o_done + w, 1);
+    for (int s = 0; s < 2; ++s) mbar_init(mx_bar + s, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -264,9 +286,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                  (m >= NWG || ks > 0) ? 1u : 0u);
         }
         // l += P . 1: every 16 x 16 step reads the same block of ones
+        if constexpr (!C::SPLIT) {
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ts(tmem + C::L_COL, tmem + C::S_COL + sb * BN + ks * 8, ones_desc, idL, (m >= NWG || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < BN / 16; ++ks)
+            mma_ts(tmem + C::L_COL, tmem + C::S_COL + sb * BN + ks * 8, ones_desc, idL, (m >= NWG || ks > 0) ? 1u : 0u);
+        }
         mma_commit(o_done + (m % NWG));
         mma_commit(v_empty + st);
         return true;
@@ -289,9 +313,105 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       if (ok) issue_pv(nt - 1);
     }
-  } else if (warp >= 4) {
+  } else if (C::SPLIT && warp >= 2) {
+    // ---------------- softmax, two warpgroups per tile (64 columns each) ----------------
+    constexpr int HC = BN / 2;
+    const int wg = (warp - 2) >> 2;
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int i = i0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int cb0 = wg * HC;
+    const float sl2 = g.scale * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int n = 0; n < nt; ++n) {
+      const int sb = n & 1;
+      const int j0 = (t_lo + n) * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + kBM - 1 - j0 < g.W);
+      uint32_t sr[HC];
+#pragma unroll
+      for (int c = 0; c < HC / 32; ++c)
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + cb0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+      tmem_wait_ld();
+      // visible key columns of this row, relative to this warpgroup's half
+      const int clo = ((g.W > 0) ? max(0, i - g.W + 1 - j0) : 0) - cb0;
+      const int chi = min(BN - 1, i - j0) - cb0;
+      const float pmax = full ? softmax_tile_max<HC, true>(sr, sl2, clo, chi)
+                              : softmax_tile_max<HC, false>(sr, sl2, clo, chi);
+      // combine the two halves' maxima; after this barrier both warpgroups have
+      // also read their S columns, so packed P may overwrite them
+      xm[(sb * 2 + wg) * 128 + r] = pmax;
+      mbar_arrive(mx_bar + sb);
+      if (!__all_sync(0xffffffffu, mbar_wait(mx_bar + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      const float tmax = fmaxf(pmax, xm[(sb * 2 + (wg ^ 1)) * 128 + r]);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (tmax > m_run + kRescaleLog2) {
+        if (m_run != -INFINITY) {
+          alpha = fast_exp2(m_run - tmax);
+          rescale = true;
+        }
+        m_run = tmax;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN + cb0 / 2;
+      const float tsum = full ? softmax_tile_p<HC, true, true>(sr, sl2, m_use, clo, chi, p_taddr)
+                              : softmax_tile_p<HC, false, true>(sr, sl2, m_use, clo, chi, p_taddr);
+      l_run = l_run * alpha + tsum;
+      // PV(n - 1) must be complete before O is rescaled (and is waited for at
+      // every tile, so the o_done phase never runs more than one ahead)
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale) && n > 0) {
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c) {  // this warpgroup's half of the O columns
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + C::O_COL + wg * (DV / 2) + c * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st32(tmem + lane_off + C::O_COL + wg * (DV / 2) + c * 32, rr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + sb);
+    }
+    if (ok && nt > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nt - 1) & 1, abort_flag));
+    // row sum = the two warpgroups' partial sums (same running max)
+    ml_x[wg * 128 + r] = make_float2(m_run, l_run);
+    tc_fence_before();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    tc_fence_after();
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    if (ok) {
+      const float l_tot = ml_x[r].y + ml_x[128 + r].y;
+      const bool row_ok = i < g.L;
+      const float inv = 1.f / l_tot;
+      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D + zs * DV;
+#pragma unroll
+      for (int cc = 0; cc < DV / 64; ++cc) {
+        const int c = wg * (DV / 64) + cc;
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, acc);
+        tmem_wait_ld();  // warp-collective: every lane loads, only valid rows store
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                make_float4(__uint_as_float(acc[e]) * inv, __uint_as_float(acc[e + 1]) * inv,
+                            __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
+        }
+      }
+      if (row_ok && wg == 0 && zs == 0) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
+    }
+  } else if (warp >= 2) {
     // ---------------- softmax / correction / epilogue ----------------
-    const int wg = (warp - 4) >> 2;  // takes key tiles n with n % NWG == wg, into its own O
+    const int wg = (warp - 2) >> 2;  // takes key tiles n with n % NWG == wg, into its own O
     const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -328,8 +448,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN;
-      if (full) softmax_tile_p<BN, true>(sr, sl2, m_use, clo, chi, p_taddr);
-      else softmax_tile_p<BN, false>(sr, sl2, m_use, clo, chi, p_taddr);
+      if (full) softmax_tile_p<BN, true, false>(sr, sl2, m_use, clo, chi, p_taddr);
+      else softmax_tile_p<BN, false, false>(sr, sl2, m_use, clo, chi, p_taddr);
       // Wait for PV(n-1) at every tile, not only when rescaling: this thread then
       // has observed every earlier PV completion, so the o_done phase can be at
       // most one ahead of the parity asked for (no aliasing of phase n-3 with
@@ -349,12 +469,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
           tmem_st32(tmem + lane_off + o_col + c * 32, rr);
         }
-        uint32_t lr[16];
-        tmem_ld16(tmem + lane_off + C::L_COL, lr);
-        tmem_wait_ld();
+        {
+          uint32_t lr[16];
+          tmem_ld16(tmem + lane_off + C::L_COL, lr);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) lr[e] = __float_as_uint(__uint_as_float(lr[e]) * alpha);
-        tmem_st16(tmem + lane_off + C::L_COL, lr);
+          for (int e = 0; e < 16; ++e) lr[e] = __float_as_uint(__uint_as_float(lr[e]) * alpha);
+          tmem_st16(tmem + lane_off + C::L_COL, lr);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
