@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--seq-len", type=int, default=0,
+                   help="override the workload's sequence length (smaller cases for profiler captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
     return p.parse_args()
@@ -78,24 +80,26 @@ KERNEL_SOURCE = {
     "bwd_dq_simt": "simt_kernels.cu", "fwd_tc": "tc_fwd.cu", "convert_f16": "tc_fwd.cu",
     "bwd_rowstats": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
 }
+# head dim 512: the backward's tensor-core launches come from the cluster kernels
+KERNEL_SOURCE_D512 = {"bwd_dkdv_tc": "tc_bwd512.cu", "bwd_dq_tc": "tc_bwd512.cu"}
 
 
-def source_digest(kernel: str) -> str:
+def source_digest(kernel: str, D: int = 0) -> str:
     """First 16 hex digits of the sha256 of the kernel's source file."""
-    name = KERNEL_SOURCE.get(kernel)
+    name = (KERNEL_SOURCE_D512.get(kernel) if D == 512 else None) or KERNEL_SOURCE.get(kernel)
     if name is None:
         return "unknown"
     with open(os.path.join(ROOT, "sliding_window_attention_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, workload: str, D: int = 0):
     """DRAM bytes per launch recorded by an ncu capture (profiles/ncu_traffic.txt),
     or None when absent or taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = source_digest(kernel)
+    digest = source_digest(kernel, D)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
@@ -404,7 +408,7 @@ def run_ours(args, w, world, rank, local_rank):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         per_pair = KERNEL_FLOPS_PER_PAIR_D.get(kname, 4)
-        if kname == "bwd_dkdv_tc" and D > 128:
+        if kname == "bwd_dkdv_tc" and D == 256:
             per_pair = 10  # dV-only pass (S^T, dV) + dK-only pass (S^T, dP^T, dK)
         alg = per_pair * D * w.pairs()
         achieved = alg / avg_s / 1e12
@@ -417,7 +421,7 @@ def run_ours(args, w, world, rank, local_rank):
                     "unit": "TFLOP/s", "peak_source": f"{peaks['source']} bf16 dense (burst)"}
     roof["kernel"] = kname
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    traffic = ncu_traffic(kname, w.name)
+    traffic = ncu_traffic(kname, w.name, D)
     roof["traffic"] = traffic
 
     line = None
@@ -465,6 +469,10 @@ def main():
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     w = WORKLOADS[args.workload]
+    if args.seq_len > 0:
+        import dataclasses
+
+        w = dataclasses.replace(w, name=f"{w.name}@L{args.seq_len}", L=args.seq_len)
     world, rank, local_rank = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
