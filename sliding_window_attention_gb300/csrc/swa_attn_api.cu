@@ -117,7 +117,7 @@ swa::Geom make_geom(int B, int Hq, int Hkv, int L, int D, int window, float scal
 size_t bwd_delta_bytes(int B, int Hq, int L) { return round_up((size_t)B * Hq * L * sizeof(float), 256); }
 
 // Backward workspace layout on the tensor-core path:
-// [row stats (lse*log2e, Delta) : B*Hq*Lpad float2][q16][k16][v16][dO16].
+// [row stats: lse*log2e plane, Delta plane, B*Hq*Lpad floats each][q16][k16][v16][dO16].
 struct BwdTcWs {
   size_t stats, q16, k16, v16, g16, total;
   int Lpad;
@@ -246,7 +246,7 @@ int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const 
     if (!status) return rc;
     const BwdTcWs w = bwd_tc_ws_layout(B, Hq, Hkv, L, D);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    float2* stats = reinterpret_cast<float2*>(ws + w.stats);
+    float* stats = reinterpret_cast<float*>(ws + w.stats);
     uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
     uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
     uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);

@@ -45,21 +45,22 @@ cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int hea
 bool bwd_tc_supported(int D);
 // Padded row count of the backward's row-statistics array.
 int bwd_stats_lpad(int L);
-// stats[bh * Lpad + i] = (lse * log2(e), dO_i . o_i), zero for i >= L.
+// Two planes of B * Hq * Lpad floats: stats[bh * Lpad + i] = lse_i * log2(e),
+// stats[(B * Hq + bh) * Lpad + i] = dO_i . o_i; zero for i >= L.
 cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint16_t* dO, const float* lse,
-                            float2* stats, cudaStream_t s);
+                            float* stats, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                               const uint16_t* g16, const float2* stats, int Lpad, float* dk, float* dv,
+                               const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                int* status, cudaStream_t s);
 // Head dim 512: thread-block-cluster kernels (tc_bwd512.cu).
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                  const uint16_t* g16, const float2* stats, int Lpad, float* dk, float* dv,
+                                  const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                   int* status, cudaStream_t s);
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                const uint16_t* g16, const float2* stats, int Lpad, float* dq, int* status,
+                                const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                                 cudaStream_t s);
 cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                             const uint16_t* g16, const float2* stats, int Lpad, float* dq, int* status,
+                             const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                              cudaStream_t s);
 
 }  // namespace swa

@@ -46,11 +46,13 @@ constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 5
 constexpr int kSmemMax = 232448;         // dynamic shared memory per block on sm_103 (227 KB)
 constexpr int clamp_stages(int n) { return n < 2 ? 2 : (n > 8 ? 8 : n); }
 
-// Row statistics for the backward: per (b*Hq + h, i < Lpad) the pair
-// (lse_i * log2(e), Delta_i = dO_i . o_i); zero for padding rows i >= L.
+// Row statistics for the backward, two planes of BH * Lpad floats: per
+// (bh = b*Hq + h, i < Lpad) stats[bh Lpad + i] = lse_i * log2(e) and
+// stats[BH Lpad + bh Lpad + i] = Delta_i = dO_i . o_i; zero for padding rows
+// i >= L.  Planar, so that one 16-byte load gives four columns' values.
 __global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, int D, const float* __restrict__ o,
                                                        const uint16_t* __restrict__ dO,
-                                                       const float* __restrict__ lse, float2* __restrict__ stats) {
+                                                       const float* __restrict__ lse, float* __restrict__ stats) {
   const long row = ((long)blockIdx.x * 256 + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (row >= (long)BH * Lpad) return;
@@ -70,7 +72,10 @@ __global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, 
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     l2 = lse[(size_t)bh * L + i] * kLog2e;
   }
-  if (lane == 0) stats[row] = make_float2(l2, acc);
+  if (lane == 0) {
+    stats[row] = l2;
+    stats[(size_t)BH * Lpad + row] = acc;
+  }
 }
 
 __device__ __forceinline__ bool in_band(int i, int j, int W) { return j <= i && (W == 0 || i - j < W); }
@@ -80,21 +85,28 @@ __device__ __forceinline__ bool in_band(int i, int j, int W) { return j <= i && 
 // every column is in the band (no mask code); otherwise columns outside
 // [clo, chi] give exactly zero.
 template <bool FULL, bool WANT_P, bool WANT_DS>
-__device__ __forceinline__ void kv_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float4* stats4,
-                                         float sl2, int cbase, int clo, int chi, uint32_t (&pp)[16],
-                                         uint32_t (&dd)[16]) {
+__device__ __forceinline__ void kv_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float* lse_s,
+                                         const float* dl_s, float sl2, int cbase, int clo, int chi,
+                                         uint32_t (&pp)[16], uint32_t (&dd)[16]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float4 rs = stats4[(cbase + e) >> 1];  // (lse0*log2e, Delta0, lse1*log2e, Delta1)
-    float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -rs.x));
-    float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -rs.z));
-    if (!FULL) {
-      p0 = (cbase + e >= clo && cbase + e <= chi) ? p0 : 0.f;
-      p1 = (cbase + e + 1 >= clo && cbase + e + 1 <= chi) ? p1 : 0.f;
+  for (int e = 0; e < 32; e += 4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + cbase + e);  // lse * log2e of 4 columns
+    float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (WANT_DS) d4 = *reinterpret_cast<const float4*>(dl_s + cbase + e);  // Delta of 4 columns
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dlv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+    for (int u = 0; u < 4; u += 2) {
+      float p0 = fast_exp2(fmaf(__uint_as_float(sv[e + u]), sl2, -lv[u]));
+      float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + u + 1]), sl2, -lv[u + 1]));
+      if (!FULL) {
+        p0 = (cbase + e + u >= clo && cbase + e + u <= chi) ? p0 : 0.f;
+        p1 = (cbase + e + u + 1 >= clo && cbase + e + u + 1 <= chi) ? p1 : 0.f;
+      }
+      if (WANT_P) pp[(e + u) >> 1] = pack_half2(p0, p1);
+      if (WANT_DS)
+        dd[(e + u) >> 1] = pack_half2(p0 * (__uint_as_float(dv[e + u]) - dlv[u]),
+                                      p1 * (__uint_as_float(dv[e + u + 1]) - dlv[u + 1]));
     }
-    if (WANT_P) pp[e >> 1] = pack_half2(p0, p1);
-    if (WANT_DS)
-      dd[e >> 1] = pack_half2(p0 * (__uint_as_float(dv[e]) - rs.y), p1 * (__uint_as_float(dv[e + 1]) - rs.w));
   }
 }
 
@@ -137,7 +149,7 @@ struct KvCfg {
   static constexpr int KCH = D / 64;
   static constexpr int KV_BYTES = BNK * D * 2;  // K (or V) tile
   static constexpr int QT_BYTES = BM * D * 2;   // Q (or dO) tile
-  static constexpr int ST_BYTES = BM * 8;       // (lse, Delta) pairs
+  static constexpr int ST_BYTES = BM * 8;       // lse * log2e of BM rows, then their Delta
   static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, stats (padded to 1 KB)
   static constexpr int RES_BYTES = (NEED_V ? 2 : 1) * KV_BYTES;  // resident K (and V)
   // Q / dO / stats stages: as many as shared memory holds (TMA latency hiding)
@@ -157,7 +169,7 @@ struct BwdParams {
   Geom g;
   float* out0;  // dkdv: dk ; dq: dq
   float* out1;  // dkdv: dv
-  const float2* stats;
+  const float* stats;  // two planes: lse * log2e, then Delta (B * Hq * Lpad floats each)
   int Lpad;
   int n_tiles;
   int* status;
@@ -244,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(stg + c * BM * 128, &tmQ, st_full + st, c * 64, t * BM, bh);
           tma_load_3d(stg + C::QT_BYTES + c * BM * 128, &tmG, st_full + st, c * 64, t * BM, bh);
         }
-        tma_load_2d(stg + 2 * C::QT_BYTES, &tmS, st_full + st, 2 * t * BM, bh);
+        tma_load_2d(stg + 2 * C::QT_BYTES, &tmS, st_full + st, t * BM, bh);
+        tma_load_2d(stg + 2 * C::QT_BYTES + BM * 4, &tmS, st_full + st, t * BM, g.B * g.Hq + bh);
       }
     }
   } else if (warp == 1) {
@@ -309,8 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i0 = (t_lo + n % ntq) * BM;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      // (lse0 * log2e, Delta0, lse1 * log2e, Delta1) for query columns 2k, 2k+1
-      const float4* stats4 = reinterpret_cast<const float4*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
+      // lse * log2e and Delta of this step's query columns
+      const float* lse_s = reinterpret_cast<const float*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
+      const float* dl_s = lse_s + BM;
       const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
       // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
       const int clo = max(0, j - i0);
@@ -338,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
         const int cb = cw0 + c * 32;  // tile-local query column of this chunk
         uint32_t pp[16], dd[16];
-        if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, cb, clo, chi, pp, dd);
-        else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, stats4, sl2, cb, clo, chi, pp, dd);
+        if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, lse_s, dl_s, sl2, cb, clo, chi, pp, dd);
+        else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, lse_s, dl_s, sl2, cb, clo, chi, pp, dd);
         // P^T / dS^T as fp16 pairs: query columns 2t, 2t+1 -> TMEM column t
         if (C::DO_DV) tmem_st16(tmem + lane_off + C::S_COL + sb * BM + cb / 2, pp);
         if (C::DO_DK) tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + cb / 2, dd);
@@ -363,6 +377,318 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
         const int c = c0 + cc;
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + col + c * 32, a);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dK / dV for head dim <= 128 with 128-row query steps, so that every MMA has
+// N = 128 (tcgen05.mma with N <= 64 costs a fixed ~50 cycles per instruction
+// and runs at ~60% of the tensor rate).
+//
+// TMEM: dV [0, 128), dK [128, 256), S^T [256, 384), dP^T [384, 512), each
+// single-buffered.  Per step n the elementwise warps read S^T(n) as soon as it
+// lands (the S buffer is then free for S^T(n + 1)) and compute P^T(n) while
+// the tensor pipe runs dV(n - 1), dK(n - 1) and dP^T(n); once dP^T(n) has been
+// read by both warpgroups they pack P^T(n) and dS^T(n) as fp16 pairs into the
+// dP buffer, where dV(n) and dK(n) read them as TMEM A operands.  The
+// per-column row statistics (lse, Delta) of a step are loaded into registers
+// before the waits for S^T and dP^T, so their latency overlaps the MMAs; dS
+// is formed from the fp16-rounded P that dV uses.  MMA issue
+// order: S(n + 1) | dV(n) dK(n) | dP(n + 1); tcgen05 MMAs of one thread run in
+// issue order, so dP(n + 1) overwrites the buffer only after dV(n) and dK(n)
+// have read it.  Q and dO travel in separate TMA rings (Q lives from S(n) to
+// dK(n), dO from dP(n) to dV(n)).
+template <int D>
+struct Kv128Cfg {
+  static constexpr int BNK = 128, BM = 128, CW = 64;  // CW: query columns per warpgroup
+  static constexpr int KCH = D / 64;
+  static constexpr int KV_BYTES = BNK * D * 2;
+  static constexpr int QT_BYTES = BM * D * 2;
+  static constexpr int NQ = (D <= 64) ? 4 : 3;  // Q ring depth
+  static constexpr int NG = (D <= 64) ? 4 : 2;  // dO ring depth
+  static constexpr int DV_COL = 0, DK_COL = 128, S_COL = 256, DP_COL = 384;
+  static constexpr size_t SMEM = 2 * (size_t)KV_BYTES + (size_t)(NQ + NG) * QT_BYTES + 1024 + 512;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
+  static_assert(D <= 128, "dV and dK below the S buffer");
+};
+
+// P^T for one key row and 64 query columns (fp32, in place over S^T); lv
+// holds lse * log2e of the 64 columns (loaded before S^T was waited for).
+template <bool FULL>
+__device__ __forceinline__ void kv_p64(uint32_t (&sv)[64], const float (&lv)[64], float sl2, int cbase, int clo,
+                                       int chi) {
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    float pv = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -lv[e]));
+    if (!FULL) pv = (cbase + e >= clo && cbase + e <= chi) ? pv : 0.f;
+    sv[e] = __float_as_uint(pv);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                      const BwdParams p) {
+  using C = Kv128Cfg<D>;
+  constexpr int BNK = C::BNK, BM = C::BM, NQ = C::NQ, NG = C::NG, KCH = C::KCH, CW = C::CW;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sK = base;
+  unsigned char* sV = sK + C::KV_BYTES;
+  unsigned char* sQ = sV + C::KV_BYTES;
+  unsigned char* sG = sQ + NQ * C::QT_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sG + NG * C::QT_BYTES);
+  uint64_t* kv_full = bars;            // [1]
+  uint64_t* q_full = kv_full + 1;      // [NQ]
+  uint64_t* q_empty = q_full + NQ;     // [NQ]
+  uint64_t* g_full = q_empty + NQ;     // [NG]
+  uint64_t* g_empty = g_full + NG;     // [NG]
+  uint64_t* s_full = g_empty + NG;     // [1] S^T(n) in TMEM
+  uint64_t* s_read = s_full + 1;       // [1] both warpgroups loaded S^T(n)
+  uint64_t* dp_full = s_read + 1;      // [1] dP^T(n) in TMEM
+  uint64_t* dp_read = dp_full + 1;     // [1] both warpgroups loaded dP^T(n)
+  uint64_t* p_full = dp_read + 1;      // [1] P^T(n), dS^T(n) packed into the dP buffer
+  uint64_t* acc_done = p_full + 1;     // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bkv = blockIdx.x;  // b * Hkv + kv head
+  const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
+  const int j0 = (int)blockIdx.y * BNK;
+  const int jhi = min(j0 + BNK, g.L) - 1;
+  const int ihi = g.W > 0 ? min(g.L - 1, jhi + g.W - 1) : g.L - 1;
+  const int t_lo = j0 / BM, t_hi = ihi / BM;
+  const int ntq = t_hi - t_lo + 1;
+  const int N = g.G * ntq;  // steps (head of group, query tile)
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(q_full + s, 1);
+      mbar_init(q_empty + s, 1);
+    }
+    for (int s = 0; s < NG; ++s) {
+      mbar_init(g_full + s, 1);
+      mbar_init(g_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_read, 256);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_read, 256);
+    mbar_init(p_full, 256);
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto step_head = [&](int n) { return b * g.Hq + kvh * g.G + n / ntq; };
+  auto step_i0 = [&](int n) { return (t_lo + n % ntq) * BM; };
+
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_3d(sK + c * BNK * 128, &tmK, kv_full, c * 64, j0, bkv);
+        tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
+      }
+      // Q(n) and dO(n), each ring refilled as soon as its slot is released;
+      // Q runs one step ahead of dO (S(n + 1) is issued before dP(n + 1))
+      int nq = 0, ng = 0;
+      bool ok = true;
+      while (ok && (nq < N || ng < N)) {
+        if (nq < N && nq <= ng + 1) {
+          const int s = nq % NQ;
+          if (nq >= NQ && !mbar_wait(q_empty + s, ((nq / NQ) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(q_full + s, C::QT_BYTES);
+          for (int c = 0; c < KCH; ++c)
+            tma_load_3d(sQ + s * C::QT_BYTES + c * BM * 128, &tmQ, q_full + s, c * 64, step_i0(nq), step_head(nq));
+          ++nq;
+        } else {
+          const int s = ng % NG;
+          if (ng >= NG && !mbar_wait(g_empty + s, ((ng / NG) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(g_full + s, C::QT_BYTES);
+          for (int c = 0; c < KCH; ++c)
+            tma_load_3d(sG + s * C::QT_BYTES + c * BM * 128, &tmG, g_full + s, c * 64, step_i0(ng), step_head(ng));
+          ++ng;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major), N = 128
+      const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (A in TMEM, B MN-major)
+      const uint64_t kdk = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vdk = smem_desc_sw128(smem_u32(sV), 16, 1024);
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      auto issue_s = [&](int n) -> bool {  // S^T(n) = K Q(n)^T
+        if (!mbar_wait(q_full + n % NQ, (n / NQ) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t qk = smem_desc_sw128(smem_u32(sQ + (n % NQ) * C::QT_BYTES), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
+          mma_ss(tmem + C::S_COL, desc_add(kdk, off), desc_add(qk, off), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        return true;
+      };
+      auto issue_dp = [&](int n) -> bool {  // dP^T(n) = V dO(n)^T
+        if (!mbar_wait(g_full + n % NG, (n / NG) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint64_t gk = smem_desc_sw128(smem_u32(sG + (n % NG) * C::QT_BYTES), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
+          mma_ss(tmem + C::DP_COL, desc_add(vdk, off), desc_add(gk, off), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(dp_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0) && issue_dp(0);
+      for (int n = 0; ok && n < N; ++n) {
+        // S buffer free once both warpgroups have loaded S^T(n)
+        if (!mbar_wait(s_read, n & 1, abort_flag)) { ok = false; break; }
+        if (n + 1 < N && !issue_s(n + 1)) { ok = false; break; }
+        if (!mbar_wait(p_full, n & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t gmn = smem_desc_sw128(smem_u32(sG + (n % NG) * C::QT_BYTES), BM * 128, 1024);
+        const uint64_t qmn = smem_desc_sw128(smem_u32(sQ + (n % NQ) * C::QT_BYTES), BM * 128, 1024);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks) {
+          const uint32_t acc = (n > 0 || ks > 0) ? 1u : 0u;
+          mma_ts(tmem + C::DV_COL, tmem + C::DP_COL + ks * 8, desc_add(gmn, ks * 2048), idG, acc);
+          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + 64 + ks * 8, desc_add(qmn, ks * 2048), idG, acc);
+        }
+        mma_commit(g_empty + n % NG);
+        mma_commit(q_empty + n % NQ);
+        if (n + 1 < N && !issue_dp(n + 1)) { ok = false; break; }
+      }
+      if (ok) mma_commit(acc_done);
+    }
+  } else {
+    // warpgroup wg (warps 2-5 / 6-9) takes query columns [64 wg, 64 wg + 64);
+    // warp % 4 fixes the TMEM lane quarter, i.e. the key rows
+    const int wg = (warp - 2) >> 2;
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int j = j0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    const int cw0 = wg * CW;
+    bool ok = true;
+    const size_t dplane = (size_t)g.B * g.Hq * p.Lpad;  // offset of the Delta plane
+    for (int n = 0; n < N; ++n) {
+      const int i0 = step_i0(n);
+      const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + i0 + cw0;
+      // lse * log2e of this warpgroup's 64 query columns, loaded while S^T(n) is computed
+      float lv[64];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_g) + q);
+        lv[4 * q] = l4.x;
+        lv[4 * q + 1] = l4.y;
+        lv[4 * q + 2] = l4.z;
+        lv[4 * q + 3] = l4.w;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, n & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(tmem + lane_off + C::S_COL + cw0, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld32(tmem + lane_off + C::S_COL + cw0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_read);
+      const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
+      // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
+      const int clo = max(0, j - i0);
+      const int chi = min(min(BM - 1, g.L - 1 - i0), g.W > 0 ? j + g.W - 1 - i0 : BM - 1);
+      if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
+      else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
+      // P^T as fp16 pairs (the dV operand); dS below uses the same rounded P
+      uint32_t pp[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) pp[e >> 1] = pack_half2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+      // Delta of the 64 columns, loaded while dP^T(n) is computed
+      float dl[64];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 d4 = __ldg(reinterpret_cast<const float4*>(lse_g + dplane) + q);
+        dl[4 * q] = d4.x;
+        dl[4 * q + 1] = d4.y;
+        dl[4 * q + 2] = d4.z;
+        dl[4 * q + 3] = d4.w;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(dp_full, n & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dd[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // two 32-column halves keep dP^T's registers small
+        uint32_t dv[32];
+        tmem_ld32(tmem + lane_off + C::DP_COL + cw0 + 32 * h, dv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pp[16 * h + (e >> 1)]));
+          dd[16 * h + (e >> 1)] = pack_half2(pf.x * (__uint_as_float(dv[e]) - dl[32 * h + e]),
+                                             pf.y * (__uint_as_float(dv[e + 1]) - dl[32 * h + e + 1]));
+        }
+      }
+      tc_fence_before();
+      // the packed results land on columns the other warpgroup reads: both
+      // finish reading dP^T(n) first (bounded wait, not bar.sync)
+      mbar_arrive(dp_read);
+      if (!__all_sync(0xffffffffu, mbar_wait(dp_read, n & 1, abort_flag))) { ok = false; break; }
+      // P^T -> dP buffer columns [32 wg, 32 wg + 32), dS^T -> [64 + 32 wg, ...)
+      tmem_st32(tmem + lane_off + C::DP_COL + cw0 / 2, pp);
+      tmem_st32(tmem + lane_off + C::DP_COL + 64 + cw0 / 2, dd);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
+      tc_fence_after();
+      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
+      const bool row_ok = j < g.L;
+      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+      const uint32_t col = wg == 0 ? C::DK_COL : C::DV_COL;
+      const float mul = wg == 0 ? g.scale : 1.f;
+      float* dst = (wg == 0 ? p.out0 : p.out1) + off;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t a[32];
         tmem_ld32(tmem + lane_off + col + c * 32, a);
         tmem_wait_ld();
@@ -532,7 +858,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
-    const float2 rs = (i < g.L) ? p.stats[(size_t)bh * p.Lpad + i] : make_float2(0.f, 0.f);
+    const float2 rs = (i < g.L) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
+                                              p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
+                                : make_float2(0.f, 0.f);
     bool ok = true;
     constexpr int CW = C::CW;
     const int cw0 = C::SPLIT ? wg * CW : 0;
@@ -780,7 +1108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
-    const float2 rs = (i < g.L) ? p.stats[(size_t)bh * p.Lpad + i] : make_float2(0.f, 0.f);
+    const float2 rs = (i < g.L) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
+                                              p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
+                                : make_float2(0.f, 0.f);
     const int cw0 = wg * CW;
     bool ok = true;
     for (int n = 0; n < nt; ++n) {
@@ -846,9 +1176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// 2-D fp32 tensor map over the row statistics [BH, 2 * Lpad] with a
-// (2 * BM) x 1 box.
-cudaError_t make_tmap_stats(CUtensorMap* m, const void* ptr, int Lpad, int BH, int box_floats) {
+// 2-D fp32 tensor map over the row statistics, viewed as [2 * BH rows, Lpad]
+// (the lse plane, then the Delta plane) with a box_floats x 1 box.
+cudaError_t make_tmap_stats(CUtensorMap* m, const void* ptr, int Lpad, int rows, int box_floats) {
   void* f = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
@@ -856,8 +1186,8 @@ cudaError_t make_tmap_stats(CUtensorMap* m, const void* ptr, int Lpad, int BH, i
       q != cudaDriverEntryPointSuccess)
     return cudaErrorNotSupported;
   auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  cuuint64_t dims[2] = {(cuuint64_t)2 * Lpad, (cuuint64_t)BH};
-  cuuint64_t strides[1] = {(cuuint64_t)2 * Lpad * 4};
+  cuuint64_t dims[2] = {(cuuint64_t)Lpad, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)Lpad * 4};
   cuuint32_t box[2] = {(cuuint32_t)box_floats, 1};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -868,7 +1198,7 @@ cudaError_t make_tmap_stats(CUtensorMap* m, const void* ptr, int Lpad, int BH, i
 
 template <int D>
 cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                     const uint16_t* g16, const float2* stats, int Lpad, float* dq, float* dk, float* dv, int* status,
+                     const uint16_t* g16, const float* stats, int Lpad, float* dq, float* dk, float* dv, int* status,
                      cudaStream_t s, int which) {
   cudaError_t e;
   BwdParams p;
@@ -886,7 +1216,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       if ((e2 = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_stats(&ts, stats, Lpad, g.B * g.Hq, 2 * C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_stats(&ts, stats, Lpad, 2 * g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
       auto kern = dkdv_tc_kernel<D, MODE>;
       if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
           cudaSuccess)
@@ -900,7 +1230,24 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       return cudaGetLastError();
     };
     if constexpr (D <= 128) {
-      return run(std::integral_constant<int, kModeBoth>{});
+      using C = Kv128Cfg<D>;
+      CUtensorMap tq, tk, tv, tg;
+      cudaError_t e2;
+      if ((e2 = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
+      auto kern = dkdv128_tc_kernel<D>;
+      if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
+          cudaSuccess)
+        return e2;
+      BwdParams pm = p;
+      pm.out0 = dk;
+      pm.out1 = dv;
+      pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
+      dim3 grid(g.B * g.Hkv, pm.n_tiles);
+      kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
+      return cudaGetLastError();
     } else {
       if ((e = run(std::integral_constant<int, kModeDV>{})) != cudaSuccess) return e;
       return run(std::integral_constant<int, kModeDK>{});
@@ -946,7 +1293,7 @@ bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 51
 int bwd_stats_lpad(int L) { return (L + 127) / 128 * 128; }
 
 cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint16_t* dO, const float* lse,
-                            float2* stats, cudaStream_t s) {
+                            float* stats, cudaStream_t s) {
   const long rows = (long)g.B * g.Hq * Lpad;
   const long blocks = (rows * 32 + 255) / 256;
   rowstats_kernel<<<(unsigned)blocks, 256, 0, s>>>(g.B * g.Hq, g.L, Lpad, g.D, o, dO, lse, stats);
@@ -954,7 +1301,7 @@ cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint1
 }
 
 cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                               const uint16_t* g16, const float2* stats, int Lpad, float* dk, float* dv,
+                               const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                int* status, cudaStream_t s) {
   switch (g.D) {
     case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, nullptr, dk, dv, status, s, 0);
@@ -966,7 +1313,7 @@ cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_
 }
 
 cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                             const uint16_t* g16, const float2* stats, int Lpad, float* dq, int* status,
+                             const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                              cudaStream_t s) {
   switch (g.D) {
     case 64: return bwd_tc_d<64>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, nullptr, status, s, 1);

@@ -100,35 +100,35 @@ struct Params512 {
   float* out0;             // KV: dk ; Q: dq
   float* out1;             // KV: dv
   const uint16_t* x16;     // resident S operand rows: KV: k16 ; Q: q16
-  const float2* stats;
+  const float* stats;      // two planes: lse * log2e, then Delta (B * Hq * Lpad floats each)
   int Lpad;
   int n_tiles;
   int* status;
 };
 
 // P for 64 columns (cb0 .. cb0 + 63 of the tile) of one row, in place over the
-// S values (fp32).  PER_COL: the lse belongs to the column (stats4 holds
-// (lse0 log2e, Delta0, lse1 log2e, Delta1) per column pair); otherwise l2 is
-// the row's.  Columns outside [clo, chi] are exactly zero unless FULL.
+// S values (fp32).  PER_COL: the lse belongs to the column (lse4 holds
+// lse * log2e of the 64 columns, four per vector); otherwise l2 is the row's.
+// Columns outside [clo, chi] are exactly zero unless FULL.
 template <bool FULL, bool PER_COL>
-__device__ __forceinline__ void p_tile64(uint32_t (&sv)[64], const float4* stats4, float l2, float sl2, int cb0,
+__device__ __forceinline__ void p_tile64(uint32_t (&sv)[64], const float4* lse4, float l2, float sl2, int cb0,
                                          int clo, int chi) {
 #pragma unroll
-  for (int e = 0; e < 64; e += 2) {
-    float la = l2, lb = l2;
+  for (int e = 0; e < 64; e += 4) {
+    float lv[4] = {l2, l2, l2, l2};
     if (PER_COL) {
-      const float4 rs = __ldg(stats4 + (e >> 1));
-      la = rs.x;
-      lb = rs.z;
+      const float4 l4 = __ldg(lse4 + (e >> 2));
+      lv[0] = l4.x;
+      lv[1] = l4.y;
+      lv[2] = l4.z;
+      lv[3] = l4.w;
     }
-    float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -la));
-    float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lb));
-    if (!FULL) {
-      p0 = (cb0 + e >= clo && cb0 + e <= chi) ? p0 : 0.f;
-      p1 = (cb0 + e + 1 >= clo && cb0 + e + 1 <= chi) ? p1 : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float pv = fast_exp2(fmaf(__uint_as_float(sv[e + u]), sl2, -lv[u]));
+      if (!FULL) pv = (cb0 + e + u >= clo && cb0 + e + u <= chi) ? pv : 0.f;
+      sv[e + u] = __float_as_uint(pv);
     }
-    sv[e] = __float_as_uint(p0);
-    sv[e + 1] = __float_as_uint(p1);
   }
 }
 
@@ -137,20 +137,25 @@ __device__ __forceinline__ void pack64(const uint32_t (&v)[64], uint32_t (&o)[32
   for (int e = 0; e < 64; e += 2) o[e >> 1] = pack_half2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
 }
 
-// dS = P (dP - Delta) for 64 columns as fp16 pairs.
+// dS = P (dP - Delta) for 64 columns as fp16 pairs (dl4: Delta of the 64
+// columns, four per vector, when PER_COL; otherwise dl is the row's).
 template <bool PER_COL>
-__device__ __forceinline__ void ds_tile64(const uint32_t (&pv)[64], const uint32_t (&dv)[64], const float4* stats4,
+__device__ __forceinline__ void ds_tile64(const uint32_t (&pv)[64], const uint32_t (&dv)[64], const float4* dl4,
                                           float dl, uint32_t (&o)[32]) {
 #pragma unroll
-  for (int e = 0; e < 64; e += 2) {
-    float da = dl, db = dl;
+  for (int e = 0; e < 64; e += 4) {
+    float dd[4] = {dl, dl, dl, dl};
     if (PER_COL) {
-      const float4 rs = __ldg(stats4 + (e >> 1));
-      da = rs.y;
-      db = rs.w;
+      const float4 d4 = __ldg(dl4 + (e >> 2));
+      dd[0] = d4.x;
+      dd[1] = d4.y;
+      dd[2] = d4.z;
+      dd[3] = d4.w;
     }
-    o[e >> 1] = pack_half2(__uint_as_float(pv[e]) * (__uint_as_float(dv[e]) - da),
-                           __uint_as_float(pv[e + 1]) * (__uint_as_float(dv[e + 1]) - db));
+    o[e >> 1] = pack_half2(__uint_as_float(pv[e]) * (__uint_as_float(dv[e]) - dd[0]),
+                           __uint_as_float(pv[e + 1]) * (__uint_as_float(dv[e + 1]) - dd[1]));
+    o[(e >> 1) + 1] = pack_half2(__uint_as_float(pv[e + 2]) * (__uint_as_float(dv[e + 2]) - dd[2]),
+                                 __uint_as_float(pv[e + 3]) * (__uint_as_float(dv[e + 3]) - dd[3]));
   }
 }
 
@@ -413,7 +418,8 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive(&bars->x_ready);
     }
     float2 rs_row = make_float2(0.f, 0.f);
-    if (DIR == kDirQ) rs_row = p.stats[(size_t)head * p.Lpad + row];
+    if (DIR == kDirQ)
+      rs_row = make_float2(p.stats[(size_t)head * p.Lpad + row], p.stats[((size_t)g.B * g.Hq + head) * p.Lpad + row]);
     const uint32_t stg = sbase + OFF_STG + wg * HALF_BYTES;
     const uint32_t stg_row = stg + r * 128;
     const bool issuer = (warp & 3) == 2;  // warp 2 / 6 copies its warpgroup's half
@@ -444,8 +450,12 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int m = 0; m < n_own; ++m) {
       const int n = (int)rank + 2 * m;
       const int c0 = step_rows(n);  // first column's query (KV) or key (Q)
-      const float4* stats4 = nullptr;
-      if (DIR == kDirKV) stats4 = reinterpret_cast<const float4*>(p.stats + (size_t)step_head(n) * p.Lpad + c0 + cb0);
+      const float4 *lse4 = nullptr, *dl4 = nullptr;
+      if (DIR == kDirKV) {
+        const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + c0 + cb0;
+        lse4 = reinterpret_cast<const float4*>(lse_g);
+        dl4 = reinterpret_cast<const float4*>(lse_g + (size_t)g.B * g.Hq * p.Lpad);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->t_full, m & 1, abort_flag, R))) {
         ok = false;
         break;
@@ -470,8 +480,8 @@ __global__ void __launch_bounds__(kThr, 1)
         clo = g.W > 0 ? max(0, row - g.W + 1 - c0) : 0;
         chi = min(T - 1, row - c0);
       }
-      if (full) p_tile64<true, DIR == kDirKV>(sv, stats4, rs_row.x, sl2, cb0, clo, chi);
-      else p_tile64<false, DIR == kDirKV>(sv, stats4, rs_row.x, sl2, cb0, clo, chi);
+      if (full) p_tile64<true, DIR == kDirKV>(sv, lse4, rs_row.x, sl2, cb0, clo, chi);
+      else p_tile64<false, DIR == kDirKV>(sv, lse4, rs_row.x, sl2, cb0, clo, chi);
       uint32_t o[32];
       if (DIR == kDirKV) {
         pack64(sv, o);
@@ -480,7 +490,7 @@ __global__ void __launch_bounds__(kThr, 1)
           break;
         }
       }
-      ds_tile64<DIR == kDirKV>(sv, dv, stats4, rs_row.y, o);
+      ds_tile64<DIR == kDirKV>(sv, dv, dl4, rs_row.y, o);
       if (!send(o, 1, DIR == kDirKV ? 3u : 2u, m)) {  // dS -> dK / dQ accumulator
         ok = false;
         break;
@@ -560,7 +570,7 @@ __global__ void __launch_bounds__(kThr, 1)
 
 template <int DIR>
 cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                       const uint16_t* g16, const float2* stats, int Lpad, float* out0, float* out1, int* status,
+                       const uint16_t* g16, const float* stats, int Lpad, float* out0, float* out1, int* status,
                        cudaStream_t s) {
   CUtensorMap tq, tk, tv, tg;
   cudaError_t e;
@@ -600,13 +610,13 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                  const uint16_t* g16, const float2* stats, int Lpad, float* dk, float* dv,
+                                  const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                   int* status, cudaStream_t s) {
   return launch_dir<kDirKV>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
 }
 
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                const uint16_t* g16, const float2* stats, int Lpad, float* dq, int* status,
+                                const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                                 cudaStream_t s) {
   return launch_dir<kDirQ>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s);
 }
