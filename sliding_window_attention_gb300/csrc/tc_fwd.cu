@@ -678,7 +678,7 @@ cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k1
     case 64: return fwd_tc_d<64>(g, q16, k16, v16, o, lse, status, s);
     case 128: return fwd_tc_d<128>(g, q16, k16, v16, o, lse, status, s);
     case 256: return fwd_tc_d<256>(g, q16, k16, v16, o, lse, status, s);
-    case 512: return fwd_tc_d<512>(g, q16, k16, v16, o, lse, status, s);
+    case 512: return launch_fwd_tc512(g, q16, k16, v16, o, lse, status, s);
     default: return cudaErrorInvalidValue;
   }
 }
