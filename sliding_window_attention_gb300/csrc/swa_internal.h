@@ -44,6 +44,11 @@ cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k1
 // 3-D fp16 tensor map over [heads, L, D] with a 64 x box_rows box and
 // 128-byte swizzle (rows at or beyond L read as zero).
 cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int heads, int box_rows);
+// The same tensor as a 4-D map whose box (64, box_rows, nchunk, 1) loads
+// nchunk 64-column chunks (consecutive [box_rows x 128 B] swizzled blocks)
+// with one TMA instruction; coordinates (0, row, first chunk, head).
+cudaError_t make_tmap_f16_chunks(CUtensorMap* m, const void* ptr, int D, int L, int heads, int box_rows,
+                                 int nchunk);
 
 bool bwd_tc_supported(int D);
 // Padded row count of the backward's row-statistics array.

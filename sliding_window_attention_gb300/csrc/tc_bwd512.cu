@@ -176,8 +176,15 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t rank = cluster_rank();
   const int role = rank < 2 ? kRoleProd : ((DIR == kDirKV && rank == 2) ? kRoleAccP : kRoleAccDS);
   const bool acc_role = role != kRoleProd;
-  const int head = blockIdx.x / R;  // KV: b * Hkv + kv head; Q: b * Hq + query head
-  const int b = (DIR == kDirKV) ? head / g.Hkv : head / g.Hq;
+  // Grid (x, y, z) = (CTAs per cluster [x query heads of the group, dQ pass],
+  // tiles, b * Hkv + kv head).  Blocks launch x fastest and z slowest, so the
+  // clusters running at any moment share one kv head: its K and V (dQ pass)
+  // or its group's Q and dO (dK/dV pass) are read from HBM about once and
+  // then served by L2.
+  const int bkv_z = (int)blockIdx.z;
+  const int b = bkv_z / g.Hkv;
+  const int head = (DIR == kDirKV) ? bkv_z  // b * Hkv + kv head
+                                   : b * g.Hq + (bkv_z - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // query head
   // resident-side tile (keys for KV, queries for Q): longest band first
   const int tile = (DIR == kDirKV) ? (int)blockIdx.y : p.n_tiles - 1 - (int)blockIdx.y;
   const int r0 = tile * T;
@@ -195,11 +202,17 @@ __global__ void __launch_bounds__(kThr, 1)
     ntq = ihi / T - t_lo + 1;
     N = ntq;
   }
-  // streamed-side rows and head of step n
-  auto step_rows = [&](int n) { return (t_lo + n % ntq) * T; };
+  // streamed-side rows and head of step n.  dK/dV pass: query tiles from the
+  // last one down, the group's query heads innermost, so that concurrent
+  // clusters of one kv head (all starting at the last query tile) read the
+  // same Q and dO tiles at about the same time.
+  auto step_rows = [&](int n) {
+    if (DIR == kDirKV) return (t_lo + ntq - 1 - n / g.G) * T;
+    return (t_lo + n) * T;
+  };
   auto step_head = [&](int n) -> int {
-    if (DIR == kDirKV) return b * g.Hq + (head - b * g.Hkv) * g.G + n / ntq;  // query head
-    return b * g.Hkv + (head - b * g.Hq) / g.G;                                // kv head
+    if (DIR == kDirKV) return b * g.Hq + (head - b * g.Hkv) * g.G + n % g.G;  // query head
+    return bkv_z;                                                              // kv head
   };
   // a producer takes steps n = rank, rank + 2, ...; m-th own step = rank + 2m
   const int n_own = role == kRoleProd ? (N - (int)rank + 1) / 2 : 0;
@@ -591,9 +604,9 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
   pm.n_tiles = (g.L + T - 1) / T;
   pm.status = status;
   const unsigned R = (DIR == kDirKV) ? 4 : 3;
-  const unsigned heads = (DIR == kDirKV) ? (unsigned)(g.B * g.Hkv) : (unsigned)(g.B * g.Hq);
+  const unsigned xs = (DIR == kDirKV) ? R : R * (unsigned)g.G;  // dQ pass: the group's query heads along x
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(R * heads, (unsigned)pm.n_tiles, 1);
+  cfg.gridDim = dim3(xs, (unsigned)pm.n_tiles, (unsigned)(g.B * g.Hkv));
   cfg.blockDim = dim3(kThr, 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;

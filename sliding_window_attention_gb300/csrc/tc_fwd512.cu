@@ -4,7 +4,9 @@
 // columns) fills one SM's Tensor Memory, so S and O cannot live on the same
 // SM.  One cluster per (query head, 128-row query tile), longest rows first:
 //   rank 0 (producer): Q sits in Tensor Memory as fp16 pairs (256 columns,
-//     the A operand of TS-form MMAs); K streams in 64-column slices;
+//     the A operand of TS-form MMAs); K streams in 128-column slices, one
+//     32 KB TMA instruction each (the per-SM TMA rate grows with the size of
+//     an instruction: about 46 B/clk for 16 KB, 81 for 32 KB);
 //     S = Q K^T (N = 128) into two TMEM buffers; online softmax with the band
 //     mask on edge tiles ("Lab 028 lab detail: Off NVIDIA, you fix the
 //     platform yourself", "What I changed, in plain terms" items 3-4); P in
@@ -53,8 +55,8 @@ constexpr int HALF_BYTES = TILE_BYTES / 2;  // one warpgroup's 64 columns (one s
 constexpr int OFF_STG = 0;
 constexpr int OFF_VEC = 2 * HALF_BYTES;  // alpha[128], inv_l[128], max exchange [2][2][128], l exchange [2][128]
 constexpr int OFF_RING_P = 40960;        // 1 KB aligned
-constexpr int SLOT_P = T * 64 * 2;       // 64-column K slice
-constexpr int NR_P = 11;
+constexpr int SLOT_P = T * 128 * 2;      // 128-column K slice: two TMA boxes under one barrier
+constexpr int NR_P = 5;
 // accumulator shared memory: two P slots, two alpha slots + 1 / l, V ring
 constexpr int OFF_RECV = 0;
 constexpr int OFF_RVEC = 2 * TILE_BYTES;  // alpha slot [2][128], inv_l [128]
@@ -155,9 +157,12 @@ __global__ void __launch_bounds__(kThr, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool producer = rank == 0;
-  const int bh = blockIdx.x / R;  // b * Hq + query head
-  const int b = bh / g.Hq, h = bh - b * g.Hq;
-  const int bkv = b * g.Hkv + h / g.G;
+  // Grid (x, y, z) = (2 x the group's query heads, query tiles, b * Hkv + kv
+  // head).  Blocks launch x fastest and z slowest, so the clusters running at
+  // any moment share one kv head, whose K and V then stay in L2.
+  const int bkv = (int)blockIdx.z;
+  const int b = bkv / g.Hkv;
+  const int bh = b * g.Hq + (bkv - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // b * Hq + query head
   const int tile = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
   const int i0 = tile * T;
   const int ihi = min(i0 + T, g.L) - 1;
@@ -213,21 +218,20 @@ __global__ void __launch_bounds__(kThr, 1)
       const int nr = producer ? NR_P : NR_A;
       for (int n = 0; ok && n < N; ++n) {
         const int j0 = (t_lo + n) * T;
-        const int per = producer ? DH / 64 : DH / 128;
-        for (int c = 0; c < per; ++c, ++issued) {
+        for (int c = 0; c < DH / 128; ++c, ++issued) {
           const int s = issued % nr;
           if (issued >= nr && !mbar_wait_cl(&bars->ring_empty[s], ((issued / nr) & 1) ^ 1, abort_flag, R)) {
             ok = false;
             break;
           }
           if (producer) {
+            unsigned char* dst = base + OFF_RING_P + s * SLOT_P;
             mbar_arrive_expect_tx(&bars->ring_full[s], SLOT_P);
-            tma_load_3d(base + OFF_RING_P + s * SLOT_P, &tmK, &bars->ring_full[s], c * 64, j0, bkv);
+            tma_load_4d(dst, &tmK, &bars->ring_full[s], 0, j0, 2 * c, bkv);  // chunks 2c, 2c + 1
           } else {
             unsigned char* dst = base + OFF_RING_A + s * SLOT_A;
             mbar_arrive_expect_tx(&bars->ring_full[s], SLOT_A);
-            tma_load_3d(dst, &tmV, &bars->ring_full[s], c * 128, j0, bkv);
-            tma_load_3d(dst + T * 128, &tmV, &bars->ring_full[s], c * 128 + 64, j0, bkv);
+            tma_load_4d(dst, &tmV, &bars->ring_full[s], 0, j0, 2 * c, bkv);
           }
         }
       }
@@ -253,7 +257,7 @@ __global__ void __launch_bounds__(kThr, 1)
             break;
           }
           tc_fence_after();
-          for (int c = 0; c < DH / 64; ++c, ++used) {
+          for (int c = 0; c < DH / 128; ++c, ++used) {
             const int s = used % NR_P;
             if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_P) & 1, abort_flag, R)) {
               ok = false;
@@ -261,10 +265,11 @@ __global__ void __launch_bounds__(kThr, 1)
             }
             tc_fence_after();
             const uint64_t kd = smem_desc_sw128(sbase + OFF_RING_P + s * SLOT_P, 16, 1024);
+            // head-dim columns [128 c, 128 c + 128): Q columns 64 c + 8 ks in TMEM
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ts(tmem + S_COL + bb * T, tmem + X_COL + c * 32 + ks * 8, desc_add(kd, ks * 32), idS,
-                     (c | ks) ? 1u : 0u);
+            for (int ks = 0; ks < 8; ++ks)
+              mma_ts(tmem + S_COL + bb * T, tmem + X_COL + c * 64 + ks * 8,
+                     desc_add(kd, (ks >> 2) * T * 128 + (ks & 3) * 32), idS, (c | ks) ? 1u : 0u);
             mma_commit(&bars->ring_empty[s]);
           }
           if (!ok) break;
@@ -534,8 +539,9 @@ cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t*
                              float* lse, int* status, cudaStream_t s) {
   CUtensorMap tk, tv;
   cudaError_t e;
-  if ((e = make_tmap_f16(&tk, k16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16(&tv, v16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
+  // 128-column slices of K and V: two 64-column chunks per TMA instruction
+  if ((e = make_tmap_f16_chunks(&tk, k16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tv, v16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(fwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
       cudaSuccess)
     return e;
@@ -547,7 +553,7 @@ cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t*
   pm.n_tiles = (g.L + T - 1) / T;
   pm.status = status;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(R * (unsigned)(g.B * g.Hq), (unsigned)pm.n_tiles, 1);
+  cfg.gridDim = dim3(R * (unsigned)g.G, (unsigned)pm.n_tiles, (unsigned)(g.B * g.Hkv));
   cfg.blockDim = dim3(kThr, 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
