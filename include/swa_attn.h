@@ -117,6 +117,17 @@ int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const 
  */
 int swa_attn_get_status(void* stream);
 
+/*
+ * swa_attn_selftest_timeout: exercises the device-side failure path without
+ * a fault.  It launches, on `stream`, one CTA that waits on a barrier that
+ * nothing completes.  The wait uses the same bounded wait as every kernel of
+ * the library, with a limit of about 1 ms.  When that limit runs out, the CTA
+ * latches SWA_ERR_DEVICE_TIMEOUT in the status word, and the next
+ * swa_attn_get_status() on the stream returns it.  The CUDA context stays
+ * usable.  Returns SWA_OK, or SWA_ERR_CUDA if the launch fails.
+ */
+int swa_attn_selftest_timeout(void* stream);
+
 /* Static, human-readable description of a return code. */
 const char* swa_attn_strerror(int code);
 

@@ -18,9 +18,10 @@ from ._native import (  # noqa: F401
     swa_attn_bwd,
     swa_attn_fwd,
     swa_attn_get_status,
+    swa_attn_selftest_timeout,
 )
 
 __all__ = [
     "SwaError", "backward", "bwd_workspace_bytes", "forward", "fwd_workspace_bytes", "load", "profile_begin", "profile_end", "strerror",
-    "swa_attn_bwd", "swa_attn_fwd", "swa_attn_get_status",
+    "swa_attn_bwd", "swa_attn_fwd", "swa_attn_get_status", "swa_attn_selftest_timeout",
 ]

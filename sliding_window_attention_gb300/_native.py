@@ -25,6 +25,7 @@ EXPORTED = (
     "swa_attn_profile_begin",
     "swa_attn_profile_end",
     "swa_attn_bwd_noalloc",
+    "swa_attn_selftest_timeout",
 )
 
 _lock = threading.Lock()
@@ -71,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.swa_attn_profile_end.restype = I
         lib.swa_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P] + shape + [F, P]
         lib.swa_attn_bwd_noalloc.restype = I
+        lib.swa_attn_selftest_timeout.argtypes = [P]
+        lib.swa_attn_selftest_timeout.restype = I
         _lib = lib
         return lib
 
@@ -154,6 +157,13 @@ def swa_attn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: fl
                                      _ptr(dv), B, Hq, Hkv, L, D, int(window), float(scale), _stream_ptr(stream))
     if rc:
         raise SwaError(rc, "swa_attn_bwd_noalloc")
+
+
+def swa_attn_selftest_timeout(stream=None) -> None:
+    """Launch the device-side timeout self-test (see include/swa_attn.h)."""
+    rc = load().swa_attn_selftest_timeout(_stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_selftest_timeout")
 
 
 def swa_attn_get_status(stream=None) -> int:

@@ -282,6 +282,18 @@ int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const 
   return SWA_OK;
 }
 
+int swa_attn_selftest_timeout(void* stream) {
+  int rc = check_device();
+  if (rc != SWA_OK) return rc;
+  int err = SWA_OK;
+  int* p = status_ptr_for_current_device(&err);
+  if (!p) return err;
+  // about 1 ms at the maximum SM clock
+  if (swa::launch_selftest_timeout(p, 2000000LL, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
 int swa_attn_get_status(void* stream) {
   int err = SWA_OK;
   int* p = status_ptr_for_current_device(&err);

@@ -34,6 +34,9 @@ cudaError_t launch_bwd_dq_simt(const Geom& g, const uint16_t* q, const uint16_t*
 // latches kStatusFp16Range in *status if a finite input overflows fp16.
 cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
                                int* status, cudaStream_t s);
+// One CTA whose bounded wait on a barrier nothing completes runs out after
+// limit_cycles and latches kStatusTimeout in *status.
+cudaError_t launch_selftest_timeout(int* status, long long limit_cycles, cudaStream_t s);
 bool fwd_tc_supported(int D);
 // Head dim 512: 2-CTA cluster forward (tc_fwd512.cu).
 cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,

@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = sdp_full + 2;         // [2]
   uint64_t* acc_done = p_full + 2;         // [1]
   uint64_t* ldd = acc_done + 1;            // [2] both warpgroups finished reading a buffer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ldd + 2);
+  uint64_t* mma_drain = ldd + 2;           // [1] every issued MMA finished (before TMEM is released)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const Geom& g = p.g;
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(ldd + s, 256);
     }
     mbar_init(acc_done, 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sK + c * BNK * 128, &tmK, kv_full, c * 64, j0, bkv);
         if (C::NEED_V) tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
       }
+      int issued = 0;
       for (int n = 0; n < N; ++n) {
         const int st = n % NS;
         const int gi = n / ntq, t = t_lo + n % ntq;
@@ -258,6 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tma_load_2d(stg + 2 * C::QT_BYTES, &tmS, st_full + st, t * BM, bh);
         tma_load_2d(stg + 2 * C::QT_BYTES + BM * 4, &tmS, st_full + st, t * BM, g.B * g.Hq + bh);
+        ++issued;
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(kv_full, 0);
+        drain_ring(st_full, NS, issued);
       }
     }
   } else if (warp == 1) {
@@ -305,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= 1 && !issue_grad(n - 1)) { ok = false; break; }
       }
       if (ok && issue_grad(N - 1)) mma_commit(acc_done);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
     }
   } else {
     // warpgroup (warps 2-5 or 6-9): takes steps n with n % 2 == wg; a warp can
@@ -471,7 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_read = dp_full + 1;     // [1] both warpgroups loaded dP^T(n)
   uint64_t* p_full = dp_read + 1;      // [1] P^T(n), dS^T(n) packed into the dP buffer
   uint64_t* acc_done = p_full + 1;     // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* mma_drain = acc_done + 1;  // [1] every issued MMA finished (before TMEM is released)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const Geom& g = p.g;
@@ -501,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_read, 256);
     mbar_init(p_full, 256);
     mbar_init(acc_done, 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -546,6 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sG + s * C::QT_BYTES + c * BM * 128, &tmG, g_full + s, c * 64, step_i0(ng), step_head(ng));
           ++ng;
         }
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(kv_full, 0);
+        drain_ring(q_full, NQ, nq);
+        drain_ring(g_full, NG, ng);
       }
     }
   } else if (warp == 1) {
@@ -599,6 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n + 1 < N && !issue_dp(n + 1)) { ok = false; break; }
       }
       if (ok) mma_commit(acc_done);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
     }
   } else {
     // warpgroup wg (warps 2-5 / 6-9) takes query columns [64 wg, 64 wg + 64);
@@ -754,7 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ds_full = sdp_full + 2;     // [2]
   uint64_t* acc_done = ds_full + 2;     // [1]
   uint64_t* ldd = acc_done + 1;         // [2] both warpgroups finished reading a buffer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ldd + 2);
+  uint64_t* mma_drain = ldd + 2;           // [1] every issued MMA finished (before TMEM is released)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const Geom& g = p.g;
@@ -781,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(ldd + s, 256);
     }
     mbar_init(acc_done, 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -804,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ + c * BMQ * 128, &tmQ, q_full, c * 64, i0, bh);
         tma_load_3d(sG + c * BMQ * 128, &tmG, q_full, c * 64, i0, bh);
       }
+      int issued = 0;
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
         const int j0 = (t_lo + n) * BN;
@@ -813,6 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sK + st * C::KV_BYTES + c * BN * 128, &tmK, kv_full + st, c * 64, j0, bkv);
           tma_load_3d(sV + st * C::KV_BYTES + c * BN * 128, &tmV, kv_full + st, c * 64, j0, bkv);
         }
+        ++issued;
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(q_full, 0);
+        drain_ring(kv_full, NS, issued);
       }
     }
   } else if (warp == 1) {
@@ -851,6 +880,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= 1 && !issue_dq(n - 1)) { ok = false; break; }
       }
       if (ok && issue_dq(nt - 1)) mma_commit(acc_done);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
     }
   } else {
     const int wg = (warp - 2) >> 2;  // warps 2-5 / 6-9, see the dK/dV kernel
@@ -981,7 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ds_full = sdp_full + 2;     // [2] dS(n) written over S buffer n % 2
   uint64_t* ldd = ds_full + 2;          // [2] both warpgroups have read step n (frees the dP buffer)
   uint64_t* acc_done = ldd + 2;         // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* mma_drain = acc_done + 1;  // [1] every issued MMA finished (before TMEM is released)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const Geom& g = p.g;
@@ -1012,6 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(ldd + s, 256);  // both warpgroups arrive; the MMA thread only waits
     }
     mbar_init(acc_done, 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1036,6 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sG + c * BMQ * 128, &tmG, q_full, c * 64, i0, bh);
       }
       // K and V of each step, each ring refilled as soon as its slot is released
+      int nk = 0, nv = 0;
       for (int n = 0; n < nt; ++n) {
         const int j0 = (t_lo + n) * BN;
         const int sk = n % NK, sv = n % NV;
@@ -1043,10 +1078,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(k_full + sk, C::KV_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(sK + sk * C::KV_BYTES + c * BN * 128, &tmK, k_full + sk, c * 64, j0, bkv);
+        ++nk;
         if (n >= NV && !mbar_wait(v_empty + sv, ((n / NV) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(v_full + sv, C::KV_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(sV + sv * C::KV_BYTES + c * BN * 128, &tmV, v_full + sv, c * 64, j0, bkv);
+        ++nv;
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(q_full, 0);
+        drain_ring(k_full, NK, nk);
+        drain_ring(v_full, NV, nv);
       }
     }
   } else if (warp == 1) {
@@ -1101,6 +1143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n + 2 < nt && !issue_s(n + 2)) { ok = false; break; }
       }
       if (ok) mma_commit(acc_done);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
     }
   } else {
     const int wg = (warp - 2) >> 2;  // warps 2-5 / 6-9; warp % 4 fixes the TMEM lane quarter

@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint64_t* p_full = s_full + 2;    // [2]
   uint64_t* o_done = p_full + 2;    // [NWG]: PV into O of warpgroup w complete
   uint64_t* mx_bar = o_done + NWG;  // [2]: both warpgroups posted their partial row max (split mode)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mx_bar + 2);
+  uint64_t* mma_drain = mx_bar + 2;  // [1] every issued MMA finished (before TMEM is released)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* ml_x = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(bars) + C::XCH_OFF);  // [2][128] (m, l)
   float* xm = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bars) + C::XM_OFF);  // [2][2][128]
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     for (int w = 0; w < NWG; ++w) mbar_init(o_done + w, 1);
     for (int s = 0; s < 2; ++s) mbar_init(mx_bar + s, 256);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tmap(&tmV);
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       tma_load_4d(sQ, &tmQ, q_full, 0, i0, 0, bh);  // all KCH chunks in one instruction
+      int nk = 0, nv = 0;
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
         const uint32_t par = ((n / NS) & 1) ^ 1;
@@ -257,9 +260,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (n >= NS && !mbar_wait(k_empty + st, par, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + st, C::K_BYTES);
         tma_load_4d(sK + st * C::K_BYTES, &tmK, k_full + st, 0, j0, 0, bkv);
+        ++nk;
         if (n >= NS && !mbar_wait(v_empty + st, par, abort_flag)) break;
         mbar_arrive_expect_tx(v_full + st, C::V_BYTES);
         tma_load_4d(sV + st * C::V_BYTES, &tmV, v_full + st, 0, j0, zs * C::VCH, bkv);
+        ++nv;
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(q_full, 0);
+        drain_ring(k_full, NS, nk);
+        drain_ring(v_full, NS, nv);
       }
     }
   } else if (warp == 1) {
@@ -310,6 +320,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(nt - 1);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
     }
   } else if (C::SPLIT && warp >= 2) {
     // ---------------- softmax, two warpgroups per tile (64 columns each) ----------------
@@ -592,6 +605,21 @@ __global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const uint16_t* s
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the device-side timeout path: one thread waits on an mbarrier
+// that nothing arrives on, with a short cycle limit, through the same bounded
+// wait every kernel uses, and latches the timeout in the status word.
+__global__ void __launch_bounds__(32) selftest_timeout_kernel(int* status, long long limit_cycles) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait_limit(&bar, 0, &abort_flag, limit_cycles)) atomicCAS(status, 0, kStatusTimeout);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -606,6 +634,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 }  // namespace
+
+cudaError_t launch_selftest_timeout(int* status, long long limit_cycles, cudaStream_t s) {
+  selftest_timeout_kernel<<<1, 32, 0, s>>>(status, limit_cycles);
+  return cudaGetLastError();
+}
 
 // 3-D fp16 tensor map over [heads, L, D] with a (64 x rows) box, 128-byte swizzle.
 cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int heads, int box_rows) {

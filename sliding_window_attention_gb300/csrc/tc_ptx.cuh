@@ -52,18 +52,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// the wait ran past the cycle limit or `abort` was raised by another thread.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// the wait ran past limit_cycles (raising `abort` for the other threads) or
+// `abort` was raised by another thread.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       *abort = 1;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_limit(bar, parity, abort, kWaitLimitCycles);
 }
 
 // ---- TMA ------------------------------------------------------------------
@@ -347,6 +353,15 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   while (!mbar_try_wait_cl(bar, parity))
     if (clock64() - t0 > kWaitLimitCycles) return false;
   return true;
+}
+
+// Unwinding after a timeout: loads 0 .. issued - 1 of a ring went to slot
+// i % depth and complete on full[i % depth]; a slot holds at most one load in
+// flight (the last one issued into it), so waiting for that load's phase in
+// every slot lets everything still in flight land before shared memory is
+// released.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int depth, int issued) {
+  for (int k = issued - 1; k >= 0 && k >= issued - depth; --k) mbar_wait_drain(full + k % depth, (k / depth) & 1);
 }
 
 // 16 bytes from another CTA's shared memory.

@@ -217,3 +217,21 @@ def test_errors_raise_through_binding():
         swa.forward(q, k, k, 0, 0.125)
     assert ei.value.code == -3
     assert swa.swa_attn_get_status() == 0
+
+
+def test_device_timeout_is_reported_and_context_survives():
+    """A bounded device wait that runs out (a barrier nothing completes)
+    latches SWA_ERR_DEVICE_TIMEOUT in the status word; reading it clears it,
+    and the library keeps working on the same context."""
+    import sliding_window_attention_gb300 as swa
+
+    assert swa.swa_attn_get_status() == 0
+    swa.swa_attn_selftest_timeout()
+    torch.cuda.synchronize()
+    code = swa.swa_attn_get_status()
+    assert code == -11, code
+    assert "timeout" in swa.strerror(code).lower() or "wait" in swa.strerror(code).lower()
+    assert swa.swa_attn_get_status() == 0
+    q, k, v, dO = make_inputs(1, 2, 1, 130, 64, seed=12)
+    got = gpu_fwd_bwd(q, k, v, dO, 0, 0.125)  # asserts a clean status afterwards
+    assert torch.isfinite(got["o"]).all()
