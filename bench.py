@@ -80,8 +80,8 @@ KERNEL_SOURCE = {
     "bwd_dq_simt": "simt_kernels.cu", "fwd_tc": "tc_fwd.cu", "convert_f16": "tc_fwd.cu",
     "bwd_rowstats": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
 }
-# head dim 512: the backward's tensor-core launches come from the cluster kernels
-KERNEL_SOURCE_D512 = {"bwd_dkdv_tc": "tc_bwd512.cu", "bwd_dq_tc": "tc_bwd512.cu"}
+# head dim 512: the tensor-core launches of the forward and backward come from the cluster kernels
+KERNEL_SOURCE_D512 = {"fwd_tc": "tc_fwd512.cu", "bwd_dkdv_tc": "tc_bwd512.cu", "bwd_dq_tc": "tc_bwd512.cu"}
 
 
 def source_digest(kernel: str, D: int = 0) -> str:

@@ -78,8 +78,6 @@ __global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, 
   }
 }
 
-__device__ __forceinline__ bool in_band(int i, int j, int W) { return j <= i && (W == 0 || i - j < W); }
-
 // dK/dV elementwise step for one key row and 32 query columns: P^T (if
 // WANT_P) and dS^T = P^T (dP^T - Delta) (if WANT_DS) as fp16 pairs.  FULL:
 // every column is in the band (no mask code); otherwise columns outside
@@ -128,21 +126,16 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_
 }
 
 // ===========================================================================
-// dK / dV.  MODE: both accumulators in one CTA (head dim <= 128), or, when
-// dK and dV of a 128-key tile do not both fit in the 512 TMEM columns (head
-// dim 256), a dV-only CTA (S^T, P^T, dV) and a dK-only CTA (S^T, dP^T, dS^T,
-// dK) launched as two kernels.
-enum { kModeBoth = 0, kModeDV = 1, kModeDK = 2 };
+// dK / dV for head dim 256.  dK and dV of a 128-key tile do not both fit in
+// the 512 TMEM columns, so a dV-only CTA (S^T, P^T, dV) and a dK-only CTA
+// (S^T, dP^T, dS^T, dK) run as two kernels.  The two elementwise warpgroups
+// take alternate 32-row query steps.
+enum { kModeDV = 0, kModeDK = 1 };
 
 template <int D, int MODE>
 struct KvCfg {
-  static constexpr int BNK = 128;                  // key rows per CTA (MMA M)
-  static constexpr int BM = (D <= 128) ? 64 : 32;  // query rows per step
-  // SPLIT: both elementwise warpgroups take every step, 32 query columns each
-  // (halves the step's latency on the S -> P -> dV/dK chain); otherwise they
-  // take alternate steps
-  static constexpr bool SPLIT = BM == 64;
-  static constexpr int CW = SPLIT ? BM / 2 : BM;  // query columns per warpgroup per step
+  static constexpr int BNK = 128;  // key rows per CTA (MMA M)
+  static constexpr int BM = 32;    // query rows per step
   static constexpr bool NEED_V = MODE != kModeDV;  // dP^T = V dO^T
   static constexpr bool DO_DV = MODE != kModeDK;
   static constexpr bool DO_DK = MODE != kModeDV;
@@ -154,14 +147,13 @@ struct KvCfg {
   static constexpr int RES_BYTES = (NEED_V ? 2 : 1) * KV_BYTES;  // resident K (and V)
   // Q / dO / stats stages: as many as shared memory holds (TMA latency hiding)
   static constexpr int NS = clamp_stages((kSmemMax - 2048 - RES_BYTES) / STAGE_BYTES);
-  // TMEM: dV at 0 and dK at D (both), or the single accumulator at 0
-  static constexpr int DV_COL = 0;
-  static constexpr int DK_COL = (MODE == kModeDK) ? 0 : D;
+  // TMEM: the CTA's one accumulator at column 0
+  static constexpr int DV_COL = 0, DK_COL = 0;
   static constexpr int S_COL = 256, DP_COL = 384;
   static constexpr size_t SMEM_USED = (size_t)RES_BYTES + NS * (size_t)STAGE_BYTES + 1024 + 1024;
   static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert((MODE == kModeBoth ? 2 * D : D) <= 256, "accumulators must fit below the S buffers");
+  static_assert(D == 256, "head dim 256 only (the accumulator fills the columns below the S buffers)");
   static_assert(S_COL + 2 * BM <= DP_COL && DP_COL + 2 * BM <= 512, "TMEM columns");
 };
 
@@ -194,8 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sdp_full = st_empty + NS;      // [2]
   uint64_t* p_full = sdp_full + 2;         // [2]
   uint64_t* acc_done = p_full + 2;         // [1]
-  uint64_t* ldd = acc_done + 1;            // [2] both warpgroups finished reading a buffer
-  uint64_t* mma_drain = ldd + 2;           // [1] every issued MMA finished (before TMEM is released)
+  uint64_t* mma_drain = acc_done + 1;      // [1] every issued MMA finished (before TMEM is released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -218,8 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sdp_full + s, 1);
-      mbar_init(p_full + s, C::SPLIT ? 256 : 128);
-      mbar_init(ldd + s, 256);
+      mbar_init(p_full + s, 128);
     }
     mbar_init(acc_done, 1);
     mbar_init(mma_drain, 1);
@@ -326,9 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
     bool ok = true;
-    constexpr int CW = C::CW;
-    const int cw0 = C::SPLIT ? wg * CW : 0;
-    for (int n = C::SPLIT ? 0 : wg; n < N; n += C::SPLIT ? 1 : 2) {
+    constexpr int CW = BM;
+    for (int n = wg; n < N; n += 2) {
       const int st = n % NS, sb = n & 1;
       const int i0 = (t_lo + n % ntq) * BM;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
@@ -344,24 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + cw0 + c * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
         if (C::NEED_V)
-          tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + cw0 + c * 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+          tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
       }
       tmem_wait_ld();
-      if (C::SPLIT) {
-        // packed fp16 results land on columns the other warpgroup reads: both
-        // finish reading this buffer first (bounded wait, not bar.sync)
-        mbar_arrive(ldd + sb);
-        if (!__all_sync(0xffffffffu, mbar_wait(ldd + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
-      }
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
         const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
-        const int cb = cw0 + c * 32;  // tile-local query column of this chunk
+        const int cb = c * 32;  // tile-local query column of this chunk
         uint32_t pp[16], dd[16];
         if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, lse_s, dl_s, sl2, cb, clo, chi, pp, dd);
         else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, lse_s, dl_s, sl2, cb, clo, chi, pp, dd);
@@ -375,16 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
-      // both accumulators: warpgroup 0 writes dK (scaled), warpgroup 1 writes dV;
-      // one accumulator: each warpgroup writes half of its columns
+      // each warpgroup writes half of the accumulator's columns (dK scaled)
       const bool row_ok = j < g.L;
       const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
-      const bool wr_dk = (MODE == kModeBoth) ? (wg == 0) : (MODE == kModeDK);
+      constexpr bool wr_dk = MODE == kModeDK;
       const uint32_t col = wr_dk ? C::DK_COL : C::DV_COL;
       const float mul = wr_dk ? g.scale : 1.f;
       float* dst = (wr_dk ? p.out0 : p.out1) + off;
-      constexpr int NCH = (MODE == kModeBoth) ? D / 32 : D / 64;  // 32-column chunks per warpgroup
-      const int c0 = (MODE == kModeBoth) ? 0 : wg * NCH;
+      constexpr int NCH = D / 64;  // 32-column chunks per warpgroup
+      const int c0 = wg * NCH;
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
         const int c = c0 + cc;
@@ -735,13 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
-// dQ
+// dQ for head dim 256 (32-row key steps; the two elementwise warpgroups take
+// alternate steps)
 template <int D>
 struct DqCfg {
-  static constexpr int BMQ = 128;                  // query rows per CTA (MMA M)
-  static constexpr int BN = (D <= 128) ? 64 : 32;  // key rows per step
-  static constexpr bool SPLIT = BN == 64;          // see KvCfg
-  static constexpr int CW = SPLIT ? BN / 2 : BN;   // key columns per warpgroup per step
+  static constexpr int BMQ = 128;  // query rows per CTA (MMA M)
+  static constexpr int BN = 32;    // key rows per step
   static constexpr int KCH = D / 64;
   static constexpr int QT_BYTES = BMQ * D * 2;  // Q (or dO) tile
   static constexpr int KV_BYTES = BN * D * 2;   // K (or V) tile
@@ -751,7 +730,7 @@ struct DqCfg {
   static constexpr size_t SMEM_USED = 2 * (size_t)QT_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 + 1024;
   static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(D <= 256, "dQ must fit below the S buffers");
+  static_assert(D == 256, "head dim 256 only (dQ fills the columns below the S buffers)");
 };
 
 template <int D>
@@ -774,8 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sdp_full = kv_empty + NS;   // [2]
   uint64_t* ds_full = sdp_full + 2;     // [2]
   uint64_t* acc_done = ds_full + 2;     // [1]
-  uint64_t* ldd = acc_done + 1;         // [2] both warpgroups finished reading a buffer
-  uint64_t* mma_drain = ldd + 2;           // [1] every issued MMA finished (before TMEM is released)
+  uint64_t* mma_drain = acc_done + 1;   // [1] every issued MMA finished (before TMEM is released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -799,8 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sdp_full + s, 1);
-      mbar_init(ds_full + s, C::SPLIT ? 256 : 128);
-      mbar_init(ldd + s, 256);
+      mbar_init(ds_full + s, 128);
     }
     mbar_init(acc_done, 1);
     mbar_init(mma_drain, 1);
@@ -894,9 +871,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
                                 : make_float2(0.f, 0.f);
     bool ok = true;
-    constexpr int CW = C::CW;
-    const int cw0 = C::SPLIT ? wg * CW : 0;
-    for (int n = C::SPLIT ? 0 : wg; n < nt; n += C::SPLIT ? 1 : 2) {
+    constexpr int CW = BN;
+    for (int n = wg; n < nt; n += 2) {
       const int sb = n & 1;
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
@@ -908,21 +884,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + cw0 + c * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + cw0 + c * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
+        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
       }
       tmem_wait_ld();
-      if (C::SPLIT) {  // see the dK/dV kernel
-        mbar_arrive(ldd + sb);
-        if (!__all_sync(0xffffffffu, mbar_wait(ldd + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
-      }
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
         const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
-        const int cb = cw0 + c * 32;
+        const int cb = c * 32;
         uint32_t dd[16];
         if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
         else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);

@@ -55,36 +55,30 @@ constexpr int kSmemMax = 232448;  // dynamic shared memory per block on sm_103 (
 template <int D>
 struct FwdCfg {
   // key tile rows: the K (and V) tiles must leave room for >= 2 pipeline stages
-  static constexpr int BN = (D <= 128) ? 128 : (D == 256 ? 64 : 32);
-  // output columns per CTA: all of D, or one 256-column half at D = 512 (O
-  // must fit in TMEM; the two halves each recompute S over the full D)
-  static constexpr int DV = (D <= 256) ? D : 256;
-  static constexpr int NSPLIT = D / DV;
-  static constexpr int NWG = 1;                      // O accumulators
+  static constexpr int BN = (D <= 128) ? 128 : 64;
   static constexpr bool SPLIT = (D <= 128);          // two softmax warpgroups share each tile's columns
   static constexpr int THREADS = 64 + 128 * (SPLIT ? 2 : 1);  // warp 0 TMA, warp 1 MMA, warps 2.. softmax
-  static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks of a Q / K row
-  static constexpr int VCH = DV / 64;               // chunks of the V columns this CTA uses
+  static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks of a Q / K / V row
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int K_BYTES = BN * D * 2;
-  static constexpr int V_BYTES = BN * DV * 2;
-  // mbarriers (512 B), (m, l) exchange ([2][128] float2), row-max exchange
-  // ([2 parity][2 warpgroups][128] float), block of ones (512 B)
+  static constexpr int V_BYTES = BN * D * 2;
+  // mbarriers (512 B), then in split mode the (m, l) exchange ([2][128]
+  // float2) and the row-max exchange ([2 parity][2 warpgroups][128] float),
+  // then a block of ones (512 B)
   static constexpr int XCH_OFF = 512;
-  static constexpr int XM_OFF = XCH_OFF + (SPLIT ? 2048 : 1024);
+  static constexpr int XM_OFF = XCH_OFF + (SPLIT ? 2048 : 0);
   static constexpr int ONES_OFF = XM_OFF + (SPLIT ? 2048 : 0);
   static constexpr int BAR_BYTES = ONES_OFF + 512;
   // as many K/V stages as shared memory holds (TMA latency hiding), 2..8
   static constexpr int NS_FIT = (kSmemMax - 1024 - BAR_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
-  static constexpr int O_COL = 0;                   // O of warpgroup w at [128 w, 128 w + DV)
+  static constexpr int O_COL = 0;                   // O at [0, D)
   static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
   // row sums l = P . 1 accumulated by the tensor core (16 identical columns)
-  static constexpr int L_COL = (DV <= 128) ? 128 : S_COL + 2 * BN;
+  static constexpr int L_COL = (D <= 128) ? 128 : S_COL + 2 * BN;
   static constexpr size_t SMEM = (size_t)Q_BYTES + (size_t)NS * (K_BYTES + V_BYTES) + BAR_BYTES + 1024 /*align*/;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(DV <= 256, "O must fit below the S buffers");
-  static_assert(NWG == 1 || DV <= 128, "two O accumulators must fit below the S buffers");
+  static_assert(D <= 256, "O must fit below the S buffers (head dim 512 has its own kernel)");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
   static_assert(SPLIT || (L_COL + 16 <= 512 && (L_COL >= S_COL + 2 * BN || L_COL + 16 <= S_COL)),
                 "TMEM columns for l");
@@ -107,7 +101,7 @@ struct FwdParams {
 template <int BN, bool FULL>
 __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], float sl2, int clo, int chi) {
   float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-  if (FULL) {
+  if constexpr (FULL) {
     if (sl2 >= 0.f) {
 #pragma unroll
       for (int e = 0; e < BN; e += 4) {
@@ -127,15 +121,16 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
       b3 = fminf(b3, __uint_as_float(sr[e + 3]));
     }
     return fminf(fminf(b0, b1), fminf(b2, b3)) * sl2;
-  }
+  } else {
 #pragma unroll
-  for (int e = 0; e < BN; e += 2) {
-    const float x0 = (e >= clo && e <= chi) ? __uint_as_float(sr[e]) * sl2 : -INFINITY;
-    const float x1 = (e + 1 >= clo && e + 1 <= chi) ? __uint_as_float(sr[e + 1]) * sl2 : -INFINITY;
-    if (e & 2) a1 = fmaxf(a1, fmaxf(x0, x1));
-    else a0 = fmaxf(a0, fmaxf(x0, x1));
+    for (int e = 0; e < BN; e += 2) {
+      const float x0 = (e >= clo && e <= chi) ? __uint_as_float(sr[e]) * sl2 : -INFINITY;
+      const float x1 = (e + 1 >= clo && e + 1 <= chi) ? __uint_as_float(sr[e + 1]) * sl2 : -INFINITY;
+      if (e & 2) a1 = fmaxf(a1, fmaxf(x0, x1));
+      else a0 = fmaxf(a0, fmaxf(x0, x1));
+    }
+    return fmaxf(a0, a1);
   }
-  return fmaxf(a0, a1);
 }
 
 // Pass 2: P = 2^(sl2 * s - m) for the row, rounded to fp16, packed two per
@@ -178,7 +173,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int BN = C::BN, NS = C::NS, KCH = C::KCH, NWG = C::NWG, DV = C::DV;
+  constexpr int BN = C::BN, NS = C::NS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sQ = base;
@@ -192,8 +187,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint64_t* v_empty = v_full + NS;
   uint64_t* s_full = v_empty + NS;  // [2]
   uint64_t* p_full = s_full + 2;    // [2]
-  uint64_t* o_done = p_full + 2;    // [NWG]: PV into O of warpgroup w complete
-  uint64_t* mx_bar = o_done + NWG;  // [2]: both warpgroups posted their partial row max (split mode)
+  uint64_t* o_done = p_full + 2;    // [1]: PV into O complete
+  uint64_t* mx_bar = o_done + 1;    // [2]: both warpgroups posted their partial row max (split mode)
   uint64_t* mma_drain = mx_bar + 2;  // [1] every issued MMA finished (before TMEM is released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -205,7 +200,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32;
   const int bh = blockIdx.x;  // b * Hq + h
-  const int zs = blockIdx.z;  // which DV-column slice of O (and V) this CTA computes
   const int b = bh / g.Hq, h = bh - b * g.Hq;
   const int bkv = b * g.Hkv + h / g.G;
   const int qt = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first
@@ -228,7 +222,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(s_full + s, 1);
       mbar_init(p_full + s, C::SPLIT ? 256 : 128);
     }
-    for (int w = 0; w < NWG; ++w) mbar_init(o_done + w, 1);
+    mbar_init(o_done, 1);
     for (int s = 0; s < 2; ++s) mbar_init(mx_bar + s, 256);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
@@ -263,7 +257,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         ++nk;
         if (n >= NS && !mbar_wait(v_empty + st, par, abort_flag)) break;
         mbar_arrive_expect_tx(v_full + st, C::V_BYTES);
-        tma_load_4d(sV + st * C::V_BYTES, &tmV, v_full + st, 0, j0, zs * C::VCH, bkv);
+        tma_load_4d(sV + st * C::V_BYTES, &tmV, v_full + st, 0, j0, 0, bkv);
         ++nv;
       }
       if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
@@ -276,7 +270,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // ---------------- MMA issuer ----------------
     if (elect_one()) {
       const uint32_t idS = idesc_f16(kBM, BN, 0, 0, 0, 0);   // Q (K-major) x K (K-major)
-      const uint32_t idPV = idesc_f16(kBM, DV, 0, 0, 0, 1);  // P (TMEM) x V (MN-major)
+      const uint32_t idPV = idesc_f16(kBM, D, 0, 0, 0, 1);   // P (TMEM) x V (MN-major)
       const uint32_t idL = idesc_f16(kBM, 16, 0, 0, 0, 0);   // P (TMEM) x ones (K-major)
       const uint64_t ones_desc = smem_desc_noswz(smem_u32(ones), 128, 256);
       const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
@@ -290,16 +284,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bdesc = desc_add(vdesc, ks * 2048);
-          mma_ts(tmem + C::O_COL + 128 * (m % NWG), tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV,
-                 (m >= NWG || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + C::O_COL, tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV, (m > 0 || ks > 0) ? 1u : 0u);
         }
         // l += P . 1: every 16 x 16 step reads the same block of ones
         if constexpr (!C::SPLIT) {
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
-            mma_ts(tmem + C::L_COL, tmem + C::S_COL + sb * BN + ks * 8, ones_desc, idL, (m >= NWG || ks > 0) ? 1u : 0u);
+            mma_ts(tmem + C::L_COL, tmem + C::S_COL + sb * BN + ks * 8, ones_desc, idL, (m > 0 || ks > 0) ? 1u : 0u);
         }
-        mma_commit(o_done + (m % NWG));
+        mma_commit(o_done);
         mma_commit(v_empty + st);
         return true;
       };
@@ -379,13 +372,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       if (__any_sync(0xffffffffu, rescale) && n > 0) {
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c) {  // this warpgroup's half of the O columns
+        for (int c = 0; c < D / 64; ++c) {  // this warpgroup's half of the O columns
           uint32_t rr[32];
-          tmem_ld32(tmem + lane_off + C::O_COL + wg * (DV / 2) + c * 32, rr);
+          tmem_ld32(tmem + lane_off + C::O_COL + wg * (D / 2) + c * 32, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st32(tmem + lane_off + C::O_COL + wg * (DV / 2) + c * 32, rr);
+          tmem_st32(tmem + lane_off + C::O_COL + wg * (D / 2) + c * 32, rr);
         }
       }
       tmem_wait_st();
@@ -403,10 +396,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const float l_tot = ml_x[r].y + ml_x[128 + r].y;
       const bool row_ok = i < g.L;
       const float inv = 1.f / l_tot;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D + zs * DV;
+      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
 #pragma unroll
-      for (int cc = 0; cc < DV / 64; ++cc) {
-        const int c = wg * (DV / 64) + cc;
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = wg * (D / 64) + cc;
         uint32_t acc[32];
         tmem_ld32(tmem + lane_off + C::O_COL + c * 32, acc);
         tmem_wait_ld();  // warp-collective: every lane loads, only valid rows store
@@ -418,20 +411,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                             __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
         }
       }
-      if (row_ok && wg == 0 && zs == 0) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
+      if (row_ok && wg == 0) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
     }
   } else if (warp >= 2) {
-    // ---------------- softmax / correction / epilogue ----------------
-    const int wg = (warp - 2) >> 2;  // takes key tiles n with n % NWG == wg, into its own O
+    // ---------------- softmax / correction / epilogue (one warpgroup) ----------------
     const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t o_col = C::O_COL + 128 * wg;
     const float sl2 = g.scale * kLog2e;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY;
     bool ok = true;
-    int k = 0;  // tiles this warpgroup has processed
-    for (int n = wg; n < nt; n += NWG, ++k) {
+    for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
@@ -465,20 +455,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // has observed every earlier PV completion, so the o_done phase can be at
       // most one ahead of the parity asked for (no aliasing of phase n-3 with
       // n-1), and a rescale never overlaps an in-flight PV.
-      if (k > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done + wg, (k - 1) & 1, abort_flag))) { ok = false; break; }
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) { ok = false; break; }
         tc_fence_after();
       }
       // tcgen05.ld/st are warp-collective: the whole warp rescales if any row needs it
-      if (__any_sync(0xffffffffu, rescale) && k > 0) {
+      if (__any_sync(0xffffffffu, rescale) && n > 0) {
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
-          tmem_ld32(tmem + lane_off + o_col + c * 32, rr);
+          tmem_ld32(tmem + lane_off + C::O_COL + c * 32, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st32(tmem + lane_off + o_col + c * 32, rr);
+          tmem_st32(tmem + lane_off + C::O_COL + c * 32, rr);
         }
         {
           uint32_t lr[16];
@@ -493,64 +483,32 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(p_full + sb);
     }
-    // this warpgroup's O is final once its last PV completes (k tiles processed)
-    if (ok && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done + wg, (k - 1) & 1, abort_flag));
-    // merge the per-warpgroup softmax states: m = max(m_w), l = sum_w l_w 2^(m_w - m),
-    // O = sum_w O_w 2^(m_w - m) / l.  Each warpgroup writes half of the columns.
-    {
+    // O and l are final once the last PV completes
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nt - 1) & 1, abort_flag));
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    if (ok) {
+      tc_fence_after();
       uint32_t lr[16];
       tmem_ld16(tmem + lane_off + C::L_COL, lr);  // warp-collective
       tmem_wait_ld();
-      l_run = (k > 0) ? __uint_as_float(lr[0]) : 0.f;
-    }
-    ml_x[wg * 128 + r] = make_float2(m_run, l_run);
-    tc_fence_before();
-    if (NWG == 2) asm volatile("bar.sync 1, 256;" ::: "memory");
-    else asm volatile("bar.sync 1, 128;" ::: "memory");
-    tc_fence_after();
-    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-    if (ok) {
-      float m_tot = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NWG; ++w) m_tot = fmaxf(m_tot, ml_x[w * 128 + r].x);
-      float f[NWG];
-      float l_tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < NWG; ++w) {
-        const float2 x = ml_x[w * 128 + r];
-        f[w] = (x.x == -INFINITY) ? 0.f : fast_exp2(x.x - m_tot);
-        l_tot += x.y * f[w];
-      }
+      const float l_tot = __uint_as_float(lr[0]);
       const bool row_ok = i < g.L;
       const float inv = 1.f / l_tot;
+      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
 #pragma unroll
-      for (int w = 0; w < NWG; ++w) f[w] *= inv;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D + zs * DV;
-      constexpr int CPW = DV / 32 / NWG;  // 32-column chunks written per warpgroup
-#pragma unroll
-      for (int cc = 0; cc < CPW; ++cc) {
-        const int c = wg * CPW + cc;
-        uint32_t acc[NWG][32];
-#pragma unroll
-        for (int w = 0; w < NWG; ++w) tmem_ld32(tmem + lane_off + C::O_COL + 128 * w + c * 32, acc[w]);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, acc);
         tmem_wait_ld();  // warp-collective: every lane loads, only valid rows store
         if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float t = 0.f;
-#pragma unroll
-              for (int w = 0; w < NWG; ++w)  // skip a state with no keys: its TMEM O was never written
-                t = (f[w] == 0.f) ? t : fmaf(__uint_as_float(acc[w][e + u]), f[w], t);
-              v[u] = t;
-            }
-            *reinterpret_cast<float4*>(orow + c * 32 + e) = make_float4(v[0], v[1], v[2], v[3]);
-          }
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                make_float4(__uint_as_float(acc[e]) * inv, __uint_as_float(acc[e + 1]) * inv,
+                            __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
         }
       }
-      if (row_ok && wg == 0 && zs == 0) p.lse[(size_t)bh * g.L + i] = (m_tot + log2f(l_tot)) * kLn2;
+      if (row_ok) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
     }
   }
 
@@ -705,10 +663,10 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
-  // one TMA instruction per tile: Q, K in all D / 64 chunks, V in the DV / 64 this CTA uses
+  // one TMA instruction per tile: Q, K and V in all D / 64 chunks
   if ((e = make_tmap_f16_chunks(&tq, q16, D, g.L, g.B * g.Hq, kBM, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::VCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   auto kern = fwd_tc_kernel<D>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
     return e;
@@ -718,7 +676,7 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   p.lse = lse;
   p.status = status;
   p.n_qtiles = (g.L + kBM - 1) / kBM;
-  dim3 grid(g.B * g.Hq, p.n_qtiles, C::NSPLIT);
+  dim3 grid(g.B * g.Hq, p.n_qtiles);
   kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
