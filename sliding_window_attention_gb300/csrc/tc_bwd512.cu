@@ -5,7 +5,7 @@
 // tile (128 KB each in fp16) do not fit one SM's shared memory together.  So
 // the work of one tile is split by role across the CTAs of a cluster, each on
 // its own SM:
-//   producers (ranks 0 and 1, alternate steps): the resident A operand of
+//   producers (ranks 0 .. NP - 1, taking steps in turn): the resident A operand of
 //     S lives in Tensor Memory (K for dK/dV, Q for dQ: 128 x 512 fp16 = 256
 //     columns, read by TS-form MMAs), the resident A operand of dP in shared
 //     memory (V, or dO); the streamed tiles come in 64-column slices.  They
@@ -14,17 +14,21 @@
 //     backward)", section 6: recompute P from the stored lse), and
 //     bulk-copy the fp16 tiles into the accumulator CTAs' operand slots;
 //   accumulators hold one full 128 x 512 fp32 accumulator in Tensor Memory:
-//     dK/dV pass (4-CTA cluster per kv head and 128-row key tile, every query
-//       head of the group and query tile in band):  rank 2  dV += P^T dO,
-//       rank 3  dK += dS^T Q;
-//     dQ pass (3-CTA cluster per query head and query tile):  rank 2
+//     dK/dV pass (NP + 2 CTAs per kv head and 128-row key tile, every query
+//       head of the group and query tile in band):  rank NP  dV += P^T dO,
+//       rank NP + 1  dK += dS^T Q;
+//     dQ pass (NP + 1 CTAs per query head and query tile):  rank NP
 //       dQ += dS K.
 // Only tiles that meet the causal / window band are visited ("Lab 028 lab
 // detail: Off NVIDIA, you fix the platform yourself", "What I changed, in
-// plain terms" items 3-4).  A producer issues 2 x 2048 MMA cycles per step
-// and takes every other step; an accumulator issues 2048 per step: the SMs
-// of a cluster carry equal MMA work, and a producer moves at most two 32 KB
-// tiles per step over distributed shared memory (bulk copies).
+// plain terms" items 3-4).  A producer issues 2 x 2048 MMA cycles per own
+// step and takes one step in NP; an accumulator issues 2048 per step.  A
+// producer's own step takes about 11,000 cycles (shared-memory traffic of
+// about 700 KB per own step, TMA issue and the copies), so three producers
+// (NP = 3: 5-CTA dK/dV and 4-CTA dQ clusters) keep the accumulators busier
+// than two, despite the SMs lost to cluster packing.  A producer moves one
+// (dQ) or two (dK/dV) 32 KB tiles per own step over distributed shared
+// memory (bulk copies).
 //
 // Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-9 elementwise (two
 // warpgroups, 64 of the 128 columns each; a warpgroup stages its 64-column
@@ -47,7 +51,7 @@ namespace {
 using namespace tc;
 
 constexpr int kDirKV = 0, kDirQ = 1;
-constexpr int kRoleProd = 0, kRoleAccP = 2, kRoleAccDS = 3;
+constexpr int kRoleProd = 0, kRoleAccP = 1, kRoleAccDS = 2;
 constexpr int T = 128;     // tile rows on both sides (MMA M and N)
 constexpr int DH = 512;    // head dim
 constexpr int kThr = 352;  // 11 warps
@@ -59,15 +63,24 @@ constexpr int TILE_BYTES = T * T * 2;  // fp16 128 x 128 operand tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // one warpgroup's 64-column half (one swizzle chunk)
 constexpr int NR_P = 4;                // producer ring of 64-column slices
 constexpr int SLOT_P = T * 64 * 2;
-constexpr int NR_ACC = 5;              // accumulator ring of 128-column chunks
-constexpr int SLOT_ACC = T * 128 * 2;
+constexpr int SLOT_ACC = T * 128 * 2;  // accumulator ring of 128-column chunks
 constexpr int OFF_STG = RES_BYTES;     // producer: two staging halves
 constexpr int OFF_RING_P = RES_BYTES + 2 * HALF_BYTES;
 constexpr int OFF_RECV = 0;            // accumulator: one operand slot per producer
-constexpr int OFF_RING_ACC = 2 * TILE_BYTES;
 constexpr int DATA_P = OFF_RING_P + NR_P * SLOT_P;
-constexpr int DATA_ACC = OFF_RING_ACC + NR_ACC * SLOT_ACC;
-constexpr int DATA_BYTES = DATA_P > DATA_ACC ? DATA_P : DATA_ACC;
+constexpr int kMaxNP = 3;
+constexpr int kMaxRing = 5;
+// accumulator layout for NP producers: NP operand slots, then as deep a ring
+// as the producers' footprint allows
+template <int NP>
+struct AccLayout {
+  static constexpr int OFF_RING = NP * TILE_BYTES;
+  static constexpr int NR = (DATA_P - OFF_RING) / SLOT_ACC;
+  static_assert(NR >= 2 && NR <= kMaxRing, "accumulator ring");
+};
+constexpr int DATA_BYTES = DATA_P;
+static_assert(AccLayout<2>::OFF_RING + AccLayout<2>::NR * SLOT_ACC <= DATA_BYTES, "accumulator footprint");
+static_assert(AccLayout<3>::OFF_RING + AccLayout<3>::NR * SLOT_ACC <= DATA_BYTES, "accumulator footprint");
 // producer Tensor Memory: resident S operand, S, dP
 constexpr uint32_t X_COL = 0, S_COL = 256, DP_COL = 384;
 
@@ -76,20 +89,20 @@ constexpr uint32_t X_COL = 0, S_COL = 256, DP_COL = 384;
 // waiter.
 struct Bars {
   uint64_t res_full, x_ready;
-  uint64_t ring_full[5], ring_empty[5];
+  uint64_t ring_full[kMaxRing], ring_empty[kMaxRing];
   uint64_t t_full, t_free;      // (producer) S and dP in TMEM / read by the elementwise warps
   uint64_t staged[2];           // (producer) a warpgroup wrote its staging half
   uint64_t stg_free[2];         // (producer) the copy out of a staging half landed
   uint64_t dst_free[2];         // (producer) accumulator slot may be written: [0] P -> dV, [1] dS -> dK / dQ
-  uint64_t recv_full[2];        // (accumulator) tile from producer 0 / 1 landed
-  uint64_t mma_done[2];         // (accumulator) MMAs of a producer's step finished
+  uint64_t recv_full[kMaxNP];   // (accumulator) tile from producer 0 .. NP - 1 landed
+  uint64_t mma_done[kMaxNP];    // (accumulator) MMAs of a producer's step finished
   uint64_t acc_done, mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
   int n_sent[2][2];             // (producer) steps copied to [dV, dK / dQ] by warpgroup [0, 1]
   int n_recv;                   // (accumulator) tiles received
 };
-static_assert(NR_P <= 5 && NR_ACC <= 5, "ring barriers");
+static_assert(NR_P <= kMaxRing, "ring barriers");
 
 constexpr size_t SMEM = (size_t)DATA_BYTES + 1024 + 1024;
 static_assert(SMEM <= 232448, "shared memory");
@@ -159,12 +172,14 @@ __device__ __forceinline__ void ds_tile64(const uint32_t (&pv)[64], const uint32
   }
 }
 
-template <int DIR>
+template <int DIR, int NP>
 __global__ void __launch_bounds__(kThr, 1)
     bwd512_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const Params512 p) {
-  constexpr uint32_t R = (DIR == kDirKV) ? 4 : 3;  // CTAs per cluster
+  constexpr uint32_t R = NP + ((DIR == kDirKV) ? 2 : 1);  // CTAs per cluster
+  constexpr int NR_ACC = AccLayout<NP>::NR;
+  constexpr int OFF_RING_ACC = AccLayout<NP>::OFF_RING;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(base + DATA_BYTES);
@@ -174,7 +189,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const int role = rank < 2 ? kRoleProd : ((DIR == kDirKV && rank == 2) ? kRoleAccP : kRoleAccDS);
+  const int role = rank < (uint32_t)NP ? kRoleProd : ((DIR == kDirKV && rank == (uint32_t)NP) ? kRoleAccP : kRoleAccDS);
   const bool acc_role = role != kRoleProd;
   // Grid (x, y, z) = (CTAs per cluster [x query heads of the group, dQ pass],
   // tiles, b * Hkv + kv head).  Blocks launch x fastest and z slowest, so the
@@ -214,15 +229,15 @@ __global__ void __launch_bounds__(kThr, 1)
     if (DIR == kDirKV) return b * g.Hq + (head - b * g.Hkv) * g.G + n % g.G;  // query head
     return bkv_z;                                                              // kv head
   };
-  // a producer takes steps n = rank, rank + 2, ...; m-th own step = rank + 2m
-  const int n_own = role == kRoleProd ? (N - (int)rank + 1) / 2 : 0;
+  // a producer takes steps n = rank, rank + NP, ...; m-th own step = rank + NP m
+  const int n_own = role == kRoleProd ? max(0, (N - (int)rank + NP - 1) / NP) : 0;
   // accumulator: which of the producer's two destinations this CTA is
   const int dst_kind = (role == kRoleAccP) ? 0 : 1;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->res_full, 1);
     mbar_init(&bars->x_ready, 256);
-    for (int s = 0; s < 5; ++s) {
+    for (int s = 0; s < kMaxRing; ++s) {
       mbar_init(&bars->ring_full[s], 1);
       mbar_init(&bars->ring_empty[s], 1);
     }
@@ -232,9 +247,11 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&bars->staged[s], 128);
       mbar_init(&bars->stg_free[s], 1);
       mbar_init(&bars->dst_free[s], 1);
+      bars->n_sent[s][0] = bars->n_sent[s][1] = 0;
+    }
+    for (int s = 0; s < kMaxNP; ++s) {
       mbar_init(&bars->recv_full[s], 1);
       mbar_init(&bars->mma_done[s], 1);
-      bars->n_sent[s][0] = bars->n_sent[s][1] = 0;
     }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_drain, 1);
@@ -269,7 +286,7 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_arrive_expect_tx(&bars->res_full, RES_BYTES);
         for (int c = 0; c < DH / 64; ++c) tma_load_3d(base + c * T * 128, mres, &bars->res_full, c * 64, r0, head);
         for (int m = 0; ok && m < n_own; ++m) {
-          const int n = (int)rank + 2 * m;
+          const int n = (int)rank + NP * m;
           const int rows = step_rows(n), hd = step_head(n);
           for (int k = 0; k < 2 * (DH / 64); ++k, ++issued) {
             const int s = issued % NR_P;
@@ -352,15 +369,12 @@ __global__ void __launch_bounds__(kThr, 1)
         const uint32_t idA = idesc_f16(T, 128, 0, 0, 0, 1);  // A K-major (fp16 tile), B MN-major
         int used = 0;
         for (int n = 0; ok && n < N; ++n) {
-          const int s2 = n & 1;  // producer of step n, and its slot
-          if (!mbar_wait_cl(&bars->recv_full[s2], (n >> 1) & 1, abort_flag, R)) {
+          const int s2 = n % NP;  // producer of step n, and its slot
+          if (!mbar_wait_cl(&bars->recv_full[s2], (n / NP) & 1, abort_flag, R)) {
             ok = false;
             break;
           }
           bars->n_recv = n + 1;
-          // both staging halves of that producer have been copied out
-          mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[0]), (uint32_t)s2));
-          mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[1]), (uint32_t)s2));
           tc_fence_after();
           const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + s2 * TILE_BYTES, 16, 1024);
           for (int c = 0; c < DH / 128; ++c, ++used) {
@@ -390,14 +404,15 @@ __global__ void __launch_bounds__(kThr, 1)
     // ------------------------------------------------------------ slot release (accumulator roles)
     if (acc_role && elect_one()) {
       // arm each producer's slot for its first step, then re-arm after each step's MMAs
-      for (int s = 0; s < 2 && s < N; ++s) {
+      for (int s = 0; s < NP && s < N; ++s) {
         mbar_arrive_expect_tx(&bars->recv_full[s], TILE_BYTES);
         mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind]), (uint32_t)s));
       }
-      for (int n = 0; n + 2 < N; ++n) {
-        if (!mbar_wait_cl(&bars->mma_done[n & 1], (n >> 1) & 1, abort_flag, R)) break;
-        mbar_arrive_expect_tx(&bars->recv_full[n & 1], TILE_BYTES);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind]), (uint32_t)(n & 1)));
+      for (int n = 0; n + NP < N; ++n) {
+        const int s2 = n % NP;
+        if (!mbar_wait_cl(&bars->mma_done[s2], (n / NP) & 1, abort_flag, R)) break;
+        mbar_arrive_expect_tx(&bars->recv_full[s2], TILE_BYTES);
+        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind]), (uint32_t)s2));
       }
     }
   } else if (!acc_role) {
@@ -461,7 +476,7 @@ __global__ void __launch_bounds__(kThr, 1)
       return true;
     };
     for (int m = 0; m < n_own; ++m) {
-      const int n = (int)rank + 2 * m;
+      const int n = (int)rank + NP * m;
       const int c0 = step_rows(n);  // first column's query (KV) or key (Q)
       const float4 *lse4 = nullptr, *dl4 = nullptr;
       if (DIR == kDirKV) {
@@ -498,13 +513,13 @@ __global__ void __launch_bounds__(kThr, 1)
       uint32_t o[32];
       if (DIR == kDirKV) {
         pack64(sv, o);
-        if (!send(o, 0, 2u, m)) {  // P^T -> dV accumulator
+        if (!send(o, 0, (uint32_t)NP, m)) {  // P^T -> dV accumulator
           ok = false;
           break;
         }
       }
       ds_tile64<DIR == kDirKV>(sv, dv, dl4, rs_row.y, o);
-      if (!send(o, 1, DIR == kDirKV ? 3u : 2u, m)) {  // dS -> dK / dQ accumulator
+      if (!send(o, 1, DIR == kDirKV ? (uint32_t)NP + 1 : (uint32_t)NP, m)) {  // dS -> dK / dQ accumulator
         ok = false;
         break;
       }
@@ -516,6 +531,17 @@ __global__ void __launch_bounds__(kThr, 1)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    if (warp == 2 && elect_one()) {
+      // as soon as a producer's tile has landed, both of its staging halves may
+      // be rewritten: tell it then, not when the MMA thread reaches the step
+      for (int n = 0; n < N; ++n) {
+        const int s2 = n % NP;
+        if (!mbar_wait_cl(&bars->recv_full[s2], (n / NP) & 1, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[0]), (uint32_t)s2));
+        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[1]), (uint32_t)s2));
+      }
+    }
+    __syncwarp();
     if (__all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R))) {
       tc_fence_after();
       const int row = r0 + r;
@@ -554,7 +580,7 @@ __global__ void __launch_bounds__(kThr, 1)
   if (acc_role && threadIdx.x == 0) {
     // unwinding: tiles the producers sent that were never consumed must land
     // before this CTA's shared memory is released
-    for (uint32_t pr = 0; pr < 2; ++pr) {
+    for (uint32_t pr = 0; pr < (uint32_t)NP; ++pr) {
       int sent0, sent1;
       asm volatile("ld.shared::cluster.u32 %0, [%1];"
                    : "=r"(sent0)
@@ -565,9 +591,9 @@ __global__ void __launch_bounds__(kThr, 1)
                    : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][1]), pr))
                    : "memory");
       const int sent = max(sent0, sent1);  // a step with either half in flight
-      // producer pr sent its own steps 0 .. sent - 1, i.e. steps pr + 2 m
+      // producer pr sent its own steps 0 .. sent - 1, i.e. steps pr + NP m
       for (int m = 0; m < sent; ++m) {
-        const int n = (int)pr + 2 * m;
+        const int n = (int)pr + NP * m;
         if (n >= bars->n_recv) mbar_wait_drain(&bars->recv_full[pr], m & 1);
       }
     }
@@ -581,7 +607,7 @@ __global__ void __launch_bounds__(kThr, 1)
   }
 }
 
-template <int DIR>
+template <int DIR, int NP>
 cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                        const uint16_t* g16, const float* stats, int Lpad, float* out0, float* out1, int* status,
                        cudaStream_t s) {
@@ -591,7 +617,7 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
   if ((e = make_tmap_f16(&tg, g16, DH, g.L, g.B * g.Hq, T)) != cudaSuccess) return e;
   if ((e = make_tmap_f16(&tk, k16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
   if ((e = make_tmap_f16(&tv, v16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
-  auto kern = bwd512_kernel<DIR>;
+  auto kern = bwd512_kernel<DIR, NP>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) != cudaSuccess)
     return e;
   Params512 pm;
@@ -603,7 +629,7 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
   pm.Lpad = Lpad;
   pm.n_tiles = (g.L + T - 1) / T;
   pm.status = status;
-  const unsigned R = (DIR == kDirKV) ? 4 : 3;
+  const unsigned R = NP + ((DIR == kDirKV) ? 2 : 1);
   const unsigned xs = (DIR == kDirKV) ? R : R * (unsigned)g.G;  // dQ pass: the group's query heads along x
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(xs, (unsigned)pm.n_tiles, (unsigned)(g.B * g.Hkv));
@@ -625,13 +651,13 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                   const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                   int* status, cudaStream_t s) {
-  return launch_dir<kDirKV>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
+  return launch_dir<kDirKV, 3>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
 }
 
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                 const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                                 cudaStream_t s) {
-  return launch_dir<kDirQ>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s);
+  return launch_dir<kDirQ, 3>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s);
 }
 
 }  // namespace swa
