@@ -10,7 +10,10 @@ header.  This wrapper only builds the shared object, converts inputs to the
 C calling convention and allocates the fp64 outputs.
 
 Inputs may be torch tensors (bf16 or float64, CPU) or numpy arrays (uint16
-holding bf16 bit patterns, or float64), all shaped [B, H, L, D].
+holding bf16 bit patterns, or float64): q and dO shaped [B, Hq, Lq, D], k and
+v [B, Hkv, Lk, D] with Lq <= Lk.  The queries are the last Lq positions of
+the key sequence (Lq = Lk is self-attention).  ``causal=False`` selects the
+non-causal band |i + Lk - Lq - j| < window (no mask at all for window 0).
 """
 from __future__ import annotations
 
@@ -51,11 +54,12 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             L, I, D, P = ctypes.c_long, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
-            lib.swa_oracle_fwd.argtypes = [P, P, P, I, L, L, L, L, L, L, D, I, P, P]
-            lib.swa_oracle_bwd.argtypes = [P, P, P, P, I, L, L, L, L, L, L, D, I, P, P, P, P, P, P, P]
-            lib.swa_oracle_rows.argtypes = [P, P, P, P, I, L, L, L, L, L, L, D, I, L, L, P, L, P, P, P, P]
-            lib.swa_oracle_key_rows.argtypes = [P, P, P, P, I, L, L, L, L, L, L, D, I, L, L, P, L, P, P]
-            for f in (lib.swa_oracle_fwd, lib.swa_oracle_bwd, lib.swa_oracle_rows, lib.swa_oracle_key_rows):
+            lib.swa_oracle_fwd_ex.argtypes = [P, P, P, I, L, L, L, L, L, L, L, I, D, I, P, P]
+            lib.swa_oracle_bwd_ex.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, I, P, P, P, P, P, P, P]
+            lib.swa_oracle_rows_ex.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, I, L, L, P, L, P, P, P, P]
+            lib.swa_oracle_key_rows_ex.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, I, L, L, P, L, P, P]
+            for f in (lib.swa_oracle_fwd_ex, lib.swa_oracle_bwd_ex, lib.swa_oracle_rows_ex,
+                      lib.swa_oracle_key_rows_ex):
                 f.restype = ctypes.c_int
             lib.swa_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -94,58 +98,61 @@ def _prep(q, k, v, dO=None):
     kinds = {a[1] for a in arrs}
     if len(kinds) != 1:
         raise TypeError("q, k, v (and dO) must share one element type")
-    B, Hq, L, D = arrs[0][0].shape
+    B, Hq, Lq, D = arrs[0][0].shape
     Bk, Hkv, Lk, Dk = arrs[1][0].shape
-    if (Bk, Lk, Dk) != (B, L, D) or arrs[2][0].shape != arrs[1][0].shape:
-        raise ValueError("k and v must be [B, Hkv, L, D] matching q's B, L, D")
+    if (Bk, Dk) != (B, D) or Lk < Lq or arrs[2][0].shape != arrs[1][0].shape:
+        raise ValueError("k and v must be [B, Hkv, Lk, D] matching q's B and D, with Lk >= Lq")
     if dO is not None and arrs[3][0].shape != arrs[0][0].shape:
         raise ValueError("dO must have q's shape")
-    return [a[0] for a in arrs], kinds.pop(), (B, Hq, Hkv, L, D)
+    return [a[0] for a in arrs], kinds.pop(), (B, Hq, Hkv, Lq, Lk, D)
 
 
 def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def forward(q, k, v, window: int, scale: float, band_only: bool = False):
-    """Return (o [B,Hq,L,D], lse [B,Hq,L]) in fp64."""
-    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v)
-    o = np.empty((B, Hq, L, D), np.float64)
-    lse = np.empty((B, Hq, L), np.float64)
-    rc = _load().swa_oracle_fwd(*map(_ptr, arrs), f64, B, Hq, Hkv, L, D, int(window), float(scale),
-                                int(band_only), _ptr(o), _ptr(lse))
+def forward(q, k, v, window: int, scale: float, band_only: bool = False, causal: bool = True):
+    """Return (o [B,Hq,Lq,D], lse [B,Hq,Lq]) in fp64."""
+    arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v)
+    o = np.empty((B, Hq, Lq, D), np.float64)
+    lse = np.empty((B, Hq, Lq), np.float64)
+    rc = _load().swa_oracle_fwd_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                   float(scale), int(band_only), _ptr(o), _ptr(lse))
     if rc:
         raise RuntimeError(f"swa_oracle_fwd failed ({rc})")
     return o, lse
 
 
-def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False):
+def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False, causal: bool = True):
     """Return dict with o, lse, delta, dq, dk, dv (fp64) and delta_gap."""
-    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v, dO)
+    arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
     out = dict(
-        o=np.empty((B, Hq, L, D)), lse=np.empty((B, Hq, L)), delta=np.empty((B, Hq, L)),
-        dq=np.empty((B, Hq, L, D)), dk=np.empty((B, Hkv, L, D)), dv=np.empty((B, Hkv, L, D)),
+        o=np.empty((B, Hq, Lq, D)), lse=np.empty((B, Hq, Lq)), delta=np.empty((B, Hq, Lq)),
+        dq=np.empty((B, Hq, Lq, D)), dk=np.empty((B, Hkv, Lk, D)), dv=np.empty((B, Hkv, Lk, D)),
     )
     gap = ctypes.c_double(0.0)
-    rc = _load().swa_oracle_bwd(*map(_ptr, arrs), f64, B, Hq, Hkv, L, D, int(window), float(scale),
-                                int(band_only), *(_ptr(out[n]) for n in ("o", "lse", "delta", "dq", "dk", "dv")),
-                                ctypes.byref(gap))
+    rc = _load().swa_oracle_bwd_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
+                                   float(scale), int(band_only),
+                                   *(_ptr(out[n]) for n in ("o", "lse", "delta", "dq", "dk", "dv")),
+                                   ctypes.byref(gap))
     if rc:
         raise RuntimeError(f"swa_oracle_bwd failed ({rc})")
     out["delta_gap"] = gap.value
     return out
 
 
-def rows(q, k, v, dO, window: int, scale: float, b: int, h: int, row_ids, band_only: bool = False):
+def rows(q, k, v, dO, window: int, scale: float, b: int, h: int, row_ids, band_only: bool = False,
+         causal: bool = True):
     """Selected query rows of head (b, h): dict o [n,D], lse [n], and with dO also delta [n], dq [n,D]."""
-    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v, dO)
+    arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
     ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
     n = ids.size
     out = dict(o=np.empty((n, D)), lse=np.empty(n), delta=np.empty(n), dq=np.empty((n, D)))
     dptr = _ptr(arrs[3]) if dO is not None else None
-    rc = _load().swa_oracle_rows(_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), dptr, f64, B, Hq, Hkv, L, D,
-                                 int(window), float(scale), int(band_only), int(b), int(h), _ptr(ids), n,
-                                 _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["delta"]), _ptr(out["dq"]))
+    rc = _load().swa_oracle_rows_ex(_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), dptr, f64, B, Hq, Hkv, Lq, Lk,
+                                    D, int(window), int(bool(causal)), float(scale), int(band_only), int(b), int(h),
+                                    _ptr(ids), n, _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["delta"]),
+                                    _ptr(out["dq"]))
     if rc:
         raise RuntimeError(f"swa_oracle_rows failed ({rc})")
     if dO is None:
@@ -153,15 +160,16 @@ def rows(q, k, v, dO, window: int, scale: float, b: int, h: int, row_ids, band_o
     return out
 
 
-def key_rows(q, k, v, dO, window: int, scale: float, b: int, kvh: int, key_ids, band_only: bool = False):
+def key_rows(q, k, v, dO, window: int, scale: float, b: int, kvh: int, key_ids, band_only: bool = False,
+             causal: bool = True):
     """Selected key rows of kv head (b, kvh): dict dk [n,D], dv [n,D]."""
-    arrs, f64, (B, Hq, Hkv, L, D) = _prep(q, k, v, dO)
+    arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
     ids = np.ascontiguousarray(np.asarray(key_ids, dtype=np.int64))
     n = ids.size
     out = dict(dk=np.empty((n, D)), dv=np.empty((n, D)))
-    rc = _load().swa_oracle_key_rows(*map(_ptr, arrs), f64, B, Hq, Hkv, L, D, int(window), float(scale),
-                                     int(band_only), int(b), int(kvh), _ptr(ids), n,
-                                     _ptr(out["dk"]), _ptr(out["dv"]))
+    rc = _load().swa_oracle_key_rows_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
+                                        int(bool(causal)), float(scale), int(band_only), int(b), int(kvh),
+                                        _ptr(ids), n, _ptr(out["dk"]), _ptr(out["dv"]))
     if rc:
         raise RuntimeError(f"swa_oracle_key_rows failed ({rc})")
     return out

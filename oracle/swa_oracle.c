@@ -9,11 +9,14 @@
  * library.
  *
  * What it computes is the plain definition, written out with no blocking,
- * fusion or reordering:
+ * fusion or reordering.  There are Lq query rows and Lk >= Lq key rows; the
+ * queries are the last Lq positions of the key sequence, so query i sits at
+ * position a = i + off with off = Lk - Lq (off = 0 for self-attention):
  *
- *   s_ij  = scale * q_i . k_j                         for every key j < L
+ *   s_ij  = scale * q_i . k_j                         for every key j < Lk
  *   s_ij  = -inf  when j is outside band(i)
- *   band(i) = { j : j <= i  and  (W == 0  or  i - j < W) }
+ *   causal:      band(i) = { j : j <= a  and  (W == 0  or  a - j < W) }
+ *   non-causal:  band(i) = { j : W == 0  or  |a - j| < W }
  *   lse_i = m_i + ln sum_j exp(s_ij - m_i),  m_i = max_j s_ij
  *   P_ij  = exp(s_ij - lse_i)                  (exactly 0 outside the band)
  *   o_i   = sum_j P_ij v_j
@@ -27,11 +30,15 @@
  * Passages followed:
  *  - Mask rule: "Lab 028 lab detail: Off NVIDIA, you fix the platform
  *    yourself", "Plan for the build" step 4 (P is zeroed where
- *    j < i + diag_off - window_size + 1, with diag_off = 0 for
- *    self-attention) and "What I changed, in plain terms" item 4 (a key that
- *    is window_size or more positions behind the query's diagonal is
- *    zeroed); causal tiles above the diagonal are skipped ("What the code
- *    says").  A window of 0 is read as plain causal.
+ *    j < i + diag_off - window_size + 1) and "What I changed, in plain
+ *    terms" item 4 (a key that is window_size or more positions from the
+ *    query's diagonal is zeroed); causal tiles above the diagonal are skipped
+ *    ("What the code says", with the diagonal shifted by diag_off).  A window
+ *    of 0 is read as no window.  The same page's item 3 (a non-causal window
+ *    also skips tiles more than window_size ahead) and item 6 (windows tested
+ *    "causal and not", including qL < kL) give the non-causal band and the
+ *    suffix case; item 5(b) says keys behind every query's window get zero
+ *    dK and dV, which the definition below gives (every term is zero).
  *  - Forward writes the logsumexp, the per-row softmax normaliser the
  *    backward reuses: same page, "What I changed, in plain terms" item 1.
  *  - Backward stores the per-row LSE and recomputes P: "Training -- design
@@ -69,9 +76,11 @@
 typedef struct {
     const void *q, *k, *v, *dO;
     int is_f64;               /* 1: fp64 arrays, 0: bf16 bit patterns */
-    long B, Hq, Hkv, L, D, W;
+    long B, Hq, Hkv, Lq, Lk, D, W;
+    int causal;
     double scale;
     int band_only;
+    long off;                 /* Lk - Lq: position of query 0 among the keys */
 } ctx_t;
 
 static double bf16_bits_to_f64(uint16_t bits) {
@@ -86,42 +95,53 @@ static double ld(const ctx_t* c, const void* base, long idx) {
     return bf16_bits_to_f64(((const uint16_t*)base)[idx]);
 }
 
-/* Offset of row i of head h of batch b in a [B, H, L, D] tensor. */
-static long row_off(const ctx_t* c, long b, long h, long H, long i) {
-    return ((b * H + h) * c->L + i) * c->D;
+/* Offset of query-side row i (q, dO, o, dq) of head h of batch b. */
+static long qrow_off(const ctx_t* c, long b, long h, long i) {
+    return ((b * c->Hq + h) * c->Lq + i) * c->D;
 }
 
-/* Key j is visible to query i. */
-static int in_band(long i, long j, long W) {
-    if (j > i) return 0;
-    if (W > 0 && i - j >= W) return 0;
+/* Offset of key-side row j (k, v, dk, dv) of kv head kvh of batch b. */
+static long krow_off(const ctx_t* c, long b, long kvh, long j) {
+    return ((b * c->Hkv + kvh) * c->Lk + j) * c->D;
+}
+
+/* Key j is visible to query i (at position a = i + off). */
+static int in_band(const ctx_t* c, long i, long j) {
+    const long a = i + c->off;
+    if (c->causal) {
+        if (j > a) return 0;
+        if (c->W > 0 && a - j >= c->W) return 0;
+        return 1;
+    }
+    if (c->W > 0 && (a - j >= c->W || j - a >= c->W)) return 0;
     return 1;
 }
 
 /* Range of key positions the row pass visits for query i. */
 static void key_range(const ctx_t* c, long i, long* j0, long* j1) {
-    if (c->band_only) {
-        *j0 = (c->W > 0 && i - c->W + 1 > 0) ? i - c->W + 1 : 0;
-        *j1 = i;
-    } else {
-        *j0 = 0;
-        *j1 = c->L - 1;
-    }
+    *j0 = 0;
+    *j1 = c->Lk - 1;
+    if (!c->band_only) return;
+    const long a = i + c->off;
+    if (c->W > 0 && a - c->W + 1 > 0) *j0 = a - c->W + 1;
+    if (c->causal) *j1 = a;
+    else if (c->W > 0 && a + c->W - 1 < c->Lk - 1) *j1 = a + c->W - 1;
 }
 
-/* Range of query positions the column pass visits for key j. */
+/* Range of query rows the column pass visits for key j (empty if i1 < i0). */
 static void query_range(const ctx_t* c, long j, long* i0, long* i1) {
-    if (c->band_only) {
-        *i0 = j;
-        *i1 = (c->W > 0 && j + c->W - 1 < c->L - 1) ? j + c->W - 1 : c->L - 1;
-    } else {
-        *i0 = 0;
-        *i1 = c->L - 1;
-    }
+    *i0 = 0;
+    *i1 = c->Lq - 1;
+    if (!c->band_only) return;
+    /* positions a that see key j: a >= j (causal) or a >= j - W + 1
+       (non-causal window), and a <= j + W - 1 (any window) */
+    long alo = c->causal ? j : (c->W > 0 ? j - c->W + 1 : c->off);
+    if (alo - c->off > *i0) *i0 = alo - c->off;
+    if (c->W > 0 && j + c->W - 1 - c->off < *i1) *i1 = j + c->W - 1 - c->off;
 }
 
 /*
- * Row pass for query row i of head h (batch b).  s and dp are scratch of L
+ * Row pass for query row i of head h (batch b).  s and dp are scratch of Lk
  * doubles.  Writes o_row[D], *lse; when dO is given also *delta (sum_j P dP),
  * *delta_alt (dO_i . o_i) and, if dq_row is not NULL, dq_row[D].
  */
@@ -130,15 +150,15 @@ static void row_pass(const ctx_t* c, long b, long h, long i, double* s, double* 
                      double* dq_row) {
     const long D = c->D;
     const long kvh = h / (c->Hq / c->Hkv);
-    const long qo = row_off(c, b, h, c->Hq, i);
+    const long qo = qrow_off(c, b, h, i);
     long j0, j1;
     key_range(c, i, &j0, &j1);
 
     /* scores */
     double m = -INFINITY;
     for (long j = j0; j <= j1; ++j) {
-        if (!in_band(i, j, c->W)) { s[j] = -INFINITY; continue; }
-        const long ko = row_off(c, b, kvh, c->Hkv, j);
+        if (!in_band(c, i, j)) { s[j] = -INFINITY; continue; }
+        const long ko = krow_off(c, b, kvh, j);
         double acc = 0.0;
         for (long d = 0; d < D; ++d) acc += ld(c, c->q, qo + d) * ld(c, c->k, ko + d);
         s[j] = c->scale * acc;
@@ -153,16 +173,16 @@ static void row_pass(const ctx_t* c, long b, long h, long i, double* s, double* 
     for (long d = 0; d < D; ++d) o_row[d] = 0.0;
     for (long j = j0; j <= j1; ++j) {
         const double p = exp(s[j] - lse_i);
-        const long vo = row_off(c, b, kvh, c->Hkv, j);
+        const long vo = krow_off(c, b, kvh, j);
         for (long d = 0; d < D; ++d) o_row[d] += p * ld(c, c->v, vo + d);
     }
     if (!c->dO) return;
 
     /* dP, Delta (both forms) */
-    const long go = row_off(c, b, h, c->Hq, i);
+    const long go = qrow_off(c, b, h, i);
     double dl = 0.0;
     for (long j = j0; j <= j1; ++j) {
-        const long vo = row_off(c, b, kvh, c->Hkv, j);
+        const long vo = krow_off(c, b, kvh, j);
         double acc = 0.0;
         for (long d = 0; d < D; ++d) acc += ld(c, c->dO, go + d) * ld(c, c->v, vo + d);
         dp[j] = acc;
@@ -179,31 +199,31 @@ static void row_pass(const ctx_t* c, long b, long h, long i, double* s, double* 
     for (long j = j0; j <= j1; ++j) {
         const double p = exp(s[j] - lse_i);
         const double ds = p * (dp[j] - dl);
-        const long ko = row_off(c, b, kvh, c->Hkv, j);
+        const long ko = krow_off(c, b, kvh, j);
         for (long d = 0; d < D; ++d) dq_row[d] += c->scale * ds * ld(c, c->k, ko + d);
     }
 }
 
 /*
  * Column pass for key row j of kv head kvh (batch b): dk_row[D], dv_row[D].
- * lse and delta are [B, Hq, L] arrays from the row pass; only the rows of
+ * lse and delta are [B, Hq, Lq] arrays from the row pass; only the rows of
  * the group's heads that can see key j are read.
  */
 static void col_pass(const ctx_t* c, long b, long kvh, long j, const double* lse,
                      const double* delta, double* dk_row, double* dv_row) {
     const long D = c->D;
     const long G = c->Hq / c->Hkv;
-    const long ko = row_off(c, b, kvh, c->Hkv, j);
+    const long ko = krow_off(c, b, kvh, j);
     long i0, i1;
     query_range(c, j, &i0, &i1);
     for (long d = 0; d < D; ++d) { dk_row[d] = 0.0; dv_row[d] = 0.0; }
     for (long g = 0; g < G; ++g) {
         const long h = kvh * G + g;
         for (long i = i0; i <= i1; ++i) {
-            const long qo = row_off(c, b, h, c->Hq, i);
-            const long ri = (b * c->Hq + h) * c->L + i;
+            const long qo = qrow_off(c, b, h, i);
+            const long ri = (b * c->Hq + h) * c->Lq + i;
             double s;
-            if (in_band(i, j, c->W)) {
+            if (in_band(c, i, j)) {
                 double acc = 0.0;
                 for (long d = 0; d < D; ++d) acc += ld(c, c->q, qo + d) * ld(c, c->k, ko + d);
                 s = c->scale * acc;
@@ -222,10 +242,17 @@ static void col_pass(const ctx_t* c, long b, long kvh, long j, const double* lse
     }
 }
 
-static int check_shape(long B, long Hq, long Hkv, long L, long D, long W) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || D < 1 || W < 0) return -1;
+static int check_shape(long B, long Hq, long Hkv, long Lq, long Lk, long D, long W) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || D < 1 || W < 0) return -1;
     if (Hq % Hkv != 0) return -1;
     return 0;
+}
+
+static ctx_t make_ctx(const void* q, const void* k, const void* v, const void* dO, int is_f64, long B,
+                      long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal, double scale,
+                      int band_only) {
+    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal ? 1 : 0, scale, band_only, Lk - Lq};
+    return c;
 }
 
 int swa_oracle_num_threads(void) {
@@ -236,17 +263,17 @@ int swa_oracle_num_threads(void) {
 #endif
 }
 
-/* Forward over every row.  o: [B,Hq,L,D], lse: [B,Hq,L]. */
-int swa_oracle_fwd(const void* q, const void* k, const void* v, int is_f64, long B, long Hq,
-                   long Hkv, long L, long D, long W, double scale, int band_only, double* o,
-                   double* lse) {
-    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
-    ctx_t c = {q, k, v, NULL, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
-    const long rows = B * Hq * L;
+/* Forward over every row.  o: [B,Hq,Lq,D], lse: [B,Hq,Lq]. */
+int swa_oracle_fwd_ex(const void* q, const void* k, const void* v, int is_f64, long B, long Hq,
+                      long Hkv, long Lq, long Lk, long D, long W, int causal, double scale,
+                      int band_only, double* o, double* lse) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
+    ctx_t c = make_ctx(q, k, v, NULL, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+    const long rows = B * Hq * Lq;
     int err = 0;
 #pragma omp parallel
     {
-        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
         if (!s) {
 #pragma omp atomic write
             err = -2;
@@ -254,7 +281,7 @@ int swa_oracle_fwd(const void* q, const void* k, const void* v, int is_f64, long
 #pragma omp for schedule(dynamic, 16)
         for (long r = 0; r < rows; ++r) {
             if (!s) continue;
-            const long i = r % L, bh = r / L, h = bh % Hq, b = bh / Hq;
+            const long i = r % Lq, bh = r / Lq, h = bh % Hq, b = bh / Hq;
             row_pass(&c, b, h, i, s, NULL, o + r * D, lse + r, NULL, NULL, NULL);
         }
         free(s);
@@ -263,24 +290,24 @@ int swa_oracle_fwd(const void* q, const void* k, const void* v, int is_f64, long
 }
 
 /*
- * Forward and backward over every row and key.  Outputs o, dq: [B,Hq,L,D];
- * dk, dv: [B,Hkv,L,D]; lse, delta: [B,Hq,L].  *delta_gap receives
+ * Forward and backward over every row and key.  Outputs o, dq: [B,Hq,Lq,D];
+ * dk, dv: [B,Hkv,Lk,D]; lse, delta: [B,Hq,Lq].  *delta_gap receives
  * max_i |sum_j P dP - dO_i . o_i|.
  */
-int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, int is_f64,
-                   long B, long Hq, long Hkv, long L, long D, long W, double scale,
-                   int band_only, double* o, double* lse, double* delta, double* dq,
-                   double* dk, double* dv, double* delta_gap) {
-    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
-    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
-    const long rows = B * Hq * L;
-    const long keys = B * Hkv * L;
+int swa_oracle_bwd_ex(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                      long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
+                      double scale, int band_only, double* o, double* lse, double* delta,
+                      double* dq, double* dk, double* dv, double* delta_gap) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+    const long rows = B * Hq * Lq;
+    const long keys = B * Hkv * Lk;
     double gap = 0.0;
     int err = 0;
 #pragma omp parallel
     {
-        double* s = (double*)malloc(sizeof(double) * (size_t)L);
-        double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);
         double my_gap = 0.0;
         if (!s || !dp) {
 #pragma omp atomic write
@@ -289,7 +316,7 @@ int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, 
 #pragma omp for schedule(dynamic, 16)
         for (long r = 0; r < rows; ++r) {
             if (!s || !dp) continue;
-            const long i = r % L, bh = r / L, h = bh % Hq, b = bh / Hq;
+            const long i = r % Lq, bh = r / Lq, h = bh % Hq, b = bh / Hq;
             double da;
             row_pass(&c, b, h, i, s, dp, o + r * D, lse + r, delta + r, &da, dq + r * D);
             const double g = fabs(delta[r] - da);
@@ -303,7 +330,7 @@ int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, 
     if (err) return err;
 #pragma omp parallel for schedule(dynamic, 16)
     for (long r = 0; r < keys; ++r) {
-        const long j = r % L, bh = r / L, kvh = bh % Hkv, b = bh / Hkv;
+        const long j = r % Lk, bh = r / Lk, kvh = bh % Hkv, b = bh / Hkv;
         col_pass(&c, b, kvh, j, lse, delta, dk + r * D, dv + r * D);
     }
     if (delta_gap) *delta_gap = gap;
@@ -314,20 +341,20 @@ int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, 
  * Selected query rows of one head: o, dq [n, D]; lse, delta [n].
  * dO may be NULL (forward only; delta and dq are then left untouched).
  */
-int swa_oracle_rows(const void* q, const void* k, const void* v, const void* dO, int is_f64,
-                    long B, long Hq, long Hkv, long L, long D, long W, double scale,
-                    int band_only, long b, long h, const long* rows, long n, double* o,
-                    double* lse, double* delta, double* dq) {
-    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
+int swa_oracle_rows_ex(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                       long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
+                       double scale, int band_only, long b, long h, const long* rows, long n,
+                       double* o, double* lse, double* delta, double* dq) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
     if (b < 0 || b >= B || h < 0 || h >= Hq) return -1;
     for (long t = 0; t < n; ++t)
-        if (rows[t] < 0 || rows[t] >= L) return -1;
-    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
+        if (rows[t] < 0 || rows[t] >= Lq) return -1;
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
     int err = 0;
 #pragma omp parallel
     {
-        double* s = (double*)malloc(sizeof(double) * (size_t)L);
-        double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);
         if (!s || !dp) {
 #pragma omp atomic write
             err = -2;
@@ -350,28 +377,32 @@ int swa_oracle_rows(const void* q, const void* k, const void* v, const void* dO,
  * for every query row, of every head in the group, that can see one of the
  * selected keys (lse_i and Delta_i), then the column pass for each key.
  */
-int swa_oracle_key_rows(const void* q, const void* k, const void* v, const void* dO,
-                        int is_f64, long B, long Hq, long Hkv, long L, long D, long W,
-                        double scale, int band_only, long b, long kvh, const long* keys, long n,
-                        double* dk, double* dv) {
-    if (check_shape(B, Hq, Hkv, L, D, W)) return -1;
+int swa_oracle_key_rows_ex(const void* q, const void* k, const void* v, const void* dO,
+                           int is_f64, long B, long Hq, long Hkv, long Lq, long Lk, long D, long W,
+                           int causal, double scale, int band_only, long b, long kvh,
+                           const long* keys, long n, double* dk, double* dv) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
     if (b < 0 || b >= B || kvh < 0 || kvh >= Hkv || n < 1 || !dO) return -1;
-    long jmin = L, jmax = -1;
+    long jmin = Lk, jmax = -1;
     for (long t = 0; t < n; ++t) {
-        if (keys[t] < 0 || keys[t] >= L) return -1;
+        if (keys[t] < 0 || keys[t] >= Lk) return -1;
         if (keys[t] < jmin) jmin = keys[t];
         if (keys[t] > jmax) jmax = keys[t];
     }
-    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, L, D, W, scale, band_only};
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
     const long G = Hq / Hkv;
-    /* query rows that can see any selected key: [jmin, jmax + W - 1] */
-    const long ilo = jmin;
-    const long ihi = (W > 0 && jmax + W - 1 < L - 1) ? jmax + W - 1 : L - 1;
+    /* query rows that can see any selected key (the others add exact zeros) */
+    long ilo, ihi, unused0, unused1;
+    ctx_t cb = c;
+    cb.band_only = 1;
+    query_range(&cb, jmin, &ilo, &unused0);
+    query_range(&cb, jmax, &unused1, &ihi);
+    if (ihi < ilo) { ilo = 0; ihi = -1; }
     const long nr = ihi - ilo + 1;
-    /* lse / delta laid out as full [B, Hq, L] arrays so col_pass can index them */
-    double* lse = (double*)calloc((size_t)(B * Hq * L), sizeof(double));
-    double* delta = (double*)calloc((size_t)(B * Hq * L), sizeof(double));
-    double* obuf = (double*)malloc(sizeof(double) * (size_t)(G * nr * D));
+    /* lse / delta laid out as full [B, Hq, Lq] arrays so col_pass can index them */
+    double* lse = (double*)calloc((size_t)(B * Hq * Lq), sizeof(double));
+    double* delta = (double*)calloc((size_t)(B * Hq * Lq), sizeof(double));
+    double* obuf = (double*)malloc(sizeof(double) * (size_t)((G * nr > 0 ? G * nr : 1) * D));
     if (!lse || !delta || !obuf) {
         free(lse); free(delta); free(obuf);
         return -2;
@@ -379,8 +410,8 @@ int swa_oracle_key_rows(const void* q, const void* k, const void* v, const void*
     int err = 0;
 #pragma omp parallel
     {
-        double* s = (double*)malloc(sizeof(double) * (size_t)L);
-        double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lk);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)Lk);
         if (!s || !dp) {
 #pragma omp atomic write
             err = -2;
@@ -389,7 +420,7 @@ int swa_oracle_key_rows(const void* q, const void* k, const void* v, const void*
         for (long r = 0; r < G * nr; ++r) {
             if (!s || !dp) continue;
             const long g = r / nr, i = ilo + r % nr, h = kvh * G + g;
-            const long ri = (b * Hq + h) * L + i;
+            const long ri = (b * Hq + h) * Lq + i;
             double da;
             row_pass(&c, b, h, i, s, dp, obuf + r * D, lse + ri, delta + ri, &da, NULL);
         }
@@ -404,4 +435,19 @@ int swa_oracle_key_rows(const void* q, const void* k, const void* v, const void*
     free(delta);
     free(obuf);
     return err;
+}
+
+/* Self-attention (Lq = Lk = L), causal: the entry points the tests started with. */
+int swa_oracle_fwd(const void* q, const void* k, const void* v, int is_f64, long B, long Hq,
+                   long Hkv, long L, long D, long W, double scale, int band_only, double* o,
+                   double* lse) {
+    return swa_oracle_fwd_ex(q, k, v, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only, o, lse);
+}
+
+int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                   long B, long Hq, long Hkv, long L, long D, long W, double scale,
+                   int band_only, double* o, double* lse, double* delta, double* dq,
+                   double* dk, double* dv, double* delta_gap) {
+    return swa_oracle_bwd_ex(q, k, v, dO, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only, o, lse,
+                             delta, dq, dk, dv, delta_gap);
 }

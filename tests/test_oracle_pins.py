@@ -300,3 +300,177 @@ def test_sampled_rows_and_keys_match_full(oracle_mod, band):
     kr = oracle_mod.key_rows(q, k, v, dO, window, 0.25, 1, 1, keys, band_only=band)
     for n in ("dk", "dv"):
         assert np.array_equal(kr[n], full[n][1, 1, keys]), n
+
+
+# ---------------------------------------------------------------------------
+# queries that are a suffix of the keys (qL < kL) and non-causal windows
+# ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself", "What I
+# changed, in plain terms" items 3-6: diag_off = kL - qL, windows "causal and
+# not", dK/dV of keys no query reaches)
+
+
+def _torch_reference_ex(q, k, v, dO, window, scale, causal):
+    """Independent path for Lq <= Lk, causal or not: torch fp64 masked softmax
+    + matmul + autograd, with the mask written out from the rule here."""
+    q = q.double().clone().requires_grad_(True)
+    k = k.double().clone().requires_grad_(True)
+    v = v.double().clone().requires_grad_(True)
+    B, Hq, Lq, D = q.shape
+    Lk = k.shape[2]
+    G = Hq // k.shape[1]
+    kr = k.repeat_interleave(G, dim=1)
+    vr = v.repeat_interleave(G, dim=1)
+    s = scale * torch.matmul(q, kr.transpose(-1, -2))
+    a = torch.arange(Lq).view(Lq, 1) + (Lk - Lq)  # the query's position among the keys
+    j = torch.arange(Lk).view(1, Lk)
+    if causal:
+        keep = j <= a
+        if window > 0:
+            keep = keep & (a - j < window)
+    else:
+        keep = torch.ones((Lq, Lk), dtype=torch.bool) if window == 0 else (a - j).abs() < window
+    s = s.masked_fill(~keep, float("-inf"))
+    p = torch.softmax(s, dim=-1)
+    o = torch.matmul(p, vr)
+    lse = torch.logsumexp(s, dim=-1)
+    (o * dO.double()).sum().backward()
+    return dict(o=o.detach(), lse=lse.detach(), dq=q.grad, dk=k.grad, dv=v.grad)
+
+
+def _suffix_inputs(B, Hq, Hkv, Lq, Lk, D, seed):
+    q, k, v, dO = make_inputs(B, Hq, Hkv, Lk, D, seed=seed)
+    return q[:, :, Lk - Lq:].contiguous(), k, v, dO[:, :, Lk - Lq:].contiguous()
+
+
+def test_suffix_mask_matches_pages_rule(oracle_mod):
+    """With V = identity (D = kL), o_i is row i of P; its zero pattern is the mask."""
+    lines = [l.split() for l in open(os.path.join(GOLD, "suffix_mask_q3_k8_w3.txt")) if l.strip() and not l.startswith("#")]
+    window = int(lines[0][1])
+    tables, cur = {}, None
+    for t in lines[1:]:
+        if t[0] == "causal":
+            cur = int(t[1])
+            tables[cur] = []
+        else:
+            tables[cur].append([int(x) for x in t])
+    Lq, Lk = len(tables[1]), len(tables[1][0])
+    q = _rand64((1, 1, Lq, Lk), 41)
+    k = _rand64((1, 1, Lk, Lk), 42)
+    v = torch.eye(Lk, dtype=torch.float64).view(1, 1, Lk, Lk).contiguous()
+    for causal, mask in tables.items():
+        o, _ = oracle_mod.forward(q, k, v, window, 0.3, causal=bool(causal))
+        np.testing.assert_array_equal((o[0, 0] > 0).astype(int), np.array(mask), err_msg=f"causal={causal}")
+
+
+@pytest.mark.parametrize(
+    "B,Hq,Hkv,Lq,Lk,D,window,causal",
+    [(1, 2, 1, 9, 40, 8, 0, True), (2, 4, 2, 17, 33, 8, 5, True), (1, 2, 2, 1, 30, 16, 7, True),
+     (1, 4, 2, 20, 20, 8, 6, False), (1, 2, 1, 13, 41, 8, 0, False), (2, 2, 1, 11, 37, 4, 9, False),
+     (1, 6, 2, 25, 64, 12, 100, False), (1, 3, 1, 5, 50, 8, 3, True)],
+)
+def test_suffix_and_noncausal_match_torch_autograd(oracle_mod, B, Hq, Hkv, Lq, Lk, D, window, causal):
+    q, k, v, dO = _suffix_inputs(B, Hq, Hkv, Lq, Lk, D, seed=300 + Lq + Lk + window)
+    scale = 1.0 / math.sqrt(D)
+    r = oracle_mod.backward(q, k, v, dO, window, scale, causal=causal)
+    ref = _torch_reference_ex(q, k, v, dO, window, scale, causal)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[n], ref[n].numpy(), rtol=1e-10, atol=1e-12, err_msg=n)
+
+
+def test_noncausal_without_window_is_torch_sdpa(oracle_mod):
+    """Non-causal, window 0: plain softmax attention over every key, which is
+    torch's own scaled_dot_product_attention with no mask."""
+    B, Hq, Hkv, Lq, Lk, D = 1, 4, 2, 12, 29, 8
+    q, k, v, dO = _suffix_inputs(B, Hq, Hkv, Lq, Lk, D, seed=51)
+    scale = 0.31
+    o, _ = oracle_mod.forward(q, k, v, 0, scale, causal=False)
+    G = Hq // Hkv
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q.double(), k.double().repeat_interleave(G, 1), v.double().repeat_interleave(G, 1), scale=scale)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("window,causal", [(0, True), (6, True), (0, False), (6, False)])
+def test_suffix_equals_rows_of_full_problem(oracle_mod, window, causal):
+    """Queries that are the last Lq of Lk positions give the same rows as the
+    self-attention problem over all Lk positions; with dO zero on the first
+    Lk - Lq rows, dK and dV agree too (those rows contribute exact zeros)."""
+    B, Hq, Hkv, Lq, Lk, D = 1, 4, 2, 11, 30, 8
+    qf, k, v, dOf = make_inputs(B, Hq, Hkv, Lk, D, seed=61)
+    dOf[:, :, :Lk - Lq] = 0
+    off = Lk - Lq
+    full = oracle_mod.backward(qf, k, v, dOf, window, 0.4, causal=causal)
+    suf = oracle_mod.backward(qf[:, :, off:].contiguous(), k, v, dOf[:, :, off:].contiguous(), window, 0.4,
+                              causal=causal)
+    for n in ("o", "lse", "dq"):
+        np.testing.assert_array_equal(suf[n], full[n][:, :, off:], err_msg=n)
+    np.testing.assert_allclose(suf["dk"], full["dk"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(suf["dv"], full["dv"], rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_keys_no_query_reaches_get_exact_zero_gradient(oracle_mod, causal):
+    """With a window and qL < kL, keys more than window - 1 positions behind
+    the first query's diagonal are seen by no query: dK = dV = 0 exactly
+    ("What I changed, in plain terms" item 5(b))."""
+    B, Hq, Hkv, Lq, Lk, D, W = 1, 2, 1, 4, 40, 8, 5
+    q, k, v, dO = _suffix_inputs(B, Hq, Hkv, Lq, Lk, D, seed=71)
+    r = oracle_mod.backward(q, k, v, dO, W, 0.35, causal=causal)
+    first = (Lk - Lq) - W + 1  # smallest key the first query sees
+    assert np.all(r["dk"][:, :, :first] == 0.0) and np.all(r["dv"][:, :, :first] == 0.0)
+    assert np.any(r["dv"][:, :, first] != 0.0)
+
+
+@pytest.mark.parametrize("window,causal", [(4, True), (0, False), (3, False)])
+def test_suffix_finite_differences(oracle_mod, window, causal):
+    B, Hq, Hkv, Lq, Lk, D = 1, 2, 1, 6, 15, 5
+    q = _rand64((B, Hq, Lq, D), 81)
+    k = _rand64((B, Hkv, Lk, D), 82)
+    v = _rand64((B, Hkv, Lk, D), 83)
+    dO = _rand64((B, Hq, Lq, D), 84)
+    scale = 0.5
+    r = oracle_mod.backward(q, k, v, dO, window, scale, causal=causal)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_mod.forward(qq, kk, vv, window, scale, causal=causal)
+        return float((o * dO.numpy()).sum())
+
+    rng = np.random.default_rng(9)
+    eps = 1e-6
+    for name, grad in (("q", r["dq"]), ("k", r["dk"]), ("v", r["dv"])):
+        base = {"q": q, "k": k, "v": v}
+        t = base[name]
+        for _ in range(10):
+            idx = tuple(int(rng.integers(0, s)) for s in t.shape)
+            plus = t.clone()
+            plus[idx] += eps
+            minus = t.clone()
+            minus[idx] -= eps
+            args_p = dict(base, **{name: plus})
+            args_m = dict(base, **{name: minus})
+            fd = (loss(args_p["q"], args_p["k"], args_p["v"]) - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_suffix_sampled_rows_and_keys_match_full(oracle_mod, causal):
+    B, Hq, Hkv, Lq, Lk, D, W = 1, 4, 2, 19, 45, 8, 7
+    q, k, v, dO = _suffix_inputs(B, Hq, Hkv, Lq, Lk, D, seed=91)
+    full = oracle_mod.backward(q, k, v, dO, W, 0.3, causal=causal)
+    rows = [0, 5, Lq - 1]
+    r = oracle_mod.rows(q, k, v, dO, W, 0.3, 0, 3, rows, band_only=True, causal=causal)
+    np.testing.assert_array_equal(r["o"], full["o"][0, 3, rows])
+    np.testing.assert_array_equal(r["dq"], full["dq"][0, 3, rows])
+    keys = [0, Lk - Lq - W, Lk - Lq - W + 1, 30, Lk - 1]
+    kr = oracle_mod.key_rows(q, k, v, dO, W, 0.3, 0, 1, keys, band_only=True, causal=causal)
+    np.testing.assert_allclose(kr["dk"], full["dk"][0, 1, keys], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(kr["dv"], full["dv"][0, 1, keys], rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_suffix_band_mode_bitwise_equals_full(oracle_mod, causal):
+    q, k, v, dO = _suffix_inputs(1, 2, 1, 21, 52, 8, seed=95)
+    a = oracle_mod.backward(q, k, v, dO, 9, 0.3, band_only=False, causal=causal)
+    b = oracle_mod.backward(q, k, v, dO, 9, 0.3, band_only=True, causal=causal)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[n], b[n], err_msg=n)
