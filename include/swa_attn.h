@@ -53,7 +53,7 @@ typedef uint16_t swa_bf16; /* bf16 bit pattern */
 /* Return codes (0 = success, negative = error). */
 #define SWA_OK 0
 #define SWA_ERR_NULL_POINTER -1   /* a required pointer is NULL */
-#define SWA_ERR_BAD_SHAPE -2      /* B, Hq, Hkv or L < 1 */
+#define SWA_ERR_BAD_SHAPE -2      /* B, Hq, Hkv or L (Lq) < 1, or Lk < Lq */
 #define SWA_ERR_BAD_GROUPS -3     /* Hq is not a multiple of Hkv */
 #define SWA_ERR_BAD_HEAD_DIM -4   /* D not in {64, 128, 256, 512} */
 #define SWA_ERR_BAD_WINDOW -5     /* window < 0 */
@@ -72,6 +72,37 @@ typedef uint16_t swa_bf16; /* bf16 bit pattern */
  * workspace is then accepted).  Pure host function, no CUDA calls.
  */
 size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window);
+
+/*
+ * Queries that are a suffix of the keys, and non-causal windows
+ * ("Lab 028 lab detail", "What I changed, in plain terms" items 3-6 and
+ * "Gradient parity": diag_off = kL - qL, windows "causal and not", and
+ * zero dK/dV for keys that no query's window reaches).
+ *
+ * q and dO are [B, Hq, Lq, D], o is [B, Hq, Lq, D], lse [B, Hq, Lq]; k, v,
+ * dk and dv are [B, Hkv, Lk, D], with 1 <= Lq <= Lk.  Query row i sits at
+ * key position a = i + (Lk - Lq), so Lq = Lk is self-attention and Lq = 1
+ * is one decode step over a cache of Lk keys.  The band of row i is
+ *
+ *   causal != 0:  { j : j <= a  and  (window == 0  or  a - j < window) }
+ *   causal == 0:  { j : window == 0  or  |a - j| < window }
+ *
+ * (causal == 0 with window == 0 is unmasked attention over all Lk keys).
+ * Every row sees at least the key at its own position.  Keys that no query
+ * sees get dk = dv = 0 exactly.  A window of Lk or more is the same as no
+ * window.  Everything else (dtypes, alignment, workspace, streams, status
+ * word, errors) is as for swa_attn_fwd / swa_attn_bwd, which are these
+ * calls with Lq = Lk = L and causal = 1.  Lk < Lq returns SWA_ERR_BAD_SHAPE.
+ */
+size_t swa_attn_fwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal);
+size_t swa_attn_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal);
+int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse,
+                    int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
+int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o,
+                    const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv,
+                    int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Forward.  Reads q [B,Hq,L,D], k and v [B,Hkv,L,D] (bf16); writes

@@ -9,19 +9,24 @@ from ._native import (  # noqa: F401
     SwaError,
     backward,
     bwd_workspace_bytes,
+    bwd_workspace_bytes_ex,
     forward,
     fwd_workspace_bytes,
+    fwd_workspace_bytes_ex,
     load,
     profile_begin,
     profile_end,
     strerror,
     swa_attn_bwd,
+    swa_attn_bwd_ex,
     swa_attn_fwd,
+    swa_attn_fwd_ex,
     swa_attn_get_status,
     swa_attn_selftest_timeout,
 )
 
 __all__ = [
-    "SwaError", "backward", "bwd_workspace_bytes", "forward", "fwd_workspace_bytes", "load", "profile_begin", "profile_end", "strerror",
-    "swa_attn_bwd", "swa_attn_fwd", "swa_attn_get_status", "swa_attn_selftest_timeout",
+    "SwaError", "backward", "bwd_workspace_bytes", "bwd_workspace_bytes_ex", "forward", "fwd_workspace_bytes",
+    "fwd_workspace_bytes_ex", "load", "profile_begin", "profile_end", "strerror", "swa_attn_bwd", "swa_attn_bwd_ex",
+    "swa_attn_fwd", "swa_attn_fwd_ex", "swa_attn_get_status", "swa_attn_selftest_timeout",
 ]

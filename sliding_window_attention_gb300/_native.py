@@ -26,6 +26,10 @@ EXPORTED = (
     "swa_attn_profile_end",
     "swa_attn_bwd_noalloc",
     "swa_attn_selftest_timeout",
+    "swa_attn_fwd_workspace_bytes_ex",
+    "swa_attn_bwd_workspace_bytes_ex",
+    "swa_attn_fwd_ex",
+    "swa_attn_bwd_ex",
 )
 
 _lock = threading.Lock()
@@ -74,6 +78,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.swa_attn_bwd_noalloc.restype = I
         lib.swa_attn_selftest_timeout.argtypes = [P]
         lib.swa_attn_selftest_timeout.restype = I
+        shape_ex = [I, I, I, I, I, I, I, I]  # B, Hq, Hkv, Lq, Lk, D, window, causal
+        lib.swa_attn_fwd_workspace_bytes_ex.argtypes = shape_ex
+        lib.swa_attn_fwd_workspace_bytes_ex.restype = Z
+        lib.swa_attn_bwd_workspace_bytes_ex.argtypes = shape_ex
+        lib.swa_attn_bwd_workspace_bytes_ex.restype = Z
+        lib.swa_attn_fwd_ex.argtypes = [P, P, P, P, P] + shape_ex + [F, P, Z, P]
+        lib.swa_attn_fwd_ex.restype = I
+        lib.swa_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, P] + shape_ex + [F, P, Z, P]
+        lib.swa_attn_bwd_ex.restype = I
         _lib = lib
         return lib
 
@@ -126,6 +139,44 @@ def fwd_workspace_bytes(B, Hq, Hkv, L, D, window) -> int:
 
 def bwd_workspace_bytes(B, Hq, Hkv, L, D, window) -> int:
     return int(load().swa_attn_bwd_workspace_bytes(B, Hq, Hkv, L, D, window))
+
+
+def fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal=True) -> int:
+    return int(load().swa_attn_fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, int(bool(causal))))
+
+
+def bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal=True) -> int:
+    return int(load().swa_attn_bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, int(bool(causal))))
+
+
+def _dims_ex(q, k):
+    B, Hq, Lq, D = q.shape
+    return B, Hq, k.shape[1], Lq, k.shape[2], D
+
+
+def swa_attn_fwd_ex(q, k, v, o, lse, window: int, causal: bool, scale: float, workspace=None, stream=None) -> None:
+    """Forward through the C ABI for q [B,Hq,Lq,D] and k, v [B,Hkv,Lk,D]
+    (Lq <= Lk; the queries are the last Lq key positions); o fp32
+    [B,Hq,Lq,D] and lse fp32 [B,Hq,Lq] are caller-allocated outputs."""
+    B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Lq, Lk, D, int(window),
+                                int(bool(causal)), float(scale), _ptr(workspace), nbytes, _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_fwd_ex")
+
+
+def swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, window: int, causal: bool, scale: float, workspace=None,
+                    stream=None) -> None:
+    """Backward through the C ABI for q, dO [B,Hq,Lq,D] and k, v [B,Hkv,Lk,D];
+    dq, dk, dv are caller-allocated fp32 outputs."""
+    B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)), float(scale),
+                                _ptr(workspace), nbytes, _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_bwd_ex")
 
 
 def swa_attn_fwd(q, k, v, o, lse, window: int, scale: float, workspace=None, stream=None) -> None:
@@ -182,26 +233,35 @@ def _workspace(nbytes, device):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def forward(q, k, v, window: int, scale: float, stream=None):
-    """Return (o fp32, lse fp32) for bf16 CUDA tensors q [B,Hq,L,D], k/v [B,Hkv,L,D]."""
+def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True):
+    """Return (o fp32, lse fp32) for bf16 CUDA tensors q [B,Hq,Lq,D], k/v
+    [B,Hkv,Lk,D] (Lq <= Lk; Lq = Lk and causal is self-attention)."""
     import torch
 
-    B, Hq, Hkv, L, D = _dims(q, k)
-    o = torch.empty((B, Hq, L, D), dtype=torch.float32, device=q.device)
-    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
-    ws = _workspace(fwd_workspace_bytes(B, Hq, Hkv, L, D, window), q.device)
-    swa_attn_fwd(q, k, v, o, lse, window, scale, ws, stream)
+    B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
+    o = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    if Lq == Lk and causal:
+        ws = _workspace(fwd_workspace_bytes(B, Hq, Hkv, Lk, D, window), q.device)
+        swa_attn_fwd(q, k, v, o, lse, window, scale, ws, stream)
+    else:
+        ws = _workspace(fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal), q.device)
+        swa_attn_fwd_ex(q, k, v, o, lse, window, causal, scale, ws, stream)
     return o, lse
 
 
-def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None):
+def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None, causal: bool = True):
     """Return (dq, dk, dv) fp32."""
     import torch
 
-    B, Hq, Hkv, L, D = _dims(q, k)
-    dq = torch.empty((B, Hq, L, D), dtype=torch.float32, device=q.device)
-    dk = torch.empty((B, Hkv, L, D), dtype=torch.float32, device=q.device)
-    dv = torch.empty((B, Hkv, L, D), dtype=torch.float32, device=q.device)
-    ws = _workspace(bwd_workspace_bytes(B, Hq, Hkv, L, D, window), q.device)
-    swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, window, scale, ws, stream)
+    B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
+    dq = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=q.device)
+    dk = torch.empty((B, Hkv, Lk, D), dtype=torch.float32, device=q.device)
+    dv = torch.empty((B, Hkv, Lk, D), dtype=torch.float32, device=q.device)
+    if Lq == Lk and causal:
+        ws = _workspace(bwd_workspace_bytes(B, Hq, Hkv, Lk, D, window), q.device)
+        swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, window, scale, ws, stream)
+    else:
+        ws = _workspace(bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal), q.device)
+        swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, window, causal, scale, ws, stream)
     return dq, dk, dv

@@ -87,8 +87,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int check_shape(int B, int Hq, int Hkv, int L, int D, int window, float scale) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return SWA_ERR_BAD_SHAPE;
+int check_shape(int B, int Hq, int Hkv, int Lq, int L, int D, int window, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || L < Lq) return SWA_ERR_BAD_SHAPE;
   if (Hq % Hkv != 0) return SWA_ERR_BAD_GROUPS;
   if (D != 64 && D != 128 && D != 256 && D != 512) return SWA_ERR_BAD_HEAD_DIM;
   if (window < 0) return SWA_ERR_BAD_WINDOW;
@@ -100,14 +100,20 @@ int check_shape(int B, int Hq, int Hkv, int L, int D, int window, float scale) {
   return SWA_OK;
 }
 
-swa::Geom make_geom(int B, int Hq, int Hkv, int L, int D, int window, float scale) {
+// L = key rows, Lq = query rows (the last Lq key positions)
+swa::Geom make_geom(int B, int Hq, int Hkv, int Lq, int L, int D, int window, int causal, float scale) {
   swa::Geom g;
   g.B = B;
   g.Hq = Hq;
   g.Hkv = Hkv;
   g.L = L;
+  g.Lq = Lq;
+  g.off = L - Lq;
   g.D = D;
-  g.W = (window >= L) ? 0 : window;  // a window of L or more is plain causal
+  // |a - j| <= L - 1 for every query position a and key j, so a window of L
+  // or more masks nothing beyond the causal rule (or nothing at all)
+  g.W = (window >= L) ? 0 : window;
+  g.causal = causal ? 1 : 0;
   g.G = Hq / Hkv;
   g.scale = scale;
   return g;
@@ -122,15 +128,15 @@ struct BwdTcWs {
   size_t stats, q16, k16, v16, g16, total;
   int Lpad;
 };
-BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int L, int D) {
+BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
   BwdTcWs w;
-  w.Lpad = swa::bwd_stats_lpad(L);
+  w.Lpad = swa::bwd_stats_lpad(Lq);
   w.stats = 0;
   w.q16 = round_up((size_t)B * Hq * w.Lpad * 8, 256);
-  w.k16 = w.q16 + round_up((size_t)B * Hq * L * D * 2, 256);
+  w.k16 = w.q16 + round_up((size_t)B * Hq * Lq * D * 2, 256);
   w.v16 = w.k16 + round_up((size_t)B * Hkv * L * D * 2, 256);
   w.g16 = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
-  w.total = w.g16 + round_up((size_t)B * Hq * L * D * 2, 256);
+  w.total = w.g16 + round_up((size_t)B * Hq * Lq * D * 2, 256);
   return w;
 }
 
@@ -138,10 +144,10 @@ BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int L, int D) {
 struct FwdWs {
   size_t q16, k16, v16, total;
 };
-FwdWs fwd_ws_layout(int B, int Hq, int Hkv, int L, int D) {
+FwdWs fwd_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
   FwdWs w;
   w.q16 = 0;
-  w.k16 = w.q16 + round_up((size_t)B * Hq * L * D * 2, 256);
+  w.k16 = w.q16 + round_up((size_t)B * Hq * Lq * D * 2, 256);
   w.v16 = w.k16 + round_up((size_t)B * Hkv * L * D * 2, 256);
   w.total = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
   return w;
@@ -157,10 +163,10 @@ const char* swa_attn_strerror(int code) {
   switch (code) {
     case SWA_OK: return "success";
     case SWA_ERR_NULL_POINTER: return "a required pointer is NULL";
-    case SWA_ERR_BAD_SHAPE: return "B, Hq, Hkv and L must be >= 1";
+    case SWA_ERR_BAD_SHAPE: return "B, Hq, Hkv and Lq must be >= 1, and Lk >= Lq";
     case SWA_ERR_BAD_GROUPS: return "Hq must be a multiple of Hkv";
     case SWA_ERR_BAD_HEAD_DIM: return "head dim D must be 64, 128, 256 or 512";
-    case SWA_ERR_BAD_WINDOW: return "window must be >= 0 (0 = plain causal)";
+    case SWA_ERR_BAD_WINDOW: return "window must be >= 0 (0 = no window)";
     case SWA_ERR_BAD_SCALE: return "scale must be finite";
     case SWA_ERR_MISALIGNED: return "tensors must be 16-byte aligned and the workspace 256-byte aligned";
     case SWA_ERR_WORKSPACE: return "workspace smaller than the size query returned";
@@ -175,53 +181,109 @@ const char* swa_attn_strerror(int code) {
   }
 }
 
-size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
+size_t swa_attn_fwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
   (void)window;
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || !swa::fwd_tc_supported(D)) return 0;
-  return fwd_ws_layout(B, Hq, Hkv, L, D).total;
+  (void)causal;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || !swa::fwd_tc_supported(D)) return 0;
+  return fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
+}
+
+size_t swa_attn_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
+  (void)window;
+  (void)causal;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq) return 0;
+  if (swa::bwd_tc_supported(D)) return bwd_tc_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
+  return bwd_delta_bytes(B, Hq, Lq);
+}
+
+size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
+  return swa_attn_fwd_workspace_bytes_ex(B, Hq, Hkv, L, L, D, window, 1);
 }
 
 size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
-  (void)window;
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1) return 0;
-  if (swa::bwd_tc_supported(D)) return bwd_tc_ws_layout(B, Hq, Hkv, L, D).total;
-  return bwd_delta_bytes(B, Hq, L);
+  return swa_attn_bwd_workspace_bytes_ex(B, Hq, Hkv, L, L, D, window, 1);
+}
+
+int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int D, int window, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return SWA_ERR_NULL_POINTER;
+  int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (rc) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
+      !aligned(workspace, 256))
+    return SWA_ERR_MISALIGNED;
+  const size_t need = swa_attn_fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal);
+  if (workspace_bytes < need || (need > 0 && !workspace)) return SWA_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = status_ptr_for_current_device(&rc);
+  if (!status) return rc;
+  const FwdWs w = fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
+  uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
+  uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+  const uint16_t* src[3] = {q, k, v};
+  uint16_t* dst[3] = {q16, k16, v16};
+  const size_t n[3] = {(size_t)B * Hq * Lq * D, (size_t)B * Hkv * Lk * D, (size_t)B * Hkv * Lk * D};
+  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 3, status, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q16, k16, v16, o, lse, status, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
 }
 
 int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
                  int Hkv, int L, int D, int window, float scale, void* workspace, size_t workspace_bytes,
                  void* stream) {
-  if (!q || !k || !v || !o || !lse) return SWA_ERR_NULL_POINTER;
-  int rc = check_shape(B, Hq, Hkv, L, D, window, scale);
+  return swa_attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, L, L, D, window, 1, scale, workspace, workspace_bytes,
+                         stream);
+}
+
+int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
+                    const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq, int Lk,
+                    int D, int window, int causal, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return SWA_ERR_NULL_POINTER;
+  int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
   if (rc) return rc;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
-      !aligned(workspace, 256))
+      !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
     return SWA_ERR_MISALIGNED;
-  const size_t need = swa_attn_fwd_workspace_bytes(B, Hq, Hkv, L, D, window);
-  if (workspace_bytes < need || (need > 0 && !workspace)) return SWA_ERR_WORKSPACE;
+  const size_t need = swa_attn_bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal);
+  if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
-  const swa::Geom g = make_geom(B, Hq, Hkv, L, D, window, scale);
+  const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (swa::fwd_tc_supported(D)) {
-    int* status = status_ptr_for_current_device(&rc);
-    if (!status) return rc;
-    const FwdWs w = fwd_ws_layout(B, Hq, Hkv, L, D);
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
-    uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
-    uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
-    const uint16_t* src[3] = {q, k, v};
-    uint16_t* dst[3] = {q16, k16, v16};
-    const size_t n[3] = {(size_t)B * Hq * L * D, (size_t)B * Hkv * L * D, (size_t)B * Hkv * L * D};
-    if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 3, status, s); }) != cudaSuccess)
-      return SWA_ERR_CUDA;
-    if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q16, k16, v16, o, lse, status, s); }) !=
-        cudaSuccess)
-      return SWA_ERR_CUDA;
-    return SWA_OK;
-  }
-  if (launch("fwd_simt", s, [&] { return swa::launch_fwd_simt(g, q, k, v, o, lse, s); }) != cudaSuccess)
+  int* status = status_ptr_for_current_device(&rc);
+  if (!status) return rc;
+  const BwdTcWs w = bwd_tc_ws_layout(B, Hq, Hkv, Lq, Lk, D);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  float* stats = reinterpret_cast<float*>(ws + w.stats);
+  uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
+  uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
+  uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
+  uint16_t* g16 = reinterpret_cast<uint16_t*>(ws + w.g16);
+  const uint16_t* src[4] = {q, k, v, dO};
+  uint16_t* dst[4] = {q16, k16, v16, g16};
+  const size_t n[4] = {(size_t)B * Hq * Lq * D, (size_t)B * Hkv * Lk * D, (size_t)B * Hkv * Lk * D,
+                       (size_t)B * Hq * Lq * D};
+  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 4, status, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (launch("bwd_rowstats", s, [&] { return swa::launch_rowstats(g, w.Lpad, o, dO, lse, stats, s); }) !=
+      cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (launch("bwd_dkdv_tc", s, [&] {
+        return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, s);
+      }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (launch("bwd_dq_tc", s, [&] {
+        return swa::launch_bwd_dq_tc(g, q16, k16, v16, g16, stats, w.Lpad, dq, status, s);
+      }) != cudaSuccess)
     return SWA_ERR_CUDA;
   return SWA_OK;
 }
@@ -229,57 +291,8 @@ int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float*
 int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
                  const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int L, int D,
                  int window, float scale, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return SWA_ERR_NULL_POINTER;
-  int rc = check_shape(B, Hq, Hkv, L, D, window, scale);
-  if (rc) return rc;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
-      !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
-    return SWA_ERR_MISALIGNED;
-  const size_t need = swa_attn_bwd_workspace_bytes(B, Hq, Hkv, L, D, window);
-  if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
-  rc = check_device();
-  if (rc) return rc;
-  const swa::Geom g = make_geom(B, Hq, Hkv, L, D, window, scale);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (swa::bwd_tc_supported(D)) {
-    int* status = status_ptr_for_current_device(&rc);
-    if (!status) return rc;
-    const BwdTcWs w = bwd_tc_ws_layout(B, Hq, Hkv, L, D);
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    float* stats = reinterpret_cast<float*>(ws + w.stats);
-    uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
-    uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
-    uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
-    uint16_t* g16 = reinterpret_cast<uint16_t*>(ws + w.g16);
-    const uint16_t* src[4] = {q, k, v, dO};
-    uint16_t* dst[4] = {q16, k16, v16, g16};
-    const size_t n[4] = {(size_t)B * Hq * L * D, (size_t)B * Hkv * L * D, (size_t)B * Hkv * L * D,
-                         (size_t)B * Hq * L * D};
-    if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 4, status, s); }) != cudaSuccess)
-      return SWA_ERR_CUDA;
-    if (launch("bwd_rowstats", s, [&] { return swa::launch_rowstats(g, w.Lpad, o, dO, lse, stats, s); }) !=
-        cudaSuccess)
-      return SWA_ERR_CUDA;
-    if (launch("bwd_dkdv_tc", s, [&] {
-          return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, s);
-        }) != cudaSuccess)
-      return SWA_ERR_CUDA;
-    if (launch("bwd_dq_tc", s, [&] {
-          return swa::launch_bwd_dq_tc(g, q16, k16, v16, g16, stats, w.Lpad, dq, status, s);
-        }) != cudaSuccess)
-      return SWA_ERR_CUDA;
-    return SWA_OK;
-  }
-  float* delta = static_cast<float*>(workspace);
-  if (launch("bwd_delta", s, [&] { return swa::launch_delta(g, o, dO, delta, s); }) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  if (launch("bwd_dkdv_simt", s,
-             [&] { return swa::launch_bwd_dkdv_simt(g, q, k, v, dO, lse, delta, dk, dv, s); }) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  if (launch("bwd_dq_simt", s, [&] { return swa::launch_bwd_dq_simt(g, q, k, v, dO, lse, delta, dq, s); }) !=
-      cudaSuccess)
-    return SWA_ERR_CUDA;
-  return SWA_OK;
+  return swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, L, L, D, window, 1, scale, workspace,
+                         workspace_bytes, stream);
 }
 
 int swa_attn_selftest_timeout(void* stream) {

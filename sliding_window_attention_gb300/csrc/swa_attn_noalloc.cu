@@ -84,6 +84,9 @@ extern "C" int swa_attn_bwd_noalloc(const swa_bf16* q, const swa_bf16* k, const 
   g.Hq = Hq;
   g.Hkv = Hkv;
   g.L = L;
+  g.Lq = L;  // self-attention only
+  g.off = 0;
+  g.causal = 1;
   g.D = D;
   g.W = (window >= L) ? 0 : window;
   g.G = Hq / Hkv;

@@ -9,11 +9,43 @@
 
 namespace swa {
 
-// Problem geometry shared by every kernel.
+// Problem geometry shared by every kernel.  There are Lq query rows and L
+// key rows (Lq <= L); the queries are the last Lq positions of the key
+// sequence, so query row i sits at key position i + off with off = L - Lq
+// (the pages' diag_off; 0 for self-attention).
 struct Geom {
-  int B, Hq, Hkv, L, D, W, G;  // G = Hq / Hkv; W = 0 means plain causal
+  int B, Hq, Hkv, L, D, W, G;  // L = key rows; G = Hq / Hkv; W = 0: no window
+  int Lq, off;                 // query rows, L - Lq
+  int causal;                  // 1: keys after the query's position are masked
   float scale;                 // softmax scale applied to q . k
 };
+
+// The band of query row i is the interval of keys [band_key_lo, band_key_hi]
+// ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself", "Plan
+// for the build" step 4 and "What I changed, in plain terms" items 3-4):
+//   causal:      j <= a and (W == 0 or a - j < W),  a = i + off
+//   non-causal:  W == 0 or |a - j| < W
+// Both ends are non-decreasing in i, and the rows that see key j form the
+// interval [band_q_lo, band_q_hi] (empty when lo > hi).
+__host__ __device__ __forceinline__ int band_key_lo(const Geom& g, int i) {
+  const int lo = i + g.off - g.W + 1;
+  return (g.W > 0 && lo > 0) ? lo : 0;
+}
+__host__ __device__ __forceinline__ int band_key_hi(const Geom& g, int i) {
+  const int a = i + g.off;
+  const int hi = g.causal ? a : (g.W > 0 ? a + g.W - 1 : g.L - 1);
+  return hi < g.L - 1 ? hi : g.L - 1;
+}
+__host__ __device__ __forceinline__ int band_q_lo(const Geom& g, int j) {
+  if (!g.causal && g.W == 0) return 0;
+  const int lo = (g.causal ? j : j - g.W + 1) - g.off;
+  return lo > 0 ? lo : 0;
+}
+__host__ __device__ __forceinline__ int band_q_hi(const Geom& g, int j) {
+  if (g.W == 0) return g.Lq - 1;
+  const int hi = j + g.W - 1 - g.off;
+  return hi < g.Lq - 1 ? hi : g.Lq - 1;
+}
 
 // Device-side status codes latched into the per-device status word.
 enum : int { kStatusOk = 0, kStatusTimeout = -11, kStatusFp16Range = -14 };

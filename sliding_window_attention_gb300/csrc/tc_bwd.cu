@@ -196,10 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
   const int j0 = (int)blockIdx.y * BNK;
   const int jhi = min(j0 + BNK, g.L) - 1;
-  const int ihi = g.W > 0 ? min(g.L - 1, jhi + g.W - 1) : g.L - 1;
-  const int t_lo = j0 / BM, t_hi = ihi / BM;
-  const int ntq = t_hi - t_lo + 1;
+  // query rows that can see a key of this tile
+  const int qlo = band_q_lo(g, j0), qhi = band_q_hi(g, jhi);
+  const int t_lo = qlo / BM, t_hi = qhi / BM;
+  const int ntq = qlo <= qhi ? t_hi - t_lo + 1 : 0;
   const int N = g.G * ntq;  // work items (head of group, query tile)
+  if (N == 0) {
+    // no query sees these keys (queries that are a suffix of the keys, with a
+    // window): their gradients are zero ("Lab 028 lab detail", "What I
+    // changed, in plain terms" item 5(b)).  Uniform over the CTA, before any
+    // barrier or Tensor Memory is set up.
+    zero_rows(MODE == kModeDK ? p.out0 : p.out1, bkv, j0, BNK, g.L, D);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -325,10 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lse * log2e and Delta of this step's query columns
       const float* lse_s = reinterpret_cast<const float*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
       const float* dl_s = lse_s + BM;
-      const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
-      // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
-      const int clo = max(0, j - i0);
-      const int chi = min(min(BM - 1, g.L - 1 - i0), g.W > 0 ? j + g.W - 1 - i0 : BM - 1);
+      const bool full = (i0 >= band_q_lo(g, jhi)) && (i0 + BM - 1 <= band_q_hi(g, j0));
+      // query columns c of this tile that see key j: i0 + c in [band_q_lo(j), band_q_hi(j)]
+      const int clo = band_q_lo(g, j) - i0;
+      const int chi = band_q_hi(g, j) - i0;
       // this warpgroup's S^T / dP^T columns with one TMEM wait
       uint32_t sv[CW], dv[CW];
 #pragma unroll
@@ -472,10 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
   const int j0 = (int)blockIdx.y * BNK;
   const int jhi = min(j0 + BNK, g.L) - 1;
-  const int ihi = g.W > 0 ? min(g.L - 1, jhi + g.W - 1) : g.L - 1;
-  const int t_lo = j0 / BM, t_hi = ihi / BM;
-  const int ntq = t_hi - t_lo + 1;
+  // query rows that can see a key of this tile
+  const int qlo = band_q_lo(g, j0), qhi = band_q_hi(g, jhi);
+  const int t_lo = qlo / BM, t_hi = qhi / BM;
+  const int ntq = qlo <= qhi ? t_hi - t_lo + 1 : 0;
   const int N = g.G * ntq;  // steps (head of group, query tile)
+  if (N == 0) {
+    // no query sees these keys: zero gradients (see dkdv_tc_kernel)
+    zero_rows(p.out0, bkv, j0, BNK, g.L, D);
+    zero_rows(p.out1, bkv, j0, BNK, g.L, D);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -633,10 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(s_read);
-      const bool full = (i0 >= j0 + BNK - 1) && (i0 + BM - 1 < g.L) && (g.W == 0 || i0 + BM - 1 - j0 < g.W);
-      // query columns c of this tile that see key j: i0 + c in [j, min(L - 1, j + W - 1)]
-      const int clo = max(0, j - i0);
-      const int chi = min(min(BM - 1, g.L - 1 - i0), g.W > 0 ? j + g.W - 1 - i0 : BM - 1);
+      const bool full = (i0 >= band_q_lo(g, jhi)) && (i0 + BM - 1 <= band_q_hi(g, j0));
+      // query columns c of this tile that see key j: i0 + c in [band_q_lo(j), band_q_hi(j)]
+      const int clo = band_q_lo(g, j) - i0;
+      const int chi = band_q_hi(g, j) - i0;
       if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
       else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
       // P^T as fp16 pairs (the dV operand); dS below uses the same rounded P
@@ -764,9 +780,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bkv = b * g.Hkv + h / g.G;
   const int qt = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
   const int i0 = qt * BMQ;
-  const int ihi = min(i0 + BMQ, g.L) - 1;
-  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
-  const int t_lo = jlo / BN, t_hi = ihi / BN;
+  const int ihi = min(i0 + BMQ, g.Lq) - 1;
+  // key tiles meeting the band of rows i0 .. ihi (never empty)
+  const int t_lo = band_key_lo(g, i0) / BN, t_hi = band_key_hi(g, ihi) / BN;
   const int nt = t_hi - t_lo + 1;
 
   if (threadIdx.x == 0) {
@@ -867,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
-    const float2 rs = (i < g.L) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
+    const float2 rs = (i < g.Lq) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
                                               p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
                                 : make_float2(0.f, 0.f);
     bool ok = true;
@@ -877,10 +893,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + BMQ - 1 - j0 < g.W);
-      // key columns c of this tile visible to row i: j0 + c in [i - W + 1, i]
-      const int clo = g.W > 0 ? max(0, i - g.W + 1 - j0) : 0;
-      const int chi = min(BN - 1, i - j0);
+      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
+      // key columns c of this tile visible to row i: j0 + c in [band_key_lo(i), band_key_hi(i)]
+      const int clo = band_key_lo(g, i) - j0;
+      const int chi = band_key_hi(g, i) - j0;
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
@@ -905,8 +921,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
       // each warpgroup writes half of the dQ columns
-      const bool row_ok = i < g.L;
-      float* row = p.out0 + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+      const bool row_ok = i < g.Lq;
+      float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
 #pragma unroll
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         uint32_t a[32];
@@ -994,9 +1010,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bkv = b * g.Hkv + h / g.G;
   const int qt = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
   const int i0 = qt * BMQ;
-  const int ihi = min(i0 + BMQ, g.L) - 1;
-  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
-  const int t_lo = jlo / BN, t_hi = ihi / BN;
+  const int ihi = min(i0 + BMQ, g.Lq) - 1;
+  // key tiles meeting the band of rows i0 .. ihi (never empty)
+  const int t_lo = band_key_lo(g, i0) / BN, t_hi = band_key_hi(g, ihi) / BN;
   const int nt = t_hi - t_lo + 1;
 
   if (threadIdx.x == 0) {
@@ -1123,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
-    const float2 rs = (i < g.L) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
+    const float2 rs = (i < g.Lq) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
                                               p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
                                 : make_float2(0.f, 0.f);
     const int cw0 = wg * CW;
@@ -1133,9 +1149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + BMQ - 1 - j0 < g.W);
-      const int clo = g.W > 0 ? max(0, i - g.W + 1 - j0) : 0;  // visible key columns [clo, chi]
-      const int chi = min(BN - 1, i - j0);
+      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
+      const int clo = band_key_lo(g, i) - j0;  // visible key columns [clo, chi]
+      const int chi = band_key_hi(g, i) - j0;
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
@@ -1163,8 +1179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
-      const bool row_ok = i < g.L;
-      float* row = p.out0 + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+      const bool row_ok = i < g.Lq;
+      float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
 #pragma unroll
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {  // each warpgroup writes half the columns
         uint32_t a[32];
@@ -1227,8 +1243,8 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       using C = KvCfg<D, MODE>;
       CUtensorMap tq, tk, tv, tg, ts;
       cudaError_t e2;
-      if ((e2 = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_stats(&ts, stats, Lpad, 2 * g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
@@ -1248,8 +1264,8 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       using C = Kv128Cfg<D>;
       CUtensorMap tq, tk, tv, tg;
       cudaError_t e2;
-      if ((e2 = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
       auto kern = dkdv128_tc_kernel<D>;
@@ -1270,8 +1286,8 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
   } else if constexpr (D <= 128) {
     using C = Dq128Cfg<D>;
     CUtensorMap tq, tk, tv, tg;
-    if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
     if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
     if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
     auto kern = dq128_tc_kernel<D>;
@@ -1279,14 +1295,14 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       return e;
     p.out0 = dq;
     p.out1 = nullptr;
-    p.n_tiles = (g.L + C::BMQ - 1) / C::BMQ;
+    p.n_tiles = (g.Lq + C::BMQ - 1) / C::BMQ;
     dim3 grid(g.B * g.Hq, p.n_tiles);
     kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
   } else {
     using C = DqCfg<D>;
     CUtensorMap tq, tk, tv, tg;
-    if ((e = make_tmap_f16(&tq, q16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tg, g16, D, g.L, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
     if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
     if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
     auto kern = dq_tc_kernel<D>;
@@ -1294,7 +1310,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       return e;
     p.out0 = dq;
     p.out1 = nullptr;
-    p.n_tiles = (g.L + C::BMQ - 1) / C::BMQ;
+    p.n_tiles = (g.Lq + C::BMQ - 1) / C::BMQ;
     dim3 grid(g.B * g.Hq, p.n_tiles);
     kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
   }
@@ -1311,7 +1327,7 @@ cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint1
                             float* stats, cudaStream_t s) {
   const long rows = (long)g.B * g.Hq * Lpad;
   const long blocks = (rows * 32 + 255) / 256;
-  rowstats_kernel<<<(unsigned)blocks, 256, 0, s>>>(g.B * g.Hq, g.L, Lpad, g.D, o, dO, lse, stats);
+  rowstats_kernel<<<(unsigned)blocks, 256, 0, s>>>(g.B * g.Hq, g.Lq, Lpad, g.D, o, dO, lse, stats);
   return cudaGetLastError();
 }
 

@@ -204,18 +204,29 @@ __global__ void __launch_bounds__(kThr, 1)
   const int tile = (DIR == kDirKV) ? (int)blockIdx.y : p.n_tiles - 1 - (int)blockIdx.y;
   const int r0 = tile * T;
   int t_lo, ntq, N;
+  // rows of the resident side, and the last one that exists
+  const int LX = (DIR == kDirKV) ? g.L : g.Lq;
+  const int rlast = min(r0 + T, LX) - 1;
   if (DIR == kDirKV) {
-    const int jhi = min(r0 + T, g.L) - 1;
-    const int ihi = g.W > 0 ? min(g.L - 1, jhi + g.W - 1) : g.L - 1;
-    t_lo = tile;
-    ntq = ihi / T - t_lo + 1;
+    // query rows that can see a key of this tile
+    const int qlo = band_q_lo(g, r0), qhi = band_q_hi(g, rlast);
+    t_lo = qlo / T;
+    ntq = qlo <= qhi ? qhi / T - t_lo + 1 : 0;
     N = g.G * ntq;
   } else {
-    const int ihi = min(r0 + T, g.L) - 1;
-    const int jlo = g.W > 0 ? max(0, r0 - g.W + 1) : 0;
-    t_lo = jlo / T;
-    ntq = ihi / T - t_lo + 1;
+    // key tiles meeting the band of rows r0 .. rlast (never empty)
+    t_lo = band_key_lo(g, r0) / T;
+    ntq = band_key_hi(g, rlast) / T - t_lo + 1;
     N = ntq;
+  }
+  if (N == 0) {
+    // dK/dV pass, and no query sees these keys (queries that are a suffix of
+    // the keys, with a window): zero gradients ("Lab 028 lab detail", "What
+    // I changed, in plain terms" item 5(b)).  Every CTA of the cluster has
+    // the same tile, so all of them leave here, before any cluster barrier.
+    if (role == kRoleAccP) zero_rows(p.out1, head, r0, T, g.L, DH);
+    if (role == kRoleAccDS) zero_rows(p.out0, head, r0, T, g.L, DH);
+    return;
   }
   // streamed-side rows and head of step n.  dK/dV pass: query tiles from the
   // last one down, the group's query heads innermost, so that concurrent
@@ -426,14 +437,14 @@ __global__ void __launch_bounds__(kThr, 1)
     {
       // resident S operand into Tensor Memory: row r, fp16 pairs -> one 32-bit column each;
       // warpgroup wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
-      const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)head * g.L + (row < g.L ? row : 0)) * DH) +
+      const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)head * LX + (row < LX ? row : 0)) * DH) +
                          wg * 32;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = row < g.L ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w4 = row < LX ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
           v[4 * q] = w4.x;
           v[4 * q + 1] = w4.y;
           v[4 * q + 2] = w4.z;
@@ -499,14 +510,14 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive(&bars->t_free);  // S and dP may be overwritten by the next own step
       bool full;
       int clo, chi;
-      if (DIR == kDirKV) {
-        full = (c0 >= r0 + T - 1) && (c0 + T - 1 < g.L) && (g.W == 0 || c0 + T - 1 - r0 < g.W);
-        clo = max(0, row - c0);
-        chi = min(min(T - 1, g.L - 1 - c0), g.W > 0 ? row + g.W - 1 - c0 : T - 1);
-      } else {
-        full = (c0 + T - 1 <= r0) && (g.W == 0 || r0 + T - 1 - c0 < g.W);
-        clo = g.W > 0 ? max(0, row - g.W + 1 - c0) : 0;
-        chi = min(T - 1, row - c0);
+      if (DIR == kDirKV) {  // columns are query rows c0 .. c0 + 127, this thread's row is key `row`
+        full = (c0 >= band_q_lo(g, rlast)) && (c0 + T - 1 <= band_q_hi(g, r0));
+        clo = band_q_lo(g, row) - c0;
+        chi = band_q_hi(g, row) - c0;
+      } else {  // columns are keys c0 .. c0 + 127, this thread's row is query `row`
+        full = (c0 >= band_key_lo(g, rlast)) && (c0 + T - 1 <= band_key_hi(g, r0));
+        clo = band_key_lo(g, row) - c0;
+        chi = band_key_hi(g, row) - c0;
       }
       if (full) p_tile64<true, DIR == kDirKV>(sv, lse4, rs_row.x, sl2, cb0, clo, chi);
       else p_tile64<false, DIR == kDirKV>(sv, lse4, rs_row.x, sl2, cb0, clo, chi);
@@ -545,7 +556,7 @@ __global__ void __launch_bounds__(kThr, 1)
     if (__all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R))) {
       tc_fence_after();
       const int row = r0 + r;
-      const bool row_ok = row < g.L;
+      const bool row_ok = row < LX;
       float* dst;
       float mul;
       if (DIR == kDirKV) {
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(kThr, 1)
         dst = p.out0;
         mul = g.scale;
       }
-      dst += ((size_t)head * g.L + (row_ok ? row : 0)) * DH;
+      dst += ((size_t)head * LX + (row_ok ? row : 0)) * DH;
 #pragma unroll 1
       for (int cc = 0; cc < 8; ++cc) {
         const int c = 256 * wg + 32 * cc;
@@ -613,8 +624,8 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
                        cudaStream_t s) {
   CUtensorMap tq, tk, tv, tg;
   cudaError_t e;
-  if ((e = make_tmap_f16(&tq, q16, DH, g.L, g.B * g.Hq, T)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16(&tg, g16, DH, g.L, g.B * g.Hq, T)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16(&tq, q16, DH, g.Lq, g.B * g.Hq, T)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16(&tg, g16, DH, g.Lq, g.B * g.Hq, T)) != cudaSuccess) return e;
   if ((e = make_tmap_f16(&tk, k16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
   if ((e = make_tmap_f16(&tv, v16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
   auto kern = bwd512_kernel<DIR, NP>;
@@ -627,7 +638,7 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
   pm.x16 = (DIR == kDirKV) ? k16 : q16;
   pm.stats = stats;
   pm.Lpad = Lpad;
-  pm.n_tiles = (g.L + T - 1) / T;
+  pm.n_tiles = ((DIR == kDirKV ? g.L : g.Lq) + T - 1) / T;  // resident-side tiles
   pm.status = status;
   const unsigned R = NP + ((DIR == kDirKV) ? 2 : 1);
   const unsigned xs = (DIR == kDirKV) ? R : R * (unsigned)g.G;  // dQ pass: the group's query heads along x

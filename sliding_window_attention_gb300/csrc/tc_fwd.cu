@@ -204,9 +204,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int bkv = b * g.Hkv + h / g.G;
   const int qt = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first
   const int i0 = qt * kBM;
-  const int ihi = min(i0 + kBM, g.L) - 1;
-  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
-  const int t_lo = jlo / BN, t_hi = ihi / BN;
+  const int ihi = min(i0 + kBM, g.Lq) - 1;
+  // key tiles meeting the band of rows i0 .. ihi (never empty: every row
+  // sees at least the key at its own position)
+  const int t_lo = band_key_lo(g, i0) / BN, t_hi = band_key_hi(g, ihi) / BN;
   const int nt = t_hi - t_lo + 1;
 
   if (threadIdx.x < 128) ones[threadIdx.x] = 0x3C003C00u;  // two fp16 1.0 per word, 512 bytes
@@ -333,15 +334,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + kBM - 1 - j0 < g.W);
+      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
       uint32_t sr[HC];
 #pragma unroll
       for (int c = 0; c < HC / 32; ++c)
         tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + cb0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
       tmem_wait_ld();
       // visible key columns of this row, relative to this warpgroup's half
-      const int clo = ((g.W > 0) ? max(0, i - g.W + 1 - j0) : 0) - cb0;
-      const int chi = min(BN - 1, i - j0) - cb0;
+      const int clo = band_key_lo(g, i) - j0 - cb0;
+      const int chi = band_key_hi(g, i) - j0 - cb0;
       const float pmax = full ? softmax_tile_max<HC, true>(sr, sl2, clo, chi)
                               : softmax_tile_max<HC, false>(sr, sl2, clo, chi);
       // combine the two halves' maxima; after this barrier both warpgroups have
@@ -394,9 +395,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     if (ok) {
       const float l_tot = ml_x[r].y + ml_x[128 + r].y;
-      const bool row_ok = i < g.L;
+      const bool row_ok = i < g.Lq;
       const float inv = 1.f / l_tot;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+      float* orow = p.o + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int c = wg * (D / 64) + cc;
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                             __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
         }
       }
-      if (row_ok && wg == 0) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
+      if (row_ok && wg == 0) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
     }
   } else if (warp >= 2) {
     // ---------------- softmax / correction / epilogue (one warpgroup) ----------------
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int j0 = (t_lo + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 + BN - 1 <= i0) && (g.W == 0 || i0 + kBM - 1 - j0 < g.W);
+      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
       // the whole S row in registers: all loads issued, then one wait
       uint32_t sr[BN];
 #pragma unroll
@@ -434,8 +435,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
       tmem_wait_ld();
       // Visible key columns of this row inside the tile: [clo, chi] (edge tiles only).
-      const int clo = (g.W > 0) ? max(0, i - g.W + 1 - j0) : 0;
-      const int chi = min(BN - 1, i - j0);
+      const int clo = band_key_lo(g, i) - j0;
+      const int chi = band_key_hi(g, i) - j0;
       const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, clo, chi)
                               : softmax_tile_max<BN, false>(sr, sl2, clo, chi);
       float alpha = 1.f;
@@ -492,9 +493,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tmem_ld16(tmem + lane_off + C::L_COL, lr);  // warp-collective
       tmem_wait_ld();
       const float l_tot = __uint_as_float(lr[0]);
-      const bool row_ok = i < g.L;
+      const bool row_ok = i < g.Lq;
       const float inv = 1.f / l_tot;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * D;
+      float* orow = p.o + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t acc[32];
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                             __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
         }
       }
-      if (row_ok) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
+      if (row_ok) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
     }
   }
 
@@ -664,7 +665,7 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   CUtensorMap tq, tk, tv;
   cudaError_t e;
   // one TMA instruction per tile: Q, K and V in all D / 64 chunks
-  if ((e = make_tmap_f16_chunks(&tq, q16, D, g.L, g.B * g.Hq, kBM, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tq, q16, D, g.Lq, g.B * g.Hq, kBM, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   auto kern = fwd_tc_kernel<D>;
@@ -675,7 +676,7 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   p.o = o;
   p.lse = lse;
   p.status = status;
-  p.n_qtiles = (g.L + kBM - 1) / kBM;
+  p.n_qtiles = (g.Lq + kBM - 1) / kBM;
   dim3 grid(g.B * g.Hq, p.n_qtiles);
   kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, p);
   return cudaGetLastError();

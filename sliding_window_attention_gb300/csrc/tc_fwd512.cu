@@ -165,10 +165,9 @@ __global__ void __launch_bounds__(kThr, 1)
   const int bh = b * g.Hq + (bkv - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // b * Hq + query head
   const int tile = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
   const int i0 = tile * T;
-  const int ihi = min(i0 + T, g.L) - 1;
-  const int jlo = g.W > 0 ? max(0, i0 - g.W + 1) : 0;
-  const int t_lo = jlo / T;
-  const int N = ihi / T - t_lo + 1;  // key steps
+  const int ihi = min(i0 + T, g.Lq) - 1;
+  const int t_lo = band_key_lo(g, i0) / T;
+  const int N = band_key_hi(g, ihi) / T - t_lo + 1;  // key steps (at least one)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 11; ++s) {
@@ -337,13 +336,13 @@ __global__ void __launch_bounds__(kThr, 1)
       // Q row i into Tensor Memory: fp16 pairs, one 32-bit column each; warpgroup
       // wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
       const uint4* src =
-          reinterpret_cast<const uint4*>(p.q16 + ((size_t)bh * g.L + (i < g.L ? i : 0)) * DH) + wg * 32;
+          reinterpret_cast<const uint4*>(p.q16 + ((size_t)bh * g.Lq + (i < g.Lq ? i : 0)) * DH) + wg * 32;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = i < g.L ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w4 = i < g.Lq ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
           v[4 * q] = w4.x;
           v[4 * q + 1] = w4.y;
           v[4 * q + 2] = w4.z;
@@ -375,10 +374,10 @@ __global__ void __launch_bounds__(kThr, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->s_free[bb]);
-      const bool full = (j0 + T - 1 <= i0) && (g.W == 0 || i0 + T - 1 - j0 < g.W);
+      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + T - 1 <= band_key_hi(g, i0));
       // visible key columns of row i in this tile, relative to this warpgroup's half
-      const int clo = (g.W > 0 ? max(0, i - g.W + 1 - j0) : 0) - cb0;
-      const int chi = min(T - 1, i - j0) - cb0;
+      const int clo = band_key_lo(g, i) - j0 - cb0;
+      const int chi = band_key_hi(g, i) - j0 - cb0;
       const float pmax = full ? half_max<true>(sr, sl2, clo, chi) : half_max<false>(sr, sl2, clo, chi);
       xm[(bb * 2 + wg) * 128 + r] = pmax;
       mbar_arrive(&bars->mx[bb]);
@@ -429,7 +428,7 @@ __global__ void __launch_bounds__(kThr, 1)
     if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->lx, 0, abort_flag, R))) {
       const float l_tot = xl[r] + xl[128 + r];
       if (wg == 0) {
-        if (i < g.L) p.lse[(size_t)bh * g.L + i] = (m_run + log2f(l_tot)) * kLn2;
+        if (i < g.Lq) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
         finl[r] = 1.f / l_tot;
         fence_proxy_async_smem();
         mbar_arrive(&bars->fin_staged);
@@ -490,8 +489,8 @@ __global__ void __launch_bounds__(kThr, 1)
                                          mbar_wait_cl(&bars->fin_full, 0, abort_flag, R))) {
       tc_fence_after();
       const float inv = rinv[r];
-      const bool row_ok = i < g.L;
-      float* orow = p.o + ((size_t)bh * g.L + (row_ok ? i : 0)) * DH;
+      const bool row_ok = i < g.Lq;
+      float* orow = p.o + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * DH;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         const int col = 256 * wg + 32 * c;
@@ -550,7 +549,7 @@ cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t*
   pm.q16 = q16;
   pm.o = o;
   pm.lse = lse;
-  pm.n_tiles = (g.L + T - 1) / T;
+  pm.n_tiles = (g.Lq + T - 1) / T;
   pm.status = status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(R * (unsigned)g.G, (unsigned)pm.n_tiles, (unsigned)(g.B * g.Hkv));

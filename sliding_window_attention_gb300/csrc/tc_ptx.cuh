@@ -409,5 +409,14 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_cluster, uint32_t 
       : "memory");
 }
 
+// Rows [r0, min(r0 + rows, L)) of head `head` of an fp32 [heads, L, D]
+// tensor set to zero by every thread of the CTA (D a multiple of 4, the
+// tensor 16-byte aligned).
+__device__ __forceinline__ void zero_rows(float* out, int head, int r0, int rows, int L, int D) {
+  const int n = (rows < L - r0 ? rows : L - r0) * D / 4;
+  float4* dst = reinterpret_cast<float4*>(out + ((size_t)head * L + r0) * D);
+  for (int e = threadIdx.x; e < n; e += blockDim.x) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 }  // namespace tc
 }  // namespace swa

@@ -96,3 +96,30 @@ def test_argument_errors_are_reported_before_any_cuda_call(lib):
     assert _bwd(lib, wsb=16) == c["SWA_ERR_WORKSPACE"]
     assert _bwd(lib, ws=0) == c["SWA_ERR_WORKSPACE"]
     assert _bwd(lib, D=32) == c["SWA_ERR_BAD_HEAD_DIM"]
+
+
+def test_suffix_entry_points_check_arguments(lib):
+    c = declared_codes()
+    P = ctypes.c_void_p
+
+    def fwd_ex(Lq=16, Lk=32, D=64, W=0, causal=1, q=0x1000, ws=None, wsb=0):
+        return lib.swa_attn_fwd_ex(P(q), P(0x2000), P(0x3000), P(0x4000), P(0x5000), 1, 2, 1, Lq, Lk, D, W, causal,
+                                   ctypes.c_float(0.125), P(ws), wsb, None)
+
+    assert fwd_ex(Lq=33, Lk=32) == c["SWA_ERR_BAD_SHAPE"]  # queries must be a suffix of the keys
+    assert fwd_ex(Lq=0) == c["SWA_ERR_BAD_SHAPE"]
+    assert fwd_ex(D=80) == c["SWA_ERR_BAD_HEAD_DIM"]
+    assert fwd_ex(W=-2, causal=0) == c["SWA_ERR_BAD_WINDOW"]
+    assert fwd_ex(q=0) == c["SWA_ERR_NULL_POINTER"]
+    assert fwd_ex(wsb=0, ws=None) == c["SWA_ERR_WORKSPACE"]
+    ptrs = [0x1000 * (i + 1) for i in range(9)]
+    rc = lib.swa_attn_bwd_ex(*(P(p) for p in ptrs), 1, 2, 1, 40, 20, 64, 0, 1, ctypes.c_float(0.1), P(0x10000),
+                             1 << 20, None)
+    assert rc == c["SWA_ERR_BAD_SHAPE"]
+    # workspace grows with Lq for the query-side copies and with Lk for the key side
+    a = lib.swa_attn_bwd_workspace_bytes_ex(1, 8, 2, 100, 4000, 128, 256, 1)
+    b = lib.swa_attn_bwd_workspace_bytes_ex(1, 8, 2, 4000, 4000, 128, 256, 1)
+    assert 0 < a < b and a % 256 == 0
+    assert lib.swa_attn_bwd_workspace_bytes_ex(1, 8, 2, 4000, 4000, 128, 256, 1) == \
+        lib.swa_attn_bwd_workspace_bytes(1, 8, 2, 4000, 128, 256)
+    assert lib.swa_attn_fwd_workspace_bytes_ex(1, 8, 2, 5, 3, 128, 0, 1) == 0

@@ -238,3 +238,61 @@ def test_device_timeout_is_reported_and_context_survives(oracle_mod):
     assert_lse_close(got["lse"].numpy(), ref["lse"])
     for n in ("o", "dq", "dk", "dv"):
         assert_close(n, got[n].numpy(), ref[n])
+
+
+# ---------------------------------------------------------------------------
+# queries that are a suffix of the keys (qL < kL), non-causal windows
+# ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself", "What I
+# changed, in plain terms" items 3-6 and "Gradient parity")
+
+SUFFIX = [
+    # B, Hq, Hkv, Lq, Lk, D, window, causal
+    (1, 2, 1, 200, 700, 64, 0, True),
+    (1, 4, 2, 129, 1000, 128, 128, True),   # keys 0 .. ~742 seen by no query
+    (2, 2, 1, 1, 300, 64, 50, True),        # one decode step over a cache
+    (1, 8, 2, 1, 2049, 128, 0, True),
+    (1, 2, 1, 300, 300, 128, 100, False),   # non-causal self-attention window
+    (1, 4, 2, 250, 777, 64, 0, False),      # unmasked
+    (1, 2, 2, 333, 900, 256, 129, False),
+    (1, 4, 2, 127, 400, 256, 0, True),
+    (1, 2, 1, 300, 1100, 512, 200, True),
+    (1, 2, 1, 260, 600, 512, 0, False),
+    (1, 2, 1, 130, 1030, 512, 100, False),  # non-causal window, unreached keys on both sides
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,D,window,causal", SUFFIX)
+def test_suffix_and_noncausal_elementwise(oracle_mod, B, Hq, Hkv, Lq, Lk, D, window, causal):
+    import sliding_window_attention_gb300 as swa
+
+    q, k, v, dO = make_inputs(B, Hq, Hkv, Lk, D, seed=2000 + Lq + Lk + D + window)
+    q, dO = q[:, :, Lk - Lq:].contiguous(), dO[:, :, Lk - Lq:].contiguous()
+    scale = 1.0 / math.sqrt(D)
+    ref = oracle_mod.backward(q, k, v, dO, window, scale, band_only=True, causal=causal)
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, dO))
+    o, lse = swa.forward(qd, kd, vd, window, scale, causal=causal)
+    dq, dk, dv = swa.backward(qd, kd, vd, o, lse, gd, window, scale, causal=causal)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    assert_lse_close(lse.cpu().numpy(), ref["lse"])
+    got = dict(o=o, dq=dq, dk=dk, dv=dv)
+    for n in ("o", "dq", "dk", "dv"):
+        assert_close(n, got[n].cpu().numpy(), ref[n])
+    # keys that no query sees: exact zeros
+    dead = [j for j in range(Lk) if not np.any(ref["dv"][:, :, j]) and not np.any(ref["dk"][:, :, j])]
+    if dead:
+        assert (dk[:, :, dead] == 0).all() and (dv[:, :, dead] == 0).all()
+
+
+def test_suffix_rows_equal_full_problem_rows():
+    """The suffix call gives the rows of the self-attention call over all Lk
+    positions (same band per row), up to the order of tile visits."""
+    import sliding_window_attention_gb300 as swa
+
+    B, Hq, Hkv, Lk, D, W, Lq = 1, 4, 2, 640, 128, 200, 256
+    q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, Lk, D, seed=77))
+    o_full, lse_full = swa.forward(q, k, v, W, 0.09)
+    o_suf, lse_suf = swa.forward(q[:, :, Lk - Lq:].contiguous(), k, v, W, 0.09, causal=True)
+    torch.cuda.synchronize()
+    assert torch.allclose(o_suf, o_full[:, :, Lk - Lq:], atol=2e-6, rtol=0)
+    assert torch.allclose(lse_suf, lse_full[:, :, Lk - Lq:], atol=2e-6, rtol=0)
