@@ -188,11 +188,29 @@ def dist_setup(args):
     return world, rank, local_rank
 
 
+def _sample_q_rows(w, Ls):
+    """Query rows of an oracle sample over the first Ls key positions: the
+    workload's suffix fraction of Ls (all Ls for self-attention)."""
+    return Ls if w.q_rows == w.L else max(1, round(Ls * w.q_rows / w.L))
+
+
+def _sample_pairs(w, Ls):
+    from sliding_window_attention_gb300.inputs import band_pairs, band_pairs_ex
+
+    if w.q_rows == w.L and w.causal:
+        return band_pairs(Ls, w.window)
+    return band_pairs_ex(_sample_q_rows(w, Ls), Ls, w.window, w.causal)
+
+
 def _oracle_sample_inputs(w, Ls):
     from sliding_window_attention_gb300.inputs import make_inputs
 
     G = w.Hq // w.Hkv
-    return make_inputs(1, G, 1, Ls, w.D, w.seed, w.do_scale, w.outlier_frac, w.outlier_mult)
+    q, k, v, dO = make_inputs(1, G, 1, Ls, w.D, w.seed, w.do_scale, w.outlier_frac, w.outlier_mult)
+    nq = _sample_q_rows(w, Ls)
+    if nq < Ls:
+        q, dO = (t[:, :, Ls - nq:].contiguous() for t in (q, dO))
+    return q, k, v, dO
 
 
 def oracle_sample_seconds(w, Ls, inputs=None):
@@ -202,7 +220,7 @@ def oracle_sample_seconds(w, Ls, inputs=None):
 
     q, k, v, dO = inputs if inputs is not None else _oracle_sample_inputs(w, Ls)
     t0 = time.perf_counter()
-    oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True)
+    oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True, causal=w.causal)
     return time.perf_counter() - t0
 
 
@@ -210,7 +228,6 @@ def oracle_sample_length(w, target_s: float) -> int:
     """Sequence length Ls whose oracle sample takes about target_s seconds
     (cost model: proportional to the in-band pair count)."""
     import oracle
-    from sliding_window_attention_gb300.inputs import band_pairs
 
     oracle.build()
     Ls = min(256, w.L)
@@ -218,11 +235,11 @@ def oracle_sample_length(w, target_s: float) -> int:
     for _ in range(4):
         if t >= 0.6 * target_s or Ls >= w.L:
             break
-        want_pairs = band_pairs(Ls, w.window) * target_s / max(t, 1e-3)
+        want_pairs = _sample_pairs(w, Ls) * target_s / max(t, 1e-3)
         lo, hi = Ls, w.L
         while lo < hi:
             mid = (lo + hi + 1) // 2
-            if band_pairs(mid, w.window) <= want_pairs:
+            if _sample_pairs(w, mid) <= want_pairs:
                 lo = mid
             else:
                 hi = mid - 1
@@ -234,9 +251,7 @@ def oracle_sample_length(w, target_s: float) -> int:
 
 
 def oracle_useful_flops(w, Ls) -> int:
-    from sliding_window_attention_gb300.inputs import band_pairs
-
-    return 14 * w.D * (w.Hq // w.Hkv) * band_pairs(Ls, w.window)
+    return 14 * w.D * (w.Hq // w.Hkv) * _sample_pairs(w, Ls)
 
 
 def cpu_oracle_sample(w, target_s: float):
@@ -268,20 +283,30 @@ def run_reference(args, w, world, rank):
     value = flops * steps / sum(secs) / 1e12
     G = w.Hq // w.Hkv
     sample = (f"fp64 oracle fwd+bwd (band mode) on 1 kv-head group ({G} query heads) x first {Ls} tokens "
-              f"of {w.name} per step; useful flops counted as on the GPU")
+              f"({_sample_q_rows(w, Ls)} query rows) of {w.name} per step; useful flops counted as on the GPU")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": round(1e3 * sum(secs) / steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "D": w.D,
-                   "window": w.window},
+        "config": dict({"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L, "D": w.D,
+                        "window": w.window}, **_variant_keys(w)),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _variant_keys(w):
+    """Config keys of a band variant (queries a suffix of the keys, or non-causal)."""
+    out = {}
+    if w.q_rows != w.L:
+        out["Lq"] = w.q_rows
+    if not w.causal:
+        out["causal"] = False
+    return out
 
 
 def run_ours(args, w, world, rank, local_rank):
@@ -302,27 +327,39 @@ def run_ours(args, w, world, rank, local_rank):
     # each rank: one independent copy of the workload (seed offset by rank)
     q_h, k_h, v_h, dO_h = make_inputs(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed + 7919 * rank, w.do_scale,
                                       w.outlier_frac, w.outlier_mult)
-    q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, dO_h))
     B, Hq, Hkv, L, D, W = w.B, w.Hq, w.Hkv, w.L, w.D, w.window
+    Lq = w.q_rows  # query rows: the last Lq of the L key positions
+    variant = Lq != L or not w.causal
+    if Lq < L:
+        q_h, dO_h = (t[:, :, L - Lq:].contiguous() for t in (q_h, dO_h))
+    q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, dO_h))
     f32 = dict(dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
     base_mem = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
-    o = torch.empty((B, Hq, L, D), **f32)
-    lse = torch.empty((B, Hq, L), **f32)
-    dq = torch.empty((B, Hq, L, D), **f32)
+    o = torch.empty((B, Hq, Lq, D), **f32)
+    lse = torch.empty((B, Hq, Lq), **f32)
+    dq = torch.empty((B, Hq, Lq, D), **f32)
     dk = torch.empty((B, Hkv, L, D), **f32)
     dv = torch.empty((B, Hkv, L, D), **f32)
-    fws_b = swa.fwd_workspace_bytes(B, Hq, Hkv, L, D, W)
-    bws_b = swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W)
+    if variant:
+        fws_b = swa.fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
+        bws_b = swa.bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
+    else:
+        fws_b = swa.fwd_workspace_bytes(B, Hq, Hkv, L, D, W)
+        bws_b = swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W)
     fws = torch.empty(max(fws_b, 256), dtype=torch.uint8, device=dev)
     bws = torch.empty(max(bws_b, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        swa.swa_attn_fwd(q, k, v, o, lse, W, w.scale, fws, stream)
-        swa.swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, W, w.scale, bws, stream)
+        if variant:
+            swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
+            swa.swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, W, w.causal, w.scale, bws, stream)
+        else:
+            swa.swa_attn_fwd(q, k, v, o, lse, W, w.scale, fws, stream)
+            swa.swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, W, w.scale, bws, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -401,9 +438,9 @@ def run_ours(args, w, world, rank, local_rank):
     avg_s = kms / kl / 1e3
     if kname in HBM_KERNELS:
         if kname in ("bwd_delta", "bwd_rowstats"):
-            alg = B * Hq * L * (D * 4 + D * 2 + 4)
+            alg = B * Hq * Lq * (D * 4 + D * 2 + 4)
         else:  # bf16 read + fp16 write of q, k, v (and dO in the backward)
-            alg = 4 * D * L * B * (Hq + 2 * Hkv)
+            alg = 4 * D * B * (Hq * Lq + 2 * Hkv * L)
         achieved = alg / avg_s / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
@@ -432,7 +469,8 @@ def run_ours(args, w, world, rank, local_rank):
             G = w.Hq // w.Hkv
             cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": f"fp64 oracle fwd+bwd (band mode), 1 kv-head group ({G} query heads) x first {Ls} "
-                             f"tokens of {w.name}, {secs:.1f} s; useful flops counted as on the GPU"}
+                             f"tokens ({_sample_q_rows(w, Ls)} query rows) of {w.name}, {secs:.1f} s; useful flops "
+                             f"counted as on the GPU"}
         per_kernel = {n: {"launches": c, "avg_ms": round(ms / c, 4), "share": round(ms / sum(x[1] for x in
                       kernels.values()), 4)} for n, (c, ms) in kernels.items()}
         line = {
@@ -441,9 +479,10 @@ def run_ours(args, w, world, rank, local_rank):
             "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if kname.endswith("_simt") else "f16",
             "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
-            "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "L": L, "D": D, "window": W,
-                       "scale": round(w.scale, 6), "parallelism": f"replicas x{world} (one workload per GPU)",
-                       "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
+            "config": dict({"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "L": L, "D": D, "window": W,
+                            "scale": round(w.scale, 6), "parallelism": f"replicas x{world} (one workload per GPU)",
+                            "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
+                           **_variant_keys(w)),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -472,7 +511,8 @@ def main():
     if args.seq_len > 0:
         import dataclasses
 
-        w = dataclasses.replace(w, name=f"{w.name}@L{args.seq_len}", L=args.seq_len)
+        lq = max(1, round(w.Lq * args.seq_len / w.L)) if w.Lq else 0  # keep the suffix fraction
+        w = dataclasses.replace(w, name=f"{w.name}@L{args.seq_len}", L=args.seq_len, Lq=lq)
     world, rank, local_rank = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, w, world, rank)

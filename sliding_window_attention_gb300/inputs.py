@@ -19,6 +19,12 @@ detail", "Starting point"), and the long step is 30,553 tokens ("Model
 step").  Peaky softmax rows (scores in the 20s on real activations, "fp32
 gradient truth", layer-level table) are imitated by scaling 1% of the key
 rows by 8.
+
+Two more workloads exercise the band variants the same page's parity sweep
+covers ("Gradient parity": qL < kL, windows causal and not): the sliding
+layer with its queries a suffix of the keys, and a non-causal window.  A
+suffix workload draws the full-length tensors with the recipe above and keeps
+the last Lq rows of q and dO.
 """
 from __future__ import annotations
 
@@ -41,6 +47,12 @@ class Workload:
     outlier_frac: float = 0.0
     outlier_mult: float = 8.0
     seed: int = 0
+    Lq: int = 0          # query rows (the last Lq of the L key positions); 0 means L
+    causal: bool = True
+
+    @property
+    def q_rows(self) -> int:
+        return self.Lq or self.L
 
     @property
     def scale(self) -> float:
@@ -48,7 +60,9 @@ class Workload:
 
     def pairs(self) -> int:
         """In-band (query, key) pairs over all batches and query heads."""
-        return self.B * self.Hq * band_pairs(self.L, self.window)
+        if self.q_rows == self.L and self.causal:
+            return self.B * self.Hq * band_pairs(self.L, self.window)
+        return self.B * self.Hq * band_pairs_ex(self.q_rows, self.L, self.window, self.causal)
 
     def fwd_flops(self) -> int:
         return 4 * self.D * self.pairs()
@@ -66,6 +80,20 @@ def band_pairs(L: int, window: int) -> int:
     return w * (w + 1) // 2 + (L - w) * w
 
 
+def band_pairs_ex(Lq: int, Lk: int, window: int, causal: bool) -> int:
+    """In-band pairs when query i sits at key position a = i + Lk - Lq:
+    causal keeps j <= a (and a - j < window), non-causal |a - j| < window
+    (window 0: every key)."""
+    w = window if 0 < window < Lk else 0
+    total = 0
+    for i in range(Lq):
+        a = i + Lk - Lq
+        lo = max(0, a - w + 1) if w else 0
+        hi = a if causal else (min(Lk - 1, a + w - 1) if w else Lk - 1)
+        total += hi - lo + 1
+    return total
+
+
 WORKLOADS = {
     w.name: w
     for w in [
@@ -75,6 +103,9 @@ WORKLOADS = {
         Workload("global_l16384_d512", 1, 32, 4, 16384, 512, 0, do_scale=0.1, seed=20260004),
         Workload("ragged_l30553_d256_w1024_outliers", 1, 32, 16, 30553, 256, 1024,
                  outlier_frac=0.01, seed=20260005),
+        Workload("suffix_q2048_k8192_d256_w1024", 1, 32, 16, 8192, 256, 1024, do_scale=0.1, seed=20260006,
+                 Lq=2048),
+        Workload("noncausal_l8192_d128_w512", 1, 8, 4, 8192, 128, 512, seed=20260007, causal=False),
     ]
 }
 
@@ -98,4 +129,7 @@ def make_inputs(B, Hq, Hkv, L, D, seed, do_scale=1.0, outlier_frac=0.0, outlier_
 
 
 def workload_inputs(w: Workload):
-    return make_inputs(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed, w.do_scale, w.outlier_frac, w.outlier_mult)
+    q, k, v, dO = make_inputs(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed, w.do_scale, w.outlier_frac, w.outlier_mult)
+    if w.q_rows < w.L:
+        q, dO = (t[:, :, w.L - w.q_rows:].contiguous() for t in (q, dO))
+    return q, k, v, dO

@@ -72,7 +72,7 @@ def _sample_keys(w, rng):
     """Key rows whose oracle cost stays within seconds: the key's column needs
     every query row that sees it, so for long causal rows keep keys late."""
     L = w.L
-    if w.window:
+    if w.window or w.q_rows < L or not w.causal:
         lo = 0
     else:
         # rows [lo, L) each cost up to L keys; keep G * D * (L^2 - lo^2) bounded
@@ -89,7 +89,7 @@ def _sample_keys(w, rng):
 def full_run(request):
     w = WORKLOADS[request.param]
     q, k, v, dO = workload_inputs(w)
-    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale)
+    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale, causal=w.causal)
     return w, (q, k, v, dO), got
 
 
@@ -100,15 +100,15 @@ def test_full_workload_sampled(oracle_mod, full_run):
     for name in ("o", "dq", "dk", "dv", "lse"):
         assert torch.isfinite(got[name]).all(), name
     heads = sorted({0, w.Hq - 1, G, w.Hq // 2})
-    rows = _sample_rows(w.L, w.window, rng)
+    rows = _sample_rows(w.q_rows, w.window, rng)
     for h in heads:
-        r = oracle_mod.rows(q, k, v, dO, w.window, w.scale, 0, h, rows, band_only=True)
+        r = oracle_mod.rows(q, k, v, dO, w.window, w.scale, 0, h, rows, band_only=True, causal=w.causal)
         assert_lse_close(got["lse"][0, h, rows].numpy(), r["lse"])
         assert_close(f"o[h={h}]", got["o"][0, h, rows].numpy(), r["o"])
         assert_close(f"dq[h={h}]", got["dq"][0, h, rows].numpy(), r["dq"])
     keys = _sample_keys(w, rng)
     for kvh in sorted({0, w.Hkv - 1}):
-        r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True)
+        r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True, causal=w.causal)
         assert_close(f"dk[kvh={kvh}]", got["dk"][0, kvh, keys].numpy(), r["dk"])
         assert_close(f"dv[kvh={kvh}]", got["dv"][0, kvh, keys].numpy(), r["dv"])
 
@@ -120,7 +120,7 @@ def test_full_workload_properties(full_run):
     w, (q, k, v, dO), got = full_run
     G = w.Hq // w.Hkv
     dv_sum = got["dv"].double().sum(2)                                  # [B, Hkv, D]
-    want = dO.double().view(w.B, w.Hkv, G, w.L, w.D).sum((2, 3))        # [B, Hkv, D]
+    want = dO.double().view(w.B, w.Hkv, G, w.q_rows, w.D).sum((2, 3))   # [B, Hkv, D]
     ma, rf = errors(dv_sum.numpy(), want.numpy())
     assert rf <= 1e-3, (ma, rf)
     dk_sum = got["dk"].double().sum(2)
