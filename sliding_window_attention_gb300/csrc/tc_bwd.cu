@@ -78,36 +78,6 @@ __global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, 
   }
 }
 
-// dK/dV elementwise step for one key row and 32 query columns: P^T (if
-// WANT_P) and dS^T = P^T (dP^T - Delta) (if WANT_DS) as fp16 pairs.  FULL:
-// every column is in the band (no mask code); otherwise columns outside
-// [clo, chi] give exactly zero.
-template <bool FULL, bool WANT_P, bool WANT_DS>
-__device__ __forceinline__ void kv_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float* lse_s,
-                                         const float* dl_s, float sl2, int cbase, int clo, int chi,
-                                         uint32_t (&pp)[16], uint32_t (&dd)[16]) {
-#pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + cbase + e);  // lse * log2e of 4 columns
-    float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (WANT_DS) d4 = *reinterpret_cast<const float4*>(dl_s + cbase + e);  // Delta of 4 columns
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dlv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-    for (int u = 0; u < 4; u += 2) {
-      float p0 = fast_exp2(fmaf(__uint_as_float(sv[e + u]), sl2, -lv[u]));
-      float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + u + 1]), sl2, -lv[u + 1]));
-      if (!FULL) {
-        p0 = (cbase + e + u >= clo && cbase + e + u <= chi) ? p0 : 0.f;
-        p1 = (cbase + e + u + 1 >= clo && cbase + e + u + 1 <= chi) ? p1 : 0.f;
-      }
-      if (WANT_P) pp[(e + u) >> 1] = pack_half2(p0, p1);
-      if (WANT_DS)
-        dd[(e + u) >> 1] = pack_half2(p0 * (__uint_as_float(dv[e + u]) - dlv[u]),
-                                      p1 * (__uint_as_float(dv[e + u + 1]) - dlv[u + 1]));
-    }
-  }
-}
-
 // dQ elementwise step for one query row (lse*log2e = l2, Delta = dl) and 32
 // key columns: dS = P (dP - Delta) as fp16 pairs.
 template <bool FULL>
@@ -125,37 +95,8 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_
   }
 }
 
-// ===========================================================================
-// dK / dV for head dim 256.  dK and dV of a 128-key tile do not both fit in
-// the 512 TMEM columns, so a dV-only CTA (S^T, P^T, dV) and a dK-only CTA
-// (S^T, dP^T, dS^T, dK) run as two kernels.  The two elementwise warpgroups
-// take alternate 32-row query steps.
+// dV-only / dK-only CTAs of the head-dim-256 dK/dV pass
 enum { kModeDV = 0, kModeDK = 1 };
-
-template <int D, int MODE>
-struct KvCfg {
-  static constexpr int BNK = 128;  // key rows per CTA (MMA M)
-  static constexpr int BM = 32;    // query rows per step
-  static constexpr bool NEED_V = MODE != kModeDV;  // dP^T = V dO^T
-  static constexpr bool DO_DV = MODE != kModeDK;
-  static constexpr bool DO_DK = MODE != kModeDV;
-  static constexpr int KCH = D / 64;
-  static constexpr int KV_BYTES = BNK * D * 2;  // K (or V) tile
-  static constexpr int QT_BYTES = BM * D * 2;   // Q (or dO) tile
-  static constexpr int ST_BYTES = BM * 8;       // lse * log2e of BM rows, then their Delta
-  static constexpr int STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q, dO, stats (padded to 1 KB)
-  static constexpr int RES_BYTES = (NEED_V ? 2 : 1) * KV_BYTES;  // resident K (and V)
-  // Q / dO / stats stages: as many as shared memory holds (TMA latency hiding)
-  static constexpr int NS = clamp_stages((kSmemMax - 2048 - RES_BYTES) / STAGE_BYTES);
-  // TMEM: the CTA's one accumulator at column 0
-  static constexpr int DV_COL = 0, DK_COL = 0;
-  static constexpr int S_COL = 256, DP_COL = 384;
-  static constexpr size_t SMEM_USED = (size_t)RES_BYTES + NS * (size_t)STAGE_BYTES + 1024 + 1024;
-  static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
-  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(D == 256, "head dim 256 only (the accumulator fills the columns below the S buffers)");
-  static_assert(S_COL + 2 * BM <= DP_COL && DP_COL + 2 * BM <= 512, "TMEM columns");
-};
 
 struct BwdParams {
   Geom g;
@@ -166,240 +107,6 @@ struct BwdParams {
   int n_tiles;
   int* status;
 };
-
-template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                   const __grid_constant__ CUtensorMap tmS, const BwdParams p) {
-  using C = KvCfg<D, MODE>;
-  constexpr int BNK = C::BNK, BM = C::BM, NS = C::NS, KCH = C::KCH;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sK = base;
-  unsigned char* sV = sK + C::KV_BYTES;  // only used when C::NEED_V
-  unsigned char* sStage = sK + C::RES_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::STAGE_BYTES);
-  uint64_t* kv_full = bars;                // [1]
-  uint64_t* st_full = kv_full + 1;         // [NS]
-  uint64_t* st_empty = st_full + NS;       // [NS]
-  uint64_t* sdp_full = st_empty + NS;      // [2]
-  uint64_t* p_full = sdp_full + 2;         // [2]
-  uint64_t* acc_done = p_full + 2;         // [1]
-  uint64_t* mma_drain = acc_done + 1;      // [1] every issued MMA finished (before TMEM is released)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const Geom& g = p.g;
-  const int warp = threadIdx.x / 32;
-  const int bkv = blockIdx.x;  // b * Hkv + kv head
-  const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
-  const int j0 = (int)blockIdx.y * BNK;
-  const int jhi = min(j0 + BNK, g.L) - 1;
-  // query rows that can see a key of this tile
-  const int qlo = band_q_lo(g, j0), qhi = band_q_hi(g, jhi);
-  const int t_lo = qlo / BM, t_hi = qhi / BM;
-  const int ntq = qlo <= qhi ? t_hi - t_lo + 1 : 0;
-  const int N = g.G * ntq;  // work items (head of group, query tile)
-  if (N == 0) {
-    // no query sees these keys (queries that are a suffix of the keys, with a
-    // window): their gradients are zero ("Lab 028 lab detail", "What I
-    // changed, in plain terms" item 5(b)).  Uniform over the CTA, before any
-    // barrier or Tensor Memory is set up.
-    zero_rows(MODE == kModeDK ? p.out0 : p.out1, bkv, j0, BNK, g.L, D);
-    return;
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(st_full + s, 1);
-      mbar_init(st_empty + s, 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(sdp_full + s, 1);
-      mbar_init(p_full + s, 128);
-    }
-    mbar_init(acc_done, 1);
-    mbar_init(mma_drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (elect_one()) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      prefetch_tmap(&tmG);
-      prefetch_tmap(&tmS);
-      mbar_arrive_expect_tx(kv_full, C::RES_BYTES);
-      for (int c = 0; c < KCH; ++c) {
-        tma_load_3d(sK + c * BNK * 128, &tmK, kv_full, c * 64, j0, bkv);
-        if (C::NEED_V) tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
-      }
-      int issued = 0;
-      for (int n = 0; n < N; ++n) {
-        const int st = n % NS;
-        const int gi = n / ntq, t = t_lo + n % ntq;
-        const int bh = b * g.Hq + kvh * g.G + gi;
-        if (n >= NS && !mbar_wait(st_empty + st, ((n / NS) & 1) ^ 1, abort_flag)) break;
-        unsigned char* stg = sStage + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(st_full + st, 2 * C::QT_BYTES + C::ST_BYTES);
-        for (int c = 0; c < KCH; ++c) {
-          tma_load_3d(stg + c * BM * 128, &tmQ, st_full + st, c * 64, t * BM, bh);
-          tma_load_3d(stg + C::QT_BYTES + c * BM * 128, &tmG, st_full + st, c * 64, t * BM, bh);
-        }
-        tma_load_2d(stg + 2 * C::QT_BYTES, &tmS, st_full + st, t * BM, bh);
-        tma_load_2d(stg + 2 * C::QT_BYTES + BM * 4, &tmS, st_full + st, t * BM, g.B * g.Hq + bh);
-        ++issued;
-      }
-      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
-        mbar_wait_drain(kv_full, 0);
-        drain_ring(st_full, NS, issued);
-      }
-    }
-  } else if (warp == 1) {
-    if (elect_one()) {
-      const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major)
-      const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (B MN-major)
-      const uint64_t kdk = smem_desc_sw128(smem_u32(sK), 16, 1024);  // K, K-major (resident)
-      const uint64_t vdk = smem_desc_sw128(smem_u32(sV), 16, 1024);  // V, K-major (resident)
-      bool ok = mbar_wait(kv_full, 0, abort_flag);
-      auto issue_grad = [&](int m) -> bool {
-        const int st = m % NS, sb = m & 1;
-        if (!mbar_wait(p_full + sb, (m >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t qaddr = smem_u32(sStage + st * C::STAGE_BYTES);
-        const uint64_t qmn = smem_desc_sw128(qaddr, BM * 128, 1024);               // Q, MN-major
-        const uint64_t gmn = smem_desc_sw128(qaddr + C::QT_BYTES, BM * 128, 1024);  // dO, MN-major
-#pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks) {
-          const uint32_t acc = (m > 0 || ks > 0) ? 1u : 0u;
-          if (C::DO_DV)
-            mma_ts(tmem + C::DV_COL, tmem + C::S_COL + sb * BM + ks * 8, desc_add(gmn, ks * 2048), idG, acc);
-          if (C::DO_DK)
-            mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + sb * BM + ks * 8, desc_add(qmn, ks * 2048), idG, acc);
-        }
-        mma_commit(st_empty + st);
-        return true;
-      };
-      for (int n = 0; ok && n < N; ++n) {
-        const int st = n % NS, sb = n & 1;
-        if (!mbar_wait(st_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t qaddr = smem_u32(sStage + st * C::STAGE_BYTES);
-        const uint64_t qk = smem_desc_sw128(qaddr, 16, 1024);               // Q, K-major
-        const uint64_t gk = smem_desc_sw128(qaddr + C::QT_BYTES, 16, 1024);  // dO, K-major
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks & 3) * 32;
-          const uint32_t ck = (ks >> 2) * BNK * 128, cq = (ks >> 2) * BM * 128;
-          mma_ss(tmem + C::S_COL + sb * BM, desc_add(kdk, ck + off), desc_add(qk, cq + off), idS, ks > 0 ? 1u : 0u);
-          if (C::NEED_V)
-            mma_ss(tmem + C::DP_COL + sb * BM, desc_add(vdk, ck + off), desc_add(gk, cq + off), idS,
-                   ks > 0 ? 1u : 0u);
-        }
-        mma_commit(sdp_full + sb);
-        if (n >= 1 && !issue_grad(n - 1)) { ok = false; break; }
-      }
-      if (ok && issue_grad(N - 1)) mma_commit(acc_done);
-      // every MMA issued so far has finished before TMEM is released
-      mma_commit(mma_drain);
-      mbar_wait_drain(mma_drain, 0);
-    }
-  } else {
-    // warpgroup (warps 2-5 or 6-9): takes steps n with n % 2 == wg; a warp can
-    // only reach TMEM lanes 32 * (warp % 4) .. +31, which fixes its rows
-    const int wg = (warp - 2) >> 2;
-    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
-    const int j = j0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const float sl2 = g.scale * kLog2e;
-    bool ok = true;
-    constexpr int CW = BM;
-    for (int n = wg; n < N; n += 2) {
-      const int st = n % NS, sb = n & 1;
-      const int i0 = (t_lo + n % ntq) * BM;
-      if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
-      tc_fence_after();
-      // lse * log2e and Delta of this step's query columns
-      const float* lse_s = reinterpret_cast<const float*>(sStage + st * C::STAGE_BYTES + 2 * C::QT_BYTES);
-      const float* dl_s = lse_s + BM;
-      const bool full = (i0 >= band_q_lo(g, jhi)) && (i0 + BM - 1 <= band_q_hi(g, j0));
-      // query columns c of this tile that see key j: i0 + c in [band_q_lo(j), band_q_hi(j)]
-      const int clo = band_q_lo(g, j) - i0;
-      const int chi = band_q_hi(g, j) - i0;
-      // this warpgroup's S^T / dP^T columns with one TMEM wait
-      uint32_t sv[CW], dv[CW];
-#pragma unroll
-      for (int c = 0; c < CW / 32; ++c) {
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
-        if (C::NEED_V)
-          tmem_ld32(tmem + lane_off + C::DP_COL + sb * BM + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
-      }
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < CW / 32; ++c) {
-        const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
-        const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
-        const int cb = c * 32;  // tile-local query column of this chunk
-        uint32_t pp[16], dd[16];
-        if (full) kv_chunk<true, C::DO_DV, C::DO_DK>(svc, dvc, lse_s, dl_s, sl2, cb, clo, chi, pp, dd);
-        else kv_chunk<false, C::DO_DV, C::DO_DK>(svc, dvc, lse_s, dl_s, sl2, cb, clo, chi, pp, dd);
-        // P^T / dS^T as fp16 pairs: query columns 2t, 2t+1 -> TMEM column t
-        if (C::DO_DV) tmem_st16(tmem + lane_off + C::S_COL + sb * BM + cb / 2, pp);
-        if (C::DO_DK) tmem_st16(tmem + lane_off + C::DP_COL + sb * BM + cb / 2, dd);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full + sb);
-    }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
-      tc_fence_after();
-      // each warpgroup writes half of the accumulator's columns (dK scaled)
-      const bool row_ok = j < g.L;
-      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
-      constexpr bool wr_dk = MODE == kModeDK;
-      const uint32_t col = wr_dk ? C::DK_COL : C::DV_COL;
-      const float mul = wr_dk ? g.scale : 1.f;
-      float* dst = (wr_dk ? p.out0 : p.out1) + off;
-      constexpr int NCH = D / 64;  // 32-column chunks per warpgroup
-      const int c0 = wg * NCH;
-#pragma unroll
-      for (int cc = 0; cc < NCH; ++cc) {
-        const int c = c0 + cc;
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + col + c * 32, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
-    }
-  }
-
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
 
 // ===========================================================================
 // dK / dV for head dim <= 128 with 128-row query steps, so that every MMA has
@@ -708,6 +415,362 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t a[32];
         tmem_ld32(tmem + lane_off + col + c * 32, a);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dK / dV for head dim 256 with 128-row query steps, so that every MMA has
+// N >= 128.  dK and dV of a 128-key tile fill all 512 TMEM columns, so a
+// dV-only CTA and a dK-only CTA share each tile (two launches).
+//
+// dV CTA (MODE kModeDV).  TMEM: dV [0, 256), S^T in two buffers [256, 384)
+//   and [384, 512).  P^T(n) goes back as fp16 pairs into its S buffer (each
+//   warpgroup into the first half of its own 64 columns), where dV(n) reads
+//   it as the TMEM A operand (N = 256).  Shared memory: K resident (64 KB),
+//   Q streamed in 64-column slices through a 6-slot ring (S^T only), and one
+//   64 KB dO tile (the MN-major B operand of dV).  MMA issue order:
+//   dV(n) | S(n + 2): the S^T double buffer lets the elementwise warps work
+//   on step n + 1 while the tensor pipe runs dV(n) and S(n + 2), and the dO
+//   tile of step n + 1 loads while S(n + 2) runs.
+// dK CTA (MODE kModeDK).  TMEM: dK [0, 256), S^T [256, 384), dP^T [384, 512);
+//   dS^T(n) goes back as fp16 pairs into the dP buffer (same column plan).
+//   Shared memory: K and V resident (128 KB), one 64 KB Q tile (K-major B
+//   of S^T, then MN-major B of dK), dO streamed in 64-column slices (dP^T
+//   only).  MMA issue order: dK(n) | dP(n + 1) | S(n + 1): dP(n + 1) runs
+//   while Q(n + 1) loads into the buffer dK(n) has just released.
+// dS is formed from the fp16-rounded P, as dV uses it.
+template <int MODE>
+struct Kv256Cfg {
+  static constexpr int D = 256, BNK = 128, BM = 128, CW = 64, KCH = 4;
+  static constexpr int TILE = 128 * D * 2;   // 64 KB: a 128-row K, V, Q or dO tile
+  static constexpr int SLICE = 128 * 128;    // 16 KB: one 64-column chunk of a tile
+  static constexpr bool DV = MODE == kModeDV;
+  static constexpr int RES = DV ? TILE : 2 * TILE;          // K (and V)
+  static constexpr int NSL = DV ? 6 : 2;                    // slice ring depth (Q for dV, dO for dK)
+  static constexpr int OFF_T = RES;                         // the one dO (dV) or Q (dK) tile
+  static constexpr int OFF_SL = RES + TILE;                 // slice ring
+  static constexpr int DATA = OFF_SL + NSL * SLICE;
+  static constexpr uint32_t ACC_COL = 0, S_COL = 256, DP_COL = 384;
+  static constexpr size_t SMEM = (size_t)DATA + 1024 + 1024;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
+};
+
+// A operand column of K-step ks (16 query rows) in a buffer where warpgroup
+// w packed its 64 columns into [64 w, 64 w + 32).
+__device__ __forceinline__ uint32_t packed_col(int ks) { return (uint32_t)((ks >> 2) * 64 + (ks & 3) * 8); }
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv256_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                      const BwdParams p) {
+  using C = Kv256Cfg<MODE>;
+  constexpr int BNK = C::BNK, BM = C::BM, CW = C::CW, KCH = C::KCH, NSL = C::NSL, D = C::D;
+  constexpr bool DVM = C::DV;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sK = base;
+  unsigned char* sV = base + C::TILE;  // dK CTA only
+  unsigned char* sT = base + C::OFF_T;
+  unsigned char* sSl = base + C::OFF_SL;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::DATA);
+  uint64_t* kv_full = bars;           // [1] resident K (and V)
+  uint64_t* t_full = kv_full + 1;     // [1] the dO (dV) or Q (dK) tile of a step landed
+  uint64_t* t_empty = t_full + 1;     // [1] ... and was released by dV / dK
+  uint64_t* sl_full = t_empty + 1;    // [NSL] slice ring
+  uint64_t* sl_empty = sl_full + NSL; // [NSL]
+  uint64_t* s_full = sl_empty + NSL;  // [2] S^T(n) in TMEM (dK CTA: buffer 0 only)
+  uint64_t* dp_full = s_full + 2;     // [1] dP^T(n) in TMEM (dK CTA)
+  uint64_t* p_full = dp_full + 1;     // [2] P^T(n) (dV) / dS^T(n) (dK) packed into TMEM by both warpgroups
+  uint64_t* acc_done = p_full + 2;    // [1]
+  uint64_t* mma_drain = acc_done + 1; // [1] every issued MMA finished (before TMEM is released)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bkv = blockIdx.x;  // b * Hkv + kv head
+  const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
+  const int j0 = (int)blockIdx.y * BNK;
+  const int jhi = min(j0 + BNK, g.L) - 1;
+  // query rows that can see a key of this tile
+  const int qlo = band_q_lo(g, j0), qhi = band_q_hi(g, jhi);
+  const int t_lo = qlo / BM, t_hi = qhi / BM;
+  const int ntq = qlo <= qhi ? t_hi - t_lo + 1 : 0;
+  const int N = g.G * ntq;  // steps (head of group, query tile)
+  if (N == 0) {
+    // no query sees these keys (queries that are a suffix of the keys, with a
+    // window): their gradients are zero ("Lab 028 lab detail", "What I
+    // changed, in plain terms" item 5(b)).  Uniform over the CTA, before any
+    // barrier or Tensor Memory is set up.
+    zero_rows(DVM ? p.out1 : p.out0, bkv, j0, BNK, g.L, D);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(t_full, 1);
+    mbar_init(t_empty, 1);
+    for (int s = 0; s < NSL; ++s) {
+      mbar_init(sl_full + s, 1);
+      mbar_init(sl_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full + s, 1);
+      mbar_init(p_full + s, 256);
+    }
+    mbar_init(dp_full, 1);
+    mbar_init(acc_done, 1);
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto step_head = [&](int n) { return b * g.Hq + kvh * g.G + n / ntq; };
+  auto step_i0 = [&](int n) { return (t_lo + n % ntq) * BM; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producers
+    // Two independent streams, each loaded in the order the MMA thread consumes
+    // it and each waiting only on its own consumer: lane 0 the resident K (and
+    // V) and the whole tiles (dO for the dV CTA, Q for the dK CTA), lane 1 the
+    // 64-column slices (Q for the dV CTA, dO for the dK CTA).
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(kv_full, C::RES);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_3d(sK + c * C::SLICE, &tmK, kv_full, c * 64, j0, bkv);
+        if (!DVM) tma_load_3d(sV + c * C::SLICE, &tmV, kv_full, c * 64, j0, bkv);
+      }
+      const CUtensorMap* mt = DVM ? &tmG : &tmQ;
+      int nt = 0;  // tiles issued
+      for (; nt < N; ++nt) {
+        if (nt >= 1 && !mbar_wait(t_empty, (nt - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(t_full, C::TILE);
+        for (int c = 0; c < KCH; ++c) tma_load_3d(sT + c * C::SLICE, mt, t_full, c * 64, step_i0(nt), step_head(nt));
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(kv_full, 0);
+        if (nt >= 1) mbar_wait_drain(t_full, (nt - 1) & 1);
+      }
+    } else if (lane == 1) {
+      const CUtensorMap* msl = DVM ? &tmQ : &tmG;
+      int ns = 0;  // slices issued
+      bool ok = true;
+      for (int m = 0; ok && m < N; ++m) {
+        for (int c = 0; c < KCH; ++c, ++ns) {
+          const int s = ns % NSL;
+          if (ns >= NSL && !mbar_wait(sl_empty + s, ((ns / NSL) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(sl_full + s, C::SLICE);
+          tma_load_3d(sSl + s * C::SLICE, msl, sl_full + s, c * 64, step_i0(m), step_head(m));
+        }
+      }
+      if (*abort_flag) drain_ring(sl_full, NSL, ns);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major), N = 128
+      const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (A in TMEM, B MN-major), N = 256
+      const uint64_t kdk = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vdk = smem_desc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t tmn = smem_desc_sw128(smem_u32(sT), BM * 128, 1024);  // the tile, MN-major
+      const uint64_t tk = smem_desc_sw128(smem_u32(sT), 16, 1024);         // the tile, K-major (dK CTA: Q)
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      int used = 0;  // slices consumed
+      // S^T or dP^T (A resident, B from the slice ring) into TMEM column col
+      auto issue_sliced = [&](uint64_t adesc, uint32_t col) -> bool {
+        for (int c = 0; c < KCH; ++c, ++used) {
+          const int s = used % NSL;
+          if (!mbar_wait(sl_full + s, (used / NSL) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint64_t bd = smem_desc_sw128(smem_u32(sSl + s * C::SLICE), 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(tmem + col, desc_add(adesc, c * C::SLICE + ks * 32), desc_add(bd, ks * 32), idS,
+                   (c | ks) ? 1u : 0u);
+          mma_commit(sl_empty + s);
+        }
+        return true;
+      };
+      // dV(n) / dK(n): accumulator += packed TMEM operand (from buffer col) x the tile (MN-major)
+      auto issue_grad = [&](int n, uint32_t col) {
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          mma_ts(tmem + C::ACC_COL, tmem + col + packed_col(ks), desc_add(tmn, ks * 2048), idG,
+                 (n > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(t_empty);
+      };
+      if (DVM) {
+        if (ok) ok = issue_sliced(kdk, C::S_COL);
+        if (ok) mma_commit(s_full + 0);
+        if (ok && N > 1) ok = issue_sliced(kdk, C::S_COL + 128);
+        if (ok && N > 1) mma_commit(s_full + 1);
+        for (int n = 0; ok && n < N; ++n) {
+          const uint32_t sb = C::S_COL + 128 * (n & 1);
+          if (!mbar_wait(p_full + (n & 1), (n >> 1) & 1, abort_flag) || !mbar_wait(t_full, n & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_grad(n, sb);  // dV(n); S(n + 2) below overwrites the buffer after it (issue order)
+          if (n + 2 < N) {
+            if (!issue_sliced(kdk, sb)) { ok = false; break; }
+            mma_commit(s_full + (n & 1));
+          }
+        }
+      } else {
+        auto issue_s = [&](int n) -> bool {  // S^T(n) = K Q(n)^T, Q from the tile (K-major)
+          if (!mbar_wait(t_full, n & 1, abort_flag)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::SLICE + (ks & 3) * 32;
+            mma_ss(tmem + C::S_COL, desc_add(kdk, off), desc_add(tk, off), idS, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(s_full);
+          return true;
+        };
+        if (ok) ok = issue_s(0) && issue_sliced(vdk, C::DP_COL);
+        if (ok) mma_commit(dp_full);
+        for (int n = 0; ok && n < N; ++n) {
+          if (!mbar_wait(p_full, n & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_grad(n, C::DP_COL);  // dK(n); releases the Q tile
+          if (n + 1 < N) {
+            if (!issue_sliced(vdk, C::DP_COL)) { ok = false; break; }  // dP(n + 1): after dK(n) in issue order
+            mma_commit(dp_full);
+            if (!issue_s(n + 1)) { ok = false; break; }
+          }
+        }
+      }
+      if (ok) mma_commit(acc_done);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    // warpgroup wg (warps 2-5 / 6-9) takes query columns [64 wg, 64 wg + 64);
+    // warp % 4 fixes the TMEM lane quarter, i.e. the key rows
+    const int wg = (warp - 2) >> 2;
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int j = j0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    const int cw0 = wg * CW;
+    bool ok = true;
+    const size_t dplane = (size_t)g.B * g.Hq * p.Lpad;  // offset of the Delta plane
+    for (int n = 0; n < N; ++n) {
+      const int i0 = step_i0(n);
+      const int sbuf = DVM ? (n & 1) : 0;
+      const uint32_t scol = C::S_COL + 128 * sbuf;
+      const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + i0 + cw0;
+      // lse * log2e of this warpgroup's 64 query columns, loaded while S^T(n) is computed
+      float lv[64];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_g) + q);
+        lv[4 * q] = l4.x;
+        lv[4 * q + 1] = l4.y;
+        lv[4 * q + 2] = l4.z;
+        lv[4 * q + 3] = l4.w;
+      }
+      const uint32_t spar = DVM ? ((n >> 1) & 1) : (n & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + sbuf, spar, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(tmem + lane_off + scol + cw0, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld32(tmem + lane_off + scol + cw0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_wait_ld();
+      const bool full = (i0 >= band_q_lo(g, jhi)) && (i0 + BM - 1 <= band_q_hi(g, j0));
+      // query columns c of this tile that see key j: i0 + c in [band_q_lo(j), band_q_hi(j)]
+      const int clo = band_q_lo(g, j) - i0;
+      const int chi = band_q_hi(g, j) - i0;
+      if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
+      else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
+      // P^T as fp16 pairs; dS below uses the same rounded P
+      uint32_t pp[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) pp[e >> 1] = pack_half2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+      if (DVM) {
+        // into the first half of this warpgroup's own columns of the S buffer
+        tmem_st32(tmem + lane_off + scol + cw0, pp);
+      } else {
+        // Delta of the 64 columns, loaded while dP^T(n) is computed
+        float dl[64];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 d4 = __ldg(reinterpret_cast<const float4*>(lse_g + dplane) + q);
+          dl[4 * q] = d4.x;
+          dl[4 * q + 1] = d4.y;
+          dl[4 * q + 2] = d4.z;
+          dl[4 * q + 3] = d4.w;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(dp_full, n & 1, abort_flag))) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dd[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two 32-column halves keep dP^T's registers small
+          uint32_t dv[32];
+          tmem_ld32(tmem + lane_off + C::DP_COL + cw0 + 32 * h, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pp[16 * h + (e >> 1)]));
+            dd[16 * h + (e >> 1)] = pack_half2(pf.x * (__uint_as_float(dv[e]) - dl[32 * h + e]),
+                                               pf.y * (__uint_as_float(dv[e + 1]) - dl[32 * h + e + 1]));
+          }
+        }
+        // into the first half of this warpgroup's own columns of the dP buffer
+        tmem_st32(tmem + lane_off + C::DP_COL + cw0, dd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + sbuf);
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
+      tc_fence_after();
+      // each warpgroup writes half of the accumulator's columns (dK scaled)
+      const bool row_ok = j < g.L;
+      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+      const float mul = DVM ? 1.f : g.scale;
+      float* dst = (DVM ? p.out1 : p.out0) + off;
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = wg * (D / 64) + cc;
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + C::ACC_COL + c * 32, a);
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
@@ -1207,26 +1270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// 2-D fp32 tensor map over the row statistics, viewed as [2 * BH rows, Lpad]
-// (the lse plane, then the Delta plane) with a box_floats x 1 box.
-cudaError_t make_tmap_stats(CUtensorMap* m, const void* ptr, int Lpad, int rows, int box_floats) {
-  void* f = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return cudaErrorNotSupported;
-  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  cuuint64_t dims[2] = {(cuuint64_t)Lpad, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)Lpad * 4};
-  cuuint32_t box[2] = {(cuuint32_t)box_floats, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int D>
 cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                      const uint16_t* g16, const float* stats, int Lpad, float* dq, float* dk, float* dv, int* status,
@@ -1238,28 +1281,6 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
   p.Lpad = Lpad;
   p.status = status;
   if (which == 0) {
-    auto run = [&](auto mode_tag) -> cudaError_t {
-      constexpr int MODE = decltype(mode_tag)::value;
-      using C = KvCfg<D, MODE>;
-      CUtensorMap tq, tk, tv, tg, ts;
-      cudaError_t e2;
-      if ((e2 = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-      if ((e2 = make_tmap_stats(&ts, stats, Lpad, 2 * g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-      auto kern = dkdv_tc_kernel<D, MODE>;
-      if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
-          cudaSuccess)
-        return e2;
-      BwdParams pm = p;
-      pm.out0 = dk;
-      pm.out1 = dv;
-      pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
-      dim3 grid(g.B * g.Hkv, pm.n_tiles);
-      kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, ts, pm);
-      return cudaGetLastError();
-    };
     if constexpr (D <= 128) {
       using C = Kv128Cfg<D>;
       CUtensorMap tq, tk, tv, tg;
@@ -1280,8 +1301,29 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
       return cudaGetLastError();
     } else {
-      if ((e = run(std::integral_constant<int, kModeDV>{})) != cudaSuccess) return e;
-      return run(std::integral_constant<int, kModeDK>{});
+      auto run256 = [&](auto mode_tag) -> cudaError_t {
+        constexpr int MODE = decltype(mode_tag)::value;
+        using C = Kv256Cfg<MODE>;
+        CUtensorMap tq, tk, tv, tg;
+        cudaError_t e2;
+        if ((e2 = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+        if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
+        if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
+        if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
+        auto kern = dkdv256_tc_kernel<MODE>;
+        if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
+            cudaSuccess)
+          return e2;
+        BwdParams pm = p;
+        pm.out0 = dk;
+        pm.out1 = dv;
+        pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
+        dim3 grid(g.B * g.Hkv, pm.n_tiles);
+        kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
+        return cudaGetLastError();
+      };
+      if ((e = run256(std::integral_constant<int, kModeDV>{})) != cudaSuccess) return e;
+      return run256(std::integral_constant<int, kModeDK>{});
     }
   } else if constexpr (D <= 128) {
     using C = Dq128Cfg<D>;
