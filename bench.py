@@ -44,7 +44,7 @@ KERNEL_FLOPS_PER_PAIR_D = {
     "bwd_dkdv_tc": 8,     # S^T, dP^T recomputed; dV += P^T dO; dK += dS^T Q (tcgen05)
     "bwd_dq_tc": 6,       # S, dP recomputed; dQ += dS K (tcgen05)
 }
-HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_rowstats"}
+HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_rowstats", "fwd_decode"}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -220,7 +220,10 @@ def oracle_sample_seconds(w, Ls, inputs=None):
 
     q, k, v, dO = inputs if inputs is not None else _oracle_sample_inputs(w, Ls)
     t0 = time.perf_counter()
-    oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True, causal=w.causal)
+    if w.fwd_only:
+        oracle.forward(q, k, v, w.window, w.scale, band_only=True, causal=w.causal)
+    else:
+        oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True, causal=w.causal)
     return time.perf_counter() - t0
 
 
@@ -251,7 +254,7 @@ def oracle_sample_length(w, target_s: float) -> int:
 
 
 def oracle_useful_flops(w, Ls) -> int:
-    return 14 * w.D * (w.Hq // w.Hkv) * _sample_pairs(w, Ls)
+    return (4 if w.fwd_only else 14) * w.D * (w.Hq // w.Hkv) * _sample_pairs(w, Ls)
 
 
 def cpu_oracle_sample(w, target_s: float):
@@ -299,6 +302,16 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+def _band_keys(w):
+    """Keys that some query row of the workload sees (the decode kernel's range)."""
+    off = w.L - w.q_rows
+    win = w.window if 0 < w.window < w.L else 0
+    lo = max(0, off - win + 1) if win else 0
+    last = w.L - 1  # the last query row sits at key position L - 1
+    hi = last if w.causal else (min(w.L - 1, last + win - 1) if win else w.L - 1)
+    return hi - lo + 1
+
+
 def _variant_keys(w):
     """Config keys of a band variant (queries a suffix of the keys, or non-causal)."""
     out = {}
@@ -306,6 +319,8 @@ def _variant_keys(w):
         out["Lq"] = w.q_rows
     if not w.causal:
         out["causal"] = False
+    if w.fwd_only:
+        out["step"] = "forward only (decode)"
     return out
 
 
@@ -339,12 +354,15 @@ def run_ours(args, w, world, rank, local_rank):
     torch.cuda.reset_peak_memory_stats(dev)
     o = torch.empty((B, Hq, Lq, D), **f32)
     lse = torch.empty((B, Hq, Lq), **f32)
-    dq = torch.empty((B, Hq, Lq, D), **f32)
-    dk = torch.empty((B, Hkv, L, D), **f32)
-    dv = torch.empty((B, Hkv, L, D), **f32)
+    if w.fwd_only:  # a decode step has no backward
+        dq = dk = dv = None
+    else:
+        dq = torch.empty((B, Hq, Lq, D), **f32)
+        dk = torch.empty((B, Hkv, L, D), **f32)
+        dv = torch.empty((B, Hkv, L, D), **f32)
     if variant:
         fws_b = swa.fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
-        bws_b = swa.bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
+        bws_b = 0 if w.fwd_only else swa.bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
     else:
         fws_b = swa.fwd_workspace_bytes(B, Hq, Hkv, L, D, W)
         bws_b = swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W)
@@ -354,7 +372,9 @@ def run_ours(args, w, world, rank, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        if variant:
+        if w.fwd_only:
+            swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
+        elif variant:
             swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
             swa.swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, W, w.causal, w.scale, bws, stream)
         else:
@@ -397,24 +417,26 @@ def run_ours(args, w, world, rank, local_rank):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, dist, dev)
-    useful = w.fwd_flops() + w.bwd_flops()
+    useful = w.fwd_flops() + (0 if w.fwd_only else w.bwd_flops())
     value = whole_job_tflops(world, useful, args.steps, total_ms)
     launches = sum(n for n, _ in kernels.values())
 
     # end to end through the public API: pinned host inputs in, results out
     pin = lambda t: t.pin_memory()  # noqa: E731
     hq, hk, hv, hdO = (pin(t) for t in (q_h, k_h, v_h, dO_h))
-    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdO))
+    results = (o, lse) if w.fwd_only else (o, lse, dq, dk, dv)
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
+    ins = ((q, hq), (k, hk), (v, hv)) if w.fwd_only else ((q, hq), (k, hk), (v, hv), (dO, hdO))
+    h2d = sum(h.numel() * h.element_size() for _, h in ins)
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
     e2e_steps = max(3, min(args.steps, 10))
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def e2e_step():
-        for dst, src in ((q, hq), (k, hk), (v, hv), (dO, hdO)):
+        for dst, src in ins:
             dst.copy_(src, non_blocking=True)
         step()
-        for dst, src in zip(outs_h, (o, lse, dq, dk, dv)):
+        for dst, src in zip(outs_h, results):
             dst.copy_(src, non_blocking=True)
 
     e2e_step()
@@ -439,6 +461,8 @@ def run_ours(args, w, world, rank, local_rank):
     if kname in HBM_KERNELS:
         if kname in ("bwd_delta", "bwd_rowstats"):
             alg = B * Hq * Lq * (D * 4 + D * 2 + 4)
+        elif kname == "fwd_decode":  # the K and V rows in band (bf16) once per kv head, q in, o and lse out
+            alg = B * Hkv * _band_keys(w) * D * 2 * 2 + B * Hq * Lq * (D * 2 + D * 4 + 4)
         else:  # bf16 read + fp16 write of q, k, v (and dO in the backward)
             alg = 4 * D * B * (Hq * Lq + 2 * Hkv * L)
         achieved = alg / avg_s / 1e9

@@ -182,9 +182,10 @@ const char* swa_attn_strerror(int code) {
 }
 
 size_t swa_attn_fwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
-  (void)window;
-  (void)causal;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || !swa::fwd_tc_supported(D)) return 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || Hq % Hkv != 0 || window < 0 || !swa::fwd_tc_supported(D))
+    return 0;
+  const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, 1.f);
+  if (swa::decode_supported(g)) return round_up(swa::decode_workspace_bytes(g), 256);
   return fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
 }
 
@@ -221,6 +222,15 @@ int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, flo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_ptr_for_current_device(&rc);
   if (!status) return rc;
+  if (swa::decode_supported(g)) {
+    // at most 16 query rows per kv head (a decode step): one pass over the
+    // bf16 cache on the CUDA cores, no fp16 copies
+    float* ws = static_cast<float*>(workspace);
+    if (launch("fwd_decode", s, [&] { return swa::launch_fwd_decode(g, q, k, v, o, lse, ws, status, s); }) !=
+        cudaSuccess)
+      return SWA_ERR_CUDA;
+    return SWA_OK;
+  }
   const FwdWs w = fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);

@@ -70,6 +70,13 @@ cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst,
 // limit_cycles and latches kStatusTimeout in *status.
 cudaError_t launch_selftest_timeout(int* status, long long limit_cycles, cudaStream_t s);
 bool fwd_tc_supported(int D);
+// Decode-shaped forward (decode.cu): at most kDecodeMaxRows = G * Lq query
+// rows per kv head, read as bf16 straight from q, k, v (no fp16 copies).
+constexpr int kDecodeMaxRows = 16;
+bool decode_supported(const Geom& g);
+size_t decode_workspace_bytes(const Geom& g);  // fp32 chunk partials; 0 when one chunk suffices
+cudaError_t launch_fwd_decode(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
+                              float* lse, float* ws, int* status, cudaStream_t s);
 // Head dim 512: 2-CTA cluster forward (tc_fwd512.cu).
 cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s);

@@ -24,7 +24,9 @@ Two more workloads exercise the band variants the same page's parity sweep
 covers ("Gradient parity": qL < kL, windows causal and not): the sliding
 layer with its queries a suffix of the keys, and a non-causal window.  A
 suffix workload draws the full-length tensors with the recipe above and keeps
-the last Lq rows of q and dO.
+the last Lq rows of q and dO.  The decode workload is one generation step
+(Lq = 1, forward only) of a batch of 8 over a 16,384-token cache of the
+global layer.
 """
 from __future__ import annotations
 
@@ -49,6 +51,7 @@ class Workload:
     seed: int = 0
     Lq: int = 0          # query rows (the last Lq of the L key positions); 0 means L
     causal: bool = True
+    fwd_only: bool = False  # a decode step: the forward alone
 
     @property
     def q_rows(self) -> int:
@@ -106,6 +109,7 @@ WORKLOADS = {
         Workload("suffix_q2048_k8192_d256_w1024", 1, 32, 16, 8192, 256, 1024, do_scale=0.1, seed=20260006,
                  Lq=2048),
         Workload("noncausal_l8192_d128_w512", 1, 8, 4, 8192, 128, 512, seed=20260007, causal=False),
+        Workload("decode_b8_q1_k16384_d512", 8, 32, 4, 16384, 512, 0, seed=20260008, Lq=1, fwd_only=True),
     ]
 }
 

@@ -296,3 +296,45 @@ def test_suffix_rows_equal_full_problem_rows():
     torch.cuda.synchronize()
     assert torch.allclose(o_suf, o_full[:, :, Lk - Lq:], atol=2e-6, rtol=0)
     assert torch.allclose(lse_suf, lse_full[:, :, Lk - Lq:], atol=2e-6, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# decode steps: at most 16 query rows per kv head (G * Lq <= 16) run on the
+# decode kernel (bf16 cache read once per kv head, chunks merged at the end)
+
+DECODE = [
+    # B, Hq, Hkv, Lq, Lk, D, window, causal
+    (1, 32, 4, 1, 16384, 512, 0, True),     # global layer, one token, many chunks
+    (2, 32, 16, 4, 9000, 256, 1024, True),  # sliding layer, 4-token suffix
+    (1, 8, 4, 3, 5000, 128, 100, False),    # non-causal window
+    (1, 16, 1, 1, 777, 64, 0, True),        # 16 heads per kv head: M = 16
+    (1, 4, 1, 4, 130, 128, 0, True),        # M = 16 from Lq x G
+    (3, 6, 3, 1, 1, 64, 0, True),           # a cache of one key
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,D,window,causal", DECODE)
+def test_decode_elementwise(oracle_mod, B, Hq, Hkv, Lq, Lk, D, window, causal):
+    import sliding_window_attention_gb300 as swa
+
+    q, k, v, dO = make_inputs(B, Hq, Hkv, Lk, D, seed=3000 + Lq + Lk + D + window)
+    q = q[:, :, Lk - Lq:].contiguous()
+    scale = 1.0 / math.sqrt(D)
+    o_ref, lse_ref = oracle_mod.forward(q, k, v, window, scale, band_only=True, causal=causal)
+    o, lse = swa.forward(q.cuda(), k.cuda(), v.cuda(), window, scale, causal=causal)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    assert_lse_close(lse.cpu().numpy(), lse_ref)
+    assert_close("o", o.cpu().numpy(), o_ref)
+
+
+def test_decode_then_backward_matches_oracle(oracle_mod):
+    """The backward of a decode-shaped call (tensor-core path) takes the
+    decode forward's o and lse."""
+    B, Hq, Hkv, Lq, Lk, D, W = 1, 8, 2, 2, 1500, 128, 300
+    q, k, v, dO = make_inputs(B, Hq, Hkv, Lk, D, seed=41)
+    q, dO = q[:, :, Lk - Lq:].contiguous(), dO[:, :, Lk - Lq:].contiguous()
+    ref = oracle_mod.backward(q, k, v, dO, W, 0.1, band_only=True)
+    got = gpu_fwd_bwd(q, k, v, dO, W, 0.1)
+    for n in ("o", "dq", "dk", "dv"):
+        assert_close(n, got[n].numpy(), ref[n])
