@@ -23,8 +23,8 @@
 // write P^T as the K-major B operand.  K and V arrive in 32 KB slots (two
 // 64-column chunks of 128 key rows, one TMA instruction each) through one
 // ring, in the order the MMAs consume them.  The key range is split into
-// chunks over about two waves of CTAs; a second kernel merges the chunks'
-// (max, sum, unnormalised O).
+// chunks so that all CTAs run in one wave; a second kernel merges the
+// chunks' (max, sum, unnormalised O).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -385,32 +385,53 @@ __global__ void __launch_bounds__(kThr, 1)
 
 // Merge of the chunks of one packed row (b * Hkv + kv head, m): with
 // w_c = 2^(max_c - max), o = sum_c w_c O_c / sum_c w_c l_c and
-// lse = (max + log2 sum_c w_c l_c) ln 2.  One block per row, a thread per
-// head-dim column.
+// lse = (max + log2 sum_c w_c l_c) ln 2.  One block per row: the chunk
+// weights are formed once in shared memory, then a thread per head-dim
+// column sums its column over the chunks with independent loads.
+constexpr int kMaxChunks = 1024;
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecParams p, int D) {
+  __shared__ float wts[kMaxChunks];
+  __shared__ float stat[2];
   const int row = blockIdx.x;  // (b * Hkv + kv head) * M + m
   const int rows = gridDim.x;
-  float mx = -INFINITY;
-  for (int c = 0; c < p.n_chunks; ++c) mx = fmaxf(mx, p.part_ml[((size_t)c * rows + row) * 2]);
-  float l = 0.f;
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const float mc = p.part_ml[((size_t)c * rows + row) * 2];
-    if (mc != -INFINITY) l += exp2f(mc - mx) * p.part_ml[((size_t)c * rows + row) * 2 + 1];
-  }
-  const float inv = 1.f / l;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float t = 0.f;
-    for (int c = 0; c < p.n_chunks; ++c) {
+  const int nc = p.n_chunks;
+  if (threadIdx.x < 32) {
+    float mx = -INFINITY;
+    for (int c = threadIdx.x; c < nc; c += 32) mx = fmaxf(mx, p.part_ml[((size_t)c * rows + row) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float l = 0.f;
+    for (int c = threadIdx.x; c < nc; c += 32) {
       const float mc = p.part_ml[((size_t)c * rows + row) * 2];
-      if (mc != -INFINITY) t = fmaf(exp2f(mc - mx), p.part_o[((size_t)c * rows + row) * D + d], t);
+      const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - mx);  // a chunk that saw no key adds nothing
+      wts[c] = w;
+      l += w * p.part_ml[((size_t)c * rows + row) * 2 + 1];
     }
-    p.o[(size_t)row * D + d] = t * inv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (threadIdx.x == 0) {
+      stat[0] = mx;
+      stat[1] = l;
+    }
   }
-  if (threadIdx.x == 0) p.lse[row] = (mx + log2f(l)) * kLn2;
+  __syncthreads();
+  const float inv = 1.f / stat[1];
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float t0 = 0.f, t1 = 0.f;
+    int c = 0;
+    for (; c + 1 < nc; c += 2) {
+      t0 = fmaf(wts[c], p.part_o[((size_t)c * rows + row) * D + d], t0);
+      t1 = fmaf(wts[c + 1], p.part_o[((size_t)(c + 1) * rows + row) * D + d], t1);
+    }
+    if (c < nc) t0 = fmaf(wts[c], p.part_o[((size_t)c * rows + row) * D + d], t0);
+    p.o[(size_t)row * D + d] = (t0 + t1) * inv;
+  }
+  if (threadIdx.x == 0) p.lse[row] = (stat[0] + log2f(stat[1])) * kLn2;
 }
 
-// Key range of the group and its split into chunks of whole blocks, aiming at
-// about two waves of CTAs on 152 SMs.
+// Key range of the group and its split into chunks of whole tiles, so that
+// all CTAs run in one wave (at most 148 of the 152 SMs: the stream is bound
+// by HBM, which that many SMs saturate, and one wave leaves no tail).
 struct DecPlan {
   int k_begin, k_end, chunk, n_chunks;
 };
@@ -421,12 +442,12 @@ DecPlan decode_plan(const Geom& g) {
   const int KB = T;
   const int range = pl.k_end - pl.k_begin;
   const int groups = g.B * g.Hkv;
-  int want = (2 * 152 + groups - 1) / groups;
+  int want = 148 / groups;
   const int max_chunks = (range + KB - 1) / KB;
   if (want > max_chunks) want = max_chunks;
   if (want < 1) want = 1;
   pl.chunk = ((range + want - 1) / want + KB - 1) / KB * KB;
-  pl.n_chunks = (range + pl.chunk - 1) / pl.chunk;
+  pl.n_chunks = (range + pl.chunk - 1) / pl.chunk;  // <= want <= 148, within the merge's kMaxChunks
   return pl;
 }
 
