@@ -335,6 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cw0 = wg * CW;
     bool ok = true;
     const size_t dplane = (size_t)g.B * g.Hq * p.Lpad;  // offset of the Delta plane
+    // loop invariants of the band: the query rows that see this thread's key
+    // j, and those that see every key of the tile (hoisted: recomputing them
+    // per step pushed the kernel past its register budget)
+    const int qlo_j = band_q_lo(g, j), qhi_j = band_q_hi(g, j);
+    const int qlo_all = band_q_lo(g, jhi), qhi_all = band_q_hi(g, j0);
     for (int n = 0; n < N; ++n) {
       const int i0 = step_i0(n);
       const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + i0 + cw0;
@@ -356,10 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(s_read);
-      const bool full = (i0 >= band_q_lo(g, jhi)) && (i0 + BM - 1 <= band_q_hi(g, j0));
-      // query columns c of this tile that see key j: i0 + c in [band_q_lo(j), band_q_hi(j)]
-      const int clo = band_q_lo(g, j) - i0;
-      const int chi = band_q_hi(g, j) - i0;
+      const bool full = (i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all);
+      // query columns c of this tile that see key j: i0 + c in [qlo_j, qhi_j]
+      const int clo = qlo_j - i0;
+      const int chi = qhi_j - i0;
       if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
       else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
       // P^T as fp16 pairs (the dV operand); dS below uses the same rounded P
@@ -691,6 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cw0 = wg * CW;
     bool ok = true;
     const size_t dplane = (size_t)g.B * g.Hq * p.Lpad;  // offset of the Delta plane
+    // loop invariants of the band: the query rows that see this thread's key
+    // j, and those that see every key of the tile (hoisted: recomputing them
+    // per step pushed the kernel past its register budget)
+    const int qlo_j = band_q_lo(g, j), qhi_j = band_q_hi(g, j);
+    const int qlo_all = band_q_lo(g, jhi), qhi_all = band_q_hi(g, j0);
     for (int n = 0; n < N; ++n) {
       const int i0 = step_i0(n);
       const int sbuf = DVM ? (n & 1) : 0;
@@ -713,10 +723,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + scol + cw0, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_ld32(tmem + lane_off + scol + cw0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld();
-      const bool full = (i0 >= band_q_lo(g, jhi)) && (i0 + BM - 1 <= band_q_hi(g, j0));
-      // query columns c of this tile that see key j: i0 + c in [band_q_lo(j), band_q_hi(j)]
-      const int clo = band_q_lo(g, j) - i0;
-      const int chi = band_q_hi(g, j) - i0;
+      const bool full = (i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all);
+      // query columns c of this tile that see key j: i0 + c in [qlo_j, qhi_j]
+      const int clo = qlo_j - i0;
+      const int chi = qhi_j - i0;
       if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
       else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
       // P^T as fp16 pairs; dS below uses the same rounded P

@@ -55,19 +55,14 @@ constexpr int kSmemMax = 232448;  // dynamic shared memory per block on sm_103 (
 template <int D>
 struct FwdCfg {
   // key tile rows: the K (and V) tiles must leave room for >= 2 pipeline stages
-  static constexpr int BN = (D <= 128) ? 128 : 64;
-  static constexpr bool SPLIT = (D <= 128);          // two softmax warpgroups share each tile's columns
-  static constexpr int THREADS = 64 + 128 * (SPLIT ? 2 : 1);  // warp 0 TMA, warp 1 MMA, warps 2.. softmax
+  static constexpr int BN = 64;
+  static constexpr int THREADS = 64 + 128;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
   static constexpr int KCH = D / 64;                // 64-column (128-byte) chunks of a Q / K / V row
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int K_BYTES = BN * D * 2;
   static constexpr int V_BYTES = BN * D * 2;
-  // mbarriers (512 B), then in split mode the (m, l) exchange ([2][128]
-  // float2) and the row-max exchange ([2 parity][2 warpgroups][128] float),
-  // then a block of ones (512 B)
-  static constexpr int XCH_OFF = 512;
-  static constexpr int XM_OFF = XCH_OFF + (SPLIT ? 2048 : 0);
-  static constexpr int ONES_OFF = XM_OFF + (SPLIT ? 2048 : 0);
+  // mbarriers (512 B), then a block of ones (512 B)
+  static constexpr int ONES_OFF = 512;
   static constexpr int BAR_BYTES = ONES_OFF + 512;
   // as many K/V stages as shared memory holds (TMA latency hiding), 2..8
   static constexpr int NS_FIT = (kSmemMax - 1024 - BAR_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
@@ -75,14 +70,12 @@ struct FwdCfg {
   static constexpr int O_COL = 0;                   // O at [0, D)
   static constexpr int S_COL = 256;                 // S buffers at [256, 256 + 2 BN)
   // row sums l = P . 1 accumulated by the tensor core (16 identical columns)
-  static constexpr int L_COL = (D <= 128) ? 128 : S_COL + 2 * BN;
+  static constexpr int L_COL = S_COL + 2 * BN;
   static constexpr size_t SMEM = (size_t)Q_BYTES + (size_t)NS * (K_BYTES + V_BYTES) + BAR_BYTES + 1024 /*align*/;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(D <= 256, "O must fit below the S buffers (head dim 512 has its own kernel)");
+  static_assert(D == 256, "head dim 256 (64 and 128: fwd_pp_kernel; 512: the cluster kernel)");
   static_assert(S_COL + 2 * BN <= 512, "TMEM columns");
-  static_assert(SPLIT || (L_COL + 16 <= 512 && (L_COL >= S_COL + 2 * BN || L_COL + 16 <= S_COL)),
-                "TMEM columns for l");
-  static_assert(!SPLIT || BN == 128, "column split assumes 128-key tiles");
+  static_assert(L_COL + 16 <= 512 && L_COL >= S_COL + 2 * BN, "TMEM columns for l");
 };
 
 struct FwdParams {
@@ -188,12 +181,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint64_t* s_full = v_empty + NS;  // [2]
   uint64_t* p_full = s_full + 2;    // [2]
   uint64_t* o_done = p_full + 2;    // [1]: PV into O complete
-  uint64_t* mx_bar = o_done + 1;    // [2]: both warpgroups posted their partial row max (split mode)
-  uint64_t* mma_drain = mx_bar + 2;  // [1] every issued MMA finished (before TMEM is released)
+  uint64_t* mma_drain = o_done + 1;  // [1] every issued MMA finished (before TMEM is released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float2* ml_x = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(bars) + C::XCH_OFF);  // [2][128] (m, l)
-  float* xm = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bars) + C::XM_OFF);  // [2][2][128]
   // 16 x 16 block of fp16 ones (B operand of the row-sum MMA), no swizzle
   uint32_t* ones = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(bars) + C::ONES_OFF);
 
@@ -221,10 +211,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + s, 1);
-      mbar_init(p_full + s, C::SPLIT ? 256 : 128);
+      mbar_init(p_full + s, 128);
     }
     mbar_init(o_done, 1);
-    for (int s = 0; s < 2; ++s) mbar_init(mx_bar + s, 256);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -288,7 +277,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           mma_ts(tmem + C::O_COL, tmem + C::S_COL + sb * BN + ks * 8, bdesc, idPV, (m > 0 || ks > 0) ? 1u : 0u);
         }
         // l += P . 1: every 16 x 16 step reads the same block of ones
-        if constexpr (!C::SPLIT) {
+        {
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
             mma_ts(tmem + C::L_COL, tmem + C::S_COL + sb * BN + ks * 8, ones_desc, idL, (m > 0 || ks > 0) ? 1u : 0u);
@@ -317,102 +306,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // every MMA issued so far has finished before TMEM is released
       mma_commit(mma_drain);
       mbar_wait_drain(mma_drain, 0);
-    }
-  } else if (C::SPLIT && warp >= 2) {
-    // ---------------- softmax, two warpgroups per tile (64 columns each) ----------------
-    constexpr int HC = BN / 2;
-    const int wg = (warp - 2) >> 2;
-    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
-    const int i = i0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const int cb0 = wg * HC;
-    const float sl2 = g.scale * kLog2e;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int n = 0; n < nt; ++n) {
-      const int sb = n & 1;
-      const int j0 = (t_lo + n) * BN;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
-      tc_fence_after();
-      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
-      uint32_t sr[HC];
-#pragma unroll
-      for (int c = 0; c < HC / 32; ++c)
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + cb0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
-      tmem_wait_ld();
-      // visible key columns of this row, relative to this warpgroup's half
-      const int clo = band_key_lo(g, i) - j0 - cb0;
-      const int chi = band_key_hi(g, i) - j0 - cb0;
-      const float pmax = full ? softmax_tile_max<HC, true>(sr, sl2, clo, chi)
-                              : softmax_tile_max<HC, false>(sr, sl2, clo, chi);
-      // combine the two halves' maxima; after this barrier both warpgroups have
-      // also read their S columns, so packed P may overwrite them
-      xm[(sb * 2 + wg) * 128 + r] = pmax;
-      mbar_arrive(mx_bar + sb);
-      if (!__all_sync(0xffffffffu, mbar_wait(mx_bar + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
-      const float tmax = fmaxf(pmax, xm[(sb * 2 + (wg ^ 1)) * 128 + r]);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (tmax > m_run + kRescaleLog2) {
-        if (m_run != -INFINITY) {
-          alpha = fast_exp2(m_run - tmax);
-          rescale = true;
-        }
-        m_run = tmax;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN + cb0 / 2;
-      const float tsum = full ? softmax_tile_p<HC, true, true>(sr, sl2, m_use, clo, chi, p_taddr)
-                              : softmax_tile_p<HC, false, true>(sr, sl2, m_use, clo, chi, p_taddr);
-      l_run = l_run * alpha + tsum;
-      // PV(n - 1) must be complete before O is rescaled (and is waited for at
-      // every tile, so the o_done phase never runs more than one ahead)
-      if (n > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) { ok = false; break; }
-        tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, rescale) && n > 0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {  // this warpgroup's half of the O columns
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_off + C::O_COL + wg * (D / 2) + c * 32, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st32(tmem + lane_off + C::O_COL + wg * (D / 2) + c * 32, rr);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full + sb);
-    }
-    if (ok && nt > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nt - 1) & 1, abort_flag));
-    // row sum = the two warpgroups' partial sums (same running max)
-    ml_x[wg * 128 + r] = make_float2(m_run, l_run);
-    tc_fence_before();
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    tc_fence_after();
-    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-    if (ok) {
-      const float l_tot = ml_x[r].y + ml_x[128 + r].y;
-      const bool row_ok = i < g.Lq;
-      const float inv = 1.f / l_tot;
-      float* orow = p.o + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = wg * (D / 64) + cc;
-        uint32_t acc[32];
-        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, acc);
-        tmem_wait_ld();  // warp-collective: every lane loads, only valid rows store
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(orow + c * 32 + e) =
-                make_float4(__uint_as_float(acc[e]) * inv, __uint_as_float(acc[e + 1]) * inv,
-                            __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
-        }
-      }
-      if (row_ok && wg == 0) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
     }
   } else if (warp >= 2) {
     // ---------------- softmax / correction / epilogue (one warpgroup) ----------------
@@ -539,6 +432,316 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 in, bool& overflow) {
     o[e] = *reinterpret_cast<const uint32_t*>(&hv);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ===========================================================================
+// Forward for head dims 64 and 128: two 128-row query tiles per CTA (rows
+// 256 p .. 256 p + 255 of one head), each with its own softmax warpgroup, O
+// accumulator and S buffer, sharing every K / V tile.  While one warpgroup
+// turns its S into P, the tensor core works on the other tile, so the softmax
+// of one tile hides behind the other's MMAs, and each K / V tile is read once
+// for 256 query rows.
+//
+// TMEM: O of tile w at [w D, w D + D), S of tile w at [256 + 128 w, +128); P
+// goes back as fp16 pairs into the first 64 columns of its S buffer.  Row
+// sums stay in registers (a thread owns a whole row).  MMA issue order per key
+// tile n: PV_A(n), S_A(n + 1), PV_B(n), S_B(n + 1): S_w(n + 1) overwrites
+// P_w(n) only after PV_w(n) (one thread issues, the tensor pipe runs in
+// order).  K and V travel in separate rings, filled by two producer lanes.
+template <int D>
+struct FwdPPCfg {
+  static constexpr int BM = 128, BN = 128, KCH = D / 64;
+  static constexpr int Q_BYTES = BM * D * 2;   // one query tile
+  static constexpr int KV_BYTES = BN * D * 2;  // one K (or V) tile
+  static constexpr int AVAIL = kSmemMax - 1024 /*align*/ - 1024 /*barriers*/ - 2 * Q_BYTES;
+  static constexpr int NT = AVAIL / KV_BYTES;  // K and V tiles that fit
+  static constexpr int NK = NT / 2 + NT % 2 > 6 ? 6 : NT / 2 + NT % 2;
+  static constexpr int NV = NT / 2 > 6 ? 6 : NT / 2;
+  static constexpr uint32_t S_COL = 256;
+  static constexpr size_t SMEM = 2 * (size_t)Q_BYTES + (size_t)(NK + NV) * KV_BYTES + 1024 + 1024;
+  static_assert(D == 64 || D == 128, "two O accumulators below the S buffers");
+  static_assert(NK >= 2 && NV >= 2, "ring depth");
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdPPCfg<D>;
+  constexpr int BM = C::BM, BN = C::BN, NK = C::NK, NV = C::NV;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = base;                    // [2][Q_BYTES]
+  unsigned char* sK = sQ + 2 * C::Q_BYTES;     // [NK][KV_BYTES]
+  unsigned char* sV = sK + NK * C::KV_BYTES;   // [NV][KV_BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NV * C::KV_BYTES);
+  uint64_t* q_full = bars;             // [1]
+  uint64_t* k_full = q_full + 1;       // [NK]
+  uint64_t* k_empty = k_full + NK;     // [NK]
+  uint64_t* v_full = k_empty + NK;     // [NV]
+  uint64_t* v_empty = v_full + NV;     // [NV]
+  uint64_t* s_full = v_empty + NV;     // [2] S of tile w in TMEM
+  uint64_t* p_full = s_full + 2;       // [2] P of tile w packed (and O rescaled) by its warpgroup
+  uint64_t* o_done = p_full + 2;       // [2] PV of tile w finished
+  uint64_t* mma_drain = o_done + 2;    // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bh = blockIdx.x;  // b * Hq + h
+  const int b = bh / g.Hq, h = bh - b * g.Hq;
+  const int bkv = b * g.Hkv + h / g.G;
+  const int pair = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first (n_qtiles: pairs here)
+  // tile w (A = 0, B = 1): query rows [i0w, ihiw]; key tiles [low, hiw]
+  // (empty when tile B has no rows).  Scalars, not arrays: an array indexed by
+  // the warpgroup would live in local memory.
+  const int i0A = 2 * pair * BM, i0B = i0A + BM;
+  const int ihiA = min(i0A + BM, g.Lq) - 1, ihiB = min(i0B + BM, g.Lq) - 1;
+  const int loA = band_key_lo(g, i0A) / BN, hiA = band_key_hi(g, ihiA) / BN;
+  const int loB = i0B < g.Lq ? band_key_lo(g, i0B) / BN : 1;
+  const int hiB = i0B < g.Lq ? band_key_hi(g, ihiB) / BN : 0;
+  const bool hasB = loB <= hiB;
+  const int u0 = loA, u1 = hasB ? max(hiA, hiB) : hiA;  // key tiles of either tile (loA <= loB)
+  auto uses = [&](int w, int n) { return w ? (n >= loB && n <= hiB) : (n >= loA && n <= hiA); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(s_full + w, 1);
+      mbar_init(p_full + w, 128);
+      mbar_init(o_done + w, 1);
+    }
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producers
+    // lane 0: both query tiles, then the K tiles; lane 1: the V tiles.  Each
+    // stream is loaded in the order the MMA thread consumes it (key tiles
+    // u0 .. u1 that either query tile uses) and waits only on its own ring.
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+      tma_load_4d(sQ, &tmQ, q_full, 0, i0A, 0, bh);
+      tma_load_4d(sQ + C::Q_BYTES, &tmQ, q_full, 0, i0B, 0, bh);  // rows past Lq read as zero
+      int nk = 0;
+      for (int n = u0; n <= u1; ++n) {
+        if (!uses(0, n) && !uses(1, n)) continue;
+        const int s = nk % NK;
+        if (nk >= NK && !mbar_wait(k_empty + s, ((nk / NK) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(k_full + s, C::KV_BYTES);
+        tma_load_4d(sK + s * C::KV_BYTES, &tmK, k_full + s, 0, n * BN, 0, bkv);
+        ++nk;
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(q_full, 0);
+        drain_ring(k_full, NK, nk);
+      }
+    } else if (lane == 1) {
+      int nv = 0;
+      for (int n = u0; n <= u1; ++n) {
+        if (!uses(0, n) && !uses(1, n)) continue;
+        const int s = nv % NV;
+        if (nv >= NV && !mbar_wait(v_empty + s, ((nv / NV) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(v_full + s, C::KV_BYTES);
+        tma_load_4d(sV + s * C::KV_BYTES, &tmV, v_full + s, 0, n * BN, 0, bkv);
+        ++nv;
+      }
+      if (*abort_flag) drain_ring(v_full, NV, nv);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BM, BN, 0, 0, 0, 0);  // Q (K-major) x K (K-major)
+      const uint32_t idPV = idesc_f16(BM, D, 0, 0, 0, 1);  // P (TMEM) x V (MN-major)
+      int kc = 0, vc = 0;  // K / V tiles consumed
+      int kpA = 0, kpB = 0;  // PV issued per query tile
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      // S_w from the K tile in slot kc % NK (waited for by the caller)
+      auto issue_s = [&](int w) {
+        const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ + w * C::Q_BYTES), 16, 1024);
+        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + (kc % NK) * C::KV_BYTES), 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32;
+          mma_ss(tmem + C::S_COL + 128 * w, desc_add(qdesc, (ks >> 2) * BM * 128 + off),
+                 desc_add(kdesc, (ks >> 2) * BN * 128 + off), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full + w);
+      };
+      auto wait_k = [&]() { return mbar_wait(k_full + kc % NK, (kc / NK) & 1, abort_flag); };
+      // first key tile: S of each tile that uses it
+      if (ok && (ok = wait_k())) {
+        tc_fence_after();
+        for (int w = 0; w < 2; ++w)
+          if (uses(w, u0)) issue_s(w);
+        mma_commit(k_empty + kc % NK);
+        ++kc;
+      }
+      for (int n = u0; ok && n <= u1; ++n) {
+        if (!uses(0, n) && !uses(1, n)) continue;
+        int m = n + 1;  // the next key tile either query tile uses
+        while (m <= u1 && !uses(0, m) && !uses(1, m)) ++m;
+        const bool next = m <= u1;
+        if (!mbar_wait(v_full + vc % NV, (vc / NV) & 1, abort_flag) || (next && !wait_k())) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t vdesc = smem_desc_sw128(smem_u32(sV + (vc % NV) * C::KV_BYTES), BN * 128, 1024);
+        for (int w = 0; w < 2 && ok; ++w) {
+          if (uses(w, n)) {
+            int& kp = w ? kpB : kpA;
+            if (!mbar_wait(p_full + w, kp & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+              mma_ts(tmem + D * w, tmem + C::S_COL + 128 * w + ks * 8, desc_add(vdesc, ks * 2048), idPV,
+                     (kp > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(o_done + w);
+            ++kp;
+          }
+          if (next && uses(w, m)) issue_s(w);  // after PV_w(n): S_w(m) overwrites P_w(n)
+        }
+        if (!ok) break;
+        mma_commit(v_empty + vc % NV);
+        ++vc;
+        if (next) {
+          mma_commit(k_empty + kc % NK);
+          ++kc;
+        }
+      }
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(mma_drain);
+      mbar_wait_drain(mma_drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax, one warpgroup per query tile
+    const int w = (warp - 2) >> 2;  // warps 2-5: tile A, 6-9: tile B
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int i0w = w ? i0B : i0A, ihiw = w ? ihiB : ihiA, low = w ? loB : loA, hiw = w ? hiB : hiA;
+    const int i = i0w + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t s_col = C::S_COL + 128 * w, o_col = D * w;
+    const float sl2 = g.scale * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    const int cnt = hiw - low + 1;  // key tiles of this query tile (0 for a missing tile B)
+    for (int k = 0; k < cnt; ++k) {
+      const int j0 = (low + k) * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + w, k & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      const bool full = (j0 >= band_key_lo(g, ihiw)) && (j0 + BN - 1 <= band_key_hi(g, i0w));
+      const int clo = band_key_lo(g, i) - j0;
+      const int chi = band_key_hi(g, i) - j0;
+      // the row in two 64-column halves (registers stay below the spill
+      // limit): first the maximum, then P; half h's packed P lands on columns
+      // [32 h, 32 h + 32), which half h has already read
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_off + s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_wait_ld();
+        tmax = fmaxf(tmax, full ? softmax_tile_max<64, true>(sr, sl2, clo - 64 * hf, chi - 64 * hf)
+                                : softmax_tile_max<64, false>(sr, sl2, clo - 64 * hf, chi - 64 * hf));
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (tmax > m_run + kRescaleLog2) {
+        if (m_run != -INFINITY) {
+          alpha = fast_exp2(m_run - tmax);
+          rescale = true;
+        }
+        m_run = tmax;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float tsum = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_off + s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_wait_ld();
+        const uint32_t p_taddr = tmem + lane_off + s_col + 32 * hf;
+        tsum += full ? softmax_tile_p<64, true, true>(sr, sl2, m_use, clo - 64 * hf, chi - 64 * hf, p_taddr)
+                     : softmax_tile_p<64, false, true>(sr, sl2, m_use, clo - 64 * hf, chi - 64 * hf, p_taddr);
+      }
+      l_run = l_run * alpha + tsum;
+      // PV_w(k - 1) must be complete before O is rescaled (waited for at every
+      // tile, so the o_done phase never runs more than one ahead)
+      if (k > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done + w, (k - 1) & 1, abort_flag))) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale) && k > 0) {  // tcgen05.ld/st are warp-collective
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + o_col + c * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st32(tmem + lane_off + o_col + c * 32, rr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + w);
+    }
+    if (ok && cnt > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done + w, (cnt - 1) & 1, abort_flag));
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+    if (ok && cnt > 0) {
+      tc_fence_after();
+      const bool row_ok = i < g.Lq;
+      const float inv = 1.f / l_run;
+      float* orow = p.o + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_off + o_col + c * 32, acc);
+        tmem_wait_ld();  // warp-collective: every lane loads, only valid rows store
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                make_float4(__uint_as_float(acc[e]) * inv, __uint_as_float(acc[e + 1]) * inv,
+                            __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
+        }
+      }
+      if (row_ok) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_run)) * kLn2;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 __global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const uint16_t* s0, uint16_t* d0, long long n0,
@@ -682,13 +885,38 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+                            float* lse, int* status, cudaStream_t s) {
+  using C = FwdPPCfg<D>;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e;
+  // one TMA instruction per tile: all D / 64 chunks
+  if ((e = make_tmap_f16_chunks(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
+  auto kern = fwd_pp_kernel<D>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
+    return e;
+  FwdParams p;
+  p.g = g;
+  p.o = o;
+  p.lse = lse;
+  p.status = status;
+  const int n_qtiles = (g.Lq + C::BM - 1) / C::BM;
+  p.n_qtiles = (n_qtiles + 1) / 2;  // pairs of query tiles
+  dim3 grid(g.B * g.Hq, p.n_qtiles);
+  kern<<<grid, 320, C::SMEM, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
 bool fwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
 cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
                           float* lse, int* status, cudaStream_t s) {
   switch (g.D) {
-    case 64: return fwd_tc_d<64>(g, q16, k16, v16, o, lse, status, s);
-    case 128: return fwd_tc_d<128>(g, q16, k16, v16, o, lse, status, s);
+    case 64: return fwd_pp_d<64>(g, q16, k16, v16, o, lse, status, s);
+    case 128: return fwd_pp_d<128>(g, q16, k16, v16, o, lse, status, s);
     case 256: return fwd_tc_d<256>(g, q16, k16, v16, o, lse, status, s);
     case 512: return launch_fwd_tc512(g, q16, k16, v16, o, lse, status, s);
     default: return cudaErrorInvalidValue;
