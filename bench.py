@@ -44,7 +44,7 @@ KERNEL_FLOPS_PER_PAIR_D = {
     "bwd_dkdv_tc": 8,     # S^T, dP^T recomputed; dV += P^T dO; dK += dS^T Q (tcgen05)
     "bwd_dq_tc": 6,       # S, dP recomputed; dQ += dS K (tcgen05)
 }
-HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_rowstats", "fwd_decode"}
+HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_prep", "fwd_decode"}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -78,7 +78,7 @@ def load_peaks():
 KERNEL_SOURCE = {
     "fwd_simt": "simt_kernels.cu", "bwd_delta": "simt_kernels.cu", "bwd_dkdv_simt": "simt_kernels.cu",
     "bwd_dq_simt": "simt_kernels.cu", "fwd_tc": "tc_fwd.cu", "convert_f16": "tc_fwd.cu",
-    "bwd_rowstats": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
+    "bwd_prep": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
 }
 # head dim 512: the tensor-core launches of the forward and backward come from the cluster kernels
 KERNEL_SOURCE_D512 = {"fwd_tc": "tc_fwd512.cu", "bwd_dkdv_tc": "tc_bwd512.cu", "bwd_dq_tc": "tc_bwd512.cu"}
@@ -459,8 +459,10 @@ def run_ours(args, w, world, rank, local_rank):
     kname, (kl, kms) = top
     avg_s = kms / kl / 1e3
     if kname in HBM_KERNELS:
-        if kname in ("bwd_delta", "bwd_rowstats"):
+        if kname == "bwd_delta":
             alg = B * Hq * Lq * (D * 4 + D * 2 + 4)
+        elif kname == "bwd_prep":  # q, k, v, dO: bf16 read + fp16 write; o (fp32) and lse read; stats written
+            alg = 4 * D * B * (2 * Hq * Lq + 2 * Hkv * L) + B * Hq * Lq * (4 * D + 4 + 8)
         elif kname == "fwd_decode":  # the K and V rows in band (bf16) once per kv head, q in, o and lse out
             alg = B * Hkv * _band_keys(w) * D * 2 * 2 + B * Hq * Lq * (D * 2 + D * 4 + 4)
         else:  # bf16 read + fp16 write of q, k, v (and dO in the backward)

@@ -278,14 +278,9 @@ int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, con
   uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
   uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
   uint16_t* g16 = reinterpret_cast<uint16_t*>(ws + w.g16);
-  const uint16_t* src[4] = {q, k, v, dO};
-  uint16_t* dst[4] = {q16, k16, v16, g16};
-  const size_t n[4] = {(size_t)B * Hq * Lq * D, (size_t)B * Hkv * Lk * D, (size_t)B * Hkv * Lk * D,
-                       (size_t)B * Hq * Lq * D};
-  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 4, status, s); }) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  if (launch("bwd_rowstats", s, [&] { return swa::launch_rowstats(g, w.Lpad, o, dO, lse, stats, s); }) !=
-      cudaSuccess)
+  if (launch("bwd_prep", s, [&] {
+        return swa::launch_bwd_prep(g, w.Lpad, q, k, v, dO, o, lse, q16, k16, v16, g16, stats, status, s);
+      }) != cudaSuccess)
     return SWA_ERR_CUDA;
   if (launch("bwd_dkdv_tc", s, [&] {
         return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, s);

@@ -95,10 +95,13 @@ cudaError_t make_tmap_f16_chunks(CUtensorMap* m, const void* ptr, int D, int L, 
 bool bwd_tc_supported(int D);
 // Padded row count of the backward's row-statistics array.
 int bwd_stats_lpad(int L);
-// Two planes of B * Hq * Lpad floats: stats[bh * Lpad + i] = lse_i * log2(e),
-// stats[(B * Hq + bh) * Lpad + i] = dO_i . o_i; zero for i >= L.
-cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint16_t* dO, const float* lse,
-                            float* stats, cudaStream_t s);
+// The backward's preparation in one pass: fp16 copies of q, k, v and dO, and
+// the row statistics, two planes of B * Hq * Lpad floats:
+// stats[bh * Lpad + i] = lse_i * log2(e), stats[(B * Hq + bh) * Lpad + i] =
+// dO_i . o_i (zero for i >= Lq); dO is read once.
+cudaError_t launch_bwd_prep(const Geom& g, int Lpad, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            const uint16_t* dO, const float* o, const float* lse, uint16_t* q16, uint16_t* k16,
+                            uint16_t* v16, uint16_t* g16, float* stats, int* status, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                int* status, cudaStream_t s);

@@ -46,37 +46,91 @@ constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 5
 constexpr int kSmemMax = 232448;         // dynamic shared memory per block on sm_103 (227 KB)
 constexpr int clamp_stages(int n) { return n < 2 ? 2 : (n > 8 ? 8 : n); }
 
-// Row statistics for the backward, two planes of BH * Lpad floats: per
-// (bh = b*Hq + h, i < Lpad) stats[bh Lpad + i] = lse_i * log2(e) and
-// stats[BH Lpad + bh Lpad + i] = Delta_i = dO_i . o_i; zero for padding rows
-// i >= L.  Planar, so that one 16-byte load gives four columns' values.
-__global__ void __launch_bounds__(256) rowstats_kernel(int BH, int L, int Lpad, int D, const float* __restrict__ o,
-                                                       const uint16_t* __restrict__ dO,
-                                                       const float* __restrict__ lse, float* __restrict__ stats) {
-  const long row = ((long)blockIdx.x * 256 + threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
-  if (row >= (long)BH * Lpad) return;
-  const int bh = (int)(row / Lpad), i = (int)(row % Lpad);
-  float acc = 0.f, l2 = 0.f;
-  if (i < L) {
-    const size_t off = ((size_t)bh * L + i) * D;
-    for (int d = lane * 4; d < D; d += 128) {
-      const float4 ov = *reinterpret_cast<const float4*>(o + off + d);
-      const uint2 gv = *reinterpret_cast<const uint2*>(dO + off + d);
-      acc = fmaf(ov.x, __uint_as_float(gv.x << 16), acc);
-      acc = fmaf(ov.y, __uint_as_float(gv.x & 0xffff0000u), acc);
-      acc = fmaf(ov.z, __uint_as_float(gv.y << 16), acc);
-      acc = fmaf(ov.w, __uint_as_float(gv.y & 0xffff0000u), acc);
-    }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    l2 = lse[(size_t)bh * L + i] * kLog2e;
-  }
-  if (lane == 0) {
-    stats[row] = l2;
-    stats[(size_t)BH * Lpad + row] = acc;
-  }
+// Backward preparation in one launch.  Segments 0-2 (blockIdx.y): fp16
+// copies of q, k and v, four 16-byte vectors in flight per thread.  Segment 3:
+// for every row of dO, its fp16 copy together with the row statistics, so dO
+// is read once for both; a warp per row, grid-stride.  The statistics are two
+// planes of BH * Lpad floats: per (bh = b*Hq + h, i < Lpad)
+// stats[bh Lpad + i] = lse_i * log2(e) and stats[BH Lpad + bh Lpad + i] =
+// Delta_i = dO_i . o_i; zero for padding rows i >= Lq.  Planar, so that one
+// 16-byte load gives four columns' values.  A finite input that overflows
+// fp16 latches kStatusFp16Range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& overflow) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  const __half2 hv = __floats2half2_rn(lo, hi);
+  const float2 back = __half22float2(hv);
+  overflow |= (isinf(back.x) && !isinf(lo)) || (isinf(back.y) && !isinf(hi));
+  return *reinterpret_cast<const uint32_t*>(&hv);
 }
+
+struct PrepParams {
+  const uint16_t* src[3];
+  uint16_t* dst[3];
+  long long n[3];  // elements (multiples of 8)
+  int BH, L, Lpad, D;  // rows of dO: BH x L (L = query rows), padded to Lpad
+  const float* o;
+  const uint16_t* dO;
+  uint16_t* g16;
+  const float* lse;
+  float* stats;
+  int* status;
+};
+
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepParams p) {
+  bool overflow = false;
+  const int seg = blockIdx.y;
+  if (seg < 3) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.src[seg]);
+    uint4* dst = reinterpret_cast<uint4*>(p.dst[seg]);
+    const long long n16 = p.n[seg] / 8;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; idx + 3 * stride < n16; idx += 4 * stride) {
+      const uint4 a = __ldcs(src + idx), b = __ldcs(src + idx + stride);
+      const uint4 c = __ldcs(src + idx + 2 * stride), d = __ldcs(src + idx + 3 * stride);
+      const uint4 v4[4] = {a, b, c, d};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        dst[idx + u * stride] = make_uint4(bf16x2_to_f16x2(v4[u].x, overflow), bf16x2_to_f16x2(v4[u].y, overflow),
+                                           bf16x2_to_f16x2(v4[u].z, overflow), bf16x2_to_f16x2(v4[u].w, overflow));
+    }
+    for (; idx < n16; idx += stride) {
+      const uint4 a = __ldcs(src + idx);
+      dst[idx] = make_uint4(bf16x2_to_f16x2(a.x, overflow), bf16x2_to_f16x2(a.y, overflow),
+                            bf16x2_to_f16x2(a.z, overflow), bf16x2_to_f16x2(a.w, overflow));
+    }
+  } else {
+    const int lane = threadIdx.x & 31;
+    const long rows = (long)p.BH * p.Lpad;
+    const long nwarps = (long)gridDim.x * (blockDim.x / 32);
+    for (long row = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; row < rows; row += nwarps) {
+      const int bh = (int)(row / p.Lpad), i = (int)(row % p.Lpad);
+      float acc = 0.f, l2 = 0.f;
+      if (i < p.L) {
+        const size_t off = ((size_t)bh * p.L + i) * p.D;
+        for (int d = lane * 4; d < p.D; d += 128) {
+          const float4 ov = __ldcs(reinterpret_cast<const float4*>(p.o + off + d));
+          const uint2 gv = __ldcs(reinterpret_cast<const uint2*>(p.dO + off + d));
+          acc = fmaf(ov.x, __uint_as_float(gv.x << 16), acc);
+          acc = fmaf(ov.y, __uint_as_float(gv.x & 0xffff0000u), acc);
+          acc = fmaf(ov.z, __uint_as_float(gv.y << 16), acc);
+          acc = fmaf(ov.w, __uint_as_float(gv.y & 0xffff0000u), acc);
+          *reinterpret_cast<uint2*>(p.g16 + off + d) =
+              make_uint2(bf16x2_to_f16x2(gv.x, overflow), bf16x2_to_f16x2(gv.y, overflow));
+        }
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+        l2 = p.lse[(size_t)bh * p.L + i] * kLog2e;
+      }
+      if (lane == 0) {
+        p.stats[row] = l2;
+        p.stats[(size_t)p.BH * p.Lpad + row] = acc;
+      }
+    }
+  }
+  if (overflow) atomicCAS(p.status, 0, kStatusFp16Range);
+}
+
 
 // dQ elementwise step for one query row (lse*log2e = l2, Delta = dl) and 32
 // key columns: dS = P (dP - Delta) as fp16 pairs.
@@ -1375,13 +1429,37 @@ bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 51
 
 int bwd_stats_lpad(int L) { return (L + 127) / 128 * 128; }
 
-cudaError_t launch_rowstats(const Geom& g, int Lpad, const float* o, const uint16_t* dO, const float* lse,
-                            float* stats, cudaStream_t s) {
-  const long rows = (long)g.B * g.Hq * Lpad;
-  const long blocks = (rows * 32 + 255) / 256;
-  rowstats_kernel<<<(unsigned)blocks, 256, 0, s>>>(g.B * g.Hq, g.Lq, Lpad, g.D, o, dO, lse, stats);
+cudaError_t launch_bwd_prep(const Geom& g, int Lpad, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            const uint16_t* dO, const float* o, const float* lse, uint16_t* q16, uint16_t* k16,
+                            uint16_t* v16, uint16_t* g16, float* stats, int* status, cudaStream_t s) {
+  PrepParams p;
+  p.src[0] = q;
+  p.src[1] = k;
+  p.src[2] = v;
+  p.dst[0] = q16;
+  p.dst[1] = k16;
+  p.dst[2] = v16;
+  p.n[0] = (long long)g.B * g.Hq * g.Lq * g.D;
+  p.n[1] = p.n[2] = (long long)g.B * g.Hkv * g.L * g.D;
+  p.BH = g.B * g.Hq;
+  p.L = g.Lq;
+  p.Lpad = Lpad;
+  p.D = g.D;
+  p.o = o;
+  p.dO = dO;
+  p.g16 = g16;
+  p.lse = lse;
+  p.stats = stats;
+  p.status = status;
+  // about 8 resident blocks of 256 threads per SM over the four segments
+  const long rows = (long)p.BH * Lpad;
+  long blocks = (rows + 7) / 8;
+  if (blocks > 152L * 4) blocks = 152L * 4;
+  if (blocks < 1) blocks = 1;
+  bwd_prep_kernel<<<dim3((unsigned)blocks, 4), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
+
 
 cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,

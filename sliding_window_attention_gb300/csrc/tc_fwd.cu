@@ -756,13 +756,18 @@ __global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const uint16_t* s
   bool overflow = false;
   const long long stride = (long long)gridDim.x * blockDim.x;
   long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; idx + stride < n16; idx += 2 * stride) {
+  // four 16-byte vectors in flight per thread
+  for (; idx + 3 * stride < n16; idx += 4 * stride) {
     const uint4 a = __ldcs(src + idx);
     const uint4 b = __ldcs(src + idx + stride);
+    const uint4 c = __ldcs(src + idx + 2 * stride);
+    const uint4 d = __ldcs(src + idx + 3 * stride);
     dst[idx] = bf16x8_to_f16x8(a, overflow);
     dst[idx + stride] = bf16x8_to_f16x8(b, overflow);
+    dst[idx + 2 * stride] = bf16x8_to_f16x8(c, overflow);
+    dst[idx + 3 * stride] = bf16x8_to_f16x8(d, overflow);
   }
-  if (idx < n16) dst[idx] = bf16x8_to_f16x8(__ldcs(src + idx), overflow);
+  for (; idx < n16; idx += stride) dst[idx] = bf16x8_to_f16x8(__ldcs(src + idx), overflow);
   if (overflow) atomicCAS(status, 0, kStatusFp16Range);
 }
 
