@@ -465,8 +465,8 @@ def run_ours(args, w, world, rank, local_rank):
             alg = 4 * D * B * (2 * Hq * Lq + 2 * Hkv * L) + B * Hq * Lq * (4 * D + 4 + 8)
         elif kname == "fwd_decode":  # the K and V rows in band (bf16) once per kv head, q in, o and lse out
             alg = B * Hkv * _band_keys(w) * D * 2 * 2 + B * Hq * Lq * (D * 2 + D * 4 + 4)
-        else:  # bf16 read + fp16 write of q, k, v (and dO in the backward)
-            alg = 4 * D * B * (Hq * Lq + 2 * Hkv * L)
+        else:  # convert_f16 (forward): bf16 read + fp16 write of v
+            alg = 4 * D * B * Hkv * L
         achieved = alg / avg_s / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:

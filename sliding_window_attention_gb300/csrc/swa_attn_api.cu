@@ -140,15 +140,16 @@ BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
   return w;
 }
 
-// Forward workspace layout on the tensor-core path: fp16 copies of q, k, v.
+// Forward workspace layout on the tensor-core path: an fp16 copy of v (S =
+// Q K^T reads the bf16 q and k directly; O += P V pairs v with fp16 P).
 struct FwdWs {
-  size_t q16, k16, v16, total;
+  size_t v16, total;
 };
 FwdWs fwd_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
+  (void)Hq;
+  (void)Lq;
   FwdWs w;
-  w.q16 = 0;
-  w.k16 = w.q16 + round_up((size_t)B * Hq * Lq * D * 2, 256);
-  w.v16 = w.k16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  w.v16 = 0;
   w.total = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
   return w;
 }
@@ -224,7 +225,7 @@ int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, flo
   if (!status) return rc;
   if (swa::decode_supported(g)) {
     // at most 16 query rows per kv head (a decode step): one pass over the
-    // bf16 cache on the CUDA cores, no fp16 copies
+    // bf16 cache, no fp16 copies
     float* ws = static_cast<float*>(workspace);
     if (launch("fwd_decode", s, [&] { return swa::launch_fwd_decode(g, q, k, v, o, lse, ws, status, s); }) !=
         cudaSuccess)
@@ -233,15 +234,13 @@ int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, flo
   }
   const FwdWs w = fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + w.q16);
-  uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
   uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
-  const uint16_t* src[3] = {q, k, v};
-  uint16_t* dst[3] = {q16, k16, v16};
-  const size_t n[3] = {(size_t)B * Hq * Lq * D, (size_t)B * Hkv * Lk * D, (size_t)B * Hkv * Lk * D};
-  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 3, status, s); }) != cudaSuccess)
+  const uint16_t* src[1] = {v};
+  uint16_t* dst[1] = {v16};
+  const size_t n[1] = {(size_t)B * Hkv * Lk * D};
+  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 1, status, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;
-  if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q16, k16, v16, o, lse, status, s); }) != cudaSuccess)
+  if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q, k, v16, o, lse, status, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;
   return SWA_OK;
 }

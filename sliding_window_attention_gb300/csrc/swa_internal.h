@@ -78,9 +78,11 @@ size_t decode_workspace_bytes(const Geom& g);  // fp32 chunk partials; 0 when on
 cudaError_t launch_fwd_decode(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
                               float* lse, float* ws, int* status, cudaStream_t s);
 // Head dim 512: 2-CTA cluster forward (tc_fwd512.cu).
-cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s);
-cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+// Forward on the tensor cores: q and k are the caller's bf16 tensors (S = Q K^T
+// runs on bf16 operands), v16 an fp16 copy of v (O += P V pairs it with fp16 P).
+cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                           float* lse, int* status, cudaStream_t s);
 
 // 3-D fp16 tensor map over [heads, L, D] with a 64 x box_rows box and

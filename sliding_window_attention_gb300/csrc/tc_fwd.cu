@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (elect_one()) {
-      const uint32_t idS = idesc_f16(kBM, BN, 0, 0, 0, 0);   // Q (K-major) x K (K-major)
+      const uint32_t idS = idesc_f16(kBM, BN, 1, 1, 0, 0);   // Q (K-major) x K (K-major), both bf16
       const uint32_t idPV = idesc_f16(kBM, D, 0, 0, 0, 1);   // P (TMEM) x V (MN-major)
       const uint32_t idL = idesc_f16(kBM, 16, 0, 0, 0, 0);   // P (TMEM) x ones (K-major)
       const uint64_t ones_desc = smem_desc_noswz(smem_u32(ones), 128, 256);
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (elect_one()) {
-      const uint32_t idS = idesc_f16(BM, BN, 0, 0, 0, 0);  // Q (K-major) x K (K-major)
+      const uint32_t idS = idesc_f16(BM, BN, 1, 1, 0, 0);  // Q (K-major) x K (K-major), both bf16
       const uint32_t idPV = idesc_f16(BM, D, 0, 0, 0, 1);  // P (TMEM) x V (MN-major)
       int kc = 0, vc = 0;  // K / V tiles consumed
       int kpA = 0, kpB = 0;  // PV issued per query tile
@@ -867,14 +867,14 @@ cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst,
 }
 
 template <int D>
-static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                             float* lse, int* status, cudaStream_t s) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
   // one TMA instruction per tile: Q, K and V in all D / 64 chunks
-  if ((e = make_tmap_f16_chunks(&tq, q16, D, g.Lq, g.B * g.Hq, kBM, C::KCH)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tq, q, D, g.Lq, g.B * g.Hq, kBM, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tk, k, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   auto kern = fwd_tc_kernel<D>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
@@ -891,14 +891,14 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* 
 }
 
 template <int D>
-static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                             float* lse, int* status, cudaStream_t s) {
   using C = FwdPPCfg<D>;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
   // one TMA instruction per tile: all D / 64 chunks
-  if ((e = make_tmap_f16_chunks(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM, C::KCH)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tq, q, D, g.Lq, g.B * g.Hq, C::BM, C::KCH)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tk, k, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   auto kern = fwd_pp_kernel<D>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
@@ -917,13 +917,13 @@ static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q16, const uint16_t* 
 
 bool fwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
-cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                           float* lse, int* status, cudaStream_t s) {
   switch (g.D) {
-    case 64: return fwd_pp_d<64>(g, q16, k16, v16, o, lse, status, s);
-    case 128: return fwd_pp_d<128>(g, q16, k16, v16, o, lse, status, s);
-    case 256: return fwd_tc_d<256>(g, q16, k16, v16, o, lse, status, s);
-    case 512: return launch_fwd_tc512(g, q16, k16, v16, o, lse, status, s);
+    case 64: return fwd_pp_d<64>(g, q, k, v16, o, lse, status, s);
+    case 128: return fwd_pp_d<128>(g, q, k, v16, o, lse, status, s);
+    case 256: return fwd_tc_d<256>(g, q, k, v16, o, lse, status, s);
+    case 512: return launch_fwd_tc512(g, q, k, v16, o, lse, status, s);
     default: return cudaErrorInvalidValue;
   }
 }

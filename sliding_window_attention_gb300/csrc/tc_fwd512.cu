@@ -99,7 +99,7 @@ static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 struct FwdParams512 {
   Geom g;
-  const uint16_t* q16;
+  const uint16_t* q;  // bf16: S = Q K^T reads the caller's q and k as they are
   float* o;
   float* lse;
   int n_tiles;
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThr, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       bool ok = true;
-      const uint32_t idS = idesc_f16(T, T, 0, 0, 0, 0);     // Q (TMEM) x K slice (K-major)
+      const uint32_t idS = idesc_f16(T, T, 1, 1, 0, 0);     // Q (TMEM) x K slice (K-major), both bf16
       const uint32_t idPV = idesc_f16(T, 128, 0, 0, 0, 1);  // P (K-major) x V chunk (MN-major)
       int used = 0;
       if (producer) {
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThr, 1)
       // Q row i into Tensor Memory: fp16 pairs, one 32-bit column each; warpgroup
       // wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
       const uint4* src =
-          reinterpret_cast<const uint4*>(p.q16 + ((size_t)bh * g.Lq + (i < g.Lq ? i : 0)) * DH) + wg * 32;
+          reinterpret_cast<const uint4*>(p.q + ((size_t)bh * g.Lq + (i < g.Lq ? i : 0)) * DH) + wg * 32;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
@@ -534,19 +534,19 @@ __global__ void __launch_bounds__(kThr, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16, float* o,
+cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s) {
   CUtensorMap tk, tv;
   cudaError_t e;
   // 128-column slices of K and V: two 64-column chunks per TMA instruction
-  if ((e = make_tmap_f16_chunks(&tk, k16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
+  if ((e = make_tmap_f16_chunks(&tk, k, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(fwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
       cudaSuccess)
     return e;
   FwdParams512 pm;
   pm.g = g;
-  pm.q16 = q16;
+  pm.q = q;
   pm.o = o;
   pm.lse = lse;
   pm.n_tiles = (g.Lq + T - 1) / T;
