@@ -108,12 +108,14 @@ cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_
                                const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                int* status, cudaStream_t s);
 // Head dim 512: thread-block-cluster kernels (tc_bwd512.cu).
+// Head dim 512: the dK/dV and dQ passes on clusters of CTA pairs (tcgen05
+// .cta_group::2).
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                  const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
-                                  int* status, cudaStream_t s);
+                                   const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
+                                   int* status, cudaStream_t s);
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
-                                cudaStream_t s);
+                                 const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
+                                 cudaStream_t s);
 cudaError_t launch_bwd_dq_tc(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                              const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                              cudaStream_t s);

@@ -1,41 +1,40 @@
-// Tensor-core backward for head dim 512 on thread-block clusters.
+// Tensor-core backward for head dim 512 on clusters of CTA pairs.
 //
 // At D = 512 the two accumulators of a 128-key tile (dK and dV, 512 fp32
 // columns each) need twice the Tensor Memory of one SM, and K plus V of the
 // tile (128 KB each in fp16) do not fit one SM's shared memory together.  So
-// the work of one tile is split by role across the CTAs of a cluster, each on
-// its own SM:
-//   producers (ranks 0 .. NP - 1, taking steps in turn): the resident A operand of
-//     S lives in Tensor Memory (K for dK/dV, Q for dQ: 128 x 512 fp16 = 256
-//     columns, read by TS-form MMAs), the resident A operand of dP in shared
-//     memory (V, or dO); the streamed tiles come in 64-column slices.  They
-//     form S and dP, then P = exp(scale S - lse) and dS = P (dP - Delta)
-//     ("Training -- design (ORPO, flash-CCE head, prefix sharing, segmented
-//     backward)", section 6: recompute P from the stored lse), and
-//     bulk-copy the fp16 tiles into the accumulator CTAs' operand slots;
-//   accumulators hold one full 128 x 512 fp32 accumulator in Tensor Memory:
-//     dK/dV pass (NP + 2 CTAs per kv head and 128-row key tile, every query
-//       head of the group and query tile in band):  rank NP  dV += P^T dO,
-//       rank NP + 1  dK += dS^T Q;
-//     dQ pass (NP + 1 CTAs per query head and query tile):  rank NP
-//       dQ += dS K.
+// the work is split by role across the CTAs of a cluster, and every role runs
+// on a CTA pair (tcgen05 .cta_group::2): the pair owns two adjacent 128-row
+// tiles of the resident side (keys in the dK/dV pass, queries in the dQ
+// pass), one per CTA, and each MMA of M = 256 rows takes its B operand half
+// from each CTA.  Every streamed tile therefore crosses each SM's TMA engine
+// and shared memory only once per pair, half in each CTA.
+//   producers (ranks 0-1 and 2-3, two pairs taking the streamed steps in
+//     turn): the A operand of S (K for dK/dV, Q for dQ: 128 x 512 fp16 per
+//     CTA = 256 columns) lives in Tensor Memory and feeds TS-form MMAs, the A
+//     operand of dP (V, or dO) in shared memory; the streamed tile arrives as
+//     two 64-row halves, one per CTA, in 16 KB slices of 128 columns.  Each
+//     CTA forms S and dP for its 128 rows and all 128 streamed columns, then
+//     P = exp(scale S - lse) and dS = P (dP - Delta) ("Training -- design
+//     (ORPO, flash-CCE head, prefix sharing, segmented backward)", section 6:
+//     recompute P from the stored lse), and bulk-copies the fp16 tiles into
+//     the accumulator CTA of the same half;
+//   accumulators (one pair per accumulator: ranks 4-5 dV += P^T dO and 6-7
+//     dK += dS^T Q in the dK/dV pass, ranks 4-5 dQ += dS K in the dQ pass)
+//     hold one 128 x 512 fp32 accumulator per CTA in Tensor Memory; the
+//     streamed operand arrives in 128-column halves of 256-column chunks and
+//     each step is 16 MMAs of M = 256, N = 256.
 // Only tiles that meet the causal / window band are visited ("Lab 028 lab
 // detail: Off NVIDIA, you fix the platform yourself", "What I changed, in
-// plain terms" items 3-4).  A producer issues 2 x 2048 MMA cycles per own
-// step and takes one step in NP; an accumulator issues 2048 per step.  A
-// producer's own step takes about 11,000 cycles (shared-memory traffic of
-// about 700 KB per own step, TMA issue and the copies), so three producers
-// (NP = 3: 5-CTA dK/dV and 4-CTA dQ clusters) keep the accumulators busier
-// than two, despite the SMs lost to cluster packing.  A producer moves one
-// (dQ) or two (dK/dV) 32 KB tiles per own step over distributed shared
-// memory (bulk copies).
+// plain terms" items 3-4); the two tiles of a pair walk the union of their
+// bands, and the columns outside a row's band are zero in P and dS.
 //
-// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-9 elementwise (two
-// warpgroups, 64 of the 128 columns each; a warpgroup stages its 64-column
-// half of a tile and warp 2 / 6 issues the copy), 10 slot release
-// (accumulator roles).  Every wait is bounded; a timeout in one CTA is
-// broadcast to the whole cluster, every CTA drains its TMA loads, copies and
-// MMAs in flight, and the status word records the timeout.
+// Warps: 0 TMA, 1 Tensor Memory owner and (leader CTA) MMA issuer, 2-9
+// elementwise (two warpgroups, 64 of the 128 columns each; a warpgroup
+// stages its 64-column half of a tile and warp 2 / 6 issues the copy), 10
+// slot release (accumulator roles).  Every wait is bounded; a timeout in one
+// CTA is broadcast to the whole cluster, every CTA drains its loads, copies
+// and MMAs in flight, and the status word records the timeout.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -52,85 +51,93 @@ using namespace tc;
 
 constexpr int kDirKV = 0, kDirQ = 1;
 constexpr int kRoleProd = 0, kRoleAccP = 1, kRoleAccDS = 2;
-constexpr int T = 128;     // tile rows on both sides (MMA M and N)
+constexpr int T = 128;     // rows of a resident tile, columns of a streamed step
+constexpr int HT = 64;     // streamed rows per CTA of a pair
 constexpr int DH = 512;    // head dim
+constexpr int NPP = 2;     // producer pairs
 constexpr int kThr = 352;  // 11 warps
 constexpr int kSigWarp = 10;
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr int RES_BYTES = T * DH * 2;  // resident dP A operand (V or dO), fp16
-constexpr int TILE_BYTES = T * T * 2;  // fp16 128 x 128 operand tile
+constexpr int RES_BYTES = T * DH * 2;       // resident dP A operand (V or dO), fp16
+constexpr int TILE_BYTES = T * T * 2;       // fp16 128 x 128 operand tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // one warpgroup's 64-column half (one swizzle chunk)
-constexpr int NR_P = 4;                // producer ring of 64-column slices
-constexpr int SLOT_P = T * 64 * 2;
-constexpr int SLOT_ACC = T * 128 * 2;  // accumulator ring of 128-column chunks
-constexpr int OFF_STG = RES_BYTES;     // producer: two staging halves
+// producer: resident operand, two staging halves, ring of 16 KB slices (two
+// 64-column chunks of this CTA's 64 streamed rows)
+constexpr int NR_P = 4;
+constexpr int SLOT_P = 2 * HT * 128;
+constexpr int OFF_STG = RES_BYTES;
 constexpr int OFF_RING_P = RES_BYTES + 2 * HALF_BYTES;
-constexpr int OFF_RECV = 0;            // accumulator: one operand slot per producer
-constexpr int DATA_P = OFF_RING_P + NR_P * SLOT_P;
-constexpr int kMaxNP = 3;
-constexpr int kMaxRing = 5;
-// accumulator layout for NP producers: NP operand slots, then as deep a ring
-// as the producers' footprint allows
-template <int NP>
-struct AccLayout {
-  static constexpr int OFF_RING = NP * TILE_BYTES;
-  static constexpr int NR = (DATA_P - OFF_RING) / SLOT_ACC;
-  static_assert(NR >= 2 && NR <= kMaxRing, "accumulator ring");
-};
-constexpr int DATA_BYTES = DATA_P;
-static_assert(AccLayout<2>::OFF_RING + AccLayout<2>::NR * SLOT_ACC <= DATA_BYTES, "accumulator footprint");
-static_assert(AccLayout<3>::OFF_RING + AccLayout<3>::NR * SLOT_ACC <= DATA_BYTES, "accumulator footprint");
-// producer Tensor Memory: resident S operand, S, dP
+constexpr int DATA_BYTES = OFF_RING_P + NR_P * SLOT_P;
+// accumulator: RS operand slots per producer pair (a producer can send its
+// next tile while the accumulator still works on the previous one), then a
+// ring of 32 KB slots (two 64-column chunks of the 128 streamed rows)
+constexpr int RS = 2;
+constexpr int NRECV = NPP * RS;
+constexpr int OFF_RECV = 0;
+constexpr int OFF_RING_A = NRECV * TILE_BYTES;
+constexpr int SLOT_A = 2 * T * 128;
+constexpr int NR_A = (DATA_BYTES - OFF_RING_A) / SLOT_A;
+constexpr int kMaxRing = NR_A > NR_P ? NR_A : NR_P;
+static_assert(NR_A >= 2 && OFF_RING_A + NR_A * SLOT_A <= DATA_BYTES, "accumulator footprint");
+// producer, dK/dV pass: each warpgroup's step statistics (lse * log2e and
+// Delta of its 64 columns) staged in shared memory
+constexpr int OFF_STATS = DATA_BYTES;
+constexpr int STATS_BYTES = 2 * 512;
+// producer Tensor Memory: resident S operand (fp16 pairs), S, dP
 constexpr uint32_t X_COL = 0, S_COL = 256, DP_COL = 384;
 
-// A producer can be at most one step (of its own) ahead of an accumulator's
-// release, so no cross-CTA barrier is ever more than one phase ahead of its
-// waiter.
 struct Bars {
-  uint64_t res_full, x_ready;
-  uint64_t ring_full[kMaxRing], ring_empty[kMaxRing];
-  uint64_t t_full, t_free;      // (producer) S and dP in TMEM / read by the elementwise warps
-  uint64_t staged[2];           // (producer) a warpgroup wrote its staging half
-  uint64_t stg_free[2];         // (producer) the copy out of a staging half landed
-  uint64_t dst_free[2];         // (producer) accumulator slot may be written: [0] P -> dV, [1] dS -> dK / dQ
-  uint64_t recv_full[kMaxNP];   // (accumulator) tile from producer 0 .. NP - 1 landed
-  uint64_t mma_done[kMaxNP];    // (accumulator) MMAs of a producer's step finished
+  uint64_t res_full;              // (leader) both CTAs' resident dP operand landed
+  uint64_t x_ready;               // (own) resident S operand written to Tensor Memory
+  uint64_t pair_ready;            // (leader) both CTAs' resident S operand ready
+  uint64_t ring_full[kMaxRing];   // (leader) both halves of a ring slot landed
+  uint64_t ring_empty[kMaxRing];  // (both) the pair's MMAs finished reading a slot
+  uint64_t s_full, p_full;        // (producer, both) S / dP of a step in Tensor Memory
+  uint64_t s_free, p_free;        // (producer) S / dP read: leader counts its 8 warps and the peer's relay
+  uint64_t staged[2];             // (producer) a warpgroup wrote its staging half
+  uint64_t stg_free[2];           // (producer) the copy out of a staging half landed
+  uint64_t dst_free[2][RS];       // (producer) accumulator slot may be written: [0] P -> dV, [1] dS -> dK / dQ
+  uint64_t stats_full[2];         // (producer, dK/dV) a warpgroup's step statistics landed
+  uint64_t stats_free[2];         // (producer, dK/dV) a warpgroup read its step statistics
+  uint64_t recv_full[NRECV][2];   // (accumulator, own) a warpgroup's half of the tile landed in slot
+  uint64_t peer_recv[NRECV];      // (accumulator leader) the peer's tile landed in slot
+  uint64_t mma_done[NRECV];       // (accumulator, both) MMAs reading slot finished
   uint64_t acc_done, mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
-  int n_sent[2][2];             // (producer) steps copied to [dV, dK / dQ] by warpgroup [0, 1]
-  int n_recv;                   // (accumulator) tiles received
+  int n_sent[2][2];               // (producer) steps copied to [dV, dK / dQ] by warpgroup [0, 1]
+  int n_recv[NPP];                // (accumulator) own steps of producer pair p observed landed
+  int n_issued;                   // ring loads issued by this CTA
 };
-static_assert(NR_P <= kMaxRing, "ring barriers");
 
-constexpr size_t SMEM = (size_t)DATA_BYTES + 1024 + 1024;
+constexpr size_t SMEM = (size_t)DATA_BYTES + STATS_BYTES + 1024 + 1024;
 static_assert(SMEM <= 232448, "shared memory");
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
-struct Params512 {
+struct ParamsPair {
   Geom g;
-  float* out0;             // KV: dk ; Q: dq
-  float* out1;             // KV: dv
-  const uint16_t* x16;     // resident S operand rows: KV: k16 ; Q: q16
-  const float* stats;      // two planes: lse * log2e, then Delta (B * Hq * Lpad floats each)
+  float* out0;          // KV: dk ; Q: dq
+  float* out1;          // KV: dv
+  const uint16_t* x16;  // resident S operand rows: KV: k16 ; Q: q16
+  const float* stats;   // two planes: lse * log2e, then Delta (B * Hq * Lpad floats each)
   int Lpad;
-  int n_tiles;
+  int n_tiles;          // resident-side 128-row tiles
   int* status;
 };
 
 // P for 64 columns (cb0 .. cb0 + 63 of the tile) of one row, in place over the
-// S values (fp32).  PER_COL: the lse belongs to the column (lse4 holds
-// lse * log2e of the 64 columns, four per vector); otherwise l2 is the row's.
+// S values (fp32).  PER_COL: the lse belongs to the column (lse_s is the
+// shared address of lse * log2e of the 64 columns); otherwise l2 is the row's.
 // Columns outside [clo, chi] are exactly zero unless FULL.
 template <bool FULL, bool PER_COL>
-__device__ __forceinline__ void p_tile64(uint32_t (&sv)[64], const float4* lse4, float l2, float sl2, int cb0,
+__device__ __forceinline__ void p_tile64(uint32_t (&sv)[64], uint32_t lse_s, float l2, float sl2, int cb0,
                                          int clo, int chi) {
 #pragma unroll
   for (int e = 0; e < 64; e += 4) {
     float lv[4] = {l2, l2, l2, l2};
     if (PER_COL) {
-      const float4 l4 = __ldg(lse4 + (e >> 2));
+      const float4 l4 = ld_smem_f4(lse_s + 4 * e);
       lv[0] = l4.x;
       lv[1] = l4.y;
       lv[2] = l4.z;
@@ -150,16 +157,16 @@ __device__ __forceinline__ void pack64(const uint32_t (&v)[64], uint32_t (&o)[32
   for (int e = 0; e < 64; e += 2) o[e >> 1] = pack_half2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
 }
 
-// dS = P (dP - Delta) for 64 columns as fp16 pairs (dl4: Delta of the 64
-// columns, four per vector, when PER_COL; otherwise dl is the row's).
+// dS = P (dP - Delta) for 64 columns as fp16 pairs (dl_s: shared address of
+// the Delta of the 64 columns when PER_COL; otherwise dl is the row's).
 template <bool PER_COL>
-__device__ __forceinline__ void ds_tile64(const uint32_t (&pv)[64], const uint32_t (&dv)[64], const float4* dl4,
+__device__ __forceinline__ void ds_tile64(const uint32_t (&pv)[64], const uint32_t (&dv)[64], uint32_t dl_s,
                                           float dl, uint32_t (&o)[32]) {
 #pragma unroll
   for (int e = 0; e < 64; e += 4) {
     float dd[4] = {dl, dl, dl, dl};
     if (PER_COL) {
-      const float4 d4 = __ldg(dl4 + (e >> 2));
+      const float4 d4 = ld_smem_f4(dl_s + 4 * e);
       dd[0] = d4.x;
       dd[1] = d4.y;
       dd[2] = d4.z;
@@ -172,58 +179,73 @@ __device__ __forceinline__ void ds_tile64(const uint32_t (&pv)[64], const uint32
   }
 }
 
-template <int DIR, int NP>
+// Arrive on `bar` of the pair's leader CTA (locally when this CTA is the leader).
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader, uint32_t lead) {
+  if (leader) mbar_arrive(bar);
+  else mbar_arrive_remote(mapa(smem_u32(bar), lead));
+}
+
+template <int DIR>
 __global__ void __launch_bounds__(kThr, 1)
-    bwd512_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                  const Params512 p) {
-  constexpr uint32_t R = NP + ((DIR == kDirKV) ? 2 : 1);  // CTAs per cluster
-  constexpr int NR_ACC = AccLayout<NP>::NR;
-  constexpr int OFF_RING_ACC = AccLayout<NP>::OFF_RING;
+    bwd512_kernel(const __grid_constant__ CUtensorMap tmS,   // streamed S operand, 64 rows x 2 chunks: Q / K
+                   const __grid_constant__ CUtensorMap tmP,   // streamed dP operand, 64 rows x 2 chunks: dO / V
+                   const __grid_constant__ CUtensorMap tmR,   // resident dP operand, 128 rows x 1 chunk: V / dO
+                   const __grid_constant__ CUtensorMap tmA0,  // dV accumulator operand, 128 rows x 2 chunks: dO
+                   const __grid_constant__ CUtensorMap tmA1,  // dK / dQ accumulator operand: Q / K
+                   const ParamsPair p) {
+  constexpr uint32_t R = (DIR == kDirKV) ? 8 : 6;  // CTAs per cluster
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(base + DATA_BYTES);
+  Bars* bars = reinterpret_cast<Bars*>(base + DATA_BYTES + STATS_BYTES);
   volatile int* abort_flag = &bars->abort_flag;
   const uint32_t sbase = smem_u32(base);
 
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const int role = rank < (uint32_t)NP ? kRoleProd : ((DIR == kDirKV && rank == (uint32_t)NP) ? kRoleAccP : kRoleAccDS);
+  const uint32_t h = rank & 1u;      // half of the pair: which resident tile, which streamed rows
+  const uint32_t lead = rank & ~1u;  // the pair's leader
+  const bool leader = h == 0;
+  const uint16_t pmask = (uint16_t)(3u << lead);
+  const int role = rank < 4 ? kRoleProd : ((DIR == kDirKV && rank < 6) ? kRoleAccP : kRoleAccDS);
   const bool acc_role = role != kRoleProd;
+  const int pp = (int)(rank >> 1);  // producer pair (producers only)
   // Grid (x, y, z) = (CTAs per cluster [x query heads of the group, dQ pass],
-  // tiles, b * Hkv + kv head).  Blocks launch x fastest and z slowest, so the
-  // clusters running at any moment share one kv head: its K and V (dQ pass)
-  // or its group's Q and dO (dK/dV pass) are read from HBM about once and
-  // then served by L2.
+  // tile pairs, b * Hkv + kv head).  Blocks launch x fastest and z slowest, so
+  // the clusters running at any moment share one kv head: its K and V (dQ
+  // pass) or its group's Q and dO (dK/dV pass) are read from HBM about once
+  // and then served by L2.
   const int bkv_z = (int)blockIdx.z;
   const int b = bkv_z / g.Hkv;
   const int head = (DIR == kDirKV) ? bkv_z  // b * Hkv + kv head
                                    : b * g.Hq + (bkv_z - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // query head
-  // resident-side tile (keys for KV, queries for Q): longest band first
-  const int tile = (DIR == kDirKV) ? (int)blockIdx.y : p.n_tiles - 1 - (int)blockIdx.y;
-  const int r0 = tile * T;
+  const int LX = (DIR == kDirKV) ? g.L : g.Lq;  // rows of the resident side
+  const int npairs = (p.n_tiles + 1) / 2;
+  // resident-side tile pair (dQ pass: longest band first) and this CTA's tile
+  const int tp = (DIR == kDirKV) ? (int)blockIdx.y : npairs - 1 - (int)blockIdx.y;
+  const int pr0 = 2 * tp * T;
+  const int prlast = min(pr0 + 2 * T, LX) - 1;
+  const int r0 = pr0 + (int)h * T;
+  const bool own_rows = r0 < LX;  // false for the second tile of an odd last pair
+  const int rlast = own_rows ? min(r0 + T, LX) - 1 : r0;
   int t_lo, ntq, N;
-  // rows of the resident side, and the last one that exists
-  const int LX = (DIR == kDirKV) ? g.L : g.Lq;
-  const int rlast = min(r0 + T, LX) - 1;
   if (DIR == kDirKV) {
-    // query rows that can see a key of this tile
-    const int qlo = band_q_lo(g, r0), qhi = band_q_hi(g, rlast);
+    // query rows that can see a key of the pair
+    const int qlo = band_q_lo(g, pr0), qhi = band_q_hi(g, prlast);
     t_lo = qlo / T;
     ntq = qlo <= qhi ? qhi / T - t_lo + 1 : 0;
     N = g.G * ntq;
   } else {
-    // key tiles meeting the band of rows r0 .. rlast (never empty)
-    t_lo = band_key_lo(g, r0) / T;
-    ntq = band_key_hi(g, rlast) / T - t_lo + 1;
+    // key tiles meeting the band of the pair's rows (never empty)
+    t_lo = band_key_lo(g, pr0) / T;
+    ntq = band_key_hi(g, prlast) / T - t_lo + 1;
     N = ntq;
   }
   if (N == 0) {
     // dK/dV pass, and no query sees these keys (queries that are a suffix of
     // the keys, with a window): zero gradients ("Lab 028 lab detail", "What
     // I changed, in plain terms" item 5(b)).  Every CTA of the cluster has
-    // the same tile, so all of them leave here, before any cluster barrier.
+    // the same pair, so all of them leave here, before any cluster barrier.
     if (role == kRoleAccP) zero_rows(p.out1, head, r0, T, g.L, DH);
     if (role == kRoleAccDS) zero_rows(p.out0, head, r0, T, g.L, DH);
     return;
@@ -240,211 +262,244 @@ __global__ void __launch_bounds__(kThr, 1)
     if (DIR == kDirKV) return b * g.Hq + (head - b * g.Hkv) * g.G + n % g.G;  // query head
     return bkv_z;                                                              // kv head
   };
-  // a producer takes steps n = rank, rank + NP, ...; m-th own step = rank + NP m
-  const int n_own = role == kRoleProd ? max(0, (N - (int)rank + NP - 1) / NP) : 0;
+  // producer pair pp takes steps n = pp, pp + NPP, ...; m-th own step = pp + NPP m
+  const int n_own = role == kRoleProd ? max(0, (N - pp + NPP - 1) / NPP) : 0;
   // accumulator: which of the producer's two destinations this CTA is
   const int dst_kind = (role == kRoleAccP) ? 0 : 1;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->res_full, 1);
     mbar_init(&bars->x_ready, 256);
+    mbar_init(&bars->pair_ready, 2);
     for (int s = 0; s < kMaxRing; ++s) {
       mbar_init(&bars->ring_full[s], 1);
       mbar_init(&bars->ring_empty[s], 1);
     }
-    mbar_init(&bars->t_full, 1);
-    mbar_init(&bars->t_free, 256);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 1);
+    // 8 elementwise warps, plus (leader) the one arrival the peer's relay warp forwards
+    mbar_init(&bars->s_free, leader ? 9 : 8);
+    mbar_init(&bars->p_free, leader ? 9 : 8);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->staged[s], 128);
       mbar_init(&bars->stg_free[s], 1);
-      mbar_init(&bars->dst_free[s], 1);
+      for (int j = 0; j < RS; ++j) mbar_init(&bars->dst_free[s][j], 1);
+      mbar_init(&bars->stats_full[s], 1);
+      mbar_init(&bars->stats_free[s], 128);
       bars->n_sent[s][0] = bars->n_sent[s][1] = 0;
     }
-    for (int s = 0; s < kMaxNP; ++s) {
-      mbar_init(&bars->recv_full[s], 1);
+    for (int s = 0; s < NRECV; ++s) {
+      mbar_init(&bars->recv_full[s][0], 1);
+      mbar_init(&bars->recv_full[s][1], 1);
+      mbar_init(&bars->peer_recv[s], 1);
       mbar_init(&bars->mma_done[s], 1);
     }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
-    bars->n_recv = 0;
+    for (int s = 0; s < NPP; ++s) bars->n_recv[s] = 0;
+    bars->n_issued = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(&bars->tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // every CTA's barriers exist before any remote arrive or copy
+  cluster_sync();  // every CTA's barriers exist before any remote arrive, load or copy
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA (both CTAs of a pair)
     if (elect_one()) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      prefetch_tmap(&tmG);
+      prefetch_tmap(&tmS);
+      prefetch_tmap(&tmP);
+      prefetch_tmap(&tmR);
+      prefetch_tmap(&tmA0);
+      prefetch_tmap(&tmA1);
       int issued = 0;  // ring loads issued
       bool ok = true;
       if (!acc_role) {
-        // resident dP operand, then per own step 8 slices for S and 8 for dP
-        const CUtensorMap* mres = (DIR == kDirKV) ? &tmV : &tmG;
-        const CUtensorMap* ms = (DIR == kDirKV) ? &tmQ : &tmK;
-        const CUtensorMap* mp = (DIR == kDirKV) ? &tmG : &tmV;
-        mbar_arrive_expect_tx(&bars->res_full, RES_BYTES);
-        for (int c = 0; c < DH / 64; ++c) tma_load_3d(base + c * T * 128, mres, &bars->res_full, c * 64, r0, head);
+        // resident dP operand (this CTA's 128 rows), then per own step four
+        // slices for S and then four for dP (this CTA's 64 rows)
+        if (leader) mbar_arrive_expect_tx(&bars->res_full, 2 * RES_BYTES);
+        const uint32_t res_bar = mapa(smem_u32(&bars->res_full), lead);
+        for (int c = 0; c < DH / 64; ++c) tma_load_3d_pair(base + c * T * 128, &tmR, res_bar, c * 64, r0, head);
         for (int m = 0; ok && m < n_own; ++m) {
-          const int n = (int)rank + NP * m;
-          const int rows = step_rows(n), hd = step_head(n);
-          for (int k = 0; k < 2 * (DH / 64); ++k, ++issued) {
+          const int n = pp + NPP * m;
+          const int rows = step_rows(n) + HT * (int)h, hd = step_head(n);
+          for (int k = 0; k < 2 * (DH / 128); ++k, ++issued) {
             const int s = issued % NR_P;
             if (issued >= NR_P && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_P) & 1) ^ 1, abort_flag, R)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&bars->ring_full[s], SLOT_P);
-            tma_load_3d(base + OFF_RING_P + s * SLOT_P, (k & 1) ? mp : ms, &bars->ring_full[s], (k >> 1) * 64, rows,
-                        hd);
+            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_P);
+            tma_load_4d_pair(base + OFF_RING_P + s * SLOT_P, k >= 4 ? &tmP : &tmS,
+                             mapa(smem_u32(&bars->ring_full[s]), lead), 0, rows, 2 * (k & 3), hd);
           }
         }
-        if (!ok) mbar_wait_drain(&bars->res_full, 0);
       } else {
-        // 128-column chunks of dO (dV), Q (dK) or K (dQ)
-        const CUtensorMap* mstr = (role == kRoleAccP) ? &tmG : ((DIR == kDirKV) ? &tmQ : &tmK);
+        // this CTA's 128-column half of each 256-column chunk of dO (dV), Q (dK) or K (dQ)
+        const CUtensorMap* mb = (role == kRoleAccP) ? &tmA0 : &tmA1;
         for (int n = 0; ok && n < N; ++n) {
           const int rows = step_rows(n), hd = step_head(n);
-          for (int c = 0; c < DH / 128; ++c, ++issued) {
-            const int s = issued % NR_ACC;
-            if (issued >= NR_ACC &&
-                !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_ACC) & 1) ^ 1, abort_flag, R)) {
+          for (int c = 0; c < DH / 256; ++c, ++issued) {
+            const int s = issued % NR_A;
+            if (issued >= NR_A && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_A) & 1) ^ 1, abort_flag, R)) {
               ok = false;
               break;
             }
-            unsigned char* dst = base + OFF_RING_ACC + s * SLOT_ACC;
-            mbar_arrive_expect_tx(&bars->ring_full[s], SLOT_ACC);
-            tma_load_3d(dst, mstr, &bars->ring_full[s], c * 128, rows, hd);
-            tma_load_3d(dst + T * 128, mstr, &bars->ring_full[s], c * 128 + 64, rows, hd);
+            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_A);
+            tma_load_4d_pair(base + OFF_RING_A + s * SLOT_A, mb, mapa(smem_u32(&bars->ring_full[s]), lead), 0,
+                             rows, 4 * c + 2 * (int)h, hd);
           }
         }
       }
-      if (!ok) {
-        // unwinding: let the loads in flight land (at most one per slot)
-        const int nr = acc_role ? NR_ACC : NR_P;
-        for (int k = issued - 1; k >= 0 && k >= issued - nr; --k)
-          mbar_wait_drain(&bars->ring_full[k % nr], (k / nr) & 1);
-      }
+      bars->n_issued = issued;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (leader)
     if (elect_one()) {
       bool ok = true;
-      const uint32_t idS = idesc_f16(T, T, 0, 0, 0, 0);  // both operands K-major
       if (!acc_role) {
-        const uint64_t yd = smem_desc_sw128(sbase, 16, 1024);  // resident dP operand
-        ok = mbar_wait_cl(&bars->res_full, 0, abort_flag, R) && mbar_wait_cl(&bars->x_ready, 0, abort_flag, R);
-        int used = 0;
-        for (int m = 0; ok && m < n_own; ++m) {
-          if (m >= 1 && !mbar_wait_cl(&bars->t_free, (m - 1) & 1, abort_flag, R)) {
-            ok = false;
-            break;
-          }
+        // both CTAs: the resident S operand is in Tensor Memory -> tell the leader
+        ok = mbar_wait_cl(&bars->x_ready, 0, abort_flag, R);
+        if (ok) {
           tc_fence_after();
-          for (int k = 0; k < 2 * (DH / 64); ++k, ++used) {
-            const int s = used % NR_P, c = k >> 1;
-            if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_P) & 1, abort_flag, R)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t sd = smem_desc_sw128(sbase + OFF_RING_P + s * SLOT_P, 16, 1024);
-            if ((k & 1) == 0) {
-              // S += X[:, 64c .. 64c + 63] slice^T, X from Tensor Memory (8 columns per 16 elements)
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_ts(tmem + S_COL, tmem + X_COL + c * 32 + ks * 8, desc_add(sd, ks * 32), idS, (c | ks) ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_ss(tmem + DP_COL, desc_add(yd, c * T * 128 + ks * 32), desc_add(sd, ks * 32), idS,
-                       (c | ks) ? 1u : 0u);
-            }
-            mma_commit(&bars->ring_empty[s]);
-          }
-          if (!ok) break;
-          mma_commit(&bars->t_full);
+          tc_fence_before();
+          arrive_leader(&bars->pair_ready, leader, lead);
         }
-      } else {
-        const uint32_t idA = idesc_f16(T, 128, 0, 0, 0, 1);  // A K-major (fp16 tile), B MN-major
+        if (leader && ok) {
+          const uint32_t idS = idesc_f16(2 * T, T, 0, 0, 0, 0);  // M = 256 (the pair's rows), both K-major
+          const uint64_t yd = smem_desc_sw128(sbase, 16, 1024);  // resident dP operand
+          ok = mbar_wait_cl(&bars->res_full, 0, abort_flag, R) && mbar_wait_cl(&bars->pair_ready, 0, abort_flag, R);
+          int used = 0;
+          for (int m = 0; ok && m < n_own; ++m) {
+            // S of step m (slices 0-3) once the elementwise warps read S of step m - 1, then dP
+            // (slices 4-7) once they read dP of step m - 1: each overlaps the other's readout
+            for (int k = 0; k < 2 * (DH / 128); ++k, ++used) {
+              if ((k & 3) == 0) {
+                if (m >= 1 && !mbar_wait_cl(k == 0 ? &bars->s_free : &bars->p_free, (m - 1) & 1, abort_flag, R)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
+              const int s = used % NR_P;
+              if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_P) & 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t sd = smem_desc_sw128(sbase + OFF_RING_P + s * SLOT_P, 16, 1024);
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * (k & 3) + cc;  // 64-column chunk of the head dim
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                  const uint64_t bdk = desc_add(sd, cc * HT * 128 + ks * 32);
+                  if (k < 4)  // S += X[:, chunk] slice^T, X from Tensor Memory (8 columns per 16 elements)
+                    mma_pair_ts(tmem + S_COL, tmem + X_COL + c * 32 + ks * 8, bdk, idS, (c | ks) ? 1u : 0u);
+                  else
+                    mma_pair_ss(tmem + DP_COL, desc_add(yd, c * T * 128 + ks * 32), bdk, idS, (c | ks) ? 1u : 0u);
+                }
+              }
+              mma_commit_pair(&bars->ring_empty[s], pmask);
+              if (k == 3) mma_commit_pair(&bars->s_full, pmask);
+              if (k == 7) mma_commit_pair(&bars->p_full, pmask);
+            }
+          }
+        }
+      } else if (leader) {
+        const uint32_t idA = idesc_f16(2 * T, 256, 0, 0, 0, 1);  // A K-major (fp16 tile), B MN-major
         int used = 0;
         for (int n = 0; ok && n < N; ++n) {
-          const int s2 = n % NP;  // producer of step n, and its slot
-          if (!mbar_wait_cl(&bars->recv_full[s2], (n / NP) & 1, abort_flag, R)) {
+          // step n comes from producer pair n % NPP, its own step j = n / NPP, into slot (n % NPP) RS + j % RS
+          const int j = n / NPP, slot = (n % NPP) * RS + j % RS, ph = (j / RS) & 1;
+          if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R) ||
+              !mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R) ||
+              !mbar_wait_cl(&bars->peer_recv[slot], ph, abort_flag, R)) {
             ok = false;
             break;
           }
-          bars->n_recv = n + 1;
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + s2 * TILE_BYTES, 16, 1024);
-          for (int c = 0; c < DH / 128; ++c, ++used) {
-            const int s = used % NR_ACC;
-            if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_ACC) & 1, abort_flag, R)) {
+          const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + slot * TILE_BYTES, 16, 1024);
+          for (int c = 0; c < DH / 256; ++c, ++used) {
+            const int s = used % NR_A;
+            if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_A) & 1, abort_flag, R)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t bd = smem_desc_sw128(sbase + OFF_RING_ACC + s * SLOT_ACC, T * 128, 1024);
+            const uint64_t bd = smem_desc_sw128(sbase + OFF_RING_A + s * SLOT_A, T * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < T / 16; ++ks)
-              mma_ss(tmem + c * 128, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32), desc_add(bd, ks * 2048),
-                     idA, (n | ks) ? 1u : 0u);
-            mma_commit(&bars->ring_empty[s]);
+              mma_pair_ss(tmem + c * 256, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32), desc_add(bd, ks * 2048),
+                          idA, (n | ks) ? 1u : 0u);
+            mma_commit_pair(&bars->ring_empty[s], pmask);
           }
           if (!ok) break;
-          mma_commit(&bars->mma_done[s2]);
+          mma_commit_pair(&bars->mma_done[slot], pmask);
         }
-        if (ok) mma_commit(&bars->acc_done);
+        if (ok) mma_commit_pair(&bars->acc_done, pmask);
       }
-      // every MMA issued so far has finished before TMEM is released
-      mma_commit(&bars->mma_drain);
+      // every MMA the leader issued has finished before either CTA releases Tensor Memory
+      if (leader) mma_commit_pair(&bars->mma_drain, pmask);
       mbar_wait_drain(&bars->mma_drain, 0);
     }
   } else if (warp == kSigWarp) {
+    // ------------------------------------------------------------ relay (producer peer)
+    if (!acc_role && !leader && elect_one()) {
+      // the peer's 8 warps arrive locally; one remote arrival per step tells the leader
+      for (int m = 0; m < n_own; ++m) {
+        if (!mbar_wait_cl(&bars->s_free, m & 1, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->s_free), lead));
+        if (!mbar_wait_cl(&bars->p_free, m & 1, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->p_free), lead));
+      }
+    }
     // ------------------------------------------------------------ slot release (accumulator roles)
     if (acc_role && elect_one()) {
-      // arm each producer's slot for its first step, then re-arm after each step's MMAs
-      for (int s = 0; s < NP && s < N; ++s) {
-        mbar_arrive_expect_tx(&bars->recv_full[s], TILE_BYTES);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind]), (uint32_t)s));
+      // arm the slots for the first NRECV steps, then re-arm a slot for step
+      // n + NRECV once the MMAs of step n have read it; the producer CTA of the
+      // same half writes this CTA's slots
+      for (int n = 0; n < NRECV && n < N; ++n) {
+        const int j = n / NPP, slot = (n % NPP) * RS + j % RS;
+        mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
+        mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
+        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind][j % RS]), (uint32_t)(2 * (n % NPP)) + h));
       }
-      for (int n = 0; n + NP < N; ++n) {
-        const int s2 = n % NP;
-        if (!mbar_wait_cl(&bars->mma_done[s2], (n / NP) & 1, abort_flag, R)) break;
-        mbar_arrive_expect_tx(&bars->recv_full[s2], TILE_BYTES);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind]), (uint32_t)s2));
+      for (int n = 0; n + NRECV < N; ++n) {
+        const int j = n / NPP, slot = (n % NPP) * RS + j % RS;
+        if (!mbar_wait_cl(&bars->mma_done[slot], (j / RS) & 1, abort_flag, R)) break;
+        mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
+        mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
+        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind][j % RS]), (uint32_t)(2 * (n % NPP)) + h));
       }
     }
   } else if (!acc_role) {
-    // ------------------------------------------------------------ elementwise (producers)
+    // ------------------------------------------------------------ elementwise (producers, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const float sl2 = g.scale * kLog2e;
     const int cb0 = 64 * wg;
     const int row = r0 + r;  // key (KV) or query (Q) of this thread
+    const bool row_ok = row < LX;
     {
       // resident S operand into Tensor Memory: row r, fp16 pairs -> one 32-bit column each;
       // warpgroup wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
-      const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)head * LX + (row < LX ? row : 0)) * DH) +
+      const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)head * LX + (row_ok ? row : 0)) * DH) +
                          wg * 32;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = row < LX ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
           v[4 * q] = w4.x;
           v[4 * q + 1] = w4.y;
           v[4 * q + 2] = w4.z;
@@ -457,14 +512,14 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive(&bars->x_ready);
     }
     float2 rs_row = make_float2(0.f, 0.f);
-    if (DIR == kDirQ)
+    if (DIR == kDirQ && row_ok)
       rs_row = make_float2(p.stats[(size_t)head * p.Lpad + row], p.stats[((size_t)g.B * g.Hq + head) * p.Lpad + row]);
     const uint32_t stg = sbase + OFF_STG + wg * HALF_BYTES;
     const uint32_t stg_row = stg + r * 128;
     const bool issuer = (warp & 3) == 2;  // warp 2 / 6 copies its warpgroup's half
     int copies = 0;                       // copies out of this warpgroup's staging half
     bool ok = true;
-    // stage one 64-column half tile and copy it into accumulator rank `dst`'s slot
+    // stage one 64-column half tile and copy it into accumulator rank `dst`'s slot for this producer pair
     auto send = [&](const uint32_t (&o)[32], int kind, uint32_t dst, int m) -> bool {
       if (copies > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[wg], (copies - 1) & 1, abort_flag, R)))
         return false;
@@ -475,27 +530,38 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive(&bars->staged[wg]);
       if (issuer) {
         if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->staged[wg], copies & 1, abort_flag, R) &&
-                                         mbar_wait_cl(&bars->dst_free[kind], m & 1, abort_flag, R)))
+                                         mbar_wait_cl(&bars->dst_free[kind][m % RS], (m / RS) & 1, abort_flag, R)))
           return false;
         if (lane == 0) {
-          bulk_copy_to_cta(mapa(sbase + OFF_RECV + rank * TILE_BYTES + wg * HALF_BYTES, dst), stg, HALF_BYTES,
-                           mapa(smem_u32(&bars->recv_full[rank]), dst));
+          const int slot = pp * RS + m % RS;
+          bulk_copy_to_cta(mapa(sbase + OFF_RECV + slot * TILE_BYTES + wg * HALF_BYTES, dst), stg, HALF_BYTES,
+                           mapa(smem_u32(&bars->recv_full[slot][wg]), dst));
           bars->n_sent[kind][wg] = m + 1;
         }
       }
       ++copies;
       return true;
     };
+    const uint32_t dst_p = 4u + h;                                  // dV accumulator of this half (KV)
+    const uint32_t dst_ds = (DIR == kDirKV ? 6u : 4u) + h;          // dK / dQ accumulator of this half
+    // dK/dV pass: the statistics of own step m's 64 columns of this warpgroup
+    // (lse * log2e, then Delta) are bulk-copied into shared memory while the
+    // previous step is finished; every thread then reads them by broadcast
+    const uint32_t lse_s = sbase + OFF_STATS + wg * 512, dl_s = lse_s + 256;
+    int st_issued = 0;
+    auto load_stats = [&](int m) {
+      const int n = pp + NPP * m;
+      const float* src = p.stats + (size_t)step_head(n) * p.Lpad + step_rows(n) + cb0;
+      mbar_arrive_expect_tx(&bars->stats_full[wg], 512);
+      bulk_load_g2s(lse_s, src, 256, &bars->stats_full[wg]);
+      bulk_load_g2s(dl_s, src + (size_t)g.B * g.Hq * p.Lpad, 256, &bars->stats_full[wg]);
+      ++st_issued;
+    };
+    if (DIR == kDirKV && issuer && lane == 0 && n_own > 0) load_stats(0);
     for (int m = 0; m < n_own; ++m) {
-      const int n = (int)rank + NP * m;
+      const int n = pp + NPP * m;
       const int c0 = step_rows(n);  // first column's query (KV) or key (Q)
-      const float4 *lse4 = nullptr, *dl4 = nullptr;
-      if (DIR == kDirKV) {
-        const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + c0 + cb0;
-        lse4 = reinterpret_cast<const float4*>(lse_g);
-        dl4 = reinterpret_cast<const float4*>(lse_g + (size_t)g.B * g.Hq * p.Lpad);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->t_full, m & 1, abort_flag, R))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full, m & 1, abort_flag, R))) {
         ok = false;
         break;
       }
@@ -503,53 +569,88 @@ __global__ void __launch_bounds__(kThr, 1)
       uint32_t sv[64], dv[64];
       tmem_ld32(tmem + lane_off + S_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_ld32(tmem + lane_off + S_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-      tmem_ld32(tmem + lane_off + DP_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(dv));
-      tmem_ld32(tmem + lane_off + DP_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars->t_free);  // S and dP may be overwritten by the next own step
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free);  // S may be overwritten (the peer's relay tells the leader)
       bool full;
       int clo, chi;
       if (DIR == kDirKV) {  // columns are query rows c0 .. c0 + 127, this thread's row is key `row`
-        full = (c0 >= band_q_lo(g, rlast)) && (c0 + T - 1 <= band_q_hi(g, r0));
+        full = own_rows && (c0 >= band_q_lo(g, rlast)) && (c0 + T - 1 <= band_q_hi(g, r0));
         clo = band_q_lo(g, row) - c0;
         chi = band_q_hi(g, row) - c0;
       } else {  // columns are keys c0 .. c0 + 127, this thread's row is query `row`
-        full = (c0 >= band_key_lo(g, rlast)) && (c0 + T - 1 <= band_key_hi(g, r0));
+        full = own_rows && (c0 >= band_key_lo(g, rlast)) && (c0 + T - 1 <= band_key_hi(g, r0));
         clo = band_key_lo(g, row) - c0;
         chi = band_key_hi(g, row) - c0;
       }
-      if (full) p_tile64<true, DIR == kDirKV>(sv, lse4, rs_row.x, sl2, cb0, clo, chi);
-      else p_tile64<false, DIR == kDirKV>(sv, lse4, rs_row.x, sl2, cb0, clo, chi);
+      if (DIR == kDirKV && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stats_full[wg], m & 1, abort_flag, R))) {
+        ok = false;
+        break;
+      }
+      if (full) p_tile64<true, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, clo, chi);
+      else p_tile64<false, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, clo, chi);
       uint32_t o[32];
       if (DIR == kDirKV) {
         pack64(sv, o);
-        if (!send(o, 0, (uint32_t)NP, m)) {  // P^T -> dV accumulator
+        if (!send(o, 0, dst_p, m)) {  // P^T -> dV accumulator
           ok = false;
           break;
         }
       }
-      ds_tile64<DIR == kDirKV>(sv, dv, dl4, rs_row.y, o);
-      if (!send(o, 1, DIR == kDirKV ? (uint32_t)NP + 1 : (uint32_t)NP, m)) {  // dS -> dK / dQ accumulator
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->p_full, m & 1, abort_flag, R))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + DP_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(dv));
+      tmem_ld32(tmem + lane_off + DP_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_free);  // dP may be overwritten
+      ds_tile64<DIR == kDirKV>(sv, dv, dl_s, rs_row.y, o);
+      if (DIR == kDirKV) {
+        // the warpgroup has read this step's statistics: the next step's may land
+        mbar_arrive(&bars->stats_free[wg]);
+        if (issuer && lane == 0 && m + 1 < n_own) {
+          if (!mbar_wait_cl(&bars->stats_free[wg], m & 1, abort_flag, R)) ok = false;
+          else load_stats(m + 1);
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!send(o, 1, dst_ds, m)) {  // dS -> dK / dQ accumulator
         ok = false;
         break;
       }
     }
-    // unwinding: the last copy out of the staging half must have been read
+    // unwinding: the last copy out of the staging half must have been read,
+    // and the last statistics load must have landed
     if (!ok && issuer && copies > 0) mbar_wait_drain(&bars->stg_free[wg], (copies - 1) & 1);
+    if (st_issued > 0) mbar_wait_drain(&bars->stats_full[wg], (st_issued - 1) & 1);
   } else {
-    // ------------------------------------------------------------ epilogue (accumulator roles)
+    // ------------------------------------------------------------ epilogue (accumulator roles, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    if (warp == 2 && elect_one()) {
-      // as soon as a producer's tile has landed, both of its staging halves may
-      // be rewritten: tell it then, not when the MMA thread reaches the step
-      for (int n = 0; n < N; ++n) {
-        const int s2 = n % NP;
-        if (!mbar_wait_cl(&bars->recv_full[s2], (n / NP) & 1, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[0]), (uint32_t)s2));
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[1]), (uint32_t)s2));
+    if ((warp == 2 || warp == 3) && elect_one()) {
+      // one warp per producer pair: as soon as a warpgroup's half of a tile
+      // has landed, that staging half of the producer may be rewritten (tell
+      // it then, not when the MMAs reach the step); the peer also tells the
+      // leader that its rows of the step's A operand are here
+      const int p2 = warp - 2;
+      const uint32_t prod = (uint32_t)(2 * p2) + h;
+      for (int j = 0; p2 + NPP * j < N; ++j) {
+        const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
+        if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[0]), prod));
+        if (!mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[1]), prod));
+        bars->n_recv[p2] = j + 1;
+        if (!leader) mbar_arrive_remote(mapa(smem_u32(&bars->peer_recv[slot]), lead));
       }
     }
     __syncwarp();
@@ -587,26 +688,42 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA issues a copy or a remote arrival past this point
-  if (acc_role && threadIdx.x == 0) {
-    // unwinding: tiles the producers sent that were never consumed must land
-    // before this CTA's shared memory is released
-    for (uint32_t pr = 0; pr < (uint32_t)NP; ++pr) {
-      int sent0, sent1;
-      asm volatile("ld.shared::cluster.u32 %0, [%1];"
-                   : "=r"(sent0)
-                   : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][0]), pr))
-                   : "memory");
-      asm volatile("ld.shared::cluster.u32 %0, [%1];"
-                   : "=r"(sent1)
-                   : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][1]), pr))
-                   : "memory");
-      const int sent = max(sent0, sent1);  // a step with either half in flight
-      // producer pr sent its own steps 0 .. sent - 1, i.e. steps pr + NP m
-      for (int m = 0; m < sent; ++m) {
-        const int n = (int)pr + NP * m;
-        if (n >= bars->n_recv) mbar_wait_drain(&bars->recv_full[pr], m & 1);
+  cluster_sync();  // no CTA issues a load, a copy or a remote arrival past this point
+  if (threadIdx.x == 0 && *abort_flag) {
+    // unwinding only.  Accumulators: tiles the producers sent that were never
+    // observed must land before this CTA's shared memory is released.
+    if (acc_role) {
+      for (int pr = 0; pr < NPP; ++pr) {
+        const uint32_t prod = (uint32_t)(2 * pr) + h;
+        int sent0, sent1;
+        asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                     : "=r"(sent0)
+                     : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][0]), prod))
+                     : "memory");
+        asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                     : "=r"(sent1)
+                     : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][1]), prod))
+                     : "memory");
+        // warpgroup w of producer pair pr sent the halves of its own steps 0 .. sent_w - 1
+        for (int m = bars->n_recv[pr]; m < sent0; ++m)
+          mbar_wait_drain(&bars->recv_full[pr * RS + m % RS][0], (m / RS) & 1);
+        for (int m = bars->n_recv[pr]; m < sent1; ++m)
+          mbar_wait_drain(&bars->recv_full[pr * RS + m % RS][1], (m / RS) & 1);
       }
+    }
+    // Leader: the ring loads of both CTAs complete on its barriers; let the
+    // last load of each slot (of either CTA) land.
+    if (leader) {
+      int peer_issued;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                   : "=r"(peer_issued)
+                   : "r"(mapa(smem_u32(&bars->n_issued), lead + 1))
+                   : "memory");
+      const int issued = max(bars->n_issued, peer_issued);
+      const int nr = acc_role ? NR_A : NR_P;
+      for (int k = issued - 1; k >= 0 && k >= issued - nr; --k)
+        mbar_wait_drain(&bars->ring_full[k % nr], (k / nr) & 1);
+      if (!acc_role) mbar_wait_drain(&bars->res_full, 0);
     }
   }
   __syncthreads();
@@ -614,24 +731,36 @@ __global__ void __launch_bounds__(kThr, 1)
   if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
-template <int DIR, int NP>
-cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                       const uint16_t* g16, const float* stats, int Lpad, float* out0, float* out1, int* status,
-                       cudaStream_t s) {
-  CUtensorMap tq, tk, tv, tg;
+template <int DIR>
+cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
+                        const uint16_t* g16, const float* stats, int Lpad, float* out0, float* out1, int* status,
+                        cudaStream_t s) {
+  // streamed operands (64-row halves, two chunks per slice), the resident dP
+  // operand (one chunk of 128 rows per load), accumulator operands (two chunks
+  // of 128 rows per load)
+  CUtensorMap tmS, tmP, tmR, tmA0, tmA1;
   cudaError_t e;
-  if ((e = make_tmap_f16(&tq, q16, DH, g.Lq, g.B * g.Hq, T)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16(&tg, g16, DH, g.Lq, g.B * g.Hq, T)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16(&tk, k16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
-  if ((e = make_tmap_f16(&tv, v16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
-  auto kern = bwd512_kernel<DIR, NP>;
+  if (DIR == kDirKV) {
+    if ((e = make_tmap_f16_chunks(&tmS, q16, DH, g.Lq, g.B * g.Hq, HT, 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tmP, g16, DH, g.Lq, g.B * g.Hq, HT, 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tmR, v16, DH, g.L, g.B * g.Hkv, T)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tmA0, g16, DH, g.Lq, g.B * g.Hq, T, 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tmA1, q16, DH, g.Lq, g.B * g.Hq, T, 2)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_tmap_f16_chunks(&tmS, k16, DH, g.L, g.B * g.Hkv, HT, 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tmP, v16, DH, g.L, g.B * g.Hkv, HT, 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16(&tmR, g16, DH, g.Lq, g.B * g.Hq, T)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tmA0, k16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tmA1, k16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
+  }
+  auto kern = bwd512_kernel<DIR>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) != cudaSuccess)
     return e;
-  Params512 pm;
+  ParamsPair pm;
   pm.g = g;
   pm.out0 = out0;
   pm.out1 = out1;
@@ -640,10 +769,10 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
   pm.Lpad = Lpad;
   pm.n_tiles = ((DIR == kDirKV ? g.L : g.Lq) + T - 1) / T;  // resident-side tiles
   pm.status = status;
-  const unsigned R = NP + ((DIR == kDirKV) ? 2 : 1);
+  const unsigned R = (DIR == kDirKV) ? 8u : 6u;
   const unsigned xs = (DIR == kDirKV) ? R : R * (unsigned)g.G;  // dQ pass: the group's query heads along x
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(xs, (unsigned)pm.n_tiles, (unsigned)(g.B * g.Hkv));
+  cfg.gridDim = dim3(xs, (unsigned)((pm.n_tiles + 1) / 2), (unsigned)(g.B * g.Hkv));
   cfg.blockDim = dim3(kThr, 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
@@ -654,21 +783,21 @@ cudaError_t launch_dir(const Geom& g, const uint16_t* q16, const uint16_t* k16, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tg, pm);
+  return cudaLaunchKernelEx(&cfg, kern, tmS, tmP, tmR, tmA0, tmA1, pm);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                  const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
-                                  int* status, cudaStream_t s) {
-  return launch_dir<kDirKV, 3>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
+                                   const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
+                                   int* status, cudaStream_t s) {
+  return launch_pair<kDirKV>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
 }
 
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
-                                const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
-                                cudaStream_t s) {
-  return launch_dir<kDirQ, 3>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s);
+                                 const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
+                                 cudaStream_t s) {
+  return launch_pair<kDirQ>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s);
 }
 
 }  // namespace swa
