@@ -376,11 +376,19 @@ __global__ void __launch_bounds__(kThr, 1)
           const uint32_t idS = idesc_f16(2 * T, T, 0, 0, 0, 0);  // M = 256 (the pair's rows), both K-major
           const uint64_t yd = smem_desc_sw128(sbase, 16, 1024);  // resident dP operand
           ok = mbar_wait_cl(&bars->res_full, 0, abort_flag, R) && mbar_wait_cl(&bars->pair_ready, 0, abort_flag, R);
-          int used = 0;
+          // Own step m takes ring loads 8 m .. 8 m + 7: load k of the step sits
+          // in slot k % 4 with phase parity k / 4, both fixed at compile time,
+          // so the unrolled issue below is MMAs with constant operand offsets
+          // (a single thread issues every MMA of the pair; its per-instruction
+          // work bounds the rate at which the tensor pipe is fed).
+          static_assert(NR_P == 4 && 2 * (DH / 128) == 8, "slot and parity of load k are k % 4 and k / 4");
+          const uint32_t x_tm = tmem + X_COL, s_tm = tmem + S_COL, dp_tm = tmem + DP_COL;
+          const uint64_t rd = smem_desc_sw128(sbase + OFF_RING_P, 16, 1024);
           for (int m = 0; ok && m < n_own; ++m) {
             // S of step m (slices 0-3) once the elementwise warps read S of step m - 1, then dP
             // (slices 4-7) once they read dP of step m - 1: each overlaps the other's readout
-            for (int k = 0; k < 2 * (DH / 128); ++k, ++used) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
               if ((k & 3) == 0) {
                 if (m >= 1 && !mbar_wait_cl(k == 0 ? &bars->s_free : &bars->p_free, (m - 1) & 1, abort_flag, R)) {
                   ok = false;
@@ -388,26 +396,25 @@ __global__ void __launch_bounds__(kThr, 1)
                 }
                 tc_fence_after();
               }
-              const int s = used % NR_P;
-              if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_P) & 1, abort_flag, R)) {
+              if (!mbar_wait_cl(&bars->ring_full[k & 3], (k >> 2) & 1, abort_flag, R)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint64_t sd = smem_desc_sw128(sbase + OFF_RING_P + s * SLOT_P, 16, 1024);
+              const uint64_t sd = desc_add(rd, (k & 3) * SLOT_P);
 #pragma unroll
               for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * (k & 3) + cc;  // 64-column chunk of the head dim
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
+                  const int c = 2 * (k & 3) + cc;  // 64-column chunk of the head dim
                   const uint64_t bdk = desc_add(sd, cc * HT * 128 + ks * 32);
                   if (k < 4)  // S += X[:, chunk] slice^T, X from Tensor Memory (8 columns per 16 elements)
-                    mma_pair_ts(tmem + S_COL, tmem + X_COL + c * 32 + ks * 8, bdk, idS, (c | ks) ? 1u : 0u);
+                    mma_pair_ts(s_tm, x_tm + c * 32 + ks * 8, bdk, idS, (c | ks) ? 1u : 0u);
                   else
-                    mma_pair_ss(tmem + DP_COL, desc_add(yd, c * T * 128 + ks * 32), bdk, idS, (c | ks) ? 1u : 0u);
+                    mma_pair_ss(dp_tm, desc_add(yd, c * T * 128 + ks * 32), bdk, idS, (c | ks) ? 1u : 0u);
                 }
               }
-              mma_commit_pair(&bars->ring_empty[s], pmask);
+              mma_commit_pair(&bars->ring_empty[k & 3], pmask);
               if (k == 3) mma_commit_pair(&bars->s_full, pmask);
               if (k == 7) mma_commit_pair(&bars->p_full, pmask);
             }
