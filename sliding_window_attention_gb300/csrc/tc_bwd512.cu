@@ -30,9 +30,10 @@
 // bands, and the columns outside a row's band are zero in P and dS.
 //
 // Warps: 0 TMA, 1 Tensor Memory owner and (leader CTA) MMA issuer, 2-9
-// elementwise (two warpgroups, 64 of the 128 columns each; a warpgroup
-// stages its 64-column half of a tile and warp 2 / 6 issues the copy), 10
-// slot release (accumulator roles).  Every wait is bounded; a timeout in one
+// elementwise (two warpgroups, 64 of the 128 columns each; each warp stages
+// its 32 rows of the warpgroup's 64-column half and copies them on at once),
+// 10 relay of the peer's releases (producers) or slot release
+// (accumulators).  Every wait is bounded; a timeout in one
 // CTA is broadcast to the whole cluster, every CTA drains its loads, copies
 // and MMAs in flight, and the status word records the timeout.
 #include <cuda.h>
@@ -95,7 +96,6 @@ struct Bars {
   uint64_t ring_empty[kMaxRing];  // (both) the pair's MMAs finished reading a slot
   uint64_t s_full, p_full;        // (producer, both) S / dP of a step in Tensor Memory
   uint64_t s_free, p_free;        // (producer) S / dP read: leader counts its 8 warps and the peer's relay
-  uint64_t staged[2];             // (producer) a warpgroup wrote its staging half
   uint64_t stg_free[2];           // (producer) the copy out of a staging half landed
   uint64_t dst_free[2][RS];       // (producer) accumulator slot may be written: [0] P -> dV, [1] dS -> dK / dQ
   uint64_t stats_full[2];         // (producer, dK/dV) a warpgroup's step statistics landed
@@ -281,7 +281,6 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(&bars->s_free, leader ? 9 : 8);
     mbar_init(&bars->p_free, leader ? 9 : 8);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->staged[s], 128);
       mbar_init(&bars->stg_free[s], 1);
       for (int j = 0; j < RS; ++j) mbar_init(&bars->dst_free[s][j], 1);
       mbar_init(&bars->stats_full[s], 1);
@@ -523,7 +522,7 @@ __global__ void __launch_bounds__(kThr, 1)
       rs_row = make_float2(p.stats[(size_t)head * p.Lpad + row], p.stats[((size_t)g.B * g.Hq + head) * p.Lpad + row]);
     const uint32_t stg = sbase + OFF_STG + wg * HALF_BYTES;
     const uint32_t stg_row = stg + r * 128;
-    const bool issuer = (warp & 3) == 2;  // warp 2 / 6 copies its warpgroup's half
+    const bool issuer = (warp & 3) == 2;  // warp 2 / 6 loads its warpgroup's step statistics
     int copies = 0;                       // copies out of this warpgroup's staging half
     bool ok = true;
     // stage one 64-column half tile and copy it into accumulator rank `dst`'s slot for this producer pair
@@ -534,17 +533,16 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int u = 0; u < 8; ++u)
         st_smem_v4(stg_row + ((u ^ (r & 7)) << 4), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
       fence_proxy_async_smem();
-      mbar_arrive(&bars->staged[wg]);
-      if (issuer) {
-        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->staged[wg], copies & 1, abort_flag, R) &&
-                                         mbar_wait_cl(&bars->dst_free[kind][m % RS], (m / RS) & 1, abort_flag, R)))
-          return false;
-        if (lane == 0) {
-          const int slot = pp * RS + m % RS;
-          bulk_copy_to_cta(mapa(sbase + OFF_RECV + slot * TILE_BYTES + wg * HALF_BYTES, dst), stg, HALF_BYTES,
-                           mapa(smem_u32(&bars->recv_full[slot][wg]), dst));
-          bars->n_sent[kind][wg] = m + 1;
-        }
+      // each warp copies its own 32 rows (4 KB) as soon as they are written:
+      // four copies in flight per warpgroup half instead of one
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->dst_free[kind][m % RS], (m / RS) & 1, abort_flag, R)))
+        return false;
+      if (lane == 0) {
+        const int slot = pp * RS + m % RS;
+        const uint32_t off = (uint32_t)(slot * TILE_BYTES + wg * HALF_BYTES + q4 * 32 * 128);
+        bulk_copy_to_cta(mapa(sbase + OFF_RECV + off, dst), stg + q4 * 32 * 128, 32 * 128,
+                         mapa(smem_u32(&bars->recv_full[slot][wg]), dst));
+        bars->n_sent[kind][wg] = m + 1;
       }
       ++copies;
       return true;
@@ -636,7 +634,7 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     // unwinding: the last copy out of the staging half must have been read,
     // and the last statistics load must have landed
-    if (!ok && issuer && copies > 0) mbar_wait_drain(&bars->stg_free[wg], (copies - 1) & 1);
+    if (!ok && lane == 0 && copies > 0) mbar_wait_drain(&bars->stg_free[wg], (copies - 1) & 1);
     if (st_issued > 0) mbar_wait_drain(&bars->stats_full[wg], (st_issued - 1) & 1);
   } else {
     // ------------------------------------------------------------ epilogue (accumulator roles, both CTAs)
