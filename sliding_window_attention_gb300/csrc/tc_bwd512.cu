@@ -56,8 +56,9 @@ constexpr int T = 128;     // rows of a resident tile, columns of a streamed ste
 constexpr int HT = 64;     // streamed rows per CTA of a pair
 constexpr int DH = 512;    // head dim
 constexpr int NPP = 2;     // producer pairs
-constexpr int kThr = 352;  // 11 warps
+constexpr int kThr = 384;  // 12 warps
 constexpr int kSigWarp = 10;
+constexpr int kStoreWarp = 11;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int RES_BYTES = T * DH * 2;       // resident dP A operand (V or dO), fp16
@@ -88,6 +89,15 @@ constexpr int STATS_BYTES = 2 * 512;
 // producer Tensor Memory: resident S operand (fp16 pairs), S, dP
 constexpr uint32_t X_COL = 0, S_COL = 256, DP_COL = 384;
 
+// Producer -> accumulator tiles travel through L2: the producer bulk-stores
+// a staged tile into the scratch of the accumulator CTA's SM (its staging is
+// free again as soon as the store has read it) and the accumulator loads it
+// into its operand slot.  One CTA of these kernels fills an SM, so the
+// scratch of an SM belongs to one accumulator CTA at a time: NRECV slots of
+// two 16 KB halves per SM.
+constexpr int kScratchSms = 192;
+__device__ __align__(1024) unsigned char g_tile_scratch[(size_t)kScratchSms * NRECV * TILE_BYTES];
+
 struct Bars {
   uint64_t res_full;              // (leader) both CTAs' resident dP operand landed
   uint64_t x_ready;               // (own) resident S operand written to Tensor Memory
@@ -96,17 +106,20 @@ struct Bars {
   uint64_t ring_empty[kMaxRing];  // (both) the pair's MMAs finished reading a slot
   uint64_t s_full, p_full;        // (producer, both) S / dP of a step in Tensor Memory
   uint64_t s_free, p_free;        // (producer) S / dP read: leader counts its 8 warps and the peer's relay
-  uint64_t stg_free[2];           // (producer) the copy out of a staging half landed
-  uint64_t dst_free[2][RS];       // (producer) accumulator slot may be written: [0] P -> dV, [1] dS -> dK / dQ
+  uint64_t staged[2];             // (producer) a warpgroup wrote its staging half
+  uint64_t stg_free[2];           // (producer) the store thread has read a staging half out
+  uint64_t scratch_free[2][RS];   // (producer) the accumulator loaded the scratch slot: [0] P -> dV, [1] dS -> dK / dQ
   uint64_t stats_full[2];         // (producer, dK/dV) a warpgroup's step statistics landed
   uint64_t stats_free[2];         // (producer, dK/dV) a warpgroup read its step statistics
-  uint64_t recv_full[NRECV][2];   // (accumulator, own) a warpgroup's half of the tile landed in slot
+  uint64_t tile_ready[NRECV];     // (accumulator) the producer's tile for slot is in the scratch
+  uint64_t recv_full[NRECV][2];   // (accumulator, own) half of the tile loaded into slot
   uint64_t peer_recv[NRECV];      // (accumulator leader) the peer's tile landed in slot
   uint64_t mma_done[NRECV];       // (accumulator, both) MMAs reading slot finished
   uint64_t acc_done, mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
-  int n_sent[2][2];               // (producer) steps copied to [dV, dK / dQ] by warpgroup [0, 1]
+  int smid;                       // (accumulator) SM this CTA runs on: the scratch it loads from
+  int n_loaded[NPP];              // (accumulator) own steps of producer pair p whose loads were issued
   int n_recv[NPP];                // (accumulator) own steps of producer pair p observed landed
   int n_issued;                   // ring loads issued by this CTA
 };
@@ -281,13 +294,14 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(&bars->s_free, leader ? 9 : 8);
     mbar_init(&bars->p_free, leader ? 9 : 8);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->staged[s], 128);
       mbar_init(&bars->stg_free[s], 1);
-      for (int j = 0; j < RS; ++j) mbar_init(&bars->dst_free[s][j], 1);
+      for (int j = 0; j < RS; ++j) mbar_init(&bars->scratch_free[s][j], 1);
       mbar_init(&bars->stats_full[s], 1);
       mbar_init(&bars->stats_free[s], 128);
-      bars->n_sent[s][0] = bars->n_sent[s][1] = 0;
     }
     for (int s = 0; s < NRECV; ++s) {
+      mbar_init(&bars->tile_ready[s], 1);
       mbar_init(&bars->recv_full[s][0], 1);
       mbar_init(&bars->recv_full[s][1], 1);
       mbar_init(&bars->peer_recv[s], 1);
@@ -296,7 +310,10 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
-    for (int s = 0; s < NPP; ++s) bars->n_recv[s] = 0;
+    uint32_t sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    bars->smid = sm < (uint32_t)kScratchSms ? (int)sm : -1;
+    for (int s = 0; s < NPP; ++s) bars->n_recv[s] = bars->n_loaded[s] = 0;
     bars->n_issued = 0;
     fence_mbar_init();
   }
@@ -467,24 +484,49 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_arrive_remote(mapa(smem_u32(&bars->p_free), lead));
       }
     }
-    // ------------------------------------------------------------ slot release (accumulator roles)
-    if (acc_role && elect_one()) {
-      // arm the slots for the first NRECV steps, then re-arm a slot for step
-      // n + NRECV once the MMAs of step n have read it; the producer CTA of the
-      // same half writes this CTA's slots
-      for (int n = 0; n < NRECV && n < N; ++n) {
-        const int j = n / NPP, slot = (n % NPP) * RS + j % RS;
-        mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
-        mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind][j % RS]), (uint32_t)(2 * (n % NPP)) + h));
+  } else if (warp == kStoreWarp) {
+    // ------------------------------------------------------------ tile stores (producers)
+    if (!acc_role && elect_one()) {
+      // in the order the warpgroups stage them: per own step P (dK/dV pass)
+      // then dS, each as two 16 KB halves into the scratch of the accumulator
+      // CTA of this half, which is told once both halves are written
+      int sm_dst[2];
+      for (int kind = 0; kind < 2; ++kind) {
+        const uint32_t dst = kind == 0 ? 4u + h : (DIR == kDirKV ? 6u : 4u) + h;
+        asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sm_dst[kind]) : "r"(mapa(smem_u32(&bars->smid), dst))
+                     : "memory");
       }
-      for (int n = 0; n + NRECV < N; ++n) {
-        const int j = n / NPP, slot = (n % NPP) * RS + j % RS;
-        if (!mbar_wait_cl(&bars->mma_done[slot], (j / RS) & 1, abort_flag, R)) break;
-        mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
-        mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[dst_kind][j % RS]), (uint32_t)(2 * (n % NPP)) + h));
+      bool ok = (DIR == kDirQ || sm_dst[0] >= 0) && sm_dst[1] >= 0;
+      if (!ok) cluster_abort(abort_flag, R);
+      int ci = 0;  // tiles staged per warpgroup so far
+      for (int m = 0; ok && m < n_own; ++m) {
+        const int slot = pp * RS + m % RS;
+        for (int kind = (DIR == kDirKV ? 0 : 1); ok && kind < 2; ++kind, ++ci) {
+          const uint32_t dst = kind == 0 ? 4u + h : (DIR == kDirKV ? 6u : 4u) + h;
+          if (m >= RS && !mbar_wait_cl(&bars->scratch_free[kind][m % RS], ((m / RS) - 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          unsigned char* gdst = g_tile_scratch + ((size_t)sm_dst[kind] * NRECV + slot) * TILE_BYTES;
+          for (int w = 0; w < 2; ++w) {
+            if (!mbar_wait_cl(&bars->staged[w], ci & 1, abort_flag, R)) {
+              ok = false;
+              break;
+            }
+            bulk_store_s2g(gdst + w * HALF_BYTES, sbase + OFF_STG + w * HALF_BYTES, HALF_BYTES);
+            bulk_commit_group();
+          }
+          if (!ok) break;
+          bulk_wait_read_all();
+          mbar_arrive(&bars->stg_free[0]);
+          mbar_arrive(&bars->stg_free[1]);
+          bulk_wait_all();
+          fence_proxy_async_global();
+          mbar_arrive_remote(mapa(smem_u32(&bars->tile_ready[slot]), dst));
+        }
       }
+      bulk_wait_all();  // no store still reads this CTA's shared memory
     }
   } else if (!acc_role) {
     // ------------------------------------------------------------ elementwise (producers, both CTAs)
@@ -526,29 +568,18 @@ __global__ void __launch_bounds__(kThr, 1)
     int copies = 0;                       // copies out of this warpgroup's staging half
     bool ok = true;
     // stage one 64-column half tile and copy it into accumulator rank `dst`'s slot for this producer pair
-    auto send = [&](const uint32_t (&o)[32], int kind, uint32_t dst, int m) -> bool {
+    // stage one 64-column half tile for the store thread
+    auto send = [&](const uint32_t (&o)[32]) -> bool {
       if (copies > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[wg], (copies - 1) & 1, abort_flag, R)))
         return false;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         st_smem_v4(stg_row + ((u ^ (r & 7)) << 4), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
       fence_proxy_async_smem();
-      // each warp copies its own 32 rows (4 KB) as soon as they are written:
-      // four copies in flight per warpgroup half instead of one
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->dst_free[kind][m % RS], (m / RS) & 1, abort_flag, R)))
-        return false;
-      if (lane == 0) {
-        const int slot = pp * RS + m % RS;
-        const uint32_t off = (uint32_t)(slot * TILE_BYTES + wg * HALF_BYTES + q4 * 32 * 128);
-        bulk_copy_to_cta(mapa(sbase + OFF_RECV + off, dst), stg + q4 * 32 * 128, 32 * 128,
-                         mapa(smem_u32(&bars->recv_full[slot][wg]), dst));
-        bars->n_sent[kind][wg] = m + 1;
-      }
+      mbar_arrive(&bars->staged[wg]);
       ++copies;
       return true;
     };
-    const uint32_t dst_p = 4u + h;                                  // dV accumulator of this half (KV)
-    const uint32_t dst_ds = (DIR == kDirKV ? 6u : 4u) + h;          // dK / dQ accumulator of this half
     // dK/dV pass: the statistics of own step m's 64 columns of this warpgroup
     // (lse * log2e, then Delta) are bulk-copied into shared memory while the
     // previous step is finished; every thread then reads them by broadcast
@@ -598,7 +629,7 @@ __global__ void __launch_bounds__(kThr, 1)
       uint32_t o[32];
       if (DIR == kDirKV) {
         pack64(sv, o);
-        if (!send(o, 0, dst_p, m)) {  // P^T -> dV accumulator
+        if (!send(o)) {  // P^T -> dV accumulator
           ok = false;
           break;
         }
@@ -627,34 +658,56 @@ __global__ void __launch_bounds__(kThr, 1)
           break;
         }
       }
-      if (!send(o, 1, dst_ds, m)) {  // dS -> dK / dQ accumulator
+      if (!send(o)) {  // dS -> dK / dQ accumulator
         ok = false;
         break;
       }
     }
-    // unwinding: the last copy out of the staging half must have been read,
-    // and the last statistics load must have landed
-    if (!ok && lane == 0 && copies > 0) mbar_wait_drain(&bars->stg_free[wg], (copies - 1) & 1);
+    // unwinding: the last statistics load must have landed (the store thread
+    // waits for its own stores)
     if (st_issued > 0) mbar_wait_drain(&bars->stats_full[wg], (st_issued - 1) & 1);
   } else {
     // ------------------------------------------------------------ epilogue (accumulator roles, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    if ((warp == 4 || warp == 5) && elect_one()) {
+      // one loader per producer pair: once the MMAs are done with a slot and
+      // the producer's tile is in the scratch, load it into the slot
+      const int p2 = warp - 4;
+      const unsigned char* scr = g_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * NRECV * TILE_BYTES;
+      bool ok = bars->smid >= 0;
+      if (!ok) cluster_abort(abort_flag, R);
+      for (int j = 0; ok && p2 + NPP * j < N; ++j) {
+        const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
+        if (j >= RS && !mbar_wait_cl(&bars->mma_done[slot], ((j / RS) - 1) & 1, abort_flag, R)) break;
+        mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
+        mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
+        if (!mbar_wait_cl(&bars->tile_ready[slot], ph, abort_flag, R)) {
+          // armed but never loaded: complete the phases so the drain below does not wait on them
+          ok = false;
+          break;
+        }
+        fence_proxy_async_global();
+        bulk_load_g2s(sbase + OFF_RECV + slot * TILE_BYTES, scr + (size_t)slot * TILE_BYTES, HALF_BYTES,
+                      &bars->recv_full[slot][0]);
+        bulk_load_g2s(sbase + OFF_RECV + slot * TILE_BYTES + HALF_BYTES, scr + (size_t)slot * TILE_BYTES + HALF_BYTES,
+                      HALF_BYTES, &bars->recv_full[slot][1]);
+        bars->n_loaded[p2] = j + 1;
+      }
+    }
     if ((warp == 2 || warp == 3) && elect_one()) {
-      // one warp per producer pair: as soon as a warpgroup's half of a tile
-      // has landed, that staging half of the producer may be rewritten (tell
-      // it then, not when the MMAs reach the step); the peer also tells the
-      // leader that its rows of the step's A operand are here
+      // one warp per producer pair: when both halves of a tile are in the
+      // slot, the producer may reuse that scratch slot; the peer also tells
+      // the leader that its rows of the step's A operand are here
       const int p2 = warp - 2;
       const uint32_t prod = (uint32_t)(2 * p2) + h;
       for (int j = 0; p2 + NPP * j < N; ++j) {
         const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
         if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[0]), prod));
         if (!mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[1]), prod));
         bars->n_recv[p2] = j + 1;
+        mbar_arrive_remote(mapa(smem_u32(&bars->scratch_free[dst_kind][j % RS]), prod));
         if (!leader) mbar_arrive_remote(mapa(smem_u32(&bars->peer_recv[slot]), lead));
       }
     }
@@ -695,26 +748,14 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   cluster_sync();  // no CTA issues a load, a copy or a remote arrival past this point
   if (threadIdx.x == 0 && *abort_flag) {
-    // unwinding only.  Accumulators: tiles the producers sent that were never
-    // observed must land before this CTA's shared memory is released.
+    // unwinding only.  Accumulators: tile loads issued but never observed
+    // must land before this CTA's shared memory is released.
     if (acc_role) {
-      for (int pr = 0; pr < NPP; ++pr) {
-        const uint32_t prod = (uint32_t)(2 * pr) + h;
-        int sent0, sent1;
-        asm volatile("ld.shared::cluster.u32 %0, [%1];"
-                     : "=r"(sent0)
-                     : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][0]), prod))
-                     : "memory");
-        asm volatile("ld.shared::cluster.u32 %0, [%1];"
-                     : "=r"(sent1)
-                     : "r"(mapa(smem_u32(&bars->n_sent[dst_kind][1]), prod))
-                     : "memory");
-        // warpgroup w of producer pair pr sent the halves of its own steps 0 .. sent_w - 1
-        for (int m = bars->n_recv[pr]; m < sent0; ++m)
-          mbar_wait_drain(&bars->recv_full[pr * RS + m % RS][0], (m / RS) & 1);
-        for (int m = bars->n_recv[pr]; m < sent1; ++m)
-          mbar_wait_drain(&bars->recv_full[pr * RS + m % RS][1], (m / RS) & 1);
-      }
+      for (int pr = 0; pr < NPP; ++pr)
+        for (int j = bars->n_recv[pr]; j < bars->n_loaded[pr]; ++j) {
+          mbar_wait_drain(&bars->recv_full[pr * RS + j % RS][0], (j / RS) & 1);
+          mbar_wait_drain(&bars->recv_full[pr * RS + j % RS][1], (j / RS) & 1);
+        }
     }
     // Leader: the ring loads of both CTAs complete on its barriers; let the
     // last load of each slot (of either CTA) land.
