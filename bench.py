@@ -497,6 +497,19 @@ def run_ours(args, w, world, rank, local_rank):
                    "sample": f"fp64 oracle fwd+bwd (band mode), 1 kv-head group ({G} query heads) x first {Ls} "
                              f"tokens ({_sample_q_rows(w, Ls)} query rows) of {w.name}, {secs:.1f} s; useful flops "
                              f"counted as on the GPU"}
+        # forward and backward separately, from the same per-launch events
+        # (forward: the v conversion and the forward or decode kernel;
+        # backward: everything launched by the backward call)
+        fwd_ms = sum(ms for n, (c, ms) in kernels.items() if n.startswith(("fwd", "convert"))) / args.steps
+        bwd_ms = sum(ms for n, (c, ms) in kernels.items() if n.startswith("bwd")) / args.steps
+        pk = peaks["bf16_tflops"]
+        split = {"fwd": {"ms": round(fwd_ms, 4), "tflops": round(w.fwd_flops() / (fwd_ms * 1e9), 2) if fwd_ms else None}}
+        split["fwd"]["pct_bf16_peak"] = round(100 * split["fwd"]["tflops"] / pk, 2) if fwd_ms else None
+        if not w.fwd_only and bwd_ms:
+            t10 = w.bwd_flops() / (bwd_ms * 1e9)
+            t8 = 8 * w.D * w.pairs() / (bwd_ms * 1e9)
+            split["bwd"] = {"ms": round(bwd_ms, 4), "tflops_10d": round(t10, 2), "pct_bf16_peak_10d": round(100 * t10 / pk, 2),
+                            "tflops_8d": round(t8, 2), "pct_bf16_peak_8d": round(100 * t8 / pk, 2)}
         per_kernel = {n: {"launches": c, "avg_ms": round(ms / c, 4), "share": round(ms / sum(x[1] for x in
                       kernels.values()), 4)} for n, (c, ms) in kernels.items()}
         line = {
@@ -516,6 +529,7 @@ def run_ours(args, w, world, rank, local_rank):
             "gpu_launches": launches,
             "clocks": clock_info,
             "kernels": per_kernel,
+            "split": split,
             "workspace_gb": {"fwd": round(fws_b / 1e9, 4), "bwd": round(bws_b / 1e9, 4),
                              "peak_above_inputs": round(peak_above_inputs / 1e9, 4)},
             "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),

@@ -132,6 +132,20 @@ def test_full_workload_properties(full_run):
 # invariants on the GPU
 
 
+def test_wide_group_elementwise_and_deterministic(oracle_mod):
+    # causal, eight query heads on one kv head (G = 8) at head dim 64: the
+    # dK/dV pass of each key tile runs up to 64 steps over the whole group
+    q, k, v, dO = make_inputs(1, 8, 1, 1024, 64, seed=4242)
+    scale = 0.125
+    ref = oracle_mod.backward(q, k, v, dO, 0, scale, band_only=True)
+    a = gpu_fwd_bwd(q, k, v, dO, 0, scale)
+    for n in ("dq", "dk", "dv"):
+        assert_close(n, a[n].numpy(), ref[n])
+    b = gpu_fwd_bwd(q, k, v, dO, 0, scale)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+
+
 def test_deterministic_bitwise():
     q, k, v, dO = make_inputs(1, 4, 2, 777, 128, seed=5)
     a = gpu_fwd_bwd(q, k, v, dO, 100, 0.09)
