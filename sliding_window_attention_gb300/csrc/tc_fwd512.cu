@@ -51,12 +51,14 @@ constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int TILE_BYTES = T * T * 2;       // fp16 128 x 128 P tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // one warpgroup's 64 columns (one swizzle chunk)
-// producer shared memory: two staging halves, row vectors, K ring
+// producer shared memory: two staging tiles (P of step n goes to tile n % 2,
+// so its copy is in flight while the next step's P is formed), row vectors,
+// K ring
 constexpr int OFF_STG = 0;
-constexpr int OFF_VEC = 2 * HALF_BYTES;  // alpha[128], inv_l[128], max exchange [2][2][128], l exchange [2][128]
-constexpr int OFF_RING_P = 40960;        // 1 KB aligned
+constexpr int OFF_VEC = 2 * TILE_BYTES;  // alpha[2][128], inv_l[128], max exchange [2][2][128], l exchange [2][128]
+constexpr int OFF_RING_P = OFF_VEC + 8192;  // 1 KB aligned
 constexpr int SLOT_P = T * 128 * 2;      // 128-column K slice: two TMA boxes under one barrier
-constexpr int NR_P = 5;
+constexpr int NR_P = 4;
 // accumulator shared memory: two P slots, two alpha slots + 1 / l, V ring
 constexpr int OFF_RECV = 0;
 constexpr int OFF_RVEC = 2 * TILE_BYTES;  // alpha slot [2][128], inv_l [128]
@@ -67,7 +69,7 @@ constexpr int DATA_P = OFF_RING_P + NR_P * SLOT_P;
 constexpr int DATA_A = OFF_RING_A + NR_A * SLOT_A;
 constexpr int DATA_BYTES = DATA_P > DATA_A ? DATA_P : DATA_A;
 constexpr uint32_t X_COL = 0, S_COL = 256;  // producer TMEM: Q [0, 256), S buffers [256, 512)
-static_assert(OFF_VEC + 512 + 512 + 2048 + 1024 <= OFF_RING_P, "producer vectors");
+static_assert(OFF_VEC + 1024 + 512 + 2048 + 1024 <= OFF_RING_P, "producer vectors");
 static_assert(OFF_RING_A % 1024 == 0 && OFF_RING_P % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 struct Bars {
@@ -76,7 +78,7 @@ struct Bars {
   uint64_t s_full[2], s_free[2];      // (producer) S buffers
   uint64_t mx[2];                     // (producer) both warpgroups posted their partial row max
   uint64_t staged[2];                 // (producer) a warpgroup wrote its staging half
-  uint64_t stg_free[2];               // (producer) the copy out of a staging half landed
+  uint64_t stg_free[2][2];            // (producer) the copy out of staging half [tile][warpgroup] landed
   uint64_t dst_free[2];               // (producer) accumulator slot may be written
   uint64_t lx;                        // (producer) both warpgroups posted their row sums
   uint64_t fin_staged;                // (producer) 1 / l written
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&bars->s_free[s], 256);
       mbar_init(&bars->mx[s], 256);
       mbar_init(&bars->staged[s], 128);
-      mbar_init(&bars->stg_free[s], 1);
+      mbar_init(&bars->stg_free[s][0], 1);
+      mbar_init(&bars->stg_free[s][1], 1);
       mbar_init(&bars->dst_free[s], 1);
       mbar_init(&bars->recv_full[s], 1);
       mbar_init(&bars->o_ready[s], 256);
@@ -328,8 +331,8 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int cb0 = 64 * wg;
     const float sl2 = g.scale * kLog2e;
-    float* alph = reinterpret_cast<float*>(base + OFF_VEC);  // [128]
-    float* finl = alph + 128;                                 // [128]
+    float* alph = reinterpret_cast<float*>(base + OFF_VEC);  // [2 tile][128]
+    float* finl = alph + 256;                                 // [128]
     float* xm = finl + 128;                                   // [2 parity][2 wg][128]
     float* xl = xm + 512;                                     // [2 wg][128]
     {
@@ -354,8 +357,7 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_before();
       mbar_arrive(&bars->q_ready);
     }
-    const uint32_t stg = sbase + OFF_STG + wg * HALF_BYTES;
-    const uint32_t stg_row = stg + r * 128;
+    const uint32_t stg0 = sbase + OFF_STG + wg * HALF_BYTES;
     const bool issuer = (warp & 3) == 2;  // warp 2 / 6 copies its warpgroup's half
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -395,15 +397,17 @@ __global__ void __launch_bounds__(kThr, 1)
       uint32_t pk[32];
       const float tsum = full ? half_p<true>(sr, sl2, m_use, clo, chi, pk) : half_p<false>(sr, sl2, m_use, clo, chi, pk);
       l_run = l_run * alpha + tsum;
-      // the previous copy out of this staging half (and of alpha) must have landed
-      if (n >= 1 && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[wg], (n - 1) & 1, abort_flag, R))) {
+      // the copy out of this staging half two steps ago (and of that alpha) must have landed
+      if (n >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[bb][wg], ((n >> 1) - 1) & 1, abort_flag, R))) {
         ok = false;
         break;
       }
+      const uint32_t stg = stg0 + bb * TILE_BYTES;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        st_smem_v4(stg_row + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      if (wg == 0) alph[r] = alpha;
+        st_smem_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      if (wg == 0) alph[bb * 128 + r] = alpha;
       fence_proxy_async_smem();
       mbar_arrive(&bars->staged[wg]);
       if (issuer) {
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kThr, 1)
           bulk_copy_to_cta(mapa(sbase + OFF_RECV + bb * TILE_BYTES + wg * HALF_BYTES, 1), stg, HALF_BYTES,
                            full_bar);
           if (wg == 0)
-            bulk_copy_to_cta(mapa(sbase + OFF_RVEC + bb * 512, 1), smem_u32(alph), 512, full_bar);
+            bulk_copy_to_cta(mapa(sbase + OFF_RVEC + bb * 512, 1), smem_u32(alph + bb * 128), 512, full_bar);
           bars->n_sent[wg] = n + 1;
         }
       }
@@ -440,7 +444,9 @@ __global__ void __launch_bounds__(kThr, 1)
       }
     }
     // unwinding: the last copy out of the staging half must have been read
-    if (!ok && issuer && bars->n_sent[wg] > 0) mbar_wait_drain(&bars->stg_free[wg], (bars->n_sent[wg] - 1) & 1);
+    if (!ok && issuer)
+      for (int m = bars->n_sent[wg] - 1; m >= 0 && m >= bars->n_sent[wg] - 2; --m)
+        mbar_wait_drain(&bars->stg_free[m & 1][wg], (m >> 1) & 1);
   } else {
     // ------------------------------------------------------------ rescale + epilogue (accumulator)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
@@ -458,9 +464,9 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       if (threadIdx.x == 64) {
         bars->n_recv = n + 1;
-        // both staging halves of the producer have been copied out
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[0]), 0));
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[1]), 0));
+        // both staging halves of the producer's tile n % 2 have been copied out
+        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[bb][0]), 0));
+        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[bb][1]), 0));
       }
       const float a = ralph[bb * 128 + r];
       if (__any_sync(0xffffffffu, a != 1.f)) {
