@@ -17,8 +17,8 @@
 //     CTA forms S and dP for its 128 rows and all 128 streamed columns, then
 //     P = exp(scale S - lse) and dS = P (dP - Delta) ("Training -- design
 //     (ORPO, flash-CCE head, prefix sharing, segmented backward)", section 6:
-//     recompute P from the stored lse), and bulk-copies the fp16 tiles into
-//     the accumulator CTA of the same half;
+//     recompute P from the stored lse), and hands the fp16 tiles to the
+//     accumulator CTA of the same half through an L2 scratch (below);
 //   accumulators (one pair per accumulator: ranks 4-5 dV += P^T dO and 6-7
 //     dK += dS^T Q in the dK/dV pass, ranks 4-5 dQ += dS K in the dQ pass)
 //     hold one 128 x 512 fp32 accumulator per CTA in Tensor Memory; the
@@ -30,12 +30,13 @@
 // bands, and the columns outside a row's band are zero in P and dS.
 //
 // Warps: 0 TMA, 1 Tensor Memory owner and (leader CTA) MMA issuer, 2-9
-// elementwise (two warpgroups, 64 of the 128 columns each; each warp stages
-// its 32 rows of the warpgroup's 64-column half and copies them on at once),
-// 10 relay of the peer's releases (producers) or slot release
-// (accumulators).  Every wait is bounded; a timeout in one
-// CTA is broadcast to the whole cluster, every CTA drains its loads, copies
-// and MMAs in flight, and the status word records the timeout.
+// elementwise (two warpgroups, 64 of the 128 columns each: producers stage
+// their half of each tile; in accumulators warps 2-3 watch the tiles land and
+// warps 4-5 load them, one warp per producer pair, before all of 2-9 write
+// the result), 10 relay of the peer's releases (producers), 11 tile stores
+// (producers).  Every wait is bounded; a timeout in one CTA is broadcast to
+// the whole cluster, every CTA drains its loads, stores and MMAs in flight,
+// and the status word records the timeout.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
