@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kThr, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
+cudaError_t launch_fwd_tc512_two_cta(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s) {
   CUtensorMap tk, tv;
   cudaError_t e;
