@@ -1,31 +1,37 @@
-// Tensor-core forward for head dim 512 on 2-CTA thread-block clusters.
+// Tensor-core forward for head dim 512 on clusters of CTA pairs.
 //
 // At D = 512 the output accumulator O of a 128-row query tile (512 fp32
 // columns) fills one SM's Tensor Memory, so S and O cannot live on the same
-// SM.  One cluster per (query head, 128-row query tile), longest rows first:
-//   rank 0 (producer): Q sits in Tensor Memory as fp16 pairs (256 columns,
-//     the A operand of TS-form MMAs); K streams in 128-column slices, one
-//     32 KB TMA instruction each (the per-SM TMA rate grows with the size of
-//     an instruction: about 46 B/clk for 16 KB, 81 for 32 KB);
-//     S = Q K^T (N = 128) into two TMEM buffers; online softmax with the band
-//     mask on edge tiles ("Lab 028 lab detail: Off NVIDIA, you fix the
-//     platform yourself", "What I changed, in plain terms" items 3-4); P in
-//     fp16 is staged and bulk-copied into the accumulator's operand slot with
-//     the per-row factor by which O must be rescaled; at the end it writes
-//     the row logsumexp (same section, item 1) and sends 1 / l.
-//   rank 1 (accumulator): O (512 columns) in Tensor Memory; V streams in
-//     128-column chunks; before O += P V of a step its elementwise warps
-//     rescale the rows whose running maximum moved (the maximum moves lazily,
-//     only when it grows by more than 2^8, so this is rare); at the end it
-//     writes O / l.
-// Each side issues 2048 MMA cycles per 128 x 128 step and one 32 KB tile
-// crosses distributed shared memory per step.
+// SM.  One 4-CTA cluster per (query head, two adjacent 128-row query tiles),
+// longest rows first.  Every role runs on a CTA pair (tcgen05 .cta_group::2):
+// each CTA of a pair owns one of the two query tiles, and each MMA of M = 256
+// rows takes its B operand half from each CTA, so every K and V tile crosses
+// each SM's TMA engine and shared memory once per pair, half in each CTA.
+//   producers (ranks 0-1): Q sits in Tensor Memory as fp16 pairs (256
+//     columns, the A operand of TS-form MMAs); each CTA streams its 64-key
+//     half of the step's K tile in 32 KB slices of 256 columns; S = Q K^T
+//     (N = 128 keys) into two TMEM buffers; online softmax with the band mask
+//     on edge tiles ("Lab 028 lab detail: Off NVIDIA, you fix the platform
+//     yourself", "What I changed, in plain terms" items 3-4); P in fp16 is
+//     staged (two staging tiles, so a tile is stored while the next P is
+//     formed) and handed, with the per-row factor by which O must be
+//     rescaled, to the accumulator CTA of the same half through an L2 scratch
+//     (below); at the end each CTA writes its rows' logsumexp (same section,
+//     item 1) and sends 1 / l.
+//   accumulators (ranks 2-3): O (512 columns) in Tensor Memory; each CTA
+//     streams its 128-column half of each 256-column V chunk; before O += P V
+//     of a step its elementwise warps rescale the rows whose running maximum
+//     moved (the maximum moves lazily, only when it grows by more than 2^8,
+//     so this is rare); at the end it writes O / l.
+// The pair's even CTA (the leader) issues the pair's MMAs; the peer's warps
+// arrive locally and one relay warp forwards one arrival per step.
 //
-// Warps: 0 TMA, 1 TMEM owner and MMA issuer, 2-9 elementwise (two
-// warpgroups, 64 columns of S or 256 columns of O each), 10 slot release
-// (accumulator).  Every wait is bounded; a timeout in one CTA is broadcast to
-// the cluster, every CTA drains its loads, copies and MMAs, and the status
-// word records it.
+// Warps: 0 TMA, 1 TMEM owner and (leader) MMA issuer, 2-9 elementwise (two
+// warpgroups, 64 columns of S or 256 columns of O each), 10 tile loads
+// (accumulators) or relay (producer peer), 11 tile stores (producers) or
+// relay (accumulator peer).  Every wait is bounded; a timeout in one CTA is
+// broadcast to the cluster, every CTA drains its loads, stores, copies and
+// MMAs, and the status word records it.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -40,71 +46,88 @@ namespace {
 
 using namespace tc;
 
-constexpr int T = 128;     // query rows per tile and key rows per step
+constexpr int T = 128;     // query rows per tile and keys per step
+constexpr int HT = 64;     // keys per CTA per step (producers)
 constexpr int DH = 512;    // head dim
-constexpr int kThr = 352;  // 11 warps
-constexpr int kSigWarp = 10;
-constexpr uint32_t R = 2;  // CTAs per cluster
+constexpr int kThr = 384;  // 12 warps
+constexpr int kSigWarp = 10, kRelayWarp = 11;  // 11: tile stores in producers, relay in accumulators
+constexpr uint32_t R = 4;  // CTAs per cluster
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int TILE_BYTES = T * T * 2;       // fp16 128 x 128 P tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // one warpgroup's 64 columns (one swizzle chunk)
-// producer shared memory: two staging tiles (P of step n goes to tile n % 2,
-// so its copy is in flight while the next step's P is formed), row vectors,
-// K ring
+// producer shared memory: two staging tiles, row vectors, K ring of 32 KB
+// slices (four 64-column chunks of this CTA's 64 keys)
 constexpr int OFF_STG = 0;
 constexpr int OFF_VEC = 2 * TILE_BYTES;  // alpha[2][128], inv_l[128], max exchange [2][2][128], l exchange [2][128]
-constexpr int OFF_RING_P = OFF_VEC + 8192;  // 1 KB aligned
-constexpr int SLOT_P = T * 128 * 2;      // 128-column K slice: two TMA boxes under one barrier
+constexpr int OFF_RING_P = OFF_VEC + 8192;
+constexpr int SLOT_P = HT * 256 * 2;
 constexpr int NR_P = 4;
-// accumulator shared memory: two P slots, two alpha slots + 1 / l, V ring
+// accumulator shared memory: two P slots, two alpha slots + 1 / l, V ring of
+// 32 KB slots (two 64-column chunks of the 128 keys)
 constexpr int OFF_RECV = 0;
 constexpr int OFF_RVEC = 2 * TILE_BYTES;  // alpha slot [2][128], inv_l [128]
 constexpr int OFF_RING_A = 2 * TILE_BYTES + 2048;
-constexpr int SLOT_A = T * 128 * 2;       // 128-column V chunk
+constexpr int SLOT_A = T * 128 * 2;
 constexpr int NR_A = 4;
 constexpr int DATA_P = OFF_RING_P + NR_P * SLOT_P;
 constexpr int DATA_A = OFF_RING_A + NR_A * SLOT_A;
 constexpr int DATA_BYTES = DATA_P > DATA_A ? DATA_P : DATA_A;
+constexpr int kMaxRing = NR_P > NR_A ? NR_P : NR_A;
 constexpr uint32_t X_COL = 0, S_COL = 256;  // producer TMEM: Q [0, 256), S buffers [256, 512)
 static_assert(OFF_VEC + 1024 + 512 + 2048 + 1024 <= OFF_RING_P, "producer vectors");
+
+// Producer -> accumulator P tiles (with their row factors) travel through L2:
+// a producer warp bulk-stores the staged tile into the scratch of the
+// accumulator CTA's SM (the staging is free as soon as the store has read
+// it) and the accumulator bulk-loads it into its operand slot.  One CTA of
+// this kernel fills an SM, so the scratch of an SM belongs to one
+// accumulator CTA at a time: two slots of a 32 KB tile + 512 B of factors.
+constexpr int kScratchSms = 192;
+constexpr int SCR_SLOT = TILE_BYTES + 1024;
+__device__ __align__(1024) unsigned char g_fwd_tile_scratch[(size_t)kScratchSms * 2 * SCR_SLOT];
 static_assert(OFF_RING_A % 1024 == 0 && OFF_RING_P % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 struct Bars {
-  uint64_t ring_full[11], ring_empty[11];
-  uint64_t q_ready;                   // (producer) Q in TMEM
-  uint64_t s_full[2], s_free[2];      // (producer) S buffers
-  uint64_t mx[2];                     // (producer) both warpgroups posted their partial row max
-  uint64_t staged[2];                 // (producer) a warpgroup wrote its staging half
-  uint64_t stg_free[2][2];            // (producer) the copy out of staging half [tile][warpgroup] landed
-  uint64_t dst_free[2];               // (producer) accumulator slot may be written
-  uint64_t lx;                        // (producer) both warpgroups posted their row sums
-  uint64_t fin_staged;                // (producer) 1 / l written
-  uint64_t recv_full[2];              // (accumulator) P tile + alpha landed
-  uint64_t o_ready[2];                // (accumulator) O rescaled for the step
-  uint64_t mma_done[2];               // (accumulator) PV of a step finished
-  uint64_t fin_full;                  // (accumulator) 1 / l landed
+  uint64_t ring_full[kMaxRing];  // (leader) both halves of a slot landed
+  uint64_t ring_empty[kMaxRing]; // (both) the pair's MMAs finished reading a slot
+  uint64_t q_ready;              // (producer, own) Q in TMEM
+  uint64_t pair_ready;           // (producer leader) both CTAs' Q in TMEM
+  uint64_t s_full[2], s_free[2]; // (producer) S buffers: filled (both) / read (leader: 8 warps + relay)
+  uint64_t mx[2];                // (producer) both warpgroups posted their partial row max
+  uint64_t staged[2][2];         // (producer) a warpgroup wrote its half of staging tile [tile][warpgroup]
+  uint64_t stg_free[2][2];       // (producer) the store warp has read staging half [tile][warpgroup] out
+  uint64_t scratch_free[2];      // (producer) the accumulator loaded scratch slot
+  uint64_t tile_ready[2];        // (accumulator) the producer's tile for slot is in the scratch
+  uint64_t recv_full[2];         // (accumulator) P tile + alpha landed in slot
+  uint64_t o_ready[2];           // (accumulator) rows rescaled for the step (leader: 8 warps + relay)
+  uint64_t mma_done[2];          // (accumulator, both) PV of a slot finished
+  uint64_t lx;                   // (producer) both warpgroups posted their row sums
+  uint64_t fin_staged;           // (producer) 1 / l written
+  uint64_t fin_full;             // (accumulator) 1 / l landed
   uint64_t acc_done, mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
-  int n_sent[2];                      // (producer) steps copied, per warpgroup
+  int n_sent[2];                 // (producer) steps copied, per warpgroup
   int fin_sent;
-  int n_recv;                         // (accumulator) steps received
+  int n_recv;                    // (accumulator) steps whose tile landed
+  int n_loaded;                  // (accumulator) steps whose tile loads were issued
+  int smid;                      // (accumulator) SM this CTA runs on: the scratch it loads from
+  int n_issued;                  // ring loads issued by this CTA
 };
-static_assert(NR_P <= 11 && NR_A <= 11, "ring barriers");
 
 constexpr size_t SMEM = (size_t)DATA_BYTES + 1024 + 1024;
 static_assert(SMEM <= 232448, "shared memory");
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
-struct FwdParams512 {
+struct FwdPairParams {
   Geom g;
   const uint16_t* q;  // bf16: S = Q K^T reads the caller's q and k as they are
   float* o;
   float* lse;
-  int n_tiles;
+  int n_tiles;        // 128-row query tiles
   int* status;
 };
 
@@ -148,7 +171,7 @@ __device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, flo
 
 __global__ void __launch_bounds__(kThr, 1)
     fwd512_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const FwdParams512 p) {
+                   const FwdPairParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(base + DATA_BYTES);
@@ -158,35 +181,46 @@ __global__ void __launch_bounds__(kThr, 1)
   const Geom& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const bool producer = rank == 0;
-  // Grid (x, y, z) = (2 x the group's query heads, query tiles, b * Hkv + kv
-  // head).  Blocks launch x fastest and z slowest, so the clusters running at
-  // any moment share one kv head, whose K and V then stay in L2.
+  const uint32_t h = rank & 1u;      // half of the pair: which query tile, which keys / columns
+  const uint32_t lead = rank & ~1u;  // the pair's leader
+  const bool leader = h == 0;
+  const uint16_t pmask = (uint16_t)(3u << lead);
+  const bool producer = rank < 2;
+  // Grid (x, y, z) = (4 x the group's query heads, query tile pairs, b * Hkv
+  // + kv head).  Blocks launch x fastest and z slowest, so the clusters
+  // running at any moment share one kv head, whose K and V then stay in L2.
   const int bkv = (int)blockIdx.z;
   const int b = bkv / g.Hkv;
   const int bh = b * g.Hq + (bkv - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // b * Hq + query head
-  const int tile = p.n_tiles - 1 - (int)blockIdx.y;  // longest rows first
-  const int i0 = tile * T;
-  const int ihi = min(i0 + T, g.Lq) - 1;
-  const int t_lo = band_key_lo(g, i0) / T;
-  const int N = band_key_hi(g, ihi) / T - t_lo + 1;  // key steps (at least one)
+  const int npairs = (p.n_tiles + 1) / 2;
+  const int tp = npairs - 1 - (int)blockIdx.y;  // longest rows first
+  const int pr0 = 2 * tp * T, prlast = min(pr0 + 2 * T, g.Lq) - 1;
+  const int i0 = pr0 + (int)h * T;  // this CTA's query tile
+  const bool own_rows = i0 < g.Lq;  // false for the second tile of an odd last pair
+  const int ihi = own_rows ? min(i0 + T, g.Lq) - 1 : i0;
+  // key steps meeting the band of the pair's rows (at least one)
+  const int t_lo = band_key_lo(g, pr0) / T;
+  const int N = band_key_hi(g, prlast) / T - t_lo + 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 11; ++s) {
+    for (int s = 0; s < kMaxRing; ++s) {
       mbar_init(&bars->ring_full[s], 1);
       mbar_init(&bars->ring_empty[s], 1);
     }
     mbar_init(&bars->q_ready, 256);
+    mbar_init(&bars->pair_ready, 2);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 256);
+      mbar_init(&bars->s_free[s], leader ? 9 : 8);
       mbar_init(&bars->mx[s], 256);
-      mbar_init(&bars->staged[s], 128);
+      mbar_init(&bars->staged[s][0], 128);
+      mbar_init(&bars->staged[s][1], 128);
       mbar_init(&bars->stg_free[s][0], 1);
       mbar_init(&bars->stg_free[s][1], 1);
-      mbar_init(&bars->dst_free[s], 1);
+      mbar_init(&bars->scratch_free[s], 1);
+      mbar_init(&bars->tile_ready[s], 1);
       mbar_init(&bars->recv_full[s], 1);
-      mbar_init(&bars->o_ready[s], 256);
+      mbar_init(&bars->o_ready[s], leader ? 9 : 8);
       mbar_init(&bars->mma_done[s], 1);
       bars->n_sent[s] = 0;
     }
@@ -198,20 +232,25 @@ __global__ void __launch_bounds__(kThr, 1)
     bars->abort_flag = 0;
     bars->fin_sent = 0;
     bars->n_recv = 0;
+    bars->n_loaded = 0;
+    bars->n_issued = 0;
+    uint32_t sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    bars->smid = sm < (uint32_t)kScratchSms ? (int)sm : -1;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(&bars->tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // every CTA's barriers exist before any remote arrive or copy
+  cluster_sync();  // every CTA's barriers exist before any remote arrive, load or copy
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA (both CTAs of a pair)
     if (elect_one()) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -220,114 +259,188 @@ __global__ void __launch_bounds__(kThr, 1)
       const int nr = producer ? NR_P : NR_A;
       for (int n = 0; ok && n < N; ++n) {
         const int j0 = (t_lo + n) * T;
-        for (int c = 0; c < DH / 128; ++c, ++issued) {
+        for (int c = 0; c < 2; ++c, ++issued) {
           const int s = issued % nr;
           if (issued >= nr && !mbar_wait_cl(&bars->ring_empty[s], ((issued / nr) & 1) ^ 1, abort_flag, R)) {
             ok = false;
             break;
           }
+          const uint32_t fb = mapa(smem_u32(&bars->ring_full[s]), lead);
           if (producer) {
-            unsigned char* dst = base + OFF_RING_P + s * SLOT_P;
-            mbar_arrive_expect_tx(&bars->ring_full[s], SLOT_P);
-            tma_load_4d(dst, &tmK, &bars->ring_full[s], 0, j0, 2 * c, bkv);  // chunks 2c, 2c + 1
+            // this CTA's 64 keys, head-dim columns [256 c, 256 c + 256)
+            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_P);
+            tma_load_4d_pair(base + OFF_RING_P + s * SLOT_P, &tmK, fb, 0, j0 + HT * (int)h, 4 * c, bkv);
           } else {
-            unsigned char* dst = base + OFF_RING_A + s * SLOT_A;
-            mbar_arrive_expect_tx(&bars->ring_full[s], SLOT_A);
-            tma_load_4d(dst, &tmV, &bars->ring_full[s], 0, j0, 2 * c, bkv);
+            // the 128 keys, this CTA's 128 columns of chunk c (head-dim columns [256 c + 128 h, +128))
+            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_A);
+            tma_load_4d_pair(base + OFF_RING_A + s * SLOT_A, &tmV, fb, 0, j0, 4 * c + 2 * (int)h, bkv);
           }
         }
       }
-      if (!ok) {
-        // unwinding: let the loads in flight land (at most one per slot)
-        for (int k = issued - 1; k >= 0 && k >= issued - nr; --k)
-          mbar_wait_drain(&bars->ring_full[k % nr], (k / nr) & 1);
-      }
+      bars->n_issued = issued;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (leader)
     if (elect_one()) {
       bool ok = true;
-      const uint32_t idS = idesc_f16(T, T, 1, 1, 0, 0);     // Q (TMEM) x K slice (K-major), both bf16
-      const uint32_t idPV = idesc_f16(T, 128, 0, 0, 0, 1);  // P (K-major) x V chunk (MN-major)
-      int used = 0;
       if (producer) {
+        // both CTAs: Q is in Tensor Memory -> tell the leader
         ok = mbar_wait_cl(&bars->q_ready, 0, abort_flag, R);
-        for (int n = 0; ok && n < N; ++n) {
-          const int bb = n & 1;
-          if (n >= 2 && !mbar_wait_cl(&bars->s_free[bb], ((n >> 1) & 1) ^ 1, abort_flag, R)) {
-            ok = false;
-            break;
-          }
+        if (ok) {
           tc_fence_after();
-          for (int c = 0; c < DH / 128; ++c, ++used) {
-            const int s = used % NR_P;
-            if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_P) & 1, abort_flag, R)) {
+          tc_fence_before();
+          if (leader) mbar_arrive(&bars->pair_ready);
+          else mbar_arrive_remote(mapa(smem_u32(&bars->pair_ready), lead));
+        }
+        if (leader && ok) {
+          const uint32_t idS = idesc_f16(2 * T, T, 1, 1, 0, 0);  // Q (TMEM) x K half (K-major), both bf16
+          const uint64_t rd = smem_desc_sw128(sbase + OFF_RING_P, 16, 1024);
+          const uint32_t x_tm = tmem + X_COL;
+          ok = mbar_wait_cl(&bars->pair_ready, 0, abort_flag, R);
+          for (int n = 0; ok && n < N; ++n) {
+            const int bb = n & 1;
+            if (n >= 2 && !mbar_wait_cl(&bars->s_free[bb], ((n >> 1) - 1) & 1, abort_flag, R)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t kd = smem_desc_sw128(sbase + OFF_RING_P + s * SLOT_P, 16, 1024);
-            // head-dim columns [128 c, 128 c + 128): Q columns 64 c + 8 ks in TMEM
+            const uint32_t s_tm = tmem + S_COL + bb * T;
+            // unrolled over the step: constant operand offsets from a per-slot
+            // base keep the single issuing thread ahead of the tensor pipe
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma_ts(tmem + S_COL + bb * T, tmem + X_COL + c * 64 + ks * 8,
-                     desc_add(kd, (ks >> 2) * T * 128 + (ks & 3) * 32), idS, (c | ks) ? 1u : 0u);
-            mma_commit(&bars->ring_empty[s]);
+            for (int k = 0; k < 2; ++k) {
+              const int li = 2 * n + k, s = li % NR_P;
+              if (!mbar_wait_cl(&bars->ring_full[s], (li / NR_P) & 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t kd = rd + (uint64_t)(s * (SLOT_P >> 4));
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                  // head-dim columns 256 k + 64 cc + 16 ks: Q columns 128 k + 32 cc + 8 ks in TMEM
+                  mma_pair_ts(s_tm, x_tm + 128 * k + 32 * cc + 8 * ks, desc_add(kd, cc * HT * 128 + ks * 32), idS,
+                              (k | cc | ks) ? 1u : 0u);
+                }
+              }
+              mma_commit_pair(&bars->ring_empty[s], pmask);
+            }
+            if (!ok) break;
+            mma_commit_pair(&bars->s_full[bb], pmask);
           }
-          if (!ok) break;
-          mma_commit(&bars->s_full[bb]);
         }
-      } else {
+      } else if (leader) {
+        const uint32_t idPV = idesc_f16(2 * T, 256, 0, 0, 0, 1);  // P (K-major) x V half chunks (MN-major)
+        int used = 0;
         for (int n = 0; ok && n < N; ++n) {
           const int bb = n & 1;
+          // both CTAs rescaled their rows, which they do once their P tile landed
           if (!mbar_wait_cl(&bars->o_ready[bb], (n >> 1) & 1, abort_flag, R)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + bb * TILE_BYTES, 16, 1024);
-          for (int c = 0; c < DH / 128; ++c, ++used) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
             const int s = used % NR_A;
             if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_A) & 1, abort_flag, R)) {
               ok = false;
               break;
             }
+            ++used;
             tc_fence_after();
             const uint64_t vd = smem_desc_sw128(sbase + OFF_RING_A + s * SLOT_A, T * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < T / 16; ++ks)
-              mma_ss(tmem + c * 128, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32), desc_add(vd, ks * 2048),
-                     idPV, (n | ks) ? 1u : 0u);
-            mma_commit(&bars->ring_empty[s]);
+              mma_pair_ss(tmem + 256 * c, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32), desc_add(vd, ks * 2048),
+                          idPV, (n | ks) ? 1u : 0u);
+            mma_commit_pair(&bars->ring_empty[s], pmask);
           }
           if (!ok) break;
-          mma_commit(&bars->mma_done[bb]);
+          mma_commit_pair(&bars->mma_done[bb], pmask);
         }
-        if (ok) mma_commit(&bars->acc_done);
+        if (ok) mma_commit_pair(&bars->acc_done, pmask);
       }
-      // every MMA issued so far has finished before TMEM is released
-      mma_commit(&bars->mma_drain);
+      // every MMA the leader issued has finished before either CTA releases Tensor Memory
+      if (leader) mma_commit_pair(&bars->mma_drain, pmask);
       mbar_wait_drain(&bars->mma_drain, 0);
     }
   } else if (warp == kSigWarp) {
-    // ------------------------------------------------------------ slot release (accumulator)
     if (!producer && elect_one()) {
+      // ------------------------------------------------------------ tile loads (accumulators)
+      // once the MMAs of step n - 2 are done with slot n % 2 and the producer's
+      // tile for step n is in the scratch, load it (P tile, then its factors)
       mbar_arrive_expect_tx(&bars->fin_full, 512);
-      for (int s = 0; s < 2 && s < N; ++s) {
-        mbar_arrive_expect_tx(&bars->recv_full[s], TILE_BYTES + 512);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[s]), 0));
+      const unsigned char* scr = g_fwd_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * 2 * SCR_SLOT;
+      bool ok = bars->smid >= 0;
+      if (!ok) cluster_abort(abort_flag, R);
+      for (int n = 0; ok && n < N; ++n) {
+        const int bb = n & 1;
+        if (n >= 2 && !mbar_wait_cl(&bars->mma_done[bb], ((n >> 1) - 1) & 1, abort_flag, R)) break;
+        mbar_arrive_expect_tx(&bars->recv_full[bb], TILE_BYTES + 512);
+        if (!mbar_wait_cl(&bars->tile_ready[bb], (n >> 1) & 1, abort_flag, R)) break;
+        fence_proxy_async_global();
+        bulk_load_g2s(sbase + OFF_RECV + bb * TILE_BYTES, scr + bb * SCR_SLOT, TILE_BYTES, &bars->recv_full[bb]);
+        bulk_load_g2s(sbase + OFF_RVEC + bb * 512, scr + bb * SCR_SLOT + TILE_BYTES, 512, &bars->recv_full[bb]);
+        bars->n_loaded = n + 1;
       }
-      for (int n = 0; n + 2 < N; ++n) {
-        if (!mbar_wait_cl(&bars->mma_done[n & 1], (n >> 1) & 1, abort_flag, R)) break;
-        mbar_arrive_expect_tx(&bars->recv_full[n & 1], TILE_BYTES + 512);
-        mbar_arrive_remote(mapa(smem_u32(&bars->dst_free[n & 1]), 0));
+    } else if (producer && !leader && elect_one()) {
+      // ------------------------------------------------------------ relay (producer peer)
+      for (int n = 0; n < N; ++n) {
+        if (!mbar_wait_cl(&bars->s_free[n & 1], (n >> 1) & 1, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->s_free[n & 1]), lead));
+      }
+    }
+  } else if (warp == kRelayWarp) {
+    if (producer && elect_one()) {
+      // ------------------------------------------------------------ tile stores (producers)
+      int sm_dst;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sm_dst) : "r"(mapa(smem_u32(&bars->smid), 2u + h))
+                   : "memory");
+      bool ok = sm_dst >= 0;
+      if (!ok) cluster_abort(abort_flag, R);
+      unsigned char* scr = g_fwd_tile_scratch + (size_t)(sm_dst < 0 ? 0 : sm_dst) * 2 * SCR_SLOT;
+      for (int n = 0; ok && n < N; ++n) {
+        const int bb = n & 1;
+        if (n >= 2 && !mbar_wait_cl(&bars->scratch_free[bb], ((n >> 1) - 1) & 1, abort_flag, R)) break;
+        fence_proxy_async_global();
+        unsigned char* gdst = scr + bb * SCR_SLOT;
+        for (int w = 0; w < 2; ++w) {
+          // one barrier per staging tile: the warpgroups can be a step ahead of this warp
+          if (!mbar_wait_cl(&bars->staged[bb][w], (n >> 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          bulk_store_s2g(gdst + w * HALF_BYTES, sbase + OFF_STG + bb * TILE_BYTES + w * HALF_BYTES, HALF_BYTES);
+        }
+        if (!ok) break;
+        bulk_store_s2g(gdst + TILE_BYTES, sbase + OFF_VEC + bb * 512, 512);  // the step's row factors
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(&bars->stg_free[bb][0]);
+        mbar_arrive(&bars->stg_free[bb][1]);
+        bulk_wait_all();
+        fence_proxy_async_global();
+        mbar_arrive_remote(mapa(smem_u32(&bars->tile_ready[bb]), 2u + h));
+      }
+      bulk_wait_all();  // no store still reads this CTA's shared memory
+    }
+    // ------------------------------------------------------------ relay (accumulator peer)
+    if (!producer && !leader && elect_one()) {
+      for (int n = 0; n < N; ++n) {
+        if (!mbar_wait_cl(&bars->o_ready[n & 1], (n >> 1) & 1, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->o_ready[n & 1]), lead));
       }
     }
   } else if (producer) {
-    // ------------------------------------------------------------ softmax (producer)
+    // ------------------------------------------------------------ softmax (producers, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const int i = i0 + r;
+    const bool row_ok = i < g.Lq;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int cb0 = 64 * wg;
     const float sl2 = g.scale * kLog2e;
@@ -335,17 +448,17 @@ __global__ void __launch_bounds__(kThr, 1)
     float* finl = alph + 256;                                 // [128]
     float* xm = finl + 128;                                   // [2 parity][2 wg][128]
     float* xl = xm + 512;                                     // [2 wg][128]
+    const uint32_t acc = 2u + h;                              // accumulator CTA of this half
     {
-      // Q row i into Tensor Memory: fp16 pairs, one 32-bit column each; warpgroup
+      // Q row i into Tensor Memory: bf16 pairs, one 32-bit column each; warpgroup
       // wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + ((size_t)bh * g.Lq + (i < g.Lq ? i : 0)) * DH) + wg * 32;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * DH) + wg * 32;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = i < g.Lq ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
           v[4 * q] = w4.x;
           v[4 * q + 1] = w4.y;
           v[4 * q + 2] = w4.z;
@@ -361,8 +474,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const bool issuer = (warp & 3) == 2;  // warp 2 / 6 copies its warpgroup's half
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    int n = 0;
-    for (; n < N; ++n) {
+    for (int n = 0; n < N; ++n) {
       const int bb = n & 1;
       const int j0 = (t_lo + n) * T;
       if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full[bb], (n >> 1) & 1, abort_flag, R))) {
@@ -375,8 +487,9 @@ __global__ void __launch_bounds__(kThr, 1)
       tmem_ld32(tmem + lane_off + S_COL + bb * T + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars->s_free[bb]);
-      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + T - 1 <= band_key_hi(g, i0));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free[bb]);  // the peer's relay tells the leader
+      const bool full = own_rows && (j0 >= band_key_lo(g, ihi)) && (j0 + T - 1 <= band_key_hi(g, i0));
       // visible key columns of row i in this tile, relative to this warpgroup's half
       const int clo = band_key_lo(g, i) - j0 - cb0;
       const int chi = band_key_hi(g, i) - j0 - cb0;
@@ -397,7 +510,7 @@ __global__ void __launch_bounds__(kThr, 1)
       uint32_t pk[32];
       const float tsum = full ? half_p<true>(sr, sl2, m_use, clo, chi, pk) : half_p<false>(sr, sl2, m_use, clo, chi, pk);
       l_run = l_run * alpha + tsum;
-      // the copy out of this staging half two steps ago (and of that alpha) must have landed
+      // the store of this staging half two steps ago (and of that alpha) must have read it
       if (n >= 2 &&
           !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[bb][wg], ((n >> 1) - 1) & 1, abort_flag, R))) {
         ok = false;
@@ -409,22 +522,8 @@ __global__ void __launch_bounds__(kThr, 1)
         st_smem_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       if (wg == 0) alph[bb * 128 + r] = alpha;
       fence_proxy_async_smem();
-      mbar_arrive(&bars->staged[wg]);
-      if (issuer) {
-        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->staged[wg], n & 1, abort_flag, R) &&
-                                         mbar_wait_cl(&bars->dst_free[bb], (n >> 1) & 1, abort_flag, R))) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t full_bar = mapa(smem_u32(&bars->recv_full[bb]), 1);
-          bulk_copy_to_cta(mapa(sbase + OFF_RECV + bb * TILE_BYTES + wg * HALF_BYTES, 1), stg, HALF_BYTES,
-                           full_bar);
-          if (wg == 0)
-            bulk_copy_to_cta(mapa(sbase + OFF_RVEC + bb * 512, 1), smem_u32(alph + bb * 128), 512, full_bar);
-          bars->n_sent[wg] = n + 1;
-        }
-      }
+      mbar_arrive(&bars->staged[bb][wg]);  // the store warp takes the tile from here
+      bars->n_sent[wg] = n + 1;
     }
     // row sum = the two warpgroups' partial sums (same running max); lse; send 1 / l
     xl[wg * 128 + r] = l_run;
@@ -432,23 +531,20 @@ __global__ void __launch_bounds__(kThr, 1)
     if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->lx, 0, abort_flag, R))) {
       const float l_tot = xl[r] + xl[128 + r];
       if (wg == 0) {
-        if (i < g.Lq) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
+        if (row_ok) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
         finl[r] = 1.f / l_tot;
         fence_proxy_async_smem();
         mbar_arrive(&bars->fin_staged);
         if (issuer && __all_sync(0xffffffffu, mbar_wait_cl(&bars->fin_staged, 0, abort_flag, R)) && lane == 0) {
-          bulk_copy_to_cta(mapa(sbase + OFF_RVEC + 1024, 1), smem_u32(finl), 512,
-                           mapa(smem_u32(&bars->fin_full), 1));
+          bulk_copy_to_cta(mapa(sbase + OFF_RVEC + 1024, acc), smem_u32(finl), 512,
+                           mapa(smem_u32(&bars->fin_full), acc));
           bars->fin_sent = 1;
         }
       }
     }
-    // unwinding: the last copy out of the staging half must have been read
-    if (!ok && issuer)
-      for (int m = bars->n_sent[wg] - 1; m >= 0 && m >= bars->n_sent[wg] - 2; --m)
-        mbar_wait_drain(&bars->stg_free[m & 1][wg], (m >> 1) & 1);
+    // (unwinding: the store warp waits for its own stores)
   } else {
-    // ------------------------------------------------------------ rescale + epilogue (accumulator)
+    // ------------------------------------------------------------ rescale + epilogue (accumulators, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const int i = i0 + r;
@@ -464,9 +560,8 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       if (threadIdx.x == 64) {
         bars->n_recv = n + 1;
-        // both staging halves of the producer's tile n % 2 have been copied out
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[bb][0]), 0));
-        mbar_arrive_remote(mapa(smem_u32(&bars->stg_free[bb][1]), 0));
+        // the producer may store its next tile into this scratch slot
+        mbar_arrive_remote(mapa(smem_u32(&bars->scratch_free[bb]), h));
       }
       const float a = ralph[bb * 128 + r];
       if (__any_sync(0xffffffffu, a != 1.f)) {
@@ -489,7 +584,8 @@ __global__ void __launch_bounds__(kThr, 1)
         tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(&bars->o_ready[bb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_ready[bb]);  // the peer's relay tells the leader
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R) &&
                                          mbar_wait_cl(&bars->fin_full, 0, abort_flag, R))) {
@@ -517,40 +613,53 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA issues a copy or a remote arrival past this point
-  if (!producer && threadIdx.x == 0) {
-    // unwinding: tiles the producer sent that were never consumed must land
-    // before this CTA's shared memory is released
-    int sent0, sent1, fsent;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sent0) : "r"(mapa(smem_u32(&bars->n_sent[0]), 0)) : "memory");
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sent1) : "r"(mapa(smem_u32(&bars->n_sent[1]), 0)) : "memory");
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(fsent) : "r"(mapa(smem_u32(&bars->fin_sent), 0)) : "memory");
-    const int sent = max(sent0, sent1);
-    for (int m = bars->n_recv; m < sent; ++m) mbar_wait_drain(&bars->recv_full[m & 1], (m >> 1) & 1);
-    if (fsent && *abort_flag) mbar_wait_drain(&bars->fin_full, 0);
+  cluster_sync();  // no CTA issues a load, a copy or a remote arrival past this point
+  if (threadIdx.x == 0 && *abort_flag) {
+    // unwinding only.  Accumulators: tiles the producer of this half sent
+    // that never landed must land before this CTA's shared memory is released.
+    if (!producer) {
+      int fsent;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(fsent) : "r"(mapa(smem_u32(&bars->fin_sent), h)) : "memory");
+      for (int m = bars->n_recv; m < bars->n_loaded; ++m) mbar_wait_drain(&bars->recv_full[m & 1], (m >> 1) & 1);
+      if (fsent) mbar_wait_drain(&bars->fin_full, 0);
+    }
+    // Leader: the ring loads of both CTAs complete on its barriers; let the
+    // last load of each slot (of either CTA) land.
+    if (leader) {
+      int peer_issued;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                   : "=r"(peer_issued)
+                   : "r"(mapa(smem_u32(&bars->n_issued), lead + 1))
+                   : "memory");
+      const int issued = max(bars->n_issued, peer_issued);
+      const int nr = producer ? NR_P : NR_A;
+      for (int k = issued - 1; k >= 0 && k >= issued - nr; --k)
+        mbar_wait_drain(&bars->ring_full[k % nr], (k / nr) & 1);
+    }
   }
   __syncthreads();
   cluster_sync();
   if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_tc512_two_cta(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
+cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s) {
   CUtensorMap tk, tv;
   cudaError_t e;
-  // 128-column slices of K and V: two 64-column chunks per TMA instruction
-  if ((e = make_tmap_f16_chunks(&tk, k, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
+  // K: 64 keys x four 64-column chunks per instruction (32 KB, one CTA's half
+  // of a 256-column slice); V: 128 keys x two chunks (32 KB)
+  if ((e = make_tmap_f16_chunks(&tk, k, DH, g.L, g.B * g.Hkv, HT, 4)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(fwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
       cudaSuccess)
     return e;
-  FwdParams512 pm;
+  FwdPairParams pm;
   pm.g = g;
   pm.q = q;
   pm.o = o;
@@ -558,7 +667,7 @@ cudaError_t launch_fwd_tc512_two_cta(const Geom& g, const uint16_t* q, const uin
   pm.n_tiles = (g.Lq + T - 1) / T;
   pm.status = status;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(R * (unsigned)g.G, (unsigned)pm.n_tiles, (unsigned)(g.B * g.Hkv));
+  cfg.gridDim = dim3(R * (unsigned)g.G, (unsigned)((pm.n_tiles + 1) / 2), (unsigned)(g.B * g.Hkv));
   cfg.blockDim = dim3(kThr, 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
