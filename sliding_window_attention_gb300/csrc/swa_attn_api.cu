@@ -83,6 +83,45 @@ int check_device() {
   return ok_cache[dev] == 1 ? SWA_OK : SWA_ERR_UNSUPPORTED_DEVICE;
 }
 
+// Per-device side stream for the dK/dV pass of the backward, with the two
+// events that fork it from and join it back to the caller's stream.  The
+// dK/dV and dQ passes read the same inputs and write disjoint outputs; run
+// side by side, the dQ pass takes the SMs that the dK/dV pass's clusters
+// leave idle (8-CTA clusters fit 120 of 152 SMs at head dim 512).  The side
+// stream has the highest priority, so a dK/dV cluster is placed first
+// whenever SMs free up.  `mu` serialises the record/wait sequence, so that
+// host threads sharing the events cannot interleave their forks.
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+
+SideStream* side_stream_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = g_side[dev];
+  std::lock_guard<std::mutex> lk(ss.mu);
+  if (!ss.stream) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+      if (f) cudaEventDestroy(f);
+      cudaStreamDestroy(st);
+      return nullptr;
+    }
+    ss.fork = f;
+    ss.join = j;
+    ss.stream = st;
+  }
+  return &ss;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -281,14 +320,25 @@ int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, con
         return swa::launch_bwd_prep(g, w.Lpad, q, k, v, dO, o, lse, q16, k16, v16, g16, stats, status, s);
       }) != cudaSuccess)
     return SWA_ERR_CUDA;
-  if (launch("bwd_dkdv_tc", s, [&] {
-        return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, s);
-      }) != cudaSuccess)
+  // dK/dV on the side stream (forked after the prep), dQ on the caller's
+  // stream, then the caller's stream waits for the side stream.
+  SideStream* side = side_stream_for_current_device();
+  if (!side) return SWA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(side->mu);
+  cudaStream_t t = side->stream;
+  if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(t, side->fork, 0) != cudaSuccess)
     return SWA_ERR_CUDA;
-  if (launch("bwd_dq_tc", s, [&] {
-        return swa::launch_bwd_dq_tc(g, q16, k16, v16, g16, stats, w.Lpad, dq, status, s);
-      }) != cudaSuccess)
+  const cudaError_t e_dkdv = launch("bwd_dkdv_tc", t, [&] {
+    return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, t);
+  });
+  const cudaError_t e_dq = launch("bwd_dq_tc", s, [&] {
+    return swa::launch_bwd_dq_tc(g, q16, k16, v16, g16, stats, w.Lpad, dq, status, s);
+  });
+  // the join is recorded even after a failed launch, so that the caller's
+  // stream never runs ahead of work already queued on the side stream
+  if (cudaEventRecord(side->join, t) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
     return SWA_ERR_CUDA;
+  if (e_dkdv != cudaSuccess || e_dq != cudaSuccess) return SWA_ERR_CUDA;
   return SWA_OK;
 }
 

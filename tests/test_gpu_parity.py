@@ -32,6 +32,7 @@ SMALL = [
     (1, 4, 2, 700, 512, 0),
     (1, 2, 1, 1100, 128, 300),
     (1, 4, 1, 2048, 512, 0),
+    (1, 2, 2, 300, 512, 0),  # one query head per kv head: a key pair with a single step
 ]
 
 
@@ -144,6 +145,44 @@ def test_wide_group_elementwise_and_deterministic(oracle_mod):
     b = gpu_fwd_bwd(q, k, v, dO, 0, scale)
     for n in a:
         assert torch.equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("D,L,W", [(128, 777, 100), (512, 700, 0)])
+def test_backward_on_user_stream_and_in_cuda_graph(D, L, W):
+    # The backward forks its dK/dV pass onto an internal stream and joins it
+    # back before returning.  On a caller's non-default stream, and captured
+    # into a CUDA graph and replayed, it must give the eager result bit for bit.
+    import sliding_window_attention_gb300 as swa
+
+    B, Hq, Hkv, scale = 1, 4, 2, 1.0 / math.sqrt(D)
+    q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, L, D, seed=77))
+    o, lse = swa.forward(q, k, v, W, scale)
+    ref = swa.backward(q, k, v, o, lse, dO, W, scale)
+    torch.cuda.synchronize()
+    f32 = dict(dtype=torch.float32, device="cuda")
+    outs = [torch.full((B, Hq, L, D), float("nan"), **f32), torch.full((B, Hkv, L, D), float("nan"), **f32),
+            torch.full((B, Hkv, L, D), float("nan"), **f32)]
+    ws = torch.empty(swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        swa.swa_attn_bwd(q, k, v, o, lse, dO, *outs, W, scale, ws, side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for a, b, n in zip(outs, ref, ("dq", "dk", "dv")):
+        assert torch.equal(a, b), n
+    for t in outs:
+        t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        swa.swa_attn_bwd(q, k, v, o, lse, dO, *outs, W, scale, ws)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    for a, b, n in zip(outs, ref, ("dq", "dk", "dv")):
+        assert torch.equal(a, b), n
 
 
 def test_deterministic_bitwise():

@@ -83,3 +83,21 @@ def test_reference_arm_two_ranks_rank0_only():
     line = json.loads(outs[1].splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_dominant_unit_groups_the_concurrent_backward_passes():
+    import bench
+
+    # two steps: forward 0.12 ms, prep 0.03 ms, dK/dV and dQ overlapping
+    # inside a 0.36 ms backward (their own spans add up to more than that)
+    k = {"convert_f16": (2, 0.02), "fwd_tc": (2, 0.24), "bwd_prep": (2, 0.06),
+         "bwd_dkdv_tc": (2, 0.54), "bwd_dq_tc": (2, 0.64)}
+    name, ms = bench.dominant_unit(k, 0.36, 2)
+    assert name == "bwd_dkdv_tc+bwd_dq_tc"
+    assert abs(ms - 0.33) < 1e-12
+    # a forward that outweighs the backward's pair stays the dominant unit
+    name, ms = bench.dominant_unit(dict(k, fwd_tc=(2, 0.80)), 0.36, 2)
+    assert (name, ms) == ("fwd_tc", 0.40)
+    # without the pair (the SIMT backward) each launch stands alone
+    s = {"fwd_simt": (2, 1.0), "bwd_delta": (2, 0.1), "bwd_dkdv_simt": (2, 4.0), "bwd_dq_simt": (2, 3.0)}
+    assert bench.dominant_unit(s, 3.55, 2) == ("bwd_dkdv_simt", 2.0)
