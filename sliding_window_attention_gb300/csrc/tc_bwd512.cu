@@ -9,8 +9,8 @@
 // pass), one per CTA, and each MMA of M = 256 rows takes its B operand half
 // from each CTA.  Every streamed tile therefore crosses each SM's TMA engine
 // and shared memory only once per pair, half in each CTA.
-//   producers (ranks 0-1 and 2-3, two pairs taking the streamed steps in
-//     turn): the A operand of S (K for dK/dV, Q for dQ: 128 x 512 fp16 per
+//   producers (three pairs in the dK/dV pass, ranks 0-5, two in the dQ
+//     pass, ranks 0-3, taking the streamed steps in turn): the A operand of S (K for dK/dV, Q for dQ: 128 x 512 fp16 per
 //     CTA = 256 columns) lives in Tensor Memory and feeds TS-form MMAs, the A
 //     operand of dP (V, or dO) in shared memory; the streamed tile arrives as
 //     two 64-row halves, one per CTA, in 16 KB slices of 128 columns.  Each
@@ -19,7 +19,7 @@
 //     (ORPO, flash-CCE head, prefix sharing, segmented backward)", section 6:
 //     recompute P from the stored lse), and hands the fp16 tiles to the
 //     accumulator CTA of the same half through an L2 scratch (below);
-//   accumulators (one pair per accumulator: ranks 4-5 dV += P^T dO and 6-7
+//   accumulators (one pair per accumulator: ranks 6-7 dV += P^T dO and 8-9
 //     dK += dS^T Q in the dK/dV pass, ranks 4-5 dQ += dS K in the dQ pass)
 //     hold one 128 x 512 fp32 accumulator per CTA in Tensor Memory; the
 //     streamed operand arrives in 128-column halves of 256-column chunks and
@@ -31,9 +31,9 @@
 //
 // Warps: 0 TMA, 1 Tensor Memory owner and (leader CTA) MMA issuer, 2-9
 // elementwise (two warpgroups, 64 of the 128 columns each: producers stage
-// their half of each tile; in accumulators warps 2-3 watch the tiles land and
-// warps 4-5 load them, one warp per producer pair, before all of 2-9 write
-// the result), 10 relay of the peer's releases (producers), 11 tile stores
+// their half of each tile; in accumulators warps 2 .. 1 + NPP watch the
+// tiles land and the next NPP warps load them, one warp per producer pair,
+// before all of 2-9 write the result), 10 relay of the peer's releases (producers), 11 tile stores
 // (producers).  Every wait is bounded; a timeout in one CTA is broadcast to
 // the whole cluster, every CTA drains its loads, stores and MMAs in flight,
 // and the status word records the timeout.
@@ -56,7 +56,6 @@ constexpr int kRoleProd = 0, kRoleAccP = 1, kRoleAccDS = 2;
 constexpr int T = 128;     // rows of a resident tile, columns of a streamed step
 constexpr int HT = 64;     // streamed rows per CTA of a pair
 constexpr int DH = 512;    // head dim
-constexpr int NPP = 2;     // producer pairs
 constexpr int kThr = 384;  // 12 warps
 constexpr int kSigWarp = 10;
 constexpr int kStoreWarp = 11;
@@ -72,17 +71,29 @@ constexpr int SLOT_P = 2 * HT * 128;
 constexpr int OFF_STG = RES_BYTES;
 constexpr int OFF_RING_P = RES_BYTES + 2 * HALF_BYTES;
 constexpr int DATA_BYTES = OFF_RING_P + NR_P * SLOT_P;
-// accumulator: RS operand slots per producer pair (a producer can send its
-// next tile while the accumulator still works on the previous one), then a
-// ring of 32 KB slots (two 64-column chunks of the 128 streamed rows)
-constexpr int RS = 2;
-constexpr int NRECV = NPP * RS;
+// Per pass: NPP producer pairs take the streamed steps in turn.  The dK/dV
+// pass has two accumulator pairs to feed per step and three producer pairs
+// (10-CTA clusters); the dQ pass has one accumulator pair and two producer
+// pairs (6-CTA clusters).  An accumulator holds RS operand slots per producer
+// pair (with two, a producer can send its next tile while the accumulator
+// still works on the previous one), then a ring of 32 KB slots (two 64-column
+// chunks of the 128 streamed rows).
 constexpr int OFF_RECV = 0;
-constexpr int OFF_RING_A = NRECV * TILE_BYTES;
 constexpr int SLOT_A = 2 * T * 128;
-constexpr int NR_A = (DATA_BYTES - OFF_RING_A) / SLOT_A;
-constexpr int kMaxRing = NR_A > NR_P ? NR_A : NR_P;
-static_assert(NR_A >= 2 && OFF_RING_A + NR_A * SLOT_A <= DATA_BYTES, "accumulator footprint");
+template <int DIR>
+struct PassCfg {
+  static constexpr int NPP = DIR == kDirKV ? 3 : 2;
+  static constexpr int RS = DIR == kDirKV ? 1 : 2;
+  static constexpr int NRECV = NPP * RS;
+  static constexpr uint32_t R = 2 * NPP + (DIR == kDirKV ? 4 : 2);  // CTAs per cluster
+  static constexpr int OFF_RING_A = NRECV * TILE_BYTES;
+  static constexpr int NR_A = (DATA_BYTES - OFF_RING_A) / SLOT_A;
+  static_assert(NR_A >= 2 && OFF_RING_A + NR_A * SLOT_A <= DATA_BYTES, "accumulator footprint");
+};
+constexpr int kMaxNpp = 3, kMaxRs = 2, kMaxRecv = 4;
+constexpr int kMaxRing = 4;
+static_assert(PassCfg<kDirKV>::NRECV <= kMaxRecv && PassCfg<kDirQ>::NRECV <= kMaxRecv, "receive slots");
+static_assert(PassCfg<kDirKV>::NR_A <= kMaxRing && PassCfg<kDirQ>::NR_A <= kMaxRing && NR_P <= kMaxRing, "rings");
 // producer, dK/dV pass: each warpgroup's step statistics (lse * log2e and
 // Delta of its 64 columns) staged in shared memory
 constexpr int OFF_STATS = DATA_BYTES;
@@ -94,10 +105,11 @@ constexpr uint32_t X_COL = 0, S_COL = 256, DP_COL = 384;
 // a staged tile into the scratch of the accumulator CTA's SM (its staging is
 // free again as soon as the store has read it) and the accumulator loads it
 // into its operand slot.  One CTA of these kernels fills an SM, so the
-// scratch of an SM belongs to one accumulator CTA at a time: NRECV slots of
-// two 16 KB halves per SM.
+// scratch of an SM belongs to one accumulator CTA at a time, whichever pass
+// it belongs to (the two passes run side by side): kMaxRecv slots of two
+// 16 KB halves per SM, of which a pass uses its NRECV.
 constexpr int kScratchSms = 192;
-__device__ __align__(1024) unsigned char g_tile_scratch[(size_t)kScratchSms * NRECV * TILE_BYTES];
+__device__ __align__(1024) unsigned char g_tile_scratch[(size_t)kScratchSms * kMaxRecv * TILE_BYTES];
 
 struct Bars {
   uint64_t res_full;              // (leader) both CTAs' resident dP operand landed
@@ -109,19 +121,19 @@ struct Bars {
   uint64_t s_free, p_free;        // (producer) S / dP read: leader counts its 8 warps and the peer's relay
   uint64_t staged[2];             // (producer) a warpgroup wrote its staging half
   uint64_t stg_free[2];           // (producer) the store thread has read a staging half out
-  uint64_t scratch_free[2][RS];   // (producer) the accumulator loaded the scratch slot: [0] P -> dV, [1] dS -> dK / dQ
+  uint64_t scratch_free[2][kMaxRs];  // (producer) the accumulator loaded the scratch slot: [0] P -> dV, [1] dS -> dK / dQ
   uint64_t stats_full[2];         // (producer, dK/dV) a warpgroup's step statistics landed
   uint64_t stats_free[2];         // (producer, dK/dV) a warpgroup read its step statistics
-  uint64_t tile_ready[NRECV];     // (accumulator) the producer's tile for slot is in the scratch
-  uint64_t recv_full[NRECV][2];   // (accumulator, own) half of the tile loaded into slot
-  uint64_t peer_recv[NRECV];      // (accumulator leader) the peer's tile landed in slot
-  uint64_t mma_done[NRECV];       // (accumulator, both) MMAs reading slot finished
+  uint64_t tile_ready[kMaxRecv];     // (accumulator) the producer's tile for slot is in the scratch
+  uint64_t recv_full[kMaxRecv][2];   // (accumulator, own) half of the tile loaded into slot
+  uint64_t peer_recv[kMaxRecv];      // (accumulator leader) the peer's tile landed in slot
+  uint64_t mma_done[kMaxRecv];       // (accumulator, both) MMAs reading slot finished
   uint64_t acc_done, mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
   int smid;                       // (accumulator) SM this CTA runs on: the scratch it loads from
-  int n_loaded[NPP];              // (accumulator) own steps of producer pair p whose loads were issued
-  int n_recv[NPP];                // (accumulator) own steps of producer pair p observed landed
+  int n_loaded[kMaxNpp];          // (accumulator) own steps of producer pair p whose loads were issued
+  int n_recv[kMaxNpp];            // (accumulator) own steps of producer pair p observed landed
   int n_issued;                   // ring loads issued by this CTA
 };
 
@@ -207,7 +219,12 @@ __global__ void __launch_bounds__(kThr, 1)
                    const __grid_constant__ CUtensorMap tmA0,  // dV accumulator operand, 128 rows x 2 chunks: dO
                    const __grid_constant__ CUtensorMap tmA1,  // dK / dQ accumulator operand: Q / K
                    const ParamsPair p) {
-  constexpr uint32_t R = (DIR == kDirKV) ? 8 : 6;  // CTAs per cluster
+  using C = PassCfg<DIR>;
+  constexpr int NPP = C::NPP, RS = C::RS, NRECV = C::NRECV, NR_A = C::NR_A, OFF_RING_A = C::OFF_RING_A;
+  constexpr uint32_t R = C::R;
+  // cluster ranks: producers 0 .. 2 NPP - 1, then the accumulator pairs (dV,
+  // then dK, in the dK/dV pass; dQ in the dQ pass)
+  constexpr uint32_t kAccP = 2 * NPP, kAccDS = 2 * NPP + (DIR == kDirKV ? 2 : 0);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(base + DATA_BYTES + STATS_BYTES);
@@ -221,7 +238,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t lead = rank & ~1u;  // the pair's leader
   const bool leader = h == 0;
   const uint16_t pmask = (uint16_t)(3u << lead);
-  const int role = rank < 4 ? kRoleProd : ((DIR == kDirKV && rank < 6) ? kRoleAccP : kRoleAccDS);
+  const int role = rank < kAccP ? kRoleProd : ((DIR == kDirKV && rank < kAccDS) ? kRoleAccP : kRoleAccDS);
   const bool acc_role = role != kRoleProd;
   const int pp = (int)(rank >> 1);  // producer pair (producers only)
   // Grid (x, y, z) = (CTAs per cluster [x query heads of the group, dQ pass],
@@ -493,7 +510,7 @@ __global__ void __launch_bounds__(kThr, 1)
       // CTA of this half, which is told once both halves are written
       int sm_dst[2];
       for (int kind = 0; kind < 2; ++kind) {
-        const uint32_t dst = kind == 0 ? 4u + h : (DIR == kDirKV ? 6u : 4u) + h;
+        const uint32_t dst = (kind == 0 ? kAccP : kAccDS) + h;
         asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sm_dst[kind]) : "r"(mapa(smem_u32(&bars->smid), dst))
                      : "memory");
       }
@@ -503,13 +520,13 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int m = 0; ok && m < n_own; ++m) {
         const int slot = pp * RS + m % RS;
         for (int kind = (DIR == kDirKV ? 0 : 1); ok && kind < 2; ++kind, ++ci) {
-          const uint32_t dst = kind == 0 ? 4u + h : (DIR == kDirKV ? 6u : 4u) + h;
+          const uint32_t dst = (kind == 0 ? kAccP : kAccDS) + h;
           if (m >= RS && !mbar_wait_cl(&bars->scratch_free[kind][m % RS], ((m / RS) - 1) & 1, abort_flag, R)) {
             ok = false;
             break;
           }
           fence_proxy_async_global();
-          unsigned char* gdst = g_tile_scratch + ((size_t)sm_dst[kind] * NRECV + slot) * TILE_BYTES;
+          unsigned char* gdst = g_tile_scratch + ((size_t)sm_dst[kind] * kMaxRecv + slot) * TILE_BYTES;
           for (int w = 0; w < 2; ++w) {
             if (!mbar_wait_cl(&bars->staged[w], ci & 1, abort_flag, R)) {
               ok = false;
@@ -672,11 +689,12 @@ __global__ void __launch_bounds__(kThr, 1)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    if ((warp == 4 || warp == 5) && elect_one()) {
-      // one loader per producer pair: once the MMAs are done with a slot and
-      // the producer's tile is in the scratch, load it into the slot
-      const int p2 = warp - 4;
-      const unsigned char* scr = g_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * NRECV * TILE_BYTES;
+    if (warp >= 2 + NPP && warp < 2 + 2 * NPP && elect_one()) {
+      // one loader per producer pair (warps 2 + NPP ..): once the MMAs are
+      // done with a slot and the producer's tile is in the scratch, load it
+      // into the slot
+      const int p2 = warp - 2 - NPP;
+      const unsigned char* scr = g_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * kMaxRecv * TILE_BYTES;
       bool ok = bars->smid >= 0;
       if (!ok) cluster_abort(abort_flag, R);
       for (int j = 0; ok && p2 + NPP * j < N; ++j) {
@@ -697,8 +715,8 @@ __global__ void __launch_bounds__(kThr, 1)
         bars->n_loaded[p2] = j + 1;
       }
     }
-    if ((warp == 2 || warp == 3) && elect_one()) {
-      // one warp per producer pair: when both halves of a tile are in the
+    if (warp >= 2 && warp < 2 + NPP && elect_one()) {
+      // one warp per producer pair (warps 2 ..): when both halves of a tile are in the
       // slot, the producer may reuse that scratch slot; the peer also tells
       // the leader that its rows of the step's A operand are here
       const int p2 = warp - 2;
@@ -752,8 +770,10 @@ __global__ void __launch_bounds__(kThr, 1)
     // unwinding only.  Accumulators: tile loads issued but never observed
     // must land before this CTA's shared memory is released.
     if (acc_role) {
+      // (the last load into each slot: earlier ones on the same barrier
+      // completed before it)
       for (int pr = 0; pr < NPP; ++pr)
-        for (int j = bars->n_recv[pr]; j < bars->n_loaded[pr]; ++j) {
+        for (int j = max(bars->n_recv[pr], bars->n_loaded[pr] - RS); j < bars->n_loaded[pr]; ++j) {
           mbar_wait_drain(&bars->recv_full[pr * RS + j % RS][0], (j / RS) & 1);
           mbar_wait_drain(&bars->recv_full[pr * RS + j % RS][1], (j / RS) & 1);
         }
@@ -816,7 +836,9 @@ cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16,
   pm.Lpad = Lpad;
   pm.n_tiles = ((DIR == kDirKV ? g.L : g.Lq) + T - 1) / T;  // resident-side tiles
   pm.status = status;
-  const unsigned R = (DIR == kDirKV) ? 8u : 6u;
+  constexpr unsigned R = PassCfg<DIR>::R;
+  if (R > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
   const unsigned xs = (DIR == kDirKV) ? R : R * (unsigned)g.G;  // dQ pass: the group's query heads along x
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(xs, (unsigned)((pm.n_tiles + 1) / 2), (unsigned)(g.B * g.Hkv));
