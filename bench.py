@@ -393,20 +393,25 @@ def run_ours(args, w, world, rank, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(mid=None):
+    def step(mid=None, after_fwd=None):
         # `mid`: an event recorded on the caller's stream between the forward
-        # and the backward call, which splits the step's time between them
+        # and the backward call, which splits the step's time between them;
+        # `after_fwd`: called on the host between the two calls
         if w.fwd_only:
             swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
         elif variant:
             swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
             if mid is not None:
                 mid.record(stream)
+            if after_fwd is not None:
+                after_fwd()
             swa.swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, W, w.causal, w.scale, bws, stream)
         else:
             swa.swa_attn_fwd(q, k, v, o, lse, W, w.scale, fws, stream)
             if mid is not None:
                 mid.record(stream)
+            if after_fwd is not None:
+                after_fwd()
             swa.swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, W, w.scale, bws, stream)
 
     for _ in range(args.warmup):
@@ -466,12 +471,39 @@ def run_ours(args, w, world, rank, local_rank):
     e2e_steps = max(3, min(args.steps, 10))
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
+    # Every step copies all of its inputs in and all of its results out.  With
+    # a backward, two of the copies run on a copy stream beside the kernels:
+    # dO's upload beside the forward, and the download of o and lse beside
+    # the backward.  The step ends when every copy has.
+    cs = torch.cuda.Stream(dev)
+    ev_dO, ev_fwd = torch.cuda.Event(), torch.cuda.Event()
+
     def e2e_step():
         for dst, src in ins:
+            if w.fwd_only or dst is not dO:
+                dst.copy_(src, non_blocking=True)
+        if w.fwd_only:
+            step()
+            for dst, src in zip(outs_h, results):
+                dst.copy_(src, non_blocking=True)
+            return
+        cs.wait_stream(stream)  # the previous step's backward has read dO
+        with torch.cuda.stream(cs):
+            dO.copy_(hdO, non_blocking=True)
+        ev_dO.record(cs)
+
+        def between():
+            stream.wait_event(ev_dO)
+            ev_fwd.record(stream)
+            cs.wait_event(ev_fwd)
+            with torch.cuda.stream(cs):
+                for dst, src in zip(outs_h[:2], results[:2]):  # o, lse
+                    dst.copy_(src, non_blocking=True)
+
+        step(after_fwd=between)
+        for dst, src in zip(outs_h[2:], results[2:]):  # dq, dk, dv
             dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in zip(outs_h, results):
-            dst.copy_(src, non_blocking=True)
+        stream.wait_stream(cs)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -559,7 +591,10 @@ def run_ours(args, w, world, rank, local_rank):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "copies": "pinned host memory; q, k, v in before the forward and dq, dk, dv out after the "
+                              "backward on the compute stream" + ("" if w.fwd_only else
+                              "; dO in beside the forward and o, lse out beside the backward on a copy stream")},
             "gpu_launches": launches,
             "clocks": clock_info,
             "kernels": per_kernel,

@@ -28,6 +28,15 @@
  *  - All tensor and workspace pointers are DEVICE pointers owned by the
  *    caller.  The library allocates no device or host memory on these
  *    paths.  Every output is fully overwritten (no accumulate-into).
+ *  - The first swa_attn_bwd / swa_attn_bwd_ex call on a device creates one
+ *    CUDA stream (highest priority, non-blocking) and two events for that
+ *    device, kept until the process exits; make that first call outside
+ *    stream capture.  Each backward runs its dK/dV pass on that stream,
+ *    beside the dQ pass on `stream`: the internal stream waits for the work
+ *    already on `stream`, and `stream` waits for the dK/dV pass before the
+ *    call returns.  Everything a call enqueues is therefore ordered on
+ *    `stream` as one sequence, and a call captured into a CUDA graph from
+ *    `stream` captures both passes.
  *  - Tensor pointers must be 16-byte aligned; the workspace 256-byte aligned.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) of the current device, which must be an sm_103
@@ -195,7 +204,7 @@ int swa_attn_version(void);
  * recorded on the launch stream.  profile_end() waits for those events and
  * writes per-kernel totals into out[0 .. *n_out - 1] (at most max_entries;
  * kernels are named by what they compute).  This mode allocates host memory
- * and CUDA events; it is the only one that does.
+ * and CUDA events per launch; it is the only one that allocates host memory.
  */
 typedef struct {
     char name[48];       /* kernel name, NUL-terminated */
