@@ -86,8 +86,9 @@ int check_device() {
 // Per-device side stream for the dK/dV pass of the backward, with the two
 // events that fork it from and join it back to the caller's stream.  The
 // dK/dV and dQ passes read the same inputs and write disjoint outputs; run
-// side by side, the dQ pass takes the SMs that the dK/dV pass's clusters
-// leave idle (8-CTA clusters fit 120 of 152 SMs at head dim 512).  The side
+// side by side, the dQ pass takes the SMs that the dK/dV pass leaves idle
+// (its last wave of one-SM CTAs at head dim 64-256; the 22 SMs outside its
+// 10-CTA clusters at head dim 512).  The side
 // stream has the highest priority, so a dK/dV cluster is placed first
 // whenever SMs free up.  `mu` serialises the record/wait sequence, so that
 // host threads sharing the events cannot interleave their forks.
