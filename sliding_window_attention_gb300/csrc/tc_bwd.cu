@@ -44,7 +44,6 @@ constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9: two
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kMinSmem = 120 * 1024;  // keep one CTA per SM (each owns all 512 TMEM columns)
 constexpr int kSmemMax = 232448;         // dynamic shared memory per block on sm_103 (227 KB)
-constexpr int clamp_stages(int n) { return n < 2 ? 2 : (n > 8 ? 8 : n); }
 
 // Backward preparation in one launch.  Segments 0-2 (blockIdx.y): fp16
 // copies of q, k and v, four 16-byte vectors in flight per thread.  Segment 3:
@@ -157,6 +156,7 @@ struct BwdParams {
   float* out0;  // dkdv: dk ; dq: dq
   float* out1;  // dkdv: dv
   const float* stats;  // two planes: lse * log2e, then Delta (B * Hq * Lpad floats each)
+  const uint16_t* x16;  // dQ at head dim 256: the fp16 copy of q (its rows go into Tensor Memory)
   int Lpad;
   int n_tiles;
   int* status;
@@ -858,44 +858,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
-// dQ for head dim 256 (32-row key steps; the two elementwise warpgroups take
-// alternate steps)
+// dQ for head dim 256 with 64-row key steps.  Q of the CTA's 128 rows sits in
+// Tensor Memory as fp16 pairs and is the A operand of S = Q K^T (TS form), so
+// shared memory holds only dO (64 KB) and two stages of K and V (32 KB each):
+// with Q and dO both in shared memory only 32-row key steps fit, and an MMA
+// of N = 32 runs at about 29% of the tensor rate, against about 60% for
+// N = 64.
+// TMEM: dQ [0, 256), Q [256, 384), S [384, 448), dP and then dS [448, 512).
+// Both elementwise warpgroups take every step, 32 of its 64 key columns
+// each.  dS (fp16 pairs) goes back over dP, the A operand of dQ += dS K, once
+// both warpgroups have read dP; dP(n + 1) is issued after dQ(n), and S(n + 1)
+// as soon as S(n) and dP(n) are read.
 template <int D>
 struct DqCfg {
   static constexpr int BMQ = 128;  // query rows per CTA (MMA M)
-  static constexpr int BN = 32;    // key rows per step
+  static constexpr int BN = 64;    // key rows per step (MMA N of S and dP)
+  static constexpr int CW = 32;    // key columns per warpgroup
   static constexpr int KCH = D / 64;
-  static constexpr int QT_BYTES = BMQ * D * 2;  // Q (or dO) tile
-  static constexpr int KV_BYTES = BN * D * 2;   // K (or V) tile
-  // K / V stages: as many as shared memory holds (TMA latency hiding)
-  static constexpr int NS = clamp_stages((kSmemMax - 2048 - 2 * QT_BYTES) / (2 * KV_BYTES));
-  static constexpr int DQ_COL = 0, S_COL = 256, DP_COL = 384;
-  static constexpr size_t SMEM_USED = 2 * (size_t)QT_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 + 1024;
+  static constexpr int QT_BYTES = BMQ * D * 2;  // dO tile
+  static constexpr int KV_BYTES = BN * D * 2;   // K or V tile (one 4-D TMA instruction)
+  static constexpr int NS = 2;                  // K / V stages
+  static constexpr uint32_t DQ_COL = 0, Q_COL = 256, S_COL = 384, DP_COL = 448;
+  static constexpr size_t SMEM_USED = (size_t)QT_BYTES + 2 * (size_t)NS * KV_BYTES + 1024 + 1024;
   static constexpr size_t SMEM = SMEM_USED > kMinSmem ? SMEM_USED : kMinSmem;
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-  static_assert(D == 256, "head dim 256 only (dQ fills the columns below the S buffers)");
+  static_assert(D == 256, "head dim 256 only (dQ fills the columns below Q, S and dP)");
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                 const BwdParams p) {
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
   using C = DqCfg<D>;
-  constexpr int BMQ = C::BMQ, BN = C::BN, NS = C::NS, KCH = C::KCH;
+  constexpr int BMQ = C::BMQ, BN = C::BN, NS = C::NS, KCH = C::KCH, CW = C::CW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sQ = base;
-  unsigned char* sG = sQ + C::QT_BYTES;
+  unsigned char* sG = base;
   unsigned char* sK = sG + C::QT_BYTES;
   unsigned char* sV = sK + NS * C::KV_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::KV_BYTES);
-  uint64_t* q_full = bars;              // [1]
-  uint64_t* kv_full = q_full + 1;       // [NS]
-  uint64_t* kv_empty = kv_full + NS;    // [NS]
-  uint64_t* sdp_full = kv_empty + NS;   // [2]
-  uint64_t* ds_full = sdp_full + 2;     // [2]
-  uint64_t* acc_done = ds_full + 2;     // [1]
+  uint64_t* g_full = bars;              // [1] dO landed
+  uint64_t* kv_full = g_full + 1;       // [NS] K and V of a stage landed
+  uint64_t* kv_empty = kv_full + NS;    // [NS] dQ of the stage's step finished (S and dP before it)
+  uint64_t* q_ready = kv_empty + NS;    // [1] the elementwise threads wrote Q into Tensor Memory
+  uint64_t* sdp_full = q_ready + 1;     // [1] S and dP of a step in Tensor Memory
+  uint64_t* sdp_read = sdp_full + 1;    // [1] every elementwise thread read S and dP of the step
+  uint64_t* ds_full = sdp_read + 1;     // [1] dS of the step written over dP
+  uint64_t* acc_done = ds_full + 1;     // [1]
   uint64_t* mma_drain = acc_done + 1;   // [1] every issued MMA finished (before TMEM is released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -913,15 +922,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt = t_hi - t_lo + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(g_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(sdp_full + s, 1);
-      mbar_init(ds_full + s, 128);
-    }
+    mbar_init(q_ready, 256);
+    mbar_init(sdp_full, 1);
+    mbar_init(sdp_read, 256);
+    mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
     mbar_init(mma_drain, 1);
     *abort_flag = 0;
@@ -938,66 +947,66 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (elect_one()) {
-      prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmG);
-      mbar_arrive_expect_tx(q_full, 2 * C::QT_BYTES);
-      for (int c = 0; c < KCH; ++c) {
-        tma_load_3d(sQ + c * BMQ * 128, &tmQ, q_full, c * 64, i0, bh);
-        tma_load_3d(sG + c * BMQ * 128, &tmG, q_full, c * 64, i0, bh);
-      }
+      mbar_arrive_expect_tx(g_full, C::QT_BYTES);
+      for (int c = 0; c < KCH; ++c) tma_load_3d(sG + c * BMQ * 128, &tmG, g_full, c * 64, i0, bh);
       int issued = 0;
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
         const int j0 = (t_lo + n) * BN;
         if (n >= NS && !mbar_wait(kv_empty + st, ((n / NS) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(kv_full + st, 2 * C::KV_BYTES);
-        for (int c = 0; c < KCH; ++c) {
-          tma_load_3d(sK + st * C::KV_BYTES + c * BN * 128, &tmK, kv_full + st, c * 64, j0, bkv);
-          tma_load_3d(sV + st * C::KV_BYTES + c * BN * 128, &tmV, kv_full + st, c * 64, j0, bkv);
-        }
+        // all KCH 64-column chunks of the BN rows in one instruction each
+        tma_load_4d(sK + st * C::KV_BYTES, &tmK, kv_full + st, 0, j0, 0, bkv);
+        tma_load_4d(sV + st * C::KV_BYTES, &tmV, kv_full + st, 0, j0, 0, bkv);
         ++issued;
       }
       if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
-        mbar_wait_drain(q_full, 0);
+        mbar_wait_drain(g_full, 0);
         drain_ring(kv_full, NS, issued);
       }
     }
   } else if (warp == 1) {
     if (elect_one()) {
-      const uint32_t idS = idesc_f16(BMQ, BN, 0, 0, 0, 0);  // Q x K^T, dO x V^T
-      const uint32_t idQ = idesc_f16(BMQ, D, 0, 0, 0, 1);   // dS x K (K MN-major)
-      const uint64_t qdk = smem_desc_sw128(smem_u32(sQ), 16, 1024);  // Q, K-major (resident)
+      const uint32_t idS = idesc_f16(BMQ, BN, 0, 0, 0, 0);  // Q x K^T (Q from TMEM), dO x V^T
+      const uint32_t idQ = idesc_f16(BMQ, D, 0, 0, 0, 1);   // dS x K (dS from TMEM, K MN-major)
       const uint64_t gdk = smem_desc_sw128(smem_u32(sG), 16, 1024);  // dO, K-major (resident)
-      bool ok = mbar_wait(q_full, 0, abort_flag);
+      bool ok = mbar_wait(g_full, 0, abort_flag) && mbar_wait(q_ready, 0, abort_flag);
       auto issue_dq = [&](int m) -> bool {
-        const int st = m % NS, sb = m & 1;
-        if (!mbar_wait(ds_full + sb, (m >> 1) & 1, abort_flag)) return false;
+        const int st = m % NS;
+        if (!mbar_wait(ds_full, m & 1, abort_flag)) return false;
         tc_fence_after();
         const uint64_t kmn = smem_desc_sw128(smem_u32(sK + st * C::KV_BYTES), BN * 128, 1024);  // K, MN-major
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ts(tmem + C::DQ_COL, tmem + C::DP_COL + sb * BN + ks * 8, desc_add(kmn, ks * 2048), idQ,
+          mma_ts(tmem + C::DQ_COL, tmem + C::DP_COL + ks * 8, desc_add(kmn, ks * 2048), idQ,
                  (m > 0 || ks > 0) ? 1u : 0u);
         mma_commit(kv_empty + st);
         return true;
       };
       for (int n = 0; ok && n < nt; ++n) {
-        const int st = n % NS, sb = n & 1;
+        const int st = n % NS;
         if (!mbar_wait(kv_full + st, (n / NS) & 1, abort_flag)) { ok = false; break; }
+        // S(n) overwrites S(n - 1): every elementwise thread has read it
+        if (n >= 1 && !mbar_wait(sdp_read, (n - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kk = smem_desc_sw128(smem_u32(sK + st * C::KV_BYTES), 16, 1024);  // K, K-major
         const uint64_t vk = smem_desc_sw128(smem_u32(sV + st * C::KV_BYTES), 16, 1024);  // V, K-major
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks & 3) * 32;
-          const uint32_t cq = (ks >> 2) * BMQ * 128, ck = (ks >> 2) * BN * 128;
-          mma_ss(tmem + C::S_COL + sb * BN, desc_add(qdk, cq + off), desc_add(kk, ck + off), idS, ks > 0 ? 1u : 0u);
-          mma_ss(tmem + C::DP_COL + sb * BN, desc_add(gdk, cq + off), desc_add(vk, ck + off), idS, ks > 0 ? 1u : 0u);
+          const uint32_t off = (ks & 3) * 32, ck = (ks >> 2) * BN * 128;
+          mma_ts(tmem + C::S_COL, tmem + C::Q_COL + ks * 8, desc_add(kk, ck + off), idS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(sdp_full + sb);
+        // dP(n) overwrites dS(n - 1), which dQ(n - 1) reads: issue that first
         if (n >= 1 && !issue_dq(n - 1)) { ok = false; break; }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks & 3) * 32, cq = (ks >> 2) * BMQ * 128, ck = (ks >> 2) * BN * 128;
+          mma_ss(tmem + C::DP_COL, desc_add(gdk, cq + off), desc_add(vk, ck + off), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full);
       }
       if (ok && issue_dq(nt - 1)) mma_commit(acc_done);
       // every MMA issued so far has finished before TMEM is released
@@ -1008,47 +1017,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - 2) >> 2;  // warps 2-5 / 6-9, see the dK/dV kernel
     const int r = 32 * (warp & 3) + (threadIdx.x & 31);
     const int i = i0 + r;
+    const bool row_ok = i < g.Lq;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sl2 = g.scale * kLog2e;
-    const float2 rs = (i < g.Lq) ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
-                                              p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
-                                : make_float2(0.f, 0.f);
+    {
+      // Q row i into Tensor Memory as fp16 pairs (one 32-bit column per two
+      // head-dim elements): warpgroup wg fills columns [64 wg, 64 wg + 64) of
+      // Q, head-dim elements [128 wg, 128 wg + 128)
+      const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D) + wg * 16;
+#pragma unroll 1
+      for (int j = 0; j < 2; ++j) {
+        uint32_t v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * q] = w4.x;
+          v[4 * q + 1] = w4.y;
+          v[4 * q + 2] = w4.z;
+          v[4 * q + 3] = w4.w;
+        }
+        tmem_st32(tmem + lane_off + C::Q_COL + wg * 64 + j * 32, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_ready);
+    }
+    const float2 rs = row_ok ? make_float2(p.stats[(size_t)bh * p.Lpad + i],
+                                           p.stats[((size_t)g.B * g.Hq + bh) * p.Lpad + i])
+                             : make_float2(0.f, 0.f);
+    // key columns of this warpgroup: cb0 .. cb0 + CW - 1 of each step
+    const int cb0 = wg * CW;
     bool ok = true;
-    constexpr int CW = BN;
-    for (int n = wg; n < nt; n += 2) {
-      const int sb = n & 1;
+    for (int n = 0; n < nt; ++n) {
       const int j0 = (t_lo + n) * BN;
-      if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(sdp_full, n & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
+      uint32_t sv[CW], dv[CW];
+      tmem_ld32(tmem + lane_off + C::S_COL + cb0, sv);
+      tmem_ld32(tmem + lane_off + C::DP_COL + cb0, dv);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(sdp_read);  // S may be overwritten; dP once both warpgroups have read it
       const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
       // key columns c of this tile visible to row i: j0 + c in [band_key_lo(i), band_key_hi(i)]
       const int clo = band_key_lo(g, i) - j0;
       const int chi = band_key_hi(g, i) - j0;
-      uint32_t sv[CW], dv[CW];
-#pragma unroll
-      for (int c = 0; c < CW / 32; ++c) {
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + c * 32));
-        tmem_ld32(tmem + lane_off + C::DP_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(dv + c * 32));
-      }
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < CW / 32; ++c) {
-        const uint32_t(&svc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(sv + c * 32);
-        const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
-        const int cb = c * 32;
-        uint32_t dd[16];
-        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
-        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
-        tmem_st16(tmem + lane_off + C::DP_COL + sb * BN + cb / 2, dd);
-      }
+      uint32_t dd[CW / 2];
+      if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, cb0, clo, chi, dd);
+      else dq_chunk<false>(sv, dv, sl2, rs.x, rs.y, cb0, clo, chi, dd);
+      // dS of keys cb0 .. cb0 + 31 goes to columns cb0 / 2 .. of the dP
+      // buffer, which the other warpgroup may still be reading
+      if (!__all_sync(0xffffffffu, mbar_wait(sdp_read, n & 1, abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      tmem_st16(tmem + lane_off + C::DP_COL + cb0 / 2, dd);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(ds_full + sb);
+      mbar_arrive(ds_full);
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
       // each warpgroup writes half of the dQ columns
-      const bool row_ok = i < g.Lq;
       float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
 #pragma unroll
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
@@ -1342,6 +1370,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
   BwdParams p;
   p.g = g;
   p.stats = stats;
+  p.x16 = nullptr;
   p.Lpad = Lpad;
   p.status = status;
   if (which == 0) {
@@ -1406,19 +1435,19 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
     kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
   } else {
     using C = DqCfg<D>;
-    CUtensorMap tq, tk, tv, tg;
-    if ((e = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
+    CUtensorMap tk, tv, tg;
     if ((e = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
+    if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
     auto kern = dq_tc_kernel<D>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
       return e;
     p.out0 = dq;
     p.out1 = nullptr;
+    p.x16 = q16;
     p.n_tiles = (g.Lq + C::BMQ - 1) / C::BMQ;
     dim3 grid(g.B * g.Hq, p.n_tiles);
-    kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
+    kern<<<grid, kThreads, C::SMEM, s>>>(tk, tv, tg, p);
   }
   return cudaGetLastError();
 }

@@ -33,6 +33,7 @@ SMALL = [
     (1, 2, 1, 1100, 128, 300),
     (1, 4, 1, 2048, 512, 0),
     (1, 2, 2, 300, 512, 0),  # one query head per kv head: a key pair with a single step
+    (1, 2, 1, 700, 256, 0),  # causal at head dim 256: up to 11 dQ key steps over two K/V stages
 ]
 
 
