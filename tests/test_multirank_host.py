@@ -101,3 +101,23 @@ def test_dominant_unit_groups_the_concurrent_backward_passes():
     # without the pair (the SIMT backward) each launch stands alone
     s = {"fwd_simt": (2, 1.0), "bwd_delta": (2, 0.1), "bwd_dkdv_simt": (2, 4.0), "bwd_dq_simt": (2, 3.0)}
     assert bench.dominant_unit(s, 3.55, 2) == ("bwd_dkdv_simt", 2.0)
+
+
+def test_cpu_baseline_adds_kv_groups_up_to_the_workload():
+    import dataclasses
+
+    import bench
+    from sliding_window_attention_gb300.inputs import WORKLOADS
+
+    # a whole-sequence sample of one group far shorter than the target: more
+    # kv-head groups are added, at most B * Hkv of them
+    w = dataclasses.replace(WORKLOADS["tiny_l256_d64_w64"], B=2, Hq=4, Hkv=2)
+    tf, secs, Ls, threads, groups = bench.cpu_oracle_sample(w, 30.0)
+    assert Ls == w.L and groups == w.B * w.Hkv and secs > 0 and tf > 0 and threads >= 1
+    # the rate counts every group's flops over the summed time
+    one = bench.oracle_useful_flops(w, Ls)
+    assert abs(tf - groups * one / secs / 1e12) <= 1e-9 * tf
+    # each added group draws its own inputs
+    a = bench._oracle_sample_inputs(w, Ls, 0)[0]
+    b = bench._oracle_sample_inputs(w, Ls, 1)[0]
+    assert not (a == b).all()
