@@ -12,6 +12,12 @@ divided by the device time of the K timed steps (max over ranks).  Each rank
 runs its own independent copy of the workload (weak scaling, no collective on
 the data path).  L2 is flushed (256 MiB write) before every timed step and
 the flush is outside the timed events.
+
+The default workload is the wide-head global layer at 16,384 tokens (B 1,
+32 query heads, 4 kv heads, D 512, causal).  The two windowed head-dim-256
+layers (8,192 tokens, and the ragged 30,553-token step with outlier keys)
+are measured after it, the same way, and reported in the same line under
+`sub_workloads`, each with its own value, split, roofline and workspace.
 """
 from __future__ import annotations
 
@@ -30,12 +36,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "causal_gqa_l8192_d128"
+# the wide-head global layer at 16,384 tokens; the two windowed D = 256 layers
+# the metric is quoted for run as sub-records of the same line
+DEFAULT_WORKLOAD = "global_l16384_d512"
+DEFAULT_SUB_WORKLOADS = ("sliding_l8192_d256_w1024", "ragged_l30553_d256_w1024_outliers")
 METRIC = "windowed attn fwd+bwd useful TFLOP/s & % bf16 TC peak; peak workspace GB"
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
-# per-kernel algorithmic flops per in-band (query, key) pair, in units of D
+# per-kernel flops the tensor cores ISSUE per in-band (query, key) pair, in
+# units of D (the backward recomputes S and dP in both of its passes)
 KERNEL_FLOPS_PER_PAIR_D = {
     "fwd_tc": 4,          # S = Q K^T, O += P V (tcgen05)
     "fwd_simt": 4,        # S = Q K^T, O += P V
@@ -46,6 +56,10 @@ KERNEL_FLOPS_PER_PAIR_D = {
 }
 # the backward's two passes, launched on two streams that run concurrently
 CONCURRENT_BWD = ("bwd_dkdv_tc", "bwd_dq_tc")
+# USEFUL flops per in-band pair, in units of D: forward Q K^T and P V (4 D);
+# backward S, dP, dV, dQ, dK once each (10 D, the convention the metric uses)
+USEFUL_FWD_PER_PAIR_D = 4
+USEFUL_BWD_PER_PAIR_D = 10
 HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_prep", "fwd_decode"}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -59,6 +73,10 @@ def parse_args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--seq-len", type=int, default=0,
                    help="override the workload's sequence length (smaller cases for profiler captures)")
+    p.add_argument("--sub-workloads", default=None,
+                   help="comma-separated workloads measured after the main one and reported in its line under "
+                        "sub_workloads ('' for none; default: the two windowed D = 256 layers when the main "
+                        "workload is the default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU baseline sample")
     return p.parse_args()
@@ -354,21 +372,89 @@ def _variant_keys(w):
     return out
 
 
-def run_ours(args, w, world, rank, local_rank):
+def roofline_record(kname: str, avg_ms: float, w, peaks: dict) -> dict:
+    """Roofline entry of the dominant unit `kname` (one kernel, or the
+    backward's two concurrent passes joined by '+') at `avg_ms` per launch.
+
+    Tensor-core units count USEFUL flops: 4 D per in-band pair for the
+    forward and 10 D for the backward (S, dP, dV, dQ, dK once each), so frac
+    is the useful-flop fraction of the bf16 peak.  What the kernels issue (the
+    backward recomputes S and dP in each pass) is reported beside it as
+    issued_flops_per_pair_d.  HBM-bound units count their algorithmic bytes."""
+    B, Hq, Hkv, L, D, Lq = w.B, w.Hq, w.Hkv, w.L, w.D, w.q_rows
+    avg_s = avg_ms / 1e3
+    if kname in HBM_KERNELS:
+        if kname == "bwd_delta":
+            alg = B * Hq * Lq * (D * 4 + D * 2 + 4)
+        elif kname == "bwd_prep":  # q, k, v, dO: bf16 read + fp16 write; o (fp32) and lse read; stats written
+            alg = 4 * D * B * (2 * Hq * Lq + 2 * Hkv * L) + B * Hq * Lq * (4 * D + 4 + 8)
+        elif kname == "fwd_decode":  # the K and V rows in band (bf16) once per kv head, q in, o and lse out
+            alg = B * Hkv * _band_keys(w) * D * 2 * 2 + B * Hq * Lq * (D * 2 + D * 4 + 4)
+        else:  # convert_f16 (forward): bf16 read + fp16 write of v
+            alg = 4 * D * B * Hkv * L
+        achieved = alg / avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "bytes_per_launch": alg}
+    else:
+        names = kname.split("+")
+
+        def issued_per_pair(n):
+            if n == "bwd_dkdv_tc" and D == 256:
+                return 10  # dV-only pass (S^T, dV) + dK-only pass (S^T, dP^T, dK)
+            return KERNEL_FLOPS_PER_PAIR_D.get(n, 4)
+
+        issued = sum(issued_per_pair(n) for n in names)
+        if names[0].startswith("fwd"):
+            useful = USEFUL_FWD_PER_PAIR_D
+        elif tuple(names) == CONCURRENT_BWD or set(names) == {"bwd_dkdv_simt", "bwd_dq_simt"}:
+            useful = USEFUL_BWD_PER_PAIR_D
+        else:  # one backward pass on its own: its share of the useful work is not defined; count issued
+            useful = issued
+        achieved = useful * D * w.pairs() / avg_s / 1e12
+        if kname.endswith("_simt"):
+            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
+        else:
+            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "peak_source": f"{peaks['source']} bf16 dense (burst)"}
+        roof["flops_per_pair_d"] = useful
+        roof["issued_flops_per_pair_d"] = issued
+        roof["pairs"] = w.pairs()
+    roof["kernel"] = kname
+    roof["ms_per_launch"] = round(avg_ms, 5)
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    parts = [ncu_traffic(n, w.name, D) for n in kname.split("+")]
+    roof["traffic"] = None if None in parts else sum(parts)
+    return roof
+
+
+def split_record(w, fwd_ms: float, bwd_ms: float, peaks: dict) -> dict:
+    """Forward and backward separately, from events on the caller's stream
+    around each call: forward at 4 D useful flops per pair, backward at 10 D
+    (and at 8 D, the count without the S / dP recompute)."""
+    pk = peaks["bf16_tflops"]
+    split = {"fwd": {"ms": round(fwd_ms, 4), "tflops": round(w.fwd_flops() / (fwd_ms * 1e9), 2) if fwd_ms else None}}
+    split["fwd"]["pct_bf16_peak"] = round(100 * split["fwd"]["tflops"] / pk, 2) if fwd_ms else None
+    if not w.fwd_only and bwd_ms:
+        t10 = w.bwd_flops() / (bwd_ms * 1e9)
+        t8 = 8 * w.D * w.pairs() / (bwd_ms * 1e9)
+        split["bwd"] = {"ms": round(bwd_ms, 4), "tflops_10d": round(t10, 2),
+                        "pct_bf16_peak_10d": round(100 * t10 / pk, 2), "tflops_8d": round(t8, 2),
+                        "pct_bf16_peak_8d": round(100 * t8 / pk, 2)}
+    return split
+
+
+def measure_workload(args, w, world, rank, local_rank, dist, peaks):
+    """Time K steps (after W warm-up steps) of workload `w` on this rank's GPU
+    and the same through pinned host buffers (e2e); returns the fields of one
+    bench record (rank 0's view, timings already maxed over ranks)."""
     import torch
 
     import sliding_window_attention_gb300 as swa
     from sliding_window_attention_gb300.inputs import make_inputs
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
-    torch.cuda.set_device(local_rank)
     dev = torch.device(f"cuda:{local_rank}")
-    peaks = load_peaks()
-
     # each rank: one independent copy of the workload (seed offset by rank)
     q_h, k_h, v_h, dO_h = make_inputs(w.B, w.Hq, w.Hkv, w.L, w.D, w.seed + 7919 * rank, w.do_scale,
                                       w.outlier_frac, w.outlier_mult)
@@ -377,6 +463,8 @@ def run_ours(args, w, world, rank, local_rank):
     variant = Lq != L or not w.causal
     if Lq < L:
         q_h, dO_h = (t[:, :, L - Lq:].contiguous() for t in (q_h, dO_h))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, dO_h))
     f32 = dict(dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
@@ -428,7 +516,7 @@ def run_ours(args, w, world, rank, local_rank):
     torch.cuda.synchronize()
     status = swa.swa_attn_get_status(stream)
     if status != 0:
-        raise RuntimeError(f"device status after warm-up: {swa.strerror(status)}")
+        raise RuntimeError(f"{w.name}: device status after warm-up: {swa.strerror(status)}")
     peak_above_inputs = torch.cuda.max_memory_allocated(dev) - base_mem - L2_FLUSH_BYTES
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -455,7 +543,7 @@ def run_ours(args, w, world, rank, local_rank):
     clock_info = clocks.stop() if clocks else None
     status = swa.swa_attn_get_status(stream)
     if status != 0:
-        raise RuntimeError(f"device status after timed steps: {swa.strerror(status)}")
+        raise RuntimeError(f"{w.name}: device status after timed steps: {swa.strerror(status)}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if w.fwd_only:
         fwd_ms, bwd_ms = sum(step_ms) / args.steps, 0.0
@@ -527,43 +615,56 @@ def run_ours(args, w, world, rank, local_rank):
         e2e_ms += es.elapsed_time(ee)
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = whole_job_tflops(world, useful, e2e_steps, e2e_ms)
+    status = swa.swa_attn_get_status(stream)
+    if status != 0:
+        raise RuntimeError(f"{w.name}: device status after the e2e steps: {swa.strerror(status)}")
 
     # roofline of the dominant kernel (or concurrent pair of kernels)
     kname, avg_ms = dominant_unit(kernels, bwd_ms, args.steps)
-    avg_s = avg_ms / 1e3
-    if kname in HBM_KERNELS:
-        if kname == "bwd_delta":
-            alg = B * Hq * Lq * (D * 4 + D * 2 + 4)
-        elif kname == "bwd_prep":  # q, k, v, dO: bf16 read + fp16 write; o (fp32) and lse read; stats written
-            alg = 4 * D * B * (2 * Hq * Lq + 2 * Hkv * L) + B * Hq * Lq * (4 * D + 4 + 8)
-        elif kname == "fwd_decode":  # the K and V rows in band (bf16) once per kv head, q in, o and lse out
-            alg = B * Hkv * _band_keys(w) * D * 2 * 2 + B * Hq * Lq * (D * 2 + D * 4 + 4)
-        else:  # convert_f16 (forward): bf16 read + fp16 write of v
-            alg = 4 * D * B * Hkv * L
-        achieved = alg / avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        def flops_per_pair(n):
-            if n == "bwd_dkdv_tc" and D == 256:
-                return 10  # dV-only pass (S^T, dV) + dK-only pass (S^T, dP^T, dK)
-            return KERNEL_FLOPS_PER_PAIR_D.get(n, 4)
+    roof = roofline_record(kname, avg_ms, w, peaks)
+    per_kernel = {n: {"launches": c, "avg_ms": round(ms / c, 4), "share": round(ms / sum(x[1] for x in
+                  kernels.values()), 4)} for n, (c, ms) in kernels.items()}
+    rec = {
+        "value": round(value, 3), "ms_per_step": round(total_ms / args.steps, 4),
+        "dtype": "f32" if kname.endswith("_simt") else "f16",
+        "config": dict({"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "L": L, "D": D, "window": W,
+                        "scale": round(w.scale, 6), "parallelism": f"replicas x{world} (one workload per GPU)",
+                        "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
+                       **_variant_keys(w)),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "copies": "pinned host memory; q, k, v in before the forward and dq, dk, dv out after the "
+                          "backward on the compute stream" + ("" if w.fwd_only else
+                          "; dO in beside the forward and o, lse out beside the backward on a copy stream")},
+        "gpu_launches": launches,
+        "clocks": clock_info,
+        "kernels": per_kernel,
+        "split": split_record(w, fwd_ms, bwd_ms, peaks),
+        "workspace_gb": {"fwd": round(fws_b / 1e9, 4), "bwd": round(bws_b / 1e9, 4),
+                         "peak_above_inputs": round(peak_above_inputs / 1e9, 4)},
+        "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+        "wall_s": round(wall, 3),
+    }
+    del q, k, v, dO, o, lse, dq, dk, dv, fws, bws, flush, outs_h, hq, hk, hv, hdO
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
-        per_pair = sum(flops_per_pair(n) for n in kname.split("+"))
-        alg = per_pair * D * w.pairs()
-        achieved = alg / avg_s / 1e12
-        if kname.endswith("_simt"):
-            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-            roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
-                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
-        else:
-            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "peak_source": f"{peaks['source']} bf16 dense (burst)"}
-    roof["kernel"] = kname
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    parts = [ncu_traffic(n, w.name, D) for n in kname.split("+")]
-    roof["traffic"] = None if None in parts else sum(parts)
 
-    line = None
+def run_ours(args, w, world, rank, local_rank, subs=()):
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    torch.cuda.set_device(local_rank)
+    peaks = load_peaks()
+    main_rec = measure_workload(args, w, world, rank, local_rank, dist, peaks)
+    sub_recs = [measure_workload(args, s, world, rank, local_rank, dist, peaks) for s in subs]
+
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -573,45 +674,20 @@ def run_ours(args, w, world, rank, local_rank):
                    "sample": f"fp64 oracle fwd+bwd (band mode), {groups} kv-head group(s) ({G} query heads each) "
                              f"x first {Ls} tokens ({_sample_q_rows(w, Ls)} query rows) of {w.name}, {secs:.1f} s; "
                              f"useful flops counted as on the GPU"}
-        # forward and backward separately: events on the caller's stream
-        # around each call (the backward's dK/dV and dQ passes overlap, so
-        # per-launch times do not add up to the backward's)
-        pk = peaks["bf16_tflops"]
-        split = {"fwd": {"ms": round(fwd_ms, 4), "tflops": round(w.fwd_flops() / (fwd_ms * 1e9), 2) if fwd_ms else None}}
-        split["fwd"]["pct_bf16_peak"] = round(100 * split["fwd"]["tflops"] / pk, 2) if fwd_ms else None
-        if not w.fwd_only and bwd_ms:
-            t10 = w.bwd_flops() / (bwd_ms * 1e9)
-            t8 = 8 * w.D * w.pairs() / (bwd_ms * 1e9)
-            split["bwd"] = {"ms": round(bwd_ms, 4), "tflops_10d": round(t10, 2), "pct_bf16_peak_10d": round(100 * t10 / pk, 2),
-                            "tflops_8d": round(t8, 2), "pct_bf16_peak_8d": round(100 * t8 / pk, 2)}
-        per_kernel = {n: {"launches": c, "avg_ms": round(ms / c, 4), "share": round(ms / sum(x[1] for x in
-                      kernels.values()), 4)} for n, (c, ms) in kernels.items()}
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if kname.endswith("_simt") else "f16",
+            "metric": METRIC, "value": main_rec["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": main_rec["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": main_rec["dtype"],
             "data": "synthetic (seeded N(0,1) inputs rounded to bf16)",
-            "config": dict({"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "L": L, "D": D, "window": W,
-                            "scale": round(w.scale, 6), "parallelism": f"replicas x{world} (one workload per GPU)",
-                            "l2": "flushed before every step (256 MiB write), flush outside the timed events"},
-                           **_variant_keys(w)),
-            "roofline": roof,
+            "config": main_rec["config"],
+            "roofline": main_rec["roofline"],
             "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
-                    "copies": "pinned host memory; q, k, v in before the forward and dq, dk, dv out after the "
-                              "backward on the compute stream" + ("" if w.fwd_only else
-                              "; dO in beside the forward and o, lse out beside the backward on a copy stream")},
-            "gpu_launches": launches,
-            "clocks": clock_info,
-            "kernels": per_kernel,
-            "split": split,
-            "workspace_gb": {"fwd": round(fws_b / 1e9, 4), "bwd": round(bws_b / 1e9, 4),
-                             "peak_above_inputs": round(peak_above_inputs / 1e9, 4)},
-            "pct_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
-            "wall_s": round(wall, 3),
         }
+        for key in ("e2e", "gpu_launches", "clocks", "kernels", "split", "workspace_gb", "pct_bf16_peak",
+                    "wall_s"):
+            line[key] = main_rec[key]
+        if sub_recs:
+            line["sub_workloads"] = sub_recs
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -633,7 +709,13 @@ def main():
     world, rank, local_rank = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
-    return run_ours(args, w, world, rank, local_rank)
+    subs = ()
+    if args.sub_workloads is None:
+        if args.workload == DEFAULT_WORKLOAD and args.seq_len <= 0:
+            subs = tuple(WORKLOADS[n] for n in DEFAULT_SUB_WORKLOADS)
+    elif args.sub_workloads:
+        subs = tuple(WORKLOADS[n] for n in args.sub_workloads.split(","))
+    return run_ours(args, w, world, rank, local_rank, subs)
 
 
 if __name__ == "__main__":

@@ -121,3 +121,39 @@ def test_cpu_baseline_adds_kv_groups_up_to_the_workload():
     a = bench._oracle_sample_inputs(w, Ls, 0)[0]
     b = bench._oracle_sample_inputs(w, Ls, 1)[0]
     assert not (a == b).all()
+
+
+def test_roofline_counts_useful_flops_of_the_backward_pair():
+    """The backward pair's frac is pairs x 10 D over (backward - prep) over the
+    peak; the flops the passes issue (14 D; 16 D at head dim 256) are a
+    separate field."""
+    import bench
+    from sliding_window_attention_gb300.inputs import WORKLOADS
+
+    peaks = dict(hbm_gbs=6789.0, bf16_tflops=1897.1, bf16_tflops_sustained=1690.9, sm_max_mhz=2070.0,
+                 source="measured")
+    w = WORKLOADS["global_l16384_d512"]
+    k = {"convert_f16": (2, 0.2), "fwd_tc": (2, 14.8), "bwd_prep": (2, 1.2),
+         "bwd_dkdv_tc": (2, 25.0), "bwd_dq_tc": (2, 40.0)}
+    name, ms = bench.dominant_unit(k, 22.39, 2)
+    assert name == "bwd_dkdv_tc+bwd_dq_tc" and abs(ms - 21.79) < 1e-9
+    roof = bench.roofline_record(name, ms, w, peaks)
+    want = w.pairs() * 10 * w.D / (21.79e-3) / 1e12 / 1897.1
+    assert abs(roof["frac"] - want) < 1e-4
+    assert roof["flops_per_pair_d"] == 10 and roof["issued_flops_per_pair_d"] == 14
+    assert roof["pairs"] == w.pairs()
+    s = WORKLOADS["sliding_l8192_d256_w1024"]
+    assert bench.roofline_record(name, 1.0, s, peaks)["issued_flops_per_pair_d"] == 16
+    f = bench.roofline_record("fwd_tc", 7.4, w, peaks)
+    assert f["flops_per_pair_d"] == 4 and abs(f["achieved"] - w.fwd_flops() / 7.4e-3 / 1e12) < 0.01
+
+
+def test_split_record_backward_at_10d():
+    import bench
+    from sliding_window_attention_gb300.inputs import WORKLOADS
+
+    peaks = dict(bf16_tflops=1897.1)
+    w = WORKLOADS["sliding_l8192_d256_w1024"]
+    s = bench.split_record(w, 0.375, 1.38, peaks)
+    assert abs(s["bwd"]["pct_bf16_peak_10d"] - 100 * w.bwd_flops() / 1.38e9 / 1897.1) < 0.01
+    assert abs(s["fwd"]["tflops"] - w.fwd_flops() / 0.375e9) < 0.01
