@@ -60,7 +60,9 @@ CONCURRENT_BWD = ("bwd_dkdv_tc", "bwd_dq_tc")
 # backward S, dP, dV, dQ, dK once each (10 D, the convention the metric uses)
 USEFUL_FWD_PER_PAIR_D = 4
 USEFUL_BWD_PER_PAIR_D = 10
-HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_prep", "fwd_decode"}
+HBM_KERNELS = {"bwd_delta", "convert_f16", "bwd_prep", "bwd_dscale", "fwd_decode"}
+# the backward's launches before its two concurrent passes
+BWD_PREP_KERNELS = ("bwd_dscale", "bwd_prep")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -98,7 +100,7 @@ def load_peaks():
 KERNEL_SOURCE = {
     "fwd_simt": "simt_kernels.cu", "bwd_delta": "simt_kernels.cu", "bwd_dkdv_simt": "simt_kernels.cu",
     "bwd_dq_simt": "simt_kernels.cu", "fwd_tc": "tc_fwd.cu", "convert_f16": "tc_fwd.cu",
-    "bwd_prep": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
+    "bwd_prep": "tc_bwd.cu", "bwd_dscale": "tc_bwd.cu", "bwd_dkdv_tc": "tc_bwd.cu", "bwd_dq_tc": "tc_bwd.cu",
 }
 # head dim 512: the tensor-core launches of the forward and backward come from the cluster kernels
 KERNEL_SOURCE_D512 = {"fwd_tc": "tc_fwd512.cu", "bwd_dkdv_tc": "tc_bwd512.cu", "bwd_dq_tc": "tc_bwd512.cu"}
@@ -121,11 +123,11 @@ def dominant_unit(kernels: dict, bwd_ms: float, steps: int):
     tensor-core backward runs its dK/dV and dQ passes side by side on two
     streams, so their per-launch spans overlap and each includes time spent
     waiting for SMs the other holds.  They count as one unit, timed from the
-    end of the backward prep to the join: `bwd_ms` minus the prep's average
-    launch time."""
+    end of the backward prep to the join: `bwd_ms` minus the average launch
+    times of the prep kernels (the max |dO| pass and the prep)."""
     group_ms = None
     if all(n in kernels for n in CONCURRENT_BWD) and "bwd_prep" in kernels and bwd_ms:
-        group_ms = bwd_ms - kernels["bwd_prep"][1] / kernels["bwd_prep"][0]
+        group_ms = bwd_ms - sum(kernels[n][1] / kernels[n][0] for n in BWD_PREP_KERNELS if n in kernels)
     singles = {n: v for n, v in kernels.items() if group_ms is None or n not in CONCURRENT_BWD}
     name, (launches, total) = max(singles.items(), key=lambda kv: kv[1][1])
     if group_ms is not None and group_ms * steps > total:
@@ -388,6 +390,8 @@ def roofline_record(kname: str, avg_ms: float, w, peaks: dict) -> dict:
             alg = B * Hq * Lq * (D * 4 + D * 2 + 4)
         elif kname == "bwd_prep":  # q, k, v, dO: bf16 read + fp16 write; o (fp32) and lse read; stats written
             alg = 4 * D * B * (2 * Hq * Lq + 2 * Hkv * L) + B * Hq * Lq * (4 * D + 4 + 8)
+        elif kname == "bwd_dscale":  # dO (bf16) read once
+            alg = 2 * D * B * Hq * Lq
         elif kname == "fwd_decode":  # the K and V rows in band (bf16) once per kv head, q in, o and lse out
             alg = B * Hkv * _band_keys(w) * D * 2 * 2 + B * Hq * Lq * (D * 2 + D * 4 + 4)
         else:  # convert_f16 (forward): bf16 read + fp16 write of v

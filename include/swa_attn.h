@@ -40,12 +40,37 @@
  *  - Tensor pointers must be 16-byte aligned; the workspace 256-byte aligned.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) of the current device, which must be an sm_103
- *    GPU.  Return values report argument and launch errors only; failures
- *    detected on the device (a bounded wait that ran out) are latched in a
- *    per-device status word read by swa_attn_get_status().
+ *    GPU.  Return values report argument and launch errors only: SWA_OK
+ *    says the work was enqueued, not that it succeeded.  Failures detected
+ *    on the device are latched in a per-device status word read by
+ *    swa_attn_get_status(): a bounded wait that ran out
+ *    (SWA_ERR_DEVICE_TIMEOUT), an input that overflowed an fp16 operand copy
+ *    (SWA_ERR_FP16_RANGE), an SM id outside the head-dim-512 scratch
+ *    (SWA_ERR_SCRATCH_LAYOUT).  The outputs of such a call are undefined
+ *    (they may hold inf or NaN); poll the status to detect it.
+ *  - Operand precision.  The tensor cores multiply fp16 copies of the bf16
+ *    inputs, with fp32 accumulation; S and dP stay fp32, P and
+ *    dS = P (dP - Delta) are rounded to fp16.  The copies are exact for
+ *    2^-14 <= |x| < 65504.  The forward copies v; the backward copies q, k,
+ *    v and dO.  A q, k or v entry of magnitude 65504 or more latches
+ *    SWA_ERR_FP16_RANGE; entries below 2^-14 lose precision (fp16
+ *    subnormals).  dO is different: the backward scales its copy by a power
+ *    of two s chosen from max |dO| (the scaled maximum lies in [4, 8)), keeps
+ *    Delta scaled the same way and multiplies dq, dk and dv by 1/s at the
+ *    end, all exactly.  So any finite dO works, tiny cotangents keep their
+ *    precision, and scaling dO by a power of two scales dq, dk and dv by the
+ *    same power bit for bit.
  *  - Supported head dims: 64, 128, 256, 512.  scale is any finite float.
+ *  - Head dim 512 hands tiles between the CTAs of a cluster through a static
+ *    L2 scratch of the library (36 MB per device) indexed by the receiving
+ *    CTA's SM id.  Its kernels fill an SM (one CTA per SM), and SM ids must be
+ *    below 192.  The first head-dim-512 call on a device checks both on the
+ *    host and returns SWA_ERR_SCRATCH_LAYOUT if the device does not meet
+ *    them.
  *  - Thread safety: calls on different streams may overlap if they use
- *    different workspaces.
+ *    different workspaces.  At head dim 512 this holds because no two CTAs
+ *    of these kernels share an SM, so no two share a scratch slot (checked as
+ *    above).  swa_attn_bwd_noalloc is the exception: see there.
  */
 #ifndef SWA_ATTN_H
 #define SWA_ATTN_H
@@ -75,6 +100,7 @@ typedef uint16_t swa_bf16; /* bf16 bit pattern */
 #define SWA_ERR_UNSUPPORTED_DEVICE -12 /* current device is not sm_103 */
 #define SWA_ERR_NOALLOC_LIMIT -13 /* B*Hq*L above swa_attn_bwd_noalloc's fixed scratch */
 #define SWA_ERR_FP16_RANGE -14    /* device: an input magnitude overflowed the fp16 operand copy */
+#define SWA_ERR_SCRATCH_LAYOUT -15 /* head dim 512: device cannot hold the per-SM tile scratch (see below) */
 
 /*
  * Workspace bytes swa_attn_fwd needs for this shape (may be 0; a NULL
@@ -172,11 +198,18 @@ int swa_attn_selftest_timeout(void* stream);
 const char* swa_attn_strerror(int code);
 
 /*
- * swa_attn_bwd_noalloc: the same backward as swa_attn_bwd, for callers that
+ * swa_attn_bwd_noalloc: the backward of swa_attn_bwd, for callers that
  * cannot allocate device memory or pass a workspace -- for example code whose
  * device memory all belongs to a host framework's allocator, or a plugin
  * entry point whose fixed signature has no workspace argument.  (The pages
  * have no counterpart; this is a deployment convenience of this library.)
+ *
+ * It computes the same quantities but runs fp32 kernels on the CUDA cores,
+ * not the tensor cores: no fp16 operand copies (any finite bf16 input is
+ * exact), and a throughput bound of about 80 TFLOP/s (152 SMs x 128 fp32
+ * lanes x 2 flop x 2.07 GHz) against roughly a petaflop for swa_attn_bwd on
+ * the same shapes.  Its results match swa_attn_bwd within the parity
+ * tolerance of this library, not bit for bit.
  *
  * It takes no workspace: the per-row term Delta lives in a fixed array built
  * into the library (8 MiB of fp32 on every GPU that loads the library, held

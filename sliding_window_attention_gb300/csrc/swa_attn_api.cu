@@ -83,6 +83,21 @@ int check_device() {
   return ok_cache[dev] == 1 ? SWA_OK : SWA_ERR_UNSUPPORTED_DEVICE;
 }
 
+// Head dim 512: whether the device can hold the cluster kernels' per-SM
+// tile scratch (checked once per device and direction).
+int check_scratch_layout(bool fwd) {
+  static int cache[2][kMaxDevices] = {};  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SWA_ERR_CUDA;
+  int& c = cache[fwd ? 0 : 1][dev];
+  if (c == 0) {
+    const int r = fwd ? swa::scratch_layout_fwd512() : swa::scratch_layout_bwd512();
+    if (r < 0) return SWA_ERR_CUDA;
+    c = r == 0 ? 1 : 2;
+  }
+  return c == 1 ? SWA_OK : SWA_ERR_SCRATCH_LAYOUT;
+}
+
 // Per-device side stream for the dK/dV pass of the backward, with the two
 // events that fork it from and join it back to the caller's stream.  The
 // dK/dV and dQ passes read the same inputs and write disjoint outputs; run
@@ -163,7 +178,8 @@ swa::Geom make_geom(int B, int Hq, int Hkv, int Lq, int L, int D, int window, in
 size_t bwd_delta_bytes(int B, int Hq, int L) { return round_up((size_t)B * Hq * L * sizeof(float), 256); }
 
 // Backward workspace layout on the tensor-core path:
-// [row stats: lse*log2e plane, Delta plane, B*Hq*Lpad floats each][q16][k16][v16][dO16].
+// [row stats: lse*log2e plane, Delta plane, B*Hq*Lpad floats each; the dO
+// scale tail][q16][k16][v16][dO16].
 struct BwdTcWs {
   size_t stats, q16, k16, v16, g16, total;
   int Lpad;
@@ -172,7 +188,7 @@ BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
   BwdTcWs w;
   w.Lpad = swa::bwd_stats_lpad(Lq);
   w.stats = 0;
-  w.q16 = round_up((size_t)B * Hq * w.Lpad * 8, 256);
+  w.q16 = round_up((size_t)B * Hq * w.Lpad * 8 + (size_t)swa::kDScaleTailFloats * 4, 256);
   w.k16 = w.q16 + round_up((size_t)B * Hq * Lq * D * 2, 256);
   w.v16 = w.k16 + round_up((size_t)B * Hkv * L * D * 2, 256);
   w.g16 = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
@@ -216,6 +232,8 @@ const char* swa_attn_strerror(int code) {
     case SWA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
     case SWA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
     case SWA_ERR_FP16_RANGE: return "an input magnitude overflowed the fp16 operand copy (|x| > 65504)";
+    case SWA_ERR_SCRATCH_LAYOUT:
+      return "head dim 512 needs at most one CTA per SM and SM ids below 192 for its per-SM tile scratch";
     case SWA_ERR_NOALLOC_LIMIT:
       return "B*Hq*L exceeds the fixed scratch of swa_attn_bwd_noalloc (2,097,152 rows); use swa_attn_bwd";
     default: return "unknown error code";
@@ -272,6 +290,7 @@ int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, flo
       return SWA_ERR_CUDA;
     return SWA_OK;
   }
+  if (D == 512 && (rc = check_scratch_layout(true)) != SWA_OK) return rc;
   const FwdWs w = fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
@@ -306,6 +325,7 @@ int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, con
   if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
+  if (D == 512 && (rc = check_scratch_layout(false)) != SWA_OK) return rc;
   const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_ptr_for_current_device(&rc);
@@ -317,6 +337,9 @@ int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, con
   uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + w.k16);
   uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
   uint16_t* g16 = reinterpret_cast<uint16_t*>(ws + w.g16);
+  // max |dO| first: the prep scales dO's fp16 copy by a power of two from it
+  if (launch("bwd_dscale", s, [&] { return swa::launch_bwd_dscale(g, w.Lpad, dO, stats, s); }) != cudaSuccess)
+    return SWA_ERR_CUDA;
   if (launch("bwd_prep", s, [&] {
         return swa::launch_bwd_prep(g, w.Lpad, q, k, v, dO, o, lse, q16, k16, v16, g16, stats, status, s);
       }) != cudaSuccess)

@@ -48,7 +48,15 @@ __host__ __device__ __forceinline__ int band_q_hi(const Geom& g, int j) {
 }
 
 // Device-side status codes latched into the per-device status word.
-enum : int { kStatusOk = 0, kStatusTimeout = -11, kStatusFp16Range = -14 };
+enum : int { kStatusOk = 0, kStatusTimeout = -11, kStatusFp16Range = -14, kStatusScratch = -15 };
+
+// The head-dim-512 kernels hand tiles between the CTAs of a cluster through
+// a static L2 scratch indexed by the SM id of the receiving CTA (192 SM ids).
+// That needs at most one CTA of these kernels per SM and SM ids below 192.
+// Each returns 0 when the current device meets that, 1 when it does not,
+// and -1 when the CUDA queries fail.
+int scratch_layout_fwd512();
+int scratch_layout_bwd512();
 
 // ---- SIMT kernels (fp32 arithmetic on bf16 inputs; any D in {64..512}) ----
 cudaError_t launch_fwd_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -97,10 +105,28 @@ cudaError_t make_tmap_f16_chunks(CUtensorMap* m, const void* ptr, int D, int L, 
 bool bwd_tc_supported(int D);
 // Padded row count of the backward's row-statistics array.
 int bwd_stats_lpad(int L);
-// The backward's preparation in one pass: fp16 copies of q, k, v and dO, and
-// the row statistics, two planes of B * Hq * Lpad floats:
-// stats[bh * Lpad + i] = lse_i * log2(e), stats[(B * Hq + bh) * Lpad + i] =
-// dO_i . o_i (zero for i >= Lq); dO is read once.
+
+// The fp16 copy of dO is scaled by a power of two s, chosen from max |dO| so
+// that the scaled maximum lies in [4, 8): tiny cotangents then keep their
+// precision in fp16 (and large ones cannot overflow it) in dO and in
+// dS = P (dP - Delta), which are linear in dO.  Delta is stored scaled by s
+// too, and the dq, dk and dv epilogues multiply by 1/s, exactly.
+// The backward's row-statistics block ends with a tail of
+// kDScaleTailFloats floats at stats + dscale_offset(): [0] = s, [1] = 1/s,
+// [2, 4) unused, [4, 4 + kAbsmaxBlocks) per-block maxima of |dO| (bf16 bit
+// patterns with the sign cleared, as uint32) written by the absmax pass.
+constexpr int kAbsmaxBlocks = 304;
+constexpr int kDScaleTailFloats = 4 + kAbsmaxBlocks;
+__host__ __device__ __forceinline__ size_t dscale_offset(const Geom& g, int Lpad) {
+  return 2 * (size_t)g.B * g.Hq * Lpad;
+}
+// max |dO| per block of the absmax pass into the stats tail (one launch).
+cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float* stats, cudaStream_t s);
+// The backward's preparation in one pass (after launch_bwd_dscale): fp16
+// copies of q, k, v and s * dO, and the row statistics, two planes of
+// B * Hq * Lpad floats: stats[bh * Lpad + i] = lse_i * log2(e),
+// stats[(B * Hq + bh) * Lpad + i] = s * (dO_i . o_i) (zero for i >= Lq); dO
+// is read once here.  Also writes s and 1/s into the stats tail.
 cudaError_t launch_bwd_prep(const Geom& g, int Lpad, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                             const uint16_t* dO, const float* o, const float* lse, uint16_t* q16, uint16_t* k16,
                             uint16_t* v16, uint16_t* g16, float* stats, int* status, cudaStream_t s);

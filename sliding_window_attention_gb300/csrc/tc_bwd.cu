@@ -47,19 +47,68 @@ constexpr int kSmemMax = 232448;         // dynamic shared memory per block on s
 
 // Backward preparation in one launch.  Segments 0-2 (blockIdx.y): fp16
 // copies of q, k and v, four 16-byte vectors in flight per thread.  Segment 3:
-// for every row of dO, its fp16 copy together with the row statistics, so dO
-// is read once for both; a warp per row, grid-stride.  The statistics are two
-// planes of BH * Lpad floats: per (bh = b*Hq + h, i < Lpad)
+// for every row of dO, its fp16 copy (scaled by the power of two s that the
+// absmax pass fixed, see dscale_offset) together with the row statistics, so
+// dO is read once for both; a warp per row, grid-stride.  The statistics are
+// two planes of BH * Lpad floats: per (bh = b*Hq + h, i < Lpad)
 // stats[bh Lpad + i] = lse_i * log2(e) and stats[BH Lpad + bh Lpad + i] =
-// Delta_i = dO_i . o_i; zero for padding rows i >= Lq.  Planar, so that one
-// 16-byte load gives four columns' values.  A finite input that overflows
-// fp16 latches kStatusFp16Range.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& overflow) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+// s * Delta_i = s * (dO_i . o_i); zero for padding rows i >= Lq.  Planar, so
+// that one 16-byte load gives four columns' values.  A finite input that
+// overflows fp16 latches kStatusFp16Range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& overflow, float mul = 1.f) {
+  const float lo = __uint_as_float(w << 16) * mul, hi = __uint_as_float(w & 0xffff0000u) * mul;
   const __half2 hv = __floats2half2_rn(lo, hi);
   const float2 back = __half22float2(hv);
   overflow |= (isinf(back.x) && !isinf(lo)) || (isinf(back.y) && !isinf(hi));
   return *reinterpret_cast<const uint32_t*>(&hv);
+}
+
+// The dO scale s = 2^k from the largest |dO| (as a bf16 bit pattern with the
+// sign cleared): the scaled maximum lands in [4, 8).  All-zero dO, or a
+// non-finite maximum, keeps s = 1; k is clamped to [-125, 125] so that s and
+// 1/s are normal floats.
+__device__ __forceinline__ int dscale_log2(uint32_t maxbits) {
+  if (maxbits == 0u || maxbits >= 0x7f80u) return 0;
+  const int e = (int)(maxbits >> 7) - 127;  // floor(log2 max) (bf16 subnormals give -127)
+  const int k = 2 - e;
+  return k < -125 ? -125 : (k > 125 ? 125 : k);
+}
+
+// Per-block maxima of |dO| (bit patterns of bf16 with the sign cleared,
+// which order like the magnitudes for every non-NaN value) into the stats
+// tail; kAbsmaxBlocks blocks, grid-stride over 16-byte vectors.
+__global__ void __launch_bounds__(256) bwd_dscale_kernel(const uint4* __restrict__ dO, long long n16,
+                                                          uint32_t* __restrict__ partial) {
+  uint32_t m = 0;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  auto upd = [&](const uint4 a) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t lo = w[u] & 0x7fffu, hi = (w[u] >> 16) & 0x7fffu;
+      m = max(m, max(lo, hi));
+    }
+  };
+  for (; idx + 3 * stride < n16; idx += 4 * stride) {
+    const uint4 a = __ldg(dO + idx), b = __ldg(dO + idx + stride);
+    const uint4 c = __ldg(dO + idx + 2 * stride), d = __ldg(dO + idx + 3 * stride);
+    upd(a);
+    upd(b);
+    upd(c);
+    upd(d);
+  }
+  for (; idx < n16; idx += stride) upd(__ldg(dO + idx));
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ uint32_t wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b = max(b, wmax[i]);
+    partial[blockIdx.x] = b;
+  }
 }
 
 struct PrepParams {
@@ -72,6 +121,7 @@ struct PrepParams {
   uint16_t* g16;
   const float* lse;
   float* stats;
+  float* dscale;  // stats tail: [0] = s, [1] = 1/s, [4 ...] absmax partials
   int* status;
 };
 
@@ -99,6 +149,24 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepParams p) {
                             bf16x2_to_f16x2(a.z, overflow), bf16x2_to_f16x2(a.w, overflow));
     }
   } else {
+    // the dO scale from the absmax pass's per-block maxima (every block of
+    // this segment reduces them; they are 1.2 KB and sit in L2)
+    __shared__ uint32_t smax[8];
+    const uint32_t* part = reinterpret_cast<const uint32_t*>(p.dscale + 4);
+    uint32_t m = 0;
+    for (int b = threadIdx.x; b < kAbsmaxBlocks; b += blockDim.x) m = max(m, part[b]);
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0) smax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = max(m, smax[i]);
+    const int kexp = dscale_log2(m);
+    const float sc = __int_as_float((127 + kexp) << 23), inv_sc = __int_as_float((127 - kexp) << 23);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      p.dscale[0] = sc;
+      p.dscale[1] = inv_sc;
+    }
     const int lane = threadIdx.x & 31;
     const long rows = (long)p.BH * p.Lpad;
     const long nwarps = (long)gridDim.x * (blockDim.x / 32);
@@ -115,10 +183,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepParams p) {
           acc = fmaf(ov.z, __uint_as_float(gv.y << 16), acc);
           acc = fmaf(ov.w, __uint_as_float(gv.y & 0xffff0000u), acc);
           *reinterpret_cast<uint2*>(p.g16 + off + d) =
-              make_uint2(bf16x2_to_f16x2(gv.x, overflow), bf16x2_to_f16x2(gv.y, overflow));
+              make_uint2(bf16x2_to_f16x2(gv.x, overflow, sc), bf16x2_to_f16x2(gv.y, overflow, sc));
         }
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+        acc *= sc;  // exact: a power of two
         l2 = p.lse[(size_t)bh * p.L + i] * kLog2e;
       }
       if (lane == 0) {
@@ -468,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = j < g.L;
       const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
       const uint32_t col = wg == 0 ? C::DK_COL : C::DV_COL;
-      const float mul = wg == 0 ? g.scale : 1.f;
+      const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
+      const float mul = wg == 0 ? g.scale * inv_s : inv_s;
       float* dst = (wg == 0 ? p.out0 : p.out1) + off;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -828,7 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // each warpgroup writes half of the accumulator's columns (dK scaled)
       const bool row_ok = j < g.L;
       const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
-      const float mul = DVM ? 1.f : g.scale;
+      const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
+      const float mul = DVM ? inv_s : g.scale * inv_s;
       float* dst = (DVM ? p.out1 : p.out0) + off;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -1078,6 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // each warpgroup writes half of the dQ columns
       float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
+      const float mul = g.scale * p.stats[dscale_offset(g, p.Lpad) + 1];  // scale / s
 #pragma unroll
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         uint32_t a[32];
@@ -1087,8 +1159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(row + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * g.scale, __uint_as_float(a[e + 1]) * g.scale,
-                            __uint_as_float(a[e + 2]) * g.scale, __uint_as_float(a[e + 3]) * g.scale);
+                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
         }
       }
     }
@@ -1336,6 +1408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool row_ok = i < g.Lq;
       float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
+      const float mul = g.scale * p.stats[dscale_offset(g, p.Lpad) + 1];  // scale / s
 #pragma unroll
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {  // each warpgroup writes half the columns
         uint32_t a[32];
@@ -1345,8 +1418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(row + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * g.scale, __uint_as_float(a[e + 1]) * g.scale,
-                            __uint_as_float(a[e + 2]) * g.scale, __uint_as_float(a[e + 3]) * g.scale);
+                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
         }
       }
     }
@@ -1456,6 +1529,13 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
 
 bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
+cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float* stats, cudaStream_t s) {
+  const long long n16 = (long long)g.B * g.Hq * g.Lq * g.D / 8;
+  uint32_t* partial = reinterpret_cast<uint32_t*>(stats + dscale_offset(g, Lpad) + 4);
+  bwd_dscale_kernel<<<kAbsmaxBlocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(dO), n16, partial);
+  return cudaGetLastError();
+}
+
 int bwd_stats_lpad(int L) { return (L + 127) / 128 * 128; }
 
 cudaError_t launch_bwd_prep(const Geom& g, int Lpad, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -1479,6 +1559,7 @@ cudaError_t launch_bwd_prep(const Geom& g, int Lpad, const uint16_t* q, const ui
   p.g16 = g16;
   p.lse = lse;
   p.stats = stats;
+  p.dscale = stats + dscale_offset(g, Lpad);
   p.status = status;
   // about 8 resident blocks of 256 threads per SM over the four segments
   const long rows = (long)p.BH * Lpad;

@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(kThr, 1)
     uint32_t sm;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
     bars->smid = sm < (uint32_t)kScratchSms ? (int)sm : -1;
+    // an SM id outside the scratch: a capacity error, latched before the
+    // abort it causes can latch a timeout
+    if (bars->smid < 0) atomicCAS(p.status, 0, kStatusScratch);
     for (int s = 0; s < NPP; ++s) bars->n_recv[s] = bars->n_loaded[s] = 0;
     bars->n_issued = 0;
     fence_mbar_init();
@@ -737,12 +740,13 @@ __global__ void __launch_bounds__(kThr, 1)
       const bool row_ok = row < LX;
       float* dst;
       float mul;
+      const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
       if (DIR == kDirKV) {
         dst = (role == kRoleAccP) ? p.out1 : p.out0;
-        mul = (role == kRoleAccP) ? 1.f : g.scale;
+        mul = (role == kRoleAccP) ? inv_s : g.scale * inv_s;
       } else {
         dst = p.out0;
-        mul = g.scale;
+        mul = g.scale * inv_s;
       }
       dst += ((size_t)head * LX + (row_ok ? row : 0)) * DH;
 #pragma unroll 1
@@ -856,6 +860,18 @@ cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16,
 }
 
 }  // namespace
+
+int scratch_layout_bwd512() {
+  int n0 = 0, n1 = 0, nsm = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev))
+    return -1;
+  if (cudaFuncSetAttribute(bwd512_kernel<kDirKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) ||
+      cudaFuncSetAttribute(bwd512_kernel<kDirQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, bwd512_kernel<kDirKV>, kThr, SMEM) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, bwd512_kernel<kDirQ>, kThr, SMEM))
+    return -1;
+  return (n0 == 1 && n1 == 1 && nsm <= kScratchSms) ? 0 : 1;
+}
 
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                    const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,

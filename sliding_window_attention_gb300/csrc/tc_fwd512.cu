@@ -237,6 +237,9 @@ __global__ void __launch_bounds__(kThr, 1)
     uint32_t sm;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
     bars->smid = sm < (uint32_t)kScratchSms ? (int)sm : -1;
+    // an SM id outside the scratch: a capacity error, latched before the
+    // abort it causes can latch a timeout
+    if (bars->smid < 0) atomicCAS(p.status, 0, kStatusScratch);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -647,6 +650,16 @@ __global__ void __launch_bounds__(kThr, 1)
 }
 
 }  // namespace
+
+int scratch_layout_fwd512() {
+  int n = 0, nsm = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev))
+    return -1;
+  if (cudaFuncSetAttribute(fwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd512_kernel, kThr, SMEM))
+    return -1;
+  return (n == 1 && nsm <= kScratchSms) ? 0 : 1;
+}
 
 cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s) {

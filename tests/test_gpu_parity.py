@@ -95,6 +95,18 @@ def full_run(request):
     return w, (q, k, v, dO), got
 
 
+def _log_errors(workload, what, errs):
+    """Append the measured errors of one parity check to the file named by
+    SWA_PARITY_LOG (one JSON object per line), when that is set."""
+    import json
+    import os
+
+    path = os.environ.get("SWA_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"workload": workload, "check": what, **errs}) + "\n")
+
+
 def test_full_workload_sampled(oracle_mod, full_run):
     w, (q, k, v, dO), got = full_run
     rng = np.random.default_rng(w.seed)
@@ -103,16 +115,45 @@ def test_full_workload_sampled(oracle_mod, full_run):
         assert torch.isfinite(got[name]).all(), name
     heads = sorted({0, w.Hq - 1, G, w.Hq // 2})
     rows = _sample_rows(w.q_rows, w.window, rng)
+    worst = {}
+
+    def keep(name, ma_rf):
+        ma, rf = ma_rf if isinstance(ma_rf, tuple) else (ma_rf, 0.0)
+        a, r = worst.get(name, (0.0, 0.0))
+        worst[name] = (max(a, ma), max(r, rf))
+
     for h in heads:
         r = oracle_mod.rows(q, k, v, dO, w.window, w.scale, 0, h, rows, band_only=True, causal=w.causal)
-        assert_lse_close(got["lse"][0, h, rows].numpy(), r["lse"])
-        assert_close(f"o[h={h}]", got["o"][0, h, rows].numpy(), r["o"])
-        assert_close(f"dq[h={h}]", got["dq"][0, h, rows].numpy(), r["dq"])
+        keep("lse", assert_lse_close(got["lse"][0, h, rows].numpy(), r["lse"]))
+        keep("o", assert_close(f"o[h={h}]", got["o"][0, h, rows].numpy(), r["o"]))
+        keep("dq", assert_close(f"dq[h={h}]", got["dq"][0, h, rows].numpy(), r["dq"]))
     keys = _sample_keys(w, rng)
     for kvh in sorted({0, w.Hkv - 1}):
         r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True, causal=w.causal)
-        assert_close(f"dk[kvh={kvh}]", got["dk"][0, kvh, keys].numpy(), r["dk"])
-        assert_close(f"dv[kvh={kvh}]", got["dv"][0, kvh, keys].numpy(), r["dv"])
+        keep("dk", assert_close(f"dk[kvh={kvh}]", got["dk"][0, kvh, keys].numpy(), r["dk"]))
+        keep("dv", assert_close(f"dv[kvh={kvh}]", got["dv"][0, kvh, keys].numpy(), r["dv"]))
+    _log_errors(w.name, "sampled rows and keys",
+                {n: {"max_abs": a, "rel_fro": f} for n, (a, f) in sorted(worst.items())})
+
+
+@pytest.mark.parametrize("name", ["causal_gqa_l8192_d128",
+                                  pytest.param("global_l16384_d512", marks=pytest.mark.slow)])
+def test_full_workload_first_key_tile(oracle_mod, name):
+    """Keys 0..127 of a causal workload accumulate dK and dV over every query
+    row of every head of their group: the longest sums the dK/dV pass forms
+    (at 16,384 tokens and 8 heads per kv head, 1,024 steps of 128 rows).
+    Every element of that key tile against the oracle.  The oracle's cost is
+    one row pass per query row, the same as for key 0 alone."""
+    w = WORKLOADS[name]
+    q, k, v, dO = workload_inputs(w)
+    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale, causal=w.causal)
+    keys = list(range(128))
+    errs = {}
+    for kvh in sorted({0, w.Hkv - 1}) if w.D <= 128 else (0,):
+        r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True, causal=w.causal)
+        errs[f"dk[kvh={kvh}]"] = assert_close(f"dk[kvh={kvh}]", got["dk"][0, kvh, keys].numpy(), r["dk"])
+        errs[f"dv[kvh={kvh}]"] = assert_close(f"dv[kvh={kvh}]", got["dv"][0, kvh, keys].numpy(), r["dv"])
+    _log_errors(name, "keys 0..127", {n: {"max_abs": a, "rel_fro": f} for n, (a, f) in errs.items()})
 
 
 def test_full_workload_properties(full_run):
@@ -396,3 +437,120 @@ def test_decode_then_backward_matches_oracle(oracle_mod):
     got = gpu_fwd_bwd(q, k, v, dO, W, 0.1)
     for n in ("o", "dq", "dk", "dv"):
         assert_close(n, got[n].numpy(), ref[n])
+
+
+# ---------------------------------------------------------------------------
+# fp16 operand range: the backward scales its fp16 copy of dO by a power of
+# two from max |dO|; q, k and v outside fp16's range latch a status code
+
+
+@pytest.mark.parametrize("D,L,W", [(128, 300, 0), (256, 333, 100), (512, 300, 0)])
+def test_do_power_of_two_scaling_bitwise_and_against_oracle(oracle_mod, D, L, W):
+    """The backward is linear in dO.  With dO scaled by 2^-20 (cotangents far
+    below fp16's normal range) and by 2^12, dq, dk and dv are the unscaled
+    results times the same power of two, bit for bit, and 2^20 times the
+    tiny-cotangent result matches the oracle on the unscaled dO."""
+    q, k, v, dO = make_inputs(1, 4, 2, L, D, seed=31 + D)
+    scale = 1.0 / math.sqrt(D)
+    base = gpu_fwd_bwd(q, k, v, dO, W, scale)
+    ref = oracle_mod.backward(q, k, v, dO, W, scale, band_only=True)
+    for e in (-20, 12):
+        dOs = (dO.float() * 2.0 ** e).to(torch.bfloat16)  # exact: a power of two
+        assert torch.equal(dOs.float(), dO.float() * 2.0 ** e)
+        got = gpu_fwd_bwd(q, k, v, dOs, W, scale)
+        for n in ("dq", "dk", "dv"):
+            assert torch.equal(got[n], base[n] * 2.0 ** e), (e, n)
+        if e == -20:
+            for n in ("dq", "dk", "dv"):
+                assert_close(f"2^20 {n}", got[n].double().numpy() * 2.0 ** 20, ref[n])
+
+
+@pytest.mark.parametrize("D", [64, 512])
+def test_large_do_entry_needs_no_status(oracle_mod, D):
+    """A dO entry of 1e5 (above fp16's largest finite value) is scaled into
+    range with the rest of dO: no status, finite results, and the oracle's
+    gradients within the parity bar relative to their size."""
+    import sliding_window_attention_gb300 as swa
+
+    L, W = 260, 0
+    q, k, v, dO = make_inputs(1, 2, 1, L, D, seed=33 + D)
+    dO[0, 1, 100, 7] = 1e5
+    scale = 1.0 / math.sqrt(D)
+    got = gpu_fwd_bwd(q, k, v, dO, W, scale)  # asserts a clean status
+    ref = oracle_mod.backward(q, k, v, dO, W, scale, band_only=True)
+    for n in ("dq", "dk", "dv"):
+        assert torch.isfinite(got[n]).all(), n
+        big = float(np.abs(ref[n]).max())
+        assert_close(n, got[n].numpy() / big, ref[n] / big)
+    assert swa.swa_attn_get_status() == 0
+
+
+@pytest.mark.parametrize("D", [128, 512])
+def test_fp16_range_status_then_clean_call(oracle_mod, D):
+    """A bf16 v entry of 1e5 overflows the forward's fp16 copy of v, and a q
+    entry of 1e5 the backward's copy of q: each call still returns SWA_OK
+    (the check runs on the device), the status word reads
+    SWA_ERR_FP16_RANGE (-14), reading it clears it, and a following call on
+    clean inputs matches the oracle."""
+    import sliding_window_attention_gb300 as swa
+
+    B, Hq, Hkv, L, W = 1, 2, 1, 256, 0
+    scale = 1.0 / math.sqrt(D)
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=35 + D)
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, dO))
+    assert swa.swa_attn_get_status() == 0
+    v_bad = vd.clone()
+    v_bad[0, 0, 17, 3] = 1e5
+    swa.forward(qd, kd, v_bad, W, scale)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == -14
+    assert swa.swa_attn_get_status() == 0
+    assert "fp16" in swa.strerror(-14)
+    o, lse = swa.forward(qd, kd, vd, W, scale)
+    q_bad = qd.clone()
+    q_bad[0, 1, 40, 5] = -1e5
+    swa.backward(q_bad, kd, vd, o, lse, gd, W, scale)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == -14
+    assert swa.swa_attn_get_status() == 0
+    got = gpu_fwd_bwd(q, k, v, dO, W, scale)  # asserts a clean status
+    ref = oracle_mod.backward(q, k, v, dO, W, scale, band_only=True)
+    assert_lse_close(got["lse"].numpy(), ref["lse"])
+    for n in ("o", "dq", "dk", "dv"):
+        assert_close(n, got[n].numpy(), ref[n])
+
+
+# ---------------------------------------------------------------------------
+# head dim 512: two backwards overlapping on two streams (the tile scratch is
+# per SM, and no two CTAs of these kernels share an SM)
+
+
+def test_d512_backwards_overlap_on_two_streams():
+    import sliding_window_attention_gb300 as swa
+
+    B, Hq, Hkv, L, D, W = 1, 8, 2, 2048, 512, 0
+    scale = 1.0 / math.sqrt(D)
+    runs = []
+    for seed in (51, 52):
+        q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, L, D, seed=seed))
+        o, lse = swa.forward(q, k, v, W, scale)
+        ref = swa.backward(q, k, v, o, lse, dO, W, scale)
+        torch.cuda.synchronize()
+        outs = [torch.full_like(t, float("nan")) for t in ref]
+        ws = torch.empty(swa.bwd_workspace_bytes(B, Hq, Hkv, L, D, W), dtype=torch.uint8, device="cuda")
+        runs.append(((q, k, v, o, lse, dO), ref, outs, ws))
+    assert swa.swa_attn_get_status() == 0
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for rep in range(3):
+        for (ins, _, outs, ws), s in zip(runs, streams):
+            with torch.cuda.stream(s):
+                swa.swa_attn_bwd(*ins, *outs, W, scale, ws, s)
+    for s in streams:
+        torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    for _, ref, outs, _ in runs:
+        for a, b, n in zip(outs, ref, ("dq", "dk", "dv")):
+            assert torch.equal(a, b), n

@@ -133,12 +133,12 @@ def test_roofline_counts_useful_flops_of_the_backward_pair():
     peaks = dict(hbm_gbs=6789.0, bf16_tflops=1897.1, bf16_tflops_sustained=1690.9, sm_max_mhz=2070.0,
                  source="measured")
     w = WORKLOADS["global_l16384_d512"]
-    k = {"convert_f16": (2, 0.2), "fwd_tc": (2, 14.8), "bwd_prep": (2, 1.2),
+    k = {"convert_f16": (2, 0.2), "fwd_tc": (2, 14.8), "bwd_dscale": (2, 0.16), "bwd_prep": (2, 1.2),
          "bwd_dkdv_tc": (2, 25.0), "bwd_dq_tc": (2, 40.0)}
     name, ms = bench.dominant_unit(k, 22.39, 2)
-    assert name == "bwd_dkdv_tc+bwd_dq_tc" and abs(ms - 21.79) < 1e-9
+    assert name == "bwd_dkdv_tc+bwd_dq_tc" and abs(ms - 21.71) < 1e-9
     roof = bench.roofline_record(name, ms, w, peaks)
-    want = w.pairs() * 10 * w.D / (21.79e-3) / 1e12 / 1897.1
+    want = w.pairs() * 10 * w.D / (21.71e-3) / 1e12 / 1897.1
     assert abs(roof["frac"] - want) < 1e-4
     assert roof["flops_per_pair_d"] == 10 and roof["issued_flops_per_pair_d"] == 14
     assert roof["pairs"] == w.pairs()

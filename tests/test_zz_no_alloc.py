@@ -6,8 +6,9 @@ signature with no workspace argument.  swa_attn_bwd_noalloc serves them by
 keeping its scratch in a fixed array built into the library.  These tests
 call it through the C ABI and check that its output matches swa_attn_bwd's
 (the existing entry point, which takes a caller workspace) within the parity
-tolerance used everywhere else, on two calls in a row -- the second call sees
-the scratch exactly as the first call left it.
+tolerance used everywhere else, and against the fp64 oracle, on two calls in
+a row with different cotangents -- the second call finds the scratch as the
+first call left it.
 
 This file is named so that pytest collects it last.
 """
@@ -42,19 +43,42 @@ def _run_noalloc(lib, q, k, v, o, lse, dO, window, scale):
 
 @pytest.mark.parametrize("B,Hq,Hkv,L,D,window", [(1, 4, 2, 333, 64, 50), (2, 8, 2, 1029, 128, 0)])
 def test_noalloc_matches_workspace_backward_twice(B, Hq, Hkv, L, D, window):
+    """Two calls in a row with different cotangents (dO, then 3 dO): the
+    second call's Delta differs from what the first left in the scratch, and
+    its result must still match swa_attn_bwd on its own inputs."""
     import sliding_window_attention_gb300 as swa
 
     lib = swa.load()
     scale = D ** -0.5
     q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, L, D, seed=4242 + L))
     o, lse = swa.forward(q, k, v, window, scale)
-    ref = swa.backward(q, k, v, o, lse, dO, window, scale)
-    torch.cuda.synchronize()
-    for call in range(2):
-        got = _run_noalloc(lib, q, k, v, o, lse, dO, window, scale)
-        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-            assert torch.isfinite(g).all(), (call, name)
-            assert_close(f"{name} (call {call})", g.cpu().numpy(), r.cpu().numpy())
+    for call, g in enumerate((dO, (dO.float() * 3).to(torch.bfloat16))):
+        ref = swa.backward(q, k, v, o, lse, g, window, scale)
+        torch.cuda.synchronize()
+        got = _run_noalloc(lib, q, k, v, o, lse, g, window, scale)
+        for name, a, r in zip(("dq", "dk", "dv"), got, ref):
+            assert torch.isfinite(a).all(), (call, name)
+            assert_close(f"{name} (call {call})", a.cpu().numpy(), r.cpu().numpy())
+    assert swa.swa_attn_get_status() == 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,D,window", [(1, 4, 2, 300, 256, 64), (1, 2, 1, 257, 512, 0)])
+def test_noalloc_matches_oracle_at_wide_heads(oracle_mod, B, Hq, Hkv, L, D, window):
+    """Head dims 256 and 512 (the widest per-thread accumulators of its
+    kernels) against the fp64 oracle, two calls in a row with different
+    cotangents."""
+    import sliding_window_attention_gb300 as swa
+
+    lib = swa.load()
+    scale = D ** -0.5
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=4343 + L)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    o, lse = swa.forward(qd, kd, vd, window, scale)
+    for call, g in enumerate((dO, (dO.float() * -0.5).to(torch.bfloat16))):
+        ref = oracle_mod.backward(q, k, v, g, window, scale, band_only=True)
+        got = _run_noalloc(lib, qd, kd, vd, o, lse, g.cuda(), window, scale)
+        for name, a in zip(("dq", "dk", "dv"), got):
+            assert_close(f"{name} (call {call})", a.cpu().numpy(), ref[name])
     assert swa.swa_attn_get_status() == 0
 
 
