@@ -14,6 +14,12 @@ holding bf16 bit patterns, or float64): q and dO shaped [B, Hq, Lq, D], k and
 v [B, Hkv, Lk, D] with Lq <= Lk.  The queries are the last Lq positions of
 the key sequence (Lq = Lk is self-attention).  ``causal=False`` selects the
 non-causal band |i + Lk - Lq - j| < window (no mask at all for window 0).
+
+``prefix=(P, Rc)`` selects the shared-prefix mask over one sequence
+[prompt (P rows); chosen response (Rc rows); rejected response (the rest)]:
+causal self-attention in which rejected rows do not see chosen keys and the
+window is measured on logical positions (the rejected response restarts at
+position P).  It needs Lq = Lk and causal.
 """
 from __future__ import annotations
 
@@ -58,8 +64,14 @@ def _load():
             lib.swa_oracle_bwd_ex.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, I, P, P, P, P, P, P, P]
             lib.swa_oracle_rows_ex.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, I, L, L, P, L, P, P, P, P]
             lib.swa_oracle_key_rows_ex.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, I, L, L, P, L, P, P]
+            # shared-prefix plan: (B, Hq, Hkv, L, D, W, P, Rc) instead of (B, Hq, Hkv, Lq, Lk, D, W, causal)
+            lib.swa_oracle_fwd_px.argtypes = [P, P, P, I, L, L, L, L, L, L, L, L, D, I, P, P]
+            lib.swa_oracle_bwd_px.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, L, D, I, P, P, P, P, P, P, P]
+            lib.swa_oracle_rows_px.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, L, D, I, L, L, P, L, P, P, P, P]
+            lib.swa_oracle_key_rows_px.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, L, D, I, L, L, P, L, P, P]
             for f in (lib.swa_oracle_fwd_ex, lib.swa_oracle_bwd_ex, lib.swa_oracle_rows_ex,
-                      lib.swa_oracle_key_rows_ex):
+                      lib.swa_oracle_key_rows_ex, lib.swa_oracle_fwd_px, lib.swa_oracle_bwd_px,
+                      lib.swa_oracle_rows_px, lib.swa_oracle_key_rows_px):
                 f.restype = ctypes.c_int
             lib.swa_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -111,30 +123,49 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def forward(q, k, v, window: int, scale: float, band_only: bool = False, causal: bool = True):
+def _plan(prefix, causal, Lq, Lk):
+    """(P, Rc) of a shared-prefix plan, checked, or None."""
+    if prefix is None:
+        return None
+    P, Rc = (int(x) for x in prefix)
+    if not causal or Lq != Lk or P < 0 or Rc < 0 or P + Rc > Lk:
+        raise ValueError("a shared-prefix plan needs causal self-attention and 0 <= P, Rc with P + Rc <= L")
+    return P, Rc
+
+
+def forward(q, k, v, window: int, scale: float, band_only: bool = False, causal: bool = True, prefix=None):
     """Return (o [B,Hq,Lq,D], lse [B,Hq,Lq]) in fp64."""
     arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v)
+    plan = _plan(prefix, causal, Lq, Lk)
     o = np.empty((B, Hq, Lq, D), np.float64)
     lse = np.empty((B, Hq, Lq), np.float64)
-    rc = _load().swa_oracle_fwd_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
-                                   float(scale), int(band_only), _ptr(o), _ptr(lse))
+    if plan:
+        rc = _load().swa_oracle_fwd_px(*map(_ptr, arrs), f64, B, Hq, Hkv, Lk, D, int(window), *plan, float(scale),
+                                       int(band_only), _ptr(o), _ptr(lse))
+    else:
+        rc = _load().swa_oracle_fwd_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
+                                       int(bool(causal)), float(scale), int(band_only), _ptr(o), _ptr(lse))
     if rc:
         raise RuntimeError(f"swa_oracle_fwd failed ({rc})")
     return o, lse
 
 
-def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False, causal: bool = True):
+def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False, causal: bool = True, prefix=None):
     """Return dict with o, lse, delta, dq, dk, dv (fp64) and delta_gap."""
     arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
+    plan = _plan(prefix, causal, Lq, Lk)
     out = dict(
         o=np.empty((B, Hq, Lq, D)), lse=np.empty((B, Hq, Lq)), delta=np.empty((B, Hq, Lq)),
         dq=np.empty((B, Hq, Lq, D)), dk=np.empty((B, Hkv, Lk, D)), dv=np.empty((B, Hkv, Lk, D)),
     )
     gap = ctypes.c_double(0.0)
-    rc = _load().swa_oracle_bwd_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)),
-                                   float(scale), int(band_only),
-                                   *(_ptr(out[n]) for n in ("o", "lse", "delta", "dq", "dk", "dv")),
-                                   ctypes.byref(gap))
+    outs = [_ptr(out[n]) for n in ("o", "lse", "delta", "dq", "dk", "dv")]
+    if plan:
+        rc = _load().swa_oracle_bwd_px(*map(_ptr, arrs), f64, B, Hq, Hkv, Lk, D, int(window), *plan, float(scale),
+                                       int(band_only), *outs, ctypes.byref(gap))
+    else:
+        rc = _load().swa_oracle_bwd_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
+                                       int(bool(causal)), float(scale), int(band_only), *outs, ctypes.byref(gap))
     if rc:
         raise RuntimeError(f"swa_oracle_bwd failed ({rc})")
     out["delta_gap"] = gap.value
@@ -142,17 +173,21 @@ def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False, ca
 
 
 def rows(q, k, v, dO, window: int, scale: float, b: int, h: int, row_ids, band_only: bool = False,
-         causal: bool = True):
+         causal: bool = True, prefix=None):
     """Selected query rows of head (b, h): dict o [n,D], lse [n], and with dO also delta [n], dq [n,D]."""
     arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
+    plan = _plan(prefix, causal, Lq, Lk)
     ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
     n = ids.size
     out = dict(o=np.empty((n, D)), lse=np.empty(n), delta=np.empty(n), dq=np.empty((n, D)))
     dptr = _ptr(arrs[3]) if dO is not None else None
-    rc = _load().swa_oracle_rows_ex(_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), dptr, f64, B, Hq, Hkv, Lq, Lk,
-                                    D, int(window), int(bool(causal)), float(scale), int(band_only), int(b), int(h),
-                                    _ptr(ids), n, _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["delta"]),
-                                    _ptr(out["dq"]))
+    qkv = (_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), dptr, f64)
+    tail = (float(scale), int(band_only), int(b), int(h), _ptr(ids), n, _ptr(out["o"]), _ptr(out["lse"]),
+            _ptr(out["delta"]), _ptr(out["dq"]))
+    if plan:
+        rc = _load().swa_oracle_rows_px(*qkv, B, Hq, Hkv, Lk, D, int(window), *plan, *tail)
+    else:
+        rc = _load().swa_oracle_rows_ex(*qkv, B, Hq, Hkv, Lq, Lk, D, int(window), int(bool(causal)), *tail)
     if rc:
         raise RuntimeError(f"swa_oracle_rows failed ({rc})")
     if dO is None:
@@ -161,15 +196,19 @@ def rows(q, k, v, dO, window: int, scale: float, b: int, h: int, row_ids, band_o
 
 
 def key_rows(q, k, v, dO, window: int, scale: float, b: int, kvh: int, key_ids, band_only: bool = False,
-             causal: bool = True):
+             causal: bool = True, prefix=None):
     """Selected key rows of kv head (b, kvh): dict dk [n,D], dv [n,D]."""
     arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
+    plan = _plan(prefix, causal, Lq, Lk)
     ids = np.ascontiguousarray(np.asarray(key_ids, dtype=np.int64))
     n = ids.size
     out = dict(dk=np.empty((n, D)), dv=np.empty((n, D)))
-    rc = _load().swa_oracle_key_rows_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
-                                        int(bool(causal)), float(scale), int(band_only), int(b), int(kvh),
-                                        _ptr(ids), n, _ptr(out["dk"]), _ptr(out["dv"]))
+    tail = (float(scale), int(band_only), int(b), int(kvh), _ptr(ids), n, _ptr(out["dk"]), _ptr(out["dv"]))
+    if plan:
+        rc = _load().swa_oracle_key_rows_px(*map(_ptr, arrs), f64, B, Hq, Hkv, Lk, D, int(window), *plan, *tail)
+    else:
+        rc = _load().swa_oracle_key_rows_ex(*map(_ptr, arrs), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
+                                            int(bool(causal)), *tail)
     if rc:
         raise RuntimeError(f"swa_oracle_key_rows failed ({rc})")
     return out

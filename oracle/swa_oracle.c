@@ -27,6 +27,21 @@
  *   dk_j  = scale * sum_{h in group} sum_i dS_ij q_i
  *   dv_j  = sum_{h in group} sum_i P_ij dO_i
  *
+ * Shared prompt prefix ("Training -- design (ORPO, flash-CCE head, prefix
+ * sharing, segmented backward)", section 5.4 "Shared prompt-prefix
+ * forward"): one self-attention pass over [prompt (P rows); chosen response
+ * (Rc rows); rejected response (Rr rows)], L = P + Rc + Rr, with the
+ * block-sparse mask "causal AND NOT rejected->chosen" and the window measured
+ * on logical positions, where each response starts at logical position P
+ * (block-wise positions).  Written out, with lp(x) = x - Rc for x >= P + Rc
+ * (a rejected row) and lp(x) = x otherwise:
+ *
+ *   key j visible to query i  iff  j <= i
+ *                              and not (i >= P + Rc and P <= j < P + Rc)
+ *                              and (W == 0 or lp(i) - lp(j) < W)
+ *
+ * The *_px entry points take (P, Rc); they are causal self-attention.
+ *
  * Passages followed:
  *  - Mask rule: "Lab 028 lab detail: Off NVIDIA, you fix the platform
  *    yourself", "Plan for the build" step 4 (P is zeroed where
@@ -81,7 +96,15 @@ typedef struct {
     double scale;
     int band_only;
     long off;                 /* Lk - Lq: position of query 0 among the keys */
+    int plan;                 /* 1: shared-prefix mask over [prompt; chosen; rejected] */
+    long P, Rc;               /* prompt and chosen-response lengths (plan only) */
 } ctx_t;
+
+/* Logical position of sequence position x under the shared-prefix plan: the
+ * rejected response restarts at logical position P, right after the prompt. */
+static long logical_pos(const ctx_t* c, long x) {
+    return (c->plan && x >= c->P + c->Rc) ? x - c->Rc : x;
+}
 
 static double bf16_bits_to_f64(uint16_t bits) {
     uint32_t u = ((uint32_t)bits) << 16;
@@ -108,6 +131,12 @@ static long krow_off(const ctx_t* c, long b, long kvh, long j) {
 /* Key j is visible to query i (at position a = i + off). */
 static int in_band(const ctx_t* c, long i, long j) {
     const long a = i + c->off;
+    if (c->plan) {
+        if (j > i) return 0;                                          /* causal */
+        if (i >= c->P + c->Rc && j >= c->P && j < c->P + c->Rc) return 0;  /* rejected -> chosen */
+        if (c->W > 0 && logical_pos(c, i) - logical_pos(c, j) >= c->W) return 0;
+        return 1;
+    }
     if (c->causal) {
         if (j > a) return 0;
         if (c->W > 0 && a - j >= c->W) return 0;
@@ -123,6 +152,15 @@ static void key_range(const ctx_t* c, long i, long* j0, long* j1) {
     *j1 = c->Lk - 1;
     if (!c->band_only) return;
     const long a = i + c->off;
+    if (c->plan) {
+        /* the smallest visible key has logical position lp(i) - W + 1 (a
+           prompt key, or a key of i's own segment); keys in between that
+           the mask drops are exact zeros */
+        const long lo = logical_pos(c, i) - c->W + 1;
+        if (c->W > 0 && lo > 0) *j0 = lo;
+        *j1 = i;
+        return;
+    }
     if (c->W > 0 && a - c->W + 1 > 0) *j0 = a - c->W + 1;
     if (c->causal) *j1 = a;
     else if (c->W > 0 && a + c->W - 1 < c->Lk - 1) *j1 = a + c->W - 1;
@@ -133,6 +171,13 @@ static void query_range(const ctx_t* c, long j, long* i0, long* i1) {
     *i0 = 0;
     *i1 = c->Lq - 1;
     if (!c->band_only) return;
+    if (c->plan) {
+        /* rows i >= j with lp(i) <= lp(j) + W - 1; a rejected row sits Rc
+           positions after its logical position */
+        *i0 = j;
+        if (c->W > 0 && logical_pos(c, j) + c->W - 1 + c->Rc < *i1) *i1 = logical_pos(c, j) + c->W - 1 + c->Rc;
+        return;
+    }
     /* positions a that see key j: a >= j (causal) or a >= j - W + 1
        (non-causal window), and a <= j + W - 1 (any window) */
     long alo = c->causal ? j : (c->W > 0 ? j - c->W + 1 : c->off);
@@ -251,8 +296,19 @@ static int check_shape(long B, long Hq, long Hkv, long Lq, long Lk, long D, long
 static ctx_t make_ctx(const void* q, const void* k, const void* v, const void* dO, int is_f64, long B,
                       long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal, double scale,
                       int band_only) {
-    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal ? 1 : 0, scale, band_only, Lk - Lq};
+    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal ? 1 : 0, scale, band_only, Lk - Lq, 0, 0, 0};
     return c;
+}
+
+/* The shared-prefix plan, for self-attention over L = Lq = Lk rows.  A plan
+ * needs 0 <= P and 0 <= Rc with P + Rc <= L. */
+static int set_plan(ctx_t* c, long P, long Rc) {
+    if (P < 0 || Rc < 0 || P + Rc > c->Lk || c->Lq != c->Lk) return -1;
+    c->plan = 1;
+    c->P = P;
+    c->Rc = Rc;
+    c->causal = 1;
+    return 0;
 }
 
 int swa_oracle_num_threads(void) {
@@ -264,11 +320,9 @@ int swa_oracle_num_threads(void) {
 }
 
 /* Forward over every row.  o: [B,Hq,Lq,D], lse: [B,Hq,Lq]. */
-int swa_oracle_fwd_ex(const void* q, const void* k, const void* v, int is_f64, long B, long Hq,
-                      long Hkv, long Lq, long Lk, long D, long W, int causal, double scale,
-                      int band_only, double* o, double* lse) {
-    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
-    ctx_t c = make_ctx(q, k, v, NULL, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+static int fwd_impl(const ctx_t* cp, double* o, double* lse) {
+    const ctx_t c = *cp;
+    const long B = c.B, Hq = c.Hq, Lq = c.Lq, Lk = c.Lk, D = c.D;
     const long rows = B * Hq * Lq;
     int err = 0;
 #pragma omp parallel
@@ -294,12 +348,10 @@ int swa_oracle_fwd_ex(const void* q, const void* k, const void* v, int is_f64, l
  * dk, dv: [B,Hkv,Lk,D]; lse, delta: [B,Hq,Lq].  *delta_gap receives
  * max_i |sum_j P dP - dO_i . o_i|.
  */
-int swa_oracle_bwd_ex(const void* q, const void* k, const void* v, const void* dO, int is_f64,
-                      long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
-                      double scale, int band_only, double* o, double* lse, double* delta,
-                      double* dq, double* dk, double* dv, double* delta_gap) {
-    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
-    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+static int bwd_impl(const ctx_t* cp, double* o, double* lse, double* delta, double* dq, double* dk,
+                    double* dv, double* delta_gap) {
+    const ctx_t c = *cp;
+    const long B = c.B, Hq = c.Hq, Hkv = c.Hkv, Lq = c.Lq, Lk = c.Lk, D = c.D;
     const long rows = B * Hq * Lq;
     const long keys = B * Hkv * Lk;
     double gap = 0.0;
@@ -341,15 +393,14 @@ int swa_oracle_bwd_ex(const void* q, const void* k, const void* v, const void* d
  * Selected query rows of one head: o, dq [n, D]; lse, delta [n].
  * dO may be NULL (forward only; delta and dq are then left untouched).
  */
-int swa_oracle_rows_ex(const void* q, const void* k, const void* v, const void* dO, int is_f64,
-                       long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
-                       double scale, int band_only, long b, long h, const long* rows, long n,
-                       double* o, double* lse, double* delta, double* dq) {
-    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
-    if (b < 0 || b >= B || h < 0 || h >= Hq) return -1;
+static int rows_impl(const ctx_t* cp, long b, long h, const long* rows, long n, double* o, double* lse,
+                     double* delta, double* dq) {
+    const ctx_t c = *cp;
+    const void* dO = c.dO;
+    const long D = c.D, Lk = c.Lk;
+    if (b < 0 || b >= c.B || h < 0 || h >= c.Hq) return -1;
     for (long t = 0; t < n; ++t)
-        if (rows[t] < 0 || rows[t] >= Lq) return -1;
-    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+        if (rows[t] < 0 || rows[t] >= c.Lq) return -1;
     int err = 0;
 #pragma omp parallel
     {
@@ -377,26 +428,26 @@ int swa_oracle_rows_ex(const void* q, const void* k, const void* v, const void* 
  * for every query row, of every head in the group, that can see one of the
  * selected keys (lse_i and Delta_i), then the column pass for each key.
  */
-int swa_oracle_key_rows_ex(const void* q, const void* k, const void* v, const void* dO,
-                           int is_f64, long B, long Hq, long Hkv, long Lq, long Lk, long D, long W,
-                           int causal, double scale, int band_only, long b, long kvh,
-                           const long* keys, long n, double* dk, double* dv) {
-    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
-    if (b < 0 || b >= B || kvh < 0 || kvh >= Hkv || n < 1 || !dO) return -1;
-    long jmin = Lk, jmax = -1;
-    for (long t = 0; t < n; ++t) {
+static int key_rows_impl(const ctx_t* cp, long b, long kvh, const long* keys, long n, double* dk,
+                         double* dv) {
+    const ctx_t c = *cp;
+    const long B = c.B, Hq = c.Hq, Hkv = c.Hkv, Lq = c.Lq, Lk = c.Lk, D = c.D;
+    if (b < 0 || b >= B || kvh < 0 || kvh >= Hkv || n < 1 || !c.dO) return -1;
+    for (long t = 0; t < n; ++t)
         if (keys[t] < 0 || keys[t] >= Lk) return -1;
-        if (keys[t] < jmin) jmin = keys[t];
-        if (keys[t] > jmax) jmax = keys[t];
-    }
-    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
     const long G = Hq / Hkv;
     /* query rows that can see any selected key (the others add exact zeros) */
-    long ilo, ihi, unused0, unused1;
+    long ilo = Lq, ihi = -1;
     ctx_t cb = c;
     cb.band_only = 1;
-    query_range(&cb, jmin, &ilo, &unused0);
-    query_range(&cb, jmax, &unused1, &ihi);
+    for (long t = 0; t < n; ++t) {
+        long a, z;
+        query_range(&cb, keys[t], &a, &z);
+        if (a <= z) {
+            if (a < ilo) ilo = a;
+            if (z > ihi) ihi = z;
+        }
+    }
     if (ihi < ilo) { ilo = 0; ihi = -1; }
     const long nr = ihi - ilo + 1;
     /* lse / delta laid out as full [B, Hq, Lq] arrays so col_pass can index them */
@@ -435,6 +486,97 @@ int swa_oracle_key_rows_ex(const void* q, const void* k, const void* v, const vo
     free(delta);
     free(obuf);
     return err;
+}
+
+/* Forward over every row.  o: [B,Hq,Lq,D], lse: [B,Hq,Lq]. */
+int swa_oracle_fwd_ex(const void* q, const void* k, const void* v, int is_f64, long B, long Hq,
+                      long Hkv, long Lq, long Lk, long D, long W, int causal, double scale,
+                      int band_only, double* o, double* lse) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
+    const ctx_t c = make_ctx(q, k, v, NULL, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+    return fwd_impl(&c, o, lse);
+}
+
+/*
+ * Forward and backward over every row and key.  Outputs o, dq: [B,Hq,Lq,D];
+ * dk, dv: [B,Hkv,Lk,D]; lse, delta: [B,Hq,Lq].  *delta_gap receives
+ * max_i |sum_j P dP - dO_i . o_i|.
+ */
+int swa_oracle_bwd_ex(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                      long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
+                      double scale, int band_only, double* o, double* lse, double* delta,
+                      double* dq, double* dk, double* dv, double* delta_gap) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
+    const ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+    return bwd_impl(&c, o, lse, delta, dq, dk, dv, delta_gap);
+}
+
+/*
+ * Selected query rows of one head: o, dq [n, D]; lse, delta [n].
+ * dO may be NULL (forward only; delta and dq are then left untouched).
+ */
+int swa_oracle_rows_ex(const void* q, const void* k, const void* v, const void* dO, int is_f64,
+                       long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
+                       double scale, int band_only, long b, long h, const long* rows, long n,
+                       double* o, double* lse, double* delta, double* dq) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
+    const ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+    return rows_impl(&c, b, h, rows, n, o, lse, delta, dq);
+}
+
+/*
+ * Selected key rows of one kv head: dk, dv [n, D].  First runs the row pass
+ * for every query row, of every head in the group, that can see one of the
+ * selected keys (lse_i and Delta_i), then the column pass for each key.
+ */
+int swa_oracle_key_rows_ex(const void* q, const void* k, const void* v, const void* dO,
+                           int is_f64, long B, long Hq, long Hkv, long Lq, long Lk, long D, long W,
+                           int causal, double scale, int band_only, long b, long kvh,
+                           const long* keys, long n, double* dk, double* dv) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W)) return -1;
+    const ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, band_only);
+    return key_rows_impl(&c, b, kvh, keys, n, dk, dv);
+}
+
+/* The same four over [prompt (P); chosen (Rc); rejected (L - P - Rc)] with
+ * the shared-prefix mask (causal self-attention, Lq = Lk = L). */
+int swa_oracle_fwd_px(const void* q, const void* k, const void* v, int is_f64, long B, long Hq, long Hkv,
+                      long L, long D, long W, long P, long Rc, double scale, int band_only, double* o,
+                      double* lse) {
+    if (check_shape(B, Hq, Hkv, L, L, D, W)) return -1;
+    ctx_t c = make_ctx(q, k, v, NULL, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only);
+    if (set_plan(&c, P, Rc)) return -1;
+    return fwd_impl(&c, o, lse);
+}
+
+int swa_oracle_bwd_px(const void* q, const void* k, const void* v, const void* dO, int is_f64, long B,
+                      long Hq, long Hkv, long L, long D, long W, long P, long Rc, double scale,
+                      int band_only, double* o, double* lse, double* delta, double* dq, double* dk,
+                      double* dv, double* delta_gap) {
+    if (check_shape(B, Hq, Hkv, L, L, D, W)) return -1;
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only);
+    if (set_plan(&c, P, Rc)) return -1;
+    return bwd_impl(&c, o, lse, delta, dq, dk, dv, delta_gap);
+}
+
+int swa_oracle_rows_px(const void* q, const void* k, const void* v, const void* dO, int is_f64, long B,
+                       long Hq, long Hkv, long L, long D, long W, long P, long Rc, double scale,
+                       int band_only, long b, long h, const long* rows, long n, double* o, double* lse,
+                       double* delta, double* dq) {
+    if (check_shape(B, Hq, Hkv, L, L, D, W)) return -1;
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only);
+    if (set_plan(&c, P, Rc)) return -1;
+    return rows_impl(&c, b, h, rows, n, o, lse, delta, dq);
+}
+
+int swa_oracle_key_rows_px(const void* q, const void* k, const void* v, const void* dO, int is_f64, long B,
+                           long Hq, long Hkv, long L, long D, long W, long P, long Rc, double scale,
+                           int band_only, long b, long kvh, const long* keys, long n, double* dk,
+                           double* dv) {
+    if (check_shape(B, Hq, Hkv, L, L, D, W)) return -1;
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only);
+    if (set_plan(&c, P, Rc)) return -1;
+    return key_rows_impl(&c, b, kvh, keys, n, dk, dv);
 }
 
 /* Self-attention (Lq = Lk = L), causal: the entry points the tests started with. */

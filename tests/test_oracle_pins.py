@@ -474,3 +474,160 @@ def test_suffix_band_mode_bitwise_equals_full(oracle_mod, causal):
     b = oracle_mod.backward(q, k, v, dO, 9, 0.3, band_only=True, causal=causal)
     for n in ("o", "lse", "dq", "dk", "dv"):
         np.testing.assert_array_equal(a[n], b[n], err_msg=n)
+
+
+# ---------------------------------------------------------------------------
+# shared prompt prefix: one pass over [prompt; chosen; rejected] with the
+# block-sparse mask "causal AND NOT rejected->chosen" and a window on logical
+# positions ("Training -- design (ORPO, flash-CCE head, prefix sharing,
+# segmented backward)", section 5.4 "Shared prompt-prefix forward")
+
+
+def test_prefix_mask_matches_hand_table(oracle_mod):
+    """With V = identity (D = L), o_i is row i of P; its zero pattern is the mask."""
+    lines = [l.split() for l in open(os.path.join(GOLD, "prefix_mask_p3_c2_r3.txt")) if l.strip() and not l.startswith("#")]
+    P, Rc = int(lines[0][1]), int(lines[1][1])
+    tables, cur = {}, None
+    for t in lines[2:]:
+        if t[0] == "window":
+            cur = int(t[1])
+            tables[cur] = []
+        else:
+            tables[cur].append([int(x) for x in t])
+    L = len(tables[0])
+    q = _rand64((1, 1, L, L), 141)
+    k = _rand64((1, 1, L, L), 142)
+    v = torch.eye(L, dtype=torch.float64).view(1, 1, L, L).contiguous()
+    for window, mask in tables.items():
+        for band in (False, True):
+            o, _ = oracle_mod.forward(q, k, v, window, 0.3, band_only=band, prefix=(P, Rc))
+            np.testing.assert_array_equal((o[0, 0] > 0).astype(int), np.array(mask), err_msg=f"window={window}")
+            np.testing.assert_allclose(o[0, 0].sum(-1), 1.0, atol=1e-14)
+
+
+def _two_forward(oracle_mod, q, k, v, dO, window, scale, P, Rc):
+    """The pages' reference for the shared prefix: two plain causal passes,
+    [prompt; chosen] and [prompt; rejected] (the rejected response placed
+    right after the prompt, where its logical positions put it), assembled
+    into the outputs of the single pass.  In the second pass the prompt rows'
+    cotangents are zero, so its dK / dV holds only the rejected rows' share
+    (the prompt rows are counted once, in the first pass)."""
+    L = q.shape[2]
+    chosen = slice(0, P + Rc)
+    rej = list(range(P)) + list(range(P + Rc, L))
+    a = oracle_mod.backward(q[:, :, chosen], k[:, :, chosen], v[:, :, chosen], dO[:, :, chosen], window, scale,
+                            band_only=True)
+    dOb = dO[:, :, rej].clone()
+    dOb[:, :, :P] = 0
+    b = oracle_mod.backward(q[:, :, rej].contiguous(), k[:, :, rej].contiguous(), v[:, :, rej].contiguous(),
+                            dOb.contiguous(), window, scale, band_only=True)
+    out = {}
+    for n in ("o", "lse", "dq"):
+        full = np.concatenate([a[n], b[n][:, :, P:]], axis=2)
+        out[n] = full
+    for n in ("dk", "dv"):
+        x = np.zeros((q.shape[0], k.shape[1], L, q.shape[3]))
+        x[:, :, :P + Rc] = a[n]
+        x[:, :, :P] += b[n][:, :, :P]
+        x[:, :, P + Rc:] = b[n][:, :, P:]
+        out[n] = x
+    return out
+
+
+@pytest.mark.parametrize("P,Rc,Rr,window,G", [(5, 4, 6, 0, 1), (9, 3, 7, 4, 2), (6, 7, 5, 3, 2), (0, 4, 5, 3, 1),
+                                              (12, 2, 9, 6, 1), (7, 5, 4, 100, 2)])
+def test_prefix_equals_two_forward_construction(oracle_mod, P, Rc, Rr, window, G):
+    """One pass with the shared-prefix mask gives what two plain passes give
+    ([prompt; chosen] and [prompt; rejected]), the prompt's key gradients
+    being the sum over both; the pages report this construction exact for
+    the forward."""
+    B, Hkv, D = 1, 2, 8
+    L = P + Rc + Rr
+    q, k, v, dO = make_inputs(B, G * Hkv, Hkv, L, D, seed=150 + L + window)
+    scale = 1.0 / math.sqrt(D)
+    r = oracle_mod.backward(q, k, v, dO, window, scale, band_only=True, prefix=(P, Rc))
+    ref = _two_forward(oracle_mod, q, k, v, dO, window, scale, P, Rc)
+    for n in ("o", "lse", "dq"):
+        np.testing.assert_array_equal(r[n], ref[n], err_msg=n)
+    for n in ("dk", "dv"):
+        np.testing.assert_allclose(r[n], ref[n], rtol=1e-12, atol=1e-14, err_msg=n)
+
+
+@pytest.mark.parametrize("window", [0, 4])
+def test_prefix_finite_differences(oracle_mod, window):
+    B, Hq, Hkv, D, P, Rc, Rr = 1, 2, 1, 5, 4, 3, 5
+    L = P + Rc + Rr
+    q = _rand64((B, Hq, L, D), 161)
+    k = _rand64((B, Hkv, L, D), 162)
+    v = _rand64((B, Hkv, L, D), 163)
+    dO = _rand64((B, Hq, L, D), 164)
+    scale = 0.5
+    r = oracle_mod.backward(q, k, v, dO, window, scale, prefix=(P, Rc))
+
+    def loss(qq, kk, vv):
+        o, _ = oracle_mod.forward(qq, kk, vv, window, scale, prefix=(P, Rc))
+        return float((o * dO.numpy()).sum())
+
+    rng = np.random.default_rng(17)
+    eps = 1e-6
+    for name, grad in (("q", r["dq"]), ("k", r["dk"]), ("v", r["dv"])):
+        base = {"q": q, "k": k, "v": v}
+        t = base[name]
+        for _ in range(12):
+            idx = tuple(int(rng.integers(0, s)) for s in t.shape)
+            plus = t.clone()
+            plus[idx] += eps
+            minus = t.clone()
+            minus[idx] -= eps
+            args_p = dict(base, **{name: plus})
+            args_m = dict(base, **{name: minus})
+            fd = (loss(args_p["q"], args_p["k"], args_p["v"]) - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_prefix_degenerate_plans_are_plain_causal(oracle_mod, window):
+    """No chosen response (Rc = 0), or no rejected one (P + Rc = L): the mask
+    is the plain causal window, bit for bit."""
+    q, k, v, dO = make_inputs(1, 4, 2, 23, 8, seed=171)
+    plain = oracle_mod.backward(q, k, v, dO, window, 0.3)
+    for plan in ((9, 0), (0, 0), (15, 8), (23, 0)):
+        r = oracle_mod.backward(q, k, v, dO, window, 0.3, prefix=plan)
+        for n in ("o", "lse", "dq", "dk", "dv"):
+            np.testing.assert_array_equal(r[n], plain[n], err_msg=(plan, n))
+
+
+@pytest.mark.parametrize("window", [0, 6])
+def test_prefix_band_mode_and_sampled_rows_keys(oracle_mod, window):
+    """Band mode is bitwise equal to full mode under the plan, and the row /
+    key samplers reproduce the full result (key samples that mix prompt,
+    chosen and rejected keys need every row that sees any of them)."""
+    P, Rc, Rr = 11, 6, 9
+    L = P + Rc + Rr
+    q, k, v, dO = make_inputs(1, 4, 2, L, 8, seed=181)
+    a = oracle_mod.backward(q, k, v, dO, window, 0.3, band_only=False, prefix=(P, Rc))
+    b = oracle_mod.backward(q, k, v, dO, window, 0.3, band_only=True, prefix=(P, Rc))
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[n], b[n], err_msg=n)
+    rows = [0, P - 1, P, P + Rc - 1, P + Rc, L - 1]
+    r = oracle_mod.rows(q, k, v, dO, window, 0.3, 0, 3, rows, band_only=True, prefix=(P, Rc))
+    np.testing.assert_array_equal(r["o"], a["o"][0, 3, rows])
+    np.testing.assert_array_equal(r["dq"], a["dq"][0, 3, rows])
+    for keys in ([0, P - 1, P + Rc + 2], [P + Rc, L - 1, 2], [P, P + 1]):
+        kr = oracle_mod.key_rows(q, k, v, dO, window, 0.3, 0, 1, keys, band_only=True, prefix=(P, Rc))
+        np.testing.assert_allclose(kr["dk"], a["dk"][0, 1, keys], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(kr["dv"], a["dv"][0, 1, keys], rtol=1e-13, atol=1e-15)
+
+
+def test_prefix_chosen_keys_get_no_gradient_from_rejected_rows(oracle_mod):
+    """dO nonzero only on the rejected rows: the chosen keys' dK and dV are
+    exactly zero (no rejected row sees them), and so is dq on every other
+    row."""
+    P, Rc, Rr = 6, 5, 7
+    L = P + Rc + Rr
+    q, k, v, dO = make_inputs(1, 2, 1, L, 8, seed=191)
+    dO[:, :, :P + Rc] = 0
+    r = oracle_mod.backward(q, k, v, dO, 0, 0.3, prefix=(P, Rc))
+    assert np.all(r["dk"][:, :, P:P + Rc] == 0.0) and np.all(r["dv"][:, :, P:P + Rc] == 0.0)
+    assert np.all(r["dq"][:, :, :P + Rc] == 0.0)
+    assert np.any(r["dk"][:, :, :P] != 0.0) and np.any(r["dv"][:, :, P + Rc:] != 0.0)
