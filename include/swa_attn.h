@@ -101,6 +101,7 @@ typedef uint16_t swa_bf16; /* bf16 bit pattern */
 #define SWA_ERR_NOALLOC_LIMIT -13 /* B*Hq*L above swa_attn_bwd_noalloc's fixed scratch */
 #define SWA_ERR_FP16_RANGE -14    /* device: an input magnitude overflowed the fp16 operand copy */
 #define SWA_ERR_SCRATCH_LAYOUT -15 /* head dim 512: device cannot hold the per-SM tile scratch (see below) */
+#define SWA_ERR_BAD_PLAN -16      /* shared-prefix plan: prompt_len or chosen_len out of range */
 
 /*
  * Workspace bytes swa_attn_fwd needs for this shape (may be 0; a NULL
@@ -138,6 +139,43 @@ int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, con
                     const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv,
                     int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Shared prompt prefix ("Training -- design (ORPO, flash-CCE head, prefix
+ * sharing, segmented backward)", section 5.4 "Shared prompt-prefix
+ * forward"): one causal self-attention pass over a sequence of L rows laid
+ * out as [prompt (prompt_len rows); chosen response (chosen_len rows);
+ * rejected response (the remaining rows)], in place of two passes over
+ * [prompt; chosen] and [prompt; rejected].  The mask is "causal AND NOT
+ * rejected -> chosen", and the window is measured on logical positions:
+ * each response starts right after the prompt, so with lp(x) = x - chosen_len
+ * for rejected rows and lp(x) = x otherwise,
+ *
+ *   key j visible to query i  iff  j <= i,
+ *                                  not (i rejected and j chosen),
+ *                                  and (window == 0 or lp(i) - lp(j) < window).
+ *
+ * A rejected row therefore sees two key intervals (part of the prompt and
+ * its own response), and the kernels visit only the key tiles those
+ * intervals meet.  The prompt rows are computed once; their keys' dk and dv
+ * sum the contributions of both responses.  Tensors, dtypes, streams,
+ * status word and errors are as for swa_attn_fwd / swa_attn_bwd (which are
+ * these calls with chosen_len = 0).  prompt_len >= 0, chosen_len >= 0 and
+ * prompt_len + chosen_len <= L, else SWA_ERR_BAD_PLAN; a plan without a
+ * chosen or without a rejected response is the plain causal window.  The
+ * workspace sizes come from the *_prefix queries (pure host functions).
+ */
+size_t swa_attn_fwd_workspace_bytes_prefix(int B, int Hq, int Hkv, int L, int D, int window, int prompt_len,
+                                            int chosen_len);
+size_t swa_attn_bwd_workspace_bytes_prefix(int B, int Hq, int Hkv, int L, int D, int window, int prompt_len,
+                                            int chosen_len);
+int swa_attn_fwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B,
+                        int Hq, int Hkv, int L, int D, int window, int prompt_len, int chosen_len, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream);
+int swa_attn_bwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
+                        const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int L, int D,
+                        int window, int prompt_len, int chosen_len, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /*
  * Forward.  Reads q [B,Hq,L,D], k and v [B,Hkv,L,D] (bf16); writes

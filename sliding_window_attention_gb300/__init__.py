@@ -10,17 +10,21 @@ from ._native import (  # noqa: F401
     backward,
     bwd_workspace_bytes,
     bwd_workspace_bytes_ex,
+    bwd_workspace_bytes_prefix,
     forward,
     fwd_workspace_bytes,
     fwd_workspace_bytes_ex,
+    fwd_workspace_bytes_prefix,
     load,
     profile_begin,
     profile_end,
     strerror,
     swa_attn_bwd,
     swa_attn_bwd_ex,
+    swa_attn_bwd_prefix,
     swa_attn_fwd,
     swa_attn_fwd_ex,
+    swa_attn_fwd_prefix,
     swa_attn_get_status,
     swa_attn_selftest_timeout,
 )
@@ -29,4 +33,5 @@ __all__ = [
     "SwaError", "backward", "bwd_workspace_bytes", "bwd_workspace_bytes_ex", "forward", "fwd_workspace_bytes",
     "fwd_workspace_bytes_ex", "load", "profile_begin", "profile_end", "strerror", "swa_attn_bwd", "swa_attn_bwd_ex",
     "swa_attn_fwd", "swa_attn_fwd_ex", "swa_attn_get_status", "swa_attn_selftest_timeout",
+    "fwd_workspace_bytes_prefix", "bwd_workspace_bytes_prefix", "swa_attn_fwd_prefix", "swa_attn_bwd_prefix",
 ]

@@ -30,6 +30,10 @@ EXPORTED = (
     "swa_attn_bwd_workspace_bytes_ex",
     "swa_attn_fwd_ex",
     "swa_attn_bwd_ex",
+    "swa_attn_fwd_workspace_bytes_prefix",
+    "swa_attn_bwd_workspace_bytes_prefix",
+    "swa_attn_fwd_prefix",
+    "swa_attn_bwd_prefix",
 )
 
 _lock = threading.Lock()
@@ -87,6 +91,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.swa_attn_fwd_ex.restype = I
         lib.swa_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, P] + shape_ex + [F, P, Z, P]
         lib.swa_attn_bwd_ex.restype = I
+        shape_px = [I, I, I, I, I, I, I, I]  # B, Hq, Hkv, L, D, window, prompt_len, chosen_len
+        lib.swa_attn_fwd_workspace_bytes_prefix.argtypes = shape_px
+        lib.swa_attn_fwd_workspace_bytes_prefix.restype = Z
+        lib.swa_attn_bwd_workspace_bytes_prefix.argtypes = shape_px
+        lib.swa_attn_bwd_workspace_bytes_prefix.restype = Z
+        lib.swa_attn_fwd_prefix.argtypes = [P, P, P, P, P] + shape_px + [F, P, Z, P]
+        lib.swa_attn_fwd_prefix.restype = I
+        lib.swa_attn_bwd_prefix.argtypes = [P, P, P, P, P, P, P, P, P] + shape_px + [F, P, Z, P]
+        lib.swa_attn_bwd_prefix.restype = I
         _lib = lib
         return lib
 
@@ -179,6 +192,39 @@ def swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, window: int, causal: bool, 
         raise SwaError(rc, "swa_attn_bwd_ex")
 
 
+def fwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, window, prompt_len, chosen_len) -> int:
+    return int(load().swa_attn_fwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, window, prompt_len, chosen_len))
+
+
+def bwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, window, prompt_len, chosen_len) -> int:
+    return int(load().swa_attn_bwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, window, prompt_len, chosen_len))
+
+
+def swa_attn_fwd_prefix(q, k, v, o, lse, window: int, prompt_len: int, chosen_len: int, scale: float,
+                        workspace=None, stream=None) -> None:
+    """Forward over [prompt; chosen; rejected] with the shared-prefix mask
+    (see include/swa_attn.h); q, k, v bf16 [B,H,L,D]; o, lse fp32 outputs."""
+    B, Hq, Hkv, L, D = _dims(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_fwd_prefix(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, D, int(window),
+                                    int(prompt_len), int(chosen_len), float(scale), _ptr(workspace), nbytes,
+                                    _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_fwd_prefix")
+
+
+def swa_attn_bwd_prefix(q, k, v, o, lse, dO, dq, dk, dv, window: int, prompt_len: int, chosen_len: int,
+                        scale: float, workspace=None, stream=None) -> None:
+    """Backward of swa_attn_fwd_prefix; dq, dk, dv are caller-allocated fp32 outputs."""
+    B, Hq, Hkv, L, D = _dims(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_bwd_prefix(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), B, Hq, Hkv, L, D, int(window), int(prompt_len), int(chosen_len),
+                                    float(scale), _ptr(workspace), nbytes, _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_bwd_prefix")
+
+
 def swa_attn_fwd(q, k, v, o, lse, window: int, scale: float, workspace=None, stream=None) -> None:
     """Forward through the C ABI.  q,k,v: bf16 CUDA tensors [B,H,L,D]; o fp32
     [B,Hq,L,D] and lse fp32 [B,Hq,L] are caller-allocated outputs."""
@@ -233,15 +279,20 @@ def _workspace(nbytes, device):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True):
+def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True, prefix=None):
     """Return (o fp32, lse fp32) for bf16 CUDA tensors q [B,Hq,Lq,D], k/v
-    [B,Hkv,Lk,D] (Lq <= Lk; Lq = Lk and causal is self-attention)."""
+    [B,Hkv,Lk,D] (Lq <= Lk; Lq = Lk and causal is self-attention).
+    prefix=(prompt_len, chosen_len): the shared-prefix mask over one
+    [prompt; chosen; rejected] sequence (self-attention, causal)."""
     import torch
 
     B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
     o = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
-    if Lq == Lk and causal:
+    if prefix is not None:
+        ws = _workspace(fwd_workspace_bytes_prefix(B, Hq, Hkv, Lk, D, window, *prefix), q.device)
+        swa_attn_fwd_prefix(q, k, v, o, lse, window, prefix[0], prefix[1], scale, ws, stream)
+    elif Lq == Lk and causal:
         ws = _workspace(fwd_workspace_bytes(B, Hq, Hkv, Lk, D, window), q.device)
         swa_attn_fwd(q, k, v, o, lse, window, scale, ws, stream)
     else:
@@ -250,7 +301,7 @@ def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True
     return o, lse
 
 
-def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None, causal: bool = True):
+def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None, causal: bool = True, prefix=None):
     """Return (dq, dk, dv) fp32."""
     import torch
 
@@ -258,7 +309,10 @@ def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None, causal
     dq = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=q.device)
     dk = torch.empty((B, Hkv, Lk, D), dtype=torch.float32, device=q.device)
     dv = torch.empty((B, Hkv, Lk, D), dtype=torch.float32, device=q.device)
-    if Lq == Lk and causal:
+    if prefix is not None:
+        ws = _workspace(bwd_workspace_bytes_prefix(B, Hq, Hkv, Lk, D, window, *prefix), q.device)
+        swa_attn_bwd_prefix(q, k, v, o, lse, dO, dq, dk, dv, window, prefix[0], prefix[1], scale, ws, stream)
+    elif Lq == Lk and causal:
         ws = _workspace(bwd_workspace_bytes(B, Hq, Hkv, Lk, D, window), q.device)
         swa_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, window, scale, ws, stream)
     else:

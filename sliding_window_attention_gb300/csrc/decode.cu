@@ -490,7 +490,7 @@ cudaError_t decode_d(const Geom& g, const uint16_t* q, const uint16_t* k, const 
 
 }  // namespace
 
-bool decode_supported(const Geom& g) { return g.G * g.Lq <= kDecodeMaxRows; }
+bool decode_supported(const Geom& g) { return g.Rc == 0 && g.G * g.Lq <= kDecodeMaxRows; }
 
 size_t decode_workspace_bytes(const Geom& g) {
   const DecPlan pl = decode_plan(g);

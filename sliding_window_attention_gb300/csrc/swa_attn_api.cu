@@ -171,6 +171,26 @@ swa::Geom make_geom(int B, int Hq, int Hkv, int Lq, int L, int D, int window, in
   g.causal = causal ? 1 : 0;
   g.G = Hq / Hkv;
   g.scale = scale;
+  g.P = 0;
+  g.Rc = 0;
+  return g;
+}
+
+// A shared-prefix plan over L rows (prompt P, chosen response Rc, rejected
+// response L - P - Rc): 0 for a valid plan, SWA_ERR_BAD_PLAN otherwise.
+int check_plan(int L, int P, int Rc) {
+  if (P < 0 || Rc < 0 || (long long)P + Rc > L) return SWA_ERR_BAD_PLAN;
+  return SWA_OK;
+}
+
+// The geometry of a plan; a plan without a chosen or without a rejected
+// response is the plain causal window (Rc = 0).
+swa::Geom make_plan_geom(int B, int Hq, int Hkv, int L, int D, int window, int P, int Rc, float scale) {
+  swa::Geom g = make_geom(B, Hq, Hkv, L, L, D, window, 1, scale);
+  if (Rc > 0 && P + Rc < L) {
+    g.P = P;
+    g.Rc = Rc;
+  }
   return g;
 }
 
@@ -212,72 +232,25 @@ FwdWs fwd_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
 
 }  // namespace
 
-extern "C" {
-
-int swa_attn_version(void) { return 100; }
-
-const char* swa_attn_strerror(int code) {
-  switch (code) {
-    case SWA_OK: return "success";
-    case SWA_ERR_NULL_POINTER: return "a required pointer is NULL";
-    case SWA_ERR_BAD_SHAPE: return "B, Hq, Hkv and Lq must be >= 1, and Lk >= Lq";
-    case SWA_ERR_BAD_GROUPS: return "Hq must be a multiple of Hkv";
-    case SWA_ERR_BAD_HEAD_DIM: return "head dim D must be 64, 128, 256 or 512";
-    case SWA_ERR_BAD_WINDOW: return "window must be >= 0 (0 = no window)";
-    case SWA_ERR_BAD_SCALE: return "scale must be finite";
-    case SWA_ERR_MISALIGNED: return "tensors must be 16-byte aligned and the workspace 256-byte aligned";
-    case SWA_ERR_WORKSPACE: return "workspace smaller than the size query returned";
-    case SWA_ERR_CUDA: return "CUDA runtime or launch error";
-    case SWA_ERR_TOO_LARGE: return "sizes exceed the supported range";
-    case SWA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
-    case SWA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
-    case SWA_ERR_FP16_RANGE: return "an input magnitude overflowed the fp16 operand copy (|x| > 65504)";
-    case SWA_ERR_SCRATCH_LAYOUT:
-      return "head dim 512 needs at most one CTA per SM and SM ids below 192 for its per-SM tile scratch";
-    case SWA_ERR_NOALLOC_LIMIT:
-      return "B*Hq*L exceeds the fixed scratch of swa_attn_bwd_noalloc (2,097,152 rows); use swa_attn_bwd";
-    default: return "unknown error code";
-  }
-}
-
-size_t swa_attn_fwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || Hq % Hkv != 0 || window < 0 || !swa::fwd_tc_supported(D))
-    return 0;
-  const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, 1.f);
+// Workspace bytes of the forward on geometry g (the decode kernel serves at
+// most 16 query rows per kv head, without a shared-prefix plan).
+static size_t fwd_need(const swa::Geom& g) {
   if (swa::decode_supported(g)) return round_up(swa::decode_workspace_bytes(g), 256);
-  return fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
+  return fwd_ws_layout(g.B, g.Hq, g.Hkv, g.Lq, g.L, g.D).total;
 }
 
-size_t swa_attn_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
-  (void)window;
-  (void)causal;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq) return 0;
-  if (swa::bwd_tc_supported(D)) return bwd_tc_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
-  return bwd_delta_bytes(B, Hq, Lq);
-}
-
-size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
-  return swa_attn_fwd_workspace_bytes_ex(B, Hq, Hkv, L, L, D, window, 1);
-}
-
-size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
-  return swa_attn_bwd_workspace_bytes_ex(B, Hq, Hkv, L, L, D, window, 1);
-}
-
-int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
-                    int Hkv, int Lq, int Lk, int D, int window, int causal, float scale, void* workspace,
-                    size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse) return SWA_ERR_NULL_POINTER;
-  int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
-  if (rc) return rc;
+// The forward on a shape-checked geometry (the tail of swa_attn_fwd_ex and
+// swa_attn_fwd_prefix).
+static int fwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  const int B = g.B, Hq = g.Hq, Hkv = g.Hkv, Lq = g.Lq, Lk = g.L, D = g.D;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
       !aligned(workspace, 256))
     return SWA_ERR_MISALIGNED;
-  const size_t need = swa_attn_fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal);
+  const size_t need = fwd_need(g);
   if (workspace_bytes < need || (need > 0 && !workspace)) return SWA_ERR_WORKSPACE;
-  rc = check_device();
+  int rc = check_device();
   if (rc) return rc;
-  const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_ptr_for_current_device(&rc);
   if (!status) return rc;
@@ -304,29 +277,21 @@ int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, flo
   return SWA_OK;
 }
 
-int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
-                 int Hkv, int L, int D, int window, float scale, void* workspace, size_t workspace_bytes,
-                 void* stream) {
-  return swa_attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, L, L, D, window, 1, scale, workspace, workspace_bytes,
-                         stream);
-}
 
-int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
-                    const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq, int Lk,
-                    int D, int window, int causal, float scale, void* workspace, size_t workspace_bytes,
-                    void* stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return SWA_ERR_NULL_POINTER;
-  int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
-  if (rc) return rc;
+// The backward on a shape-checked geometry (the tail of swa_attn_bwd_ex and
+// swa_attn_bwd_prefix).
+static int bwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o,
+                   const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  const int B = g.B, Hq = g.Hq, Hkv = g.Hkv, Lq = g.Lq, Lk = g.L, D = g.D;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
       !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
     return SWA_ERR_MISALIGNED;
-  const size_t need = swa_attn_bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal);
+  const size_t need = bwd_tc_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
   if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
-  rc = check_device();
+  int rc = check_device();
   if (rc) return rc;
   if (D == 512 && (rc = check_scratch_layout(false)) != SWA_OK) return rc;
-  const swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_ptr_for_current_device(&rc);
   if (!status) return rc;
@@ -366,11 +331,129 @@ int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, con
   return SWA_OK;
 }
 
+
+extern "C" {
+
+int swa_attn_version(void) { return 100; }
+
+const char* swa_attn_strerror(int code) {
+  switch (code) {
+    case SWA_OK: return "success";
+    case SWA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case SWA_ERR_BAD_SHAPE: return "B, Hq, Hkv and Lq must be >= 1, and Lk >= Lq";
+    case SWA_ERR_BAD_GROUPS: return "Hq must be a multiple of Hkv";
+    case SWA_ERR_BAD_HEAD_DIM: return "head dim D must be 64, 128, 256 or 512";
+    case SWA_ERR_BAD_WINDOW: return "window must be >= 0 (0 = no window)";
+    case SWA_ERR_BAD_SCALE: return "scale must be finite";
+    case SWA_ERR_MISALIGNED: return "tensors must be 16-byte aligned and the workspace 256-byte aligned";
+    case SWA_ERR_WORKSPACE: return "workspace smaller than the size query returned";
+    case SWA_ERR_CUDA: return "CUDA runtime or launch error";
+    case SWA_ERR_TOO_LARGE: return "sizes exceed the supported range";
+    case SWA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+    case SWA_ERR_UNSUPPORTED_DEVICE: return "current device is not an sm_103 GPU";
+    case SWA_ERR_FP16_RANGE: return "an input magnitude overflowed the fp16 operand copy (|x| > 65504)";
+    case SWA_ERR_BAD_PLAN:
+      return "shared-prefix plan needs prompt_len >= 0, chosen_len >= 0 and prompt_len + chosen_len <= L";
+    case SWA_ERR_SCRATCH_LAYOUT:
+      return "head dim 512 needs at most one CTA per SM and SM ids below 192 for its per-SM tile scratch";
+    case SWA_ERR_NOALLOC_LIMIT:
+      return "B*Hq*L exceeds the fixed scratch of swa_attn_bwd_noalloc (2,097,152 rows); use swa_attn_bwd";
+    default: return "unknown error code";
+  }
+}
+
+size_t swa_attn_fwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq || Hq % Hkv != 0 || window < 0 || !swa::fwd_tc_supported(D))
+    return 0;
+  return fwd_need(make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, 1.f));
+}
+
+size_t swa_attn_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal) {
+  (void)window;
+  (void)causal;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lk < Lq) return 0;
+  if (swa::bwd_tc_supported(D)) return bwd_tc_ws_layout(B, Hq, Hkv, Lq, Lk, D).total;
+  return bwd_delta_bytes(B, Hq, Lq);
+}
+
+size_t swa_attn_fwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
+  return swa_attn_fwd_workspace_bytes_ex(B, Hq, Hkv, L, L, D, window, 1);
+}
+
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int L, int D, int window) {
+  return swa_attn_bwd_workspace_bytes_ex(B, Hq, Hkv, L, L, D, window, 1);
+}
+
+int swa_attn_fwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int D, int window, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return SWA_ERR_NULL_POINTER;
+  const int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (rc) return rc;
+  return fwd_run(make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale), q, k, v, o, lse, workspace,
+                 workspace_bytes, stream);
+}
+
+int swa_attn_fwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B, int Hq,
+                 int Hkv, int L, int D, int window, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return swa_attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, L, L, D, window, 1, scale, workspace, workspace_bytes,
+                         stream);
+}
+
+int swa_attn_bwd_ex(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
+                    const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int Lq, int Lk,
+                    int D, int window, int causal, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return SWA_ERR_NULL_POINTER;
+  const int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (rc) return rc;
+  return bwd_run(make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale), q, k, v, o, lse, dO, dq, dk, dv,
+                 workspace, workspace_bytes, stream);
+}
+
 int swa_attn_bwd(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
                  const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int L, int D,
                  int window, float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, L, L, D, window, 1, scale, workspace,
                          workspace_bytes, stream);
+}
+
+size_t swa_attn_fwd_workspace_bytes_prefix(int B, int Hq, int Hkv, int L, int D, int window, int prompt_len,
+                                            int chosen_len) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || Hq % Hkv != 0 || window < 0 || !swa::fwd_tc_supported(D) ||
+      check_plan(L, prompt_len, chosen_len))
+    return 0;
+  return fwd_need(make_plan_geom(B, Hq, Hkv, L, D, window, prompt_len, chosen_len, 1.f));
+}
+
+size_t swa_attn_bwd_workspace_bytes_prefix(int B, int Hq, int Hkv, int L, int D, int window, int prompt_len,
+                                            int chosen_len) {
+  if (check_plan(L, prompt_len, chosen_len)) return 0;
+  return swa_attn_bwd_workspace_bytes(B, Hq, Hkv, L, D, window);
+}
+
+int swa_attn_fwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float* o, float* lse, int B,
+                        int Hq, int Hkv, int L, int D, int window, int prompt_len, int chosen_len, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return SWA_ERR_NULL_POINTER;
+  int rc = check_shape(B, Hq, Hkv, L, L, D, window, scale);
+  if (rc) return rc;
+  if ((rc = check_plan(L, prompt_len, chosen_len))) return rc;
+  return fwd_run(make_plan_geom(B, Hq, Hkv, L, D, window, prompt_len, chosen_len, scale), q, k, v, o, lse,
+                 workspace, workspace_bytes, stream);
+}
+
+int swa_attn_bwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o, const float* lse,
+                        const swa_bf16* dO, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int L, int D,
+                        int window, int prompt_len, int chosen_len, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return SWA_ERR_NULL_POINTER;
+  int rc = check_shape(B, Hq, Hkv, L, L, D, window, scale);
+  if (rc) return rc;
+  if ((rc = check_plan(L, prompt_len, chosen_len))) return rc;
+  return bwd_run(make_plan_geom(B, Hq, Hkv, L, D, window, prompt_len, chosen_len, scale), q, k, v, o, lse, dO, dq,
+                 dk, dv, workspace, workspace_bytes, stream);
 }
 
 int swa_attn_selftest_timeout(void* stream) {

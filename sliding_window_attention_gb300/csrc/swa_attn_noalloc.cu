@@ -91,6 +91,8 @@ extern "C" int swa_attn_bwd_noalloc(const swa_bf16* q, const swa_bf16* k, const 
   g.W = (window >= L) ? 0 : window;
   g.G = Hq / Hkv;
   g.scale = scale;
+  g.P = 0;
+  g.Rc = 0;  // no shared-prefix plan
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (swa::launch_delta(g, o, dO, delta, s) != cudaSuccess) return SWA_ERR_CUDA;
   if (swa::launch_bwd_dkdv_simt(g, q, k, v, dO, lse, delta, dk, dv, s) != cudaSuccess) return SWA_ERR_CUDA;

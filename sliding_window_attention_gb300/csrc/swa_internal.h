@@ -18,6 +18,13 @@ struct Geom {
   int Lq, off;                 // query rows, L - Lq
   int causal;                  // 1: keys after the query's position are masked
   float scale;                 // softmax scale applied to q . k
+  // Shared-prefix plan (Rc > 0): one causal self-attention pass over
+  // [prompt (P rows); chosen response (Rc rows); rejected response (the
+  // rest)] in which rejected rows do not see chosen keys and the window is
+  // measured on logical positions, the rejected response restarting at P.
+  // Rc == 0: no plan.  With a plan, Lq == L, off == 0, causal == 1 and
+  // P + Rc < L.
+  int P, Rc;
 };
 
 // The band of query row i is the interval of keys [band_key_lo, band_key_hi]
@@ -27,24 +34,141 @@ struct Geom {
 //   non-causal:  W == 0 or |a - j| < W
 // Both ends are non-decreasing in i, and the rows that see key j form the
 // interval [band_q_lo, band_q_hi] (empty when lo > hi).
-__host__ __device__ __forceinline__ int band_key_lo(const Geom& g, int i) {
+//
+// Under a shared-prefix plan ("Training -- design (ORPO, flash-CCE head,
+// prefix sharing, segmented backward)", section 5.4: causal AND NOT
+// rejected -> chosen, window on logical positions) a row or a key sees up to
+// two intervals, `part` 0 and 1, which are disjoint:
+//   rejected row i:  part 0 = prompt keys [i - Rc - W + 1, P - 1],
+//                    part 1 = rejected keys [max(P + Rc, i - W + 1), i];
+//   other rows:      part 0 = the plain causal window, part 1 empty;
+//   prompt key j:    part 0 = prompt and chosen rows [j, min(P + Rc - 1, j + W - 1)],
+//                    part 1 = rejected rows [P + Rc, j + Rc + W - 1];
+//   other keys:      part 0 = the rows of their own response within the
+//                    window, part 1 empty.
+// (W == 0 drops the window bounds.)  Without a plan part 0 is the band above
+// and part 1 is empty.  An empty interval has lo > hi.
+__host__ __device__ __forceinline__ int band_key_lo(const Geom& g, int i, int part = 0) {
+  if (g.Rc > 0 && i >= g.P + g.Rc) {
+    const int lo = part ? i - g.W + 1 : i - g.Rc - g.W + 1;
+    const int floor_ = part ? g.P + g.Rc : 0;
+    return (g.W > 0 && lo > floor_) ? lo : floor_;
+  }
+  if (part) return g.L;
   const int lo = i + g.off - g.W + 1;
   return (g.W > 0 && lo > 0) ? lo : 0;
 }
-__host__ __device__ __forceinline__ int band_key_hi(const Geom& g, int i) {
+__host__ __device__ __forceinline__ int band_key_hi(const Geom& g, int i, int part = 0) {
+  if (g.Rc > 0 && i >= g.P + g.Rc) return part ? i : g.P - 1;
+  if (part) return -1;
   const int a = i + g.off;
   const int hi = g.causal ? a : (g.W > 0 ? a + g.W - 1 : g.L - 1);
   return hi < g.L - 1 ? hi : g.L - 1;
 }
-__host__ __device__ __forceinline__ int band_q_lo(const Geom& g, int j) {
+__host__ __device__ __forceinline__ int band_q_lo(const Geom& g, int j, int part = 0) {
+  if (part) return (g.Rc > 0 && j < g.P) ? g.P + g.Rc : g.Lq;
   if (!g.causal && g.W == 0) return 0;
   const int lo = (g.causal ? j : j - g.W + 1) - g.off;
   return lo > 0 ? lo : 0;
 }
-__host__ __device__ __forceinline__ int band_q_hi(const Geom& g, int j) {
+__host__ __device__ __forceinline__ int band_q_hi(const Geom& g, int j, int part = 0) {
+  if (g.Rc > 0) {
+    if (part) {
+      if (j >= g.P) return -1;
+      const int hi = g.W > 0 ? j + g.Rc + g.W - 1 : g.L - 1;
+      return hi < g.L - 1 ? hi : g.L - 1;
+    }
+    const int seg_end = j < g.P + g.Rc ? g.P + g.Rc - 1 : g.L - 1;  // rows of the key's own block
+    const int hi = g.W > 0 ? j + g.W - 1 : g.L - 1;
+    return hi < seg_end ? hi : seg_end;
+  }
+  if (part) return -1;
   if (g.W == 0) return g.Lq - 1;
   const int hi = j + g.W - 1 - g.off;
   return hi < g.Lq - 1 ? hi : g.Lq - 1;
+}
+
+// Visible columns of one row (or key) inside a tile starting at c0: the two
+// intervals [x, y] and [z, w] in tile-local coordinates.
+__host__ __device__ __forceinline__ int4 row_vis(const Geom& g, int i, int c0) {
+  return make_int4(band_key_lo(g, i, 0) - c0, band_key_hi(g, i, 0) - c0, band_key_lo(g, i, 1) - c0,
+                   band_key_hi(g, i, 1) - c0);
+}
+__host__ __device__ __forceinline__ int4 key_vis(const Geom& g, int j, int c0) {
+  return make_int4(band_q_lo(g, j, 0) - c0, band_q_hi(g, j, 0) - c0, band_q_lo(g, j, 1) - c0,
+                   band_q_hi(g, j, 1) - c0);
+}
+// The same intervals seen from a column offset d further into the tile.
+__host__ __device__ __forceinline__ int4 vshift(const int4& v, int d) {
+  return make_int4(v.x - d, v.y - d, v.z - d, v.w - d);
+}
+// Column c of a masked tile is visible: in [v.x, v.y], or (TWO: a plan is
+// active) in [v.z, v.w].
+template <bool TWO>
+__host__ __device__ __forceinline__ bool vis(int c, const int4& v) {
+  return (c >= v.x && c <= v.y) || (TWO && c >= v.z && c <= v.w);
+}
+
+// The tiles one CTA visits: those that meet the part-0 hull, then those that
+// meet the part-1 hull and not the part-0 one (a tile that meets both is
+// visited once, masked with both intervals).
+struct TileSteps {
+  int lo0, n0, lo1, n1;
+  __host__ __device__ int count() const { return n0 + n1; }
+  __host__ __device__ int tile(int n) const { return n < n0 ? lo0 + n : lo1 + (n - n0); }
+};
+__host__ __device__ __forceinline__ TileSteps make_steps(int lo0, int hi0, int lo1, int hi1, int T) {
+  TileSteps s;
+  s.lo0 = lo0 <= hi0 ? lo0 / T : 0;
+  s.n0 = lo0 <= hi0 ? hi0 / T - lo0 / T + 1 : 0;
+  int a = lo1 / T, z = hi1 / T;
+  if (s.n0 > 0 && a <= s.lo0 + s.n0 - 1) a = s.lo0 + s.n0;  // tiles already in part 0
+  s.lo1 = a;
+  s.n1 = (lo1 <= hi1 && a <= z) ? z - a + 1 : 0;
+  return s;
+}
+// Key tiles (of T keys) that rows [r0, r1] see.
+__host__ __device__ __forceinline__ TileSteps row_steps(const Geom& g, int r0, int r1, int T) {
+  if (g.Rc == 0) return make_steps(band_key_lo(g, r0), band_key_hi(g, r1), 1, 0, T);
+  const int R = g.P + g.Rc;  // first rejected row
+  int lo0 = g.L, hi0 = -1;
+  if (r0 < R) {  // rows of the prompt and the chosen response: the plain causal window
+    lo0 = band_key_lo(g, r0, 0);
+    hi0 = band_key_hi(g, r1 < R ? r1 : R - 1, 0);
+  }
+  int lo1 = g.L, hi1 = -1;
+  if (r1 >= R) {  // rejected rows: prompt keys (part 0, shrinking) and rejected keys (part 1)
+    const int a = r0 > R ? r0 : R;
+    const int l = band_key_lo(g, a, 0), h = band_key_hi(g, a, 0);
+    if (l <= h) {
+      lo0 = l < lo0 ? l : lo0;
+      hi0 = h > hi0 ? h : hi0;
+    }
+    lo1 = band_key_lo(g, a, 1);
+    hi1 = r1;
+  }
+  return make_steps(lo0, hi0, lo1, hi1, T);
+}
+// Query tiles (of T rows) that see keys [j0, j1].
+__host__ __device__ __forceinline__ TileSteps key_steps(const Geom& g, int j0, int j1, int T) {
+  const int lo0 = band_q_lo(g, j0, 0), hi0 = band_q_hi(g, j1, 0);
+  if (g.Rc == 0 || j0 >= g.P) return make_steps(lo0, hi0, 1, 0, T);
+  const int jp = j1 < g.P - 1 ? j1 : g.P - 1;  // the tile's last prompt key
+  return make_steps(lo0, hi0, g.P + g.Rc, band_q_hi(g, jp, 1), T);
+}
+// Every row of [r0, r1] sees every key of [c0, c1] (no mask needed).
+__host__ __device__ __forceinline__ bool rows_tile_full(const Geom& g, int r0, int r1, int c0, int c1) {
+  if (g.Rc == 0) return c0 >= band_key_lo(g, r1) && c1 <= band_key_hi(g, r0);
+  const int R = g.P + g.Rc;
+  if (r1 < R) return c0 >= band_key_lo(g, r1, 0) && c1 <= band_key_hi(g, r0, 0);
+  if (r0 < R) return false;
+  return (c0 >= band_key_lo(g, r1, 0) && c1 <= band_key_hi(g, r0, 0)) ||
+         (c0 >= band_key_lo(g, r1, 1) && c1 <= band_key_hi(g, r0, 1));
+}
+// Every key of [j0, j1] is seen by every row of [c0, c1].
+__host__ __device__ __forceinline__ bool keys_tile_full(const Geom& g, int j0, int j1, int c0, int c1) {
+  if (c0 >= band_q_lo(g, j1, 0) && c1 <= band_q_hi(g, j0, 0)) return true;
+  return g.Rc > 0 && j1 < g.P && c0 >= g.P + g.Rc && c1 <= band_q_hi(g, j0, 1);
 }
 
 // Device-side status codes latched into the per-device status word.

@@ -202,16 +202,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const PrepParams p) {
 
 // dQ elementwise step for one query row (lse*log2e = l2, Delta = dl) and 32
 // key columns: dS = P (dP - Delta) as fp16 pairs.
-template <bool FULL>
+// Unless FULL, key columns outside the row's visible keys v (tile-local;
+// see vis(), TWO under a shared-prefix plan) get P = 0.
+template <bool FULL, bool TWO = false>
 __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float sl2, float l2,
-                                         float dl, int cbase, int clo, int chi, uint32_t (&dd)[16]) {
+                                         float dl, int cbase, const int4& v, uint32_t (&dd)[16]) {
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
     float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -l2));
     float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -l2));
     if (!FULL) {
-      p0 = (cbase + e >= clo && cbase + e <= chi) ? p0 : 0.f;
-      p1 = (cbase + e + 1 >= clo && cbase + e + 1 <= chi) ? p1 : 0.f;
+      p0 = vis<TWO>(cbase + e, v) ? p0 : 0.f;
+      p1 = vis<TWO>(cbase + e + 1, v) ? p1 : 0.f;
     }
     dd[e >> 1] = pack_half2(p0 * (__uint_as_float(dv[e]) - dl), p1 * (__uint_as_float(dv[e + 1]) - dl));
   }
@@ -265,18 +267,22 @@ struct Kv128Cfg {
 
 // P^T for one key row and 64 query columns (fp32, in place over S^T); lv
 // holds lse * log2e of the 64 columns (loaded before S^T was waited for).
-template <bool FULL>
-__device__ __forceinline__ void kv_p64(uint32_t (&sv)[64], const float (&lv)[64], float sl2, int cbase, int clo,
-                                       int chi) {
+// Unless FULL, columns outside the key's visible rows v (tile-local; see
+// vis(), TWO under a shared-prefix plan) get P = 0.
+template <bool FULL, bool TWO = false>
+__device__ __forceinline__ void kv_p64(uint32_t (&sv)[64], const float (&lv)[64], float sl2, int cbase,
+                                       const int4& v) {
 #pragma unroll
   for (int e = 0; e < 64; ++e) {
     float pv = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -lv[e]));
-    if (!FULL) pv = (cbase + e >= clo && cbase + e <= chi) ? pv : 0.f;
+    if (!FULL) pv = vis<TWO>(cbase + e, v) ? pv : 0.f;
     sv[e] = __float_as_uint(pv);
   }
 }
 
-template <int D>
+// TWO: a shared-prefix plan is active (a key may be seen by two row
+// intervals); a separate instantiation keeps the plain kernel's registers.
+template <int D, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -311,10 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
   const int j0 = (int)blockIdx.y * BNK;
   const int jhi = min(j0 + BNK, g.L) - 1;
-  // query rows that can see a key of this tile
-  const int qlo = band_q_lo(g, j0), qhi = band_q_hi(g, jhi);
-  const int t_lo = qlo / BM, t_hi = qhi / BM;
-  const int ntq = qlo <= qhi ? t_hi - t_lo + 1 : 0;
+  // query tiles that can see a key of this tile
+  const TileSteps qsteps = key_steps(g, j0, jhi, BM);
+  const int ntq = qsteps.count();
   const int N = g.G * ntq;  // steps (head of group, query tile)
   if (N == 0) {
     // no query sees these keys: zero gradients (see dkdv_tc_kernel)
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto step_head = [&](int n) { return b * g.Hq + kvh * g.G + n / ntq; };
-  auto step_i0 = [&](int n) { return (t_lo + n % ntq) * BM; };
+  auto step_i0 = [&](int n) { return qsteps.tile(n % ntq) * BM; };
 
   if (warp == 0) {
     if (elect_one()) {
@@ -463,6 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per step pushed the kernel past its register budget)
     const int qlo_j = band_q_lo(g, j), qhi_j = band_q_hi(g, j);
     const int qlo_all = band_q_lo(g, jhi), qhi_all = band_q_hi(g, j0);
+    constexpr bool two = TWO;  // shared-prefix plan: a key may see two row intervals
+    const int4 vj = key_vis(g, j, 0);  // (plan only) both row intervals of key j
     for (int n = 0; n < N; ++n) {
       const int i0 = step_i0(n);
       const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + i0 + cw0;
@@ -484,12 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(s_read);
-      const bool full = (i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all);
+      // every key of the tile seen by every query of the step: the hoisted
+      // plain-band bounds, or (shared-prefix plan) the two-interval test
+      const bool full = ((i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all)) ||
+                        (two && keys_tile_full(g, j0, jhi, i0, i0 + BM - 1));
       // query columns c of this tile that see key j: i0 + c in [qlo_j, qhi_j]
-      const int clo = qlo_j - i0;
-      const int chi = qhi_j - i0;
-      if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
-      else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
+      // (and, under a plan, in its second interval)
+      if (full) {
+        kv_p64<true>(sv, lv, sl2, cw0, make_int4(0, 0, 0, 0));
+      } else if constexpr (two) {
+        kv_p64<false, true>(sv, lv, sl2, cw0, vshift(vj, i0));
+      } else {
+        kv_p64<false>(sv, lv, sl2, cw0, make_int4(qlo_j - i0, qhi_j - i0, 1, 0));
+      }
       // P^T as fp16 pairs (the dV operand); dS below uses the same rounded P
       uint32_t pp[32];
 #pragma unroll
@@ -607,7 +621,7 @@ struct Kv256Cfg {
 // w packed its 64 columns into [64 w, 64 w + 32).
 __device__ __forceinline__ uint32_t packed_col(int ks) { return (uint32_t)((ks >> 2) * 64 + (ks & 3) * 8); }
 
-template <int MODE>
+template <int MODE, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv256_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -641,10 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
   const int j0 = (int)blockIdx.y * BNK;
   const int jhi = min(j0 + BNK, g.L) - 1;
-  // query rows that can see a key of this tile
-  const int qlo = band_q_lo(g, j0), qhi = band_q_hi(g, jhi);
-  const int t_lo = qlo / BM, t_hi = qhi / BM;
-  const int ntq = qlo <= qhi ? t_hi - t_lo + 1 : 0;
+  // query tiles that can see a key of this tile
+  const TileSteps qsteps = key_steps(g, j0, jhi, BM);
+  const int ntq = qsteps.count();
   const int N = g.G * ntq;  // steps (head of group, query tile)
   if (N == 0) {
     // no query sees these keys (queries that are a suffix of the keys, with a
@@ -682,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto step_head = [&](int n) { return b * g.Hq + kvh * g.G + n / ntq; };
-  auto step_i0 = [&](int n) { return (t_lo + n % ntq) * BM; };
+  auto step_i0 = [&](int n) { return qsteps.tile(n % ntq) * BM; };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producers
@@ -825,6 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per step pushed the kernel past its register budget)
     const int qlo_j = band_q_lo(g, j), qhi_j = band_q_hi(g, j);
     const int qlo_all = band_q_lo(g, jhi), qhi_all = band_q_hi(g, j0);
+    constexpr bool two = TWO;  // shared-prefix plan: a key may see two row intervals
+    const int4 vj = key_vis(g, j, 0);  // (plan only) both row intervals of key j
     for (int n = 0; n < N; ++n) {
       const int i0 = step_i0(n);
       const int sbuf = DVM ? (n & 1) : 0;
@@ -847,12 +862,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + scol + cw0, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_ld32(tmem + lane_off + scol + cw0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld();
-      const bool full = (i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all);
+      // every key of the tile seen by every query of the step: the hoisted
+      // plain-band bounds, or (shared-prefix plan) the two-interval test
+      const bool full = ((i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all)) ||
+                        (two && keys_tile_full(g, j0, jhi, i0, i0 + BM - 1));
       // query columns c of this tile that see key j: i0 + c in [qlo_j, qhi_j]
-      const int clo = qlo_j - i0;
-      const int chi = qhi_j - i0;
-      if (full) kv_p64<true>(sv, lv, sl2, cw0, clo, chi);
-      else kv_p64<false>(sv, lv, sl2, cw0, clo, chi);
+      // (and, under a plan, in its second interval)
+      if (full) {
+        kv_p64<true>(sv, lv, sl2, cw0, make_int4(0, 0, 0, 0));
+      } else if constexpr (two) {
+        kv_p64<false, true>(sv, lv, sl2, cw0, vshift(vj, i0));
+      } else {
+        kv_p64<false>(sv, lv, sl2, cw0, make_int4(qlo_j - i0, qhi_j - i0, 1, 0));
+      }
       // P^T as fp16 pairs; dS below uses the same rounded P
       uint32_t pp[32];
 #pragma unroll
@@ -989,8 +1011,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i0 = qt * BMQ;
   const int ihi = min(i0 + BMQ, g.Lq) - 1;
   // key tiles meeting the band of rows i0 .. ihi (never empty)
-  const int t_lo = band_key_lo(g, i0) / BN, t_hi = band_key_hi(g, ihi) / BN;
-  const int nt = t_hi - t_lo + 1;
+  const TileSteps ksteps = row_steps(g, i0, ihi, BN);
+  const int nt = ksteps.count();
+  const bool two = g.Rc > 0;  // shared-prefix plan: a row may see two key intervals
 
   if (threadIdx.x == 0) {
     mbar_init(g_full, 1);
@@ -1026,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
-        const int j0 = (t_lo + n) * BN;
+        const int j0 = ksteps.tile(n) * BN;
         if (n >= NS && !mbar_wait(kv_empty + st, ((n / NS) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(kv_full + st, 2 * C::KV_BYTES);
         // all KCH 64-column chunks of the BN rows in one instruction each
@@ -1120,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb0 = wg * CW;
     bool ok = true;
     for (int n = 0; n < nt; ++n) {
-      const int j0 = (t_lo + n) * BN;
+      const int j0 = ksteps.tile(n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full, n & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[CW], dv[CW];
@@ -1129,13 +1152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(sdp_read);  // S may be overwritten; dP once both warpgroups have read it
-      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
-      // key columns c of this tile visible to row i: j0 + c in [band_key_lo(i), band_key_hi(i)]
-      const int clo = band_key_lo(g, i) - j0;
-      const int chi = band_key_hi(g, i) - j0;
+      const bool full = rows_tile_full(g, i0, ihi, j0, j0 + BN - 1);
+      // key columns c of this tile visible to row i: j0 + c in the row's band
+      const int4 vv = row_vis(g, i, j0);
       uint32_t dd[CW / 2];
-      if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, cb0, clo, chi, dd);
-      else dq_chunk<false>(sv, dv, sl2, rs.x, rs.y, cb0, clo, chi, dd);
+      if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
+      else if (two) dq_chunk<false, true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
+      else dq_chunk<false>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
       // dS of keys cb0 .. cb0 + 31 goes to columns cb0 / 2 .. of the dP
       // buffer, which the other warpgroup may still be reading
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_read, n & 1, abort_flag))) { ok = false; break; }
@@ -1239,8 +1262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i0 = qt * BMQ;
   const int ihi = min(i0 + BMQ, g.Lq) - 1;
   // key tiles meeting the band of rows i0 .. ihi (never empty)
-  const int t_lo = band_key_lo(g, i0) / BN, t_hi = band_key_hi(g, ihi) / BN;
-  const int nt = t_hi - t_lo + 1;
+  const TileSteps ksteps = row_steps(g, i0, ihi, BN);
+  const int nt = ksteps.count();
+  const bool two = g.Rc > 0;  // shared-prefix plan: a row may see two key intervals
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -1285,7 +1309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K and V of each step, each ring refilled as soon as its slot is released
       int nk = 0, nv = 0;
       for (int n = 0; n < nt; ++n) {
-        const int j0 = (t_lo + n) * BN;
+        const int j0 = ksteps.tile(n) * BN;
         const int sk = n % NK, sv = n % NV;
         if (n >= NK && !mbar_wait(k_empty + sk, ((n / NK) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + sk, C::KV_BYTES);
@@ -1373,12 +1397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
-      const int j0 = (t_lo + n) * BN;
+      const int j0 = ksteps.tile(n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
-      const int clo = band_key_lo(g, i) - j0;  // visible key columns [clo, chi]
-      const int chi = band_key_hi(g, i) - j0;
+      const bool full = rows_tile_full(g, i0, ihi, j0, j0 + BN - 1);
+      const int4 vv = row_vis(g, i, j0);  // visible key columns of row i
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
@@ -1396,8 +1419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t(&dvc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(dv + c * 32);
         const int cb = cw0 + c * 32;
         uint32_t dd[16];
-        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
-        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, clo, chi, dd);
+        if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
+        else if (two) dq_chunk<false, true>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
+        else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
         tmem_st16(tmem + lane_off + C::S_COL + sb * BN + cb / 2, dd);
       }
       tmem_wait_st();
@@ -1455,7 +1479,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
       if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-      auto kern = dkdv128_tc_kernel<D>;
+      auto kern = g.Rc > 0 ? dkdv128_tc_kernel<D, true> : dkdv128_tc_kernel<D, false>;
       if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
           cudaSuccess)
         return e2;
@@ -1476,7 +1500,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
         if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
         if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
         if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-        auto kern = dkdv256_tc_kernel<MODE>;
+        auto kern = g.Rc > 0 ? dkdv256_tc_kernel<MODE, true> : dkdv256_tc_kernel<MODE, false>;
         if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
             cudaSuccess)
           return e2;

@@ -155,10 +155,11 @@ struct ParamsPair {
 // P for 64 columns (cb0 .. cb0 + 63 of the tile) of one row, in place over the
 // S values (fp32).  PER_COL: the lse belongs to the column (lse_s is the
 // shared address of lse * log2e of the 64 columns); otherwise l2 is the row's.
-// Columns outside [clo, chi] are exactly zero unless FULL.
-template <bool FULL, bool PER_COL>
+// Columns outside the row's visible columns v (tile-local; see vis(), TWO
+// under a shared-prefix plan) are exactly zero unless FULL.
+template <bool FULL, bool PER_COL, bool TWO = false>
 __device__ __forceinline__ void p_tile64(uint32_t (&sv)[64], uint32_t lse_s, float l2, float sl2, int cb0,
-                                         int clo, int chi) {
+                                         const int4& v) {
 #pragma unroll
   for (int e = 0; e < 64; e += 4) {
     float lv[4] = {l2, l2, l2, l2};
@@ -172,7 +173,7 @@ __device__ __forceinline__ void p_tile64(uint32_t (&sv)[64], uint32_t lse_s, flo
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float pv = fast_exp2(fmaf(__uint_as_float(sv[e + u]), sl2, -lv[u]));
-      if (!FULL) pv = (cb0 + e + u >= clo && cb0 + e + u <= chi) ? pv : 0.f;
+      if (!FULL) pv = vis<TWO>(cb0 + e + u, v) ? pv : 0.f;
       sv[e + u] = __float_as_uint(pv);
     }
   }
@@ -259,19 +260,12 @@ __global__ void __launch_bounds__(kThr, 1)
   const int r0 = pr0 + (int)h * T;
   const bool own_rows = r0 < LX;  // false for the second tile of an odd last pair
   const int rlast = own_rows ? min(r0 + T, LX) - 1 : r0;
-  int t_lo, ntq, N;
-  if (DIR == kDirKV) {
-    // query rows that can see a key of the pair
-    const int qlo = band_q_lo(g, pr0), qhi = band_q_hi(g, prlast);
-    t_lo = qlo / T;
-    ntq = qlo <= qhi ? qhi / T - t_lo + 1 : 0;
-    N = g.G * ntq;
-  } else {
-    // key tiles meeting the band of the pair's rows (never empty)
-    t_lo = band_key_lo(g, pr0) / T;
-    ntq = band_key_hi(g, prlast) / T - t_lo + 1;
-    N = ntq;
-  }
+  // dK/dV pass: the query tiles that can see a key of the pair; dQ pass: the
+  // key tiles meeting the band of the pair's rows (never empty)
+  const TileSteps tsteps = (DIR == kDirKV) ? key_steps(g, pr0, prlast, T) : row_steps(g, pr0, prlast, T);
+  const int ntq = tsteps.count();
+  const int N = (DIR == kDirKV) ? g.G * ntq : ntq;
+  const bool two = g.Rc > 0;  // shared-prefix plan: two visible intervals per row
   if (N == 0) {
     // dK/dV pass, and no query sees these keys (queries that are a suffix of
     // the keys, with a window): zero gradients ("Lab 028 lab detail", "What
@@ -286,8 +280,8 @@ __global__ void __launch_bounds__(kThr, 1)
   // clusters of one kv head (all starting at the last query tile) read the
   // same Q and dO tiles at about the same time.
   auto step_rows = [&](int n) {
-    if (DIR == kDirKV) return (t_lo + ntq - 1 - n / g.G) * T;
-    return (t_lo + n) * T;
+    if (DIR == kDirKV) return tsteps.tile(ntq - 1 - n / g.G) * T;
+    return tsteps.tile(n) * T;
   };
   auto step_head = [&](int n) -> int {
     if (DIR == kDirKV) return b * g.Hq + (head - b * g.Hkv) * g.G + n % g.G;  // query head
@@ -631,22 +625,21 @@ __global__ void __launch_bounds__(kThr, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free);  // S may be overwritten (the peer's relay tells the leader)
       bool full;
-      int clo, chi;
+      int4 vv;
       if (DIR == kDirKV) {  // columns are query rows c0 .. c0 + 127, this thread's row is key `row`
-        full = own_rows && (c0 >= band_q_lo(g, rlast)) && (c0 + T - 1 <= band_q_hi(g, r0));
-        clo = band_q_lo(g, row) - c0;
-        chi = band_q_hi(g, row) - c0;
+        full = own_rows && keys_tile_full(g, r0, rlast, c0, c0 + T - 1);
+        vv = key_vis(g, row, c0);
       } else {  // columns are keys c0 .. c0 + 127, this thread's row is query `row`
-        full = own_rows && (c0 >= band_key_lo(g, rlast)) && (c0 + T - 1 <= band_key_hi(g, r0));
-        clo = band_key_lo(g, row) - c0;
-        chi = band_key_hi(g, row) - c0;
+        full = own_rows && rows_tile_full(g, r0, rlast, c0, c0 + T - 1);
+        vv = row_vis(g, row, c0);
       }
       if (DIR == kDirKV && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stats_full[wg], m & 1, abort_flag, R))) {
         ok = false;
         break;
       }
-      if (full) p_tile64<true, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, clo, chi);
-      else p_tile64<false, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, clo, chi);
+      if (full) p_tile64<true, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
+      else if (two) p_tile64<false, DIR == kDirKV, true>(sv, lse_s, rs_row.x, sl2, cb0, vv);
+      else p_tile64<false, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
       uint32_t o[32];
       if (DIR == kDirKV) {
         pack64(sv, o);

@@ -89,10 +89,11 @@ struct FwdParams {
 // One tile of the forward softmax for one row held in registers (raw scores
 // sr[BN]): returns the tile's scaled row maximum through *tmax_out after
 // pass 1; pass 2 (exp) runs in softmax_tile_p.  FULL: every entry is in the
-// band (no masking code at all); otherwise entries outside [clo, chi] are
+// band (no masking code at all); otherwise entries outside the visible
+// columns v (see vis(); TWO: two intervals, under a shared-prefix plan) are
 // masked in the scaled domain, which is correct for any sign of the scale.
-template <int BN, bool FULL>
-__device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], float sl2, int clo, int chi) {
+template <int BN, bool FULL, bool TWO = false>
+__device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], float sl2, const int4& v) {
   float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
   if constexpr (FULL) {
     if (sl2 >= 0.f) {
@@ -117,8 +118,8 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
   } else {
 #pragma unroll
     for (int e = 0; e < BN; e += 2) {
-      const float x0 = (e >= clo && e <= chi) ? __uint_as_float(sr[e]) * sl2 : -INFINITY;
-      const float x1 = (e + 1 >= clo && e + 1 <= chi) ? __uint_as_float(sr[e + 1]) * sl2 : -INFINITY;
+      const float x0 = vis<TWO>(e, v) ? __uint_as_float(sr[e]) * sl2 : -INFINITY;
+      const float x1 = vis<TWO>(e + 1, v) ? __uint_as_float(sr[e + 1]) * sl2 : -INFINITY;
       if (e & 2) a1 = fmaxf(a1, fmaxf(x0, x1));
       else a0 = fmaxf(a0, fmaxf(x0, x1));
     }
@@ -129,8 +130,8 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
 // Pass 2: P = 2^(sl2 * s - m) for the row, rounded to fp16, packed two per
 // 32-bit TMEM column at p_taddr.  SUM: also returns the row sum of P (fp32);
 // otherwise the tensor core takes it.
-template <int BN, bool FULL, bool SUM>
-__device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, int clo, int chi,
+template <int BN, bool FULL, bool SUM, bool TWO = false>
+__device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, const int4& v,
                                                  uint32_t p_taddr) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -144,8 +145,8 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float 
         p0 = fast_exp2(fmaf(__uint_as_float(sr[col]), sl2, -m_use));
         p1 = fast_exp2(fmaf(__uint_as_float(sr[col + 1]), sl2, -m_use));
       } else {
-        const float x0 = (col >= clo && col <= chi) ? __uint_as_float(sr[col]) * sl2 : -INFINITY;
-        const float x1 = (col + 1 >= clo && col + 1 <= chi) ? __uint_as_float(sr[col + 1]) * sl2 : -INFINITY;
+        const float x0 = vis<TWO>(col, v) ? __uint_as_float(sr[col]) * sl2 : -INFINITY;
+        const float x1 = vis<TWO>(col + 1, v) ? __uint_as_float(sr[col + 1]) * sl2 : -INFINITY;
         p0 = fast_exp2(x0 - m_use);
         p1 = fast_exp2(x1 - m_use);
       }
@@ -197,8 +198,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int ihi = min(i0 + kBM, g.Lq) - 1;
   // key tiles meeting the band of rows i0 .. ihi (never empty: every row
   // sees at least the key at its own position)
-  const int t_lo = band_key_lo(g, i0) / BN, t_hi = band_key_hi(g, ihi) / BN;
-  const int nt = t_hi - t_lo + 1;
+  const TileSteps steps = row_steps(g, i0, ihi, BN);
+  const int nt = steps.count();
+  const bool two = g.Rc > 0;  // shared-prefix plan: up to two visible intervals per row
 
   if (threadIdx.x < 128) ones[threadIdx.x] = 0x3C003C00u;  // two fp16 1.0 per word, 512 bytes
   if (threadIdx.x == 0) {
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
         const uint32_t par = ((n / NS) & 1) ^ 1;
-        const int j0 = (t_lo + n) * BN;
+        const int j0 = steps.tile(n) * BN;
         if (n >= NS && !mbar_wait(k_empty + st, par, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + st, C::K_BYTES);
         tma_load_4d(sK + st * C::K_BYTES, &tmK, k_full + st, 0, j0, 0, bkv);
@@ -317,21 +319,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     bool ok = true;
     for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
-      const int j0 = (t_lo + n) * BN;
+      const int j0 = steps.tile(n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 >= band_key_lo(g, ihi)) && (j0 + BN - 1 <= band_key_hi(g, i0));
+      const bool full = rows_tile_full(g, i0, ihi, j0, j0 + BN - 1);
       // the whole S row in registers: all loads issued, then one wait
       uint32_t sr[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c)
         tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
       tmem_wait_ld();
-      // Visible key columns of this row inside the tile: [clo, chi] (edge tiles only).
-      const int clo = band_key_lo(g, i) - j0;
-      const int chi = band_key_hi(g, i) - j0;
-      const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, clo, chi)
-                              : softmax_tile_max<BN, false>(sr, sl2, clo, chi);
+      // Visible key columns of this row inside the tile (edge tiles only).
+      const int4 vv = row_vis(g, i, j0);
+      const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, vv)
+                              : (two ? softmax_tile_max<BN, false, true>(sr, sl2, vv)
+                                     : softmax_tile_max<BN, false>(sr, sl2, vv));
       float alpha = 1.f;
       bool rescale = false;
       if (tmax > m_run + kRescaleLog2) {
@@ -343,8 +345,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN;
-      if (full) softmax_tile_p<BN, true, false>(sr, sl2, m_use, clo, chi, p_taddr);
-      else softmax_tile_p<BN, false, false>(sr, sl2, m_use, clo, chi, p_taddr);
+      if (full) softmax_tile_p<BN, true, false>(sr, sl2, m_use, vv, p_taddr);
+      else if (two) softmax_tile_p<BN, false, false, true>(sr, sl2, m_use, vv, p_taddr);
+      else softmax_tile_p<BN, false, false>(sr, sl2, m_use, vv, p_taddr);
       // Wait for PV(n-1) at every tile, not only when rescaling: this thread then
       // has observed every earlier PV completion, so the o_done phase can be at
       // most one ahead of the parity asked for (no aliasing of phase n-3 with
@@ -494,17 +497,24 @@ __global__ void __launch_bounds__(320, 1)
   const int b = bh / g.Hq, h = bh - b * g.Hq;
   const int bkv = b * g.Hkv + h / g.G;
   const int pair = p.n_qtiles - 1 - (int)blockIdx.y;  // longest rows first (n_qtiles: pairs here)
-  // tile w (A = 0, B = 1): query rows [i0w, ihiw]; key tiles [low, hiw]
-  // (empty when tile B has no rows).  Scalars, not arrays: an array indexed by
-  // the warpgroup would live in local memory.
+  // tile w (A = 0, B = 1): query rows [i0w, ihiw]; its key tiles stA / stB
+  // in ascending order (none when tile B has no rows).  Scalars, not arrays:
+  // an array indexed by the warpgroup would live in local memory.
   const int i0A = 2 * pair * BM, i0B = i0A + BM;
   const int ihiA = min(i0A + BM, g.Lq) - 1, ihiB = min(i0B + BM, g.Lq) - 1;
-  const int loA = band_key_lo(g, i0A) / BN, hiA = band_key_hi(g, ihiA) / BN;
-  const int loB = i0B < g.Lq ? band_key_lo(g, i0B) / BN : 1;
-  const int hiB = i0B < g.Lq ? band_key_hi(g, ihiB) / BN : 0;
-  const bool hasB = loB <= hiB;
-  const int u0 = loA, u1 = hasB ? max(hiA, hiB) : hiA;  // key tiles of either tile (loA <= loB)
-  auto uses = [&](int w, int n) { return w ? (n >= loB && n <= hiB) : (n >= loA && n <= hiA); };
+  const TileSteps stA = row_steps(g, i0A, ihiA, BN);
+  const TileSteps stB = i0B < g.Lq ? row_steps(g, i0B, ihiB, BN) : TileSteps{0, 0, 0, 0};
+  const bool hasB = stB.count() > 0;
+  const bool two = g.Rc > 0;  // shared-prefix plan: up to two visible intervals per row
+  auto first_tile = [](const TileSteps& s) { return s.n0 ? s.lo0 : s.lo1; };
+  auto last_tile = [](const TileSteps& s) { return s.n1 ? s.lo1 + s.n1 - 1 : s.lo0 + s.n0 - 1; };
+  // key tiles of either query tile
+  const int u0 = hasB ? min(first_tile(stA), first_tile(stB)) : first_tile(stA);
+  const int u1 = hasB ? max(last_tile(stA), last_tile(stB)) : last_tile(stA);
+  auto in_steps = [](const TileSteps& s, int n) {
+    return (n >= s.lo0 && n < s.lo0 + s.n0) || (n >= s.lo1 && n < s.lo1 + s.n1);
+  };
+  auto uses = [&](int w, int n) { return w ? in_steps(stB, n) : in_steps(stA, n); };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -639,21 +649,21 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- softmax, one warpgroup per query tile
     const int w = (warp - 2) >> 2;  // warps 2-5: tile A, 6-9: tile B
     const int r = 32 * (warp & 3) + (threadIdx.x & 31);
-    const int i0w = w ? i0B : i0A, ihiw = w ? ihiB : ihiA, low = w ? loB : loA, hiw = w ? hiB : hiA;
+    const int i0w = w ? i0B : i0A, ihiw = w ? ihiB : ihiA;
+    const TileSteps stw = w ? stB : stA;
     const int i = i0w + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t s_col = C::S_COL + 128 * w, o_col = D * w;
     const float sl2 = g.scale * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    const int cnt = hiw - low + 1;  // key tiles of this query tile (0 for a missing tile B)
+    const int cnt = stw.count();  // key tiles of this query tile (0 for a missing tile B)
     for (int k = 0; k < cnt; ++k) {
-      const int j0 = (low + k) * BN;
+      const int j0 = stw.tile(k) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + w, k & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = (j0 >= band_key_lo(g, ihiw)) && (j0 + BN - 1 <= band_key_hi(g, i0w));
-      const int clo = band_key_lo(g, i) - j0;
-      const int chi = band_key_hi(g, i) - j0;
+      const bool full = rows_tile_full(g, i0w, ihiw, j0, j0 + BN - 1);
+      const int4 vv = row_vis(g, i, j0);
       // the row in two 64-column halves (registers stay below the spill
       // limit): first the maximum, then P; half h's packed P lands on columns
       // [32 h, 32 h + 32), which half h has already read
@@ -664,8 +674,10 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_off + s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(sr));
         tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
-        tmax = fmaxf(tmax, full ? softmax_tile_max<64, true>(sr, sl2, clo - 64 * hf, chi - 64 * hf)
-                                : softmax_tile_max<64, false>(sr, sl2, clo - 64 * hf, chi - 64 * hf));
+        const int4 vh = vshift(vv, 64 * hf);
+        tmax = fmaxf(tmax, full ? softmax_tile_max<64, true>(sr, sl2, vh)
+                                : (two ? softmax_tile_max<64, false, true>(sr, sl2, vh)
+                                       : softmax_tile_max<64, false>(sr, sl2, vh)));
       }
       float alpha = 1.f;
       bool rescale = false;
@@ -685,8 +697,10 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
         const uint32_t p_taddr = tmem + lane_off + s_col + 32 * hf;
-        tsum += full ? softmax_tile_p<64, true, true>(sr, sl2, m_use, clo - 64 * hf, chi - 64 * hf, p_taddr)
-                     : softmax_tile_p<64, false, true>(sr, sl2, m_use, clo - 64 * hf, chi - 64 * hf, p_taddr);
+        const int4 vh = vshift(vv, 64 * hf);
+        tsum += full ? softmax_tile_p<64, true, true>(sr, sl2, m_use, vh, p_taddr)
+                     : (two ? softmax_tile_p<64, false, true, true>(sr, sl2, m_use, vh, p_taddr)
+                            : softmax_tile_p<64, false, true>(sr, sl2, m_use, vh, p_taddr));
       }
       l_run = l_run * alpha + tsum;
       // PV_w(k - 1) must be complete before O is rescaled (waited for at every

@@ -131,17 +131,18 @@ struct FwdPairParams {
   int* status;
 };
 
-// Scaled maximum over 64 raw scores of one row; entries outside [clo, chi]
-// are excluded unless FULL (correct for any sign of the scale).
-template <bool FULL>
-__device__ __forceinline__ float half_max(const uint32_t (&sr)[64], float sl2, int clo, int chi) {
+// Scaled maximum over 64 raw scores of one row; entries outside the row's
+// visible columns v (see vis(); TWO under a shared-prefix plan) are excluded
+// unless FULL (correct for any sign of the scale).
+template <bool FULL, bool TWO = false>
+__device__ __forceinline__ float half_max(const uint32_t (&sr)[64], float sl2, const int4& v) {
   float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
     float x0 = __uint_as_float(sr[e]) * sl2, x1 = __uint_as_float(sr[e + 1]) * sl2;
     if (!FULL) {
-      x0 = (e >= clo && e <= chi) ? x0 : -INFINITY;
-      x1 = (e + 1 >= clo && e + 1 <= chi) ? x1 : -INFINITY;
+      x0 = vis<TWO>(e, v) ? x0 : -INFINITY;
+      x1 = vis<TWO>(e + 1, v) ? x1 : -INFINITY;
     }
     a0 = fmaxf(a0, x0);
     a1 = fmaxf(a1, x1);
@@ -150,8 +151,8 @@ __device__ __forceinline__ float half_max(const uint32_t (&sr)[64], float sl2, i
 }
 
 // P = 2^(sl2 s - m) for 64 entries as fp16 pairs; returns the fp32 row sum.
-template <bool FULL>
-__device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, float m_use, int clo, int chi,
+template <bool FULL, bool TWO = false>
+__device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, float m_use, const int4& v,
                                         uint32_t (&pk)[32]) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -159,8 +160,8 @@ __device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, flo
     float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), sl2, -m_use));
     float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), sl2, -m_use));
     if (!FULL) {
-      p0 = (e >= clo && e <= chi) ? p0 : 0.f;
-      p1 = (e + 1 >= clo && e + 1 <= chi) ? p1 : 0.f;
+      p0 = vis<TWO>(e, v) ? p0 : 0.f;
+      p1 = vis<TWO>(e + 1, v) ? p1 : 0.f;
     }
     s0 += p0;
     s1 += p1;
@@ -199,8 +200,9 @@ __global__ void __launch_bounds__(kThr, 1)
   const bool own_rows = i0 < g.Lq;  // false for the second tile of an odd last pair
   const int ihi = own_rows ? min(i0 + T, g.Lq) - 1 : i0;
   // key steps meeting the band of the pair's rows (at least one)
-  const int t_lo = band_key_lo(g, pr0) / T;
-  const int N = band_key_hi(g, prlast) / T - t_lo + 1;
+  const TileSteps ksteps = row_steps(g, pr0, prlast, T);
+  const int N = ksteps.count();
+  const bool two = g.Rc > 0;  // shared-prefix plan: two visible key intervals per row
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxRing; ++s) {
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(kThr, 1)
       bool ok = true;
       const int nr = producer ? NR_P : NR_A;
       for (int n = 0; ok && n < N; ++n) {
-        const int j0 = (t_lo + n) * T;
+        const int j0 = ksteps.tile(n) * T;
         for (int c = 0; c < 2; ++c, ++issued) {
           const int s = issued % nr;
           if (issued >= nr && !mbar_wait_cl(&bars->ring_empty[s], ((issued / nr) & 1) ^ 1, abort_flag, R)) {
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(kThr, 1)
     bool ok = true;
     for (int n = 0; n < N; ++n) {
       const int bb = n & 1;
-      const int j0 = (t_lo + n) * T;
+      const int j0 = ksteps.tile(n) * T;
       if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full[bb], (n >> 1) & 1, abort_flag, R))) {
         ok = false;
         break;
@@ -492,11 +494,11 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free[bb]);  // the peer's relay tells the leader
-      const bool full = own_rows && (j0 >= band_key_lo(g, ihi)) && (j0 + T - 1 <= band_key_hi(g, i0));
+      const bool full = own_rows && rows_tile_full(g, i0, ihi, j0, j0 + T - 1);
       // visible key columns of row i in this tile, relative to this warpgroup's half
-      const int clo = band_key_lo(g, i) - j0 - cb0;
-      const int chi = band_key_hi(g, i) - j0 - cb0;
-      const float pmax = full ? half_max<true>(sr, sl2, clo, chi) : half_max<false>(sr, sl2, clo, chi);
+      const int4 vv = row_vis(g, i, j0 + cb0);
+      const float pmax = full ? half_max<true>(sr, sl2, vv)
+                              : (two ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
       xm[(bb * 2 + wg) * 128 + r] = pmax;
       mbar_arrive(&bars->mx[bb]);
       if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->mx[bb], (n >> 1) & 1, abort_flag, R))) {
@@ -511,7 +513,8 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       uint32_t pk[32];
-      const float tsum = full ? half_p<true>(sr, sl2, m_use, clo, chi, pk) : half_p<false>(sr, sl2, m_use, clo, chi, pk);
+      const float tsum = full ? half_p<true>(sr, sl2, m_use, vv, pk)
+                              : (two ? half_p<false, true>(sr, sl2, m_use, vv, pk) : half_p<false>(sr, sl2, m_use, vv, pk));
       l_run = l_run * alpha + tsum;
       // the store of this staging half two steps ago (and of that alpha) must have read it
       if (n >= 2 &&

@@ -123,3 +123,34 @@ def test_suffix_entry_points_check_arguments(lib):
     assert lib.swa_attn_bwd_workspace_bytes_ex(1, 8, 2, 4000, 4000, 128, 256, 1) == \
         lib.swa_attn_bwd_workspace_bytes(1, 8, 2, 4000, 128, 256)
     assert lib.swa_attn_fwd_workspace_bytes_ex(1, 8, 2, 5, 3, 128, 0, 1) == 0
+
+
+def test_prefix_entry_points_check_arguments(lib):
+    """The shared-prefix entry points reject plans out of range before any
+    CUDA call, and size their workspaces like the plain calls (the decode
+    kernel does not take a plan, so tiny shapes size the tensor-core path)."""
+    c = declared_codes()
+    P = ctypes.c_void_p
+
+    def fwd_px(L=64, D=64, W=0, prompt=20, chosen=10, q=0x1000):
+        return lib.swa_attn_fwd_prefix(P(q), P(0x2000), P(0x3000), P(0x4000), P(0x5000), 1, 2, 1, L, D, W, prompt,
+                                       chosen, ctypes.c_float(0.125), P(0x10000), 1 << 20, None)
+
+    assert fwd_px(prompt=-1) == c["SWA_ERR_BAD_PLAN"]
+    assert fwd_px(chosen=-3) == c["SWA_ERR_BAD_PLAN"]
+    assert fwd_px(prompt=40, chosen=25) == c["SWA_ERR_BAD_PLAN"]  # prompt + chosen > L
+    assert fwd_px(q=0) == c["SWA_ERR_NULL_POINTER"]
+    assert fwd_px(D=96) == c["SWA_ERR_BAD_HEAD_DIM"]
+    assert "prompt_len" in lib.swa_attn_strerror(c["SWA_ERR_BAD_PLAN"]).decode()
+    ptrs = [0x1000 * (i + 1) for i in range(9)]
+    rc = lib.swa_attn_bwd_prefix(*(P(p) for p in ptrs), 1, 2, 1, 64, 64, 0, 60, 5, ctypes.c_float(0.1),
+                                 P(0x10000), 1 << 20, None)
+    assert rc == c["SWA_ERR_BAD_PLAN"]
+    assert lib.swa_attn_bwd_workspace_bytes_prefix(1, 8, 2, 4000, 128, 256, 3000, 400) == \
+        lib.swa_attn_bwd_workspace_bytes(1, 8, 2, 4000, 128, 256)
+    assert lib.swa_attn_fwd_workspace_bytes_prefix(1, 8, 2, 4000, 128, 256, 3000, 400) == \
+        lib.swa_attn_fwd_workspace_bytes(1, 8, 2, 4000, 128, 256)
+    assert lib.swa_attn_fwd_workspace_bytes_prefix(1, 8, 2, 100, 128, 0, 90, 20) == 0
+    # two query rows per kv head: the plain call takes the decode kernel, the
+    # plan the tensor-core path with its fp16 copy of v
+    assert lib.swa_attn_fwd_workspace_bytes_prefix(1, 2, 1, 8, 64, 0, 3, 2) >= 8 * 64 * 2

@@ -554,3 +554,85 @@ def test_d512_backwards_overlap_on_two_streams():
     for _, ref, outs, _ in runs:
         for a, b, n in zip(outs, ref, ("dq", "dk", "dv")):
             assert torch.equal(a, b), n
+
+
+# ---------------------------------------------------------------------------
+# shared prompt prefix: one pass over [prompt; chosen; rejected] with the
+# mask "causal AND NOT rejected->chosen" and a window on logical positions
+# ("Training -- design (ORPO, flash-CCE head, prefix sharing, segmented
+# backward)", section 5.4 "Shared prompt-prefix forward")
+
+PREFIX = [
+    # B, Hq, Hkv, P, Rc, Rr, D, window
+    (1, 2, 1, 300, 150, 200, 64, 0),
+    (1, 4, 2, 257, 60, 190, 128, 100),   # chosen shorter than a tile: prompt, chosen and rejected keys share tiles
+    (2, 2, 1, 0, 130, 140, 64, 50),      # no prompt: rejected rows see only their own response
+    (1, 8, 2, 1000, 300, 400, 128, 0),
+    (1, 4, 2, 500, 200, 300, 128, 256),
+    (1, 2, 1, 200, 100, 150, 256, 0),
+    (1, 4, 2, 333, 77, 210, 256, 129),
+    (1, 2, 1, 300, 130, 270, 512, 0),
+    (1, 4, 1, 260, 40, 300, 512, 200),
+    (1, 2, 2, 700, 5, 3, 128, 64),       # three rejected rows, five chosen
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,P,Rc,Rr,D,window", PREFIX)
+def test_prefix_plan_elementwise(oracle_mod, B, Hq, Hkv, P, Rc, Rr, D, window):
+    import sliding_window_attention_gb300 as swa
+
+    L = P + Rc + Rr
+    q, k, v, dO = make_inputs(B, Hq, Hkv, L, D, seed=6000 + L + D + window)
+    scale = 1.0 / math.sqrt(D)
+    ref = oracle_mod.backward(q, k, v, dO, window, scale, band_only=True, prefix=(P, Rc))
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, dO))
+    o, lse = swa.forward(qd, kd, vd, window, scale, prefix=(P, Rc))
+    dq, dk, dv = swa.backward(qd, kd, vd, o, lse, gd, window, scale, prefix=(P, Rc))
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    assert_lse_close(lse.cpu().numpy(), ref["lse"])
+    got = dict(o=o, dq=dq, dk=dk, dv=dv)
+    for n in ("o", "dq", "dk", "dv"):
+        assert_close(n, got[n].cpu().numpy(), ref[n])
+
+
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_prefix_plan_exact_zeros_and_deterministic(D):
+    """dO only on the rejected rows: the chosen keys' dk and dv are exactly
+    zero (no rejected row sees them), dq is exactly zero on every other row,
+    and two runs agree bit for bit."""
+    import sliding_window_attention_gb300 as swa
+
+    P, Rc, Rr, W = 260, 150, 200, 0
+    L = P + Rc + Rr
+    q, k, v, dO = (t.cuda() for t in make_inputs(1, 4, 2, L, D, seed=6100 + D))
+    dO[:, :, :P + Rc] = 0
+    scale = 1.0 / math.sqrt(D)
+    runs = []
+    for _ in range(2):
+        o, lse = swa.forward(q, k, v, W, scale, prefix=(P, Rc))
+        runs.append((o, lse) + swa.backward(q, k, v, o, lse, dO, W, scale, prefix=(P, Rc)))
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    o, lse, dq, dk, dv = runs[0]
+    assert (dk[:, :, P:P + Rc] == 0).all() and (dv[:, :, P:P + Rc] == 0).all()
+    assert (dq[:, :, :P + Rc] == 0).all()
+    assert dk[:, :, :P].abs().max() > 0 and dv[:, :, P + Rc:].abs().max() > 0
+    for a, b in zip(runs[0], runs[1]):
+        assert torch.equal(a, b)
+
+
+def test_prefix_degenerate_plan_is_the_plain_call():
+    """A plan without a chosen response runs the plain causal window."""
+    import sliding_window_attention_gb300 as swa
+
+    B, Hq, Hkv, L, D, W = 1, 4, 2, 500, 128, 100
+    q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, L, D, seed=6200))
+    o, lse = swa.forward(q, k, v, W, 0.1)
+    o2, lse2 = swa.forward(q, k, v, W, 0.1, prefix=(300, 0))
+    a = swa.backward(q, k, v, o, lse, dO, W, 0.1)
+    b = swa.backward(q, k, v, o2, lse2, dO, W, 0.1, prefix=(300, 0))
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
