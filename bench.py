@@ -236,9 +236,22 @@ def _sample_q_rows(w, Ls):
     return Ls if w.q_rows == w.L else max(1, round(Ls * w.q_rows / w.L))
 
 
-def _sample_pairs(w, Ls):
-    from sliding_window_attention_gb300.inputs import band_pairs, band_pairs_ex
+def _sample_prefix(w, Ls):
+    """The shared-prefix plan of an oracle sample over the first Ls tokens:
+    the workload's prompt and chosen lengths scaled by Ls / L (None without
+    a plan)."""
+    if not w.prefix:
+        return None
+    P = round(w.prompt_len * Ls / w.L)
+    Rc = min(Ls - P, round(w.chosen_len * Ls / w.L))
+    return P, Rc
 
+
+def _sample_pairs(w, Ls):
+    from sliding_window_attention_gb300.inputs import band_pairs, band_pairs_ex, band_pairs_prefix
+
+    if w.prefix:
+        return band_pairs_prefix(Ls, w.window, *_sample_prefix(w, Ls))
     if w.q_rows == w.L and w.causal:
         return band_pairs(Ls, w.window)
     return band_pairs_ex(_sample_q_rows(w, Ls), Ls, w.window, w.causal)
@@ -263,10 +276,11 @@ def oracle_sample_seconds(w, Ls, inputs=None):
 
     q, k, v, dO = inputs if inputs is not None else _oracle_sample_inputs(w, Ls)
     t0 = time.perf_counter()
+    plan = _sample_prefix(w, q.shape[2])
     if w.fwd_only:
-        oracle.forward(q, k, v, w.window, w.scale, band_only=True, causal=w.causal)
+        oracle.forward(q, k, v, w.window, w.scale, band_only=True, causal=w.causal, prefix=plan)
     else:
-        oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True, causal=w.causal)
+        oracle.backward(q, k, v, dO, w.window, w.scale, band_only=True, causal=w.causal, prefix=plan)
     return time.perf_counter() - t0
 
 
@@ -371,6 +385,9 @@ def _variant_keys(w):
         out["causal"] = False
     if w.fwd_only:
         out["step"] = "forward only (decode)"
+    if w.prefix:
+        out["prompt_len"], out["chosen_len"] = w.prefix
+        out["rejected_len"] = w.L - sum(w.prefix)
     return out
 
 
@@ -482,7 +499,11 @@ def measure_workload(args, w, world, rank, local_rank, dist, peaks):
         dq = torch.empty((B, Hq, Lq, D), **f32)
         dk = torch.empty((B, Hkv, L, D), **f32)
         dv = torch.empty((B, Hkv, L, D), **f32)
-    if variant:
+    plan = w.prefix
+    if plan:
+        fws_b = swa.fwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, W, *plan)
+        bws_b = swa.bwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, W, *plan)
+    elif variant:
         fws_b = swa.fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
         bws_b = 0 if w.fwd_only else swa.bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, L, D, W, w.causal)
     else:
@@ -499,6 +520,13 @@ def measure_workload(args, w, world, rank, local_rank, dist, peaks):
         # `after_fwd`: called on the host between the two calls
         if w.fwd_only:
             swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
+        elif plan:
+            swa.swa_attn_fwd_prefix(q, k, v, o, lse, W, plan[0], plan[1], w.scale, fws, stream)
+            if mid is not None:
+                mid.record(stream)
+            if after_fwd is not None:
+                after_fwd()
+            swa.swa_attn_bwd_prefix(q, k, v, o, lse, dO, dq, dk, dv, W, plan[0], plan[1], w.scale, bws, stream)
         elif variant:
             swa.swa_attn_fwd_ex(q, k, v, o, lse, W, w.causal, w.scale, fws, stream)
             if mid is not None:

@@ -27,6 +27,12 @@ suffix workload draws the full-length tensors with the recipe above and keeps
 the last Lq rows of q and dO.  The decode workload is one generation step
 (Lq = 1, forward only) of a batch of 8 over a 16,384-token cache of the
 global layer.
+
+The shared-prefix workload is the sliding layer over one preference pair
+laid out as [prompt (6,144 tokens); chosen response (1,024); rejected
+response (1,024)], the single-pass layout of "Training -- design (ORPO,
+flash-CCE head, prefix sharing, segmented backward)", section 5.4, with the
+window on logical positions.
 """
 from __future__ import annotations
 
@@ -52,6 +58,13 @@ class Workload:
     Lq: int = 0          # query rows (the last Lq of the L key positions); 0 means L
     causal: bool = True
     fwd_only: bool = False  # a decode step: the forward alone
+    prompt_len: int = 0  # shared-prefix plan [prompt; chosen; rejected] when chosen_len > 0
+    chosen_len: int = 0
+
+    @property
+    def prefix(self):
+        """(prompt_len, chosen_len) of a shared-prefix plan, or None."""
+        return (self.prompt_len, self.chosen_len) if self.chosen_len > 0 else None
 
     @property
     def q_rows(self) -> int:
@@ -63,6 +76,8 @@ class Workload:
 
     def pairs(self) -> int:
         """In-band (query, key) pairs over all batches and query heads."""
+        if self.prefix:
+            return self.B * self.Hq * band_pairs_prefix(self.L, self.window, *self.prefix)
         if self.q_rows == self.L and self.causal:
             return self.B * self.Hq * band_pairs(self.L, self.window)
         return self.B * self.Hq * band_pairs_ex(self.q_rows, self.L, self.window, self.causal)
@@ -97,6 +112,23 @@ def band_pairs_ex(Lq: int, Lk: int, window: int, causal: bool) -> int:
     return total
 
 
+def band_pairs_prefix(L: int, window: int, P: int, Rc: int) -> int:
+    """In-band pairs of one [prompt (P); chosen (Rc); rejected (L - P - Rc)]
+    sequence under the shared-prefix mask: rows before the rejected response
+    see the plain causal window; a rejected row i (logical position i - Rc)
+    sees the prompt keys within the window of its logical position and the
+    keys of its own response within the window."""
+    w = window if 0 < window < L else 0
+    R = P + Rc
+    total = band_pairs(R, w) if R > 0 else 0
+    for i in range(R, L):
+        a = i - Rc
+        lo = max(0, a - w + 1) if w else 0
+        total += max(0, P - lo)                      # prompt keys [lo, P - 1]
+        total += i - (max(R, i - w + 1) if w else R) + 1  # own response keys
+    return total
+
+
 WORKLOADS = {
     w.name: w
     for w in [
@@ -110,6 +142,8 @@ WORKLOADS = {
                  Lq=2048),
         Workload("noncausal_l8192_d128_w512", 1, 8, 4, 8192, 128, 512, seed=20260007, causal=False),
         Workload("decode_b8_q1_k16384_d512", 8, 32, 4, 16384, 512, 0, seed=20260008, Lq=1, fwd_only=True),
+        Workload("prefix_p6144_c1024_r1024_d256_w1024", 1, 32, 16, 8192, 256, 1024, do_scale=0.1, seed=20260009,
+                 prompt_len=6144, chosen_len=1024),
     ]
 }
 

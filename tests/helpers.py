@@ -35,15 +35,16 @@ def assert_lse_close(got, ref, tol=LSE_ABS):
     return ma
 
 
-def gpu_fwd_bwd(q, k, v, dO, window, scale, device="cuda:0", causal=True):
-    """Run forward and backward through the C ABI; return CPU fp32 tensors."""
+def gpu_fwd_bwd(q, k, v, dO, window, scale, device="cuda:0", causal=True, prefix=None):
+    """Run forward and backward through the C ABI; return CPU fp32 tensors.
+    prefix=(prompt_len, chosen_len) selects the shared-prefix entry points."""
     import torch
 
     import sliding_window_attention_gb300 as swa
 
     qd, kd, vd, gd = (t.to(device) for t in (q, k, v, dO))
-    o, lse = swa.forward(qd, kd, vd, window, scale, causal=causal)
-    dq, dk, dv = swa.backward(qd, kd, vd, o, lse, gd, window, scale, causal=causal)
+    o, lse = swa.forward(qd, kd, vd, window, scale, causal=causal, prefix=prefix)
+    dq, dk, dv = swa.backward(qd, kd, vd, o, lse, gd, window, scale, causal=causal, prefix=prefix)
     torch.cuda.synchronize()
     status = swa.swa_attn_get_status()
     assert status == 0, f"device status {status}"

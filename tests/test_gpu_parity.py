@@ -91,7 +91,7 @@ def _sample_keys(w, rng):
 def full_run(request):
     w = WORKLOADS[request.param]
     q, k, v, dO = workload_inputs(w)
-    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale, causal=w.causal)
+    got = gpu_fwd_bwd(q, k, v, dO, w.window, w.scale, causal=w.causal, prefix=w.prefix)
     return w, (q, k, v, dO), got
 
 
@@ -115,6 +115,9 @@ def test_full_workload_sampled(oracle_mod, full_run):
         assert torch.isfinite(got[name]).all(), name
     heads = sorted({0, w.Hq - 1, G, w.Hq // 2})
     rows = _sample_rows(w.q_rows, w.window, rng)
+    if w.prefix:  # both sides of the prompt / chosen / rejected boundaries
+        P, Rc = w.prefix
+        rows = sorted(set(rows) | {P - 1, P, P + Rc - 1, P + Rc, P + Rc + 1})
     worst = {}
 
     def keep(name, ma_rf):
@@ -123,13 +126,18 @@ def test_full_workload_sampled(oracle_mod, full_run):
         worst[name] = (max(a, ma), max(r, rf))
 
     for h in heads:
-        r = oracle_mod.rows(q, k, v, dO, w.window, w.scale, 0, h, rows, band_only=True, causal=w.causal)
+        r = oracle_mod.rows(q, k, v, dO, w.window, w.scale, 0, h, rows, band_only=True, causal=w.causal,
+                            prefix=w.prefix)
         keep("lse", assert_lse_close(got["lse"][0, h, rows].numpy(), r["lse"]))
         keep("o", assert_close(f"o[h={h}]", got["o"][0, h, rows].numpy(), r["o"]))
         keep("dq", assert_close(f"dq[h={h}]", got["dq"][0, h, rows].numpy(), r["dq"]))
     keys = _sample_keys(w, rng)
+    if w.prefix:
+        P, Rc = w.prefix
+        keys = sorted(set(keys) | {P - 1, P, P + Rc - 1, P + Rc})
     for kvh in sorted({0, w.Hkv - 1}):
-        r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True, causal=w.causal)
+        r = oracle_mod.key_rows(q, k, v, dO, w.window, w.scale, 0, kvh, keys, band_only=True, causal=w.causal,
+                                prefix=w.prefix)
         keep("dk", assert_close(f"dk[kvh={kvh}]", got["dk"][0, kvh, keys].numpy(), r["dk"]))
         keep("dv", assert_close(f"dv[kvh={kvh}]", got["dv"][0, kvh, keys].numpy(), r["dv"]))
     _log_errors(w.name, "sampled rows and keys",

@@ -157,3 +157,32 @@ def test_split_record_backward_at_10d():
     s = bench.split_record(w, 0.375, 1.38, peaks)
     assert abs(s["bwd"]["pct_bf16_peak_10d"] - 100 * w.bwd_flops() / 1.38e9 / 1897.1) < 0.01
     assert abs(s["fwd"]["tflops"] - w.fwd_flops() / 0.375e9) < 0.01
+
+
+def test_prefix_pair_count_brute_force():
+    """band_pairs_prefix counts the pairs the shared-prefix mask keeps
+    (causal AND NOT rejected->chosen, window on logical positions), checked
+    by enumerating every (row, key) on small sequences."""
+    import itertools
+
+    from sliding_window_attention_gb300.inputs import band_pairs_prefix
+
+    def brute(L, W, P, Rc):
+        R = P + Rc
+        lp = lambda x: x - Rc if x >= R else x  # noqa: E731
+        return sum(1 for i in range(L) for j in range(i + 1)
+                   if not (i >= R and P <= j < R) and not (W and W < L and lp(i) - lp(j) >= W))
+
+    for L, W, P, Rc in itertools.product([1, 9, 40], [0, 1, 3, 7, 50], [0, 2, 5], [0, 1, 4]):
+        if P + Rc <= L:
+            assert band_pairs_prefix(L, W, P, Rc) == brute(L, W, P, Rc), (L, W, P, Rc)
+
+
+def test_prefix_sample_plan_scales_with_the_sample():
+    import bench
+    from sliding_window_attention_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS["prefix_p6144_c1024_r1024_d256_w1024"]
+    assert bench._sample_prefix(w, w.L) == (6144, 1024)
+    P, Rc = bench._sample_prefix(w, 1024)
+    assert (P, Rc) == (768, 128) and bench._sample_pairs(w, 1024) > 0
