@@ -1142,6 +1142,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key columns of this warpgroup: cb0 .. cb0 + CW - 1 of each step
     const int cb0 = wg * CW;
     bool ok = true;
+    // loop invariants: this row's band, and the bounds every row of the tile shares
+    const int4 vrow = row_vis(g, i, 0);
+    const int lo_all = band_key_lo(g, ihi), hi_all = band_key_hi(g, i0);
     for (int n = 0; n < nt; ++n) {
       const int j0 = ksteps.tile(n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full, n & 1, abort_flag))) { ok = false; break; }
@@ -1152,9 +1155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(sdp_read);  // S may be overwritten; dP once both warpgroups have read it
-      const bool full = rows_tile_full(g, i0, ihi, j0, j0 + BN - 1);
+      const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
       // key columns c of this tile visible to row i: j0 + c in the row's band
-      const int4 vv = row_vis(g, i, j0);
+      const int4 vv = vshift(vrow, j0);
       uint32_t dd[CW / 2];
       if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
       else if (two) dq_chunk<false, true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
@@ -1395,13 +1398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 : make_float2(0.f, 0.f);
     const int cw0 = wg * CW;
     bool ok = true;
+    // loop invariants: this row's band, and the bounds every row of the tile shares
+    const int4 vrow = row_vis(g, i, 0);
+    const int lo_all = band_key_lo(g, ihi), hi_all = band_key_hi(g, i0);
     for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
       const int j0 = ksteps.tile(n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = rows_tile_full(g, i0, ihi, j0, j0 + BN - 1);
-      const int4 vv = row_vis(g, i, j0);  // visible key columns of row i
+      const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
+      const int4 vv = vshift(vrow, j0);  // visible key columns of row i
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {

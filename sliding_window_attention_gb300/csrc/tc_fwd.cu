@@ -317,12 +317,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const float sl2 = g.scale * kLog2e;
     float m_run = -INFINITY;
     bool ok = true;
+    // loop invariants: this row's band, and the bounds every row of the tile shares
+    const int4 vrow = row_vis(g, i, 0);
+    const int lo_all = band_key_lo(g, ihi), hi_all = band_key_hi(g, i0);
     for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
       const int j0 = steps.tile(n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = rows_tile_full(g, i0, ihi, j0, j0 + BN - 1);
+      const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
       // the whole S row in registers: all loads issued, then one wait
       uint32_t sr[BN];
 #pragma unroll
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
       tmem_wait_ld();
       // Visible key columns of this row inside the tile (edge tiles only).
-      const int4 vv = row_vis(g, i, j0);
+      const int4 vv = vshift(vrow, j0);
       const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, vv)
                               : (two ? softmax_tile_max<BN, false, true>(sr, sl2, vv)
                                      : softmax_tile_max<BN, false>(sr, sl2, vv));
@@ -658,12 +661,15 @@ __global__ void __launch_bounds__(320, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     const int cnt = stw.count();  // key tiles of this query tile (0 for a missing tile B)
+    const int4 vrow = row_vis(g, i, 0);
+    const int lo_all = band_key_lo(g, ihiw), hi_all = band_key_hi(g, i0w);
     for (int k = 0; k < cnt; ++k) {
       const int j0 = stw.tile(k) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + w, k & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
-      const bool full = rows_tile_full(g, i0w, ihiw, j0, j0 + BN - 1);
-      const int4 vv = row_vis(g, i, j0);
+      const bool full = two ? rows_tile_full(g, i0w, ihiw, j0, j0 + BN - 1)
+                            : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
+      const int4 vv = vshift(vrow, j0);
       // the row in two 64-column halves (registers stay below the spill
       // limit): first the maximum, then P; half h's packed P lands on columns
       // [32 h, 32 h + 32), which half h has already read
