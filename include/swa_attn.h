@@ -178,6 +178,30 @@ int swa_attn_bwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v,
                         size_t workspace_bytes, void* stream);
 
 /*
+ * Sequence sharding (context parallelism) with a halo: a sequence split into
+ * contiguous chunks, one per rank, runs each chunk's queries over [halo;
+ * own keys] through swa_attn_fwd_ex / swa_attn_bwd_ex (queries a suffix of
+ * the keys).  The halo is the keys of earlier chunks that the chunk's
+ * windows reach: the W - 1 keys before the chunk for a causal window W, all
+ * earlier keys without a window.  This follows from the band structure
+ * ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself", "What I
+ * changed, in plain terms" items 3-4: a query only meets keys within the
+ * window behind it); the pages do not describe the sharding itself.  The
+ * backward of a chunk then holds dK / dV rows for halo keys that another rank
+ * owns; that rank adds them into its own rows with this call:
+ *
+ *   dst[bh, row0 + r, d] += src[bh, r, d]   for bh < BH, r < nrows, d < D
+ *
+ * dst is [BH, dst_rows, D] fp32 (a rank's dk or dv, BH = B * Hkv), src is
+ * [BH, nrows, D] fp32 (the halo rows received); device pointers, 16-byte
+ * aligned, D a multiple of 4, 0 <= row0 and row0 + nrows <= dst_rows.
+ * Asynchronous on `stream`.  Returns SWA_OK, SWA_ERR_NULL_POINTER,
+ * SWA_ERR_BAD_SHAPE, SWA_ERR_MISALIGNED or SWA_ERR_CUDA.
+ */
+int swa_attn_add_rows_f32(float* dst, const float* src, int BH, int dst_rows, int row0, int nrows, int D,
+                          void* stream);
+
+/*
  * Forward.  Reads q [B,Hq,L,D], k and v [B,Hkv,L,D] (bf16); writes
  * o [B,Hq,L,D] (fp32, normalised attention output) and lse [B,Hq,L] (fp32,
  * natural-log sum over the band of exp(scale * q_i . k_j)).  The forward

@@ -34,6 +34,7 @@ EXPORTED = (
     "swa_attn_bwd_workspace_bytes_prefix",
     "swa_attn_fwd_prefix",
     "swa_attn_bwd_prefix",
+    "swa_attn_add_rows_f32",
 )
 
 _lock = threading.Lock()
@@ -100,6 +101,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.swa_attn_fwd_prefix.restype = I
         lib.swa_attn_bwd_prefix.argtypes = [P, P, P, P, P, P, P, P, P] + shape_px + [F, P, Z, P]
         lib.swa_attn_bwd_prefix.restype = I
+        lib.swa_attn_add_rows_f32.argtypes = [P, P, I, I, I, I, I, P]
+        lib.swa_attn_add_rows_f32.restype = I
         _lib = lib
         return lib
 
@@ -223,6 +226,18 @@ def swa_attn_bwd_prefix(q, k, v, o, lse, dO, dq, dk, dv, window: int, prompt_len
                                     float(scale), _ptr(workspace), nbytes, _stream_ptr(stream))
     if rc:
         raise SwaError(rc, "swa_attn_bwd_prefix")
+
+
+def swa_attn_add_rows_f32(dst, src, row0: int, stream=None) -> None:
+    """dst[:, :, row0 : row0 + n] += src through the C ABI, for fp32 CUDA
+    tensors dst [B, H, dst_rows, D] and src [B, H, n, D] (contiguous)."""
+    B, H, dst_rows, D = dst.shape
+    n = src.shape[2]
+    if tuple(src.shape) != (B, H, n, D) or not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("src must be a contiguous [B, H, n, D] block of dst's heads")
+    rc = load().swa_attn_add_rows_f32(_ptr(dst), _ptr(src), B * H, dst_rows, int(row0), n, D, _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_add_rows_f32")
 
 
 def swa_attn_fwd(q, k, v, o, lse, window: int, scale: float, workspace=None, stream=None) -> None:
