@@ -102,6 +102,20 @@ __host__ __device__ __forceinline__ int4 key_vis(const Geom& g, int j, int c0) {
 __host__ __device__ __forceinline__ int4 vshift(const int4& v, int d) {
   return make_int4(v.x - d, v.y - d, v.z - d, v.w - d);
 }
+// The visible columns of one row in a tile of T columns, in tile-local
+// coordinates: when only one of the two intervals meets the tile it moves to
+// the first slot (the second is emptied), and *both says whether both meet
+// it (under a shared-prefix plan only where the gap between them falls inside
+// the tile).  A row that sees nothing of the tile gets an empty first slot.
+__host__ __device__ __forceinline__ int4 vis_in_tile(const int4& v, int T, bool* both) {
+  const bool a = v.x <= v.y && v.y >= 0 && v.x < T;
+  const bool b = v.z <= v.w && v.w >= 0 && v.z < T;
+  *both = a && b;
+  if (a && b) return v;
+  if (b) return make_int4(v.z, v.w, 1, 0);
+  if (a) return make_int4(v.x, v.y, 1, 0);
+  return make_int4(1, 0, 1, 0);
+}
 // Column c of a masked tile is visible: in [v.x, v.y], or (TWO: a plan is
 // active) in [v.z, v.w].
 template <bool TWO>

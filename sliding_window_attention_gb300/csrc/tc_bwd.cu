@@ -500,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (full) {
         kv_p64<true>(sv, lv, sl2, cw0, make_int4(0, 0, 0, 0));
       } else if constexpr (two) {
-        kv_p64<false, true>(sv, lv, sl2, cw0, vshift(vj, i0));
+        bool both;
+        const int4 vq = vis_in_tile(vshift(vj, i0), BM, &both);
+        if (__any_sync(0xffffffffu, both)) kv_p64<false, true>(sv, lv, sl2, cw0, vq);
+        else kv_p64<false>(sv, lv, sl2, cw0, vq);
       } else {
         kv_p64<false>(sv, lv, sl2, cw0, make_int4(qlo_j - i0, qhi_j - i0, 1, 0));
       }
@@ -871,7 +874,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (full) {
         kv_p64<true>(sv, lv, sl2, cw0, make_int4(0, 0, 0, 0));
       } else if constexpr (two) {
-        kv_p64<false, true>(sv, lv, sl2, cw0, vshift(vj, i0));
+        bool both;
+        const int4 vq = vis_in_tile(vshift(vj, i0), BM, &both);
+        if (__any_sync(0xffffffffu, both)) kv_p64<false, true>(sv, lv, sl2, cw0, vq);
+        else kv_p64<false>(sv, lv, sl2, cw0, vq);
       } else {
         kv_p64<false>(sv, lv, sl2, cw0, make_int4(qlo_j - i0, qhi_j - i0, 1, 0));
       }
@@ -1157,10 +1163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(sdp_read);  // S may be overwritten; dP once both warpgroups have read it
       const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
       // key columns c of this tile visible to row i: j0 + c in the row's band
-      const int4 vv = vshift(vrow, j0);
+      bool both;
+      const int4 vv = vis_in_tile(vshift(vrow, j0), BN, &both);
+      const bool two_here = two && __any_sync(0xffffffffu, both);
       uint32_t dd[CW / 2];
       if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
-      else if (two) dq_chunk<false, true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
+      else if (two_here) dq_chunk<false, true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
       else dq_chunk<false>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
       // dS of keys cb0 .. cb0 + 31 goes to columns cb0 / 2 .. of the dP
       // buffer, which the other warpgroup may still be reading
@@ -1407,7 +1415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
-      const int4 vv = vshift(vrow, j0);  // visible key columns of row i
+      bool both;
+      const int4 vv = vis_in_tile(vshift(vrow, j0), BN, &both);  // visible key columns of row i
+      const bool two_here = two && __any_sync(0xffffffffu, both);
       uint32_t sv[CW], dv[CW];
 #pragma unroll
       for (int c = 0; c < CW / 32; ++c) {
@@ -1426,7 +1436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cb = cw0 + c * 32;
         uint32_t dd[16];
         if (full) dq_chunk<true>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
-        else if (two) dq_chunk<false, true>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
+        else if (two_here) dq_chunk<false, true>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
         else dq_chunk<false>(svc, dvc, sl2, rs.x, rs.y, cb, vv, dd);
         tmem_st16(tmem + lane_off + C::S_COL + sb * BN + cb / 2, dd);
       }

@@ -637,8 +637,11 @@ __global__ void __launch_bounds__(kThr, 1)
         ok = false;
         break;
       }
+      bool both;
+      vv = vis_in_tile(vv, T, &both);
+      const bool two_here = two && __any_sync(0xffffffffu, both);
       if (full) p_tile64<true, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
-      else if (two) p_tile64<false, DIR == kDirKV, true>(sv, lse_s, rs_row.x, sl2, cb0, vv);
+      else if (two_here) p_tile64<false, DIR == kDirKV, true>(sv, lse_s, rs_row.x, sl2, cb0, vv);
       else p_tile64<false, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
       uint32_t o[32];
       if (DIR == kDirKV) {

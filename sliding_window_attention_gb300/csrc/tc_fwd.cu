@@ -332,11 +332,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int c = 0; c < BN / 32; ++c)
         tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
       tmem_wait_ld();
-      // Visible key columns of this row inside the tile (edge tiles only).
-      const int4 vv = vshift(vrow, j0);
+      // Visible key columns of this row inside the tile (edge tiles only);
+      // the two-interval mask only where a row of the warp needs it
+      bool both;
+      const int4 vv = vis_in_tile(vshift(vrow, j0), BN, &both);
+      const bool two_here = two && __any_sync(0xffffffffu, both);
       const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, vv)
-                              : (two ? softmax_tile_max<BN, false, true>(sr, sl2, vv)
-                                     : softmax_tile_max<BN, false>(sr, sl2, vv));
+                              : (two_here ? softmax_tile_max<BN, false, true>(sr, sl2, vv)
+                                          : softmax_tile_max<BN, false>(sr, sl2, vv));
       float alpha = 1.f;
       bool rescale = false;
       if (tmax > m_run + kRescaleLog2) {
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint32_t p_taddr = tmem + lane_off + C::S_COL + sb * BN;
       if (full) softmax_tile_p<BN, true, false>(sr, sl2, m_use, vv, p_taddr);
-      else if (two) softmax_tile_p<BN, false, false, true>(sr, sl2, m_use, vv, p_taddr);
+      else if (two_here) softmax_tile_p<BN, false, false, true>(sr, sl2, m_use, vv, p_taddr);
       else softmax_tile_p<BN, false, false>(sr, sl2, m_use, vv, p_taddr);
       // Wait for PV(n-1) at every tile, not only when rescaling: this thread then
       // has observed every earlier PV completion, so the o_done phase can be at
@@ -680,10 +683,12 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_off + s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(sr));
         tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
-        const int4 vh = vshift(vv, 64 * hf);
+        bool both;
+        const int4 vh = vis_in_tile(vshift(vv, 64 * hf), 64, &both);
+        const bool two_here = two && __any_sync(0xffffffffu, both);
         tmax = fmaxf(tmax, full ? softmax_tile_max<64, true>(sr, sl2, vh)
-                                : (two ? softmax_tile_max<64, false, true>(sr, sl2, vh)
-                                       : softmax_tile_max<64, false>(sr, sl2, vh)));
+                                : (two_here ? softmax_tile_max<64, false, true>(sr, sl2, vh)
+                                            : softmax_tile_max<64, false>(sr, sl2, vh)));
       }
       float alpha = 1.f;
       bool rescale = false;
@@ -703,10 +708,12 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
         const uint32_t p_taddr = tmem + lane_off + s_col + 32 * hf;
-        const int4 vh = vshift(vv, 64 * hf);
+        bool both;
+        const int4 vh = vis_in_tile(vshift(vv, 64 * hf), 64, &both);
+        const bool two_here = two && __any_sync(0xffffffffu, both);
         tsum += full ? softmax_tile_p<64, true, true>(sr, sl2, m_use, vh, p_taddr)
-                     : (two ? softmax_tile_p<64, false, true, true>(sr, sl2, m_use, vh, p_taddr)
-                            : softmax_tile_p<64, false, true>(sr, sl2, m_use, vh, p_taddr));
+                     : (two_here ? softmax_tile_p<64, false, true, true>(sr, sl2, m_use, vh, p_taddr)
+                                 : softmax_tile_p<64, false, true>(sr, sl2, m_use, vh, p_taddr));
       }
       l_run = l_run * alpha + tsum;
       // PV_w(k - 1) must be complete before O is rescaled (waited for at every

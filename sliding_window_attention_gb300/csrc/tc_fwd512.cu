@@ -496,9 +496,11 @@ __global__ void __launch_bounds__(kThr, 1)
       if (lane == 0) mbar_arrive(&bars->s_free[bb]);  // the peer's relay tells the leader
       const bool full = own_rows && rows_tile_full(g, i0, ihi, j0, j0 + T - 1);
       // visible key columns of row i in this tile, relative to this warpgroup's half
-      const int4 vv = row_vis(g, i, j0 + cb0);
+      bool both;
+      const int4 vv = vis_in_tile(row_vis(g, i, j0 + cb0), 64, &both);
+      const bool two_here = two && __any_sync(0xffffffffu, both);
       const float pmax = full ? half_max<true>(sr, sl2, vv)
-                              : (two ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
+                              : (two_here ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
       xm[(bb * 2 + wg) * 128 + r] = pmax;
       mbar_arrive(&bars->mx[bb]);
       if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->mx[bb], (n >> 1) & 1, abort_flag, R))) {
@@ -514,7 +516,8 @@ __global__ void __launch_bounds__(kThr, 1)
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       uint32_t pk[32];
       const float tsum = full ? half_p<true>(sr, sl2, m_use, vv, pk)
-                              : (two ? half_p<false, true>(sr, sl2, m_use, vv, pk) : half_p<false>(sr, sl2, m_use, vv, pk));
+                              : (two_here ? half_p<false, true>(sr, sl2, m_use, vv, pk)
+                                          : half_p<false>(sr, sl2, m_use, vv, pk));
       l_run = l_run * alpha + tsum;
       // the store of this staging half two steps ago (and of that alpha) must have read it
       if (n >= 2 &&
