@@ -984,7 +984,9 @@ struct DqCfg {
   static_assert(D == 256, "head dim 256 only (dQ fills the columns below Q, S and dP)");
 };
 
-template <int D>
+// TWO: a shared-prefix plan is active (a row may see two key intervals); a
+// separate instantiation keeps the plain kernel's code.
+template <int D, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
@@ -1019,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // key tiles meeting the band of rows i0 .. ihi (never empty)
   const TileSteps ksteps = row_steps(g, i0, ihi, BN);
   const int nt = ksteps.count();
-  const bool two = g.Rc > 0;  // shared-prefix plan: a row may see two key intervals
+  constexpr bool two = TWO;  // shared-prefix plan: a row may see two key intervals
 
   if (threadIdx.x == 0) {
     mbar_init(g_full, 1);
@@ -1055,7 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
-        const int j0 = ksteps.tile(n) * BN;
+        const int j0 = (two ? ksteps.tile(n) : ksteps.lo0 + n) * BN;
         if (n >= NS && !mbar_wait(kv_empty + st, ((n / NS) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(kv_full + st, 2 * C::KV_BYTES);
         // all KCH 64-column chunks of the BN rows in one instruction each
@@ -1152,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int4 vrow = row_vis(g, i, 0);
     const int lo_all = band_key_lo(g, ihi), hi_all = band_key_hi(g, i0);
     for (int n = 0; n < nt; ++n) {
-      const int j0 = ksteps.tile(n) * BN;
+      const int j0 = (two ? ksteps.tile(n) : ksteps.lo0 + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full, n & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[CW], dv[CW];
@@ -1163,8 +1165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(sdp_read);  // S may be overwritten; dP once both warpgroups have read it
       const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
       // key columns c of this tile visible to row i: j0 + c in the row's band
-      bool both;
-      const int4 vv = vis_in_tile(vshift(vrow, j0), BN, &both);
+      bool both = false;
+      const int4 vv = two ? vis_in_tile(vshift(vrow, j0), BN, &both) : vshift(vrow, j0);
       const bool two_here = two && __any_sync(0xffffffffu, both);
       uint32_t dd[CW / 2];
       if (full) dq_chunk<true>(sv, dv, sl2, rs.x, rs.y, cb0, vv, dd);
@@ -1237,7 +1239,9 @@ struct Dq128Cfg {
   static_assert(D <= 128, "dQ below the S buffers");
 };
 
-template <int D>
+// TWO: a shared-prefix plan is active (a row may see two key intervals); a
+// separate instantiation keeps the plain kernel's code.
+template <int D, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     dq128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -1275,7 +1279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // key tiles meeting the band of rows i0 .. ihi (never empty)
   const TileSteps ksteps = row_steps(g, i0, ihi, BN);
   const int nt = ksteps.count();
-  const bool two = g.Rc > 0;  // shared-prefix plan: a row may see two key intervals
+  constexpr bool two = TWO;  // shared-prefix plan: a row may see two key intervals
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -1320,7 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K and V of each step, each ring refilled as soon as its slot is released
       int nk = 0, nv = 0;
       for (int n = 0; n < nt; ++n) {
-        const int j0 = ksteps.tile(n) * BN;
+        const int j0 = (two ? ksteps.tile(n) : ksteps.lo0 + n) * BN;
         const int sk = n % NK, sv = n % NV;
         if (n >= NK && !mbar_wait(k_empty + sk, ((n / NK) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + sk, C::KV_BYTES);
@@ -1411,12 +1415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lo_all = band_key_lo(g, ihi), hi_all = band_key_hi(g, i0);
     for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
-      const int j0 = ksteps.tile(n) * BN;
+      const int j0 = (two ? ksteps.tile(n) : ksteps.lo0 + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(sdp_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
-      bool both;
-      const int4 vv = vis_in_tile(vshift(vrow, j0), BN, &both);  // visible key columns of row i
+      bool both = false;  // visible key columns of row i
+      const int4 vv = two ? vis_in_tile(vshift(vrow, j0), BN, &both) : vshift(vrow, j0);
       const bool two_here = two && __any_sync(0xffffffffu, both);
       uint32_t sv[CW], dv[CW];
 #pragma unroll
@@ -1538,7 +1542,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
     if ((e = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
     if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
     if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BN)) != cudaSuccess) return e;
-    auto kern = dq128_tc_kernel<D>;
+    auto kern = g.Rc > 0 ? dq128_tc_kernel<D, true> : dq128_tc_kernel<D, false>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
       return e;
     p.out0 = dq;
@@ -1552,7 +1556,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
     if ((e = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BMQ)) != cudaSuccess) return e;
     if ((e = make_tmap_f16_chunks(&tk, k16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
     if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
-    auto kern = dq_tc_kernel<D>;
+    auto kern = g.Rc > 0 ? dq_tc_kernel<D, true> : dq_tc_kernel<D, false>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
       return e;
     p.out0 = dq;

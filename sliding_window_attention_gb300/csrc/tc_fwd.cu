@@ -162,7 +162,9 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float 
   return s0 + s1;
 }
 
-template <int D>
+// TWO: a shared-prefix plan is active (a row may see two key intervals); a
+// separate instantiation keeps the plain kernel's code.
+template <int D, bool TWO>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   // sees at least the key at its own position)
   const TileSteps steps = row_steps(g, i0, ihi, BN);
   const int nt = steps.count();
-  const bool two = g.Rc > 0;  // shared-prefix plan: up to two visible intervals per row
+  constexpr bool two = TWO;  // shared-prefix plan: up to two visible intervals per row
 
   if (threadIdx.x < 128) ones[threadIdx.x] = 0x3C003C00u;  // two fp16 1.0 per word, 512 bytes
   if (threadIdx.x == 0) {
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int n = 0; n < nt; ++n) {
         const int st = n % NS;
         const uint32_t par = ((n / NS) & 1) ^ 1;
-        const int j0 = steps.tile(n) * BN;
+        const int j0 = (two ? steps.tile(n) : steps.lo0 + n) * BN;
         if (n >= NS && !mbar_wait(k_empty + st, par, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + st, C::K_BYTES);
         tma_load_4d(sK + st * C::K_BYTES, &tmK, k_full + st, 0, j0, 0, bkv);
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int lo_all = band_key_lo(g, ihi), hi_all = band_key_hi(g, i0);
     for (int n = 0; n < nt; ++n) {
       const int sb = n & 1;
-      const int j0 = steps.tile(n) * BN;
+      const int j0 = (two ? steps.tile(n) : steps.lo0 + n) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       const bool full = two ? rows_tile_full(g, i0, ihi, j0, j0 + BN - 1) : (j0 >= lo_all && j0 + BN - 1 <= hi_all);
@@ -334,8 +336,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tmem_wait_ld();
       // Visible key columns of this row inside the tile (edge tiles only);
       // the two-interval mask only where a row of the warp needs it
-      bool both;
-      const int4 vv = vis_in_tile(vshift(vrow, j0), BN, &both);
+      bool both = false;
+      const int4 vv = two ? vis_in_tile(vshift(vrow, j0), BN, &both) : vshift(vrow, j0);
       const bool two_here = two && __any_sync(0xffffffffu, both);
       const float tmax = full ? softmax_tile_max<BN, true>(sr, sl2, vv)
                               : (two_here ? softmax_tile_max<BN, false, true>(sr, sl2, vv)
@@ -473,7 +475,8 @@ struct FwdPPCfg {
   static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
 };
 
-template <int D>
+// TWO: a shared-prefix plan is active (see fwd_tc_kernel).
+template <int D, bool TWO>
 __global__ void __launch_bounds__(320, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -511,14 +514,15 @@ __global__ void __launch_bounds__(320, 1)
   const TileSteps stA = row_steps(g, i0A, ihiA, BN);
   const TileSteps stB = i0B < g.Lq ? row_steps(g, i0B, ihiB, BN) : TileSteps{0, 0, 0, 0};
   const bool hasB = stB.count() > 0;
-  const bool two = g.Rc > 0;  // shared-prefix plan: up to two visible intervals per row
-  auto first_tile = [](const TileSteps& s) { return s.n0 ? s.lo0 : s.lo1; };
-  auto last_tile = [](const TileSteps& s) { return s.n1 ? s.lo1 + s.n1 - 1 : s.lo0 + s.n0 - 1; };
+  constexpr bool two = TWO;  // shared-prefix plan: up to two visible intervals per row
+  // (without a plan every query tile's key tiles are one range: part 0)
+  auto first_tile = [](const TileSteps& s) { return (!two || s.n0) ? s.lo0 : s.lo1; };
+  auto last_tile = [](const TileSteps& s) { return (two && s.n1) ? s.lo1 + s.n1 - 1 : s.lo0 + s.n0 - 1; };
   // key tiles of either query tile
   const int u0 = hasB ? min(first_tile(stA), first_tile(stB)) : first_tile(stA);
   const int u1 = hasB ? max(last_tile(stA), last_tile(stB)) : last_tile(stA);
   auto in_steps = [](const TileSteps& s, int n) {
-    return (n >= s.lo0 && n < s.lo0 + s.n0) || (n >= s.lo1 && n < s.lo1 + s.n1);
+    return (n >= s.lo0 && n < s.lo0 + s.n0) || (two && n >= s.lo1 && n < s.lo1 + s.n1);
   };
   auto uses = [&](int w, int n) { return w ? in_steps(stB, n) : in_steps(stA, n); };
 
@@ -667,7 +671,7 @@ __global__ void __launch_bounds__(320, 1)
     const int4 vrow = row_vis(g, i, 0);
     const int lo_all = band_key_lo(g, ihiw), hi_all = band_key_hi(g, i0w);
     for (int k = 0; k < cnt; ++k) {
-      const int j0 = stw.tile(k) * BN;
+      const int j0 = (two ? stw.tile(k) : stw.lo0 + k) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + w, k & 1, abort_flag))) { ok = false; break; }
       tc_fence_after();
       const bool full = two ? rows_tile_full(g, i0w, ihiw, j0, j0 + BN - 1)
@@ -683,8 +687,8 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_off + s_col + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(sr));
         tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
-        bool both;
-        const int4 vh = vis_in_tile(vshift(vv, 64 * hf), 64, &both);
+        bool both = false;
+        const int4 vh = two ? vis_in_tile(vshift(vv, 64 * hf), 64, &both) : vshift(vv, 64 * hf);
         const bool two_here = two && __any_sync(0xffffffffu, both);
         tmax = fmaxf(tmax, full ? softmax_tile_max<64, true>(sr, sl2, vh)
                                 : (two_here ? softmax_tile_max<64, false, true>(sr, sl2, vh)
@@ -708,8 +712,8 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tmem + lane_off + s_col + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
         const uint32_t p_taddr = tmem + lane_off + s_col + 32 * hf;
-        bool both;
-        const int4 vh = vis_in_tile(vshift(vv, 64 * hf), 64, &both);
+        bool both = false;
+        const int4 vh = two ? vis_in_tile(vshift(vv, 64 * hf), 64, &both) : vshift(vv, 64 * hf);
         const bool two_here = two && __any_sync(0xffffffffu, both);
         tsum += full ? softmax_tile_p<64, true, true>(sr, sl2, m_use, vh, p_taddr)
                      : (two_here ? softmax_tile_p<64, false, true, true>(sr, sl2, m_use, vh, p_taddr)
@@ -903,7 +907,7 @@ static cudaError_t fwd_tc_d(const Geom& g, const uint16_t* q, const uint16_t* k,
   if ((e = make_tmap_f16_chunks(&tq, q, D, g.Lq, g.B * g.Hq, kBM, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tk, k, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
-  auto kern = fwd_tc_kernel<D>;
+  auto kern = g.Rc > 0 ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
     return e;
   FwdParams p;
@@ -927,7 +931,7 @@ static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q, const uint16_t* k,
   if ((e = make_tmap_f16_chunks(&tq, q, D, g.Lq, g.B * g.Hq, C::BM, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tk, k, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, D, g.L, g.B * g.Hkv, C::BN, C::KCH)) != cudaSuccess) return e;
-  auto kern = fwd_pp_kernel<D>;
+  auto kern = g.Rc > 0 ? fwd_pp_kernel<D, true> : fwd_pp_kernel<D, false>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
     return e;
   FwdParams p;
