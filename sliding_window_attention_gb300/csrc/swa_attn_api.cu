@@ -83,15 +83,19 @@ int check_device() {
   return ok_cache[dev] == 1 ? SWA_OK : SWA_ERR_UNSUPPORTED_DEVICE;
 }
 
-// Head dim 512: whether the device can hold the cluster kernels' per-SM
-// tile scratch (checked once per device and direction).
-int check_scratch_layout(bool fwd) {
-  static int cache[2][kMaxDevices] = {};  // 0 unknown, 1 ok, 2 unsupported
+// Whether the device can hold the cluster kernels' per-SM tile scratch
+// (head dim 512 forward and backward, head dim 256 backward; checked once per
+// device and kernel family).
+enum ScratchUser { kScratchFwd512 = 0, kScratchBwd512 = 1, kScratchBwd256 = 2 };
+int check_scratch_layout(int user) {
+  static int cache[3][kMaxDevices] = {};  // 0 unknown, 1 ok, 2 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SWA_ERR_CUDA;
-  int& c = cache[fwd ? 0 : 1][dev];
+  int& c = cache[user][dev];
   if (c == 0) {
-    const int r = fwd ? swa::scratch_layout_fwd512() : swa::scratch_layout_bwd512();
+    const int r = user == kScratchFwd512   ? swa::scratch_layout_fwd512()
+                  : user == kScratchBwd512 ? swa::scratch_layout_bwd512()
+                                           : swa::scratch_layout_bwd256();
     if (r < 0) return SWA_ERR_CUDA;
     c = r == 0 ? 1 : 2;
   }
@@ -263,7 +267,7 @@ static int fwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, con
       return SWA_ERR_CUDA;
     return SWA_OK;
   }
-  if (D == 512 && (rc = check_scratch_layout(true)) != SWA_OK) return rc;
+  if (D == 512 && (rc = check_scratch_layout(kScratchFwd512)) != SWA_OK) return rc;
   const FwdWs w = fwd_ws_layout(B, Hq, Hkv, Lq, Lk, D);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + w.v16);
@@ -291,7 +295,8 @@ static int bwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, con
   if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
   int rc = check_device();
   if (rc) return rc;
-  if (D == 512 && (rc = check_scratch_layout(false)) != SWA_OK) return rc;
+  if (D == 512 && (rc = check_scratch_layout(kScratchBwd512)) != SWA_OK) return rc;
+  if (D == 256 && (rc = check_scratch_layout(kScratchBwd256)) != SWA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_ptr_for_current_device(&rc);
   if (!status) return rc;

@@ -195,6 +195,9 @@ enum : int { kStatusOk = 0, kStatusTimeout = -11, kStatusFp16Range = -14, kStatu
 // and -1 when the CUDA queries fail.
 int scratch_layout_fwd512();
 int scratch_layout_bwd512();
+// Head dim 256: the dK/dV clusters pass P^T through a static L2 scratch indexed
+// by the dK CTA's SM id, under the same two conditions.
+int scratch_layout_bwd256();
 
 // ---- SIMT kernels (fp32 arithmetic on bf16 inputs; any D in {64..512}) ----
 cudaError_t launch_fwd_simt(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -957,6 +957,457 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
+// dK / dV for head dim 256 on 2-CTA clusters, one cluster per (128-row key
+// tile, kv head).  dK and dV of a key tile need all 512 TMEM columns, so they
+// live in two CTAs; here the two form a cluster and P^T is computed once:
+//   rank 0 (dV):  S^T = K Q^T, P^T = exp(scale S^T - lse) (masked), dV += P^T dO,
+//                 and the fp16 P^T of each step is stored to an L2 scratch;
+//   rank 1 (dK):  dP^T = V dO^T, dS^T = P^T (dP^T - Delta) with P^T read back
+//                 from the scratch, dK += dS^T Q.
+// So the pass issues S^T, dP^T, dV and dK once (8 D per pair), and the dK CTA
+// holds no K: its 64 KB go to a second Q tile, and its dP^T is double
+// buffered in TMEM, so that Q(n + 1) loads and dP(n + 1) runs while the
+// elementwise warps form dS(n).
+// rank 0 is the dV CTA of the one-CTA design below (K resident, Q in a 6-slot
+// ring of 16 KB slices, one dO tile, S^T double buffered in TMEM).  rank 1:
+// V resident (64 KB), two Q tiles (the MN-major B of dK), dO in a 2-slot ring
+// of slices; TMEM: dK [0, 256), dP^T [256, 384) and [384, 512), where dS^T(n)
+// goes back as fp16 pairs for the TS-form dK(n).
+// P^T crosses between the SMs through global memory (L2): rank 0's
+// elementwise threads stage their 64 columns of a key row as 16-byte chunks
+// in shared memory, in a layout where a warp writes (and the matching warp of
+// rank 1 later reads) 512 contiguous bytes; rank 0's store thread bulk-stores
+// the 32 KB tile into a scratch slot and tells rank 1, whose relay thread
+// tells rank 0 when the slot has been read (one remote arrival per step each
+// way).  Two scratch slots per cluster, indexed by the SM id of rank 1: one
+// CTA of this kernel fills an SM, so no two resident clusters share a slot.
+constexpr int kPairScratchSms = 192;
+constexpr int kPairTile = 128 * 128;  // fp16 elements of one P^T tile (32 KB)
+__device__ __align__(256) uint16_t g_p256_scratch[(size_t)kPairScratchSms * 2 * kPairTile];
+
+struct Kv256PairCfg {
+  static constexpr int D = 256, BNK = 128, BM = 128, CW = 64, KCH = 4;
+  static constexpr int TILE = 128 * D * 2;  // 64 KB
+  static constexpr int SLICE = 128 * 128;   // 16 KB
+  // rank 0: K [0, TILE), dO tile [TILE, 2 TILE), Q slices [2 TILE, 2 TILE + 4 SLICE),
+  // then the 32 KB staging of P^T for the bulk store to the scratch
+  static constexpr int NSL0 = 4;
+  static constexpr int OFF_STG0 = 2 * TILE + NSL0 * SLICE;
+  static constexpr int STG_BYTES = 128 * 128 * 2;
+  // rank 1: V [0, TILE), Q tiles [TILE, 3 TILE), dO slices [3 TILE, 3 TILE + 2 SLICE)
+  static constexpr int NSL1 = 2;
+  static constexpr int DATA0 = OFF_STG0 + STG_BYTES;
+  static constexpr int DATA1 = 3 * TILE + NSL1 * SLICE;
+  static constexpr int DATA = DATA0 > DATA1 ? DATA0 : DATA1;
+  static constexpr uint32_t ACC_COL = 0, BUF_COL = 256;  // S^T (rank 0) / dP^T (rank 1) buffers at 256, 384
+  static constexpr size_t SMEM = (size_t)DATA + 1024 + 1024;
+  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
+};
+
+struct PairBars {
+  uint64_t kv_full;          // resident K (rank 0) / V (rank 1)
+  uint64_t t_full[2];        // dO tile (rank 0: slot 0 only) / Q tiles (rank 1)
+  uint64_t t_empty[2];
+  uint64_t sl_full[6];       // slice ring: Q (rank 0) / dO (rank 1)
+  uint64_t sl_empty[6];
+  uint64_t s_full[2];        // rank 0: S^T(n) in TMEM buffer n & 1; rank 1: dP^T(n)
+  uint64_t p_full[2];        // both warpgroups packed P^T (rank 0) / dS^T (rank 1) into buffer n & 1
+  uint64_t x_done[2];        // rank 0: threads stored P^T(n) to the scratch; rank 1: threads consumed it
+  uint64_t x_peer[2];        // rank 0: rank 1 consumed slot n & 1; rank 1: rank 0 stored into slot n & 1
+  uint64_t stg_free;         // rank 0: the bulk store has read the staging
+  uint64_t acc_done, mma_drain;
+  uint32_t tmem_slot;
+  int abort_flag;
+  int smid;                  // SM id of this CTA (rank 1's indexes the scratch)
+};
+
+// Warps: 0 TMA (lane 0 the resident operand and whole tiles, lane 1 the
+// slices), 1 Tensor Memory owner and MMA issuer, 2-9 elementwise, 10 the
+// cross-CTA traffic (rank 0: P^T bulk stores; rank 1: the relay).  A thread
+// that waits on the peer gets a warp of its own: lanes of one warp that spin
+// on different barriers delay each other.
+constexpr int kPairThreads = 352;
+template <bool TWO>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    dkdv256_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                        const BwdParams p) {
+  using C = Kv256PairCfg;
+  constexpr int BNK = C::BNK, BM = C::BM, CW = C::CW, KCH = C::KCH, D = C::D;
+  constexpr uint32_t R = 2;  // CTAs per cluster
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PairBars* bars = reinterpret_cast<PairBars*>(base + C::DATA);
+  volatile int* abort_flag = &bars->abort_flag;
+  const uint32_t rank = cluster_rank();
+  const bool dvr = rank == 0;  // the dV CTA (P^T producer)
+  const int NSL = dvr ? C::NSL0 : C::NSL1;
+  unsigned char* sRes = base;                                       // K (rank 0) / V (rank 1)
+  unsigned char* sT = base + C::TILE;                               // dO tile (rank 0) / Q tiles (rank 1)
+  unsigned char* sSl = base + (dvr ? 2 * C::TILE : 3 * C::TILE);    // slice ring
+  unsigned char* sStg = base + C::OFF_STG0;                         // rank 0: P^T staging
+
+  const Geom& g = p.g;
+  const int warp = threadIdx.x / 32;
+  const int bkv = blockIdx.x / 2;  // b * Hkv + kv head
+  const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
+  const int j0 = (int)blockIdx.y * BNK;
+  const int jhi = min(j0 + BNK, g.L) - 1;
+  const TileSteps qsteps = key_steps(g, j0, jhi, BM);
+  const int ntq = qsteps.count();
+  const int N = g.G * ntq;  // steps (head of group, query tile)
+  if (N == 0) {
+    // no query sees these keys: zero gradients ("Lab 028 lab detail", "What I
+    // changed, in plain terms" item 5(b)); both CTAs of the cluster leave here
+    // together, before any cluster barrier
+    zero_rows(dvr ? p.out1 : p.out0, bkv, j0, BNK, g.L, D);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->t_full[s], 1);
+      mbar_init(&bars->t_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 256);
+      mbar_init(&bars->x_done[s], 256);
+      mbar_init(&bars->x_peer[s], 1);
+    }
+    mbar_init(&bars->stg_free, 1);
+    for (int s = 0; s < 6; ++s) {
+      mbar_init(&bars->sl_full[s], 1);
+      mbar_init(&bars->sl_empty[s], 1);
+    }
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->mma_drain, 1);
+    bars->abort_flag = 0;
+    uint32_t sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    bars->smid = sm < (uint32_t)kPairScratchSms ? (int)sm : -1;
+    if (bars->smid < 0) atomicCAS(p.status, 0, kStatusScratch);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  // the scratch slots of this cluster: rank 1's SM id
+  int sm1;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sm1) : "r"(mapa(smem_u32(&bars->smid), 1u)) : "memory");
+  if (sm1 < 0 && threadIdx.x == 0) cluster_abort(abort_flag, R);
+  uint4* scratch = reinterpret_cast<uint4*>(g_p256_scratch + (size_t)(sm1 < 0 ? 0 : sm1) * 2 * kPairTile);
+  auto step_head = [&](int n) { return b * g.Hq + kvh * g.G + n / ntq; };
+  auto step_i0 = [&](int n) { return (TWO ? qsteps.tile(n % ntq) : qsteps.lo0 + n % ntq) * BM; };
+
+  if (warp == 0) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA: resident operand, whole tiles
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(&bars->kv_full, C::TILE);
+      for (int c = 0; c < KCH; ++c) tma_load_3d(sRes + c * C::SLICE, dvr ? &tmK : &tmV, &bars->kv_full, c * 64, j0, bkv);
+      // rank 0: one dO tile buffer; rank 1: two Q tile buffers
+      const int NT = dvr ? 1 : 2;
+      const CUtensorMap* mt = dvr ? &tmG : &tmQ;
+      int nt = 0;
+      for (; nt < N; ++nt) {
+        const int tb = nt % NT;
+        if (nt >= NT && !mbar_wait_cl(&bars->t_empty[tb], ((nt / NT) - 1) & 1, abort_flag, R)) break;
+        mbar_arrive_expect_tx(&bars->t_full[tb], C::TILE);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sT + tb * C::TILE + c * C::SLICE, mt, &bars->t_full[tb], c * 64, step_i0(nt), step_head(nt));
+      }
+      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
+        mbar_wait_drain(&bars->kv_full, 0);
+        for (int k = nt - 1; k >= 0 && k >= nt - NT; --k) mbar_wait_drain(&bars->t_full[k % NT], (k / NT) & 1);
+      }
+    } else if (lane == 1) {
+      // ---------------------------------------------------------------- TMA: 64-column slices
+      const CUtensorMap* msl = dvr ? &tmQ : &tmG;
+      int ns = 0;
+      bool ok = true;
+      for (int m = 0; ok && m < N; ++m) {
+        for (int c = 0; c < KCH; ++c, ++ns) {
+          const int s = ns % NSL;
+          if (ns >= NSL && !mbar_wait_cl(&bars->sl_empty[s], ((ns / NSL) & 1) ^ 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->sl_full[s], C::SLICE);
+          tma_load_3d(sSl + s * C::SLICE, msl, &bars->sl_full[s], c * 64, step_i0(m), step_head(m));
+        }
+      }
+      if (*abort_flag) drain_ring(bars->sl_full, NSL, ns);
+    }
+  } else if (warp == 10) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && dvr) {
+      // ---------------------------------------------------------------- P^T tiles to the scratch (rank 0)
+      // once the warps staged P^T(n) and rank 1 has read what step n - 2 left
+      // in slot n & 1: bulk store, staging free again once read out, rank 1
+      // told once the writes are complete
+      for (int n = 0; n < N; ++n) {
+        const int s = n & 1;
+        if (!mbar_wait_cl(&bars->x_done[s], (n >> 1) & 1, abort_flag, R)) break;
+        if (n >= 2 && !mbar_wait_cl(&bars->x_peer[s], ((n >> 1) - 1) & 1, abort_flag, R)) break;
+        fence_proxy_async_global();
+        if (sm1 >= 0) bulk_store_s2g(scratch + (size_t)s * (kPairTile / 8), smem_u32(sStg), C::STG_BYTES);
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(&bars->stg_free);
+        bulk_wait_all();
+        fence_proxy_async_global();
+        mbar_arrive_remote(mapa(smem_u32(&bars->x_peer[s]), 1u));
+      }
+      bulk_wait_all();  // no store still reads this CTA's shared memory
+    } else if (lane == 0) {
+      // ---------------------------------------------------------------- relay (rank 1)
+      // "slot n & 1 was read" -> rank 0
+      for (int n = 0; n < N; ++n) {
+        if (!mbar_wait_cl(&bars->x_done[n & 1], (n >> 1) & 1, abort_flag, R)) break;
+        mbar_arrive_remote(mapa(smem_u32(&bars->x_peer[n & 1]), 0u));
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major), N = 128
+      const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (A in TMEM, B MN-major), N = 256
+      const uint64_t rdk = smem_desc_sw128(smem_u32(sRes), 16, 1024);
+      bool ok = mbar_wait_cl(&bars->kv_full, 0, abort_flag, R);
+      int used = 0;  // slices consumed
+      // S^T (rank 0) or dP^T (rank 1): resident A, B from the slice ring, into TMEM column col
+      auto issue_sliced = [&](uint32_t col) -> bool {
+        for (int c = 0; c < KCH; ++c, ++used) {
+          const int s = used % NSL;
+          if (!mbar_wait_cl(&bars->sl_full[s], (used / NSL) & 1, abort_flag, R)) return false;
+          tc_fence_after();
+          const uint64_t bd = smem_desc_sw128(smem_u32(sSl + s * C::SLICE), 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(tmem + col, desc_add(rdk, c * C::SLICE + ks * 32), desc_add(bd, ks * 32), idS, (c | ks) ? 1u : 0u);
+          mma_commit(&bars->sl_empty[s]);
+        }
+        return true;
+      };
+      // dV(n) / dK(n): accumulator += packed TMEM operand (buffer col) x tile tb (MN-major)
+      auto issue_grad = [&](int n, uint32_t col, int tb) {
+        const uint64_t tmn = smem_desc_sw128(smem_u32(sT + tb * C::TILE), BM * 128, 1024);
+#pragma unroll
+        for (int ks = 0; ks < BM / 16; ++ks)
+          mma_ts(tmem + C::ACC_COL, tmem + col + packed_col(ks), desc_add(tmn, ks * 2048), idG,
+                 (n > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&bars->t_empty[tb]);
+      };
+      // S^T(0), S^T(1) (rank 0) or dP^T(0), dP^T(1) (rank 1) into the two buffers
+      if (ok) ok = issue_sliced(C::BUF_COL);
+      if (ok) mma_commit(&bars->s_full[0]);
+      if (ok && N > 1) ok = issue_sliced(C::BUF_COL + 128);
+      if (ok && N > 1) mma_commit(&bars->s_full[1]);
+      for (int n = 0; ok && n < N; ++n) {
+        const uint32_t sb = C::BUF_COL + 128 * (n & 1);
+        const int tb = dvr ? 0 : (n & 1);
+        const uint32_t tpar = dvr ? (n & 1) : ((n >> 1) & 1);
+        if (!mbar_wait_cl(&bars->p_full[n & 1], (n >> 1) & 1, abort_flag, R) ||
+            !mbar_wait_cl(&bars->t_full[tb], tpar, abort_flag, R)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_grad(n, sb, tb);  // dV(n) / dK(n); the next product into this buffer follows it in issue order
+        if (n + 2 < N) {
+          if (!issue_sliced(sb)) {
+            ok = false;
+            break;
+          }
+          mma_commit(&bars->s_full[n & 1]);
+        }
+      }
+      if (ok) mma_commit(&bars->acc_done);
+      // every MMA issued so far has finished before TMEM is released
+      mma_commit(&bars->mma_drain);
+      mbar_wait_drain(&bars->mma_drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    // warpgroup wg (warps 2-5 / 6-9) takes query columns [64 wg, 64 wg + 64);
+    // warp % 4 fixes the TMEM lane quarter, i.e. the key rows
+    const int wg = (warp - 2) >> 2;
+    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int j = j0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sl2 = g.scale * kLog2e;
+    const int cw0 = wg * CW;
+    const bool scratch_ok = sm1 >= 0;
+    bool ok = true;
+    const size_t dplane = (size_t)g.B * g.Hq * p.Lpad;  // offset of the Delta plane
+    // rank 0: the query rows that see this thread's key j, and those that see
+    // every key of the tile (hoisted out of the step loop)
+    const int qlo_j = band_q_lo(g, j), qhi_j = band_q_hi(g, j);
+    const int qlo_all = band_q_lo(g, jhi), qhi_all = band_q_hi(g, j0);
+    constexpr bool two = TWO;  // shared-prefix plan: a key may see two row intervals
+    const int4 vj = key_vis(g, j, 0);
+    // 16-byte chunk k of this thread's 64 columns in a scratch slot
+    // (chunk-major: a warp's 32 rows of one chunk are 512 contiguous bytes)
+    const int chunk0 = (cw0 / 8) * 128 + r;
+    for (int n = 0; n < N; ++n) {
+      const int i0 = step_i0(n);
+      const int sbuf = n & 1;
+      const uint32_t scol = C::BUF_COL + 128 * sbuf;
+      const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + i0 + cw0;
+      uint4* slot = scratch + (size_t)sbuf * (kPairTile / 8);
+      uint32_t pp[32];  // P^T of this key row and 64 query columns, fp16 pairs
+      if (dvr) {
+        // lse * log2e of this warpgroup's 64 query columns, loaded while S^T(n) is computed
+        float lv[64];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_g) + q);
+          lv[4 * q] = l4.x;
+          lv[4 * q + 1] = l4.y;
+          lv[4 * q + 2] = l4.z;
+          lv[4 * q + 3] = l4.w;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full[sbuf], (n >> 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[64];
+        tmem_ld32(tmem + lane_off + scol + cw0, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(tmem + lane_off + scol + cw0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_wait_ld();
+        const bool full = ((i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all)) ||
+                          (two && keys_tile_full(g, j0, jhi, i0, i0 + BM - 1));
+        if (full) {
+          kv_p64<true>(sv, lv, sl2, cw0, make_int4(0, 0, 0, 0));
+        } else if constexpr (two) {
+          bool both;
+          const int4 vq = vis_in_tile(vshift(vj, i0), BM, &both);
+          if (__any_sync(0xffffffffu, both)) kv_p64<false, true>(sv, lv, sl2, cw0, vq);
+          else kv_p64<false>(sv, lv, sl2, cw0, vq);
+        } else {
+          kv_p64<false>(sv, lv, sl2, cw0, make_int4(qlo_j - i0, qhi_j - i0, 1, 0));
+        }
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) pp[e >> 1] = pack_half2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+        // the dV operand: into the first half of this warpgroup's own columns of the S buffer
+        tmem_st32(tmem + lane_off + scol + cw0, pp);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[sbuf]);
+        // P^T(n) for the dK CTA: into the staging once the store of step n - 1 has read it
+        if (n >= 1 && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free, (n - 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        {
+          const uint32_t st = smem_u32(sStg) + (uint32_t)chunk0 * 16u;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st_smem_v4(st + k * 128 * 16, pp[4 * k], pp[4 * k + 1], pp[4 * k + 2], pp[4 * k + 3]);
+        }
+        fence_proxy_async_smem();  // the bulk store (async proxy) reads what these stores wrote
+        mbar_arrive(&bars->x_done[sbuf]);
+      } else {
+        // Delta of the 64 columns, loaded while P^T(n) and dP^T(n) are on their way
+        float dl[64];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 d4 = __ldg(reinterpret_cast<const float4*>(lse_g + dplane) + q);
+          dl[4 * q] = d4.x;
+          dl[4 * q + 1] = d4.y;
+          dl[4 * q + 2] = d4.z;
+          dl[4 * q + 3] = d4.w;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->x_peer[sbuf], (n >> 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        if (scratch_ok) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // L2, not L1: the slot is rewritten every other step
+            const uint4 w = __ldcg(slot + chunk0 + k * 128);
+            pp[4 * k] = w.x;
+            pp[4 * k + 1] = w.y;
+            pp[4 * k + 2] = w.z;
+            pp[4 * k + 3] = w.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) pp[k] = 0u;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full[sbuf], (n >> 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dd[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two 32-column halves keep dP^T's registers small
+          uint32_t dv[32];
+          tmem_ld32(tmem + lane_off + scol + cw0 + 32 * h, dv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pp[16 * h + (e >> 1)]));
+            dd[16 * h + (e >> 1)] = pack_half2(pf.x * (__uint_as_float(dv[e]) - dl[32 * h + e]),
+                                               pf.y * (__uint_as_float(dv[e + 1]) - dl[32 * h + e + 1]));
+          }
+        }
+        // dS^T: into the first half of this warpgroup's own columns of the dP buffer
+        tmem_st32(tmem + lane_off + scol + cw0, dd);
+        mbar_arrive(&bars->x_done[sbuf]);  // P^T(n) consumed: the slot may be rewritten
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[sbuf]);
+      }
+    }
+    if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R))) {
+      tc_fence_after();
+      // each warpgroup writes half of the accumulator's columns (dK scaled)
+      const bool row_ok = j < g.L;
+      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+      const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
+      const float mul = dvr ? inv_s : g.scale * inv_s;
+      float* dst = (dvr ? p.out1 : p.out0) + off;
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = wg * (D / 64) + cc;
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_off + C::ACC_COL + c * 32, a);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
+  cluster_sync();  // no CTA leaves while its peer may still arrive on its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
 // dQ for head dim 256 with 64-row key steps.  Q of the CTA's 128 rows sits in
 // Tensor Memory as fp16 pairs and is the A operand of S = Q K^T (TS form), so
 // shared memory holds only dO (64 KB) and two stages of K and V (32 KB each):
@@ -1532,8 +1983,23 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
         kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
         return cudaGetLastError();
       };
-      if ((e = run256(std::integral_constant<int, kModeDV>{})) != cudaSuccess) return e;
-      return run256(std::integral_constant<int, kModeDK>{});
+      (void)run256;
+      using C = Kv256PairCfg;
+      CUtensorMap tq, tk, tv, tg;
+      if ((e = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e;
+      if ((e = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e;
+      if ((e = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e;
+      auto kern = g.Rc > 0 ? dkdv256_pair_kernel<true> : dkdv256_pair_kernel<false>;
+      if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) != cudaSuccess)
+        return e;
+      BwdParams pm = p;
+      pm.out0 = dk;
+      pm.out1 = dv;
+      pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
+      dim3 grid(2 * g.B * g.Hkv, pm.n_tiles);  // clusters of 2 along x: (dV CTA, dK CTA) of a key tile
+      kern<<<grid, kPairThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
+      return cudaGetLastError();
     }
   } else if constexpr (D <= 128) {
     using C = Dq128Cfg<D>;
@@ -1572,6 +2038,19 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
 }  // namespace
 
 bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
+
+int scratch_layout_bwd256() {
+  int n0 = 0, n1 = 0, nsm = 0, dev = 0;
+  const size_t smem = Kv256PairCfg::SMEM;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev))
+    return -1;
+  if (cudaFuncSetAttribute(dkdv256_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ||
+      cudaFuncSetAttribute(dkdv256_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, dkdv256_pair_kernel<false>, kPairThreads, smem) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, dkdv256_pair_kernel<true>, kPairThreads, smem))
+    return -1;
+  return (n0 == 1 && n1 == 1 && nsm <= kPairScratchSms) ? 0 : 1;
+}
 
 cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float* stats, cudaStream_t s) {
   const long long n16 = (long long)g.B * g.Hq * g.Lq * g.D / 8;
