@@ -6,22 +6,24 @@
 // the causal / window band are visited ("Lab 028 lab detail: Off NVIDIA, you
 // fix the platform yourself", "What I changed, in plain terms" items 3-4).
 //
-// dK/dV kernel, one CTA per (128-row key tile, kv head):
-//   for every query head of the group and every 64-row query tile in band:
+// dK/dV, per (128-row key tile, kv head), for every query head of the group
+// and every 128-row query tile in band:
 //     S^T  = K Q^T,  dP^T = V dO^T                 (SS MMAs, fp32 in TMEM)
 //     P^T  = exp(scale S^T - lse),  dS^T = P^T (dP^T - Delta)   (thread = key row)
 //     dV  += P^T dO,  dK += dS^T Q                  (TS MMAs, A operand in TMEM)
 //   dK and dV stay in TMEM for the whole group loop: no atomics, deterministic.
+//   Head dim <= 128: one CTA holds both (dkdv128_tc_kernel).  Head dim 256:
+//   a 2-CTA cluster, dV on one SM and dK on the other, P^T passed between
+//   them through L2 (dkdv256_pair_kernel).
 // dQ kernel, one CTA per (128-row query tile, query head):
-//   for every 64-row key tile in band: S = Q K^T, dP = dO V^T,
+//   for every key tile in band: S = Q K^T, dP = dO V^T,
 //   dS = P (dP - Delta), dQ += dS K.  No read-modify-write of dQ in memory.
 //
-// Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner and the
-// single-thread MMA issuer, warps 2..5 and 6..9 two elementwise
-// softmax-gradient warpgroups (one TMEM lane, i.e. one row, per thread).  At
-// head dim <= 128 both warpgroups work on every step, each on half of its
-// columns, which halves the latency of the S -> P -> dV/dK chain; at head dim
-// 256 (32-column steps) they take alternate steps.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner and the single-thread
+// MMA issuer, warps 2..5 and 6..9 two elementwise softmax-gradient
+// warpgroups (one TMEM lane, i.e. one row, per thread), each on half of the
+// columns of every step; the cluster kernel adds warps for its second
+// producer and its cross-CTA traffic.
 // Every mbarrier wait is bounded (see tc_ptx.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -219,8 +221,6 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_
   }
 }
 
-// dV-only / dK-only CTAs of the head-dim-256 dK/dV pass
-enum { kModeDV = 0, kModeDK = 1 };
 
 struct BwdParams {
   Geom g;
@@ -583,378 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ===========================================================================
-// dK / dV for head dim 256 with 128-row query steps, so that every MMA has
-// N >= 128.  dK and dV of a 128-key tile fill all 512 TMEM columns, so a
-// dV-only CTA and a dK-only CTA share each tile (two launches).
-//
-// dV CTA (MODE kModeDV).  TMEM: dV [0, 256), S^T in two buffers [256, 384)
-//   and [384, 512).  P^T(n) goes back as fp16 pairs into its S buffer (each
-//   warpgroup into the first half of its own 64 columns), where dV(n) reads
-//   it as the TMEM A operand (N = 256).  Shared memory: K resident (64 KB),
-//   Q streamed in 64-column slices through a 6-slot ring (S^T only), and one
-//   64 KB dO tile (the MN-major B operand of dV).  MMA issue order:
-//   dV(n) | S(n + 2): the S^T double buffer lets the elementwise warps work
-//   on step n + 1 while the tensor pipe runs dV(n) and S(n + 2), and the dO
-//   tile of step n + 1 loads while S(n + 2) runs.
-// dK CTA (MODE kModeDK).  TMEM: dK [0, 256), S^T [256, 384), dP^T [384, 512);
-//   dS^T(n) goes back as fp16 pairs into the dP buffer (same column plan).
-//   Shared memory: K and V resident (128 KB), one 64 KB Q tile (K-major B
-//   of S^T, then MN-major B of dK), dO streamed in 64-column slices (dP^T
-//   only).  MMA issue order: dK(n) | dP(n + 1) | S(n + 1): dP(n + 1) runs
-//   while Q(n + 1) loads into the buffer dK(n) has just released.
-// dS is formed from the fp16-rounded P, as dV uses it.
-template <int MODE>
-struct Kv256Cfg {
-  static constexpr int D = 256, BNK = 128, BM = 128, CW = 64, KCH = 4;
-  static constexpr int TILE = 128 * D * 2;   // 64 KB: a 128-row K, V, Q or dO tile
-  static constexpr int SLICE = 128 * 128;    // 16 KB: one 64-column chunk of a tile
-  static constexpr bool DV = MODE == kModeDV;
-  static constexpr int RES = DV ? TILE : 2 * TILE;          // K (and V)
-  static constexpr int NSL = DV ? 6 : 2;                    // slice ring depth (Q for dV, dO for dK)
-  static constexpr int OFF_T = RES;                         // the one dO (dV) or Q (dK) tile
-  static constexpr int OFF_SL = RES + TILE;                 // slice ring
-  static constexpr int DATA = OFF_SL + NSL * SLICE;
-  static constexpr uint32_t ACC_COL = 0, S_COL = 256, DP_COL = 384;
-  static constexpr size_t SMEM = (size_t)DATA + 1024 + 1024;
-  static_assert(SMEM <= (size_t)kSmemMax, "shared memory");
-};
-
 // A operand column of K-step ks (16 query rows) in a buffer where warpgroup
 // w packed its 64 columns into [64 w, 64 w + 32).
 __device__ __forceinline__ uint32_t packed_col(int ks) { return (uint32_t)((ks >> 2) * 64 + (ks & 3) * 8); }
-
-template <int MODE, bool TWO>
-__global__ void __launch_bounds__(kThreads, 1)
-    dkdv256_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                      const BwdParams p) {
-  using C = Kv256Cfg<MODE>;
-  constexpr int BNK = C::BNK, BM = C::BM, CW = C::CW, KCH = C::KCH, NSL = C::NSL, D = C::D;
-  constexpr bool DVM = C::DV;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sK = base;
-  unsigned char* sV = base + C::TILE;  // dK CTA only
-  unsigned char* sT = base + C::OFF_T;
-  unsigned char* sSl = base + C::OFF_SL;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::DATA);
-  uint64_t* kv_full = bars;           // [1] resident K (and V)
-  uint64_t* t_full = kv_full + 1;     // [1] the dO (dV) or Q (dK) tile of a step landed
-  uint64_t* t_empty = t_full + 1;     // [1] ... and was released by dV / dK
-  uint64_t* sl_full = t_empty + 1;    // [NSL] slice ring
-  uint64_t* sl_empty = sl_full + NSL; // [NSL]
-  uint64_t* s_full = sl_empty + NSL;  // [2] S^T(n) in TMEM (dK CTA: buffer 0 only)
-  uint64_t* dp_full = s_full + 2;     // [1] dP^T(n) in TMEM (dK CTA)
-  uint64_t* p_full = dp_full + 1;     // [2] P^T(n) (dV) / dS^T(n) (dK) packed into TMEM by both warpgroups
-  uint64_t* acc_done = p_full + 2;    // [1]
-  uint64_t* mma_drain = acc_done + 1; // [1] every issued MMA finished (before TMEM is released)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const Geom& g = p.g;
-  const int warp = threadIdx.x / 32;
-  const int bkv = blockIdx.x;  // b * Hkv + kv head
-  const int b = bkv / g.Hkv, kvh = bkv - b * g.Hkv;
-  const int j0 = (int)blockIdx.y * BNK;
-  const int jhi = min(j0 + BNK, g.L) - 1;
-  // query tiles that can see a key of this tile
-  const TileSteps qsteps = key_steps(g, j0, jhi, BM);
-  const int ntq = qsteps.count();
-  const int N = g.G * ntq;  // steps (head of group, query tile)
-  if (N == 0) {
-    // no query sees these keys (queries that are a suffix of the keys, with a
-    // window): their gradients are zero ("Lab 028 lab detail", "What I
-    // changed, in plain terms" item 5(b)).  Uniform over the CTA, before any
-    // barrier or Tensor Memory is set up.
-    zero_rows(DVM ? p.out1 : p.out0, bkv, j0, BNK, g.L, D);
-    return;
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(t_full, 1);
-    mbar_init(t_empty, 1);
-    for (int s = 0; s < NSL; ++s) {
-      mbar_init(sl_full + s, 1);
-      mbar_init(sl_empty + s, 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(s_full + s, 1);
-      mbar_init(p_full + s, 256);
-    }
-    mbar_init(dp_full, 1);
-    mbar_init(acc_done, 1);
-    mbar_init(mma_drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  auto step_head = [&](int n) { return b * g.Hq + kvh * g.G + n / ntq; };
-  auto step_i0 = [&](int n) { return qsteps.tile(n % ntq) * BM; };
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producers
-    // Two independent streams, each loaded in the order the MMA thread consumes
-    // it and each waiting only on its own consumer: lane 0 the resident K (and
-    // V) and the whole tiles (dO for the dV CTA, Q for the dK CTA), lane 1 the
-    // 64-column slices (Q for the dV CTA, dO for the dK CTA).
-    const int lane = threadIdx.x & 31;
-    if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      prefetch_tmap(&tmG);
-      mbar_arrive_expect_tx(kv_full, C::RES);
-      for (int c = 0; c < KCH; ++c) {
-        tma_load_3d(sK + c * C::SLICE, &tmK, kv_full, c * 64, j0, bkv);
-        if (!DVM) tma_load_3d(sV + c * C::SLICE, &tmV, kv_full, c * 64, j0, bkv);
-      }
-      const CUtensorMap* mt = DVM ? &tmG : &tmQ;
-      int nt = 0;  // tiles issued
-      for (; nt < N; ++nt) {
-        if (nt >= 1 && !mbar_wait(t_empty, (nt - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(t_full, C::TILE);
-        for (int c = 0; c < KCH; ++c) tma_load_3d(sT + c * C::SLICE, mt, t_full, c * 64, step_i0(nt), step_head(nt));
-      }
-      if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
-        mbar_wait_drain(kv_full, 0);
-        if (nt >= 1) mbar_wait_drain(t_full, (nt - 1) & 1);
-      }
-    } else if (lane == 1) {
-      const CUtensorMap* msl = DVM ? &tmQ : &tmG;
-      int ns = 0;  // slices issued
-      bool ok = true;
-      for (int m = 0; ok && m < N; ++m) {
-        for (int c = 0; c < KCH; ++c, ++ns) {
-          const int s = ns % NSL;
-          if (ns >= NSL && !mbar_wait(sl_empty + s, ((ns / NSL) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(sl_full + s, C::SLICE);
-          tma_load_3d(sSl + s * C::SLICE, msl, sl_full + s, c * 64, step_i0(m), step_head(m));
-        }
-      }
-      if (*abort_flag) drain_ring(sl_full, NSL, ns);
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (elect_one()) {
-      const uint32_t idS = idesc_f16(BNK, BM, 0, 0, 0, 0);  // K x Q^T, V x dO^T (both K-major), N = 128
-      const uint32_t idG = idesc_f16(BNK, D, 0, 0, 0, 1);   // P^T x dO, dS^T x Q (A in TMEM, B MN-major), N = 256
-      const uint64_t kdk = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t vdk = smem_desc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t tmn = smem_desc_sw128(smem_u32(sT), BM * 128, 1024);  // the tile, MN-major
-      const uint64_t tk = smem_desc_sw128(smem_u32(sT), 16, 1024);         // the tile, K-major (dK CTA: Q)
-      bool ok = mbar_wait(kv_full, 0, abort_flag);
-      int used = 0;  // slices consumed
-      // S^T or dP^T (A resident, B from the slice ring) into TMEM column col
-      auto issue_sliced = [&](uint64_t adesc, uint32_t col) -> bool {
-        for (int c = 0; c < KCH; ++c, ++used) {
-          const int s = used % NSL;
-          if (!mbar_wait(sl_full + s, (used / NSL) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint64_t bd = smem_desc_sw128(smem_u32(sSl + s * C::SLICE), 16, 1024);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss(tmem + col, desc_add(adesc, c * C::SLICE + ks * 32), desc_add(bd, ks * 32), idS,
-                   (c | ks) ? 1u : 0u);
-          mma_commit(sl_empty + s);
-        }
-        return true;
-      };
-      // dV(n) / dK(n): accumulator += packed TMEM operand (from buffer col) x the tile (MN-major)
-      auto issue_grad = [&](int n, uint32_t col) {
-#pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks)
-          mma_ts(tmem + C::ACC_COL, tmem + col + packed_col(ks), desc_add(tmn, ks * 2048), idG,
-                 (n > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(t_empty);
-      };
-      if (DVM) {
-        if (ok) ok = issue_sliced(kdk, C::S_COL);
-        if (ok) mma_commit(s_full + 0);
-        if (ok && N > 1) ok = issue_sliced(kdk, C::S_COL + 128);
-        if (ok && N > 1) mma_commit(s_full + 1);
-        for (int n = 0; ok && n < N; ++n) {
-          const uint32_t sb = C::S_COL + 128 * (n & 1);
-          if (!mbar_wait(p_full + (n & 1), (n >> 1) & 1, abort_flag) || !mbar_wait(t_full, n & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_grad(n, sb);  // dV(n); S(n + 2) below overwrites the buffer after it (issue order)
-          if (n + 2 < N) {
-            if (!issue_sliced(kdk, sb)) { ok = false; break; }
-            mma_commit(s_full + (n & 1));
-          }
-        }
-      } else {
-        auto issue_s = [&](int n) -> bool {  // S^T(n) = K Q(n)^T, Q from the tile (K-major)
-          if (!mbar_wait(t_full, n & 1, abort_flag)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::SLICE + (ks & 3) * 32;
-            mma_ss(tmem + C::S_COL, desc_add(kdk, off), desc_add(tk, off), idS, ks > 0 ? 1u : 0u);
-          }
-          mma_commit(s_full);
-          return true;
-        };
-        if (ok) ok = issue_s(0) && issue_sliced(vdk, C::DP_COL);
-        if (ok) mma_commit(dp_full);
-        for (int n = 0; ok && n < N; ++n) {
-          if (!mbar_wait(p_full, n & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          issue_grad(n, C::DP_COL);  // dK(n); releases the Q tile
-          if (n + 1 < N) {
-            if (!issue_sliced(vdk, C::DP_COL)) { ok = false; break; }  // dP(n + 1): after dK(n) in issue order
-            mma_commit(dp_full);
-            if (!issue_s(n + 1)) { ok = false; break; }
-          }
-        }
-      }
-      if (ok) mma_commit(acc_done);
-      // every MMA issued so far has finished before TMEM is released
-      mma_commit(mma_drain);
-      mbar_wait_drain(mma_drain, 0);
-    }
-  } else {
-    // ---------------------------------------------------------------- elementwise
-    // warpgroup wg (warps 2-5 / 6-9) takes query columns [64 wg, 64 wg + 64);
-    // warp % 4 fixes the TMEM lane quarter, i.e. the key rows
-    const int wg = (warp - 2) >> 2;
-    const int r = 32 * (warp & 3) + (threadIdx.x & 31);
-    const int j = j0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const float sl2 = g.scale * kLog2e;
-    const int cw0 = wg * CW;
-    bool ok = true;
-    const size_t dplane = (size_t)g.B * g.Hq * p.Lpad;  // offset of the Delta plane
-    // loop invariants of the band: the query rows that see this thread's key
-    // j, and those that see every key of the tile (hoisted: recomputing them
-    // per step pushed the kernel past its register budget)
-    const int qlo_j = band_q_lo(g, j), qhi_j = band_q_hi(g, j);
-    const int qlo_all = band_q_lo(g, jhi), qhi_all = band_q_hi(g, j0);
-    constexpr bool two = TWO;  // shared-prefix plan: a key may see two row intervals
-    const int4 vj = key_vis(g, j, 0);  // (plan only) both row intervals of key j
-    for (int n = 0; n < N; ++n) {
-      const int i0 = step_i0(n);
-      const int sbuf = DVM ? (n & 1) : 0;
-      const uint32_t scol = C::S_COL + 128 * sbuf;
-      const float* lse_g = p.stats + (size_t)step_head(n) * p.Lpad + i0 + cw0;
-      // lse * log2e of this warpgroup's 64 query columns, loaded while S^T(n) is computed
-      float lv[64];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_g) + q);
-        lv[4 * q] = l4.x;
-        lv[4 * q + 1] = l4.y;
-        lv[4 * q + 2] = l4.z;
-        lv[4 * q + 3] = l4.w;
-      }
-      const uint32_t spar = DVM ? ((n >> 1) & 1) : (n & 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full + sbuf, spar, abort_flag))) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld32(tmem + lane_off + scol + cw0, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_ld32(tmem + lane_off + scol + cw0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-      tmem_wait_ld();
-      // every key of the tile seen by every query of the step: the hoisted
-      // plain-band bounds, or (shared-prefix plan) the two-interval test
-      const bool full = ((i0 >= qlo_all) && (i0 + BM - 1 <= qhi_all)) ||
-                        (two && keys_tile_full(g, j0, jhi, i0, i0 + BM - 1));
-      // query columns c of this tile that see key j: i0 + c in [qlo_j, qhi_j]
-      // (and, under a plan, in its second interval)
-      if (full) {
-        kv_p64<true>(sv, lv, sl2, cw0, make_int4(0, 0, 0, 0));
-      } else if constexpr (two) {
-        bool both;
-        const int4 vq = vis_in_tile(vshift(vj, i0), BM, &both);
-        if (__any_sync(0xffffffffu, both)) kv_p64<false, true>(sv, lv, sl2, cw0, vq);
-        else kv_p64<false>(sv, lv, sl2, cw0, vq);
-      } else {
-        kv_p64<false>(sv, lv, sl2, cw0, make_int4(qlo_j - i0, qhi_j - i0, 1, 0));
-      }
-      // P^T as fp16 pairs; dS below uses the same rounded P
-      uint32_t pp[32];
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) pp[e >> 1] = pack_half2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-      if (DVM) {
-        // into the first half of this warpgroup's own columns of the S buffer
-        tmem_st32(tmem + lane_off + scol + cw0, pp);
-      } else {
-        // Delta of the 64 columns, loaded while dP^T(n) is computed
-        float dl[64];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 d4 = __ldg(reinterpret_cast<const float4*>(lse_g + dplane) + q);
-          dl[4 * q] = d4.x;
-          dl[4 * q + 1] = d4.y;
-          dl[4 * q + 2] = d4.z;
-          dl[4 * q + 3] = d4.w;
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(dp_full, n & 1, abort_flag))) { ok = false; break; }
-        tc_fence_after();
-        uint32_t dd[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // two 32-column halves keep dP^T's registers small
-          uint32_t dv[32];
-          tmem_ld32(tmem + lane_off + C::DP_COL + cw0 + 32 * h, dv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pp[16 * h + (e >> 1)]));
-            dd[16 * h + (e >> 1)] = pack_half2(pf.x * (__uint_as_float(dv[e]) - dl[32 * h + e]),
-                                               pf.y * (__uint_as_float(dv[e + 1]) - dl[32 * h + e + 1]));
-          }
-        }
-        // into the first half of this warpgroup's own columns of the dP buffer
-        tmem_st32(tmem + lane_off + C::DP_COL + cw0, dd);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full + sbuf);
-    }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
-      tc_fence_after();
-      // each warpgroup writes half of the accumulator's columns (dK scaled)
-      const bool row_ok = j < g.L;
-      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
-      const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
-      const float mul = DVM ? inv_s : g.scale * inv_s;
-      float* dst = (DVM ? p.out1 : p.out0) + off;
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = wg * (D / 64) + cc;
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + C::ACC_COL + c * 32, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
-    }
-  }
-
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (*abort_flag && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeout);
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
 
 // ===========================================================================
 // dK / dV for head dim 256 on 2-CTA clusters, one cluster per (128-row key
@@ -968,8 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // holds no K: its 64 KB go to a second Q tile, and its dP^T is double
 // buffered in TMEM, so that Q(n + 1) loads and dP(n + 1) runs while the
 // elementwise warps form dS(n).
-// rank 0 is the dV CTA of the one-CTA design below (K resident, Q in a 6-slot
-// ring of 16 KB slices, one dO tile, S^T double buffered in TMEM).  rank 1:
+// rank 0: K resident (64 KB), Q in a 4-slot ring of 16 KB slices, one dO
+// tile, the P^T staging, S^T double buffered in TMEM.  rank 1:
 // V resident (64 KB), two Q tiles (the MN-major B of dK), dO in a 2-slot ring
 // of slices; TMEM: dK [0, 256), dP^T [256, 384) and [384, 512), where dS^T(n)
 // goes back as fp16 pairs for the TS-form dK(n).
@@ -1021,12 +652,12 @@ struct PairBars {
   int smid;                  // SM id of this CTA (rank 1's indexes the scratch)
 };
 
-// Warps: 0 TMA (lane 0 the resident operand and whole tiles, lane 1 the
-// slices), 1 Tensor Memory owner and MMA issuer, 2-9 elementwise, 10 the
-// cross-CTA traffic (rank 0: P^T bulk stores; rank 1: the relay).  A thread
-// that waits on the peer gets a warp of its own: lanes of one warp that spin
-// on different barriers delay each other.
-constexpr int kPairThreads = 352;
+// Warps: 0 TMA of the resident operand and the whole tiles, 11 TMA of the
+// slices, 1 Tensor Memory owner and MMA issuer, 2-9 elementwise, 10 the
+// cross-CTA traffic (rank 0: P^T bulk stores; rank 1: the relay).  Every
+// thread that spins on a barrier has a warp of its own: lanes of one warp
+// that spin on different barriers delay each other.
+constexpr int kPairThreads = 384;
 template <bool TWO>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     dkdv256_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -1129,7 +760,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         mbar_wait_drain(&bars->kv_full, 0);
         for (int k = nt - 1; k >= 0 && k >= nt - NT; --k) mbar_wait_drain(&bars->t_full[k % NT], (k / NT) & 1);
       }
-    } else if (lane == 1) {
+    }
+  } else if (warp == 11) {
+    if ((threadIdx.x & 31) == 0) {
       // ---------------------------------------------------------------- TMA: 64-column slices
       const CUtensorMap* msl = dvr ? &tmQ : &tmG;
       int ns = 0;
@@ -1962,28 +1595,6 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
       return cudaGetLastError();
     } else {
-      auto run256 = [&](auto mode_tag) -> cudaError_t {
-        constexpr int MODE = decltype(mode_tag)::value;
-        using C = Kv256Cfg<MODE>;
-        CUtensorMap tq, tk, tv, tg;
-        cudaError_t e2;
-        if ((e2 = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-        if ((e2 = make_tmap_f16(&tg, g16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e2;
-        if ((e2 = make_tmap_f16(&tk, k16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-        if ((e2 = make_tmap_f16(&tv, v16, D, g.L, g.B * g.Hkv, C::BNK)) != cudaSuccess) return e2;
-        auto kern = g.Rc > 0 ? dkdv256_tc_kernel<MODE, true> : dkdv256_tc_kernel<MODE, false>;
-        if ((e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM)) !=
-            cudaSuccess)
-          return e2;
-        BwdParams pm = p;
-        pm.out0 = dk;
-        pm.out1 = dv;
-        pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
-        dim3 grid(g.B * g.Hkv, pm.n_tiles);
-        kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
-        return cudaGetLastError();
-      };
-      (void)run256;
       using C = Kv256PairCfg;
       CUtensorMap tq, tk, tv, tg;
       if ((e = make_tmap_f16(&tq, q16, D, g.Lq, g.B * g.Hq, C::BM)) != cudaSuccess) return e;

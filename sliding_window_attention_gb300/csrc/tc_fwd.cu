@@ -477,7 +477,7 @@ struct FwdPPCfg {
 
 // TWO: a shared-prefix plan is active (see fwd_tc_kernel).
 template <int D, bool TWO>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdPPCfg<D>;
@@ -556,9 +556,11 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producers
-    // lane 0: both query tiles, then the K tiles; lane 1: the V tiles.  Each
-    // stream is loaded in the order the MMA thread consumes it (key tiles
-    // u0 .. u1 that either query tile uses) and waits only on its own ring.
+    // warp 0: both query tiles, then the K tiles; warp 10: the V tiles (a
+    // warp of its own: two lanes of one warp spinning on different rings
+    // delay each other).  Each stream is loaded in the order the MMA thread
+    // consumes it (key tiles u0 .. u1 that either query tile uses) and waits
+    // only on its own ring.
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -580,7 +582,9 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait_drain(q_full, 0);
         drain_ring(k_full, NK, nk);
       }
-    } else if (lane == 1) {
+    }
+  } else if (warp == 10) {
+    if ((threadIdx.x & 31) == 0) {
       int nv = 0;
       for (int n = u0; n <= u1; ++n) {
         if (!uses(0, n) && !uses(1, n)) continue;
@@ -942,7 +946,7 @@ static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q, const uint16_t* k,
   const int n_qtiles = (g.Lq + C::BM - 1) / C::BM;
   p.n_qtiles = (n_qtiles + 1) / 2;  // pairs of query tiles
   dim3 grid(g.B * g.Hq, p.n_qtiles);
-  kern<<<grid, 320, C::SMEM, s>>>(tq, tk, tv, p);
+  kern<<<grid, 352, C::SMEM, s>>>(tq, tk, tv, p);  // warps 0-9 and the V producer (warp 10)
   return cudaGetLastError();
 }
 
