@@ -282,8 +282,9 @@ __device__ __forceinline__ void kv_p64(uint32_t (&sv)[64], const float (&lv)[64]
 
 // TWO: a shared-prefix plan is active (a key may be seen by two row
 // intervals); a separate instantiation keeps the plain kernel's registers.
+constexpr int kThreadsKv128 = 352;  // the common roles plus the dO producer (warp 10)
 template <int D, bool TWO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsKv128, 1)
     dkdv128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                       const BwdParams p) {
@@ -370,32 +371,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sK + c * BNK * 128, &tmK, kv_full, c * 64, j0, bkv);
         tma_load_3d(sV + c * BNK * 128, &tmV, kv_full, c * 64, j0, bkv);
       }
-      // Q(n) and dO(n), each ring refilled as soon as its slot is released;
-      // Q runs one step ahead of dO (S(n + 1) is issued before dP(n + 1))
-      int nq = 0, ng = 0;
-      bool ok = true;
-      while (ok && (nq < N || ng < N)) {
-        if (nq < N && nq <= ng + 1) {
-          const int s = nq % NQ;
-          if (nq >= NQ && !mbar_wait(q_empty + s, ((nq / NQ) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(q_full + s, C::QT_BYTES);
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sQ + s * C::QT_BYTES + c * BM * 128, &tmQ, q_full + s, c * 64, step_i0(nq), step_head(nq));
-          ++nq;
-        } else {
-          const int s = ng % NG;
-          if (ng >= NG && !mbar_wait(g_empty + s, ((ng / NG) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(g_full + s, C::QT_BYTES);
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sG + s * C::QT_BYTES + c * BM * 128, &tmG, g_full + s, c * 64, step_i0(ng), step_head(ng));
-          ++ng;
-        }
+      // Q(n), the ring refilled as soon as a slot is released
+      int nq = 0;
+      for (; nq < N; ++nq) {
+        const int s = nq % NQ;
+        if (nq >= NQ && !mbar_wait(q_empty + s, ((nq / NQ) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(q_full + s, C::QT_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sQ + s * C::QT_BYTES + c * BM * 128, &tmQ, q_full + s, c * 64, step_i0(nq), step_head(nq));
       }
       if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
         mbar_wait_drain(kv_full, 0);
         drain_ring(q_full, NQ, nq);
-        drain_ring(g_full, NG, ng);
       }
+    }
+  } else if (warp == 10) {
+    // dO(n) on a warp of its own, so that a wait on one ring never holds up the other
+    if (elect_one()) {
+      int ng = 0;
+      for (; ng < N; ++ng) {
+        const int s = ng % NG;
+        if (ng >= NG && !mbar_wait(g_empty + s, ((ng / NG) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(g_full + s, C::QT_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sG + s * C::QT_BYTES + c * BM * 128, &tmG, g_full + s, c * 64, step_i0(ng), step_head(ng));
+      }
+      if (*abort_flag) drain_ring(g_full, NG, ng);
     }
   } else if (warp == 1) {
     if (elect_one()) {
@@ -1326,7 +1327,7 @@ struct Dq128Cfg {
 // TWO: a shared-prefix plan is active (a row may see two key intervals); a
 // separate instantiation keeps the plain kernel's code.
 template <int D, bool TWO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsKv128, 1)
     dq128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const BwdParams p) {
@@ -1405,27 +1406,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ + c * BMQ * 128, &tmQ, q_full, c * 64, i0, bh);
         tma_load_3d(sG + c * BMQ * 128, &tmG, q_full, c * 64, i0, bh);
       }
-      // K and V of each step, each ring refilled as soon as its slot is released
-      int nk = 0, nv = 0;
-      for (int n = 0; n < nt; ++n) {
-        const int j0 = (two ? ksteps.tile(n) : ksteps.lo0 + n) * BN;
-        const int sk = n % NK, sv = n % NV;
-        if (n >= NK && !mbar_wait(k_empty + sk, ((n / NK) & 1) ^ 1, abort_flag)) break;
+      // K of each step, the ring refilled as soon as a slot is released
+      int nk = 0;
+      for (; nk < nt; ++nk) {
+        const int j0 = (two ? ksteps.tile(nk) : ksteps.lo0 + nk) * BN;
+        const int sk = nk % NK;
+        if (nk >= NK && !mbar_wait(k_empty + sk, ((nk / NK) & 1) ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + sk, C::KV_BYTES);
         for (int c = 0; c < KCH; ++c)
           tma_load_3d(sK + sk * C::KV_BYTES + c * BN * 128, &tmK, k_full + sk, c * 64, j0, bkv);
-        ++nk;
-        if (n >= NV && !mbar_wait(v_empty + sv, ((n / NV) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(v_full + sv, C::KV_BYTES);
-        for (int c = 0; c < KCH; ++c)
-          tma_load_3d(sV + sv * C::KV_BYTES + c * BN * 128, &tmV, v_full + sv, c * 64, j0, bkv);
-        ++nv;
       }
       if (*abort_flag) {  // unwinding: the loads in flight land before shared memory is released
         mbar_wait_drain(q_full, 0);
         drain_ring(k_full, NK, nk);
-        drain_ring(v_full, NV, nv);
       }
+    }
+  } else if (warp == 10) {
+    // V on a warp of its own, so that a wait on one ring never holds up the other
+    if (elect_one()) {
+      int nv = 0;
+      for (; nv < nt; ++nv) {
+        const int j0 = (two ? ksteps.tile(nv) : ksteps.lo0 + nv) * BN;
+        const int sv = nv % NV;
+        if (nv >= NV && !mbar_wait(v_empty + sv, ((nv / NV) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(v_full + sv, C::KV_BYTES);
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sV + sv * C::KV_BYTES + c * BN * 128, &tmV, v_full + sv, c * 64, j0, bkv);
+      }
+      if (*abort_flag) drain_ring(v_full, NV, nv);
     }
   } else if (warp == 1) {
     if (elect_one()) {
@@ -1592,7 +1600,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       pm.out1 = dv;
       pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
       dim3 grid(g.B * g.Hkv, pm.n_tiles);
-      kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
+      kern<<<grid, kThreadsKv128, C::SMEM, s>>>(tq, tk, tv, tg, pm);
       return cudaGetLastError();
     } else {
       using C = Kv256PairCfg;
@@ -1626,7 +1634,7 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
     p.out1 = nullptr;
     p.n_tiles = (g.Lq + C::BMQ - 1) / C::BMQ;
     dim3 grid(g.B * g.Hq, p.n_tiles);
-    kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tg, p);
+    kern<<<grid, kThreadsKv128, C::SMEM, s>>>(tq, tk, tv, tg, p);
   } else {
     using C = DqCfg<D>;
     CUtensorMap tk, tv, tg;
