@@ -419,12 +419,7 @@ def roofline_record(kname: str, avg_ms: float, w, peaks: dict) -> dict:
     else:
         names = kname.split("+")
 
-        def issued_per_pair(n):
-            if n == "bwd_dkdv_tc" and D == 256:
-                return 10  # dV-only pass (S^T, dV) + dK-only pass (S^T, dP^T, dK)
-            return KERNEL_FLOPS_PER_PAIR_D.get(n, 4)
-
-        issued = sum(issued_per_pair(n) for n in names)
+        issued = sum(KERNEL_FLOPS_PER_PAIR_D.get(n, 4) for n in names)
         if names[0].startswith("fwd"):
             useful = USEFUL_FWD_PER_PAIR_D
         elif tuple(names) == CONCURRENT_BWD or set(names) == {"bwd_dkdv_simt", "bwd_dq_simt"}:

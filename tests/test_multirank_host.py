@@ -143,7 +143,8 @@ def test_roofline_counts_useful_flops_of_the_backward_pair():
     assert roof["flops_per_pair_d"] == 10 and roof["issued_flops_per_pair_d"] == 14
     assert roof["pairs"] == w.pairs()
     s = WORKLOADS["sliding_l8192_d256_w1024"]
-    assert bench.roofline_record(name, 1.0, s, peaks)["issued_flops_per_pair_d"] == 16
+    # D = 256 dK/dV on CTA pairs forms S^T once (S^T, dP^T, dV, dK), as at D <= 128
+    assert bench.roofline_record(name, 1.0, s, peaks)["issued_flops_per_pair_d"] == 14
     f = bench.roofline_record("fwd_tc", 7.4, w, peaks)
     assert f["flops_per_pair_d"] == 4 and abs(f["achieved"] - w.fwd_flops() / 7.4e-3 / 1e12) < 0.01
 
