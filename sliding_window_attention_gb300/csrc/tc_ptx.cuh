@@ -305,12 +305,23 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // Arrive on an mbarrier of another CTA of the cluster (shared::cluster address).
+//
+// Relaxed: the arrive is a signal and orders no memory operation.  Every
+// cross-CTA hand-off in these kernels signals work that has already finished
+// when the arrive is issued:
+//   - bulk copies waited on (cp.async.bulk.wait_group, or complete_tx seen);
+//   - Tensor Memory reads or writes ended by tcgen05.wait;
+//   - generic loads whose values the thread has already used.
+// No hand-off passes generic stores for the other CTA to read; those go
+// through cluster_sync().  A release at cluster scope stalls the issuing
+// thread about 1,000-1,300 cycles on this GB300 (clock64, every hand-off of
+// the D = 512 forward), which sat on every step's critical path.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// try_wait with cluster-scope acquire: data written by other CTAs of the
-// cluster before their release-arrive is visible afterwards.
+// try_wait with cluster-scope acquire, for barriers that other CTAs of the
+// cluster complete (remote arrives, multicast MMA commits, copies' complete_tx).
 __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
