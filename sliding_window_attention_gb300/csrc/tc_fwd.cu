@@ -99,12 +99,10 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
     if (sl2 >= 0.f) {
 #pragma unroll
       for (int e = 0; e < BN; e += 4) {
-        a0 = fmaxf(a0, __uint_as_float(sr[e]));
-        a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
-        a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
-        a3 = fmaxf(a3, __uint_as_float(sr[e + 3]));
+        a0 = fmax3(a0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+        a1 = fmax3(a1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
       }
-      return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
+      return fmaxf(a0, a1) * sl2;
     }
     float b0 = INFINITY, b1 = INFINITY, b2 = INFINITY, b3 = INFINITY;
 #pragma unroll
@@ -129,11 +127,14 @@ __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], floa
 
 // Pass 2: P = 2^(sl2 * s - m) for the row, rounded to fp16, packed two per
 // 32-bit TMEM column at p_taddr.  SUM: also returns the row sum of P (fp32);
-// otherwise the tensor core takes it.
+// otherwise the tensor core takes it.  On full tiles the scaling and the two
+// running sums use paired .f32x2 instructions (same roundings as scalar).
 template <int BN, bool FULL, bool SUM, bool TWO = false>
 __device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float sl2, float m_use, const int4& v,
                                                  uint32_t p_taddr) {
   float s0 = 0.f, s1 = 0.f;
+  const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+  uint64_t acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t pk[16];
@@ -142,8 +143,9 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float 
       const int col = c * 32 + e;
       float p0, p1;
       if (FULL) {
-        p0 = fast_exp2(fmaf(__uint_as_float(sr[col]), sl2, -m_use));
-        p1 = fast_exp2(fmaf(__uint_as_float(sr[col + 1]), sl2, -m_use));
+        const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sc2, nm2));
+        p0 = fast_exp2(x.x);
+        p1 = fast_exp2(x.y);
       } else {
         const float x0 = vis<TWO>(col, v) ? __uint_as_float(sr[col]) * sl2 : -INFINITY;
         const float x1 = vis<TWO>(col + 1, v) ? __uint_as_float(sr[col + 1]) * sl2 : -INFINITY;
@@ -151,13 +153,21 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t (&sr)[BN], float 
         p1 = fast_exp2(x1 - m_use);
       }
       if (SUM) {
-        s0 += p0;
-        s1 += p1;
+        if (FULL) {
+          acc2 = f2_add(acc2, f2_pack(p0, p1));
+        } else {
+          s0 += p0;
+          s1 += p1;
+        }
       }
       const __half2 hp = __floats2half2_rn(p0, p1);
       pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
     }
     tmem_st16(p_taddr + c * 16, pk);
+  }
+  if (FULL) {
+    const float2 t = f2_unpack(acc2);
+    return t.x + t.y;
   }
   return s0 + s1;
 }

@@ -96,8 +96,8 @@ struct Bars {
   uint64_t q_ready;              // (producer, own) Q in TMEM
   uint64_t pair_ready;           // (producer leader) both CTAs' Q in TMEM
   uint64_t s_full[2], s_free[2]; // (producer) S buffers: filled (both) / read (leader: 8 warps + relay)
-  uint64_t mx[2];                // (producer) both warpgroups posted their partial row max
-  uint64_t staged[2][2];         // (producer) a warpgroup wrote its half of staging tile [tile][warpgroup]
+  uint64_t mx[2][4];             // (producer) both warps of lane quarter q posted their partial row max [parity][q]
+  uint64_t staged[2][2];         // (producer) a warpgroup's 4 warps wrote its half of staging tile [tile][warpgroup]
   uint64_t stg_free[2][2];       // (producer) the store warp has read staging half [tile][warpgroup] out
   uint64_t scratch_free[2];      // (producer) the accumulator loaded scratch slot
   uint64_t tile_ready[2];        // (accumulator) the producer's tile for slot is in the scratch
@@ -150,24 +150,49 @@ __device__ __forceinline__ float half_max(const uint32_t (&sr)[64], float sl2, c
   return fmaxf(a0, a1);
 }
 
+// Maximum over 64 raw scores of one row, same exclusions as half_max.  For a
+// positive scale, half_max_raw * sl2 equals half_max exactly (rounding is
+// monotonic); three-input max halves the instructions.
+template <bool FULL, bool TWO = false>
+__device__ __forceinline__ float half_max_raw(const uint32_t (&sr)[64], const int4& v) {
+  float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 64; e += 4) {
+    float x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[k] = __uint_as_float(sr[e + k]);
+      if (!FULL) x[k] = vis<TWO>(e + k, v) ? x[k] : -INFINITY;
+    }
+    a0 = fmax3(a0, x[0], x[1]);
+    a1 = fmax3(a1, x[2], x[3]);
+  }
+  return fmaxf(a0, a1);
+}
+
 // P = 2^(sl2 s - m) for 64 entries as fp16 pairs; returns the fp32 row sum.
+// The scaling and the two running sums (even and odd entries) use paired
+// .f32x2 instructions: same roundings as scalar fmaf / adds, half the issue
+// slots.
 template <bool FULL, bool TWO = false>
 __device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, float m_use, const int4& v,
                                         uint32_t (&pk)[32]) {
-  float s0 = 0.f, s1 = 0.f;
+  const uint64_t sc = f2_pack(sl2, sl2), nm = f2_pack(-m_use, -m_use);
+  uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
-    float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), sl2, -m_use));
-    float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), sl2, -m_use));
+    const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc, nm));
+    float p0 = fast_exp2(x.x);
+    float p1 = fast_exp2(x.y);
     if (!FULL) {
       p0 = vis<TWO>(e, v) ? p0 : 0.f;
       p1 = vis<TWO>(e + 1, v) ? p1 : 0.f;
     }
-    s0 += p0;
-    s1 += p1;
+    acc = f2_add(acc, f2_pack(p0, p1));
     pk[e >> 1] = pack_half2(p0, p1);
   }
-  return s0 + s1;
+  const float2 t = f2_unpack(acc);
+  return t.x + t.y;
 }
 
 __global__ void __launch_bounds__(kThr, 1)
@@ -214,9 +239,9 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->s_free[s], leader ? 9 : 8);
-      mbar_init(&bars->mx[s], 256);
-      mbar_init(&bars->staged[s][0], 128);
-      mbar_init(&bars->staged[s][1], 128);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->mx[s][q], 2);  // one arrival per warp
+      mbar_init(&bars->staged[s][0], 4);
+      mbar_init(&bars->staged[s][1], 4);
       mbar_init(&bars->stg_free[s][0], 1);
       mbar_init(&bars->stg_free[s][1], 1);
       mbar_init(&bars->scratch_free[s], 1);
@@ -499,11 +524,18 @@ __global__ void __launch_bounds__(kThr, 1)
       bool both;
       const int4 vv = vis_in_tile(row_vis(g, i, j0 + cb0), 64, &both);
       const bool two_here = two && __any_sync(0xffffffffu, both);
-      const float pmax = full ? half_max<true>(sr, sl2, vv)
-                              : (two_here ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
+      float pmax;
+      if (sl2 > 0.f)
+        pmax = sl2 * (full ? half_max_raw<true>(sr, vv)
+                           : (two_here ? half_max_raw<false, true>(sr, vv) : half_max_raw<false>(sr, vv)));
+      else
+        pmax = full ? half_max<true>(sr, sl2, vv)
+                    : (two_here ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
+      // the two warps of this lane quarter exchange their halves' maxima
       xm[(bb * 2 + wg) * 128 + r] = pmax;
-      mbar_arrive(&bars->mx[bb]);
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->mx[bb], (n >> 1) & 1, abort_flag, R))) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->mx[bb][q4]);
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->mx[bb][q4], (n >> 1) & 1, abort_flag, R))) {
         ok = false;
         break;
       }
@@ -531,7 +563,8 @@ __global__ void __launch_bounds__(kThr, 1)
         st_smem_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       if (wg == 0) alph[bb * 128 + r] = alpha;
       fence_proxy_async_smem();
-      mbar_arrive(&bars->staged[bb][wg]);  // the store warp takes the tile from here
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->staged[bb][wg]);  // the store warp takes the tile from here
       bars->n_sent[wg] = n + 1;
     }
     // row sum = the two warpgroups' partial sums (same running max); lse; send 1 / l
