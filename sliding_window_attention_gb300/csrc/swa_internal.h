@@ -243,6 +243,11 @@ cudaError_t make_tmap_f16(CUtensorMap* m, const void* ptr, int D, int L, int hea
 cudaError_t make_tmap_f16_chunks(CUtensorMap* m, const void* ptr, int D, int L, int heads, int box_rows,
                                  int nchunk);
 
+// 3-D fp32 tensor map over an output [heads, L, D] for the D = 512 epilogues:
+// 32 x 32 boxes (128-byte rows) with 128-byte swizzle; TMA stores clip rows
+// at or beyond L.
+cudaError_t make_tmap_f32_out(CUtensorMap* m, void* ptr, int D, int L, int heads);
+
 bool bwd_tc_supported(int D);
 // Padded row count of the backward's row-statistics array.
 int bwd_stats_lpad(int L);

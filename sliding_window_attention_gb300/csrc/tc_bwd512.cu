@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kThr, 1)
                    const __grid_constant__ CUtensorMap tmR,   // resident dP operand, 128 rows x 1 chunk: V / dO
                    const __grid_constant__ CUtensorMap tmA0,  // dV accumulator operand, 128 rows x 2 chunks: dO
                    const __grid_constant__ CUtensorMap tmA1,  // dK / dQ accumulator operand: Q / K
+                   const __grid_constant__ CUtensorMap tmO0,  // fp32 output out0 (dk / dq), 32 x 32 boxes
+                   const __grid_constant__ CUtensorMap tmO1,  // fp32 output out1 (dv; dQ pass: out0 again)
                    const ParamsPair p) {
   using C = PassCfg<DIR>;
   constexpr int NPP = C::NPP, RS = C::RS, NRECV = C::NRECV, NR_A = C::NR_A, OFF_RING_A = C::OFF_RING_A;
@@ -686,7 +688,6 @@ __global__ void __launch_bounds__(kThr, 1)
   } else {
     // ------------------------------------------------------------ epilogue (accumulator roles, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
-    const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     if (warp >= 2 + NPP && warp < 2 + 2 * NPP && elect_one()) {
       // one loader per producer pair (warps 2 + NPP ..): once the MMAs are
@@ -732,33 +733,15 @@ __global__ void __launch_bounds__(kThr, 1)
     __syncwarp();
     if (__all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R))) {
       tc_fence_after();
-      const int row = r0 + r;
-      const bool row_ok = row < LX;
-      float* dst;
       float mul;
       const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
-      if (DIR == kDirKV) {
-        dst = (role == kRoleAccP) ? p.out1 : p.out0;
-        mul = (role == kRoleAccP) ? inv_s : g.scale * inv_s;
-      } else {
-        dst = p.out0;
-        mul = g.scale * inv_s;
-      }
-      dst += ((size_t)head * LX + (row_ok ? row : 0)) * DH;
-#pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        const int c = 256 * wg + 32 * cc;
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + c, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
+      if (DIR == kDirKV) mul = (role == kRoleAccP) ? inv_s : g.scale * inv_s;
+      else mul = g.scale * inv_s;
+      const CUtensorMap* om = (DIR == kDirKV && role == kRoleAccP) ? &tmO1 : &tmO0;
+      // every operand slot and ring load has been consumed by the finished
+      // MMAs: each of warps 2-9 stages its blocks in 16 KB of that space
+      tmem_rows_store_tma(om, tmem + lane_off + 256 * wg, 256 * wg, 256, mul, sbase + (uint32_t)(warp - 2) * 16384u,
+                          r0 + 32 * q4, head, lane);
     }
   }
 
@@ -809,8 +792,16 @@ cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16,
   // streamed operands (64-row halves, two chunks per slice), the resident dP
   // operand (one chunk of 128 rows per load), accumulator operands (two chunks
   // of 128 rows per load)
-  CUtensorMap tmS, tmP, tmR, tmA0, tmA1;
+  CUtensorMap tmS, tmP, tmR, tmA0, tmA1, tmO0, tmO1;
   cudaError_t e;
+  // fp32 outputs: [B Hkv, L, D] dk and dv (dK/dV pass), [B Hq, Lq, D] dq (dQ pass)
+  if (DIR == kDirKV) {
+    if ((e = make_tmap_f32_out(&tmO0, out0, DH, g.L, g.B * g.Hkv)) != cudaSuccess) return e;
+    if ((e = make_tmap_f32_out(&tmO1, out1, DH, g.L, g.B * g.Hkv)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_tmap_f32_out(&tmO0, out0, DH, g.Lq, g.B * g.Hq)) != cudaSuccess) return e;
+    tmO1 = tmO0;
+  }
   if (DIR == kDirKV) {
     if ((e = make_tmap_f16_chunks(&tmS, q16, DH, g.Lq, g.B * g.Hq, HT, 2)) != cudaSuccess) return e;
     if ((e = make_tmap_f16_chunks(&tmP, g16, DH, g.Lq, g.B * g.Hq, HT, 2)) != cudaSuccess) return e;
@@ -852,7 +843,7 @@ cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmS, tmP, tmR, tmA0, tmA1, pm);
+  return cudaLaunchKernelEx(&cfg, kern, tmS, tmP, tmR, tmA0, tmA1, tmO0, tmO1, pm);
 }
 
 }  // namespace

@@ -94,7 +94,7 @@ struct FwdParams {
 // masked in the scaled domain, which is correct for any sign of the scale.
 template <int BN, bool FULL, bool TWO = false>
 __device__ __forceinline__ float softmax_tile_max(const uint32_t (&sr)[BN], float sl2, const int4& v) {
-  float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+  float a0 = -INFINITY, a1 = -INFINITY;
   if constexpr (FULL) {
     if (sl2 >= 0.f) {
 #pragma unroll
@@ -884,6 +884,19 @@ cudaError_t make_tmap_f16_chunks(CUtensorMap* m, const void* ptr, int D, int L, 
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_f32_out(CUtensorMap* m, void* ptr, int D, int L, int heads) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  if (D % 32) return cudaErrorInvalidValue;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * L * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 

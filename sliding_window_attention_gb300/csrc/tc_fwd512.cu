@@ -197,6 +197,7 @@ __device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, flo
 
 __global__ void __launch_bounds__(kThr, 1)
     fwd512_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmO,  // fp32 o, 32 x 32 boxes
                    const FwdPairParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -589,7 +590,6 @@ __global__ void __launch_bounds__(kThr, 1)
     // ------------------------------------------------------------ rescale + epilogue (accumulators, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
-    const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const float* ralph = reinterpret_cast<const float*>(base + OFF_RVEC);  // [2][128]
     const float* rinv = ralph + 256;                                       // [128]
@@ -633,22 +633,10 @@ __global__ void __launch_bounds__(kThr, 1)
                                          mbar_wait_cl(&bars->fin_full, 0, abort_flag, R))) {
       tc_fence_after();
       const float inv = rinv[r];
-      const bool row_ok = i < g.Lq;
-      float* orow = p.o + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * DH;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        const int col = 256 * wg + 32 * c;
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + col, v);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(orow + col + e) =
-                make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                            __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-        }
-      }
+      // every V ring load has been consumed by the finished MMAs: each of
+      // warps 2-9 stages its O blocks in 16 KB of the ring
+      tmem_rows_store_tma(&tmO, tmem + lane_off + 256 * wg, 256 * wg, 256, inv,
+                          sbase + OFF_RING_A + (uint32_t)(warp - 2) * 16384u, i0 + 32 * q4, bh, lane);
     }
   }
 
@@ -702,12 +690,13 @@ int scratch_layout_fwd512() {
 
 cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
                              float* lse, int* status, cudaStream_t s) {
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, to;
   cudaError_t e;
   // K: 64 keys x four 64-column chunks per instruction (32 KB, one CTA's half
   // of a 256-column slice); V: 128 keys x two chunks (32 KB)
   if ((e = make_tmap_f16_chunks(&tk, k, DH, g.L, g.B * g.Hkv, HT, 4)) != cudaSuccess) return e;
   if ((e = make_tmap_f16_chunks(&tv, v16, DH, g.L, g.B * g.Hkv, T, 2)) != cudaSuccess) return e;
+  if ((e = make_tmap_f32_out(&to, o, DH, g.Lq, g.B * g.Hq)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(fwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM)) !=
       cudaSuccess)
     return e;
@@ -730,7 +719,7 @@ cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd512_kernel, tk, tv, pm);
+  return cudaLaunchKernelEx(&cfg, fwd512_kernel, tk, tv, to, pm);
 }
 
 }  // namespace swa

@@ -505,6 +505,60 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // This thread's bulk stores have completed their writes.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// All but this thread's N most recent bulk async-groups have read their sources.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Tiled TMA store of one box from this CTA's shared memory, in this thread's
+// current bulk async-group.  Box elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src_cta, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src_cta), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Epilogue of a 512-column fp32 accumulator row block through TMA stores.
+// The calling warp writes its 32 TMEM lanes (rows row0 .. row0 + 31 of
+// `head`), columns [col0, col0 + ncols) (ncols a multiple of 32), each value
+// times `mul`.  Per 32-column chunk: tcgen05.ld, the 32 x 32 fp32 block
+// written to one of four 4 KB shared-memory buffers at `buf` (1 KB aligned,
+// this warp's own) in the 128-byte swizzle of the tensor map, then lane 0
+// stores it with one TMA instruction.  Compared with per-thread 16-byte row
+// stores, whose every warp instruction touches 32 cache lines, the TMA unit
+// writes whole lines.  Rows at or beyond the tensor's length are clipped by
+// the TMA unit.  Lane 0 waits for its stores' writes before it returns.
+__device__ __forceinline__ void tmem_rows_store_tma(const CUtensorMap* map, uint32_t taddr, int col0, int ncols,
+                                                    float mul, uint32_t buf, int row0, int head, int lane) {
+#pragma unroll 1
+  for (int cc = 0; cc < ncols / 32; ++cc) {
+    uint32_t a[32];
+    tmem_ld32(taddr + 32 * cc, a);
+    tmem_wait_ld();
+    const uint32_t b = buf + (uint32_t)(cc & 3) * 4096u;
+    if (cc >= 4) {
+      // the store of chunk cc - 4 has read buffer cc & 3
+      if (lane == 0) bulk_wait_read<3>();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      st_smem_v4(b + (uint32_t)lane * 128u + ((uint32_t)(u ^ (lane & 7)) << 4),
+                 __float_as_uint(__uint_as_float(a[4 * u]) * mul), __float_as_uint(__uint_as_float(a[4 * u + 1]) * mul),
+                 __float_as_uint(__uint_as_float(a[4 * u + 2]) * mul),
+                 __float_as_uint(__uint_as_float(a[4 * u + 3]) * mul));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(map, b, col0 + 32 * cc, row0, head);
+      bulk_commit_group();
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
 // Orders generic-proxy accesses to global memory with async-proxy ones.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
