@@ -287,6 +287,8 @@ template <int D, bool TWO>
 __global__ void __launch_bounds__(kThreadsKv128, 1)
     dkdv128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                      const __grid_constant__ CUtensorMap tmO0,  // fp32 dk, 32 x 32 boxes
+                      const __grid_constant__ CUtensorMap tmO1,  // fp32 dv
                       const BwdParams p) {
   using C = Kv128Cfg<D>;
   constexpr int BNK = C::BNK, BM = C::BM, NQ = C::NQ, NG = C::NG, KCH = C::KCH, CW = C::CW;
@@ -551,26 +553,14 @@ __global__ void __launch_bounds__(kThreadsKv128, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
-      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
-      const bool row_ok = j < g.L;
-      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV, through TMA
+      // stores staged in 16 KB per warp of the (all consumed) K, V and rings
       const uint32_t col = wg == 0 ? C::DK_COL : C::DV_COL;
       const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
       const float mul = wg == 0 ? g.scale * inv_s : inv_s;
-      float* dst = (wg == 0 ? p.out0 : p.out1) + off;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + col + c * 32, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
+      tmem_rows_store_tma(wg == 0 ? &tmO0 : &tmO1, tmem + lane_off + col, 0, D, mul,
+                          smem_u32(base) + (uint32_t)(warp - 2) * 16384u, j - (int)(threadIdx.x & 31), bkv,
+                          (int)(threadIdx.x & 31));
     }
   }
 
@@ -663,6 +653,8 @@ template <bool TWO>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     dkdv256_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                        const __grid_constant__ CUtensorMap tmO0,  // fp32 dk, 32 x 32 boxes
+                        const __grid_constant__ CUtensorMap tmO1,  // fp32 dv
                         const BwdParams p) {
   using C = Kv256PairCfg;
   constexpr int BNK = C::BNK, BM = C::BM, CW = C::CW, KCH = C::KCH, D = C::D;
@@ -1007,26 +999,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R))) {
       tc_fence_after();
-      // each warpgroup writes half of the accumulator's columns (dK scaled)
-      const bool row_ok = j < g.L;
-      const size_t off = ((size_t)bkv * g.L + (row_ok ? j : 0)) * D;
+      // each warpgroup writes half of the accumulator's columns (dK scaled),
+      // through TMA stores staged in 16 KB per warp of the first 128 KB (the
+      // consumed resident operand and tiles; rank 0's P^T staging lies above)
       const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
       const float mul = dvr ? inv_s : g.scale * inv_s;
-      float* dst = (dvr ? p.out1 : p.out0) + off;
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = wg * (D / 64) + cc;
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + C::ACC_COL + c * 32, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
+      tmem_rows_store_tma(dvr ? &tmO1 : &tmO0, tmem + lane_off + C::ACC_COL + wg * (D / 2), wg * (D / 2), D / 2, mul,
+                          smem_u32(base) + (uint32_t)(warp - 2) * 16384u, j - (int)(threadIdx.x & 31), bkv,
+                          (int)(threadIdx.x & 31));
     }
   }
 
@@ -1074,7 +1054,9 @@ struct DqCfg {
 template <int D, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                 const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+                 const __grid_constant__ CUtensorMap tmG,
+                 const __grid_constant__ CUtensorMap tmO,  // fp32 dq, 32 x 32 boxes
+                 const BwdParams p) {
   using C = DqCfg<D>;
   constexpr int BMQ = C::BMQ, BN = C::BN, NS = C::NS, KCH = C::KCH, CW = C::CW;
   extern __shared__ unsigned char smem_raw[];
@@ -1268,22 +1250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
-      // each warpgroup writes half of the dQ columns
-      float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
+      // each warpgroup writes half of the dQ columns, through TMA stores
+      // staged in 16 KB per warp of the (all consumed) tiles and rings
       const float mul = g.scale * p.stats[dscale_offset(g, p.Lpad) + 1];  // scale / s
-#pragma unroll
-      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + C::DQ_COL + c * 32, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(row + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
+      tmem_rows_store_tma(&tmO, tmem + lane_off + C::DQ_COL + wg * (D / 2), wg * (D / 2), D / 2, mul,
+                          smem_u32(base) + (uint32_t)(warp - 2) * 16384u, i - (int)(threadIdx.x & 31), bh,
+                          (int)(threadIdx.x & 31));
     }
   }
 
@@ -1330,6 +1302,7 @@ template <int D, bool TWO>
 __global__ void __launch_bounds__(kThreadsKv128, 1)
     dq128_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                    const __grid_constant__ CUtensorMap tmO,  // fp32 dq, 32 x 32 boxes
                     const BwdParams p) {
   using C = Dq128Cfg<D>;
   constexpr int BMQ = C::BMQ, BN = C::BN, NK = C::NK, NV = C::NV, KCH = C::KCH, CW = C::CW;
@@ -1542,22 +1515,12 @@ __global__ void __launch_bounds__(kThreadsKv128, 1)
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag))) {
       tc_fence_after();
-      const bool row_ok = i < g.Lq;
-      float* row = p.out0 + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * D;
+      // each warpgroup writes half the columns, through TMA stores staged in
+      // 16 KB per warp of the (all consumed) dO tile and K / V stages
       const float mul = g.scale * p.stats[dscale_offset(g, p.Lpad) + 1];  // scale / s
-#pragma unroll
-      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {  // each warpgroup writes half the columns
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_off + C::DQ_COL + c * 32, a);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(row + c * 32 + e) =
-                make_float4(__uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-        }
-      }
+      tmem_rows_store_tma(&tmO, tmem + lane_off + C::DQ_COL + wg * (D / 2), wg * (D / 2), D / 2, mul,
+                          smem_u32(base) + (uint32_t)(warp - 2) * 16384u, i - (int)(threadIdx.x & 31), bh,
+                          (int)(threadIdx.x & 31));
     }
   }
 
@@ -1600,7 +1563,10 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       pm.out1 = dv;
       pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
       dim3 grid(g.B * g.Hkv, pm.n_tiles);
-      kern<<<grid, kThreadsKv128, C::SMEM, s>>>(tq, tk, tv, tg, pm);
+      CUtensorMap tdk, tdv;
+      if ((e2 = make_tmap_f32_out(&tdk, dk, D, g.L, g.B * g.Hkv)) != cudaSuccess) return e2;
+      if ((e2 = make_tmap_f32_out(&tdv, dv, D, g.L, g.B * g.Hkv)) != cudaSuccess) return e2;
+      kern<<<grid, kThreadsKv128, C::SMEM, s>>>(tq, tk, tv, tg, tdk, tdv, pm);
       return cudaGetLastError();
     } else {
       using C = Kv256PairCfg;
@@ -1617,7 +1583,10 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
       pm.out1 = dv;
       pm.n_tiles = (g.L + C::BNK - 1) / C::BNK;
       dim3 grid(2 * g.B * g.Hkv, pm.n_tiles);  // clusters of 2 along x: (dV CTA, dK CTA) of a key tile
-      kern<<<grid, kPairThreads, C::SMEM, s>>>(tq, tk, tv, tg, pm);
+      CUtensorMap tdk, tdv;
+      if ((e = make_tmap_f32_out(&tdk, dk, D, g.L, g.B * g.Hkv)) != cudaSuccess) return e;
+      if ((e = make_tmap_f32_out(&tdv, dv, D, g.L, g.B * g.Hkv)) != cudaSuccess) return e;
+      kern<<<grid, kPairThreads, C::SMEM, s>>>(tq, tk, tv, tg, tdk, tdv, pm);
       return cudaGetLastError();
     }
   } else if constexpr (D <= 128) {
@@ -1634,7 +1603,9 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
     p.out1 = nullptr;
     p.n_tiles = (g.Lq + C::BMQ - 1) / C::BMQ;
     dim3 grid(g.B * g.Hq, p.n_tiles);
-    kern<<<grid, kThreadsKv128, C::SMEM, s>>>(tq, tk, tv, tg, p);
+    CUtensorMap tdq;
+    if ((e = make_tmap_f32_out(&tdq, dq, D, g.Lq, g.B * g.Hq)) != cudaSuccess) return e;
+    kern<<<grid, kThreadsKv128, C::SMEM, s>>>(tq, tk, tv, tg, tdq, p);
   } else {
     using C = DqCfg<D>;
     CUtensorMap tk, tv, tg;
@@ -1649,7 +1620,9 @@ cudaError_t bwd_tc_d(const Geom& g, const uint16_t* q16, const uint16_t* k16, co
     p.x16 = q16;
     p.n_tiles = (g.Lq + C::BMQ - 1) / C::BMQ;
     dim3 grid(g.B * g.Hq, p.n_tiles);
-    kern<<<grid, kThreads, C::SMEM, s>>>(tk, tv, tg, p);
+    CUtensorMap tdq;
+    if ((e = make_tmap_f32_out(&tdq, dq, D, g.Lq, g.B * g.Hq)) != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::SMEM, s>>>(tk, tv, tg, tdq, p);
   }
   return cudaGetLastError();
 }

@@ -520,27 +520,30 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
-// Epilogue of a 512-column fp32 accumulator row block through TMA stores.
-// The calling warp writes its 32 TMEM lanes (rows row0 .. row0 + 31 of
-// `head`), columns [col0, col0 + ncols) (ncols a multiple of 32), each value
-// times `mul`.  Per 32-column chunk: tcgen05.ld, the 32 x 32 fp32 block
-// written to one of four 4 KB shared-memory buffers at `buf` (1 KB aligned,
-// this warp's own) in the 128-byte swizzle of the tensor map, then lane 0
-// stores it with one TMA instruction.  Compared with per-thread 16-byte row
-// stores, whose every warp instruction touches 32 cache lines, the TMA unit
-// writes whole lines.  Rows at or beyond the tensor's length are clipped by
-// the TMA unit.  Lane 0 waits for its stores' writes before it returns.
+// Epilogue of an fp32 accumulator row block through TMA stores.  The
+// calling warp writes its 32 TMEM lanes (rows row0 .. row0 + 31 of `head`),
+// columns [col0, col0 + ncols) (ncols a multiple of 32), each value times
+// `mul` (per lane).  Per 32-column chunk: tcgen05.ld, the 32 x 32 fp32 block
+// written to one of NBUF 4 KB shared-memory buffers at `buf` (1 KB aligned,
+// this warp's own) in the 128-byte swizzle of the tensor map
+// (make_tmap_f32_out), then lane 0 stores it with one TMA instruction.
+// Compared with per-thread 16-byte row stores, whose every warp instruction
+// touches 32 cache lines, the TMA unit writes whole lines.  Rows at or beyond
+// the tensor's length are clipped by the TMA unit.  Lane 0 waits for its
+// stores' writes before it returns.
+template <int NBUF = 4>
 __device__ __forceinline__ void tmem_rows_store_tma(const CUtensorMap* map, uint32_t taddr, int col0, int ncols,
                                                     float mul, uint32_t buf, int row0, int head, int lane) {
+  static_assert(NBUF >= 1 && NBUF <= 4, "buffers");
 #pragma unroll 1
   for (int cc = 0; cc < ncols / 32; ++cc) {
     uint32_t a[32];
     tmem_ld32(taddr + 32 * cc, a);
     tmem_wait_ld();
-    const uint32_t b = buf + (uint32_t)(cc & 3) * 4096u;
-    if (cc >= 4) {
-      // the store of chunk cc - 4 has read buffer cc & 3
-      if (lane == 0) bulk_wait_read<3>();
+    const uint32_t b = buf + (uint32_t)(cc % NBUF) * 4096u;
+    if (cc >= NBUF) {
+      // the store of chunk cc - NBUF has read buffer cc % NBUF
+      if (lane == 0) bulk_wait_read<NBUF - 1>();
       __syncwarp();
     }
 #pragma unroll
