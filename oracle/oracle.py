@@ -20,6 +20,10 @@ non-causal band |i + Lk - Lq - j| < window (no mask at all for window 0).
 causal self-attention in which rejected rows do not see chosen keys and the
 window is measured on logical positions (the rejected response restarts at
 position P).  It needs Lq = Lk and causal.
+
+``sinks`` (forward and backward): one sink logit per query head (Hq values),
+an extra term of every row's softmax normaliser that carries no value; the
+backward then also returns ``dsinks``.  Not combined with ``prefix``.
 """
 from __future__ import annotations
 
@@ -69,9 +73,13 @@ def _load():
             lib.swa_oracle_bwd_px.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, L, D, I, P, P, P, P, P, P, P]
             lib.swa_oracle_rows_px.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, L, D, I, L, L, P, L, P, P, P, P]
             lib.swa_oracle_key_rows_px.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, L, D, I, L, L, P, L, P, P]
+            # attention sinks: the sink logits [Hq] (fp64) after v (after dO for the backward)
+            lib.swa_oracle_fwd_sk.argtypes = [P, P, P, P, I, L, L, L, L, L, L, L, I, D, P, P]
+            lib.swa_oracle_bwd_sk.argtypes = [P, P, P, P, P, I, L, L, L, L, L, L, L, I, D, P, P, P, P, P, P, P, P]
             for f in (lib.swa_oracle_fwd_ex, lib.swa_oracle_bwd_ex, lib.swa_oracle_rows_ex,
                       lib.swa_oracle_key_rows_ex, lib.swa_oracle_fwd_px, lib.swa_oracle_bwd_px,
-                      lib.swa_oracle_rows_px, lib.swa_oracle_key_rows_px):
+                      lib.swa_oracle_rows_px, lib.swa_oracle_key_rows_px, lib.swa_oracle_fwd_sk,
+                      lib.swa_oracle_bwd_sk):
                 f.restype = ctypes.c_int
             lib.swa_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -133,13 +141,37 @@ def _plan(prefix, causal, Lq, Lk):
     return P, Rc
 
 
-def forward(q, k, v, window: int, scale: float, band_only: bool = False, causal: bool = True, prefix=None):
+def _sinks(sinks, Hq, prefix):
+    """The sink logits as a contiguous fp64 [Hq] array, checked, or None."""
+    if sinks is None:
+        return None
+    if prefix is not None:
+        raise ValueError("sinks are not combined with a shared-prefix plan")
+    try:
+        import torch
+
+        if isinstance(sinks, torch.Tensor):
+            sinks = sinks.detach().cpu().to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(sinks, dtype=np.float64).reshape(-1))
+    if a.size != Hq:
+        raise ValueError(f"sinks needs one value per query head ({Hq}), got {a.size}")
+    return a
+
+
+def forward(q, k, v, window: int, scale: float, band_only: bool = False, causal: bool = True, prefix=None,
+            sinks=None):
     """Return (o [B,Hq,Lq,D], lse [B,Hq,Lq]) in fp64."""
     arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v)
     plan = _plan(prefix, causal, Lq, Lk)
+    sk = _sinks(sinks, Hq, prefix)
     o = np.empty((B, Hq, Lq, D), np.float64)
     lse = np.empty((B, Hq, Lq), np.float64)
-    if plan:
+    if sk is not None:
+        rc = _load().swa_oracle_fwd_sk(*map(_ptr, arrs), _ptr(sk), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
+                                       int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+    elif plan:
         rc = _load().swa_oracle_fwd_px(*map(_ptr, arrs), f64, B, Hq, Hkv, Lk, D, int(window), *plan, float(scale),
                                        int(band_only), _ptr(o), _ptr(lse))
     else:
@@ -150,17 +182,24 @@ def forward(q, k, v, window: int, scale: float, band_only: bool = False, causal:
     return o, lse
 
 
-def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False, causal: bool = True, prefix=None):
-    """Return dict with o, lse, delta, dq, dk, dv (fp64) and delta_gap."""
+def backward(q, k, v, dO, window: int, scale: float, band_only: bool = False, causal: bool = True, prefix=None,
+             sinks=None):
+    """Return dict with o, lse, delta, dq, dk, dv (fp64) and delta_gap (and dsinks [Hq] with sinks)."""
     arrs, f64, (B, Hq, Hkv, Lq, Lk, D) = _prep(q, k, v, dO)
     plan = _plan(prefix, causal, Lq, Lk)
+    sk = _sinks(sinks, Hq, prefix)
     out = dict(
         o=np.empty((B, Hq, Lq, D)), lse=np.empty((B, Hq, Lq)), delta=np.empty((B, Hq, Lq)),
         dq=np.empty((B, Hq, Lq, D)), dk=np.empty((B, Hkv, Lk, D)), dv=np.empty((B, Hkv, Lk, D)),
     )
     gap = ctypes.c_double(0.0)
     outs = [_ptr(out[n]) for n in ("o", "lse", "delta", "dq", "dk", "dv")]
-    if plan:
+    if sk is not None:
+        out["dsinks"] = np.empty(Hq)
+        a = list(map(_ptr, arrs))
+        rc = _load().swa_oracle_bwd_sk(*a[:4], _ptr(sk), f64, B, Hq, Hkv, Lq, Lk, D, int(window),
+                                       int(bool(causal)), float(scale), *outs, _ptr(out["dsinks"]), ctypes.byref(gap))
+    elif plan:
         rc = _load().swa_oracle_bwd_px(*map(_ptr, arrs), f64, B, Hq, Hkv, Lk, D, int(window), *plan, float(scale),
                                        int(band_only), *outs, ctypes.byref(gap))
     else:

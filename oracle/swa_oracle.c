@@ -42,6 +42,23 @@
  *
  * The *_px entry points take (P, Rc); they are causal self-attention.
  *
+ * Attention sinks (the *_sk entry points): one logit c_h per query head, a
+ * term of every row's softmax normaliser that carries no value.  The pages
+ * name sinks only as a parameter of the attention backward primitive,
+ * beside scale and causal ("Lab 028 lab detail: Off NVIDIA, you fix the
+ * platform yourself", "What I changed, in plain terms" item 2); the reading
+ * taken is the per-head logit that the softmax normalises against:
+ *
+ *   lse_i = ln( sum_j exp(s_ij) + exp(c_h) )
+ *   P_ij  = exp(s_ij - lse_i),   o_i = sum_j P_ij v_j
+ *   dq, dk, dv and Delta_i as above (with this lse)
+ *   dc_h  = - sum_{b, i} exp(c_h - lse_i) Delta_i
+ *
+ * The last line is d(loss)/dc_h: c_h enters o_i only through lse_i, and
+ * d o_i / d c_h = -exp(c_h - lse_i) o_i, so the chain rule with dO_i gives
+ * -exp(c_h - lse_i) dO_i . o_i = -exp(c_h - lse_i) Delta_i.  A sink of -inf
+ * is no sink.
+ *
  * Passages followed:
  *  - Mask rule: "Lab 028 lab detail: Off NVIDIA, you fix the platform
  *    yourself", "Plan for the build" step 4 (P is zeroed where
@@ -98,6 +115,7 @@ typedef struct {
     long off;                 /* Lk - Lq: position of query 0 among the keys */
     int plan;                 /* 1: shared-prefix mask over [prompt; chosen; rejected] */
     long P, Rc;               /* prompt and chosen-response lengths (plan only) */
+    const double* sinks;      /* [Hq] sink logits, or NULL for none */
 } ctx_t;
 
 /* Logical position of sequence position x under the shared-prefix plan: the
@@ -209,9 +227,12 @@ static void row_pass(const ctx_t* c, long b, long h, long i, double* s, double* 
         s[j] = c->scale * acc;
         if (s[j] > m) m = s[j];
     }
-    /* logsumexp */
+    /* logsumexp (with the head's sink logit as one more term) */
+    const double sink = c->sinks ? c->sinks[h] : -INFINITY;
+    if (sink > m) m = sink;
     double sum = 0.0;
     for (long j = j0; j <= j1; ++j) sum += exp(s[j] - m);
+    if (c->sinks) sum += exp(sink - m);
     const double lse_i = m + log(sum);
     *lse = lse_i;
     /* output */
@@ -296,7 +317,8 @@ static int check_shape(long B, long Hq, long Hkv, long Lq, long Lk, long D, long
 static ctx_t make_ctx(const void* q, const void* k, const void* v, const void* dO, int is_f64, long B,
                       long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal, double scale,
                       int band_only) {
-    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal ? 1 : 0, scale, band_only, Lk - Lq, 0, 0, 0};
+    ctx_t c = {q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal ? 1 : 0, scale, band_only, Lk - Lq, 0, 0, 0,
+               NULL};
     return c;
 }
 
@@ -592,4 +614,40 @@ int swa_oracle_bwd(const void* q, const void* k, const void* v, const void* dO, 
                    double* dk, double* dv, double* delta_gap) {
     return swa_oracle_bwd_ex(q, k, v, dO, is_f64, B, Hq, Hkv, L, L, D, W, 1, scale, band_only, o, lse,
                              delta, dq, dk, dv, delta_gap);
+}
+
+/*
+ * With attention sinks (see the header): sinks [Hq] fp64.  The forward and
+ * backward are those of the _ex entry points with the sink term in every
+ * row's normaliser; the backward also writes dsinks [Hq], summed over the
+ * batch and the rows in ascending order.
+ */
+int swa_oracle_fwd_sk(const void* q, const void* k, const void* v, const double* sinks, int is_f64, long B,
+                      long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal, double scale, double* o,
+                      double* lse) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W) || !sinks) return -1;
+    ctx_t c = make_ctx(q, k, v, NULL, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, 0);
+    c.sinks = sinks;
+    return fwd_impl(&c, o, lse);
+}
+
+int swa_oracle_bwd_sk(const void* q, const void* k, const void* v, const void* dO, const double* sinks,
+                      int is_f64, long B, long Hq, long Hkv, long Lq, long Lk, long D, long W, int causal,
+                      double scale, double* o, double* lse, double* delta, double* dq, double* dk, double* dv,
+                      double* dsinks, double* delta_gap) {
+    if (check_shape(B, Hq, Hkv, Lq, Lk, D, W) || !sinks || !dsinks) return -1;
+    ctx_t c = make_ctx(q, k, v, dO, is_f64, B, Hq, Hkv, Lq, Lk, D, W, causal, scale, 0);
+    c.sinks = sinks;
+    const int err = bwd_impl(&c, o, lse, delta, dq, dk, dv, delta_gap);
+    if (err) return err;
+    for (long h = 0; h < Hq; ++h) {
+        double acc = 0.0;
+        for (long b = 0; b < B; ++b)
+            for (long i = 0; i < Lq; ++i) {
+                const long r = (b * Hq + h) * Lq + i;
+                acc += exp(sinks[h] - lse[r]) * delta[r];
+            }
+        dsinks[h] = -acc;
+    }
+    return 0;
 }

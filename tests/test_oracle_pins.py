@@ -631,3 +631,91 @@ def test_prefix_chosen_keys_get_no_gradient_from_rejected_rows(oracle_mod):
     assert np.all(r["dk"][:, :, P:P + Rc] == 0.0) and np.all(r["dv"][:, :, P:P + Rc] == 0.0)
     assert np.all(r["dq"][:, :, :P + Rc] == 0.0)
     assert np.any(r["dk"][:, :, :P] != 0.0) and np.any(r["dv"][:, :, P + Rc:] != 0.0)
+
+
+# ---------------------------------------------------------------------------
+# attention sinks: one logit per query head in every row's softmax normaliser
+# (the backward primitive's "sinks" parameter, "Lab 028 lab detail: Off
+# NVIDIA, you fix the platform yourself", "What I changed, in plain terms"
+# item 2; the reading is stated in the oracle's header)
+
+
+def _torch_reference_sinks(q, k, v, dO, window, scale, causal, sinks):
+    """Independent path: the sink as one extra logit column of a torch fp64
+    softmax (its probability dropped before P V), differentiated by autograd
+    with respect to q, k, v and the sinks."""
+    q = q.double().clone().requires_grad_(True)
+    k = k.double().clone().requires_grad_(True)
+    v = v.double().clone().requires_grad_(True)
+    c = torch.as_tensor(sinks, dtype=torch.float64).clone().requires_grad_(True)
+    B, Hq, Lq, D = q.shape
+    Lk = k.shape[2]
+    G = Hq // k.shape[1]
+    kr = k.repeat_interleave(G, dim=1)
+    vr = v.repeat_interleave(G, dim=1)
+    s = scale * torch.matmul(q, kr.transpose(-1, -2))
+    a = torch.arange(Lq).view(Lq, 1) + (Lk - Lq)
+    j = torch.arange(Lk).view(1, Lk)
+    if causal:
+        keep = j <= a
+        if window > 0:
+            keep = keep & (a - j < window)
+    else:
+        keep = torch.ones((Lq, Lk), dtype=torch.bool) if window == 0 else (a - j).abs() < window
+    s = s.masked_fill(~keep, float("-inf"))
+    col = c.view(1, Hq, 1, 1).expand(B, Hq, Lq, 1)
+    aug = torch.cat([s, col], dim=-1)
+    p = torch.softmax(aug, dim=-1)[..., :Lk]
+    o = torch.matmul(p, vr)
+    lse = torch.logsumexp(aug, dim=-1)
+    (o * dO.double()).sum().backward()
+    return dict(o=o.detach(), lse=lse.detach(), dq=q.grad, dk=k.grad, dv=v.grad, dsinks=c.grad)
+
+
+def test_sinks_of_minus_infinity_are_no_sinks(oracle_mod):
+    q, k, v, dO = make_inputs(1, 4, 2, 40, 16, seed=71)
+    plain = oracle_mod.backward(q, k, v, dO, 8, 0.25)
+    sunk = oracle_mod.backward(q, k, v, dO, 8, 0.25, sinks=[-math.inf] * 4)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(plain[n], sunk[n]), n
+    assert np.array_equal(sunk["dsinks"], np.zeros(4))
+
+
+def test_sinks_single_key_closed_form(oracle_mod):
+    # row 0 of a causal layer sees only key 0: o = v0 e^s / (e^s + e^c)
+    q = _rand64((1, 1, 3, 4), 1)
+    k = _rand64((1, 1, 3, 4), 2)
+    v = _rand64((1, 1, 3, 4), 3)
+    c = 0.7
+    o, lse = oracle_mod.forward(q, k, v, 0, 0.5, sinks=[c])
+    s = 0.5 * float((q[0, 0, 0] * k[0, 0, 0]).sum())
+    w = math.exp(s) / (math.exp(s) + math.exp(c))
+    assert np.allclose(o[0, 0, 0], w * v[0, 0, 0].numpy(), rtol=1e-13, atol=1e-15)
+    assert abs(lse[0, 0, 0] - math.log(math.exp(s) + math.exp(c))) < 1e-13
+
+
+@pytest.mark.parametrize("Lq,Lk,window,causal", [(24, 24, 0, True), (24, 24, 7, True), (10, 24, 6, True),
+                                                  (16, 16, 5, False)])
+def test_sinks_match_torch_autograd(oracle_mod, Lq, Lk, window, causal):
+    q, k, v, dO = _suffix_inputs(2, 4, 2, Lq, Lk, 16, seed=72)
+    sinks = [0.5, -1.25, 2.0, -0.25]
+    got = oracle_mod.backward(q, k, v, dO, window, 0.3, causal=causal, sinks=sinks)
+    ref = _torch_reference_sinks(q, k, v, dO, window, 0.3, causal, sinks)
+    for n in ("o", "lse", "dq", "dk", "dv", "dsinks"):
+        assert np.allclose(got[n], ref[n].numpy(), rtol=1e-10, atol=1e-12), n
+
+
+def test_sinks_gradient_finite_differences(oracle_mod):
+    q, k, v, dO = make_inputs(1, 2, 1, 20, 8, seed=73)
+    dOd = dO.double().numpy()
+    sinks = np.array([0.4, -0.8])
+    got = oracle_mod.backward(q, k, v, dO, 6, 0.35, sinks=sinks)
+    eps = 1e-6
+    for h in range(2):
+        up, dn = sinks.copy(), sinks.copy()
+        up[h] += eps
+        dn[h] -= eps
+        lo = (oracle_mod.forward(q, k, v, 6, 0.35, sinks=up)[0] * dOd).sum()
+        hi = (oracle_mod.forward(q, k, v, 6, 0.35, sinks=dn)[0] * dOd).sum()
+        fd = (lo - hi) / (2 * eps)
+        assert abs(fd - got["dsinks"][h]) < 1e-7 * max(1.0, abs(fd)), (h, fd, got["dsinks"][h])
