@@ -178,6 +178,40 @@ int swa_attn_bwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v,
                         size_t workspace_bytes, void* stream);
 
 /*
+ * Attention sinks: swa_attn_fwd_ex / swa_attn_bwd_ex with one sink logit per
+ * query head.  The pages name "sinks" only as a parameter of the attention
+ * backward primitive, beside scale and causal ("Lab 028 lab detail: Off
+ * NVIDIA, you fix the platform yourself", "What I changed, in plain terms"
+ * item 2).  The reading taken is a per-head logit c_h that joins every row's
+ * softmax normaliser and carries no value:
+ *
+ *   lse_i = ln( sum_{j in band(i)} exp(s_ij) + exp(c_h) )
+ *   o_i   = sum_j exp(s_ij - lse_i) v_j
+ *
+ * and the backward also returns dc_h = - sum_{b, i} exp(c_h - lse_i) Delta_i
+ * (Delta_i = dO_i . o_i), summed over the batch and the rows of head h.
+ *
+ *   sinks   [Hq] fp32, device memory, natural-log units (the units of
+ *           scale * q . k); -inf is no sink.  Read only.  4-byte aligned.
+ *   dsinks  [Hq] fp32, device memory, written (not accumulated).  4-byte
+ *           aligned.
+ *
+ * q, k, v, o, lse, dO, dq, dk, dv, the geometry arguments, workspace
+ * (sizes from swa_attn_*_workspace_bytes_ex), stream, status word and error
+ * codes are as for swa_attn_fwd_ex / swa_attn_bwd_ex.  The backward reads the
+ * lse the sink forward wrote; only dsinks needs the sinks themselves.  A
+ * NULL sinks or dsinks is SWA_ERR_NULL_POINTER.  The decode path
+ * (G * Lq <= 16) takes the sinks in its final normalisation too.
+ */
+int swa_attn_fwd_sinks(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* sinks, float* o,
+                       float* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale,
+                       void* workspace, size_t workspace_bytes, void* stream);
+int swa_attn_bwd_sinks(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* sinks, const float* o,
+                       const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv, float* dsinks, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * Sequence sharding (context parallelism) with a halo: a sequence split into
  * contiguous chunks, one per rank, runs each chunk's queries over [halo;
  * own keys] through swa_attn_fwd_ex / swa_attn_bwd_ex (queries a suffix of

@@ -22,9 +22,11 @@ from ._native import (  # noqa: F401
     swa_attn_bwd,
     swa_attn_bwd_ex,
     swa_attn_bwd_prefix,
+    swa_attn_bwd_sinks,
     swa_attn_fwd,
     swa_attn_fwd_ex,
     swa_attn_fwd_prefix,
+    swa_attn_fwd_sinks,
     swa_attn_get_status,
     swa_attn_selftest_timeout,
 )
@@ -34,4 +36,5 @@ __all__ = [
     "fwd_workspace_bytes_ex", "load", "profile_begin", "profile_end", "strerror", "swa_attn_bwd", "swa_attn_bwd_ex",
     "swa_attn_fwd", "swa_attn_fwd_ex", "swa_attn_get_status", "swa_attn_selftest_timeout",
     "fwd_workspace_bytes_prefix", "bwd_workspace_bytes_prefix", "swa_attn_fwd_prefix", "swa_attn_bwd_prefix",
+    "swa_attn_fwd_sinks", "swa_attn_bwd_sinks",
 ]

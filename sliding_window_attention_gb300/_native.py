@@ -35,6 +35,8 @@ EXPORTED = (
     "swa_attn_fwd_prefix",
     "swa_attn_bwd_prefix",
     "swa_attn_add_rows_f32",
+    "swa_attn_fwd_sinks",
+    "swa_attn_bwd_sinks",
 )
 
 _lock = threading.Lock()
@@ -103,6 +105,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.swa_attn_bwd_prefix.restype = I
         lib.swa_attn_add_rows_f32.argtypes = [P, P, I, I, I, I, I, P]
         lib.swa_attn_add_rows_f32.restype = I
+        # attention sinks: the sink logits after v; the backward adds dsinks after dv
+        lib.swa_attn_fwd_sinks.argtypes = [P, P, P, P, P, P] + shape_ex + [F, P, Z, P]
+        lib.swa_attn_fwd_sinks.restype = I
+        lib.swa_attn_bwd_sinks.argtypes = [P, P, P, P, P, P, P, P, P, P, P] + shape_ex + [F, P, Z, P]
+        lib.swa_attn_bwd_sinks.restype = I
         _lib = lib
         return lib
 
@@ -193,6 +200,32 @@ def swa_attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, window: int, causal: bool, 
                                 _ptr(workspace), nbytes, _stream_ptr(stream))
     if rc:
         raise SwaError(rc, "swa_attn_bwd_ex")
+
+
+def swa_attn_fwd_sinks(q, k, v, sinks, o, lse, window: int, causal: bool, scale: float, workspace=None,
+                       stream=None) -> None:
+    """swa_attn_fwd_ex with one sink logit per query head (sinks fp32 [Hq],
+    CUDA; see include/swa_attn.h)."""
+    B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_fwd_sinks(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(o), _ptr(lse), B, Hq, Hkv, Lq, Lk,
+                                   D, int(window), int(bool(causal)), float(scale), _ptr(workspace), nbytes,
+                                   _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_fwd_sinks")
+
+
+def swa_attn_bwd_sinks(q, k, v, sinks, o, lse, dO, dq, dk, dv, dsinks, window: int, causal: bool, scale: float,
+                       workspace=None, stream=None) -> None:
+    """Backward of swa_attn_fwd_sinks; dq, dk, dv and dsinks (fp32 [Hq]) are
+    caller-allocated outputs."""
+    B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().swa_attn_bwd_sinks(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), _ptr(dsinks), B, Hq, Hkv, Lq, Lk, D, int(window),
+                                   int(bool(causal)), float(scale), _ptr(workspace), nbytes, _stream_ptr(stream))
+    if rc:
+        raise SwaError(rc, "swa_attn_bwd_sinks")
 
 
 def fwd_workspace_bytes_prefix(B, Hq, Hkv, L, D, window, prompt_len, chosen_len) -> int:
@@ -294,17 +327,23 @@ def _workspace(nbytes, device):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True, prefix=None):
+def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True, prefix=None, sinks=None):
     """Return (o fp32, lse fp32) for bf16 CUDA tensors q [B,Hq,Lq,D], k/v
     [B,Hkv,Lk,D] (Lq <= Lk; Lq = Lk and causal is self-attention).
     prefix=(prompt_len, chosen_len): the shared-prefix mask over one
-    [prompt; chosen; rejected] sequence (self-attention, causal)."""
+    [prompt; chosen; rejected] sequence (self-attention, causal).
+    sinks: fp32 CUDA tensor [Hq], one sink logit per query head."""
     import torch
 
     B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
     o = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=q.device)
     lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
-    if prefix is not None:
+    if sinks is not None:
+        if prefix is not None:
+            raise ValueError("sinks are not combined with a shared-prefix plan")
+        ws = _workspace(fwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal), q.device)
+        swa_attn_fwd_sinks(q, k, v, sinks, o, lse, window, causal, scale, ws, stream)
+    elif prefix is not None:
         ws = _workspace(fwd_workspace_bytes_prefix(B, Hq, Hkv, Lk, D, window, *prefix), q.device)
         swa_attn_fwd_prefix(q, k, v, o, lse, window, prefix[0], prefix[1], scale, ws, stream)
     elif Lq == Lk and causal:
@@ -316,14 +355,22 @@ def forward(q, k, v, window: int, scale: float, stream=None, causal: bool = True
     return o, lse
 
 
-def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None, causal: bool = True, prefix=None):
-    """Return (dq, dk, dv) fp32."""
+def backward(q, k, v, o, lse, dO, window: int, scale: float, stream=None, causal: bool = True, prefix=None,
+             sinks=None):
+    """Return (dq, dk, dv) fp32, and dsinks [Hq] too when sinks are given."""
     import torch
 
     B, Hq, Hkv, Lq, Lk, D = _dims_ex(q, k)
     dq = torch.empty((B, Hq, Lq, D), dtype=torch.float32, device=q.device)
     dk = torch.empty((B, Hkv, Lk, D), dtype=torch.float32, device=q.device)
     dv = torch.empty((B, Hkv, Lk, D), dtype=torch.float32, device=q.device)
+    if sinks is not None:
+        if prefix is not None:
+            raise ValueError("sinks are not combined with a shared-prefix plan")
+        dsinks = torch.empty((Hq,), dtype=torch.float32, device=q.device)
+        ws = _workspace(bwd_workspace_bytes_ex(B, Hq, Hkv, Lq, Lk, D, window, causal), q.device)
+        swa_attn_bwd_sinks(q, k, v, sinks, o, lse, dO, dq, dk, dv, dsinks, window, causal, scale, ws, stream)
+        return dq, dk, dv, dsinks
     if prefix is not None:
         ws = _workspace(bwd_workspace_bytes_prefix(B, Hq, Hkv, Lk, D, window, *prefix), q.device)
         swa_attn_bwd_prefix(q, k, v, o, lse, dO, dq, dk, dv, window, prefix[0], prefix[1], scale, ws, stream)

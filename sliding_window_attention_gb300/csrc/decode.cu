@@ -339,6 +339,16 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int q = 0; q < kNR; ++q) l_tot[q] = (rb[q] + rb[kNR + q]) + (rb[2 * kNR + q] + rb[3 * kNR + q]);
       const bool single = p.n_chunks == 1;
       const size_t cb = (size_t)blockIdx.x * gridDim.y + bkv;
+      // a single chunk finishes the rows here: 1 / l, or with attention
+      // sinks the factor that folds the row's head sink into the normaliser
+      float fac[kNR], lse_row[kNR];
+#pragma unroll
+      for (int q = 0; q < kNR; ++q) {
+        fac[q] = 1.f / l_tot[q];
+        lse_row[q] = (m_run[q] + log2f(l_tot[q])) * kLn2;
+        if (single && g.sinks && q < M)
+          fac[q] = sink_finish(g.sinks[(bkv % g.Hkv) * g.G + q / g.Lq], m_run[q], l_tot[q], &lse_row[q]);
+      }
 #pragma unroll
       for (int h = 0; h < NDC; ++h) {
         uint32_t ov[kNR];
@@ -350,21 +360,22 @@ __global__ void __launch_bounds__(kThr, 1)
           for (int q = 0; q < kNR; ++q) {
             if (q < M) {
               const float v = __uint_as_float(ov[q]);
-              if (single) p.o[((size_t)bkv * M + q) * D + d] = v / l_tot[q];
+              if (single) p.o[((size_t)bkv * M + q) * D + d] = v * fac[q];
               else p.part_o[(cb * M + q) * D + d] = v;
             }
           }
         }
       }
       if (t < M) {
-        float mq = m_run[0], lq = l_tot[0];
+        float mq = m_run[0], lq = l_tot[0], lsq = lse_row[0];
 #pragma unroll
         for (int q = 1; q < kNR; ++q) {
           mq = (t == q) ? m_run[q] : mq;
           lq = (t == q) ? l_tot[q] : lq;
+          lsq = (t == q) ? lse_row[q] : lsq;
         }
         if (single) {
-          p.lse[(size_t)bkv * M + t] = (mq + log2f(lq)) * kLn2;
+          p.lse[(size_t)bkv * M + t] = lsq;
         } else {
           p.part_ml[(cb * M + t) * 2] = mq;
           p.part_ml[(cb * M + t) * 2 + 1] = lq;
@@ -415,7 +426,15 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecParams p, int D)
     }
   }
   __syncthreads();
-  const float inv = 1.f / stat[1];
+  // 1 / l, or with attention sinks the factor that folds the row's head sink
+  // into the normaliser (rows are (b Hkv + kv head) M + m, m = head-in-group
+  // Lq + query row)
+  float lse_out = (stat[0] + log2f(stat[1])) * kLn2;
+  float inv = 1.f / stat[1];
+  if (p.g.sinks) {
+    const int bkv = row / p.M, m = row - bkv * p.M;
+    inv = sink_finish(p.g.sinks[(bkv % p.g.Hkv) * p.g.G + m / p.g.Lq], stat[0], stat[1], &lse_out);
+  }
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     float t0 = 0.f, t1 = 0.f;
     int c = 0;
@@ -426,7 +445,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecParams p, int D)
     if (c < nc) t0 = fmaf(wts[c], p.part_o[((size_t)c * rows + row) * D + d], t0);
     p.o[(size_t)row * D + d] = (t0 + t1) * inv;
   }
-  if (threadIdx.x == 0) p.lse[row] = (stat[0] + log2f(stat[1])) * kLn2;
+  if (threadIdx.x == 0) p.lse[row] = lse_out;
 }
 
 // Key range of the group and its split into chunks of whole tiles, so that

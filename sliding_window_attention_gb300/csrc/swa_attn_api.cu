@@ -177,6 +177,7 @@ swa::Geom make_geom(int B, int Hq, int Hkv, int Lq, int L, int D, int window, in
   g.scale = scale;
   g.P = 0;
   g.Rc = 0;
+  g.sinks = nullptr;
   return g;
 }
 
@@ -286,7 +287,7 @@ static int fwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, con
 // swa_attn_bwd_prefix).
 static int bwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* o,
                    const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+                   size_t workspace_bytes, void* stream, float* dsinks = nullptr) {
   const int B = g.B, Hq = g.Hq, Hkv = g.Hkv, Lq = g.Lq, Lk = g.L, D = g.D;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 16) ||
       !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(workspace, 256))
@@ -313,6 +314,10 @@ static int bwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, con
   if (launch("bwd_prep", s, [&] {
         return swa::launch_bwd_prep(g, w.Lpad, q, k, v, dO, o, lse, q16, k16, v16, g16, stats, status, s);
       }) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  // attention sinks: their gradient needs only the row statistics
+  if (g.sinks &&
+      launch("bwd_sink_grad", s, [&] { return swa::launch_sink_grad(g, w.Lpad, stats, dsinks, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;
   // dK/dV on the side stream (forked after the prep), dQ on the caller's
   // stream, then the caller's stream waits for the side stream.
@@ -459,6 +464,31 @@ int swa_attn_bwd_prefix(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v,
   if ((rc = check_plan(L, prompt_len, chosen_len))) return rc;
   return bwd_run(make_plan_geom(B, Hq, Hkv, L, D, window, prompt_len, chosen_len, scale), q, k, v, o, lse, dO, dq,
                  dk, dv, workspace, workspace_bytes, stream);
+}
+
+int swa_attn_fwd_sinks(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* sinks, float* o,
+                       float* lse, int B, int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !sinks || !o || !lse) return SWA_ERR_NULL_POINTER;
+  const int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (rc) return rc;
+  if (!aligned(sinks, 4)) return SWA_ERR_MISALIGNED;
+  swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
+  g.sinks = sinks;
+  return fwd_run(g, q, k, v, o, lse, workspace, workspace_bytes, stream);
+}
+
+int swa_attn_bwd_sinks(const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const float* sinks, const float* o,
+                       const float* lse, const swa_bf16* dO, float* dq, float* dk, float* dv, float* dsinks, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int D, int window, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !sinks || !o || !lse || !dO || !dq || !dk || !dv || !dsinks) return SWA_ERR_NULL_POINTER;
+  const int rc = check_shape(B, Hq, Hkv, Lq, Lk, D, window, scale);
+  if (rc) return rc;
+  if (!aligned(sinks, 4) || !aligned(dsinks, 4)) return SWA_ERR_MISALIGNED;
+  swa::Geom g = make_geom(B, Hq, Hkv, Lq, Lk, D, window, causal, scale);
+  g.sinks = sinks;
+  return bwd_run(g, q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, stream, dsinks);
 }
 
 int swa_attn_selftest_timeout(void* stream) {

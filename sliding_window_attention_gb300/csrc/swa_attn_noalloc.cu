@@ -93,6 +93,7 @@ extern "C" int swa_attn_bwd_noalloc(const swa_bf16* q, const swa_bf16* k, const 
   g.scale = scale;
   g.P = 0;
   g.Rc = 0;  // no shared-prefix plan
+  g.sinks = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (swa::launch_delta(g, o, dO, delta, s) != cudaSuccess) return SWA_ERR_CUDA;
   if (swa::launch_bwd_dkdv_simt(g, q, k, v, dO, lse, delta, dk, dv, s) != cudaSuccess) return SWA_ERR_CUDA;

@@ -25,7 +25,28 @@ struct Geom {
   // Rc == 0: no plan.  With a plan, Lq == L, off == 0, causal == 1 and
   // P + Rc < L.
   int P, Rc;
+  // Attention sinks: one logit per query head ([Hq] fp32, device memory),
+  // an extra term of every row's softmax normaliser that carries no value,
+  // or nullptr for none.  Not combined with a plan.
+  const float* sinks;
 };
+
+// Folds a sink logit c (natural-log units) into a row's final softmax
+// normaliser.  m2 is the row's reference maximum in log2 units and l its sum
+// of 2^(score - m2) terms; O is the accumulated P V for those terms.  With
+// mf = max(m2, c log2 e):
+//   l' = l 2^(m2 - mf) + 2^(c log2 e - mf),   lse = (mf + log2 l') ln 2,
+// and the row's output is O times the returned factor 2^(m2 - mf) / l'
+// (1 / l when the sink is -inf).  m2 = -inf (a row without keys) gives a
+// factor of 0 and lse = c.
+__device__ __forceinline__ float sink_finish(float c, float m2, float l, float* lse) {
+  const float c2 = c * 1.4426950408889634f;
+  const float mf = fmaxf(m2, c2);
+  const float a = exp2f(m2 - mf);
+  const float lf = fmaf(l, a, exp2f(c2 - mf));
+  *lse = (mf + log2f(lf)) * 0.6931471805599453f;
+  return a / lf;
+}
 
 // The band of query row i is the interval of keys [band_key_lo, band_key_hi]
 // ("Lab 028 lab detail: Off NVIDIA, you fix the platform yourself", "Plan
@@ -268,6 +289,9 @@ __host__ __device__ __forceinline__ size_t dscale_offset(const Geom& g, int Lpad
 }
 // max |dO| per block of the absmax pass into the stats tail (one launch).
 cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float* stats, cudaStream_t s);
+// Gradient of the attention sinks g.sinks into dsinks [Hq] (fp32), from the
+// row statistics the backward prep wrote (run after the prep).
+cudaError_t launch_sink_grad(const Geom& g, int Lpad, const float* stats, float* dsinks, cudaStream_t s);
 // The backward's preparation in one pass (after launch_bwd_dscale): fp16
 // copies of q, k, v and s * dO, and the row statistics, two planes of
 // B * Hq * Lpad floats: stats[bh * Lpad + i] = lse_i * log2(e),

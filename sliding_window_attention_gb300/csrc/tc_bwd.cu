@@ -76,6 +76,38 @@ __device__ __forceinline__ int dscale_log2(uint32_t maxbits) {
   return k < -125 ? -125 : (k > 125 ? 125 : k);
 }
 
+// Gradient of the attention sinks (one logit c_h per query head, a term of
+// every row's softmax normaliser that carries no value):
+//   dc_h = - sum_{b, i} exp(c_h - lse_i) Delta_i
+// over every batch and query row of head h.  c_h enters o_i only through
+// lse_i, and d o_i / d c_h = -exp(c_h - lse_i) o_i; with dO_i that gives
+// -exp(c_h - lse_i) Delta_i, Delta_i = dO_i . o_i.  Read from the backward's
+// row statistics: lse log2 e and s Delta planes, 1/s in the scale tail.  One
+// block per head; each thread sums its rows in ascending order in fp64 and a
+// fixed tree combines the threads, so the result does not depend on timing.
+__global__ void __launch_bounds__(256) sink_grad_kernel(const float* __restrict__ stats, int Lpad, int B, int Hq,
+                                                        int Lq, const float* __restrict__ sinks,
+                                                        float* __restrict__ dsinks, long long tail) {
+  __shared__ double red[256];
+  const int h = blockIdx.x;
+  const float c2 = sinks[h] * kLog2e;
+  const size_t plane = (size_t)B * Hq * Lpad;
+  double acc = 0.0;
+  const long long n = (long long)B * Lq;
+  for (long long r = threadIdx.x; r < n; r += blockDim.x) {
+    const int b = (int)(r / Lq), i = (int)(r - (long long)b * Lq);
+    const size_t row = ((size_t)b * Hq + h) * Lpad + i;
+    acc += (double)exp2f(c2 - stats[row]) * (double)stats[plane + row];
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsinks[h] = (float)(-red[0] * (double)stats[tail + 1]);
+}
+
 // Per-block maxima of |dO| (bit patterns of bf16 with the sign cleared,
 // which order like the magnitudes for every non-NaN value) into the stats
 // tail; kAbsmaxBlocks blocks, grid-stride over 16-byte vectors.
@@ -1648,6 +1680,13 @@ cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float
   const long long n16 = (long long)g.B * g.Hq * g.Lq * g.D / 8;
   uint32_t* partial = reinterpret_cast<uint32_t*>(stats + dscale_offset(g, Lpad) + 4);
   bwd_dscale_kernel<<<kAbsmaxBlocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(dO), n16, partial);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sink_grad(const Geom& g, int Lpad, const float* stats, float* dsinks, cudaStream_t s) {
+  if (!g.sinks) return cudaErrorInvalidValue;
+  sink_grad_kernel<<<g.Hq, 256, 0, s>>>(stats, Lpad, g.B, g.Hq, g.Lq, g.sinks, dsinks,
+                                        (long long)dscale_offset(g, Lpad));
   return cudaGetLastError();
 }
 

@@ -410,12 +410,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tmem_wait_ld();
       const float l_tot = __uint_as_float(lr[0]);
       const bool row_ok = i < g.Lq;
-      const float inv = 1.f / l_tot;
+      // 1 / l, or with attention sinks the factor that folds the head's sink
+      // logit into the row's normaliser
+      float lse_row = (m_run + log2f(l_tot)) * kLn2;
+      float inv = 1.f / l_tot;
+      if (g.sinks) inv = sink_finish(g.sinks[bh % g.Hq], m_run, l_tot, &lse_row);
       // O through TMA stores, staged in 16 KB per warp of the (consumed) Q tile
       tmem_rows_store_tma(&tmO, tmem + lane_off + C::O_COL, 0, D, inv,
                           smem_u32(base) + (uint32_t)(warp - 2) * 16384u, i - (int)(threadIdx.x & 31), bh,
                           (int)(threadIdx.x & 31));
-      if (row_ok) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
+      if (row_ok) p.lse[(size_t)bh * g.Lq + i] = lse_row;
     }
   }
 
@@ -752,7 +756,11 @@ __global__ void __launch_bounds__(352, 1)
     if (ok && cnt > 0) {
       tc_fence_after();
       const bool row_ok = i < g.Lq;
-      const float inv = 1.f / l_run;
+      // 1 / l, or with attention sinks the factor that folds the head's sink
+      // logit into the row's normaliser
+      float lse_row = (m_run + log2f(l_run)) * kLn2;
+      float inv = 1.f / l_run;
+      if (g.sinks) inv = sink_finish(g.sinks[bh % g.Hq], m_run, l_run, &lse_row);
       // (row stores: at D <= 128 a warp's own quarter of its Q tile holds at
       // most two 4 KB staging buffers, and TMA stores through them measured
       // about 1% slower here)
@@ -770,7 +778,7 @@ __global__ void __launch_bounds__(352, 1)
                             __uint_as_float(acc[e + 2]) * inv, __uint_as_float(acc[e + 3]) * inv);
         }
       }
-      if (row_ok) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_run)) * kLn2;
+      if (row_ok) p.lse[(size_t)bh * g.Lq + i] = lse_row;
     }
   }
 

@@ -574,8 +574,13 @@ __global__ void __launch_bounds__(kThr, 1)
     if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->lx, 0, abort_flag, R))) {
       const float l_tot = xl[r] + xl[128 + r];
       if (wg == 0) {
-        if (row_ok) p.lse[(size_t)bh * g.Lq + i] = (m_run + log2f(l_tot)) * kLn2;
-        finl[r] = 1.f / l_tot;
+        // 1 / l, or with attention sinks the factor that folds the head's
+        // sink logit into the row's normaliser; the accumulator scales O by it
+        float lse_row = (m_run + log2f(l_tot)) * kLn2;
+        float fin = 1.f / l_tot;
+        if (g.sinks) fin = sink_finish(g.sinks[bh % g.Hq], m_run, l_tot, &lse_row);
+        if (row_ok) p.lse[(size_t)bh * g.Lq + i] = lse_row;
+        finl[r] = fin;
         fence_proxy_async_smem();
         mbar_arrive(&bars->fin_staged);
         if (issuer && __all_sync(0xffffffffu, mbar_wait_cl(&bars->fin_staged, 0, abort_flag, R)) && lane == 0) {

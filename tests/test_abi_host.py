@@ -154,3 +154,27 @@ def test_prefix_entry_points_check_arguments(lib):
     # two query rows per kv head: the plain call takes the decode kernel, the
     # plan the tensor-core path with its fp16 copy of v
     assert lib.swa_attn_fwd_workspace_bytes_prefix(1, 2, 1, 8, 64, 0, 3, 2) >= 8 * 64 * 2
+
+
+def test_sink_entry_points_check_arguments_before_any_cuda_call(lib):
+    c = declared_codes()
+    P, F = ctypes.c_void_p, ctypes.c_float
+    # fwd: q, k, v, sinks, o, lse, B, Hq, Hkv, Lq, Lk, D, window, causal, scale, ws, bytes, stream
+    def fwd(sinks=0x7000, D=64, Lq=16, Lk=16):
+        return lib.swa_attn_fwd_sinks(P(0x1000), P(0x2000), P(0x3000), P(sinks), P(0x4000), P(0x5000), 1, 2, 1, Lq,
+                                      Lk, D, 0, 1, F(0.125), P(0x10000), 1 << 20, None)
+
+    # bwd: q, k, v, sinks, o, lse, dO, dq, dk, dv, dsinks, B, Hq, Hkv, Lq, Lk, D, window, causal, scale, ...
+    def bwd(sinks=0x7000, dsinks=0x8000, D=64):
+        return lib.swa_attn_bwd_sinks(*(P(0x1000 * (i + 1)) for i in range(3)), P(sinks),
+                                      *(P(0x1000 * (i + 4)) for i in range(6)), P(dsinks), 1, 2, 1, 16, 16, D, 0, 1,
+                                      F(0.125), P(0x10000), 1 << 20, None)
+
+    assert fwd(sinks=0) == c["SWA_ERR_NULL_POINTER"]
+    assert fwd(sinks=0x7002) == c["SWA_ERR_MISALIGNED"]
+    assert fwd(D=96) == c["SWA_ERR_BAD_HEAD_DIM"]
+    assert fwd(Lq=32, Lk=16) == c["SWA_ERR_BAD_SHAPE"]
+    assert bwd(sinks=0) == c["SWA_ERR_NULL_POINTER"]
+    assert bwd(dsinks=0) == c["SWA_ERR_NULL_POINTER"]
+    assert bwd(dsinks=0x8002) == c["SWA_ERR_MISALIGNED"]
+    assert bwd(D=96) == c["SWA_ERR_BAD_HEAD_DIM"]

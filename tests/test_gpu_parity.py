@@ -644,3 +644,77 @@ def test_prefix_degenerate_plan_is_the_plain_call():
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+# attention sinks: one logit per query head in every row's softmax normaliser
+# (the backward primitive's "sinks" parameter, "Lab 028 lab detail: Off
+# NVIDIA, you fix the platform yourself", "What I changed, in plain terms"
+# item 2; the reading is stated in include/swa_attn.h)
+
+SINKS = [
+    # B, Hq, Hkv, Lq, Lk, D, window, causal
+    (1, 4, 2, 300, 300, 64, 64, True),
+    (2, 4, 1, 129, 129, 128, 0, True),
+    (1, 4, 2, 257, 257, 256, 100, True),
+    (1, 4, 2, 300, 300, 512, 0, True),
+    (1, 2, 1, 100, 400, 128, 64, True),    # queries a suffix of the keys
+    (1, 4, 2, 200, 200, 128, 50, False),   # non-causal window
+    (2, 8, 1, 1, 700, 128, 0, True),       # decode step (8 rows per kv head)
+    (1, 8, 2, 2, 1500, 512, 0, True),      # decode step at head dim 512
+]
+
+
+def _sink_values(Hq):
+    base = [-math.inf, -1.5, 0.5, 4.0, -0.25, 2.0, 7.0, -3.0]
+    return [base[h % len(base)] for h in range(Hq)]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk,D,window,causal", SINKS)
+def test_sinks_elementwise(oracle_mod, B, Hq, Hkv, Lq, Lk, D, window, causal):
+    import sliding_window_attention_gb300 as swa
+
+    q, k, v, dO = make_inputs(B, Hq, Hkv, Lk, D, seed=4000 + Lq + D + window)
+    q, dO = q[:, :, Lk - Lq:].contiguous(), dO[:, :, Lk - Lq:].contiguous()
+    scale = 1.0 / math.sqrt(D)
+    sinks = _sink_values(Hq)
+    ref = oracle_mod.backward(q, k, v, dO, window, scale, causal=causal, sinks=sinks)
+    sd = torch.tensor(sinks, dtype=torch.float32, device="cuda")
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, dO))
+    o, lse = swa.forward(qd, kd, vd, window, scale, causal=causal, sinks=sd)
+    dq, dk, dv, dsinks = swa.backward(qd, kd, vd, o, lse, gd, window, scale, causal=causal, sinks=sd)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    assert_lse_close(lse.cpu().numpy(), ref["lse"])
+    for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close(n, t.cpu().numpy(), ref[n])
+    got = dsinks.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    # dc_h sums exp(c_h - lse_i) Delta_i over B Lq rows, terms of either sign:
+    # the bar is relative to the sum of the terms' magnitudes
+    c = np.asarray(sinks).reshape(1, Hq, 1)
+    mag = np.sum(np.exp(c - ref["lse"]) * np.abs(ref["delta"]), axis=(0, 2))
+    assert np.all(np.abs(got - ref["dsinks"]) <= 2e-3 * mag + 1e-5), (got, ref["dsinks"], mag)
+    assert got[0] == 0.0  # head 0 has a sink of -inf
+
+
+@pytest.mark.parametrize("Lq,Lk,D,window", [(300, 300, 128, 64), (257, 257, 256, 0), (300, 300, 512, 0),
+                                            (1, 700, 128, 0)])
+def test_sinks_of_minus_infinity_equal_the_plain_call_bitwise(Lq, Lk, D, window):
+    import sliding_window_attention_gb300 as swa
+
+    Hq, Hkv = 8, 2
+    q, k, v, dO = make_inputs(1, Hq, Hkv, Lk, D, seed=4100 + D)
+    q, dO = q[:, :, Lk - Lq:].contiguous(), dO[:, :, Lk - Lq:].contiguous()
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, dO))
+    scale = 1.0 / math.sqrt(D)
+    sd = torch.full((Hq,), -math.inf, dtype=torch.float32, device="cuda")
+    o0, l0 = swa.forward(qd, kd, vd, window, scale)
+    o1, l1 = swa.forward(qd, kd, vd, window, scale, sinks=sd)
+    g0 = swa.backward(qd, kd, vd, o0, l0, gd, window, scale)
+    g1 = swa.backward(qd, kd, vd, o1, l1, gd, window, scale, sinks=sd)
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    for a, b in zip(g0, g1[:3]):
+        assert torch.equal(a, b)
+    assert torch.all(g1[3] == 0)
