@@ -45,6 +45,36 @@ cudaError_t launch(const char* name, cudaStream_t s, F&& f) {
   return e;
 }
 
+// Runs f1 then f2 (each enqueues one kernel on `s`, the second allowed to
+// start before the first has finished); with profiling on, both records span
+// the two launches, since an event between them would serialise them.
+template <typename F1, typename F2>
+cudaError_t launch_overlapped(const char* name1, const char* name2, cudaStream_t s, F1&& f1, F2&& f2) {
+  bool on;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    on = g_prof_on;
+  }
+  if (!on) {
+    const cudaError_t e = f1();
+    return e != cudaSuccess ? e : f2();
+  }
+  ProfRec r1{name1, nullptr, nullptr}, r2{name2, nullptr, nullptr};
+  if (cudaEventCreate(&r1.start) != cudaSuccess || cudaEventCreate(&r1.stop) != cudaSuccess ||
+      cudaEventCreate(&r2.start) != cudaSuccess || cudaEventCreate(&r2.stop) != cudaSuccess)
+    return cudaErrorUnknown;
+  cudaEventRecord(r1.start, s);
+  cudaEventRecord(r2.start, s);
+  cudaError_t e = f1();
+  if (e == cudaSuccess) e = f2();
+  cudaEventRecord(r1.stop, s);
+  cudaEventRecord(r2.stop, s);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_recs.push_back(r1);
+  g_prof_recs.push_back(r2);
+  return e;
+}
+
 constexpr int kMaxDevices = 64;
 
 // Per-device status word: kernels latch the first device-side error here.
@@ -319,8 +349,23 @@ static int bwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, con
   if (g.sinks &&
       launch("bwd_sink_grad", s, [&] { return swa::launch_sink_grad(g, w.Lpad, stats, dsinks, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;
-  // dK/dV on the side stream (forked after the prep), dQ on the caller's
-  // stream, then the caller's stream waits for the side stream.
+  // The dK/dV and dQ passes read the same inputs, write disjoint outputs
+  // and run side by side.
+  if (D == 512) {
+    // Both passes are persistent (as many clusters as fit, looping over work
+    // items).  dK/dV goes first and takes the SMs its clusters can use; dQ,
+    // launched after it on the same stream as a programmatic dependent,
+    // starts on the SMs it leaves and takes over those its clusters free as
+    // its work runs out.
+    const cudaError_t e = launch_overlapped(
+        "bwd_dkdv_tc", "bwd_dq_tc", s,
+        [&] { return swa::launch_bwd_dkdv_tc(g, q16, k16, v16, g16, stats, w.Lpad, dk, dv, status, s); },
+        [&] { return swa::launch_bwd_dq_tc(g, q16, k16, v16, g16, stats, w.Lpad, dq, status, s); });
+    return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  }
+  // Up to head dim 256: dK/dV on the side stream (forked after the prep),
+  // whose higher priority gives its waiting CTAs the SMs that free up first,
+  // dQ on the caller's stream, which then waits for the side stream.
   SideStream* side = side_stream_for_current_device();
   if (!side) return SWA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(side->mu);

@@ -280,14 +280,18 @@ int bwd_stats_lpad(int L);
 // too, and the dq, dk and dv epilogues multiply by 1/s, exactly.
 // The backward's row-statistics block ends with a tail of
 // kDScaleTailFloats floats at stats + dscale_offset(): [0] = s, [1] = 1/s,
-// [2, 4) unused, [4, 4 + kAbsmaxBlocks) per-block maxima of |dO| (bf16 bit
-// patterns with the sign cleared, as uint32) written by the absmax pass.
+// [2], [3] the work counters (int32) of the persistent head-dim-512 dK/dV and
+// dQ passes, zeroed by the absmax pass, [4, 4 + kAbsmaxBlocks) per-block
+// maxima of |dO| (bf16 bit patterns with the sign cleared, as uint32) written
+// by the absmax pass.
 constexpr int kAbsmaxBlocks = 304;
+constexpr int kWorkCounterFloat = 2;
 constexpr int kDScaleTailFloats = 4 + kAbsmaxBlocks;
 __host__ __device__ __forceinline__ size_t dscale_offset(const Geom& g, int Lpad) {
   return 2 * (size_t)g.B * g.Hq * Lpad;
 }
-// max |dO| per block of the absmax pass into the stats tail (one launch).
+// max |dO| per block of the absmax pass into the stats tail, and the work
+// counters zeroed (one launch).
 cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float* stats, cudaStream_t s);
 // Gradient of the attention sinks g.sinks into dsinks [Hq] (fp32), from the
 // row statistics the backward prep wrote (run after the prep).
@@ -309,6 +313,11 @@ cudaError_t launch_bwd_dkdv_tc(const Geom& g, const uint16_t* q16, const uint16_
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                    const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                    int* status, cudaStream_t s);
+// Both passes are persistent (as many clusters as fit at once, looping over
+// work items from the stats tail's counters).  The dQ pass is launched with
+// programmatic stream serialization: enqueued on the dK/dV pass's stream
+// right after it, it starts on the SMs that pass leaves and completes after
+// it.
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                  const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                                  cudaStream_t s);

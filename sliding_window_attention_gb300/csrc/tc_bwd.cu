@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(256) sink_grad_kernel(const float* __restrict_
 // which order like the magnitudes for every non-NaN value) into the stats
 // tail; kAbsmaxBlocks blocks, grid-stride over 16-byte vectors.
 __global__ void __launch_bounds__(256) bwd_dscale_kernel(const uint4* __restrict__ dO, long long n16,
-                                                          uint32_t* __restrict__ partial) {
+                                                          uint32_t* __restrict__ partial,
+                                                          int* __restrict__ counters) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) counters[threadIdx.x] = 0;  // persistent passes start at item 0
   uint32_t m = 0;
   const long long stride = (long long)gridDim.x * blockDim.x;
   long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1679,7 +1681,8 @@ int scratch_layout_bwd256() {
 cudaError_t launch_bwd_dscale(const Geom& g, int Lpad, const uint16_t* dO, float* stats, cudaStream_t s) {
   const long long n16 = (long long)g.B * g.Hq * g.Lq * g.D / 8;
   uint32_t* partial = reinterpret_cast<uint32_t*>(stats + dscale_offset(g, Lpad) + 4);
-  bwd_dscale_kernel<<<kAbsmaxBlocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(dO), n16, partial);
+  int* counters = reinterpret_cast<int*>(stats + dscale_offset(g, Lpad) + kWorkCounterFloat);
+  bwd_dscale_kernel<<<kAbsmaxBlocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(dO), n16, partial, counters);
   return cudaGetLastError();
 }
 

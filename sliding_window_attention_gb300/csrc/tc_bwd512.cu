@@ -43,6 +43,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "swa_internal.h"
 #include "tc_ptx.cuh"
 
@@ -52,6 +54,7 @@ namespace {
 using namespace tc;
 
 constexpr int kDirKV = 0, kDirQ = 1;
+constexpr int kMaxDevices = 64;
 constexpr int kRoleProd = 0, kRoleAccP = 1, kRoleAccDS = 2;
 constexpr int T = 128;     // rows of a resident tile, columns of a streamed step
 constexpr int HT = 64;     // streamed rows per CTA of a pair
@@ -128,13 +131,20 @@ struct Bars {
   uint64_t recv_full[kMaxRecv][2];   // (accumulator, own) half of the tile loaded into slot
   uint64_t peer_recv[kMaxRecv];      // (accumulator leader) the peer's tile landed in slot
   uint64_t mma_done[kMaxRecv];       // (accumulator, both) MMAs reading slot finished
-  uint64_t acc_done, mma_drain;
+  uint64_t acc_done;                 // (accumulator, both) an item's MMAs finished
+  uint64_t acc_free;                 // (accumulator leader) both CTAs read an item's accumulator out
+  uint64_t epi_done;                 // (accumulator, own) the epilogue's stores read their staging
+  uint64_t item_full[2];             // (every CTA) the scheduler wrote an item id into the slot
+  uint64_t item_empty[2];            // (rank 0) every reader of the slot read it
+  uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
   int smid;                       // (accumulator) SM this CTA runs on: the scratch it loads from
   int n_loaded[kMaxNpp];          // (accumulator) own steps of producer pair p whose loads were issued
   int n_recv[kMaxNpp];            // (accumulator) own steps of producer pair p observed landed
   int n_issued;                   // ring loads issued by this CTA
+  int n_res;                      // (producer) resident loads issued by this CTA
+  int item_id[2];                 // item ids, written by rank 0's scheduler
 };
 
 constexpr size_t SMEM = (size_t)DATA_BYTES + STATS_BYTES + 1024 + 1024;
@@ -143,6 +153,8 @@ static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 struct ParamsPair {
   Geom g;
+  int* work;            // the pass's work counter: the next item id (zero before the launch)
+  int n_items;          // work items
   float* out0;          // KV: dk ; Q: dq
   float* out1;          // KV: dv
   const uint16_t* x16;  // resident S operand rows: KV: k16 ; Q: q16
@@ -212,6 +224,79 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader, uint32
   else mbar_arrive_remote(mapa(smem_u32(bar), lead));
 }
 
+// One work item of a persistent cluster: a pair of resident-side tiles (keys
+// in the dK/dV pass; in the dQ pass the query rows of one query head).  Ids
+// run with the kv head (b * Hkv + kv head) slowest, then the tile pair (the
+// longest band first), then (dQ pass) the group's query head, so that the
+// clusters working at any moment share one kv head: its K and V (dQ pass) or
+// its group's Q and dO (dK/dV pass) are read from HBM about once and then
+// served by L2, and the short items come last.
+struct Item {
+  int bkv, b;       // b * Hkv + kv head, batch
+  int head;         // head of the resident rows: kv head (dK/dV) or query head (dQ), batch included
+  int pr0, prlast;  // first and last resident row of the pair
+  int r0, rlast;    // this CTA's tile (rlast = r0 when it has no rows)
+  bool own_rows;    // false for the second tile of an odd last pair
+  TileSteps ts;     // dK/dV: the query tiles that can see a key of the pair; dQ: the key tiles meeting its band
+  int ntq, N;       // streamed tiles; steps (dK/dV: tiles x the group's query heads)
+};
+
+template <int DIR>
+__device__ __forceinline__ Item make_item(const Geom& g, int id, int npairs, int LX, uint32_t h) {
+  Item x;
+  const int per_kv = DIR == kDirKV ? npairs : npairs * g.G;
+  x.bkv = id / per_kv;
+  const int rem = id - x.bkv * per_kv;
+  x.b = x.bkv / g.Hkv;
+  int tp;
+  if (DIR == kDirKV) {
+    tp = rem;  // key tile pair 0 is seen by the most queries
+    x.head = x.bkv;
+  } else {
+    const int y = rem / g.G;
+    tp = npairs - 1 - y;  // the last query tile pair has the longest band
+    x.head = x.b * g.Hq + (x.bkv - x.b * g.Hkv) * g.G + (rem - y * g.G);
+  }
+  x.pr0 = 2 * tp * T;
+  x.prlast = min(x.pr0 + 2 * T, LX) - 1;
+  x.r0 = x.pr0 + (int)h * T;
+  x.own_rows = x.r0 < LX;
+  x.rlast = x.own_rows ? min(x.r0 + T, LX) - 1 : x.r0;
+  x.ts = DIR == kDirKV ? key_steps(g, x.pr0, x.prlast, T) : row_steps(g, x.pr0, x.prlast, T);
+  x.ntq = x.ts.count();
+  x.N = DIR == kDirKV ? g.G * x.ntq : x.ntq;
+  return x;
+}
+// Streamed-side rows and head of step n of item x.  dK/dV pass: query tiles
+// from the last one down, the group's query heads innermost, so that
+// concurrent clusters of one kv head read the same Q and dO tiles at about
+// the same time.
+template <int DIR>
+__device__ __forceinline__ int step_rows(const Geom& g, const Item& x, int n) {
+  if (DIR == kDirKV) return x.ts.tile(x.ntq - 1 - n / g.G) * T;
+  return x.ts.tile(n) * T;
+}
+template <int DIR>
+__device__ __forceinline__ int step_head(const Geom& g, const Item& x, int n) {
+  if (DIR == kDirKV) return x.b * g.Hq + (x.head - x.b * g.Hkv) * g.G + n % g.G;  // query head
+  return x.bkv;                                                                  // kv head
+}
+// Producer pair pp takes steps pp, pp + NPP, ... of an item's N; its m-th
+// own step is pp + NPP m.
+template <int NPP>
+__device__ __forceinline__ int own_steps(int N, int pp) {
+  return max(0, (N - pp + NPP - 1) / NPP);
+}
+// Readers of each item id in a cluster (the scheduler counts their arrivals
+// before it reuses the id's slot): per producer pair the leader's TMA, MMA,
+// eight elementwise and store warps (11) and the peer's same plus its relay
+// warp (12); per accumulator pair the leader's TMA, MMA and eight elementwise
+// warps (10) and the peer's TMA and eight elementwise warps (9).
+template <int DIR>
+constexpr int item_readers() {
+  return PassCfg<DIR>::NPP * (11 + 12) + (DIR == kDirKV ? 2 : 1) * (10 + 9);
+}
+
 template <int DIR>
 __global__ void __launch_bounds__(kThr, 1)
     bwd512_kernel(const __grid_constant__ CUtensorMap tmS,   // streamed S operand, 64 rows x 2 chunks: Q / K
@@ -244,55 +329,14 @@ __global__ void __launch_bounds__(kThr, 1)
   const int role = rank < kAccP ? kRoleProd : ((DIR == kDirKV && rank < kAccDS) ? kRoleAccP : kRoleAccDS);
   const bool acc_role = role != kRoleProd;
   const int pp = (int)(rank >> 1);  // producer pair (producers only)
-  // Grid (x, y, z) = (CTAs per cluster [x query heads of the group, dQ pass],
-  // tile pairs, b * Hkv + kv head).  Blocks launch x fastest and z slowest, so
-  // the clusters running at any moment share one kv head: its K and V (dQ
-  // pass) or its group's Q and dO (dK/dV pass) are read from HBM about once
-  // and then served by L2.
-  const int bkv_z = (int)blockIdx.z;
-  const int b = bkv_z / g.Hkv;
-  const int head = (DIR == kDirKV) ? bkv_z  // b * Hkv + kv head
-                                   : b * g.Hq + (bkv_z - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // query head
   const int LX = (DIR == kDirKV) ? g.L : g.Lq;  // rows of the resident side
   const int npairs = (p.n_tiles + 1) / 2;
-  // resident-side tile pair (dQ pass: longest band first) and this CTA's tile
-  const int tp = (DIR == kDirKV) ? (int)blockIdx.y : npairs - 1 - (int)blockIdx.y;
-  const int pr0 = 2 * tp * T;
-  const int prlast = min(pr0 + 2 * T, LX) - 1;
-  const int r0 = pr0 + (int)h * T;
-  const bool own_rows = r0 < LX;  // false for the second tile of an odd last pair
-  const int rlast = own_rows ? min(r0 + T, LX) - 1 : r0;
-  // dK/dV pass: the query tiles that can see a key of the pair; dQ pass: the
-  // key tiles meeting the band of the pair's rows (never empty)
-  const TileSteps tsteps = (DIR == kDirKV) ? key_steps(g, pr0, prlast, T) : row_steps(g, pr0, prlast, T);
-  const int ntq = tsteps.count();
-  const int N = (DIR == kDirKV) ? g.G * ntq : ntq;
   const bool two = g.Rc > 0;  // shared-prefix plan: two visible intervals per row
-  if (N == 0) {
-    // dK/dV pass, and no query sees these keys (queries that are a suffix of
-    // the keys, with a window): zero gradients ("Lab 028 lab detail", "What
-    // I changed, in plain terms" item 5(b)).  Every CTA of the cluster has
-    // the same pair, so all of them leave here, before any cluster barrier.
-    if (role == kRoleAccP) zero_rows(p.out1, head, r0, T, g.L, DH);
-    if (role == kRoleAccDS) zero_rows(p.out0, head, r0, T, g.L, DH);
-    return;
-  }
-  // streamed-side rows and head of step n.  dK/dV pass: query tiles from the
-  // last one down, the group's query heads innermost, so that concurrent
-  // clusters of one kv head (all starting at the last query tile) read the
-  // same Q and dO tiles at about the same time.
-  auto step_rows = [&](int n) {
-    if (DIR == kDirKV) return tsteps.tile(ntq - 1 - n / g.G) * T;
-    return tsteps.tile(n) * T;
-  };
-  auto step_head = [&](int n) -> int {
-    if (DIR == kDirKV) return b * g.Hq + (head - b * g.Hkv) * g.G + n % g.G;  // query head
-    return bkv_z;                                                              // kv head
-  };
-  // producer pair pp takes steps n = pp, pp + NPP, ...; m-th own step = pp + NPP m
-  const int n_own = role == kRoleProd ? max(0, (N - pp + NPP - 1) / NPP) : 0;
   // accumulator: which of the producer's two destinations this CTA is
   const int dst_kind = (role == kRoleAccP) ? 0 : 1;
+  // the dQ pass, launched right after this one on the same stream, may start
+  // on the SMs this pass leaves once all of its clusters are resident
+  if (DIR == kDirKV && threadIdx.x == 0) grid_launch_dependents();
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->res_full, 1);
@@ -313,6 +357,8 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int j = 0; j < RS; ++j) mbar_init(&bars->scratch_free[s][j], 1);
       mbar_init(&bars->stats_full[s], 1);
       mbar_init(&bars->stats_free[s], 128);
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], item_readers<DIR>());
     }
     for (int s = 0; s < NRECV; ++s) {
       mbar_init(&bars->tile_ready[s], 1);
@@ -322,6 +368,8 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&bars->mma_done[s], 1);
     }
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->acc_free, 16);
+    mbar_init(&bars->epi_done, 8);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
     uint32_t sm;
@@ -332,6 +380,7 @@ __global__ void __launch_bounds__(kThr, 1)
     if (bars->smid < 0) atomicCAS(p.status, 0, kStatusScratch);
     for (int s = 0; s < NPP; ++s) bars->n_recv[s] = bars->n_loaded[s] = 0;
     bars->n_issued = 0;
+    bars->n_res = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -344,6 +393,30 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
+  // The k-th item of this cluster (k = 0, 1, ...): its id, or -1 once the
+  // work has run out or after a timeout (then ok is cleared).  The id sits in
+  // slot k % 2; each reader tells rank 0's scheduler that it has read it.
+  auto get_item = [&](int k, bool& ok) -> int {
+    if (!mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R)) {
+      ok = false;
+      return -1;
+    }
+    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
+    if (id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
+    return id;
+  };
+  // the same for a whole warp (lane 0 reports the read)
+  auto get_item_warp = [&](int k, bool& ok) -> int {
+    if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R))) {
+      ok = false;
+      return -1;
+    }
+    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
+    __syncwarp();
+    if (lane == 0 && id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
+    return id;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA (both CTAs of a pair)
     if (elect_one()) {
@@ -353,43 +426,60 @@ __global__ void __launch_bounds__(kThr, 1)
       prefetch_tmap(&tmA0);
       prefetch_tmap(&tmA1);
       int issued = 0;  // ring loads issued
+      int n_res = 0;   // producer: items with own steps so far
+      int M = 0;       // producer: own steps so far
       bool ok = true;
-      if (!acc_role) {
-        // resident dP operand (this CTA's 128 rows), then per own step four
-        // slices for S and then four for dP (this CTA's 64 rows)
-        if (leader) mbar_arrive_expect_tx(&bars->res_full, 2 * RES_BYTES);
-        const uint32_t res_bar = mapa(smem_u32(&bars->res_full), lead);
-        for (int c = 0; c < DH / 64; ++c) tma_load_3d_pair(base + c * T * 128, &tmR, res_bar, c * 64, r0, head);
-        for (int m = 0; ok && m < n_own; ++m) {
-          const int n = pp + NPP * m;
-          const int rows = step_rows(n) + HT * (int)h, hd = step_head(n);
-          for (int k = 0; k < 2 * (DH / 128); ++k, ++issued) {
-            const int s = issued % NR_P;
-            if (issued >= NR_P && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_P) & 1) ^ 1, abort_flag, R)) {
-              ok = false;
-              break;
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const Item x = make_item<DIR>(g, id, npairs, LX, h);
+        if (!acc_role) {
+          // resident dP operand (this CTA's 128 rows), then per own step four
+          // slices for S and then four for dP (this CTA's 64 rows)
+          const int n_own = own_steps<NPP>(x.N, pp);
+          if (n_own == 0) continue;
+          // the previous item's last dP has finished reading the resident operand
+          if (n_res > 0 && !mbar_wait_cl(&bars->p_full, (M - 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&bars->res_full, 2 * RES_BYTES);
+          const uint32_t res_bar = mapa(smem_u32(&bars->res_full), lead);
+          for (int c = 0; c < DH / 64; ++c) tma_load_3d_pair(base + c * T * 128, &tmR, res_bar, c * 64, x.r0, x.head);
+          bars->n_res = ++n_res;
+          for (int m = 0; ok && m < n_own; ++m) {
+            const int n = pp + NPP * m;
+            const int rows = step_rows<DIR>(g, x, n) + HT * (int)h, hd = step_head<DIR>(g, x, n);
+            for (int kk = 0; kk < 2 * (DH / 128); ++kk, ++issued) {
+              const int s = issued % NR_P;
+              if (issued >= NR_P && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_P) & 1) ^ 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_P);
+              tma_load_4d_pair(base + OFF_RING_P + s * SLOT_P, kk >= 4 ? &tmP : &tmS,
+                               mapa(smem_u32(&bars->ring_full[s]), lead), 0, rows, 2 * (kk & 3), hd);
             }
-            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_P);
-            tma_load_4d_pair(base + OFF_RING_P + s * SLOT_P, k >= 4 ? &tmP : &tmS,
-                             mapa(smem_u32(&bars->ring_full[s]), lead), 0, rows, 2 * (k & 3), hd);
+          }
+          M += n_own;
+        } else {
+          // this CTA's 128-column half of each 256-column chunk of dO (dV), Q (dK) or K (dQ)
+          const CUtensorMap* mb = (role == kRoleAccP) ? &tmA0 : &tmA1;
+          for (int n = 0; ok && n < x.N; ++n) {
+            const int rows = step_rows<DIR>(g, x, n), hd = step_head<DIR>(g, x, n);
+            for (int c = 0; c < DH / 256; ++c, ++issued) {
+              const int s = issued % NR_A;
+              if (issued >= NR_A && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_A) & 1) ^ 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_A);
+              tma_load_4d_pair(base + OFF_RING_A + s * SLOT_A, mb, mapa(smem_u32(&bars->ring_full[s]), lead), 0,
+                               rows, 4 * c + 2 * (int)h, hd);
+            }
           }
         }
-      } else {
-        // this CTA's 128-column half of each 256-column chunk of dO (dV), Q (dK) or K (dQ)
-        const CUtensorMap* mb = (role == kRoleAccP) ? &tmA0 : &tmA1;
-        for (int n = 0; ok && n < N; ++n) {
-          const int rows = step_rows(n), hd = step_head(n);
-          for (int c = 0; c < DH / 256; ++c, ++issued) {
-            const int s = issued % NR_A;
-            if (issued >= NR_A && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_A) & 1) ^ 1, abort_flag, R)) {
-              ok = false;
-              break;
-            }
-            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_A);
-            tma_load_4d_pair(base + OFF_RING_A + s * SLOT_A, mb, mapa(smem_u32(&bars->ring_full[s]), lead), 0,
-                             rows, 4 * c + 2 * (int)h, hd);
-          }
-        }
+        bars->n_issued = issued;
       }
       bars->n_issued = issued;
     }
@@ -398,107 +488,169 @@ __global__ void __launch_bounds__(kThr, 1)
     if (elect_one()) {
       bool ok = true;
       if (!acc_role) {
-        // both CTAs: the resident S operand is in Tensor Memory -> tell the leader
-        ok = mbar_wait_cl(&bars->x_ready, 0, abort_flag, R);
-        if (ok) {
-          tc_fence_after();
-          tc_fence_before();
-          arrive_leader(&bars->pair_ready, leader, lead);
-        }
-        if (leader && ok) {
-          const uint32_t idS = idesc_f16(2 * T, T, 0, 0, 0, 0);  // M = 256 (the pair's rows), both K-major
-          const uint64_t yd = smem_desc_sw128(sbase, 16, 1024);  // resident dP operand
-          ok = mbar_wait_cl(&bars->res_full, 0, abort_flag, R) && mbar_wait_cl(&bars->pair_ready, 0, abort_flag, R);
-          // Own step m takes ring loads 8 m .. 8 m + 7: load k of the step sits
-          // in slot k % 4 with phase parity k / 4, both fixed at compile time,
-          // so the unrolled issue below is MMAs with constant operand offsets
-          // (a single thread issues every MMA of the pair; its per-instruction
-          // work bounds the rate at which the tensor pipe is fed).
-          static_assert(NR_P == 4 && 2 * (DH / 128) == 8, "slot and parity of load k are k % 4 and k / 4");
-          const uint32_t x_tm = tmem + X_COL, s_tm = tmem + S_COL, dp_tm = tmem + DP_COL;
-          const uint64_t rd = smem_desc_sw128(sbase + OFF_RING_P, 16, 1024);
-          for (int m = 0; ok && m < n_own; ++m) {
-            // S of step m (slices 0-3) once the elementwise warps read S of step m - 1, then dP
-            // (slices 4-7) once they read dP of step m - 1: each overlaps the other's readout
+        const uint32_t idS = idesc_f16(2 * T, T, 0, 0, 0, 0);  // M = 256 (the pair's rows), both K-major
+        const uint64_t yd = smem_desc_sw128(sbase, 16, 1024);  // resident dP operand
+        const uint32_t x_tm = tmem + X_COL, s_tm = tmem + S_COL, dp_tm = tmem + DP_COL;
+        const uint64_t rd = smem_desc_sw128(sbase + OFF_RING_P, 16, 1024);
+        // Own step M takes ring loads 8 M .. 8 M + 7: load k of the step sits
+        // in slot k % 4 with phase parity k / 4, both fixed at compile time,
+        // so the unrolled issue below is MMAs with constant operand offsets
+        // (a single thread issues every MMA of the pair; its per-instruction
+        // work bounds the rate at which the tensor pipe is fed).
+        static_assert(NR_P == 4 && 2 * (DH / 128) == 8, "slot and parity of load k are k % 4 and k / 4");
+        int kp = 0, M = 0;  // items with own steps so far, own steps so far
+        for (int k = 0; ok; ++k) {
+          const int id = get_item(k, ok);
+          if (id < 0) break;
+          const Item x = make_item<DIR>(g, id, npairs, LX, h);
+          const int n_own = own_steps<NPP>(x.N, pp);
+          if (n_own == 0) continue;
+          // both CTAs: the item's resident S operand is in Tensor Memory -> tell the leader
+          ok = mbar_wait_cl(&bars->x_ready, kp & 1, abort_flag, R);
+          if (ok) {
+            tc_fence_after();
+            tc_fence_before();
+            arrive_leader(&bars->pair_ready, leader, lead);
+          }
+          if (leader && ok)
+            ok = mbar_wait_cl(&bars->res_full, kp & 1, abort_flag, R) &&
+                 mbar_wait_cl(&bars->pair_ready, kp & 1, abort_flag, R);
+          ++kp;
+          if (!leader) continue;
+          for (int m = 0; ok && m < n_own; ++m, ++M) {
+            // S of step M (slices 0-3) once the elementwise warps read S of step M - 1, then dP
+            // (slices 4-7) once they read dP of step M - 1: each overlaps the other's readout
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              if ((k & 3) == 0) {
-                if (m >= 1 && !mbar_wait_cl(k == 0 ? &bars->s_free : &bars->p_free, (m - 1) & 1, abort_flag, R)) {
+            for (int kk = 0; kk < 8; ++kk) {
+              if ((kk & 3) == 0) {
+                if (M >= 1 && !mbar_wait_cl(kk == 0 ? &bars->s_free : &bars->p_free, (M - 1) & 1, abort_flag, R)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
               }
-              if (!mbar_wait_cl(&bars->ring_full[k & 3], (k >> 2) & 1, abort_flag, R)) {
+              if (!mbar_wait_cl(&bars->ring_full[kk & 3], (kk >> 2) & 1, abort_flag, R)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint64_t sd = desc_add(rd, (k & 3) * SLOT_P);
+              const uint64_t sd = desc_add(rd, (kk & 3) * SLOT_P);
 #pragma unroll
               for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                  const int c = 2 * (k & 3) + cc;  // 64-column chunk of the head dim
+                  const int c = 2 * (kk & 3) + cc;  // 64-column chunk of the head dim
                   const uint64_t bdk = desc_add(sd, cc * HT * 128 + ks * 32);
-                  if (k < 4)  // S += X[:, chunk] slice^T, X from Tensor Memory (8 columns per 16 elements)
+                  if (kk < 4)  // S += X[:, chunk] slice^T, X from Tensor Memory (8 columns per 16 elements)
                     mma_pair_ts(s_tm, x_tm + c * 32 + ks * 8, bdk, idS, (c | ks) ? 1u : 0u);
                   else
                     mma_pair_ss(dp_tm, desc_add(yd, c * T * 128 + ks * 32), bdk, idS, (c | ks) ? 1u : 0u);
                 }
               }
-              mma_commit_pair(&bars->ring_empty[k & 3], pmask);
-              if (k == 3) mma_commit_pair(&bars->s_full, pmask);
-              if (k == 7) mma_commit_pair(&bars->p_full, pmask);
+              mma_commit_pair(&bars->ring_empty[kk & 3], pmask);
+              if (kk == 3) mma_commit_pair(&bars->s_full, pmask);
+              if (kk == 7) mma_commit_pair(&bars->p_full, pmask);
             }
           }
         }
       } else if (leader) {
         const uint32_t idA = idesc_f16(2 * T, 256, 0, 0, 0, 1);  // A K-major (fp16 tile), B MN-major
-        int used = 0;
-        for (int n = 0; ok && n < N; ++n) {
-          // step n comes from producer pair n % NPP, its own step j = n / NPP, into slot (n % NPP) RS + j % RS
-          const int j = n / NPP, slot = (n % NPP) * RS + j % RS, ph = (j / RS) & 1;
-          if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R) ||
-              !mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R) ||
-              !mbar_wait_cl(&bars->peer_recv[slot], ph, abort_flag, R)) {
+        int used = 0;      // ring loads consumed
+        int ka = 0;        // items accumulated so far
+        int J0 = 0, J1 = 0, J2 = 0;  // own steps of producer pairs 0, 1, 2 consumed so far
+        static_assert(NPP <= 3, "producer pairs");
+        for (int k = 0; ok; ++k) {
+          const int id = get_item(k, ok);
+          if (id < 0) break;
+          const Item x = make_item<DIR>(g, id, npairs, LX, h);
+          if (x.N == 0) continue;
+          // both CTAs' epilogues have read the previous item's accumulator out
+          if (ka > 0 && !mbar_wait_cl(&bars->acc_free, (ka - 1) & 1, abort_flag, R)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + slot * TILE_BYTES, 16, 1024);
-          for (int c = 0; c < DH / 256; ++c, ++used) {
-            const int s = used % NR_A;
-            if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_A) & 1, abort_flag, R)) {
+          for (int n = 0; ok && n < x.N; ++n) {
+            // step n comes from producer pair n % NPP, its own step j, into slot (n % NPP) RS + j % RS
+            const int pr = n % NPP;
+            const int j = (pr == 0 ? J0 : (pr == 1 ? J1 : J2)) + n / NPP, slot = pr * RS + j % RS, ph = (j / RS) & 1;
+            if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R) ||
+                !mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R) ||
+                !mbar_wait_cl(&bars->peer_recv[slot], ph, abort_flag, R)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t bd = smem_desc_sw128(sbase + OFF_RING_A + s * SLOT_A, T * 128, 1024);
+            const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + slot * TILE_BYTES, 16, 1024);
+            for (int c = 0; c < DH / 256; ++c, ++used) {
+              const int s = used % NR_A;
+              if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_A) & 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t bd = smem_desc_sw128(sbase + OFF_RING_A + s * SLOT_A, T * 128, 1024);
 #pragma unroll
-            for (int ks = 0; ks < T / 16; ++ks)
-              mma_pair_ss(tmem + c * 256, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32), desc_add(bd, ks * 2048),
-                          idA, (n | ks) ? 1u : 0u);
-            mma_commit_pair(&bars->ring_empty[s], pmask);
+              for (int ks = 0; ks < T / 16; ++ks)
+                mma_pair_ss(tmem + c * 256, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32),
+                            desc_add(bd, ks * 2048), idA, (n | ks) ? 1u : 0u);
+              mma_commit_pair(&bars->ring_empty[s], pmask);
+            }
+            if (!ok) break;
+            mma_commit_pair(&bars->mma_done[slot], pmask);
           }
           if (!ok) break;
-          mma_commit_pair(&bars->mma_done[slot], pmask);
+          J0 += own_steps<NPP>(x.N, 0);
+          J1 += own_steps<NPP>(x.N, 1);
+          if (NPP > 2) J2 += own_steps<NPP>(x.N, 2);
+          mma_commit_pair(&bars->acc_done, pmask);
+          ++ka;
         }
-        if (ok) mma_commit_pair(&bars->acc_done, pmask);
       }
       // every MMA the leader issued has finished before either CTA releases Tensor Memory
       if (leader) mma_commit_pair(&bars->mma_drain, pmask);
       mbar_wait_drain(&bars->mma_drain, 0);
     }
   } else if (warp == kSigWarp) {
-    // ------------------------------------------------------------ relay (producer peer)
-    if (!acc_role && !leader && elect_one()) {
+    if (rank == 0 && elect_one()) {
+      // ---------------------------------------------------------- scheduler (rank 0)
+      // Items are handed out one at a time from the pass's counter, so a
+      // cluster that starts late (the two passes run side by side) or draws
+      // short items takes more of them.  Each id goes into slot k % 2 of
+      // every CTA; the slot is reused once all readers have read it.
+      for (int k = 0;; ++k) {
+        const int s = k & 1;
+        if (k >= 2 && !mbar_wait_cl(&bars->item_empty[s], ((k >> 1) - 1) & 1, abort_flag, R)) break;
+        int id = atomicAdd(p.work, 1);
+        if (id >= p.n_items) id = -1;
+        const uint32_t slot_addr = smem_u32(&bars->item_id[s]);
+        for (uint32_t r = 0; r < R; ++r) st_cluster_u32(mapa(slot_addr, r), (uint32_t)id);
+        fence_acq_rel_cluster();  // the ids are visible before any CTA sees the arrive
+        for (uint32_t r = 0; r < R; ++r) mbar_arrive_remote(mapa(smem_u32(&bars->item_full[s]), r));
+        if (id < 0) break;
+      }
+    } else if (!acc_role && !leader && elect_one()) {
+      // ---------------------------------------------------------- relay (producer peer)
       // the peer's 8 warps arrive locally; one remote arrival per step tells the leader
-      for (int m = 0; m < n_own; ++m) {
-        if (!mbar_wait_cl(&bars->s_free, m & 1, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->s_free), lead));
-        if (!mbar_wait_cl(&bars->p_free, m & 1, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->p_free), lead));
+      bool ok = true;
+      int M = 0;
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const Item x = make_item<DIR>(g, id, npairs, LX, h);
+        const int n_own = own_steps<NPP>(x.N, pp);
+        for (int m = 0; m < n_own; ++m, ++M) {
+          if (!mbar_wait_cl(&bars->s_free, M & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(mapa(smem_u32(&bars->s_free), lead));
+          if (!mbar_wait_cl(&bars->p_free, M & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(mapa(smem_u32(&bars->p_free), lead));
+        }
       }
     }
   } else if (warp == kStoreWarp) {
@@ -516,31 +668,38 @@ __global__ void __launch_bounds__(kThr, 1)
       bool ok = (DIR == kDirQ || sm_dst[0] >= 0) && sm_dst[1] >= 0;
       if (!ok) cluster_abort(abort_flag, R);
       int ci = 0;  // tiles staged per warpgroup so far
-      for (int m = 0; ok && m < n_own; ++m) {
-        const int slot = pp * RS + m % RS;
-        for (int kind = (DIR == kDirKV ? 0 : 1); ok && kind < 2; ++kind, ++ci) {
-          const uint32_t dst = (kind == 0 ? kAccP : kAccDS) + h;
-          if (m >= RS && !mbar_wait_cl(&bars->scratch_free[kind][m % RS], ((m / RS) - 1) & 1, abort_flag, R)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();
-          unsigned char* gdst = g_tile_scratch + ((size_t)sm_dst[kind] * kMaxRecv + slot) * TILE_BYTES;
-          for (int w = 0; w < 2; ++w) {
-            if (!mbar_wait_cl(&bars->staged[w], ci & 1, abort_flag, R)) {
+      int M = 0;   // own steps so far
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const Item x = make_item<DIR>(g, id, npairs, LX, h);
+        const int n_own = own_steps<NPP>(x.N, pp);
+        for (int m = 0; ok && m < n_own; ++m, ++M) {
+          const int slot = pp * RS + M % RS;
+          for (int kind = (DIR == kDirKV ? 0 : 1); ok && kind < 2; ++kind, ++ci) {
+            const uint32_t dst = (kind == 0 ? kAccP : kAccDS) + h;
+            if (M >= RS && !mbar_wait_cl(&bars->scratch_free[kind][M % RS], ((M / RS) - 1) & 1, abort_flag, R)) {
               ok = false;
               break;
             }
-            bulk_store_s2g(gdst + w * HALF_BYTES, sbase + OFF_STG + w * HALF_BYTES, HALF_BYTES);
-            bulk_commit_group();
+            fence_proxy_async_global();
+            unsigned char* gdst = g_tile_scratch + ((size_t)sm_dst[kind] * kMaxRecv + slot) * TILE_BYTES;
+            for (int w = 0; w < 2; ++w) {
+              if (!mbar_wait_cl(&bars->staged[w], ci & 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              bulk_store_s2g(gdst + w * HALF_BYTES, sbase + OFF_STG + w * HALF_BYTES, HALF_BYTES);
+              bulk_commit_group();
+            }
+            if (!ok) break;
+            bulk_wait_read_all();
+            mbar_arrive(&bars->stg_free[0]);
+            mbar_arrive(&bars->stg_free[1]);
+            bulk_wait_all();
+            fence_proxy_async_global();
+            mbar_arrive_remote(mapa(smem_u32(&bars->tile_ready[slot]), dst));
           }
-          if (!ok) break;
-          bulk_wait_read_all();
-          mbar_arrive(&bars->stg_free[0]);
-          mbar_arrive(&bars->stg_free[1]);
-          bulk_wait_all();
-          fence_proxy_async_global();
-          mbar_arrive_remote(mapa(smem_u32(&bars->tile_ready[slot]), dst));
         }
       }
       bulk_wait_all();  // no store still reads this CTA's shared memory
@@ -552,39 +711,11 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const float sl2 = g.scale * kLog2e;
     const int cb0 = 64 * wg;
-    const int row = r0 + r;  // key (KV) or query (Q) of this thread
-    const bool row_ok = row < LX;
-    {
-      // resident S operand into Tensor Memory: row r, fp16 pairs -> one 32-bit column each;
-      // warpgroup wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
-      const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)head * LX + (row_ok ? row : 0)) * DH) +
-                         wg * 32;
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        uint32_t v[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * q] = w4.x;
-          v[4 * q + 1] = w4.y;
-          v[4 * q + 2] = w4.z;
-          v[4 * q + 3] = w4.w;
-        }
-        tmem_st32(tmem + lane_off + X_COL + wg * 128 + j * 32, v);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->x_ready);
-    }
-    float2 rs_row = make_float2(0.f, 0.f);
-    if (DIR == kDirQ && row_ok)
-      rs_row = make_float2(p.stats[(size_t)head * p.Lpad + row], p.stats[((size_t)g.B * g.Hq + head) * p.Lpad + row]);
     const uint32_t stg = sbase + OFF_STG + wg * HALF_BYTES;
     const uint32_t stg_row = stg + r * 128;
     const bool issuer = (warp & 3) == 2;  // warp 2 / 6 loads its warpgroup's step statistics
     int copies = 0;                       // copies out of this warpgroup's staging half
     bool ok = true;
-    // stage one 64-column half tile and copy it into accumulator rank `dst`'s slot for this producer pair
     // stage one 64-column half tile for the store thread
     auto send = [&](const uint32_t (&o)[32]) -> bool {
       if (copies > 0 && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[wg], (copies - 1) & 1, abort_flag, R)))
@@ -597,152 +728,242 @@ __global__ void __launch_bounds__(kThr, 1)
       ++copies;
       return true;
     };
-    // dK/dV pass: the statistics of own step m's 64 columns of this warpgroup
-    // (lse * log2e, then Delta) are bulk-copied into shared memory while the
-    // previous step is finished; every thread then reads them by broadcast
+    // dK/dV pass: the statistics of an own step's 64 columns of this
+    // warpgroup (lse * log2e, then Delta) are bulk-copied into shared memory
+    // while the previous step is finished; every thread then reads them by
+    // broadcast
     const uint32_t lse_s = sbase + OFF_STATS + wg * 512, dl_s = lse_s + 256;
     int st_issued = 0;
-    auto load_stats = [&](int m) {
+    auto load_stats = [&](const Item& x, int m) {
       const int n = pp + NPP * m;
-      const float* src = p.stats + (size_t)step_head(n) * p.Lpad + step_rows(n) + cb0;
+      const float* src = p.stats + (size_t)step_head<DIR>(g, x, n) * p.Lpad + step_rows<DIR>(g, x, n) + cb0;
       mbar_arrive_expect_tx(&bars->stats_full[wg], 512);
       bulk_load_g2s(lse_s, src, 256, &bars->stats_full[wg]);
       bulk_load_g2s(dl_s, src + (size_t)g.B * g.Hq * p.Lpad, 256, &bars->stats_full[wg]);
       ++st_issued;
     };
-    if (DIR == kDirKV && issuer && lane == 0 && n_own > 0) load_stats(0);
-    for (int m = 0; m < n_own; ++m) {
-      const int n = pp + NPP * m;
-      const int c0 = step_rows(n);  // first column's query (KV) or key (Q)
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full, m & 1, abort_flag, R))) {
+    int M = 0;  // own steps so far
+    for (int k = 0; ok; ++k) {
+      const int id = get_item_warp(k, ok);
+      if (id < 0) break;
+      const Item x = make_item<DIR>(g, id, npairs, LX, h);
+      const int n_own = own_steps<NPP>(x.N, pp);
+      if (n_own == 0) continue;
+      const int row = x.r0 + r;  // key (KV) or query (Q) of this thread
+      const bool row_ok = row < LX;
+      {
+        // resident S operand into Tensor Memory: row r, fp16 pairs -> one 32-bit column each;
+        // warpgroup wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256)).
+        // The previous item's S MMAs, the only readers, finished: their
+        // s_full was seen before its last S was read.
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.x16 + ((size_t)x.head * LX + (row_ok ? row : 0)) * DH) + wg * 32;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+            v[4 * q] = w4.x;
+            v[4 * q + 1] = w4.y;
+            v[4 * q + 2] = w4.z;
+            v[4 * q + 3] = w4.w;
+          }
+          tmem_st32(tmem + lane_off + X_COL + wg * 128 + j * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->x_ready);
+      }
+      float2 rs_row = make_float2(0.f, 0.f);
+      if (DIR == kDirQ && row_ok)
+        rs_row =
+            make_float2(p.stats[(size_t)x.head * p.Lpad + row], p.stats[((size_t)g.B * g.Hq + x.head) * p.Lpad + row]);
+      if (DIR == kDirKV && issuer && lane == 0) {
+        // the warpgroup has read the previous step's statistics
+        if (M > 0 && !mbar_wait_cl(&bars->stats_free[wg], (M - 1) & 1, abort_flag, R)) ok = false;
+        else load_stats(x, 0);
+      }
+      if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      uint32_t sv[64], dv[64];
-      tmem_ld32(tmem + lane_off + S_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_ld32(tmem + lane_off + S_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free);  // S may be overwritten (the peer's relay tells the leader)
-      bool full;
-      int4 vv;
-      if (DIR == kDirKV) {  // columns are query rows c0 .. c0 + 127, this thread's row is key `row`
-        full = own_rows && keys_tile_full(g, r0, rlast, c0, c0 + T - 1);
-        vv = key_vis(g, row, c0);
-      } else {  // columns are keys c0 .. c0 + 127, this thread's row is query `row`
-        full = own_rows && rows_tile_full(g, r0, rlast, c0, c0 + T - 1);
-        vv = row_vis(g, row, c0);
-      }
-      if (DIR == kDirKV && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stats_full[wg], m & 1, abort_flag, R))) {
-        ok = false;
-        break;
-      }
-      bool both;
-      vv = vis_in_tile(vv, T, &both);
-      const bool two_here = two && __any_sync(0xffffffffu, both);
-      if (full) p_tile64<true, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
-      else if (two_here) p_tile64<false, DIR == kDirKV, true>(sv, lse_s, rs_row.x, sl2, cb0, vv);
-      else p_tile64<false, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
-      uint32_t o[32];
-      if (DIR == kDirKV) {
-        pack64(sv, o);
-        if (!send(o)) {  // P^T -> dV accumulator
+      for (int m = 0; m < n_own; ++m, ++M) {
+        const int n = pp + NPP * m;
+        const int c0 = step_rows<DIR>(g, x, n);  // first column's query (KV) or key (Q)
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full, M & 1, abort_flag, R))) {
           ok = false;
           break;
         }
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->p_full, m & 1, abort_flag, R))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_ld32(tmem + lane_off + DP_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(dv));
-      tmem_ld32(tmem + lane_off + DP_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_free);  // dP may be overwritten
-      ds_tile64<DIR == kDirKV>(sv, dv, dl_s, rs_row.y, o);
-      if (DIR == kDirKV) {
-        // the warpgroup has read this step's statistics: the next step's may land
-        mbar_arrive(&bars->stats_free[wg]);
-        if (issuer && lane == 0 && m + 1 < n_own) {
-          if (!mbar_wait_cl(&bars->stats_free[wg], m & 1, abort_flag, R)) ok = false;
-          else load_stats(m + 1);
+        tc_fence_after();
+        uint32_t sv[64], dv[64];
+        tmem_ld32(tmem + lane_off + S_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(tmem + lane_off + S_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free);  // S may be overwritten (the peer's relay tells the leader)
+        bool full;
+        int4 vv;
+        if (DIR == kDirKV) {  // columns are query rows c0 .. c0 + 127, this thread's row is key `row`
+          full = x.own_rows && keys_tile_full(g, x.r0, x.rlast, c0, c0 + T - 1);
+          vv = key_vis(g, row, c0);
+        } else {  // columns are keys c0 .. c0 + 127, this thread's row is query `row`
+          full = x.own_rows && rows_tile_full(g, x.r0, x.rlast, c0, c0 + T - 1);
+          vv = row_vis(g, row, c0);
         }
-        if (!__all_sync(0xffffffffu, ok)) {
+        if (DIR == kDirKV && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stats_full[wg], M & 1, abort_flag, R))) {
           ok = false;
           break;
         }
-      }
-      if (!send(o)) {  // dS -> dK / dQ accumulator
-        ok = false;
-        break;
+        bool both;
+        vv = vis_in_tile(vv, T, &both);
+        const bool two_here = two && __any_sync(0xffffffffu, both);
+        if (full) p_tile64<true, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
+        else if (two_here) p_tile64<false, DIR == kDirKV, true>(sv, lse_s, rs_row.x, sl2, cb0, vv);
+        else p_tile64<false, DIR == kDirKV>(sv, lse_s, rs_row.x, sl2, cb0, vv);
+        uint32_t o[32];
+        if (DIR == kDirKV) {
+          pack64(sv, o);
+          if (!send(o)) {  // P^T -> dV accumulator
+            ok = false;
+            break;
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->p_full, M & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + DP_COL + cb0, *reinterpret_cast<uint32_t(*)[32]>(dv));
+        tmem_ld32(tmem + lane_off + DP_COL + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_free);  // dP may be overwritten
+        ds_tile64<DIR == kDirKV>(sv, dv, dl_s, rs_row.y, o);
+        if (DIR == kDirKV) {
+          // the warpgroup has read this step's statistics: the next step's may land
+          mbar_arrive(&bars->stats_free[wg]);
+          if (issuer && lane == 0 && m + 1 < n_own) {
+            if (!mbar_wait_cl(&bars->stats_free[wg], M & 1, abort_flag, R)) ok = false;
+            else load_stats(x, m + 1);
+          }
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!send(o)) {  // dS -> dK / dQ accumulator
+          ok = false;
+          break;
+        }
       }
     }
     // unwinding: the last statistics load must have landed (the store thread
     // waits for its own stores)
     if (st_issued > 0) mbar_wait_drain(&bars->stats_full[wg], (st_issued - 1) & 1);
   } else {
-    // ------------------------------------------------------------ epilogue (accumulator roles, both CTAs)
+    // ------------------------------------------------------------ accumulator warps 2-9 (both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    if (warp >= 2 + NPP && warp < 2 + 2 * NPP && elect_one()) {
-      // one loader per producer pair (warps 2 + NPP ..): once the MMAs are
-      // done with a slot and the producer's tile is in the scratch, load it
-      // into the slot
-      const int p2 = warp - 2 - NPP;
-      const unsigned char* scr = g_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * kMaxRecv * TILE_BYTES;
-      bool ok = bars->smid >= 0;
-      if (!ok) cluster_abort(abort_flag, R);
-      for (int j = 0; ok && p2 + NPP * j < N; ++j) {
-        const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
-        if (j >= RS && !mbar_wait_cl(&bars->mma_done[slot], ((j / RS) - 1) & 1, abort_flag, R)) break;
-        mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
-        mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
-        if (!mbar_wait_cl(&bars->tile_ready[slot], ph, abort_flag, R)) {
-          // armed but never loaded: complete the phases so the drain below does not wait on them
-          ok = false;
-          break;
+    const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
+    const float mul = (DIR == kDirKV && role == kRoleAccP) ? inv_s : g.scale * inv_s;
+    float* const out = (DIR == kDirKV && role == kRoleAccP) ? p.out1 : p.out0;
+    const CUtensorMap* om = (DIR == kDirKV && role == kRoleAccP) ? &tmO1 : &tmO0;
+    const bool loader = warp >= 2 + NPP && warp < 2 + 2 * NPP;  // one per producer pair
+    const bool watcher = warp >= 2 && warp < 2 + NPP;           // one per producer pair
+    const int p2 = loader ? warp - 2 - NPP : warp - 2;          // the pair a loader or watcher serves
+    const unsigned char* scr = g_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * kMaxRecv * TILE_BYTES;
+    bool ok = true;
+    if (loader && bars->smid < 0) {
+      ok = false;
+      if (lane == 0) cluster_abort(abort_flag, R);
+    }
+    int J = 0;   // own steps of pair p2 handled so far (loaders and watchers)
+    int ka = 0;  // items accumulated so far
+    for (int k = 0; ok; ++k) {
+      const int id = get_item_warp(k, ok);
+      if (id < 0) break;
+      const Item x = make_item<DIR>(g, id, npairs, LX, h);
+      if (x.N == 0) {
+        // dK/dV pass, and no query sees these keys (queries that are a suffix
+        // of the keys, with a window): zero gradients ("Lab 028 lab detail",
+        // "What I changed, in plain terms" item 5(b))
+        zero_rows(out, x.head, x.r0, T, g.L, DH, (int)threadIdx.x - 64, 256);
+        continue;
+      }
+      const int nown = (loader || watcher) ? own_steps<NPP>(x.N, p2) : 0;
+      if (loader && lane == 0) {
+        // once the MMAs are done with a slot and the producer's tile is in
+        // the scratch, load it into the slot; the receive slots held the
+        // previous item's epilogue staging until its stores had read it
+        if (ka > 0 && !mbar_wait_cl(&bars->epi_done, (ka - 1) & 1, abort_flag, R)) ok = false;
+        for (int j = J; ok && j < J + nown; ++j) {
+          const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
+          if (j >= RS && !mbar_wait_cl(&bars->mma_done[slot], ((j / RS) - 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->recv_full[slot][0], HALF_BYTES);
+          mbar_arrive_expect_tx(&bars->recv_full[slot][1], HALF_BYTES);
+          if (!mbar_wait_cl(&bars->tile_ready[slot], ph, abort_flag, R)) {
+            // armed but never loaded: the drain below does not wait on it
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          bulk_load_g2s(sbase + OFF_RECV + slot * TILE_BYTES, scr + (size_t)slot * TILE_BYTES, HALF_BYTES,
+                        &bars->recv_full[slot][0]);
+          bulk_load_g2s(sbase + OFF_RECV + slot * TILE_BYTES + HALF_BYTES,
+                        scr + (size_t)slot * TILE_BYTES + HALF_BYTES, HALF_BYTES, &bars->recv_full[slot][1]);
+          bars->n_loaded[p2] = j + 1;
         }
-        fence_proxy_async_global();
-        bulk_load_g2s(sbase + OFF_RECV + slot * TILE_BYTES, scr + (size_t)slot * TILE_BYTES, HALF_BYTES,
-                      &bars->recv_full[slot][0]);
-        bulk_load_g2s(sbase + OFF_RECV + slot * TILE_BYTES + HALF_BYTES, scr + (size_t)slot * TILE_BYTES + HALF_BYTES,
-                      HALF_BYTES, &bars->recv_full[slot][1]);
-        bars->n_loaded[p2] = j + 1;
       }
-    }
-    if (warp >= 2 && warp < 2 + NPP && elect_one()) {
-      // one warp per producer pair (warps 2 ..): when both halves of a tile are in the
-      // slot, the producer may reuse that scratch slot; the peer also tells
-      // the leader that its rows of the step's A operand are here
-      const int p2 = warp - 2;
-      const uint32_t prod = (uint32_t)(2 * p2) + h;
-      for (int j = 0; p2 + NPP * j < N; ++j) {
-        const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
-        if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R)) break;
-        if (!mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R)) break;
-        bars->n_recv[p2] = j + 1;
-        mbar_arrive_remote(mapa(smem_u32(&bars->scratch_free[dst_kind][j % RS]), prod));
-        if (!leader) mbar_arrive_remote(mapa(smem_u32(&bars->peer_recv[slot]), lead));
+      if (watcher && lane == 0) {
+        // when both halves of a tile are in the slot, the producer may reuse
+        // that scratch slot; the peer also tells the leader that its rows of
+        // the step's A operand are here
+        const uint32_t prod = (uint32_t)(2 * p2) + h;
+        for (int j = J; j < J + nown; ++j) {
+          const int slot = p2 * RS + j % RS, ph = (j / RS) & 1;
+          if (!mbar_wait_cl(&bars->recv_full[slot][0], ph, abort_flag, R) ||
+              !mbar_wait_cl(&bars->recv_full[slot][1], ph, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          bars->n_recv[p2] = j + 1;
+          mbar_arrive_remote(mapa(smem_u32(&bars->scratch_free[dst_kind][j % RS]), prod));
+          if (!leader) mbar_arrive_remote(mapa(smem_u32(&bars->peer_recv[slot]), lead));
+        }
       }
-    }
-    __syncwarp();
-    if (__all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R))) {
+      J += nown;
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, ka & 1, abort_flag, R))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      float mul;
-      const float inv_s = p.stats[dscale_offset(g, p.Lpad) + 1];  // 1/s of the scaled dO copy
-      if (DIR == kDirKV) mul = (role == kRoleAccP) ? inv_s : g.scale * inv_s;
-      else mul = g.scale * inv_s;
-      const CUtensorMap* om = (DIR == kDirKV && role == kRoleAccP) ? &tmO1 : &tmO0;
-      // every operand slot and ring load has been consumed by the finished
-      // MMAs: each of warps 2-9 stages its blocks in 16 KB of that space
-      tmem_rows_store_tma(om, tmem + lane_off + 256 * wg, 256 * wg, 256, mul, sbase + (uint32_t)(warp - 2) * 16384u,
-                          r0 + 32 * q4, head, lane);
+      // every receive slot has been consumed by the finished MMAs: each of
+      // warps 2-9 stages its blocks in NRECV 4 KB buffers there (an eighth
+      // of the slots; the ring after them may already hold the next item's
+      // loads)
+      static_assert(8 * NRECV * 4096 == NRECV * TILE_BYTES && NRECV <= 4, "epilogue staging fills the receive slots");
+      tmem_rows_store_tma<NRECV, false>(om, tmem + lane_off + 256 * wg, 256 * wg, 256, mul,
+                                        sbase + OFF_RECV + (uint32_t)(warp - 2) * (NRECV * 4096u), x.r0 + 32 * q4,
+                                        x.head, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->epi_done);                   // the staging may be overwritten
+        arrive_leader(&bars->acc_free, leader, lead);  // the accumulator may be overwritten
+      }
+      ++ka;
     }
+    if (lane == 0) bulk_wait_all();  // the epilogue stores have written
   }
 
   __syncwarp();
@@ -761,19 +982,22 @@ __global__ void __launch_bounds__(kThr, 1)
           mbar_wait_drain(&bars->recv_full[pr * RS + j % RS][1], (j / RS) & 1);
         }
     }
-    // Leader: the ring loads of both CTAs complete on its barriers; let the
-    // last load of each slot (of either CTA) land.
+    // Leader: the ring and resident loads of both CTAs complete on its
+    // barriers; let the last load of each slot (of either CTA) land.
     if (leader) {
-      int peer_issued;
+      int peer_issued, peer_res;
       asm volatile("ld.shared::cluster.u32 %0, [%1];"
                    : "=r"(peer_issued)
                    : "r"(mapa(smem_u32(&bars->n_issued), lead + 1))
+                   : "memory");
+      asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_res) : "r"(mapa(smem_u32(&bars->n_res), lead + 1))
                    : "memory");
       const int issued = max(bars->n_issued, peer_issued);
       const int nr = acc_role ? NR_A : NR_P;
       for (int k = issued - 1; k >= 0 && k >= issued - nr; --k)
         mbar_wait_drain(&bars->ring_full[k % nr], (k / nr) & 1);
-      if (!acc_role) mbar_wait_drain(&bars->res_full, 0);
+      const int n_res = max(bars->n_res, peer_res);
+      if (!acc_role && n_res > 0) mbar_wait_drain(&bars->res_full, (n_res - 1) & 1);
     }
   }
   __syncthreads();
@@ -783,12 +1007,32 @@ __global__ void __launch_bounds__(kThr, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
   }
+  // dQ pass started early beside the dK/dV pass: it completes after that
+  // pass, so that whatever follows on the stream sees both finished
+  if (DIR == kDirQ && threadIdx.x == 0) grid_dependency_wait();
+}
+
+// Clusters of a pass that fit on the current device at once (cached per
+// device; 0 on an error).
+template <int DIR>
+int max_clusters(const cudaLaunchConfig_t& cfg) {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, bwd512_kernel<DIR>, &cfg) != cudaSuccess) return 0;
+  if (dev < kMaxDevices && n > 0) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 template <int DIR>
 cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                         const uint16_t* g16, const float* stats, int Lpad, float* out0, float* out1, int* status,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool early) {
   // streamed operands (64-row halves, two chunks per slice), the resident dP
   // operand (one chunk of 128 rows per load), accumulator operands (two chunks
   // of 128 rows per load)
@@ -820,29 +1064,38 @@ cudaError_t launch_pair(const Geom& g, const uint16_t* q16, const uint16_t* k16,
     return e;
   ParamsPair pm;
   pm.g = g;
+  // the pass's work counter in the stats tail, zeroed by the absmax pass
+  pm.work = reinterpret_cast<int*>(const_cast<float*>(stats) + dscale_offset(g, Lpad) + kWorkCounterFloat + DIR);
   pm.out0 = out0;
   pm.out1 = out1;
   pm.x16 = (DIR == kDirKV) ? k16 : q16;
   pm.stats = stats;
   pm.Lpad = Lpad;
   pm.n_tiles = ((DIR == kDirKV ? g.L : g.Lq) + T - 1) / T;  // resident-side tiles
+  pm.n_items = g.B * g.Hkv * ((pm.n_tiles + 1) / 2) * (DIR == kDirQ ? g.G : 1);
   pm.status = status;
   constexpr unsigned R = PassCfg<DIR>::R;
   if (R > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
     return e;
-  const unsigned xs = (DIR == kDirKV) ? R : R * (unsigned)g.G;  // dQ pass: the group's query heads along x
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(xs, (unsigned)((pm.n_tiles + 1) / 2), (unsigned)(g.B * g.Hkv));
+  cfg.gridDim = dim3(R, 1, 1);
   cfg.blockDim = dim3(kThr, 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = R;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // persistent clusters: as many as fit on the GPU at once, at most one per item
+  const int fit = max_clusters<DIR>(cfg);
+  if (fit <= 0) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(R * (unsigned)min(fit, pm.n_items), 1, 1);
+  if (early) cfg.numAttrs = 2;  // may start before the kernel ahead of it on `s` has finished
   return cudaLaunchKernelEx(&cfg, kern, tmS, tmP, tmR, tmA0, tmA1, tmO0, tmO1, pm);
 }
 
@@ -863,13 +1116,13 @@ int scratch_layout_bwd512() {
 cudaError_t launch_bwd_dkdv_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                    const uint16_t* g16, const float* stats, int Lpad, float* dk, float* dv,
                                    int* status, cudaStream_t s) {
-  return launch_pair<kDirKV>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s);
+  return launch_pair<kDirKV>(g, q16, k16, v16, g16, stats, Lpad, dk, dv, status, s, false);
 }
 
 cudaError_t launch_bwd_dq_tc512(const Geom& g, const uint16_t* q16, const uint16_t* k16, const uint16_t* v16,
                                  const uint16_t* g16, const float* stats, int Lpad, float* dq, int* status,
                                  cudaStream_t s) {
-  return launch_pair<kDirQ>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s);
+  return launch_pair<kDirQ>(g, q16, k16, v16, g16, stats, Lpad, dq, nullptr, status, s, true);
 }
 
 }  // namespace swa

@@ -312,8 +312,10 @@ __device__ __forceinline__ void cluster_sync() {
 //   - bulk copies waited on (cp.async.bulk.wait_group, or complete_tx seen);
 //   - Tensor Memory reads or writes ended by tcgen05.wait;
 //   - generic loads whose values the thread has already used.
-// No hand-off passes generic stores for the other CTA to read; those go
-// through cluster_sync().  A release at cluster scope stalls the issuing
+// The one hand-off that passes generic stores for the other CTA to read (the
+// work-item ids of the persistent D = 512 backward) puts fence_acq_rel_cluster()
+// between the stores and the arrive; everything else goes through
+// cluster_sync().  A release at cluster scope stalls the issuing
 // thread about 1,000-1,300 cycles on this GB300 (clock64, every hand-off of
 // the D = 512 forward), which sat on every step's critical path.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
@@ -332,6 +334,24 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
+
+// Programmatic dependent launch: this CTA lets the grid launched after it on
+// its stream (with programmatic stream serialization) start; that grid is
+// dispatched once every CTA of this one has done so or exited.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible (at once when it was launched without a dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 32-bit store into another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Orders this thread's earlier memory operations before its later ones for
+// every thread of the cluster (a later relaxed arrive then publishes them).
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Raise the abort flag in every CTA of the cluster (the flag sits at the same
 // shared offset in each CTA).
@@ -530,8 +550,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
 // Compared with per-thread 16-byte row stores, whose every warp instruction
 // touches 32 cache lines, the TMA unit writes whole lines.  Rows at or beyond
 // the tensor's length are clipped by the TMA unit.  Lane 0 waits for its
-// stores' writes before it returns.
-template <int NBUF = 4>
+// stores' writes before it returns, or (WAIT_WRITES false) only until they
+// have read the buffers; it must then wait for the writes before it exits.
+template <int NBUF = 4, bool WAIT_WRITES = true>
 __device__ __forceinline__ void tmem_rows_store_tma(const CUtensorMap* map, uint32_t taddr, int col0, int ncols,
                                                     float mul, uint32_t buf, int row0, int head, int lane) {
   static_assert(NBUF >= 1 && NBUF <= 4, "buffers");
@@ -559,7 +580,10 @@ __device__ __forceinline__ void tmem_rows_store_tma(const CUtensorMap* map, uint
       bulk_commit_group();
     }
   }
-  if (lane == 0) bulk_wait_all();
+  if (lane == 0) {
+    if (WAIT_WRITES) bulk_wait_all();
+    else bulk_wait_read_all();
+  }
   __syncwarp();
 }
 // Orders generic-proxy accesses to global memory with async-proxy ones.
@@ -583,12 +607,17 @@ __device__ __forceinline__ float4 ld_smem_f4(uint32_t cta_addr) {
 }
 
 // Rows [r0, min(r0 + rows, L)) of head `head` of an fp32 [heads, L, D]
-// tensor set to zero by every thread of the CTA (D a multiple of 4, the
-// tensor 16-byte aligned).
-__device__ __forceinline__ void zero_rows(float* out, int head, int r0, int rows, int L, int D) {
+// tensor set to zero by threads tid = 0 .. nthr - 1 (by default every thread
+// of the CTA; D a multiple of 4, the tensor 16-byte aligned).
+__device__ __forceinline__ void zero_rows(float* out, int head, int r0, int rows, int L, int D, int tid = -1,
+                                          int nthr = 0) {
+  if (tid < 0) {
+    tid = threadIdx.x;
+    nthr = blockDim.x;
+  }
   const int n = (rows < L - r0 ? rows : L - r0) * D / 4;
   float4* dst = reinterpret_cast<float4*>(out + ((size_t)head * L + r0) * D);
-  for (int e = threadIdx.x; e < n; e += blockDim.x) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int e = tid; e < n; e += nthr) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 }  // namespace tc
