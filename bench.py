@@ -115,23 +115,26 @@ def source_digest(kernel: str, D: int = 0) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def dominant_unit(kernels: dict, bwd_ms: float, steps: int):
-    """(name, average ms per launch) of the unit with the most time per step.
+def unit_times(kernels: dict, bwd_ms: float, steps: int) -> dict:
+    """Launch name -> (launches, total ms), with the tensor-core backward's
+    dK/dV and dQ passes as one unit ("bwd_dkdv_tc+bwd_dq_tc").  The two run
+    side by side (two streams, or one launched early beside the other on one
+    stream), so their own spans overlap; the unit is timed from the end of
+    the backward prep to the end of the backward call: `bwd_ms` minus the
+    average launch times of the prep kernels, per step.  The units then do
+    not overlap, and their totals divide into the step."""
+    if not (all(n in kernels for n in CONCURRENT_BWD) and "bwd_prep" in kernels and bwd_ms):
+        return dict(kernels)
+    group_ms = bwd_ms - sum(kernels[n][1] / kernels[n][0] for n in BWD_PREP_KERNELS if n in kernels)
+    units = {n: v for n, v in kernels.items() if n not in CONCURRENT_BWD}
+    units["+".join(CONCURRENT_BWD)] = (kernels[CONCURRENT_BWD[0]][0], group_ms * steps)
+    return units
 
-    `kernels` maps a launch name to (launches, total ms) over `steps` steps;
-    `bwd_ms` is the backward call's average span on the caller's stream.  The
-    tensor-core backward runs its dK/dV and dQ passes side by side on two
-    streams, so their per-launch spans overlap and each includes time spent
-    waiting for SMs the other holds.  They count as one unit, timed from the
-    end of the backward prep to the join: `bwd_ms` minus the average launch
-    times of the prep kernels (the max |dO| pass and the prep)."""
-    group_ms = None
-    if all(n in kernels for n in CONCURRENT_BWD) and "bwd_prep" in kernels and bwd_ms:
-        group_ms = bwd_ms - sum(kernels[n][1] / kernels[n][0] for n in BWD_PREP_KERNELS if n in kernels)
-    singles = {n: v for n, v in kernels.items() if group_ms is None or n not in CONCURRENT_BWD}
-    name, (launches, total) = max(singles.items(), key=lambda kv: kv[1][1])
-    if group_ms is not None and group_ms * steps > total:
-        return "+".join(CONCURRENT_BWD), group_ms
+
+def dominant_unit(kernels: dict, bwd_ms: float, steps: int):
+    """(name, average ms per launch) of the unit with the most time per step
+    (`unit_times`: the concurrent dK/dV and dQ passes count as one unit)."""
+    name, (launches, total) = max(unit_times(kernels, bwd_ms, steps).items(), key=lambda kv: kv[1][1])
     return name, total / launches
 
 
@@ -649,8 +652,9 @@ def measure_workload(args, w, world, rank, local_rank, dist, peaks):
     # roofline of the dominant kernel (or concurrent pair of kernels)
     kname, avg_ms = dominant_unit(kernels, bwd_ms, args.steps)
     roof = roofline_record(kname, avg_ms, w, peaks)
+    units = unit_times(kernels, bwd_ms, args.steps)
     per_kernel = {n: {"launches": c, "avg_ms": round(ms / c, 4), "share": round(ms / sum(x[1] for x in
-                  kernels.values()), 4)} for n, (c, ms) in kernels.items()}
+                  units.values()), 4)} for n, (c, ms) in units.items()}
     rec = {
         "value": round(value, 3), "ms_per_step": round(total_ms / args.steps, 4),
         "dtype": "f32" if kname.endswith("_simt") else "f16",

@@ -136,6 +136,7 @@ struct Bars {
   uint64_t epi_done;                 // (accumulator, own) the epilogue's stores read their staging
   uint64_t item_full[2];             // (every CTA) the scheduler wrote an item id into the slot
   uint64_t item_empty[2];            // (rank 0) every reader of the slot read it
+  uint64_t item_req;                 // (rank 0) its TMA thread will soon need the next item
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&bars->item_full[s], 1);
       mbar_init(&bars->item_empty[s], item_readers<DIR>());
     }
+    mbar_init(&bars->item_req, 1);
     for (int s = 0; s < NRECV; ++s) {
       mbar_init(&bars->tile_ready[s], 1);
       mbar_init(&bars->recv_full[s][0], 1);
@@ -437,7 +439,10 @@ __global__ void __launch_bounds__(kThr, 1)
           // resident dP operand (this CTA's 128 rows), then per own step four
           // slices for S and then four for dP (this CTA's 64 rows)
           const int n_own = own_steps<NPP>(x.N, pp);
-          if (n_own == 0) continue;
+          if (n_own == 0) {
+            if (rank == 0) mbar_arrive(&bars->item_req);
+            continue;
+          }
           // the previous item's last dP has finished reading the resident operand
           if (n_res > 0 && !mbar_wait_cl(&bars->p_full, (M - 1) & 1, abort_flag, R)) {
             ok = false;
@@ -450,6 +455,7 @@ __global__ void __launch_bounds__(kThr, 1)
           for (int m = 0; ok && m < n_own; ++m) {
             const int n = pp + NPP * m;
             const int rows = step_rows<DIR>(g, x, n) + HT * (int)h, hd = step_head<DIR>(g, x, n);
+            if (rank == 0 && m == n_own - 1) mbar_arrive(&bars->item_req);  // the next item is soon needed
             for (int kk = 0; kk < 2 * (DH / 128); ++kk, ++issued) {
               const int s = issued % NR_P;
               if (issued >= NR_P && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_P) & 1) ^ 1, abort_flag, R)) {
@@ -617,9 +623,16 @@ __global__ void __launch_bounds__(kThr, 1)
       // Items are handed out one at a time from the pass's counter, so a
       // cluster that starts late (the two passes run side by side) or draws
       // short items takes more of them.  Each id goes into slot k % 2 of
-      // every CTA; the slot is reused once all readers have read it.
+      // every CTA; the slot is reused once all readers have read it.  An id
+      // is drawn only when rank 0's TMA thread starts the last step of its
+      // current item: clusters then take items in about the order they
+      // finish them, as clusters of a non-persistent grid would be
+      // dispatched, and the clusters of one kv head walk its query tiles
+      // about in step, sharing them in L2 (drawing earlier tripled the dK/dV
+      // pass's DRAM reads).
       for (int k = 0;; ++k) {
         const int s = k & 1;
+        if (k >= 1 && !mbar_wait_cl(&bars->item_req, (k - 1) & 1, abort_flag, R)) break;
         if (k >= 2 && !mbar_wait_cl(&bars->item_empty[s], ((k >> 1) - 1) & 1, abort_flag, R)) break;
         int id = atomicAdd(p.work, 1);
         if (id >= p.n_items) id = -1;

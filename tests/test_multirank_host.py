@@ -103,6 +103,26 @@ def test_dominant_unit_groups_the_concurrent_backward_passes():
     assert bench.dominant_unit(s, 3.55, 2) == ("bwd_dkdv_simt", 2.0)
 
 
+def test_unit_times_count_the_concurrent_backward_passes_once():
+    import bench
+
+    # two steps: forward 0.12 ms, prep 0.03 ms, dK/dV and dQ overlapping
+    # inside a 0.36 ms backward: one unit of 0.33 ms per step
+    k = {"convert_f16": (2, 0.02), "fwd_tc": (2, 0.24), "bwd_prep": (2, 0.06),
+         "bwd_dkdv_tc": (2, 0.54), "bwd_dq_tc": (2, 0.64)}
+    u = bench.unit_times(k, 0.36, 2)
+    assert set(u) == {"convert_f16", "fwd_tc", "bwd_prep", "bwd_dkdv_tc+bwd_dq_tc"}
+    assert u["bwd_dkdv_tc+bwd_dq_tc"][0] == 2 and abs(u["bwd_dkdv_tc+bwd_dq_tc"][1] - 0.66) < 1e-12
+    # the units add up to the steps' time
+    assert abs(sum(ms for _, ms in u.values()) - 2 * (0.01 + 0.12 + 0.36)) < 1e-12
+    # both passes bracketed together (their spans equal): the same unit
+    k2 = dict(k, bwd_dkdv_tc=(2, 0.66), bwd_dq_tc=(2, 0.66))
+    assert bench.unit_times(k2, 0.36, 2) == u
+    # without the pair (the SIMT backward) the launches stand alone
+    s = {"fwd_simt": (2, 1.0), "bwd_delta": (2, 0.1), "bwd_dkdv_simt": (2, 4.0), "bwd_dq_simt": (2, 3.0)}
+    assert bench.unit_times(s, 3.55, 2) == s
+
+
 def test_cpu_baseline_adds_kv_groups_up_to_the_workload():
     import dataclasses
 
