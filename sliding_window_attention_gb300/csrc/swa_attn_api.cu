@@ -252,16 +252,19 @@ BwdTcWs bwd_tc_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
 }
 
 // Forward workspace layout on the tensor-core path: an fp16 copy of v (S =
-// Q K^T reads the bf16 q and k directly; O += P V pairs v with fp16 P).
+// Q K^T reads the bf16 q and k directly; O += P V pairs v with fp16 P), then
+// the work counter of the persistent head-dim-512 forward (zeroed by the
+// conversion of v, which runs first).
 struct FwdWs {
-  size_t v16, total;
+  size_t v16, work, total;
 };
 FwdWs fwd_ws_layout(int B, int Hq, int Hkv, int Lq, int L, int D) {
   (void)Hq;
   (void)Lq;
   FwdWs w;
   w.v16 = 0;
-  w.total = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  w.work = w.v16 + round_up((size_t)B * Hkv * L * D * 2, 256);
+  w.total = w.work + 256;
   return w;
 }
 
@@ -305,9 +308,11 @@ static int fwd_run(const swa::Geom& g, const swa_bf16* q, const swa_bf16* k, con
   const uint16_t* src[1] = {v};
   uint16_t* dst[1] = {v16};
   const size_t n[1] = {(size_t)B * Hkv * Lk * D};
-  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 1, status, s); }) != cudaSuccess)
+  int* work = reinterpret_cast<int*>(ws + w.work);
+  if (launch("convert_f16", s, [&] { return swa::launch_convert_f16(src, dst, n, 1, status, s, work); }) !=
+      cudaSuccess)
     return SWA_ERR_CUDA;
-  if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q, k, v16, o, lse, status, s); }) != cudaSuccess)
+  if (launch("fwd_tc", s, [&] { return swa::launch_fwd_tc(g, q, k, v16, o, lse, work, status, s); }) != cudaSuccess)
     return SWA_ERR_CUDA;
   return SWA_OK;
 }

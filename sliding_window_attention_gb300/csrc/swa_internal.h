@@ -233,9 +233,11 @@ cudaError_t launch_bwd_dq_simt(const Geom& g, const uint16_t* q, const uint16_t*
 
 // ---- tensor-core path (tcgen05 + TMA + TMEM), fp16 operand copies ----
 // bf16 -> fp16 copies of up to four tensors (n[i] elements, multiples of 8);
-// latches kStatusFp16Range in *status if a finite input overflows fp16.
+// latches kStatusFp16Range in *status if a finite input overflows fp16; sets
+// *zero_word to 0 when it is not null (the work counter of a persistent
+// launch that follows on the stream).
 cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
-                               int* status, cudaStream_t s);
+                               int* status, cudaStream_t s, int* zero_word = nullptr);
 // One CTA whose bounded wait on a barrier nothing completes runs out after
 // limit_cycles and latches kStatusTimeout in *status.
 cudaError_t launch_selftest_timeout(int* status, long long limit_cycles, cudaStream_t s);
@@ -247,13 +249,15 @@ bool decode_supported(const Geom& g);
 size_t decode_workspace_bytes(const Geom& g);  // fp32 chunk partials; 0 when one chunk suffices
 cudaError_t launch_fwd_decode(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
                               float* lse, float* ws, int* status, cudaStream_t s);
-// Head dim 512: 2-CTA cluster forward (tc_fwd512.cu).
+// Head dim 512: persistent 4-CTA clusters (tc_fwd512.cu) that draw work
+// items from *work, which must be zero when the launch starts.
 cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
-                             float* lse, int* status, cudaStream_t s);
+                             float* lse, int* work, int* status, cudaStream_t s);
 // Forward on the tensor cores: q and k are the caller's bf16 tensors (S = Q K^T
 // runs on bf16 operands), v16 an fp16 copy of v (O += P V pairs it with fp16 P).
+// work: a zeroed int in the workspace (used at head dim 512).
 cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
-                          float* lse, int* status, cudaStream_t s);
+                          float* lse, int* work, int* status, cudaStream_t s);
 
 // 3-D fp16 tensor map over [heads, L, D] with a 64 x box_rows box and
 // 128-byte swizzle (rows at or beyond L read as zero).

@@ -796,7 +796,8 @@ __global__ void __launch_bounds__(256) convert_bf16_f16_kernel(const uint16_t* s
                                                                const uint16_t* s1, uint16_t* d1, long long n1,
                                                                const uint16_t* s2, uint16_t* d2, long long n2,
                                                                const uint16_t* s3, uint16_t* d3, long long n3,
-                                                               int* status) {
+                                                               int* status, int* zero_word) {
+  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *zero_word = 0;
   const int seg = blockIdx.y;
   const uint4* src = reinterpret_cast<const uint4*>(seg == 0 ? s0 : seg == 1 ? s1 : seg == 2 ? s2 : s3);
   uint4* dst = reinterpret_cast<uint4*>(seg == 0 ? d0 : seg == 1 ? d1 : seg == 2 ? d2 : d3);
@@ -904,7 +905,7 @@ cudaError_t make_tmap_f32_out(CUtensorMap* m, void* ptr, int D, int L, int heads
 }
 
 cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
-                               int* status, cudaStream_t s) {
+                               int* status, cudaStream_t s, int* zero_word) {
   if (count < 1 || count > 4) return cudaErrorInvalidValue;
   const uint16_t* sp[4] = {nullptr, nullptr, nullptr, nullptr};
   uint16_t* dp[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -923,7 +924,7 @@ cudaError_t launch_convert_f16(const uint16_t* const* src, uint16_t* const* dst,
   if (blocks < 1) blocks = 1;
   dim3 grid((unsigned)blocks, count);
   convert_bf16_f16_kernel<<<grid, 256, 0, s>>>(sp[0], dp[0], nn[0], sp[1], dp[1], nn[1], sp[2], dp[2], nn[2], sp[3],
-                                              dp[3], nn[3], status);
+                                              dp[3], nn[3], status, zero_word);
   return cudaGetLastError();
 }
 
@@ -981,12 +982,12 @@ static cudaError_t fwd_pp_d(const Geom& g, const uint16_t* q, const uint16_t* k,
 bool fwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
 cudaError_t launch_fwd_tc(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
-                          float* lse, int* status, cudaStream_t s) {
+                          float* lse, int* work, int* status, cudaStream_t s) {
   switch (g.D) {
     case 64: return fwd_pp_d<64>(g, q, k, v16, o, lse, status, s);
     case 128: return fwd_pp_d<128>(g, q, k, v16, o, lse, status, s);
     case 256: return fwd_tc_d<256>(g, q, k, v16, o, lse, status, s);
-    case 512: return launch_fwd_tc512(g, q, k, v16, o, lse, status, s);
+    case 512: return launch_fwd_tc512(g, q, k, v16, o, lse, work, status, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -38,6 +38,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "swa_internal.h"
 #include "tc_ptx.cuh"
 
@@ -55,20 +57,21 @@ constexpr uint32_t R = 4;  // CTAs per cluster
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kMaxDevices = 64;
 
 constexpr int TILE_BYTES = T * T * 2;       // fp16 128 x 128 P tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // one warpgroup's 64 columns (one swizzle chunk)
 // producer shared memory: two staging tiles, row vectors, K ring of 32 KB
 // slices (four 64-column chunks of this CTA's 64 keys)
 constexpr int OFF_STG = 0;
-constexpr int OFF_VEC = 2 * TILE_BYTES;  // alpha[2][128], inv_l[128], max exchange [2][2][128], l exchange [2][128]
+constexpr int OFF_VEC = 2 * TILE_BYTES;  // alpha[2][128], (free)[128], max exchange [2][2][128], l exchange [2][128], 1 / l [2][128]
 constexpr int OFF_RING_P = OFF_VEC + 8192;
 constexpr int SLOT_P = HT * 256 * 2;
 constexpr int NR_P = 4;
 // accumulator shared memory: two P slots, two alpha slots + 1 / l, V ring of
 // 32 KB slots (two 64-column chunks of the 128 keys)
 constexpr int OFF_RECV = 0;
-constexpr int OFF_RVEC = 2 * TILE_BYTES;  // alpha slot [2][128], inv_l [128]
+constexpr int OFF_RVEC = 2 * TILE_BYTES;  // alpha slot [2][128], inv_l [2 item parity][128]
 constexpr int OFF_RING_A = 2 * TILE_BYTES + 2048;
 constexpr int SLOT_A = T * 128 * 2;
 constexpr int NR_A = 4;
@@ -77,7 +80,7 @@ constexpr int DATA_A = OFF_RING_A + NR_A * SLOT_A;
 constexpr int DATA_BYTES = DATA_P > DATA_A ? DATA_P : DATA_A;
 constexpr int kMaxRing = NR_P > NR_A ? NR_P : NR_A;
 constexpr uint32_t X_COL = 0, S_COL = 256;  // producer TMEM: Q [0, 256), S buffers [256, 512)
-static_assert(OFF_VEC + 1024 + 512 + 2048 + 1024 <= OFF_RING_P, "producer vectors");
+static_assert(OFF_VEC + 1024 + 512 + 2048 + 1024 + 1024 <= OFF_RING_P, "producer vectors");
 
 // Producer -> accumulator P tiles (with their row factors) travel through L2:
 // a producer warp bulk-stores the staged tile into the scratch of the
@@ -93,7 +96,7 @@ static_assert(OFF_RING_A % 1024 == 0 && OFF_RING_P % 1024 == 0, "swizzled tiles 
 struct Bars {
   uint64_t ring_full[kMaxRing];  // (leader) both halves of a slot landed
   uint64_t ring_empty[kMaxRing]; // (both) the pair's MMAs finished reading a slot
-  uint64_t q_ready;              // (producer, own) Q in TMEM
+  uint64_t q_ready;              // (producer, own) an item's Q in TMEM
   uint64_t pair_ready;           // (producer leader) both CTAs' Q in TMEM
   uint64_t s_full[2], s_free[2]; // (producer) S buffers: filled (both) / read (leader: 8 warps + relay)
   uint64_t mx[2][4];             // (producer) both warps of lane quarter q posted their partial row max [parity][q]
@@ -104,18 +107,25 @@ struct Bars {
   uint64_t recv_full[2];         // (accumulator) P tile + alpha landed in slot
   uint64_t o_ready[2];           // (accumulator) rows rescaled for the step (leader: 8 warps + relay)
   uint64_t mma_done[2];          // (accumulator, both) PV of a slot finished
-  uint64_t lx;                   // (producer) both warpgroups posted their row sums
-  uint64_t fin_staged;           // (producer) 1 / l written
-  uint64_t fin_full;             // (accumulator) 1 / l landed
-  uint64_t acc_done, mma_drain;
+  uint64_t lx;                   // (producer) both warpgroups posted an item's row sums
+  uint64_t fin_staged;           // (producer) an item's 1 / l written
+  uint64_t fin_full[2];          // (accumulator) an item's 1 / l landed [item parity]
+  uint64_t acc_done;             // (accumulator, both) an item's PV MMAs finished
+  uint64_t acc_free;             // (accumulator leader) both CTAs read an item's O out
+  uint64_t epi_done;             // (accumulator, own) the epilogue's stores read their staging
+  uint64_t item_full[2];         // (every CTA) the scheduler wrote an item id into the slot
+  uint64_t item_empty[2];        // (rank 0) every reader of the slot read it
+  uint64_t item_req;             // (rank 0) its TMA thread will soon need the next item
+  uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
   int n_sent[2];                 // (producer) steps copied, per warpgroup
-  int fin_sent;
+  int fin_sent;                  // (producer) 1 / l copies issued
   int n_recv;                    // (accumulator) steps whose tile landed
   int n_loaded;                  // (accumulator) steps whose tile loads were issued
   int smid;                      // (accumulator) SM this CTA runs on: the scratch it loads from
   int n_issued;                  // ring loads issued by this CTA
+  int item_id[2];                // item ids, written by rank 0's scheduler
 };
 
 constexpr size_t SMEM = (size_t)DATA_BYTES + 1024 + 1024;
@@ -124,6 +134,8 @@ static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 struct FwdPairParams {
   Geom g;
+  int* work;          // the launch's work counter: the next item id (zero before the launch)
+  int n_items;        // work items
   const uint16_t* q;  // bf16: S = Q K^T reads the caller's q and k as they are
   float* o;
   float* lse;
@@ -195,6 +207,45 @@ __device__ __forceinline__ float half_p(const uint32_t (&sr)[64], float sl2, flo
   return t.x + t.y;
 }
 
+// One work item of a persistent cluster: two adjacent 128-row query tiles of
+// one query head.  Ids run with the kv head (b * Hkv + kv head) slowest, then
+// the tile pair (the longest band first), then the group's query head, so
+// that the clusters working at any moment share one kv head, whose K and V
+// then stay in L2, and the short items come last.
+struct FwdItem {
+  int bkv, bh;      // b * Hkv + kv head; b * Hq + query head
+  int i0, ihi;      // this CTA's query tile (ihi = i0 when it has no rows)
+  bool own_rows;    // false for the second tile of an odd last pair
+  TileSteps ks;     // key tiles meeting the band of the pair's rows (at least one)
+  int N;
+};
+
+__device__ __forceinline__ FwdItem make_fwd_item(const Geom& g, int id, int npairs, uint32_t h) {
+  FwdItem x;
+  const int per_kv = npairs * g.G;
+  x.bkv = id / per_kv;
+  const int rem = id - x.bkv * per_kv;
+  const int y = rem / g.G;
+  const int b = x.bkv / g.Hkv;
+  x.bh = b * g.Hq + (x.bkv - b * g.Hkv) * g.G + (rem - y * g.G);
+  const int tp = npairs - 1 - y;  // the last query tile pair has the longest band
+  const int pr0 = 2 * tp * T, prlast = min(pr0 + 2 * T, g.Lq) - 1;
+  x.i0 = pr0 + (int)h * T;
+  x.own_rows = x.i0 < g.Lq;
+  x.ihi = x.own_rows ? min(x.i0 + T, g.Lq) - 1 : x.i0;
+  x.ks = row_steps(g, pr0, prlast, T);
+  x.N = x.ks.count();
+  return x;
+}
+
+// Readers of each item id in a cluster (the scheduler counts their arrivals
+// before it reuses the id's slot): the producer leader's TMA, MMA, eight
+// elementwise and store warps (11), the producer peer's same plus its relay
+// warp (12), the accumulator leader's TMA, MMA, tile-load and eight
+// elementwise warps (11), the accumulator peer's TMA, tile-load, eight
+// elementwise and relay warps (11).
+constexpr int kItemReaders = 11 + 12 + 11 + 11;
+
 __global__ void __launch_bounds__(kThr, 1)
     fwd512_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmO,  // fp32 o, 32 x 32 boxes
@@ -213,21 +264,7 @@ __global__ void __launch_bounds__(kThr, 1)
   const bool leader = h == 0;
   const uint16_t pmask = (uint16_t)(3u << lead);
   const bool producer = rank < 2;
-  // Grid (x, y, z) = (4 x the group's query heads, query tile pairs, b * Hkv
-  // + kv head).  Blocks launch x fastest and z slowest, so the clusters
-  // running at any moment share one kv head, whose K and V then stay in L2.
-  const int bkv = (int)blockIdx.z;
-  const int b = bkv / g.Hkv;
-  const int bh = b * g.Hq + (bkv - b * g.Hkv) * g.G + (int)(blockIdx.x / R);  // b * Hq + query head
   const int npairs = (p.n_tiles + 1) / 2;
-  const int tp = npairs - 1 - (int)blockIdx.y;  // longest rows first
-  const int pr0 = 2 * tp * T, prlast = min(pr0 + 2 * T, g.Lq) - 1;
-  const int i0 = pr0 + (int)h * T;  // this CTA's query tile
-  const bool own_rows = i0 < g.Lq;  // false for the second tile of an odd last pair
-  const int ihi = own_rows ? min(i0 + T, g.Lq) - 1 : i0;
-  // key steps meeting the band of the pair's rows (at least one)
-  const TileSteps ksteps = row_steps(g, pr0, prlast, T);
-  const int N = ksteps.count();
   const bool two = g.Rc > 0;  // shared-prefix plan: two visible key intervals per row
 
   if (threadIdx.x == 0) {
@@ -250,12 +287,17 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&bars->recv_full[s], 1);
       mbar_init(&bars->o_ready[s], leader ? 9 : 8);
       mbar_init(&bars->mma_done[s], 1);
+      mbar_init(&bars->fin_full[s], 1);
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], kItemReaders);
       bars->n_sent[s] = 0;
     }
     mbar_init(&bars->lx, 256);
     mbar_init(&bars->fin_staged, 128);
-    mbar_init(&bars->fin_full, 1);
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->acc_free, 16);
+    mbar_init(&bars->epi_done, 8);
+    mbar_init(&bars->item_req, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
     bars->fin_sent = 0;
@@ -280,6 +322,30 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
+  // The k-th item of this cluster (k = 0, 1, ...): its id, or -1 once the
+  // work has run out or after a timeout (then ok is cleared).  The id sits in
+  // slot k % 2; each reader tells rank 0's scheduler that it has read it.
+  auto get_item = [&](int k, bool& ok) -> int {
+    if (!mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R)) {
+      ok = false;
+      return -1;
+    }
+    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
+    if (id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
+    return id;
+  };
+  // the same for a whole warp (lane 0 reports the read)
+  auto get_item_warp = [&](int k, bool& ok) -> int {
+    if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R))) {
+      ok = false;
+      return -1;
+    }
+    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
+    __syncwarp();
+    if (lane == 0 && id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
+    return id;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA (both CTAs of a pair)
     if (elect_one()) {
@@ -288,25 +354,32 @@ __global__ void __launch_bounds__(kThr, 1)
       int issued = 0;
       bool ok = true;
       const int nr = producer ? NR_P : NR_A;
-      for (int n = 0; ok && n < N; ++n) {
-        const int j0 = ksteps.tile(n) * T;
-        for (int c = 0; c < 2; ++c, ++issued) {
-          const int s = issued % nr;
-          if (issued >= nr && !mbar_wait_cl(&bars->ring_empty[s], ((issued / nr) & 1) ^ 1, abort_flag, R)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = mapa(smem_u32(&bars->ring_full[s]), lead);
-          if (producer) {
-            // this CTA's 64 keys, head-dim columns [256 c, 256 c + 256)
-            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_P);
-            tma_load_4d_pair(base + OFF_RING_P + s * SLOT_P, &tmK, fb, 0, j0 + HT * (int)h, 4 * c, bkv);
-          } else {
-            // the 128 keys, this CTA's 128 columns of chunk c (head-dim columns [256 c + 128 h, +128))
-            if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_A);
-            tma_load_4d_pair(base + OFF_RING_A + s * SLOT_A, &tmV, fb, 0, j0, 4 * c + 2 * (int)h, bkv);
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const FwdItem x = make_fwd_item(g, id, npairs, h);
+        for (int n = 0; ok && n < x.N; ++n) {
+          if (rank == 0 && n == x.N - 1) mbar_arrive(&bars->item_req);  // the next item is soon needed
+          const int j0 = x.ks.tile(n) * T;
+          for (int c = 0; c < 2; ++c, ++issued) {
+            const int s = issued % nr;
+            if (issued >= nr && !mbar_wait_cl(&bars->ring_empty[s], ((issued / nr) & 1) ^ 1, abort_flag, R)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = mapa(smem_u32(&bars->ring_full[s]), lead);
+            if (producer) {
+              // this CTA's 64 keys, head-dim columns [256 c, 256 c + 256)
+              if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_P);
+              tma_load_4d_pair(base + OFF_RING_P + s * SLOT_P, &tmK, fb, 0, j0 + HT * (int)h, 4 * c, x.bkv);
+            } else {
+              // the 128 keys, this CTA's 128 columns of chunk c (head-dim columns [256 c + 128 h, +128))
+              if (leader) mbar_arrive_expect_tx(&bars->ring_full[s], 2 * SLOT_A);
+              tma_load_4d_pair(base + OFF_RING_A + s * SLOT_A, &tmV, fb, 0, j0, 4 * c + 2 * (int)h, x.bkv);
+            }
           }
         }
+        bars->n_issued = issued;
       }
       bars->n_issued = issued;
     }
@@ -315,22 +388,28 @@ __global__ void __launch_bounds__(kThr, 1)
     if (elect_one()) {
       bool ok = true;
       if (producer) {
-        // both CTAs: Q is in Tensor Memory -> tell the leader
-        ok = mbar_wait_cl(&bars->q_ready, 0, abort_flag, R);
-        if (ok) {
-          tc_fence_after();
-          tc_fence_before();
-          if (leader) mbar_arrive(&bars->pair_ready);
-          else mbar_arrive_remote(mapa(smem_u32(&bars->pair_ready), lead));
-        }
-        if (leader && ok) {
-          const uint32_t idS = idesc_f16(2 * T, T, 1, 1, 0, 0);  // Q (TMEM) x K half (K-major), both bf16
-          const uint64_t rd = smem_desc_sw128(sbase + OFF_RING_P, 16, 1024);
-          const uint32_t x_tm = tmem + X_COL;
-          ok = mbar_wait_cl(&bars->pair_ready, 0, abort_flag, R);
-          for (int n = 0; ok && n < N; ++n) {
-            const int bb = n & 1;
-            if (n >= 2 && !mbar_wait_cl(&bars->s_free[bb], ((n >> 1) - 1) & 1, abort_flag, R)) {
+        const uint32_t idS = idesc_f16(2 * T, T, 1, 1, 0, 0);  // Q (TMEM) x K half (K-major), both bf16
+        const uint64_t rd = smem_desc_sw128(sbase + OFF_RING_P, 16, 1024);
+        const uint32_t x_tm = tmem + X_COL;
+        int kp = 0, nc = 0;  // items, steps so far
+        for (int k = 0; ok; ++k) {
+          const int id = get_item(k, ok);
+          if (id < 0) break;
+          const FwdItem x = make_fwd_item(g, id, npairs, h);
+          // both CTAs: the item's Q is in Tensor Memory -> tell the leader
+          ok = mbar_wait_cl(&bars->q_ready, kp & 1, abort_flag, R);
+          if (ok) {
+            tc_fence_after();
+            tc_fence_before();
+            if (leader) mbar_arrive(&bars->pair_ready);
+            else mbar_arrive_remote(mapa(smem_u32(&bars->pair_ready), lead));
+          }
+          if (leader && ok) ok = mbar_wait_cl(&bars->pair_ready, kp & 1, abort_flag, R);
+          ++kp;
+          if (!leader) continue;
+          for (int n = 0; ok && n < x.N; ++n, ++nc) {
+            const int bb = nc & 1;
+            if (nc >= 2 && !mbar_wait_cl(&bars->s_free[bb], ((nc >> 1) - 1) & 1, abort_flag, R)) {
               ok = false;
               break;
             }
@@ -339,8 +418,8 @@ __global__ void __launch_bounds__(kThr, 1)
             // unrolled over the step: constant operand offsets from a per-slot
             // base keep the single issuing thread ahead of the tensor pipe
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int li = 2 * n + k, s = li % NR_P;
+            for (int kk = 0; kk < 2; ++kk) {
+              const int li = 2 * nc + kk, s = li % NR_P;
               if (!mbar_wait_cl(&bars->ring_full[s], (li / NR_P) & 1, abort_flag, R)) {
                 ok = false;
                 break;
@@ -351,9 +430,9 @@ __global__ void __launch_bounds__(kThr, 1)
               for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                  // head-dim columns 256 k + 64 cc + 16 ks: Q columns 128 k + 32 cc + 8 ks in TMEM
-                  mma_pair_ts(s_tm, x_tm + 128 * k + 32 * cc + 8 * ks, desc_add(kd, cc * HT * 128 + ks * 32), idS,
-                              (k | cc | ks) ? 1u : 0u);
+                  // head-dim columns 256 kk + 64 cc + 16 ks: Q columns 128 kk + 32 cc + 8 ks in TMEM
+                  mma_pair_ts(s_tm, x_tm + 128 * kk + 32 * cc + 8 * ks, desc_add(kd, cc * HT * 128 + ks * 32), idS,
+                              (kk | cc | ks) ? 1u : 0u);
                 }
               }
               mma_commit_pair(&bars->ring_empty[s], pmask);
@@ -364,231 +443,330 @@ __global__ void __launch_bounds__(kThr, 1)
         }
       } else if (leader) {
         const uint32_t idPV = idesc_f16(2 * T, 256, 0, 0, 0, 1);  // P (K-major) x V half chunks (MN-major)
-        int used = 0;
-        for (int n = 0; ok && n < N; ++n) {
-          const int bb = n & 1;
-          // both CTAs rescaled their rows, which they do once their P tile landed
-          if (!mbar_wait_cl(&bars->o_ready[bb], (n >> 1) & 1, abort_flag, R)) {
+        int used = 0, nc = 0, ka = 0;  // ring loads consumed, steps, items so far
+        for (int k = 0; ok; ++k) {
+          const int id = get_item(k, ok);
+          if (id < 0) break;
+          const FwdItem x = make_fwd_item(g, id, npairs, h);
+          // both CTAs' epilogues have read the previous item's O out of Tensor Memory
+          if (ka > 0 && !mbar_wait_cl(&bars->acc_free, (ka - 1) & 1, abort_flag, R)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + bb * TILE_BYTES, 16, 1024);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int s = used % NR_A;
-            if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_A) & 1, abort_flag, R)) {
+          for (int n = 0; ok && n < x.N; ++n, ++nc) {
+            const int bb = nc & 1;
+            // both CTAs rescaled their rows, which they do once their P tile landed
+            if (!mbar_wait_cl(&bars->o_ready[bb], (nc >> 1) & 1, abort_flag, R)) {
               ok = false;
               break;
             }
-            ++used;
             tc_fence_after();
-            const uint64_t vd = smem_desc_sw128(sbase + OFF_RING_A + s * SLOT_A, T * 128, 1024);
+            const uint64_t ad = smem_desc_sw128(sbase + OFF_RECV + bb * TILE_BYTES, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < T / 16; ++ks)
-              mma_pair_ss(tmem + 256 * c, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32), desc_add(vd, ks * 2048),
-                          idPV, (n | ks) ? 1u : 0u);
-            mma_commit_pair(&bars->ring_empty[s], pmask);
+            for (int c = 0; c < 2; ++c) {
+              const int s = used % NR_A;
+              if (!mbar_wait_cl(&bars->ring_full[s], (used / NR_A) & 1, abort_flag, R)) {
+                ok = false;
+                break;
+              }
+              ++used;
+              tc_fence_after();
+              const uint64_t vd = smem_desc_sw128(sbase + OFF_RING_A + s * SLOT_A, T * 128, 1024);
+#pragma unroll
+              for (int ks = 0; ks < T / 16; ++ks)
+                mma_pair_ss(tmem + 256 * c, desc_add(ad, (ks >> 2) * T * 128 + (ks & 3) * 32),
+                            desc_add(vd, ks * 2048), idPV, (n | ks) ? 1u : 0u);
+              mma_commit_pair(&bars->ring_empty[s], pmask);
+            }
+            if (!ok) break;
+            mma_commit_pair(&bars->mma_done[bb], pmask);
           }
           if (!ok) break;
-          mma_commit_pair(&bars->mma_done[bb], pmask);
+          mma_commit_pair(&bars->acc_done, pmask);
+          ++ka;
         }
-        if (ok) mma_commit_pair(&bars->acc_done, pmask);
       }
       // every MMA the leader issued has finished before either CTA releases Tensor Memory
       if (leader) mma_commit_pair(&bars->mma_drain, pmask);
       mbar_wait_drain(&bars->mma_drain, 0);
     }
   } else if (warp == kSigWarp) {
-    if (!producer && elect_one()) {
-      // ------------------------------------------------------------ tile loads (accumulators)
-      // once the MMAs of step n - 2 are done with slot n % 2 and the producer's
-      // tile for step n is in the scratch, load it (P tile, then its factors)
-      mbar_arrive_expect_tx(&bars->fin_full, 512);
+    if (rank == 0 && elect_one()) {
+      // ---------------------------------------------------------- scheduler (rank 0)
+      // Items are handed out one at a time from the launch's counter, so a
+      // cluster that draws short items takes more of them.  Each id goes
+      // into slot k % 2 of every CTA; the slot is reused once all readers
+      // have read it.  An id is drawn only when rank 0's TMA thread starts
+      // the last step of its current item: clusters take items in about the
+      // order they finish them, as a non-persistent grid's clusters would be
+      // dispatched, and the clusters of one kv head read its keys at about
+      // the same place, sharing them in L2.
+      for (int k = 0;; ++k) {
+        const int s = k & 1;
+        if (k >= 1 && !mbar_wait_cl(&bars->item_req, (k - 1) & 1, abort_flag, R)) break;
+        if (k >= 2 && !mbar_wait_cl(&bars->item_empty[s], ((k >> 1) - 1) & 1, abort_flag, R)) break;
+        int id = atomicAdd(p.work, 1);
+        if (id >= p.n_items) id = -1;
+        const uint32_t slot_addr = smem_u32(&bars->item_id[s]);
+        for (uint32_t r = 0; r < R; ++r) st_cluster_u32(mapa(slot_addr, r), (uint32_t)id);
+        fence_acq_rel_cluster();  // the ids are visible before any CTA sees the arrive
+        for (uint32_t r = 0; r < R; ++r) mbar_arrive_remote(mapa(smem_u32(&bars->item_full[s]), r));
+        if (id < 0) break;
+      }
+    } else if (!producer && elect_one()) {
+      // ---------------------------------------------------------- tile loads (accumulators)
+      // once the MMAs of the step two steps back are done with the slot and
+      // the producer's tile is in the scratch, load it (P tile, then its
+      // factors); per item, arm the landing of its 1 / l
       const unsigned char* scr = g_fwd_tile_scratch + (size_t)(bars->smid < 0 ? 0 : bars->smid) * 2 * SCR_SLOT;
       bool ok = bars->smid >= 0;
       if (!ok) cluster_abort(abort_flag, R);
-      for (int n = 0; ok && n < N; ++n) {
-        const int bb = n & 1;
-        if (n >= 2 && !mbar_wait_cl(&bars->mma_done[bb], ((n >> 1) - 1) & 1, abort_flag, R)) break;
-        mbar_arrive_expect_tx(&bars->recv_full[bb], TILE_BYTES + 512);
-        if (!mbar_wait_cl(&bars->tile_ready[bb], (n >> 1) & 1, abort_flag, R)) break;
-        fence_proxy_async_global();
-        bulk_load_g2s(sbase + OFF_RECV + bb * TILE_BYTES, scr + bb * SCR_SLOT, TILE_BYTES, &bars->recv_full[bb]);
-        bulk_load_g2s(sbase + OFF_RVEC + bb * 512, scr + bb * SCR_SLOT + TILE_BYTES, 512, &bars->recv_full[bb]);
-        bars->n_loaded = n + 1;
+      int nc = 0, ka = 0;  // steps, items so far
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const FwdItem x = make_fwd_item(g, id, npairs, h);
+        mbar_arrive_expect_tx(&bars->fin_full[ka & 1], 512);
+        // the receive slots held the previous item's epilogue staging
+        if (ka > 0 && !mbar_wait_cl(&bars->epi_done, (ka - 1) & 1, abort_flag, R)) {
+          ok = false;
+          break;
+        }
+        for (int n = 0; ok && n < x.N; ++n, ++nc) {
+          const int bb = nc & 1;
+          if (nc >= 2 && !mbar_wait_cl(&bars->mma_done[bb], ((nc >> 1) - 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->recv_full[bb], TILE_BYTES + 512);
+          if (!mbar_wait_cl(&bars->tile_ready[bb], (nc >> 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          bulk_load_g2s(sbase + OFF_RECV + bb * TILE_BYTES, scr + bb * SCR_SLOT, TILE_BYTES, &bars->recv_full[bb]);
+          bulk_load_g2s(sbase + OFF_RVEC + bb * 512, scr + bb * SCR_SLOT + TILE_BYTES, 512, &bars->recv_full[bb]);
+          bars->n_loaded = nc + 1;
+        }
+        ++ka;
       }
     } else if (producer && !leader && elect_one()) {
-      // ------------------------------------------------------------ relay (producer peer)
-      for (int n = 0; n < N; ++n) {
-        if (!mbar_wait_cl(&bars->s_free[n & 1], (n >> 1) & 1, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->s_free[n & 1]), lead));
+      // ---------------------------------------------------------- relay (producer peer)
+      bool ok = true;
+      int nc = 0;
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const FwdItem x = make_fwd_item(g, id, npairs, h);
+        for (int n = 0; n < x.N; ++n, ++nc) {
+          if (!mbar_wait_cl(&bars->s_free[nc & 1], (nc >> 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(mapa(smem_u32(&bars->s_free[nc & 1]), lead));
+        }
       }
     }
   } else if (warp == kRelayWarp) {
     if (producer && elect_one()) {
-      // ------------------------------------------------------------ tile stores (producers)
+      // ---------------------------------------------------------- tile stores (producers)
       int sm_dst;
       asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sm_dst) : "r"(mapa(smem_u32(&bars->smid), 2u + h))
                    : "memory");
       bool ok = sm_dst >= 0;
       if (!ok) cluster_abort(abort_flag, R);
       unsigned char* scr = g_fwd_tile_scratch + (size_t)(sm_dst < 0 ? 0 : sm_dst) * 2 * SCR_SLOT;
-      for (int n = 0; ok && n < N; ++n) {
-        const int bb = n & 1;
-        if (n >= 2 && !mbar_wait_cl(&bars->scratch_free[bb], ((n >> 1) - 1) & 1, abort_flag, R)) break;
-        fence_proxy_async_global();
-        unsigned char* gdst = scr + bb * SCR_SLOT;
-        for (int w = 0; w < 2; ++w) {
-          // one barrier per staging tile: the warpgroups can be a step ahead of this warp
-          if (!mbar_wait_cl(&bars->staged[bb][w], (n >> 1) & 1, abort_flag, R)) {
+      int nc = 0;
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const FwdItem x = make_fwd_item(g, id, npairs, h);
+        for (int n = 0; ok && n < x.N; ++n, ++nc) {
+          const int bb = nc & 1;
+          if (nc >= 2 && !mbar_wait_cl(&bars->scratch_free[bb], ((nc >> 1) - 1) & 1, abort_flag, R)) {
             ok = false;
             break;
           }
-          bulk_store_s2g(gdst + w * HALF_BYTES, sbase + OFF_STG + bb * TILE_BYTES + w * HALF_BYTES, HALF_BYTES);
+          fence_proxy_async_global();
+          unsigned char* gdst = scr + bb * SCR_SLOT;
+          for (int w = 0; w < 2; ++w) {
+            // one barrier per staging tile: the warpgroups can be a step ahead of this warp
+            if (!mbar_wait_cl(&bars->staged[bb][w], (nc >> 1) & 1, abort_flag, R)) {
+              ok = false;
+              break;
+            }
+            bulk_store_s2g(gdst + w * HALF_BYTES, sbase + OFF_STG + bb * TILE_BYTES + w * HALF_BYTES, HALF_BYTES);
+          }
+          if (!ok) break;
+          bulk_store_s2g(gdst + TILE_BYTES, sbase + OFF_VEC + bb * 512, 512);  // the step's row factors
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(&bars->stg_free[bb][0]);
+          mbar_arrive(&bars->stg_free[bb][1]);
+          bulk_wait_all();
+          fence_proxy_async_global();
+          mbar_arrive_remote(mapa(smem_u32(&bars->tile_ready[bb]), 2u + h));
         }
-        if (!ok) break;
-        bulk_store_s2g(gdst + TILE_BYTES, sbase + OFF_VEC + bb * 512, 512);  // the step's row factors
-        bulk_commit_group();
-        bulk_wait_read_all();
-        mbar_arrive(&bars->stg_free[bb][0]);
-        mbar_arrive(&bars->stg_free[bb][1]);
-        bulk_wait_all();
-        fence_proxy_async_global();
-        mbar_arrive_remote(mapa(smem_u32(&bars->tile_ready[bb]), 2u + h));
       }
       bulk_wait_all();  // no store still reads this CTA's shared memory
     }
-    // ------------------------------------------------------------ relay (accumulator peer)
     if (!producer && !leader && elect_one()) {
-      for (int n = 0; n < N; ++n) {
-        if (!mbar_wait_cl(&bars->o_ready[n & 1], (n >> 1) & 1, abort_flag, R)) break;
-        mbar_arrive_remote(mapa(smem_u32(&bars->o_ready[n & 1]), lead));
+      // ---------------------------------------------------------- relay (accumulator peer)
+      bool ok = true;
+      int nc = 0;
+      for (int k = 0; ok; ++k) {
+        const int id = get_item(k, ok);
+        if (id < 0) break;
+        const FwdItem x = make_fwd_item(g, id, npairs, h);
+        for (int n = 0; n < x.N; ++n, ++nc) {
+          if (!mbar_wait_cl(&bars->o_ready[nc & 1], (nc >> 1) & 1, abort_flag, R)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(mapa(smem_u32(&bars->o_ready[nc & 1]), lead));
+        }
       }
     }
   } else if (producer) {
     // ------------------------------------------------------------ softmax (producers, both CTAs)
     const int wg = (warp - 2) >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;
-    const int i = i0 + r;
-    const bool row_ok = i < g.Lq;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int cb0 = 64 * wg;
     const float sl2 = g.scale * kLog2e;
     float* alph = reinterpret_cast<float*>(base + OFF_VEC);  // [2 tile][128]
-    float* finl = alph + 256;                                 // [128]
-    float* xm = finl + 128;                                   // [2 parity][2 wg][128]
+    float* xm = alph + 384;                                   // [2 parity][2 wg][128]
     float* xl = xm + 512;                                     // [2 wg][128]
+    float* finl = xl + 256;                                   // [2 item parity][128]
     const uint32_t acc = 2u + h;                              // accumulator CTA of this half
-    {
-      // Q row i into Tensor Memory: bf16 pairs, one 32-bit column each; warpgroup
-      // wg fills columns [128 wg, 128 wg + 128) (head-dim elements [256 wg, 256 wg + 256))
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * g.Lq + (row_ok ? i : 0)) * DH) + wg * 32;
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        uint32_t v[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * q] = w4.x;
-          v[4 * q + 1] = w4.y;
-          v[4 * q + 2] = w4.z;
-          v[4 * q + 3] = w4.w;
-        }
-        tmem_st32(tmem + lane_off + X_COL + wg * 128 + j * 32, v);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->q_ready);
-    }
     const uint32_t stg0 = sbase + OFF_STG + wg * HALF_BYTES;
     const bool issuer = (warp & 3) == 2;  // warp 2 / 6 copies its warpgroup's half
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int n = 0; n < N; ++n) {
-      const int bb = n & 1;
-      const int j0 = ksteps.tile(n) * T;
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full[bb], (n >> 1) & 1, abort_flag, R))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tmem + lane_off + S_COL + bb * T + cb0, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      tmem_ld32(tmem + lane_off + S_COL + bb * T + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[bb]);  // the peer's relay tells the leader
-      const bool full = own_rows && rows_tile_full(g, i0, ihi, j0, j0 + T - 1);
-      // visible key columns of row i in this tile, relative to this warpgroup's half
-      bool both;
-      const int4 vv = vis_in_tile(row_vis(g, i, j0 + cb0), 64, &both);
-      const bool two_here = two && __any_sync(0xffffffffu, both);
-      float pmax;
-      if (sl2 > 0.f)
-        pmax = sl2 * (full ? half_max_raw<true>(sr, vv)
-                           : (two_here ? half_max_raw<false, true>(sr, vv) : half_max_raw<false>(sr, vv)));
-      else
-        pmax = full ? half_max<true>(sr, sl2, vv)
-                    : (two_here ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
-      // the two warps of this lane quarter exchange their halves' maxima
-      xm[(bb * 2 + wg) * 128 + r] = pmax;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->mx[bb][q4]);
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->mx[bb][q4], (n >> 1) & 1, abort_flag, R))) {
-        ok = false;
-        break;
-      }
-      const float tmax = fmaxf(pmax, xm[(bb * 2 + (wg ^ 1)) * 128 + r]);
-      float alpha = 1.f;
-      if (tmax > m_run + kRescaleLog2) {
-        if (m_run != -INFINITY) alpha = fast_exp2(m_run - tmax);
-        m_run = tmax;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pk[32];
-      const float tsum = full ? half_p<true>(sr, sl2, m_use, vv, pk)
-                              : (two_here ? half_p<false, true>(sr, sl2, m_use, vv, pk)
-                                          : half_p<false>(sr, sl2, m_use, vv, pk));
-      l_run = l_run * alpha + tsum;
-      // the store of this staging half two steps ago (and of that alpha) must have read it
-      if (n >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[bb][wg], ((n >> 1) - 1) & 1, abort_flag, R))) {
-        ok = false;
-        break;
-      }
-      const uint32_t stg = stg0 + bb * TILE_BYTES;
+    int nc = 0, kp = 0;  // steps, items so far
+    for (int k = 0; ok; ++k) {
+      const int id = get_item_warp(k, ok);
+      if (id < 0) break;
+      const FwdItem x = make_fwd_item(g, id, npairs, h);
+      const int i = x.i0 + r;
+      const bool row_ok = i < g.Lq;
+      {
+        // Q row i into Tensor Memory: bf16 pairs, one 32-bit column each;
+        // warpgroup wg fills columns [128 wg, 128 wg + 128) (head-dim elements
+        // [256 wg, 256 wg + 256)).  The previous item's S MMAs, the only
+        // readers, finished: their s_full was seen before its last S was read.
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.q + ((size_t)x.bh * g.Lq + (row_ok ? i : 0)) * DH) + wg * 32;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_smem_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      if (wg == 0) alph[bb * 128 + r] = alpha;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->staged[bb][wg]);  // the store warp takes the tile from here
-      bars->n_sent[wg] = n + 1;
-    }
-    // row sum = the two warpgroups' partial sums (same running max); lse; send 1 / l
-    xl[wg * 128 + r] = l_run;
-    mbar_arrive(&bars->lx);
-    if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->lx, 0, abort_flag, R))) {
+          for (int q = 0; q < 8; ++q) {
+            const uint4 w4 = row_ok ? __ldg(src + j * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+            v[4 * q] = w4.x;
+            v[4 * q + 1] = w4.y;
+            v[4 * q + 2] = w4.z;
+            v[4 * q + 3] = w4.w;
+          }
+          tmem_st32(tmem + lane_off + X_COL + wg * 128 + j * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->q_ready);
+      }
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int n = 0; n < x.N; ++n, ++nc) {
+        const int bb = nc & 1;
+        const int j0 = x.ks.tile(n) * T;
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->s_full[bb], (nc >> 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_off + S_COL + bb * T + cb0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tmem + lane_off + S_COL + bb * T + cb0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[bb]);  // the peer's relay tells the leader
+        const bool full = x.own_rows && rows_tile_full(g, x.i0, x.ihi, j0, j0 + T - 1);
+        // visible key columns of row i in this tile, relative to this warpgroup's half
+        bool both;
+        const int4 vv = vis_in_tile(row_vis(g, i, j0 + cb0), 64, &both);
+        const bool two_here = two && __any_sync(0xffffffffu, both);
+        float pmax;
+        if (sl2 > 0.f)
+          pmax = sl2 * (full ? half_max_raw<true>(sr, vv)
+                             : (two_here ? half_max_raw<false, true>(sr, vv) : half_max_raw<false>(sr, vv)));
+        else
+          pmax = full ? half_max<true>(sr, sl2, vv)
+                      : (two_here ? half_max<false, true>(sr, sl2, vv) : half_max<false>(sr, sl2, vv));
+        // the two warps of this lane quarter exchange their halves' maxima
+        xm[(bb * 2 + wg) * 128 + r] = pmax;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->mx[bb][q4]);
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->mx[bb][q4], (nc >> 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        const float tmax = fmaxf(pmax, xm[(bb * 2 + (wg ^ 1)) * 128 + r]);
+        float alpha = 1.f;
+        if (tmax > m_run + kRescaleLog2) {
+          if (m_run != -INFINITY) alpha = fast_exp2(m_run - tmax);
+          m_run = tmax;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        uint32_t pk[32];
+        const float tsum = full ? half_p<true>(sr, sl2, m_use, vv, pk)
+                                : (two_here ? half_p<false, true>(sr, sl2, m_use, vv, pk)
+                                            : half_p<false>(sr, sl2, m_use, vv, pk));
+        l_run = l_run * alpha + tsum;
+        // the store of this staging half two steps ago (and of that alpha) must have read it
+        if (nc >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait_cl(&bars->stg_free[bb][wg], ((nc >> 1) - 1) & 1, abort_flag, R))) {
+          ok = false;
+          break;
+        }
+        const uint32_t stg = stg0 + bb * TILE_BYTES;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_smem_v4(stg + r * 128 + ((u ^ (r & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        if (wg == 0) alph[bb * 128 + r] = alpha;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->staged[bb][wg]);  // the store warp takes the tile from here
+        bars->n_sent[wg] = nc + 1;
+      }
+      if (!ok) break;
+      // row sum = the two warpgroups' partial sums (same running max); lse; send 1 / l
+      xl[wg * 128 + r] = l_run;
+      mbar_arrive(&bars->lx);
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->lx, kp & 1, abort_flag, R))) {
+        ok = false;
+        break;
+      }
       const float l_tot = xl[r] + xl[128 + r];
       if (wg == 0) {
         // 1 / l, or with attention sinks the factor that folds the head's
-        // sink logit into the row's normaliser; the accumulator scales O by it
+        // sink logit into the row's normaliser; the accumulator scales O by
+        // it.  Two buffers by item parity: the copy of the previous item's
+        // factors may still be reading the other one.
         float lse_row = (m_run + log2f(l_tot)) * kLn2;
         float fin = 1.f / l_tot;
-        if (g.sinks) fin = sink_finish(g.sinks[bh % g.Hq], m_run, l_tot, &lse_row);
-        if (row_ok) p.lse[(size_t)bh * g.Lq + i] = lse_row;
-        finl[r] = fin;
+        if (g.sinks) fin = sink_finish(g.sinks[x.bh % g.Hq], m_run, l_tot, &lse_row);
+        if (row_ok) p.lse[(size_t)x.bh * g.Lq + i] = lse_row;
+        float* fl = finl + (kp & 1) * 128;
+        fl[r] = fin;
         fence_proxy_async_smem();
         mbar_arrive(&bars->fin_staged);
-        if (issuer && __all_sync(0xffffffffu, mbar_wait_cl(&bars->fin_staged, 0, abort_flag, R)) && lane == 0) {
-          bulk_copy_to_cta(mapa(sbase + OFF_RVEC + 1024, acc), smem_u32(finl), 512,
-                           mapa(smem_u32(&bars->fin_full), acc));
-          bars->fin_sent = 1;
+        if (issuer && __all_sync(0xffffffffu, mbar_wait_cl(&bars->fin_staged, kp & 1, abort_flag, R)) && lane == 0) {
+          bulk_copy_to_cta(mapa(sbase + OFF_RVEC + 1024 + (uint32_t)(kp & 1) * 512u, acc), smem_u32(fl), 512,
+                           mapa(smem_u32(&bars->fin_full[kp & 1]), acc));
+          bars->fin_sent = kp + 1;
         }
       }
+      ++kp;
     }
     // (unwinding: the store warp waits for its own stores)
   } else {
@@ -597,52 +775,74 @@ __global__ void __launch_bounds__(kThr, 1)
     const int r = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const float* ralph = reinterpret_cast<const float*>(base + OFF_RVEC);  // [2][128]
-    const float* rinv = ralph + 256;                                       // [128]
+    const float* rinv = ralph + 256;                                       // [2 item parity][128]
     bool ok = true;
-    for (int n = 0; n < N; ++n) {
-      const int bb = n & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->recv_full[bb], (n >> 1) & 1, abort_flag, R))) {
-        ok = false;
-        break;
-      }
-      if (threadIdx.x == 64) {
-        bars->n_recv = n + 1;
-        // the producer may store its next tile into this scratch slot
-        mbar_arrive_remote(mapa(smem_u32(&bars->scratch_free[bb]), h));
-      }
-      const float a = ralph[bb * 128 + r];
-      if (__any_sync(0xffffffffu, a != 1.f)) {
-        // O must hold PV of every earlier step before it is rescaled
-        if (n >= 1 &&
-            !__all_sync(0xffffffffu, mbar_wait_cl(&bars->mma_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, R))) {
+    int nc = 0, ka = 0;  // steps, items so far
+    for (int k = 0; ok; ++k) {
+      const int id = get_item_warp(k, ok);
+      if (id < 0) break;
+      const FwdItem x = make_fwd_item(g, id, npairs, h);
+      for (int n = 0; n < x.N; ++n, ++nc) {
+        const int bb = nc & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->recv_full[bb], (nc >> 1) & 1, abort_flag, R))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {  // this warpgroup's 256 columns
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + 256 * wg + 32 * c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
-          tmem_st32(tmem + lane_off + 256 * wg + 32 * c, v);
+        if (threadIdx.x == 64) {
+          bars->n_recv = nc + 1;
+          // the producer may store its next tile into this scratch slot
+          mbar_arrive_remote(mapa(smem_u32(&bars->scratch_free[bb]), h));
         }
-        tmem_wait_st();
+        const float a = ralph[bb * 128 + r];
+        if (__any_sync(0xffffffffu, a != 1.f)) {
+          // O must hold PV of every earlier step of the item before it is
+          // rescaled (the first step's factor is always 1)
+          if (n >= 1 && !__all_sync(0xffffffffu, mbar_wait_cl(&bars->mma_done[(nc - 1) & 1], ((nc - 1) >> 1) & 1,
+                                                               abort_flag, R))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {  // this warpgroup's 256 columns
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + 256 * wg + 32 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+            tmem_st32(tmem + lane_off + 256 * wg + 32 * c, v);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_ready[bb]);  // the peer's relay tells the leader
       }
+      if (!ok) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, ka & 1, abort_flag, R) &&
+                                       mbar_wait_cl(&bars->fin_full[ka & 1], (ka >> 1) & 1, abort_flag, R))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv = rinv[(ka & 1) * 128 + r];
+      // the receive slots have been consumed by the finished MMAs, and the
+      // tile loads wait for epi_done: each of warps 2-9 stages its O blocks
+      // in two 4 KB buffers there (the V ring may already hold the next
+      // item's loads)
+      tmem_rows_store_tma<2, false>(&tmO, tmem + lane_off + 256 * wg, 256 * wg, 256, inv,
+                                    sbase + OFF_RECV + (uint32_t)(warp - 2) * 8192u, x.i0 + 32 * q4, x.bh, lane);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->o_ready[bb]);  // the peer's relay tells the leader
+      if (lane == 0) {
+        mbar_arrive(&bars->epi_done);  // the staging may be overwritten
+        // O may be overwritten
+        if (leader) mbar_arrive(&bars->acc_free);
+        else mbar_arrive_remote(mapa(smem_u32(&bars->acc_free), lead));
+      }
+      ++ka;
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait_cl(&bars->acc_done, 0, abort_flag, R) &&
-                                         mbar_wait_cl(&bars->fin_full, 0, abort_flag, R))) {
-      tc_fence_after();
-      const float inv = rinv[r];
-      // every V ring load has been consumed by the finished MMAs: each of
-      // warps 2-9 stages its O blocks in 16 KB of the ring
-      tmem_rows_store_tma(&tmO, tmem + lane_off + 256 * wg, 256 * wg, 256, inv,
-                          sbase + OFF_RING_A + (uint32_t)(warp - 2) * 16384u, i0 + 32 * q4, bh, lane);
-    }
+    if (lane == 0) bulk_wait_all();  // the epilogue stores have written
   }
 
   __syncwarp();
@@ -651,12 +851,13 @@ __global__ void __launch_bounds__(kThr, 1)
   cluster_sync();  // no CTA issues a load, a copy or a remote arrival past this point
   if (threadIdx.x == 0 && *abort_flag) {
     // unwinding only.  Accumulators: tiles the producer of this half sent
-    // that never landed must land before this CTA's shared memory is released.
+    // that never landed, and its last 1 / l, must land before this CTA's
+    // shared memory is released.
     if (!producer) {
       int fsent;
       asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(fsent) : "r"(mapa(smem_u32(&bars->fin_sent), h)) : "memory");
       for (int m = bars->n_recv; m < bars->n_loaded; ++m) mbar_wait_drain(&bars->recv_full[m & 1], (m >> 1) & 1);
-      if (fsent) mbar_wait_drain(&bars->fin_full, 0);
+      if (fsent > 0) mbar_wait_drain(&bars->fin_full[(fsent - 1) & 1], ((fsent - 1) >> 1) & 1);
     }
     // Leader: the ring loads of both CTAs complete on its barriers; let the
     // last load of each slot (of either CTA) land.
@@ -681,6 +882,22 @@ __global__ void __launch_bounds__(kThr, 1)
   }
 }
 
+// Clusters that fit on the current device at once (cached per device; 0 on
+// an error).
+int max_clusters(const cudaLaunchConfig_t& cfg) {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fwd512_kernel, &cfg) != cudaSuccess) return 0;
+  if (dev < kMaxDevices && n > 0) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 }  // namespace
 
 int scratch_layout_fwd512() {
@@ -694,7 +911,8 @@ int scratch_layout_fwd512() {
 }
 
 cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k, const uint16_t* v16, float* o,
-                             float* lse, int* status, cudaStream_t s) {
+                             float* lse, int* work, int* status, cudaStream_t s) {
+  if (!work) return cudaErrorInvalidValue;
   CUtensorMap tk, tv, to;
   cudaError_t e;
   // K: 64 keys x four 64-column chunks per instruction (32 KB, one CTA's half
@@ -711,9 +929,11 @@ cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k
   pm.o = o;
   pm.lse = lse;
   pm.n_tiles = (g.Lq + T - 1) / T;
+  pm.work = work;
+  pm.n_items = g.B * g.Hkv * ((pm.n_tiles + 1) / 2) * g.G;
   pm.status = status;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(R * (unsigned)g.G, (unsigned)((pm.n_tiles + 1) / 2), (unsigned)(g.B * g.Hkv));
+  cfg.gridDim = dim3(R, 1, 1);
   cfg.blockDim = dim3(kThr, 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
@@ -724,6 +944,10 @@ cudaError_t launch_fwd_tc512(const Geom& g, const uint16_t* q, const uint16_t* k
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // persistent clusters: as many as fit on the GPU at once, at most one per item
+  const int fit = max_clusters(cfg);
+  if (fit <= 0) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(R * (unsigned)min(fit, pm.n_items), 1, 1);
   return cudaLaunchKernelEx(&cfg, fwd512_kernel, tk, tv, to, pm);
 }
 
