@@ -46,6 +46,7 @@
 #include <atomic>
 
 #include "swa_internal.h"
+#include "cluster_items.cuh"
 #include "tc_ptx.cuh"
 
 namespace swa {
@@ -134,9 +135,6 @@ struct Bars {
   uint64_t acc_done;                 // (accumulator, both) an item's MMAs finished
   uint64_t acc_free;                 // (accumulator leader) both CTAs read an item's accumulator out
   uint64_t epi_done;                 // (accumulator, own) the epilogue's stores read their staging
-  uint64_t item_full[2];             // (every CTA) the scheduler wrote an item id into the slot
-  uint64_t item_empty[2];            // (rank 0) every reader of the slot read it
-  uint64_t item_req;                 // (rank 0) its TMA thread will soon need the next item
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
@@ -145,7 +143,7 @@ struct Bars {
   int n_recv[kMaxNpp];            // (accumulator) own steps of producer pair p observed landed
   int n_issued;                   // ring loads issued by this CTA
   int n_res;                      // (producer) resident loads issued by this CTA
-  int item_id[2];                 // item ids, written by rank 0's scheduler
+  ItemRing items;                // work-item ids from rank 0's scheduler
 };
 
 constexpr size_t SMEM = (size_t)DATA_BYTES + STATS_BYTES + 1024 + 1024;
@@ -358,10 +356,8 @@ __global__ void __launch_bounds__(kThr, 1)
       for (int j = 0; j < RS; ++j) mbar_init(&bars->scratch_free[s][j], 1);
       mbar_init(&bars->stats_full[s], 1);
       mbar_init(&bars->stats_free[s], 128);
-      mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], item_readers<DIR>());
     }
-    mbar_init(&bars->item_req, 1);
+    item_ring_init(&bars->items, item_readers<DIR>());
     for (int s = 0; s < NRECV; ++s) {
       mbar_init(&bars->tile_ready[s], 1);
       mbar_init(&bars->recv_full[s][0], 1);
@@ -395,29 +391,8 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  // The k-th item of this cluster (k = 0, 1, ...): its id, or -1 once the
-  // work has run out or after a timeout (then ok is cleared).  The id sits in
-  // slot k % 2; each reader tells rank 0's scheduler that it has read it.
-  auto get_item = [&](int k, bool& ok) -> int {
-    if (!mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R)) {
-      ok = false;
-      return -1;
-    }
-    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
-    if (id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
-    return id;
-  };
-  // the same for a whole warp (lane 0 reports the read)
-  auto get_item_warp = [&](int k, bool& ok) -> int {
-    if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R))) {
-      ok = false;
-      return -1;
-    }
-    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
-    __syncwarp();
-    if (lane == 0 && id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
-    return id;
-  };
+  auto get_item = [&](int k, bool& ok) { return item_get(&bars->items, k, ok, abort_flag, R); };
+  auto get_item_warp = [&](int k, bool& ok) { return item_get_warp(&bars->items, k, ok, abort_flag, R, lane); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA (both CTAs of a pair)
@@ -440,7 +415,7 @@ __global__ void __launch_bounds__(kThr, 1)
           // slices for S and then four for dP (this CTA's 64 rows)
           const int n_own = own_steps<NPP>(x.N, pp);
           if (n_own == 0) {
-            if (rank == 0) mbar_arrive(&bars->item_req);
+            if (rank == 0) item_request(&bars->items);
             continue;
           }
           // the previous item's last dP has finished reading the resident operand
@@ -455,7 +430,7 @@ __global__ void __launch_bounds__(kThr, 1)
           for (int m = 0; ok && m < n_own; ++m) {
             const int n = pp + NPP * m;
             const int rows = step_rows<DIR>(g, x, n) + HT * (int)h, hd = step_head<DIR>(g, x, n);
-            if (rank == 0 && m == n_own - 1) mbar_arrive(&bars->item_req);  // the next item is soon needed
+            if (rank == 0 && m == n_own - 1) item_request(&bars->items);  // the next item is soon needed
             for (int kk = 0; kk < 2 * (DH / 128); ++kk, ++issued) {
               const int s = issued % NR_P;
               if (issued >= NR_P && !mbar_wait_cl(&bars->ring_empty[s], ((issued / NR_P) & 1) ^ 1, abort_flag, R)) {
@@ -620,28 +595,10 @@ __global__ void __launch_bounds__(kThr, 1)
   } else if (warp == kSigWarp) {
     if (rank == 0 && elect_one()) {
       // ---------------------------------------------------------- scheduler (rank 0)
-      // Items are handed out one at a time from the pass's counter, so a
-      // cluster that starts late (the two passes run side by side) or draws
-      // short items takes more of them.  Each id goes into slot k % 2 of
-      // every CTA; the slot is reused once all readers have read it.  An id
-      // is drawn only when rank 0's TMA thread starts the last step of its
-      // current item: clusters then take items in about the order they
-      // finish them, as clusters of a non-persistent grid would be
-      // dispatched, and the clusters of one kv head walk its query tiles
-      // about in step, sharing them in L2 (drawing earlier tripled the dK/dV
-      // pass's DRAM reads).
-      for (int k = 0;; ++k) {
-        const int s = k & 1;
-        if (k >= 1 && !mbar_wait_cl(&bars->item_req, (k - 1) & 1, abort_flag, R)) break;
-        if (k >= 2 && !mbar_wait_cl(&bars->item_empty[s], ((k >> 1) - 1) & 1, abort_flag, R)) break;
-        int id = atomicAdd(p.work, 1);
-        if (id >= p.n_items) id = -1;
-        const uint32_t slot_addr = smem_u32(&bars->item_id[s]);
-        for (uint32_t r = 0; r < R; ++r) st_cluster_u32(mapa(slot_addr, r), (uint32_t)id);
-        fence_acq_rel_cluster();  // the ids are visible before any CTA sees the arrive
-        for (uint32_t r = 0; r < R; ++r) mbar_arrive_remote(mapa(smem_u32(&bars->item_full[s]), r));
-        if (id < 0) break;
-      }
+      // items one at a time, drawn on rank 0's TMA thread's request
+      // (cluster_items.cuh); a cluster that starts late or draws short
+      // items takes more of them
+      item_schedule(&bars->items, p.work, p.n_items, abort_flag, R);
     } else if (!acc_role && !leader && elect_one()) {
       // ---------------------------------------------------------- relay (producer peer)
       // the peer's 8 warps arrive locally; one remote arrival per step tells the leader

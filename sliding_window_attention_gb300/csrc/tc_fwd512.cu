@@ -41,6 +41,7 @@
 #include <atomic>
 
 #include "swa_internal.h"
+#include "cluster_items.cuh"
 #include "tc_ptx.cuh"
 
 namespace swa {
@@ -113,9 +114,6 @@ struct Bars {
   uint64_t acc_done;             // (accumulator, both) an item's PV MMAs finished
   uint64_t acc_free;             // (accumulator leader) both CTAs read an item's O out
   uint64_t epi_done;             // (accumulator, own) the epilogue's stores read their staging
-  uint64_t item_full[2];         // (every CTA) the scheduler wrote an item id into the slot
-  uint64_t item_empty[2];        // (rank 0) every reader of the slot read it
-  uint64_t item_req;             // (rank 0) its TMA thread will soon need the next item
   uint64_t mma_drain;
   uint32_t tmem_slot;
   int abort_flag;
@@ -125,7 +123,7 @@ struct Bars {
   int n_loaded;                  // (accumulator) steps whose tile loads were issued
   int smid;                      // (accumulator) SM this CTA runs on: the scratch it loads from
   int n_issued;                  // ring loads issued by this CTA
-  int item_id[2];                // item ids, written by rank 0's scheduler
+  ItemRing items;                // work-item ids from rank 0's scheduler
 };
 
 constexpr size_t SMEM = (size_t)DATA_BYTES + 1024 + 1024;
@@ -288,8 +286,6 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&bars->o_ready[s], leader ? 9 : 8);
       mbar_init(&bars->mma_done[s], 1);
       mbar_init(&bars->fin_full[s], 1);
-      mbar_init(&bars->item_full[s], 1);
-      mbar_init(&bars->item_empty[s], kItemReaders);
       bars->n_sent[s] = 0;
     }
     mbar_init(&bars->lx, 256);
@@ -297,7 +293,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->acc_free, 16);
     mbar_init(&bars->epi_done, 8);
-    mbar_init(&bars->item_req, 1);
+    item_ring_init(&bars->items, kItemReaders);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
     bars->fin_sent = 0;
@@ -322,29 +318,8 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  // The k-th item of this cluster (k = 0, 1, ...): its id, or -1 once the
-  // work has run out or after a timeout (then ok is cleared).  The id sits in
-  // slot k % 2; each reader tells rank 0's scheduler that it has read it.
-  auto get_item = [&](int k, bool& ok) -> int {
-    if (!mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R)) {
-      ok = false;
-      return -1;
-    }
-    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
-    if (id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
-    return id;
-  };
-  // the same for a whole warp (lane 0 reports the read)
-  auto get_item_warp = [&](int k, bool& ok) -> int {
-    if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->item_full[k & 1], (k >> 1) & 1, abort_flag, R))) {
-      ok = false;
-      return -1;
-    }
-    const int id = *reinterpret_cast<volatile int*>(&bars->item_id[k & 1]);
-    __syncwarp();
-    if (lane == 0 && id >= 0) mbar_arrive_remote(mapa(smem_u32(&bars->item_empty[k & 1]), 0));
-    return id;
-  };
+  auto get_item = [&](int k, bool& ok) { return item_get(&bars->items, k, ok, abort_flag, R); };
+  auto get_item_warp = [&](int k, bool& ok) { return item_get_warp(&bars->items, k, ok, abort_flag, R, lane); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA (both CTAs of a pair)
@@ -359,7 +334,7 @@ __global__ void __launch_bounds__(kThr, 1)
         if (id < 0) break;
         const FwdItem x = make_fwd_item(g, id, npairs, h);
         for (int n = 0; ok && n < x.N; ++n) {
-          if (rank == 0 && n == x.N - 1) mbar_arrive(&bars->item_req);  // the next item is soon needed
+          if (rank == 0 && n == x.N - 1) item_request(&bars->items);  // the next item is soon needed
           const int j0 = x.ks.tile(n) * T;
           for (int c = 0; c < 2; ++c, ++issued) {
             const int s = issued % nr;
@@ -494,26 +469,10 @@ __global__ void __launch_bounds__(kThr, 1)
   } else if (warp == kSigWarp) {
     if (rank == 0 && elect_one()) {
       // ---------------------------------------------------------- scheduler (rank 0)
-      // Items are handed out one at a time from the launch's counter, so a
-      // cluster that draws short items takes more of them.  Each id goes
-      // into slot k % 2 of every CTA; the slot is reused once all readers
-      // have read it.  An id is drawn only when rank 0's TMA thread starts
-      // the last step of its current item: clusters take items in about the
-      // order they finish them, as a non-persistent grid's clusters would be
-      // dispatched, and the clusters of one kv head read its keys at about
-      // the same place, sharing them in L2.
-      for (int k = 0;; ++k) {
-        const int s = k & 1;
-        if (k >= 1 && !mbar_wait_cl(&bars->item_req, (k - 1) & 1, abort_flag, R)) break;
-        if (k >= 2 && !mbar_wait_cl(&bars->item_empty[s], ((k >> 1) - 1) & 1, abort_flag, R)) break;
-        int id = atomicAdd(p.work, 1);
-        if (id >= p.n_items) id = -1;
-        const uint32_t slot_addr = smem_u32(&bars->item_id[s]);
-        for (uint32_t r = 0; r < R; ++r) st_cluster_u32(mapa(slot_addr, r), (uint32_t)id);
-        fence_acq_rel_cluster();  // the ids are visible before any CTA sees the arrive
-        for (uint32_t r = 0; r < R; ++r) mbar_arrive_remote(mapa(smem_u32(&bars->item_full[s]), r));
-        if (id < 0) break;
-      }
+      // items one at a time, drawn on rank 0's TMA thread's request
+      // (cluster_items.cuh); a cluster that starts late or draws short
+      // items takes more of them
+      item_schedule(&bars->items, p.work, p.n_items, abort_flag, R);
     } else if (!producer && elect_one()) {
       // ---------------------------------------------------------- tile loads (accumulators)
       // once the MMAs of the step two steps back are done with the slot and
