@@ -564,6 +564,41 @@ def test_d512_backwards_overlap_on_two_streams():
             assert torch.equal(a, b), n
 
 
+# head dim 512: two forwards overlapping on two streams.  Both grids are
+# persistent clusters that draw work items from a counter in their own
+# workspace, so the two calls share nothing but the per-SM tile scratch.
+
+
+def test_d512_forwards_overlap_on_two_streams():
+    import sliding_window_attention_gb300 as swa
+
+    shapes = [(1, 8, 2, 2048, 512, 0), (1, 4, 1, 1500, 512, 300)]  # different item counts and band lengths
+    runs = []
+    for seed, (B, Hq, Hkv, L, D, W) in zip((53, 54), shapes):
+        q, k, v, _ = (t.cuda() for t in make_inputs(B, Hq, Hkv, L, D, seed=seed))
+        scale = 1.0 / math.sqrt(D)
+        o_ref, lse_ref = swa.forward(q, k, v, W, scale)
+        torch.cuda.synchronize()
+        o, lse = torch.full_like(o_ref, float("nan")), torch.full_like(lse_ref, float("nan"))
+        ws = torch.empty(swa.fwd_workspace_bytes(B, Hq, Hkv, L, D, W), dtype=torch.uint8, device="cuda")
+        runs.append(((q, k, v), (o, lse), (o_ref, lse_ref), ws, W, scale))
+    assert swa.swa_attn_get_status() == 0
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for rep in range(3):
+        for (ins, outs, _, ws, W, scale), s in zip(runs, streams):
+            with torch.cuda.stream(s):
+                swa.swa_attn_fwd(*ins, *outs, W, scale, ws, s)
+    for s in streams:
+        torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert swa.swa_attn_get_status() == 0
+    for _, outs, refs, _, _, _ in runs:
+        for a, b, n in zip(outs, refs, ("o", "lse")):
+            assert torch.equal(a, b), n
+
+
 # ---------------------------------------------------------------------------
 # shared prompt prefix: one pass over [prompt; chosen; rejected] with the
 # mask "causal AND NOT rejected->chosen" and a window on logical positions
