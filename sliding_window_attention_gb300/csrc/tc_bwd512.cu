@@ -33,8 +33,13 @@
 // elementwise (two warpgroups, 64 of the 128 columns each: producers stage
 // their half of each tile; in accumulators warps 2 .. 1 + NPP watch the
 // tiles land and the next NPP warps load them, one warp per producer pair,
-// before all of 2-9 write the result), 10 relay of the peer's releases (producers), 11 tile stores
-// (producers).  Every wait is bounded; a timeout in one CTA is broadcast to
+// before all of 2-9 write the result), 10 relay of the peer's releases
+// (producer peers) or the work-item scheduler (rank 0), 11 tile stores
+// (producers).  Both passes are persistent: as many clusters as fit on the
+// GPU loop over work items (cluster_items.cuh), the next item's resident
+// operands loading while the accumulators finish the previous one; the dQ
+// pass starts beside the dK/dV pass as a programmatic dependent launch.
+// Every wait is bounded; a timeout in one CTA is broadcast to
 // the whole cluster, every CTA drains its loads, stores and MMAs in flight,
 // and the status word records the timeout.
 #include <cuda.h>

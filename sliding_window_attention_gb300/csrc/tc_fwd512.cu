@@ -2,8 +2,10 @@
 //
 // At D = 512 the output accumulator O of a 128-row query tile (512 fp32
 // columns) fills one SM's Tensor Memory, so S and O cannot live on the same
-// SM.  One 4-CTA cluster per (query head, two adjacent 128-row query tiles),
-// longest rows first.  Every role runs on a CTA pair (tcgen05 .cta_group::2):
+// SM.  Persistent 4-CTA clusters, as many as fit on the GPU, loop over work
+// items of (query head, two adjacent 128-row query tiles), longest rows first
+// (cluster_items.cuh); the next item's Q is loaded while the accumulator
+// writes the previous item's O.  Every role runs on a CTA pair (tcgen05 .cta_group::2):
 // each CTA of a pair owns one of the two query tiles, and each MMA of M = 256
 // rows takes its B operand half from each CTA, so every K and V tile crosses
 // each SM's TMA engine and shared memory once per pair, half in each CTA.
@@ -28,8 +30,8 @@
 //
 // Warps: 0 TMA, 1 TMEM owner and (leader) MMA issuer, 2-9 elementwise (two
 // warpgroups, 64 columns of S or 256 columns of O each), 10 tile loads
-// (accumulators) or relay (producer peer), 11 tile stores (producers) or
-// relay (accumulator peer).  Every wait is bounded; a timeout in one CTA is
+// (accumulators), relay (producer peer) or the work-item scheduler (rank 0),
+// 11 tile stores (producers) or relay (accumulator peer).  Every wait is bounded; a timeout in one CTA is
 // broadcast to the cluster, every CTA drains its loads, stores, copies and
 // MMAs, and the status word records it.
 #include <cuda.h>
