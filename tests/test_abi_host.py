@@ -60,6 +60,16 @@ def test_workspace_sizes(lib):
         assert nf % 256 == 0
 
 
+def test_forward_workspace_is_the_v_copy_and_the_work_counter(lib):
+    # tensor-core forward (not a decode shape): an fp16 copy of v, rounded up
+    # to 256 bytes, then 256 bytes for the persistent head-dim-512 launch's
+    # work counter
+    for (B, Hq, Hkv, L, D, W) in [(1, 32, 4, 16384, 512, 0), (1, 32, 16, 8192, 256, 1024), (2, 8, 2, 1000, 128, 0),
+                                  (1, 2, 1, 300, 512, 129)]:
+        v16 = -(-B * Hkv * L * D * 2 // 256) * 256
+        assert lib.swa_attn_fwd_workspace_bytes(B, Hq, Hkv, L, D, W) == v16 + 256
+
+
 def _fwd(lib, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, Hq=2, Hkv=1, L=16, D=64, W=0, scale=0.125,
          ws=None, wsb=0):
     P = ctypes.c_void_p
